@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""KLA forward (prefill) and decode benchmark on GB300.
+
+Headline: forward tokens/s on the 1B-scale layer (B=4, T=4096, H=16,
+dk=dv=128, C=64; bf16 q/k/v/o, fp32 state and gates), one kla_chunk_fwd call
+per step over synthetic inputs resident in HBM.  Also reported on the same
+line: the decode step (256 sequences x 16 heads, dk=dv=128, fp32 state, 1000
+consecutive steps) as steps/s and HBM GB/s, roofline fractions for both, an
+end-to-end number through host buffers, and the fp64 CPU oracle timed on the
+host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica (the work is
+independent per sequence and head; no collective on the data path) and rank 0
+prints the line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from linear_attention_delta_gb300 import inputs as gen  # noqa: E402
+from linear_attention_delta_gb300 import kla  # noqa: E402
+
+METRIC = ("KLA fwd tokens/s (H16,d128,T4096); decode steps/s + HBM GB/s; "
+          "% roofline")
+L2_FLUSH_BYTES = 512 << 20          # > 2 x the 129 MB L2
+
+
+# ----------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops"]),
+                float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "measured")
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def prefill_bytes(w) -> int:
+    """Algorithmic HBM bytes of one forward pass: q, k, v read and o written
+    once (bf16), log_alpha and eta read once (fp32), h0 read and hT written
+    once (fp32 dk x dv per sequence-head)."""
+    th = w.B * w.T * w.H
+    esz = 2 if w.dtype == "bf16" else 4
+    per_th = esz * (2 * w.dk + 2 * w.dv) + 8
+    state = 4 * w.dk * w.dv * w.B * w.H
+    return th * per_th + 2 * state
+
+
+def prefill_flops(w) -> int:
+    """Algorithmic FLOPs of the chunkwise form per token-head: K K^T and
+    Q K^T (2 C dk each), the forward substitution on [B V | B Gamma K]
+    ((C-1)(dk+dv)), P U~ (2 C dv) and W S, Q S, K^T U~ (6 dk dv)."""
+    C, dk, dv = w.C, w.dk, w.dv
+    per = 4 * C * dk + (C - 1) * (dk + dv) + 2 * C * dv + 6 * dk * dv
+    return w.B * w.T * w.H * per
+
+
+def decode_bytes(w) -> int:
+    heads = w.B * w.H
+    esz = 2 if w.dtype == "bf16" else 4
+    return heads * (2 * 4 * w.dk * w.dv + esz * (2 * w.dk + 2 * w.dv) + 8)
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, p in zip(names, parts[3:]):
+                if p.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ our arm
+
+def bench_prefill(w, steps, warmup, world, gpu_index):
+    inp = gen.prefill_inputs(w)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
+           for k, v in inp.items()}
+    o = torch.empty_like(dev["v"])
+    hT = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32,
+                     device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kla.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["log_alpha"],
+                      dev["eta"], dev["eps"], dev["h0"], C=w.C, o=o, hT=hT)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if kla.device_status() != 0:
+        raise RuntimeError("device-side timeout during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index) as clk:
+        t0 = time.perf_counter()
+        for i in range(steps):
+            flush.zero_()                      # L2 flushed between steps
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier(world)
+    if kla.device_status() != 0:
+        raise RuntimeError("device-side timeout in the timed region")
+    per = [a.elapsed_time(b) for a, b in ev]
+    ms = max_over_ranks(float(np.mean(per)), world)
+    return dict(ms=ms, per_step_ms=per, wall_s=wall, clocks=clk.summary(),
+                launches=steps, inputs=inp)
+
+
+def bench_prefill_e2e(w, inp, steps, warmup):
+    """Same forward pass, host buffers in and out: pinned host -> device
+    copies of every input, the kernel, device -> host copies of o and hT,
+    all inside the timed region."""
+    names = ("q", "k", "v", "log_alpha", "eta", "h0")
+    host = {n: inp[n].pin_memory() for n in names}
+    dev = {n: torch.empty_like(host[n], device="cuda") for n in names}
+    o = torch.empty_like(dev["v"])
+    hT = torch.empty_like(dev["h0"])
+    o_h = torch.empty_like(o, device="cpu").pin_memory()
+    hT_h = torch.empty_like(hT, device="cpu").pin_memory()
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = o.numel() * o.element_size() + hT.numel() * hT.element_size()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for n in names:
+            dev[n].copy_(host[n], non_blocking=True)
+        kla.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["log_alpha"],
+                      dev["eta"], inp["eps"], dev["h0"], C=w.C, o=o, hT=hT)
+        o_h.copy_(o, non_blocking=True)
+        hT_h.copy_(hT, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = (torch.cuda.Event(enable_timing=True),
+              torch.cuda.Event(enable_timing=True))
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, h2d, d2h
+
+
+def bench_decode(w, steps, warmup, distinct=50):
+    """`steps` consecutive decode steps over the full state; token inputs
+    cycle through `distinct` independently drawn steps (the state itself
+    evolves through every step)."""
+    d = gen.decode_inputs(w, steps=distinct)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
+           for k, v in d.items()}
+    S = dev["S0"].clone()
+    o = torch.empty((w.B, w.H, w.dv), dtype=dev["q"].dtype, device="cuda")
+    toks = [[dev[n][i] for n in ("q", "k", "v", "log_alpha", "eta")]
+            for i in range(distinct)]
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        q, k, v, la, eta = toks[i % distinct]
+        kla.decode_step(q, k, v, la, eta, S, eps=d["eps"], o=o)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = (torch.cuda.Event(enable_timing=True),
+              torch.cuda.Event(enable_timing=True))
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if kla.device_status() != 0:
+        raise RuntimeError("device-side timeout in decode")
+    return ms / steps
+
+
+def cpu_baseline_prefill(inp, budget_s=30.0):
+    """The fp64 oracle, as it stands, on the host cores: the whole workload,
+    repeated until ~10 s have passed (never past the budget)."""
+    import oracle
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.kla_fwd(inp["q"], inp["k"], inp["v"], inp["log_alpha"],
+                       inp["eta"], inp["eps"], inp["h0"])
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= 10.0 or el * (n + 1) / n > budget_s:
+            break
+    w = inp["workload"]
+    return dict(value=n * w.B * w.T / el, unit="tokens/s",
+                cores=oracle.max_threads(), kind="oracle",
+                sample=f"full {w.name} workload x{n} "
+                       f"(fp64 C recurrence, OpenMP over batch x head)")
+
+
+def run_ours(args):
+    world, rank, local = dist_setup()
+    hbm, tf_burst, tf_sus, peak_src = peaks()
+    w = gen.LAYER_1B
+    kla.load_library()
+    pf = bench_prefill(w, args.steps, args.warmup, world, local)
+    ms = pf["ms"]
+    tokens = w.B * w.T
+    value = world * tokens / (ms * 1e-3)
+
+    nbytes = prefill_bytes(w)
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    flops = prefill_flops(w)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4),
+                "traffic": args.traffic,
+                "kernel": "kla_chunk_fwd (tensor-core path)"
+                if w.dtype == "bf16" else "kla_chunk_fwd",
+                "algorithmic_bytes_per_launch": nbytes,
+                "tensor_view": {"flops_per_launch": flops,
+                                "achieved_tflops": round(
+                                    flops / (ms * 1e-3) / 1e12, 2),
+                                "peak_tflops": tf_burst,
+                                "frac": round(flops / (ms * 1e-3) / 1e12
+                                              / tf_burst, 4)},
+                "peak_source": peak_src}
+
+    e2e_ms, h2d, d2h = bench_prefill_e2e(w, pf["inputs"], max(3, args.steps
+                                                              // 2), 2)
+    e2e = {"value": round(world * tokens / (e2e_ms * 1e-3), 1),
+           "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+
+    decode = None
+    if not args.no_decode:
+        dw = gen.DECODE
+        dms = bench_decode(dw, args.decode_steps, 20)
+        dbytes = decode_bytes(dw)
+        gbs = dbytes / (dms * 1e-3) / 1e9
+        decode = {"workload": dw.name, "steps_per_s": round(1e3 / dms, 1),
+                  "ms_per_step": round(dms, 5), "hbm_gbs": round(gbs, 1),
+                  "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
+                               "peak": hbm, "unit": "GB/s",
+                               "frac": round(gbs / hbm, 4),
+                               "bytes_per_step": dbytes},
+                  "timed_steps": args.decode_steps,
+                  "token_inputs": "50 distinct draws cycled"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_prefill(pf["inputs"])
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; 1B-layer distributions)",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H,
+                       "dk": w.dk, "dv": w.dv, "C": w.C,
+                       "state": "fp32", "parallelism": f"replicas x{world}",
+                       "l2": "flushed between timed steps (512 MiB write)"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": pf["launches"], "clocks": pf["clocks"],
+            "decode": decode,
+            "per_step_ms": [round(x, 5) for x in pf["per_step_ms"]]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    """The oracle as it stands on the host cores: each step runs the fp64
+    recurrence over one of the four sequences (all 16 heads, 4096 tokens)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    w = gen.LAYER_1B
+    inp = gen.prefill_inputs(w)
+    sl = {k: (v[:1] if isinstance(v, torch.Tensor) else v)
+          for k, v in inp.items()}
+
+    def step():
+        oracle.kla_fwd(sl["q"], sl["k"], sl["v"], sl["log_alpha"],
+                       sl["eta"], sl["eps"], sl["h0"])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    ms = el * 1e3 / args.steps
+    value = w.T / (ms * 1e-3)
+    sample = f"1 of {w.B} sequences of {w.name} (all heads) per step"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded; 1B-layer "
+                                    "distributions)",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H,
+                       "dk": w.dk, "dv": w.dv, "C": w.C},
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s",
+                             "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per launch of the forward kernel")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,150 @@
+/*
+ * kla.h -- C ABI of libkla.so: Kaczmarz Linear Attention (KLA) on GB300
+ * (sm_103a).
+ *
+ * The operation (gist.science/es/paper/2605.08587, "Atencion Lineal
+ * Kaczmarz", sections "Derivacion Teorica" and "La Regla de Actualizacion
+ * KLA"; the German and French versions carry the same formulas):
+ *
+ *   for every (batch b, head h), starting from S_0 = h0[b,h] (dk x dv, fp32):
+ *     S~_{t-1} = alpha_t S_{t-1},          alpha_t = exp(log_alpha_t)
+ *     beta_t   = eta_t / (||k_t||_2^2 + eps)   (beta_t = 0 if the denominator
+ *                                                is exactly 0)
+ *     e_t      = v_t - S~_{t-1}^T k_t
+ *     S_t      = S~_{t-1} + beta_t k_t e_t^T
+ *     o_t      = S_t^T q_t
+ *
+ * The page names a "decayed previous state" without a formula; this library
+ * reads it as the scalar gate above, applied before the residual.  The
+ * read-out o_t = S_t^T q_t (after the write, no 1/sqrt(dk) scale) is likewise
+ * this library's reading; a caller wanting a scale pre-scales q.
+ *
+ * Conventions for every entry point below:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library keeps no pointer after a call returns and allocates no device
+ *     memory.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream).
+ *     A status other than KLA_OK means nothing was launched (argument errors
+ *     are detected on the host before any launch) or that the launch itself
+ *     failed (KLA_ERR_CUDA).  Faults during execution surface at the caller's
+ *     next synchronisation, as with any CUDA call; bounded device-side waits
+ *     that give up are reported by kla_device_status().
+ *   - No C++ exception crosses this interface.
+ *   - Tensors are contiguous and row-major.  Pointers to bf16 data must be
+ *     2-byte aligned and pointers to fp32 data 4-byte aligned; the tensor-core
+ *     forward path additionally wants 16-byte aligned q, k, v, o (it falls
+ *     back to the CUDA-core path otherwise, see kla_chunk_fwd_ex).
+ */
+#ifndef KLA_H
+#define KLA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KLA_API __attribute__((visibility("default")))
+#else
+#define KLA_API
+#endif
+
+typedef enum {
+    KLA_OK = 0,
+    KLA_ERR_INVALID_ARG = -1,       /* null pointer, negative size, bad enum */
+    KLA_ERR_UNSUPPORTED_SHAPE = -2, /* (dk, dv, C, dtype) outside the set   */
+    KLA_ERR_CUDA = -3,              /* a CUDA runtime call failed            */
+    KLA_ERR_TIMEOUT = -4,           /* a bounded device-side wait gave up    */
+    KLA_ERR_NOT_IMPLEMENTED = -5    /* requested variant is not available    */
+} kla_status;
+
+/* Element type of q, k, v and o.  log_alpha, eta, the states h0/hT/S and all
+ * internal accumulation are always fp32. */
+typedef enum { KLA_F32 = 0, KLA_BF16 = 1 } kla_dtype;
+
+/* Forward-pass kernel selection for kla_chunk_fwd_ex. */
+typedef enum {
+    KLA_ALGO_AUTO = 0,   /* tensor-core path when eligible, else CUDA cores */
+    KLA_ALGO_SIMT = 1,   /* fp32 CUDA-core chunkwise kernel (any supported shape) */
+    KLA_ALGO_TC = 2      /* tcgen05 tensor-core kernel: bf16, dk=dv=128, C=64 */
+} kla_algo;
+
+/* Opaque stream handle; ABI-compatible with cudaStream_t / CUstream. */
+typedef struct CUstream_st* kla_stream_t;
+
+/*
+ * kla_chunk_fwd -- full forward pass (prefill) over T tokens, evaluated in the
+ * chunkwise-parallel form (section "Implementacion" of the page: the block
+ * solver of gated DeltaNet with the diagonal B = Diag(beta_1..beta_C) as the
+ * only change).  The result equals the token-by-token recurrence above up to
+ * floating-point rounding; C only changes how the work is blocked.
+ *
+ *   q, k       [B, T, H, dk]  dtype        (read)
+ *   v          [B, T, H, dv]  dtype        (read)
+ *   log_alpha  [B, T, H]      fp32, <= 0   (read) per-token log decay
+ *   eta        [B, T, H]      fp32         (read) relaxation gate
+ *   eps        scalar >= 0                 stabiliser added to ||k||^2
+ *   h0         [B, H, dk, dv] fp32, row index = key dim; NULL -> zero state
+ *   o          [B, T, H, dv]  dtype        (written)
+ *   hT         [B, H, dk, dv] fp32 final state; NULL -> not written
+ *   C          chunk length
+ *
+ * Supported: dk, dv in {16, 32, 64, 128}; C in {16, 32, 64}; any T >= 0
+ * (a ragged last chunk is handled in-kernel); B, H >= 0.  T == 0 copies h0
+ * (or zeros) to hT.  o must not alias any input; hT may alias h0.
+ * Errors: KLA_ERR_INVALID_ARG (null required pointer, negative size,
+ * eps < 0 or not finite, bad dtype), KLA_ERR_UNSUPPORTED_SHAPE, KLA_ERR_CUDA.
+ */
+KLA_API kla_status kla_chunk_fwd(const void* q, const void* k, const void* v,
+                         const float* log_alpha, const float* eta, float eps,
+                         const float* h0, void* o, float* hT,
+                         int B, int T, int H, int dk, int dv, int C,
+                         kla_dtype dtype, kla_stream_t stream);
+
+/*
+ * kla_chunk_fwd_ex -- kla_chunk_fwd with an explicit kernel choice.
+ * KLA_ALGO_TC returns KLA_ERR_UNSUPPORTED_SHAPE unless dtype == KLA_BF16,
+ * dk == dv == 128, C == 64 and q, k, v, o are 16-byte aligned.
+ */
+KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
+                            const float* log_alpha, const float* eta,
+                            float eps, const float* h0, void* o, float* hT,
+                            int B, int T, int H, int dk, int dv, int C,
+                            kla_dtype dtype, kla_algo algo,
+                            kla_stream_t stream);
+
+/*
+ * kla_decode_step -- one new token for each of N sequences x H heads (the
+ * recurrence above for a single t), updating the recurrent state in place.
+ *
+ *   q, k       [N, H, dk]      dtype   (read)
+ *   v          [N, H, dv]      dtype   (read)
+ *   log_alpha  [N, H]          fp32    (read)
+ *   eta        [N, H]          fp32    (read)
+ *   S          [N, H, dk, dv]  fp32    (read, then overwritten with S_t)
+ *   o          [N, H, dv]      dtype   (written) = S_t^T q
+ *
+ * Supported: dk, dv in {16, 32, 64, 128}; N, H >= 0.  o must not alias S or
+ * any input.  Errors as for kla_chunk_fwd.
+ */
+KLA_API kla_status kla_decode_step(const void* q, const void* k, const void* v,
+                           const float* log_alpha, const float* eta, float eps,
+                           float* S, void* o, int N, int H, int dk, int dv,
+                           kla_dtype dtype, kla_stream_t stream);
+
+/*
+ * kla_device_status -- synchronises `stream`, then reads and clears the
+ * library's device-side fault word.  Returns KLA_ERR_TIMEOUT if a bounded
+ * wait inside a kernel gave up since the last call (the kernel then skipped
+ * its remaining work and returned; its outputs are invalid), KLA_ERR_CUDA if
+ * synchronisation failed, else KLA_OK.
+ */
+KLA_API kla_status kla_device_status(kla_stream_t stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+KLA_API const char* kla_status_string(kla_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KLA_H */

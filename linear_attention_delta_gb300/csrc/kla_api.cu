@@ -1,0 +1,134 @@
+// C ABI of libkla.so: argument validation and kernel dispatch.
+// Every check runs on the host before any launch; no exception crosses the
+// interface.  See include/kla.h for the contract of each entry point.
+#include <cmath>
+#include <cstdint>
+
+#include "kla_internal.cuh"
+
+namespace {
+
+bool supported_dim(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool supported_chunk(int c) { return c == 16 || c == 32 || c == 64; }
+
+bool aligned(const void* p, size_t n) {
+    return (reinterpret_cast<uintptr_t>(p) % n) == 0;
+}
+
+kla_status from_cuda(cudaError_t e) {
+    return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" kla_status kla_chunk_fwd_ex(const void* q, const void* k,
+                                       const void* v, const float* log_alpha,
+                                       const float* eta, float eps,
+                                       const float* h0, void* o, float* hT,
+                                       int B, int T, int H, int dk, int dv,
+                                       int C, kla_dtype dtype, kla_algo algo,
+                                       kla_stream_t stream) {
+    if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || C <= 0)
+        return KLA_ERR_INVALID_ARG;
+    if (dtype != KLA_F32 && dtype != KLA_BF16) return KLA_ERR_INVALID_ARG;
+    if (algo != KLA_ALGO_AUTO && algo != KLA_ALGO_SIMT && algo != KLA_ALGO_TC)
+        return KLA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return KLA_ERR_INVALID_ARG;
+    if (!supported_dim(dk) || !supported_dim(dv) || !supported_chunk(C))
+        return KLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H > 0x7fffffffLL) return KLA_ERR_UNSUPPORTED_SHAPE;
+
+    const size_t elt = dtype == KLA_BF16 ? 2 : 4;
+    const bool empty = (long long)B * H == 0;
+    if (!empty && T > 0) {
+        if (!q || !k || !v || !log_alpha || !eta || !o)
+            return KLA_ERR_INVALID_ARG;
+        if (!aligned(q, elt) || !aligned(k, elt) || !aligned(v, elt) ||
+            !aligned(o, elt) || !aligned(log_alpha, 4) || !aligned(eta, 4))
+            return KLA_ERR_INVALID_ARG;
+        if (o == q || o == k || o == v || o == (const void*)log_alpha ||
+            o == (const void*)eta || o == (const void*)h0 || o == (void*)hT)
+            return KLA_ERR_INVALID_ARG;
+    }
+    if ((h0 && !aligned(h0, 4)) || (hT && !aligned(hT, 4)))
+        return KLA_ERR_INVALID_ARG;
+    if (empty) return KLA_OK;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        if (!hT) return KLA_OK;
+        const size_t bytes = sizeof(float) * (size_t)B * H * dk * dv;
+        if (h0 == hT) return KLA_OK;
+        if (h0)
+            return from_cuda(
+                cudaMemcpyAsync(hT, h0, bytes, cudaMemcpyDeviceToDevice, s));
+        return from_cuda(cudaMemsetAsync(hT, 0, bytes, s));
+    }
+
+    kla::FwdArgs a{q, k, v, log_alpha, eta, eps, h0, o, hT,
+                   B, T, H, dk, dv, C, dtype};
+    const bool tc_ok = kla::chunk_tc_eligible(a);
+    if (algo == KLA_ALGO_TC) {
+        if (!tc_ok) return KLA_ERR_UNSUPPORTED_SHAPE;
+        return from_cuda(kla::launch_chunk_tc(a, s));
+    }
+    if (algo == KLA_ALGO_AUTO && tc_ok)
+        return from_cuda(kla::launch_chunk_tc(a, s));
+    return from_cuda(kla::launch_chunk_simt(a, s));
+}
+
+extern "C" kla_status kla_chunk_fwd(const void* q, const void* k,
+                                    const void* v, const float* log_alpha,
+                                    const float* eta, float eps,
+                                    const float* h0, void* o, float* hT,
+                                    int B, int T, int H, int dk, int dv,
+                                    int C, kla_dtype dtype,
+                                    kla_stream_t stream) {
+    return kla_chunk_fwd_ex(q, k, v, log_alpha, eta, eps, h0, o, hT, B, T, H,
+                            dk, dv, C, dtype, KLA_ALGO_AUTO, stream);
+}
+
+extern "C" kla_status kla_decode_step(const void* q, const void* k,
+                                      const void* v, const float* log_alpha,
+                                      const float* eta, float eps, float* S,
+                                      void* o, int N, int H, int dk, int dv,
+                                      kla_dtype dtype, kla_stream_t stream) {
+    if (N < 0 || H < 0 || dk <= 0 || dv <= 0) return KLA_ERR_INVALID_ARG;
+    if (dtype != KLA_F32 && dtype != KLA_BF16) return KLA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return KLA_ERR_INVALID_ARG;
+    if (!supported_dim(dk) || !supported_dim(dv))
+        return KLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)N * H > 0x7fffffffLL) return KLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)N * H == 0) return KLA_OK;
+    if (!q || !k || !v || !log_alpha || !eta || !S || !o)
+        return KLA_ERR_INVALID_ARG;
+    const size_t elt = dtype == KLA_BF16 ? 2 : 4;
+    if (!aligned(q, elt) || !aligned(k, elt) || !aligned(v, elt) ||
+        !aligned(o, elt) || !aligned(log_alpha, 4) || !aligned(eta, 4) ||
+        !aligned(S, 16))
+        return KLA_ERR_INVALID_ARG;
+    if (o == (void*)S || o == q || o == k || o == v) return KLA_ERR_INVALID_ARG;
+    kla::DecodeArgs a{q, k, v, log_alpha, eta, eps, S, o, N, H, dk, dv, dtype};
+    return from_cuda(
+        kla::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" kla_status kla_device_status(kla_stream_t stream) {
+    unsigned int word = 0;
+    cudaError_t e = kla::read_and_clear_fault(
+        reinterpret_cast<cudaStream_t>(stream), &word);
+    if (e != cudaSuccess) return KLA_ERR_CUDA;
+    return word ? KLA_ERR_TIMEOUT : KLA_OK;
+}
+
+extern "C" const char* kla_status_string(kla_status status) {
+    switch (status) {
+        case KLA_OK: return "ok";
+        case KLA_ERR_INVALID_ARG: return "invalid argument";
+        case KLA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape or dtype";
+        case KLA_ERR_CUDA: return "CUDA runtime error";
+        case KLA_ERR_TIMEOUT: return "device-side wait timed out";
+        case KLA_ERR_NOT_IMPLEMENTED: return "not implemented";
+    }
+    return "unknown status";
+}

@@ -1,0 +1,258 @@
+// Chunkwise KLA forward pass on CUDA cores, all arithmetic in fp32.
+//
+// This is the general path: every supported (dk, dv, C) and both I/O types,
+// and the only path for fp32 inputs (whose tolerance tensor-core operand
+// rounding cannot meet).  One CTA owns one (batch, head, dv tile) and walks
+// the chunks of its sequence in order, keeping its dk x dvt slice of the
+// state in shared memory.
+//
+// Per chunk (rows r, i = 0..C-1; g = in-chunk cumulative log decay,
+// gamma_r = exp(g_r), Gamma_ri = exp(g_r - g_i) for r >= i):
+//   beta_r = eta_r / (||k_r||^2 + eps)                    Kaczmarz step
+//   A = I + strict_lower(Diag(beta) (Gamma o K K^T))      C x C, unit lower
+//   [U | W] = A^{-1} [Diag(beta) V | Diag(beta gamma) K]  forward substitution
+//   U~ = U - W S                                          chunk residuals
+//   O  = Diag(gamma) Q S + lower_incl(Gamma o Q K^T) U~
+//   S  = gamma_C S + (Diag(Gamma_{C,.}) K)^T U~
+// This is the gated-DeltaNet block solver with B = Diag(beta) as the only
+// change (gist.science/es/paper/2605.08587, section "Implementacion").  The
+// decay-aware W = A^{-1} B Diag(gamma) K follows from the recurrence with a
+// per-token scalar decay; only exponents g_r - g_i with r >= i (and g_r,
+// g_C - g_i) are ever exponentiated, so no factor exceeds 1.
+//
+// A ragged last chunk is padded in-kernel with k = q = v = 0, eta = 0,
+// log_alpha = 0: such a step has beta = 0 and alpha = 1, an exact identity.
+#include "kla_internal.cuh"
+
+namespace kla {
+namespace {
+
+constexpr int kSimtThreads = 256;
+constexpr int kSimtMaxC = 64;
+
+template <int DK, int DVT>
+struct SimtSmem {
+    static constexpr int LDK = DK + 1;     // padded rows: conflict-free dots
+    static constexpr int LDV = DVT + 1;
+    static constexpr int LDC = kSimtMaxC + 1;
+    static constexpr int Q = 0;
+    static constexpr int K = Q + kSimtMaxC * LDK;
+    static constexpr int W = K + kSimtMaxC * LDK;
+    static constexpr int U = W + kSimtMaxC * LDK;
+    static constexpr int S = U + kSimtMaxC * LDV;
+    static constexpr int A = S + DK * LDV;
+    static constexpr int P = A + kSimtMaxC * LDC;
+    static constexpr int G = P + kSimtMaxC * LDC;      // cumulative log decay
+    static constexpr int BETA = G + kSimtMaxC;
+    static constexpr int KDEC = BETA + kSimtMaxC;      // exp(g_last - g_r)
+    static constexpr int TOTAL = KDEC + kSimtMaxC;
+    static constexpr size_t BYTES = sizeof(float) * (size_t)TOTAL;
+};
+
+template <int DK, int DVT, typename IO>
+__global__ void __launch_bounds__(kSimtThreads)
+kla_chunk_simt_kernel(FwdArgs a) {
+    using L = SimtSmem<DK, DVT>;
+    extern __shared__ float sm[];
+    float* Qs = sm + L::Q;
+    float* Ks = sm + L::K;
+    float* Ws = sm + L::W;
+    float* Us = sm + L::U;
+    float* Ss = sm + L::S;
+    float* As = sm + L::A;
+    float* Ps = sm + L::P;
+    float* gs = sm + L::G;
+    float* bs = sm + L::BETA;
+    float* kd = sm + L::KDEC;
+
+    const int bh = blockIdx.x;
+    const int b = bh / a.H, h = bh % a.H;
+    const int j0 = blockIdx.y * DVT;
+    const int tid = threadIdx.x;
+    const int C = a.C, T = a.T, H = a.H, dv = a.dv;
+    const IO* q = static_cast<const IO*>(a.q);
+    const IO* k = static_cast<const IO*>(a.k);
+    const IO* v = static_cast<const IO*>(a.v);
+    IO* o = static_cast<IO*>(a.o);
+
+    // initial state slice
+    for (int idx = tid; idx < DK * DVT; idx += kSimtThreads) {
+        const int c = idx / DVT, j = idx % DVT;
+        Ss[c * L::LDV + j] =
+            a.h0 ? a.h0[((size_t)bh * DK + c) * dv + j0 + j] : 0.f;
+    }
+
+    for (int t0 = 0; t0 < T; t0 += C) {
+        // ---- load the chunk (zero-padded past T) ----
+        for (int idx = tid; idx < C * DK; idx += kSimtThreads) {
+            const int r = idx / DK, c = idx % DK;
+            const int t = t0 + r;
+            float qv = 0.f, kv = 0.f;
+            if (t < T) {
+                const size_t off = (((size_t)b * T + t) * H + h) * DK + c;
+                qv = to_f32(q[off]);
+                kv = to_f32(k[off]);
+            }
+            Qs[r * L::LDK + c] = qv;
+            Ks[r * L::LDK + c] = kv;
+        }
+        for (int idx = tid; idx < C * DVT; idx += kSimtThreads) {
+            const int r = idx / DVT, j = idx % DVT;
+            const int t = t0 + r;
+            Us[r * L::LDV + j] =
+                t < T ? to_f32(v[(((size_t)b * T + t) * H + h) * dv + j0 + j])
+                      : 0.f;
+        }
+        if (tid < C) {
+            const int t = t0 + tid;
+            const size_t off = ((size_t)b * T + t) * H + h;
+            gs[tid] = t < T ? a.log_alpha[off] : 0.f;
+            bs[tid] = t < T ? a.eta[off] : 0.f;
+        }
+        __syncthreads();
+
+        // ---- beta_r and the in-chunk cumulative log decay ----
+        if (tid < C) {
+            float n = 0.f;
+            for (int c = 0; c < DK; ++c) {
+                const float x = Ks[tid * L::LDK + c];
+                n = fmaf(x, x, n);
+            }
+            const float denom = n + a.eps;
+            bs[tid] = denom == 0.f ? 0.f : bs[tid] / denom;
+        }
+        if (tid == 32) {
+            float acc = 0.f;
+            for (int r = 0; r < C; ++r) {
+                acc += gs[r];
+                gs[r] = acc;
+            }
+        }
+        __syncthreads();
+        if (tid < C) kd[tid] = expf(gs[C - 1] - gs[tid]);
+
+        // ---- A (strictly lower part scaled by beta) and P = Gamma o QK^T ----
+        for (int idx = tid; idx < C * C; idx += kSimtThreads) {
+            const int r = idx / C, i = idx % C;
+            float av = (i == r) ? 1.f : 0.f;
+            float pv = 0.f;
+            if (i <= r) {
+                float kk = 0.f, qk = 0.f;
+#pragma unroll 8
+                for (int c = 0; c < DK; ++c) {
+                    const float ki = Ks[i * L::LDK + c];
+                    kk = fmaf(Ks[r * L::LDK + c], ki, kk);
+                    qk = fmaf(Qs[r * L::LDK + c], ki, qk);
+                }
+                const float dec = expf(gs[r] - gs[i]);
+                pv = dec * qk;
+                if (i < r) av = bs[r] * dec * kk;
+            }
+            As[r * L::LDC + i] = av;
+            Ps[r * L::LDC + i] = pv;
+        }
+        __syncthreads();
+
+        // ---- forward substitution: one thread per right-hand-side column --
+        if (tid < DVT + DK) {
+            const bool is_u = tid < DVT;
+            const int col = is_u ? tid : tid - DVT;
+            float* X = is_u ? Us : Ws;
+            const int ld = is_u ? L::LDV : L::LDK;
+            for (int r = 0; r < C; ++r) {
+                float x = is_u ? bs[r] * Us[r * L::LDV + col]
+                               : bs[r] * expf(gs[r]) * Ks[r * L::LDK + col];
+                for (int i = 0; i < r; ++i)
+                    x = fmaf(-As[r * L::LDC + i], X[i * ld + col], x);
+                X[r * ld + col] = x;
+            }
+        }
+        __syncthreads();
+
+        // ---- U~ = U - W S ----
+        for (int idx = tid; idx < C * DVT; idx += kSimtThreads) {
+            const int r = idx / DVT, j = idx % DVT;
+            float acc = Us[r * L::LDV + j];
+#pragma unroll 8
+            for (int c = 0; c < DK; ++c)
+                acc = fmaf(-Ws[r * L::LDK + c], Ss[c * L::LDV + j], acc);
+            Us[r * L::LDV + j] = acc;
+        }
+        __syncthreads();
+
+        // ---- O = Diag(gamma) Q S + P U~ ----
+        for (int idx = tid; idx < C * DVT; idx += kSimtThreads) {
+            const int r = idx / DVT, j = idx % DVT;
+            const int t = t0 + r;
+            float qs = 0.f;
+#pragma unroll 8
+            for (int c = 0; c < DK; ++c)
+                qs = fmaf(Qs[r * L::LDK + c], Ss[c * L::LDV + j], qs);
+            float acc = expf(gs[r]) * qs;
+            for (int i = 0; i <= r; ++i)
+                acc = fmaf(Ps[r * L::LDC + i], Us[i * L::LDV + j], acc);
+            if (t < T)
+                o[(((size_t)b * T + t) * H + h) * dv + j0 + j] =
+                    from_f32<IO>(acc);
+        }
+        __syncthreads();
+
+        // ---- S = gamma_C S + (Diag(Gamma_C) K)^T U~ ----
+        const float gC = expf(gs[C - 1]);
+        for (int idx = tid; idx < DK * DVT; idx += kSimtThreads) {
+            const int c = idx / DVT, j = idx % DVT;
+            float acc = gC * Ss[c * L::LDV + j];
+            for (int r = 0; r < C; ++r)
+                acc = fmaf(kd[r] * Ks[r * L::LDK + c], Us[r * L::LDV + j],
+                           acc);
+            Ss[c * L::LDV + j] = acc;
+        }
+        __syncthreads();
+    }
+
+    if (a.hT) {
+        for (int idx = tid; idx < DK * DVT; idx += kSimtThreads) {
+            const int c = idx / DVT, j = idx % DVT;
+            a.hT[((size_t)bh * DK + c) * dv + j0 + j] = Ss[c * L::LDV + j];
+        }
+    }
+}
+
+template <int DK, int DVT, typename T>
+cudaError_t launch_shape(const FwdArgs& a, cudaStream_t stream) {
+    using L = SimtSmem<DK, DVT>;
+    auto kern = kla_chunk_simt_kernel<DK, DVT, T>;
+    cudaError_t err = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
+    if (err != cudaSuccess) return err;
+    dim3 grid((unsigned)((long)a.B * a.H), (unsigned)(a.dv / DVT));
+    kern<<<grid, kSimtThreads, L::BYTES, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_dtype(const FwdArgs& a, cudaStream_t stream) {
+    // dv tile: all of dv when dv == 16, else 32 columns.
+#define KLA_SIMT_DK(DKV)                                                    \
+    if (a.dk == DKV) {                                                      \
+        if (a.dv == 16) return launch_shape<DKV, 16, T>(a, stream);         \
+        return launch_shape<DKV, 32, T>(a, stream);                         \
+    }
+    KLA_SIMT_DK(16)
+    KLA_SIMT_DK(32)
+    KLA_SIMT_DK(64)
+    KLA_SIMT_DK(128)
+#undef KLA_SIMT_DK
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_simt(const FwdArgs& a, cudaStream_t stream) {
+    if ((long)a.B * a.H == 0 || a.T == 0) return cudaSuccess;
+    if (a.C > kSimtMaxC) return cudaErrorInvalidValue;
+    if (a.dtype == KLA_BF16) return launch_dtype<__nv_bfloat16>(a, stream);
+    return launch_dtype<float>(a, stream);
+}
+
+}  // namespace kla

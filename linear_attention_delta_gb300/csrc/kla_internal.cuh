@@ -1,0 +1,65 @@
+// Internal launchers of libkla.so (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "kla.h"
+
+namespace kla {
+
+// Element load/store helpers for the two I/O types.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) {
+    return x;
+}
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(
+    float x) {
+    return __float2bfloat16_rn(x);
+}
+
+struct FwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* log_alpha;
+    const float* eta;
+    float eps;
+    const float* h0;   // may be null
+    void* o;
+    float* hT;         // may be null
+    int B, T, H, dk, dv, C;
+    kla_dtype dtype;
+};
+
+struct DecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* log_alpha;
+    const float* eta;
+    float eps;
+    float* S;
+    void* o;
+    int N, H, dk, dv;
+    kla_dtype dtype;
+};
+
+// Each returns cudaSuccess or the launch error.  Shapes are validated by the
+// caller (kla_api.cu); a launcher returning cudaErrorInvalidValue means the
+// shape has no instantiation.
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_chunk_simt(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_chunk_tc(const FwdArgs& a, cudaStream_t stream);
+bool chunk_tc_eligible(const FwdArgs& a);
+
+// Device fault word of the tensor-core kernels (bounded waits that gave up).
+// read_and_clear_fault synchronises the stream first.
+cudaError_t read_and_clear_fault(cudaStream_t stream, unsigned int* word);
+
+}  // namespace kla

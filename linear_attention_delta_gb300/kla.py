@@ -1,0 +1,149 @@
+"""ctypes binding of libkla.so (argument marshalling only).
+
+Every entry point mirrors a C function of ``include/kla.h`` under the same
+name without the ``kla_`` prefix.  Tensors are torch CUDA tensors (torch
+provides device memory and the current stream; all arithmetic runs in the
+library's kernels).  There is no CPU fallback: without the built library or
+without CUDA tensors these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+KLA_OK = 0
+STATUS_NAMES = {0: "KLA_OK", -1: "KLA_ERR_INVALID_ARG",
+                -2: "KLA_ERR_UNSUPPORTED_SHAPE", -3: "KLA_ERR_CUDA",
+                -4: "KLA_ERR_TIMEOUT", -5: "KLA_ERR_NOT_IMPLEMENTED"}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+ALGOS = {"auto": 0, "simt": 1, "tc": 2}
+
+# name -> (restype, argtypes) of every symbol include/kla.h declares
+_VP, _FP, _F, _I = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, \
+    ctypes.c_int
+SIGNATURES = {
+    "kla_chunk_fwd": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP, _FP,
+                           _I, _I, _I, _I, _I, _I, _I, _VP]),
+    "kla_chunk_fwd_ex": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP, _FP,
+                              _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
+    "kla_decode_step": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
+                             _I, _I, _I, _I, _I, _VP]),
+    "kla_device_status": (_I, [_VP]),
+    "kla_status_string": (ctypes.c_char_p, [_I]),
+}
+
+_lib = None
+
+
+class KlaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}: "
+                         f"{status_string(status)}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libkla.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise KlaError("load_library", -5) from FileNotFoundError(path)
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().kla_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_cuda(name, t, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor (no CPU fallback)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def chunk_fwd(q, k, v, log_alpha, eta, eps: float = 1e-6, h0=None,
+              C: int = 64, algo: str = "auto", o=None, hT=None,
+              want_state: bool = True, stream=None):
+    """KLA forward pass (``kla_chunk_fwd_ex``).
+
+    q, k [B,T,H,dk]; v [B,T,H,dv] (fp32 or bf16, same dtype); log_alpha, eta
+    [B,T,H] fp32; h0 [B,H,dk,dv] fp32 or None.  Returns (o, hT); hT is None
+    when ``want_state`` is False.  ``o``/``hT`` may be passed preallocated.
+    """
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(n, t, q.dtype)
+    _check_cuda("log_alpha", log_alpha, torch.float32)
+    _check_cuda("eta", eta, torch.float32)
+    if h0 is not None:
+        _check_cuda("h0", h0, torch.float32)
+    if q.dtype not in DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and want_state:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    st = load_library().kla_chunk_fwd_ex(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(eta), float(eps),
+        _ptr(h0), _ptr(o), _ptr(hT), B, T, H, dk, dv, int(C),
+        DTYPES[q.dtype], ALGOS[algo], _stream(stream))
+    if st != KLA_OK:
+        raise KlaError("kla_chunk_fwd_ex", st)
+    return o, hT
+
+
+def decode_step(q, k, v, log_alpha, eta, S, eps: float = 1e-6, o=None,
+                stream=None):
+    """One KLA decode token (``kla_decode_step``); S [N,H,dk,dv] fp32 is
+    updated in place.  Returns o [N,H,dv]."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(n, t, q.dtype)
+    _check_cuda("log_alpha", log_alpha, torch.float32)
+    _check_cuda("eta", eta, torch.float32)
+    _check_cuda("S", S, torch.float32)
+    N, H, dk = k.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    st = load_library().kla_decode_step(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(eta), float(eps),
+        _ptr(S), _ptr(o), N, H, dk, dv, DTYPES[q.dtype], _stream(stream))
+    if st != KLA_OK:
+        raise KlaError("kla_decode_step", st)
+    return o
+
+
+def device_status(stream=None) -> int:
+    """``kla_device_status``: sync the stream, read and clear the fault word."""
+    return int(load_library().kla_device_status(_stream(stream)))

@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI: the library builds, loads, exports every
+symbol ``include/kla.h`` declares, and rejects bad arguments before touching
+the device.  No test here launches a kernel (these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_delta_gb300 import build as kbuild
+from linear_attention_delta_gb300 import kla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kla.h")
+
+INVALID, UNSUPPORTED, OK = -1, -2, 0
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"KLA_API\s+[\w\s\*]+?\b(kla_\w+)\s*\(",
+                                 text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return kla.load_library()
+
+
+def test_header_declares_expected_entry_points():
+    syms = declared_symbols()
+    for name in ("kla_chunk_fwd", "kla_chunk_fwd_ex", "kla_decode_step",
+                 "kla_device_status", "kla_status_string"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    # and the binding knows the signature of each of them
+    assert set(declared_symbols()) <= set(kla.SIGNATURES)
+
+
+def test_build_is_fresh():
+    assert kbuild.up_to_date()
+
+
+def test_status_strings(lib):
+    for code in kla.STATUS_NAMES:
+        s = kla.status_string(code)
+        assert isinstance(s, str) and s
+    assert kla.status_string(12345) == "unknown status"
+
+
+P = ctypes.c_void_p(0x1000)      # never dereferenced: calls fail validation
+
+
+def fwd(lib, *, q=P, k=P, v=P, la=P, eta=P, eps=1e-6, h0=None, o=P, hT=None,
+        B=1, T=8, H=1, dk=16, dv=16, C=16, dtype=1, algo=0):
+    return lib.kla_chunk_fwd_ex(q, k, v, la, eta, eps, h0, o, hT, B, T, H, dk,
+                                dv, C, dtype, algo, None)
+
+
+def dec(lib, *, q=P, k=P, v=P, la=P, eta=P, eps=1e-6, S=P, o=P, N=1, H=1,
+        dk=16, dv=16, dtype=1):
+    return lib.kla_decode_step(q, k, v, la, eta, eps, S, o, N, H, dk, dv,
+                               dtype, None)
+
+
+def test_fwd_rejects_bad_arguments_on_host(lib):
+    assert fwd(lib, q=None) == INVALID
+    assert fwd(lib, o=None) == INVALID
+    assert fwd(lib, eta=None) == INVALID
+    assert fwd(lib, B=-1) == INVALID
+    assert fwd(lib, T=-3) == INVALID
+    assert fwd(lib, C=0) == INVALID
+    assert fwd(lib, dtype=7) == INVALID
+    assert fwd(lib, algo=9) == INVALID
+    assert fwd(lib, eps=-1.0) == INVALID
+    assert fwd(lib, eps=float("nan")) == INVALID
+    assert fwd(lib, eps=float("inf")) == INVALID
+    assert fwd(lib, o=P, q=P) == INVALID                 # o aliases q
+    assert fwd(lib, q=ctypes.c_void_p(0x1001)) == INVALID  # misaligned bf16
+    assert fwd(lib, dtype=0, v=ctypes.c_void_p(0x1002)) == INVALID
+
+
+def test_fwd_rejects_unsupported_shapes(lib):
+    q, k, v, o = (ctypes.c_void_p(0x1000 * i) for i in (1, 2, 3, 4))
+    la, eta = ctypes.c_void_p(0x5000), ctypes.c_void_p(0x6000)
+    kw = dict(q=q, k=k, v=v, o=o, la=la, eta=eta)
+    assert fwd(lib, dk=24, **kw) == UNSUPPORTED
+    assert fwd(lib, dv=256, **kw) == UNSUPPORTED
+    assert fwd(lib, C=48, **kw) == UNSUPPORTED
+    assert fwd(lib, C=128, **kw) == UNSUPPORTED
+    # the tensor-core kernel only takes bf16, dk = dv = 128, C = 64
+    assert fwd(lib, algo=2, dtype=0, dk=128, dv=128, C=64, **kw) == UNSUPPORTED
+    assert fwd(lib, algo=2, dk=64, dv=64, C=64, **kw) == UNSUPPORTED
+    assert fwd(lib, algo=2, dk=128, dv=128, C=32, **kw) == UNSUPPORTED
+
+
+def test_fwd_empty_batch_is_a_no_op(lib):
+    # nothing to compute: returns before any CUDA call, pointers unused
+    assert fwd(lib, B=0, q=None, k=None, v=None, la=None, eta=None,
+               o=None) == OK
+    assert fwd(lib, H=0, q=None, k=None, v=None, la=None, eta=None,
+               o=None) == OK
+
+
+def test_decode_rejects_bad_arguments_on_host(lib):
+    assert dec(lib, S=None) == INVALID
+    assert dec(lib, N=-1) == INVALID
+    assert dec(lib, dtype=3) == INVALID
+    assert dec(lib, S=ctypes.c_void_p(0x1004)) == INVALID   # S not 16B aligned
+    assert dec(lib, o=P, S=P) == INVALID                     # o aliases S
+    assert dec(lib, dk=8) == UNSUPPORTED
+    assert dec(lib, eps=-1e-3) == INVALID
+    assert dec(lib, N=0, q=None, S=None, o=None) == OK
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 4, 1, 16)
+    la = torch.zeros(1, 4, 1)
+    with pytest.raises(TypeError):
+        kla.chunk_fwd(x, x, x, la, la)
+    with pytest.raises(TypeError):
+        kla.decode_step(x[0], x[0], x[0], la[0], la[0],
+                        torch.zeros(4, 1, 16, 16))

@@ -1,0 +1,216 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Metric (per output tensor): err = max|x - x_ref| / max|x_ref|.
+Bounds: fp32 I/O <= 1e-4, bf16 I/O <= 2e-2, for o and for the final state.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_attention_delta_gb300 import inputs as gen
+from linear_attention_delta_gb300 import kla
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    kla.load_library()
+    yield
+    assert kla.device_status() == 0
+
+
+def rel_err(x, ref):
+    x = x.detach().double().cpu().numpy() if hasattr(x, "detach") else x
+    return float(np.max(np.abs(x - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def to_dev(d):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
+            for k, v in d.items()}
+
+
+def run_fwd(inp, algo="auto", C=None):
+    d = to_dev(inp)
+    o, hT = kla.chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["eta"],
+                          d["eps"], d["h0"], C=C or inp["C"], algo=algo)
+    torch.cuda.synchronize()
+    return o, hT
+
+
+def oracle_fwd(inp):
+    return oracle.kla_fwd(inp["q"], inp["k"], inp["v"], inp["log_alpha"],
+                          inp["eta"], inp["eps"], inp["h0"])
+
+
+def check_fwd(inp, algo="auto", C=None):
+    o, hT = run_fwd(inp, algo, C)
+    o_ref, h_ref = oracle_fwd(inp)
+    tol = TOL[inp["q"].dtype]
+    eo, eh = rel_err(o, o_ref), rel_err(hT, h_ref)
+    assert np.isfinite(eo) and eo <= tol, f"o err {eo:.3e} > {tol}"
+    assert np.isfinite(eh) and eh <= tol, f"hT err {eh:.3e} > {tol}"
+    return eo, eh
+
+
+# ---------------------------------------------------------------- tiny fp32
+
+@pytest.mark.parametrize("algo", ["auto", "simt"])
+def test_tiny_fp32(algo):
+    check_fwd(gen.prefill_inputs(gen.TINY), algo)
+
+
+def test_tiny_unrelaxed_projection_through_gpu():
+    """eta=1, eps=0, alpha=1: with q := k every output equals its value
+    (S_t^T k_t = v_t, the projection property) through the CUDA path."""
+    inp = gen.prefill_inputs(gen.TINY_UNRELAXED)
+    inp["q"] = inp["k"].clone()
+    o, _ = run_fwd(inp)
+    assert rel_err(o, inp["v"].double().numpy()) <= 1e-4
+    check_fwd(inp)
+
+
+@pytest.mark.parametrize("C", [16, 32, 64])
+@pytest.mark.parametrize("T", [1, 17, 64, 100])
+def test_fp32_chunk_sizes_and_ragged_tails(C, T):
+    inp = gen.prefill_inputs(gen.TINY, T=T, B=2, H=3)
+    check_fwd(inp, "simt", C)
+
+
+@pytest.mark.parametrize("dk,dv", [(16, 32), (32, 16), (64, 64), (128, 16),
+                                   (32, 128)])
+def test_fp32_head_dims(dk, dv):
+    from dataclasses import replace
+    w = replace(gen.TINY, dk=dk, dv=dv)
+    check_fwd(gen.prefill_inputs(w, T=40, B=1, H=2), "simt", 16)
+
+
+# ---------------------------------------------------------------- bf16 d=128
+
+SMALL_BF16 = [
+    (gen.LAYER_340M, dict(B=2, T=200, H=3)),
+    (gen.LAYER_1B, dict(B=1, T=257, H=4)),
+    (gen.LONG_CTX, dict(B=1, T=1000, H=2)),
+]
+
+
+@pytest.mark.parametrize("w,sizes", SMALL_BF16,
+                         ids=[w.name for w, _ in SMALL_BF16])
+@pytest.mark.parametrize("algo", ["auto", "simt"])
+def test_bf16_reduced_sizes(w, sizes, algo):
+    check_fwd(gen.prefill_inputs(w, **sizes), algo)
+
+
+def test_bf16_chunk_size_invariance():
+    inp = gen.prefill_inputs(gen.LAYER_1B, B=1, T=192, H=2)
+    outs = [run_fwd(inp, "simt", C) for C in (16, 32, 64)]
+    o_ref, h_ref = oracle_fwd(inp)
+    for o, hT in outs:
+        assert rel_err(o, o_ref) <= 2e-2 and rel_err(hT, h_ref) <= 2e-2
+    assert rel_err(outs[0][1], outs[2][1].double().cpu().numpy()) <= 1e-3
+
+
+def test_zero_length_sequence_copies_state():
+    inp = gen.prefill_inputs(gen.LAYER_1B, B=2, T=0, H=2)
+    o, hT = run_fwd(inp)
+    assert o.numel() == 0
+    assert torch.equal(hT.cpu(), inp["h0"])
+
+
+def test_hT_may_alias_h0():
+    inp = gen.prefill_inputs(gen.LAYER_1B, B=1, T=130, H=2)
+    d = to_dev(inp)
+    h = d["h0"].clone()
+    kla.chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["eta"], d["eps"],
+                  h, C=64, hT=h)
+    torch.cuda.synchronize()
+    _, h_ref = oracle_fwd(inp)
+    assert rel_err(h, h_ref) <= 2e-2
+
+
+def test_zero_keys_with_zero_eps():
+    inp = gen.prefill_inputs(gen.TINY, B=1, T=48, H=2)
+    inp["k"][:, 5] = 0.0
+    inp["k"][:, 30:33] = 0.0
+    inp["eps"] = 0.0
+    check_fwd(inp, "simt")
+
+
+# ---------------------------------------------------------------- full size
+
+@pytest.mark.parametrize("w", [gen.LAYER_340M, gen.LAYER_1B, gen.LONG_CTX],
+                         ids=lambda w: w.name)
+def test_full_size_against_oracle(w):
+    """The workloads at their full sizes, every element compared."""
+    check_fwd(gen.prefill_inputs(w))
+
+
+# ---------------------------------------------------------------- decode
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(16, 16), (128, 128), (64, 32),
+                                   (32, 128)])
+def test_decode_steps(dtype, dk, dv):
+    from dataclasses import replace
+    w = replace(gen.DECODE, dtype=dtype, dk=dk, dv=dv, B=5, H=3)
+    d = gen.decode_inputs(w, steps=6)
+    S = d["S0"].cuda()
+    S_ref = d["S0"].double().numpy()
+    tol = TOL[d["q"].dtype]
+    for t in range(6):
+        args = [d[n][t] for n in ("q", "k", "v", "log_alpha", "eta")]
+        o = kla.decode_step(*[a.cuda() for a in args], S, eps=d["eps"])
+        o_ref, S_ref = oracle.kla_decode_step(*args, d["eps"], S_ref)
+        assert rel_err(o, o_ref) <= tol
+    torch.cuda.synchronize()
+    assert rel_err(S, S_ref) <= 1e-4
+
+
+def test_decode_full_size_sampled():
+    """256 sequences x 16 heads for 60 steps on the GPU; the first 8
+    sequences (every head) are followed by the oracle for all steps."""
+    w = gen.DECODE
+    steps, ns = 60, 8
+    d = gen.decode_inputs(w, steps=steps)
+    dd = {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
+          for k, v in d.items()}
+    S = dd["S0"].clone()
+    S_ref = d["S0"][:ns].double().numpy()
+    worst = 0.0
+    for t in range(steps):
+        o = kla.decode_step(dd["q"][t], dd["k"][t], dd["v"][t],
+                            dd["log_alpha"][t], dd["eta"][t], S, eps=d["eps"])
+        o_ref, S_ref = oracle.kla_decode_step(
+            d["q"][t, :ns], d["k"][t, :ns], d["v"][t, :ns],
+            d["log_alpha"][t, :ns], d["eta"][t, :ns], d["eps"], S_ref)
+        worst = max(worst, rel_err(o[:ns], o_ref))
+    torch.cuda.synchronize()
+    assert worst <= 2e-2
+    assert rel_err(S[:ns], S_ref) <= 1e-4
+
+
+def test_prefill_then_decode_handoff():
+    """A forward pass over the first 100 tokens followed by decode steps for
+    the next 20 equals one recurrence over all 120 tokens."""
+    inp = gen.prefill_inputs(gen.LAYER_1B, B=2, T=120, H=2)
+    o_ref, h_ref = oracle_fwd(inp)
+    d = to_dev(inp)
+    sl = slice(0, 100)
+    o, S = kla.chunk_fwd(d["q"][:, sl].contiguous(), d["k"][:, sl].contiguous(),
+                         d["v"][:, sl].contiguous(),
+                         d["log_alpha"][:, sl].contiguous(),
+                         d["eta"][:, sl].contiguous(), d["eps"], d["h0"],
+                         C=64)
+    outs = [o]
+    for t in range(100, 120):
+        outs.append(kla.decode_step(
+            d["q"][:, t].contiguous(), d["k"][:, t].contiguous(),
+            d["v"][:, t].contiguous(), d["log_alpha"][:, t].contiguous(),
+            d["eta"][:, t].contiguous(), S, eps=d["eps"])[:, None])
+    torch.cuda.synchronize()
+    assert rel_err(torch.cat(outs, 1), o_ref) <= 2e-2
+    assert rel_err(S, h_ref) <= 2e-2

@@ -214,3 +214,32 @@ def test_prefill_then_decode_handoff():
     torch.cuda.synchronize()
     assert rel_err(torch.cat(outs, 1), o_ref) <= 2e-2
     assert rel_err(S, h_ref) <= 2e-2
+
+
+# ---------------------------------------------------------------- kernel paths
+
+@pytest.mark.parametrize("T", [64, 65, 128, 200, 1000])
+def test_tensor_core_path_against_oracle(T):
+    """The tcgen05 kernel alone (bf16, d=128, C=64), several chunks with and
+    without a ragged tail, with a random initial state."""
+    inp = gen.prefill_inputs(gen.LAYER_1B, B=2, T=T, H=3)
+    check_fwd(inp, "tc")
+
+
+def test_tensor_core_and_cuda_core_paths_agree():
+    inp = gen.prefill_inputs(gen.LONG_CTX, B=1, T=640, H=2)
+    o1, h1 = run_fwd(inp, "tc")
+    o2, h2 = run_fwd(inp, "simt")
+    assert rel_err(o1, o2.double().cpu().numpy()) <= 2e-2
+    assert rel_err(h1, h2.double().cpu().numpy()) <= 2e-2
+
+
+def test_tensor_core_zero_initial_state_and_no_hT():
+    inp = gen.prefill_inputs(gen.LAYER_340M, B=1, T=130, H=2)
+    d = to_dev(inp)
+    o, hT = kla.chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["eta"],
+                          d["eps"], None, C=64, algo="tc", want_state=False)
+    torch.cuda.synchronize()
+    assert hT is None
+    o_ref, _ = oracle_fwd(inp)
+    assert rel_err(o, o_ref) <= 2e-2

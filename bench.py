@@ -80,66 +80,140 @@ def decode_bytes(w) -> int:
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    """SM clock and throttle reasons sampled during the timed region.
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,"
-              "clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    Reads NVML directly through ctypes (every ~1 ms, so that even a timed
+    region of a few milliseconds is covered); falls back to `nvidia-smi -lms
+    200` when NVML cannot be loaded.  Only reads; changes no GPU setting."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, index: int):
         self.index = index
+        self.samples = []           # (sm_mhz, max_mhz, reason_bits)
+        self.stop = threading.Event()
+        self.nvml = None
         self.proc = None
-        self.lines = []
+
+    def _nvml_handle(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        bus = None
+        try:
+            pr = torch.cuda.get_device_properties(self.index)
+            bus = "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id,
+                                        pr.pci_device_id)
+        except Exception:
+            bus = None
+        if bus is None or lib.nvmlDeviceGetHandleByPciBusId_v2(
+                bus.encode(), ctypes.byref(h)) != 0:
+            if lib.nvmlDeviceGetHandleByIndex_v2(self.index,
+                                                 ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+        fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, fn
+
+    def _run_nvml(self):
+        import ctypes
+        lib, h, reasons_fn = self.nvml
+        cur, mx = ctypes.c_uint(), ctypes.c_uint()
+        bits = ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(cur)) == 0 and
+                    lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0
+                    and reasons_fn(h, ctypes.byref(bits)) == 0):
+                self.samples.append((cur.value, mx.value, bits.value))
+            time.sleep(0.001)
+
+    def _run_smi(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                b = 0
+                for bit, p in zip((0x8, 0x40, 0x20, 0x4), parts[2:]):
+                    if p.lower().startswith("active"):
+                        b |= bit
+                self.samples.append((float(parts[0]), float(parts[1]), b))
+            except ValueError:
+                continue
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index),
-                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE,
-                stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.nvml = self._nvml_handle()
+            self.thread = threading.Thread(target=self._run_nvml, daemon=True)
+        except Exception:
+            self.nvml = None
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index),
+                     "--query-gpu=clocks.sm,clocks.max.sm,"
+                     "clocks_event_reasons.hw_slowdown,"
+                     "clocks_event_reasons.hw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_power_cap",
+                     "--format=csv,noheader,nounits", "-lms", "200"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                    text=True)
+                self.thread = threading.Thread(target=self._run_smi,
+                                               daemon=True)
+            except OSError:
+                self.thread = None
+        if self.thread is not None:
             self.thread.start()
-        except OSError:
-            self.proc = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
+        self.stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread is not None:
             self.thread.join(timeout=2)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
-                 "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) != 7:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for n, p in zip(names, parts[3:]):
-                if p.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+        if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
                     "samples": 0}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        sm = [s[0] for s in self.samples]
+        reasons = set()
+        for _, _, b in self.samples:
+            for bit, name in self.REASONS.items():
+                if b & bit:
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)),
+                "sm_max_mhz": float(max(s[1] for s in self.samples)),
+                "reasons": sorted(reasons), "samples": len(self.samples),
+                "source": "nvml" if self.nvml else "nvidia-smi"}
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu capture of `kernel`, or
+    None when the kernel's sources changed since that capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            entry = json.load(f)[kernel]
+        h = hashlib.sha256()
+        for name in entry["sources"]:
+            with open(os.path.join(ROOT, "linear_attention_delta_gb300",
+                                   "csrc", name), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] != entry["source_sha16"]:
+            return None
+        return entry["dram_read_bytes"] + entry["dram_write_bytes"]
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def dist_setup():
@@ -307,6 +381,23 @@ def cpu_baseline_prefill(inp, budget_s=30.0):
                        f"(fp64 C recurrence, OpenMP over batch x head)")
 
 
+def run_only(args):
+    """A single kernel on its workload, for profiler captures: warm-up
+    launches then `--steps` launches, no other GPU work besides input setup
+    (and, for the forward pass, the L2 flush between launches)."""
+    kla.load_library()
+    if args.only == "prefill":
+        w = gen.LAYER_1B
+        pf = bench_prefill(w, args.steps, args.warmup, 1, 0)
+        print(json.dumps({"only": "prefill", "workload": w.name,
+                          "ms_per_launch": round(pf["ms"], 5)}))
+    else:
+        w = gen.DECODE
+        ms = bench_decode(w, args.steps, args.warmup)
+        print(json.dumps({"only": "decode", "workload": w.name,
+                          "ms_per_launch": round(ms, 5)}))
+
+
 def run_ours(args):
     world, rank, local = dist_setup()
     hbm, tf_burst, tf_sus, peak_src = peaks()
@@ -323,7 +414,7 @@ def run_ours(args):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1),
                 "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4),
-                "traffic": args.traffic,
+                "traffic": profiled_traffic("kla_chunk_tc"),
                 "kernel": "kla_chunk_fwd (tensor-core path)"
                 if w.dtype == "bf16" else "kla_chunk_fwd",
                 "algorithmic_bytes_per_launch": nbytes,
@@ -352,7 +443,8 @@ def run_ours(args):
                   "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
                                "peak": hbm, "unit": "GB/s",
                                "frac": round(gbs / hbm, 4),
-                               "bytes_per_step": dbytes},
+                               "bytes_per_step": dbytes,
+                               "traffic": profiled_traffic("kla_decode")},
                   "timed_steps": args.decode_steps,
                   "token_inputs": "50 distinct draws cycled"}
 
@@ -431,9 +523,12 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu dram bytes per launch of the forward kernel")
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="run one kernel alone (profiler captures)")
     args = ap.parse_args()
+    if args.only:
+        run_only(args)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

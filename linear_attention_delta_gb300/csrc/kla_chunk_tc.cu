@@ -63,9 +63,12 @@ constexpr int kBD = kSBuf + 16384;           // blockdiag(TW, TU), 2 x 16 KB
 constexpr int kPBuf = kBD + 32768;           // P, 64 x 64 K-major
 constexpr int kUtBuf = kPBuf + 8192;         // U~ (bf16), MN-major B
 constexpr int kUtsBuf = kUtBuf + 8192;       // Gamma_C U~ (bf16), MN-major B
-constexpr int kAStride = 68;                 // fp32 A row stride (floats)
+constexpr int kAStride = 68;                 // fp32 A / T row stride (floats)
 constexpr int kAF32 = kUtsBuf + 8192;        // fp32 strictly-lower A
-constexpr int kGF32 = kAF32 + kC * kAStride * 4;
+constexpr int kTF32 = kAF32 + kC * kAStride * 4;   // fp32 T = A^{-1}
+constexpr int kYStride = 17;
+constexpr int kYF32 = kTF32 + kC * kAStride * 4;   // 6 blocks T_ii A_im
+constexpr int kGF32 = kYF32 + 6 * 16 * kYStride * 4;
 constexpr int kBeta = kGF32 + 256;
 constexpr int kWTot = kBeta + 256;
 constexpr int kBars = kWTot + 16;
@@ -141,6 +144,112 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t addr, uint32_t lbo) {
     return tc::sdesc_sw128(addr, lbo, 1024);
 }
 
+// T = A^{-1} for the 64 x 64 unit lower-triangular A (strictly lower part in
+// Af, zeros elsewhere), blocked in 16 x 16 tiles and computed in fp32 by all
+// 128 threads:
+//   T_ii = A_ii^{-1}                       (column substitution, 64 threads)
+//   Y_im = T_ii A_im                       (i > m, six tiles in parallel)
+//   T_ij = -sum_{m=j}^{i-1} Y_im T_mj      (by distance i - j = 1, 2, 3)
+// Tiles of T above the diagonal are never read.
+__device__ __forceinline__ void invert_unit_lower64(const float* Af, float* Tf,
+                                                    float* Yf, int tid) {
+    if (tid < kC) {
+        const int bb = tid >> 4, cl = tid & 15;
+        const float* Ab = Af + (16 * bb) * kAStride + 16 * bb;
+        float t[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) t[r] = (r == cl) ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < 16; ++r) {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < r; i += 2) {
+                a0 = fmaf(Ab[r * kAStride + i], t[i], a0);
+                if (i + 1 < r) a1 = fmaf(Ab[r * kAStride + i + 1], t[i + 1], a1);
+            }
+            if (r > cl) t[r] = -(a0 + a1);
+        }
+        float* Tb = Tf + (16 * bb) * kAStride + 16 * bb + cl;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Tb[r * kAStride] = t[r];
+    }
+    __syncthreads();
+    // Y_im = T_ii A_im, tile yb = i(i-1)/2 + m
+#pragma unroll
+    for (int j = 0; j < 12; ++j) {
+        const int e = tid + kThreads * j;
+        const int yb = e >> 8, r = (e >> 4) & 15, c = e & 15;
+        const int i = yb < 1 ? 1 : (yb < 3 ? 2 : 3);
+        const int m = yb - i * (i - 1) / 2;
+        const float* Tr = Tf + (16 * i + r) * kAStride + 16 * i;
+        const float* Ac = Af + (16 * i) * kAStride + 16 * m + c;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+            a0 = fmaf(Tr[k], Ac[k * kAStride], a0);
+            a1 = fmaf(Tr[k + 1], Ac[(k + 1) * kAStride], a1);
+        }
+        Yf[(yb * 16 + r) * kYStride + c] = a0 + a1;
+    }
+    __syncthreads();
+    // distance 1: T_{i,i-1} = -Y_{i,i-1} T_{i-1,i-1}
+#pragma unroll
+    for (int j = 0; j < 6; ++j) {
+        const int e = tid + kThreads * j;
+        const int i = 1 + (e >> 8), r = (e >> 4) & 15, c = e & 15;
+        const float* Y = Yf + ((i * (i - 1) / 2 + i - 1) * 16 + r) * kYStride;
+        const float* Tc = Tf + (16 * (i - 1)) * kAStride + 16 * (i - 1) + c;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+            a0 = fmaf(Y[k], Tc[k * kAStride], a0);
+            a1 = fmaf(Y[k + 1], Tc[(k + 1) * kAStride], a1);
+        }
+        Tf[(16 * i + r) * kAStride + 16 * (i - 1) + c] = -(a0 + a1);
+    }
+    __syncthreads();
+    // distance 2: T_{i,i-2} = -(Y_{i,i-2} T_{i-2,i-2} + Y_{i,i-1} T_{i-1,i-2})
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int e = tid + kThreads * j;
+        const int i = 2 + (e >> 8), r = (e >> 4) & 15, c = e & 15;
+        const int jj = i - 2;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm) {
+            const int m = jj + mm;
+            const float* Y = Yf + ((i * (i - 1) / 2 + m) * 16 + r) * kYStride;
+            const float* Tc = Tf + (16 * m) * kAStride + 16 * jj + c;
+#pragma unroll
+            for (int k = 0; k < 16; k += 2) {
+                a0 = fmaf(Y[k], Tc[k * kAStride], a0);
+                a1 = fmaf(Y[k + 1], Tc[(k + 1) * kAStride], a1);
+            }
+        }
+        Tf[(16 * i + r) * kAStride + 16 * jj + c] = -(a0 + a1);
+    }
+    __syncthreads();
+    // distance 3: T_30 = -(Y_30 T_00 + Y_31 T_10 + Y_32 T_20)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int e = tid + kThreads * j;
+        const int r = (e >> 4) & 15, c = e & 15;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 3; ++m) {
+            const float* Y = Yf + ((3 + m) * 16 + r) * kYStride;
+            const float* Tc = Tf + (16 * m) * kAStride + c;
+#pragma unroll
+            for (int k = 0; k < 16; k += 2) {
+                a0 = fmaf(Y[k], Tc[k * kAStride], a0);
+                a1 = fmaf(Y[k + 1], Tc[(k + 1) * kAStride], a1);
+            }
+        }
+        Tf[(48 + r) * kAStride + c] = -(a0 + a1);
+    }
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -150,6 +259,8 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = tc::smem_u32(sm);
     float* Af = reinterpret_cast<float*>(sm + kAF32);
+    float* Tf = reinterpret_cast<float*>(sm + kTF32);
+    float* Yf = reinterpret_cast<float*>(sm + kYF32);
     float* gS = reinterpret_cast<float*>(sm + kGF32);
     float* betaS = reinterpret_cast<float*>(sm + kBeta);
     float* wtot = reinterpret_cast<float*>(sm + kWTot);
@@ -178,13 +289,12 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc::tmem_alloc(tmem_slot, kTmemCols);
         tc::tmem_relinquish();
     }
-    // zero blocks of blockdiag(TW, TU): box0 rows 64..127, box1 rows 0..63
+    // blockdiag(TW, TU) starts all zero; per chunk only the lower 16x16
+    // tiles of TW (box0 rows 0..63) and TU (box1 rows 64..127) are written.
     {
         uint4 z = make_uint4(0, 0, 0, 0);
-        for (int i = tid; i < 512; i += kThreads) {
-            *reinterpret_cast<uint4*>(sm + kBD + 8192 + 16 * i) = z;
-            *reinterpret_cast<uint4*>(sm + kBD + 16384 + 16 * i) = z;
-        }
+        for (int i = tid; i < 2048; i += kThreads)
+            *reinterpret_cast<uint4*>(sm + kBD + 16 * i) = z;
     }
     // initial state: row tid of S (64 columns of this CTA's half)
     float S[kNV];
@@ -330,36 +440,34 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         __syncthreads();
 
-        // ---- T = A^{-1}: column substitution, thread c owns column c ----
-        if (tid < kC) {
-            const int cc = tid;
-            float t[kC];
+        // ---- T = A^{-1} (blocked, fp32) ----
+        invert_unit_lower64(Af, Tf, Yf, tid);
+        // TW = T Diag(beta gamma) -> box0 rows 0..63, TU = T Diag(beta) ->
+        // box1 rows 64..127, lower 16x16 tiles only (the rest stays zero).
+        // Item = (row r, 8-column chunk q): 64 rows x 8 chunks.
 #pragma unroll
-            for (int r = 0; r < kC; ++r) t[r] = (r == cc) ? 1.f : 0.f;
+        for (int j = 0; j < 4; ++j) {
+            const int e = tid + kThreads * j;
+            const int r = e >> 3, q = e & 7;
+            if ((q >> 1) <= (r >> 4)) {
+                const float* Tr = Tf + r * kAStride + 8 * q;
+                float vw[8], vu[8];
 #pragma unroll
-            for (int r = 1; r < kC; ++r) {
-                const float* Ar = Af + r * kAStride;
-                float acc = 0.f;
-#pragma unroll
-                for (int i = 0; i < r; i += 4) {
-                    const float4 a = *reinterpret_cast<const float4*>(Ar + i);
-                    acc = fmaf(a.x, t[i], acc);
-                    if (i + 1 < r) acc = fmaf(a.y, t[i + 1], acc);
-                    if (i + 2 < r) acc = fmaf(a.z, t[i + 2], acc);
-                    if (i + 3 < r) acc = fmaf(a.w, t[i + 3], acc);
+                for (int k = 0; k < 8; ++k) {
+                    const float tv = (8 * q + k <= r) ? Tr[k] : 0.f;
+                    const float bc = betaS[8 * q + k];
+                    vu[k] = tv * bc;
+                    vw[k] = vu[k] * __expf(gS[8 * q + k]);
                 }
-                if (r > cc) t[r] = -acc;
-            }
-            const float bc = betaS[cc];
-            const float bgc = bc * __expf(gS[cc]);
-            __nv_bfloat16* bd0 = reinterpret_cast<__nv_bfloat16*>(sm + kBD);
-            __nv_bfloat16* bd1 =
-                reinterpret_cast<__nv_bfloat16*>(sm + kBD + 16384);
-#pragma unroll
-            for (int r = 0; r < kC; ++r) {
-                bd0[tc::sw128_offset(r, cc) >> 1] = __float2bfloat16_rn(t[r] * bgc);
-                bd1[tc::sw128_offset(kC + r, cc) >> 1] =
-                    __float2bfloat16_rn(t[r] * bc);
+                uint4 w4, u4;
+                w4.x = pack_bf16(vw[0], vw[1]); w4.y = pack_bf16(vw[2], vw[3]);
+                w4.z = pack_bf16(vw[4], vw[5]); w4.w = pack_bf16(vw[6], vw[7]);
+                u4.x = pack_bf16(vu[0], vu[1]); u4.y = pack_bf16(vu[2], vu[3]);
+                u4.z = pack_bf16(vu[4], vu[5]); u4.w = pack_bf16(vu[6], vu[7]);
+                *reinterpret_cast<uint4*>(sm + kBD + r * 128 +
+                                          ((q ^ (r & 7)) << 4)) = w4;
+                *reinterpret_cast<uint4*>(sm + kBD + 16384 + (64 + r) * 128 +
+                                          ((q ^ (r & 7)) << 4)) = u4;
             }
         }
         tc::fence_proxy_async_smem();

@@ -12,23 +12,25 @@
 // i.e. the gated-DeltaNet block solver with B = Diag(beta) as the only
 // change (gist.science/es/paper/2605.08587, section "Implementacion").
 //
-// Work decomposition: one CTA per (batch, head, half of dv); the CTA walks
-// the chunks of its sequence in order with its 128 x 64 slice of S resident
-// in registers (fp32, one key row per thread) and a bf16 copy in shared
-// memory as the MMA operand.  Per chunk, five tcgen05 MMAs (bf16 operands,
-// fp32 accumulation in TMEM):
-//   (1) G  = [K; Q] K^T                  -> K K^T, Q K^T          (128x64x128)
-//   (2) [W; U] = blockdiag(TW, TU) [K; V] -> W, U                 (128x128x128)
-//   (3) X  = [Q; W] S                    -> Q S, W S              (128x64x128)
-//   (4) dS = K^T Diag(Gamma_C) U~                                 (128x64x64)
-//   (5) OI = [P; -] U~,  P = Gamma o Q K^T (lower incl.)          (128x64x64)
-// CUDA cores do the elementwise work, the gates, and T = A^{-1} (fp32 column
-// substitution).  q, k, v tiles arrive by TMA (128-byte swizzle, double
-// buffered one chunk ahead); o and hT are written with vector stores.
+// Work decomposition: one CTA per (batch, head, half of dv), 256 threads in
+// two specialised warpgroups that run one chunk apart:
+//   * intra warpgroup (warps 0-3), chunk c+1:  G = [K;Q] K^T on the tensor
+//     cores, beta and the cumulative decay, the Gamma-masked A and P,
+//     T = A^{-1} (fp32 substitution on the 16x16 diagonal tiles, warp-level
+//     mma for the off-diagonal tiles), TW = T Diag(beta gamma) and
+//     TU = T Diag(beta), then W = TW K and U = TU V on the tensor cores and
+//     W as a bf16 operand in shared memory;
+//   * state warpgroup (warps 4-7), chunk c:  W S and Q S, U~ = U - W S,
+//     dS = K^T Diag(Gamma_C) U~ and P U~ on the tensor cores; the 128 x 64
+//     fp32 state slice lives in registers (one key row per thread), its bf16
+//     copy in shared memory is the MMA operand; o is written from registers.
+// The warpgroups hand over through mbarriers (W ready / U consumed / chunk
+// done).  q, k, v tiles arrive by TMA (128-byte swizzle) in a three-deep
+// ring, refilled by the state warpgroup as it frees each stage.
 //
-// Every mbarrier wait is bounded (2 s): on time-out the CTA records a fault
-// in the library's fault word, drains its outstanding copies and MMAs (again
-// bounded), frees TMEM and returns.
+// Every mbarrier wait is bounded (2 s) and also gives up when the other
+// warpgroup has failed: the CTA then records a fault in the library's fault
+// word, drains what it issued (bounded), frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -46,50 +48,70 @@ __device__ unsigned int g_fault_word = 0;
 constexpr int kC = 64;        // chunk length
 constexpr int kD = 128;       // dk = dv
 constexpr int kNV = 64;       // dv columns per CTA
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
+constexpr int kNS = 3;        // TMA stages
 
 // ---- shared memory map (bytes from a 1024-aligned base) -------------------
-// stage s (s = 0, 1) at s * kStage:  per key half h in {0, 1}:
-//   K_h at h*24K, Q_h at h*24K + 8K, W_h at h*24K + 16K   (each 64 x 64 bf16)
-//   V   at 48K                                           (64 x 64 bf16)
-// [K_h; Q_h] and [Q_h; W_h] are therefore contiguous 128-row K-major operands.
-constexpr int kHalfStride = 24576;
+// stage (40 KB): K_0 | Q_0 | K_1 | Q_1 | V   (each 64 rows x 128 B, swizzled;
+// K_h / Q_h hold key dims 64h..64h+63).  [K_h; Q_h] is a 128-row K-major
+// operand; the 64 rows after Q_h, W_h, TU and P are don't-care rows of padded
+// M=128 MMAs whose TMEM lanes 64..127 are never read.
 constexpr int kOffQ = 8192;
-constexpr int kOffW = 16384;
-constexpr int kOffV = 49152;
-constexpr int kStage = 57344;
-constexpr int kSBuf = 2 * kStage;            // bf16 S, 128 x 64, MN-major B
-constexpr int kBD = kSBuf + 16384;           // blockdiag(TW, TU), 2 x 16 KB
-constexpr int kPBuf = kBD + 32768;           // P, 64 x 64 K-major
-constexpr int kUtBuf = kPBuf + 8192;         // U~ (bf16), MN-major B
-constexpr int kUtsBuf = kUtBuf + 8192;       // Gamma_C U~ (bf16), MN-major B
-constexpr int kAStride = 68;                 // fp32 A / T row stride (floats)
-constexpr int kAF32 = kUtsBuf + 8192;        // fp32 strictly-lower A
-constexpr int kTF32 = kAF32 + kC * kAStride * 4;   // fp32 T = A^{-1}
-constexpr int kYStride = 17;
-constexpr int kYF32 = kTF32 + kC * kAStride * 4;   // 6 blocks T_ii A_im
-constexpr int kGF32 = kYF32 + 6 * 16 * kYStride * 4;
-constexpr int kBeta = kGF32 + 256;
-constexpr int kWTot = kBeta + 256;
-constexpr int kBars = kWTot + 16;
-constexpr int kSmemUsed = kBars + 64;
+constexpr int kHalf = 16384;
+constexpr int kOffV = 32768;
+constexpr int kStage = 40960;
+constexpr int kWBuf = kNS * kStage;          // W_0 | W_1   (K-major, 64 rows)
+constexpr int kSBuf = kWBuf + 16384;         // bf16 S, 128 x 64, MN-major
+constexpr int kTWU = kSBuf + 16384;          // TW (rows 0..63) | TU
+constexpr int kPBuf = kTWU + 16384;          // P, two buffers
+constexpr int kUtBuf = kPBuf + 16384;        // U~ bf16, MN-major
+constexpr int kUtsBuf = kUtBuf + 8192;       // Diag(Gamma_C) U~ bf16
+constexpr int kTileF = 16 * 17;              // fp32 16x16 tile, row stride 17
+constexpr int kADiag = kUtsBuf + 8192;       // 4 fp32 diagonal tiles of A
+constexpr int kAOff = kADiag + 4 * kTileF * 4;   // 6 bf16 tiles A_im, i > m
+constexpr int kTF = kAOff + 6 * 256 * 2;     // 10 fp32 tiles T_ij, i >= j
+constexpr int kGBuf = kTF + 10 * kTileF * 4; // 2 x {g2, beta, beta*gamma}
+constexpr int kGBufStride = 3 * 64;          // floats per buffer
+constexpr int kBars = kGBuf + 2 * kGBufStride * 4;
+constexpr int kNumBars = 10;
+constexpr int kMisc = kBars + 8 * kNumBars;  // abort flag, warp total, TMEM
+constexpr int kSmemUsed = kMisc + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kBars % 8 == 0, "mbarrier alignment");
 constexpr uint32_t kTmaBytes = 2 * 16384 + 8192;
 
+// mbarrier slots
+constexpr int kBarTma = 0;     // kNS: stage full (TMA)
+constexpr int kBarG = 3;       // G MMA done
+constexpr int kBarWU = 4;      // W, U MMAs done
+constexpr int kBarX = 5;       // W S done
+constexpr int kBarDS = 6;      // Q S, dS, P U~ done
+constexpr int kBarWReady = 7;  // intra -> state: W (smem), U (TMEM), P, gates
+constexpr int kBarWUFree = 8;  // state -> intra: U read and W S done
+constexpr int kBarSDone = 9;   // state -> intra: chunk finished
+
 // ---- TMEM columns ----------------------------------------------------------
-constexpr uint32_t kColG = 0;      // 64
-constexpr uint32_t kColWU = 64;    // 128
-constexpr uint32_t kColX = 192;    // 64
-constexpr uint32_t kColDS = 256;   // 64
-constexpr uint32_t kColOI = 320;   // 64
+constexpr uint32_t kColG = 0;      // 64: lanes 0..63 K K^T, 64..127 Q K^T
+constexpr uint32_t kColW = 64;     // 128: lanes 0..63 W
+constexpr uint32_t kColU = 192;    // 64: lanes 0..63 U
+constexpr uint32_t kColWS = 256;   // 64: lanes 0..63 W S
+constexpr uint32_t kColQS = 320;   // 64: lanes 0..63 Q S
+constexpr uint32_t kColDS = 384;   // 64: lane = key row
+constexpr uint32_t kColOI = 448;   // 64: lanes 0..63 P U~
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kIdG = tc::idesc_bf16(128, 64, false, false);
-constexpr uint32_t kIdWU = tc::idesc_bf16(128, 128, false, true);
-constexpr uint32_t kIdX = tc::idesc_bf16(128, 64, false, true);
+constexpr uint32_t kIdW = tc::idesc_bf16(128, 128, false, true);
+constexpr uint32_t kIdN64 = tc::idesc_bf16(128, 64, false, true);
 constexpr uint32_t kIdDS = tc::idesc_bf16(128, 64, true, true);
-constexpr uint32_t kIdOI = tc::idesc_bf16(128, 64, false, true);
+
+constexpr int kBarIntra = 1;   // named barrier ids
+constexpr int kBarState = 2;
+constexpr int kBarW13 = 3;     // intra warps 1..3
+constexpr int kBarW23 = 4;     // intra warps 2..3
+
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct TcParams {
     const float* log_alpha;
@@ -101,23 +123,17 @@ struct TcParams {
     int T, H;
 };
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
 // Write 64 fp32 values as one 128-byte swizzled bf16 row.
 __device__ __forceinline__ void st_row_sw128(uint8_t* base, int row,
                                              const float* x) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         uint4 v;
-        v.x = pack_bf16(x[8 * j + 0], x[8 * j + 1]);
-        v.y = pack_bf16(x[8 * j + 2], x[8 * j + 3]);
-        v.z = pack_bf16(x[8 * j + 4], x[8 * j + 5]);
-        v.w = pack_bf16(x[8 * j + 6], x[8 * j + 7]);
-        const int chunk = j ^ (row & 7);
-        *reinterpret_cast<uint4*>(base + row * 128 + chunk * 16) = v;
+        v.x = tc::pack_bf16x2(x[8 * j + 0], x[8 * j + 1]);
+        v.y = tc::pack_bf16x2(x[8 * j + 2], x[8 * j + 3]);
+        v.z = tc::pack_bf16x2(x[8 * j + 4], x[8 * j + 5]);
+        v.w = tc::pack_bf16x2(x[8 * j + 6], x[8 * j + 7]);
+        *reinterpret_cast<uint4*>(base + row * 128 + ((j ^ (row & 7)) << 4)) = v;
     }
 }
 
@@ -130,32 +146,154 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* x) {
     tc::tmem_ld_wait();
 }
 
-__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity) {
-    const bool ok = tc::mbar_wait(bar, parity);
-    return __syncthreads_or(ok ? 0 : 1) == 0;
-}
-
-// K-major SW128 descriptor (rows 128 B apart, 8-row atoms 1024 B apart).
 __device__ __forceinline__ uint64_t desc_k(uint32_t addr) {
     return tc::sdesc_sw128(addr, 16, 1024);
 }
-// MN-major SW128 descriptor: `lbo` = bytes between 64-wide MN atoms.
 __device__ __forceinline__ uint64_t desc_mn(uint32_t addr, uint32_t lbo) {
     return tc::sdesc_sw128(addr, lbo, 1024);
 }
 
-// T = A^{-1} for the 64 x 64 unit lower-triangular A (strictly lower part in
-// Af, zeros elsewhere), blocked in 16 x 16 tiles and computed in fp32 by all
-// 128 threads:
-//   T_ii = A_ii^{-1}                       (column substitution, 64 threads)
-//   Y_im = T_ii A_im                       (i > m, six tiles in parallel)
-//   T_ij = -sum_{m=j}^{i-1} Y_im T_mj      (by distance i - j = 1, 2, 3)
-// Tiles of T above the diagonal are never read.
-__device__ __forceinline__ void invert_unit_lower64(const float* Af, float* Tf,
-                                                    float* Yf, int tid) {
-    if (tid < kC) {
+// Every thread of a warpgroup waits on the mbarrier, then the warpgroup
+// agrees on the outcome (true = all saw the phase complete).  On failure the
+// CTA-wide abort flag is raised so that the other warpgroup stops too.
+__device__ __forceinline__ bool wg_wait(uint64_t* bar, uint32_t parity,
+                                        int* abort_flag, int bar_id) {
+    const bool ok = tc::mbar_wait_or_abort(bar, parity, abort_flag);
+    const bool any_fail = tc::named_bar_or(bar_id, 128, !ok);
+    if (any_fail) *reinterpret_cast<volatile int*>(abort_flag) = 1;
+    return !any_fail;
+}
+
+__device__ __forceinline__ uint32_t ld_bf16_pair(const __nv_bfloat16* p0,
+                                                 const __nv_bfloat16* p1) {
+    const uint32_t lo = *reinterpret_cast<const unsigned short*>(p0);
+    const uint32_t hi = *reinterpret_cast<const unsigned short*>(p1);
+    return lo | (hi << 16);
+}
+
+// packed index of lower tile (i, j), i >= j
+__host__ __device__ constexpr int tri(int i) { return i * (i + 1) / 2; }
+
+// A fragment (16x16, row-major) of an fp32 tile with row stride 17.
+__device__ __forceinline__ void afrag_f32(const float* t, int g, int q,
+                                          uint32_t (&a)[4]) {
+    a[0] = tc::pack_bf16x2(t[g * 17 + 2 * q], t[g * 17 + 2 * q + 1]);
+    a[1] = tc::pack_bf16x2(t[(g + 8) * 17 + 2 * q],
+                           t[(g + 8) * 17 + 2 * q + 1]);
+    a[2] = tc::pack_bf16x2(t[g * 17 + 2 * q + 8], t[g * 17 + 2 * q + 9]);
+    a[3] = tc::pack_bf16x2(t[(g + 8) * 17 + 2 * q + 8],
+                           t[(g + 8) * 17 + 2 * q + 9]);
+}
+
+// acc[nt] += X * Z for the two 8-column halves nt; X an A fragment, Z a
+// 16x16 fp32 tile (row stride 17).
+__device__ __forceinline__ void mm_tile_f32(float (&acc)[2][4],
+                                            const uint32_t (&x)[4],
+                                            const float* z, int g, int q) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int n = nt * 8 + g;
+        const uint32_t b0 = tc::pack_bf16x2(z[(2 * q) * 17 + n],
+                                            z[(2 * q + 1) * 17 + n]);
+        const uint32_t b1 = tc::pack_bf16x2(z[(2 * q + 8) * 17 + n],
+                                            z[(2 * q + 9) * 17 + n]);
+        tc::mma_m16n8k16(acc[nt], x, b0, b1);
+    }
+}
+
+// Same with Z a bf16 16x16 tile (row stride 16).
+__device__ __forceinline__ void mm_tile_bf16(float (&acc)[2][4],
+                                             const uint32_t (&x)[4],
+                                             const __nv_bfloat16* z, int g,
+                                             int q) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int n = nt * 8 + g;
+        const uint32_t b0 = ld_bf16_pair(z + (2 * q) * 16 + n,
+                                         z + (2 * q + 1) * 16 + n);
+        const uint32_t b1 = ld_bf16_pair(z + (2 * q + 8) * 16 + n,
+                                         z + (2 * q + 9) * 16 + n);
+        tc::mma_m16n8k16(acc[nt], x, b0, b1);
+    }
+}
+
+// -acc (a 16x16 result in accumulator-fragment layout) -> fp32 tile.
+__device__ __forceinline__ void store_neg_tile(float* t,
+                                               const float (&acc)[2][4], int g,
+                                               int q) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int c = nt * 8 + 2 * q;
+        t[g * 17 + c] = -acc[nt][0];
+        t[g * 17 + c + 1] = -acc[nt][1];
+        t[(g + 8) * 17 + c] = -acc[nt][2];
+        t[(g + 8) * 17 + c + 1] = -acc[nt][3];
+    }
+}
+
+__device__ __forceinline__ void zero_acc(float (&acc)[2][4]) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[nt][k] = 0.f;
+}
+
+// Off-diagonal tiles of block row I of T = A^{-1}, by warp I (I = 1..3):
+//   Y_Im = T_II A_Im (m < I), kept in registers as A fragments;
+//   T_Ij = -sum_{m=j}^{I-1} Y_Im T_mj, for j = I-1, I-2, I-3 in turn, with
+//   barriers between the distances because T_mj comes from other warps.
+template <int I>
+__device__ __forceinline__ void offdiag_row(const __nv_bfloat16* Ao, float* Tt,
+                                            int lane) {
+    const int g = lane >> 2, q = lane & 3;
+    uint32_t ta[4];
+    afrag_f32(Tt + (tri(I) + I) * kTileF, g, q, ta);
+    uint32_t ya[I][4];
+#pragma unroll
+    for (int m = 0; m < I; ++m) {
+        float acc[2][4];
+        zero_acc(acc);
+        mm_tile_bf16(acc, ta, Ao + (tri(I - 1) + m) * 256, g, q);
+        ya[m][0] = tc::pack_bf16x2(acc[0][0], acc[0][1]);
+        ya[m][1] = tc::pack_bf16x2(acc[0][2], acc[0][3]);
+        ya[m][2] = tc::pack_bf16x2(acc[1][0], acc[1][1]);
+        ya[m][3] = tc::pack_bf16x2(acc[1][2], acc[1][3]);
+    }
+    {   // distance 1
+        float acc[2][4];
+        zero_acc(acc);
+        mm_tile_f32(acc, ya[I - 1], Tt + (tri(I - 1) + I - 1) * kTileF, g, q);
+        store_neg_tile(Tt + (tri(I) + I - 1) * kTileF, acc, g, q);
+    }
+    tc::named_bar_sync(kBarW13, 96);
+    if constexpr (I >= 2) {   // distance 2
+        float acc[2][4];
+        zero_acc(acc);
+        mm_tile_f32(acc, ya[I - 2], Tt + (tri(I - 2) + I - 2) * kTileF, g, q);
+        mm_tile_f32(acc, ya[I - 1], Tt + (tri(I - 1) + I - 2) * kTileF, g, q);
+        store_neg_tile(Tt + (tri(I) + I - 2) * kTileF, acc, g, q);
+        tc::named_bar_sync(kBarW23, 64);
+    }
+    if constexpr (I == 3) {   // distance 3
+        float acc[2][4];
+        zero_acc(acc);
+        mm_tile_f32(acc, ya[0], Tt + tri(0) * kTileF, g, q);
+        mm_tile_f32(acc, ya[1], Tt + tri(1) * kTileF, g, q);
+        mm_tile_f32(acc, ya[2], Tt + tri(2) * kTileF, g, q);
+        store_neg_tile(Tt + tri(3) * kTileF, acc, g, q);
+    }
+}
+
+// T = A^{-1} (64x64 unit lower triangular) by the 128 intra threads.
+// A: fp32 diagonal tiles (strictly lower part, zero above) and bf16 tiles
+// A_im (i > m) at tri(i-1) + m.  T: fp32 tiles (i >= j) at tri(i) + j.
+__device__ __forceinline__ void invert_tiles(const float* Ad,
+                                             const __nv_bfloat16* Ao,
+                                             float* Tt, int tid) {
+    const int warp = tid >> 5;
+    if (warp < 2) {   // T_ii = A_ii^{-1}: column substitution, fp32
         const int bb = tid >> 4, cl = tid & 15;
-        const float* Ab = Af + (16 * bb) * kAStride + 16 * bb;
+        const float* Ab = Ad + bb * kTileF;
         float t[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) t[r] = (r == cl) ? 1.f : 0.f;
@@ -164,90 +302,21 @@ __device__ __forceinline__ void invert_unit_lower64(const float* Af, float* Tf,
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll
             for (int i = 0; i < r; i += 2) {
-                a0 = fmaf(Ab[r * kAStride + i], t[i], a0);
-                if (i + 1 < r) a1 = fmaf(Ab[r * kAStride + i + 1], t[i + 1], a1);
+                a0 = fmaf(Ab[r * 17 + i], t[i], a0);
+                if (i + 1 < r) a1 = fmaf(Ab[r * 17 + i + 1], t[i + 1], a1);
             }
             if (r > cl) t[r] = -(a0 + a1);
         }
-        float* Tb = Tf + (16 * bb) * kAStride + 16 * bb + cl;
+        float* Tb = Tt + (tri(bb) + bb) * kTileF + cl;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Tb[r * kAStride] = t[r];
+        for (int r = 0; r < 16; ++r) Tb[r * 17] = t[r];
     }
-    __syncthreads();
-    // Y_im = T_ii A_im, tile yb = i(i-1)/2 + m
-#pragma unroll
-    for (int j = 0; j < 12; ++j) {
-        const int e = tid + kThreads * j;
-        const int yb = e >> 8, r = (e >> 4) & 15, c = e & 15;
-        const int i = yb < 1 ? 1 : (yb < 3 ? 2 : 3);
-        const int m = yb - i * (i - 1) / 2;
-        const float* Tr = Tf + (16 * i + r) * kAStride + 16 * i;
-        const float* Ac = Af + (16 * i) * kAStride + 16 * m + c;
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-            a0 = fmaf(Tr[k], Ac[k * kAStride], a0);
-            a1 = fmaf(Tr[k + 1], Ac[(k + 1) * kAStride], a1);
-        }
-        Yf[(yb * 16 + r) * kYStride + c] = a0 + a1;
-    }
-    __syncthreads();
-    // distance 1: T_{i,i-1} = -Y_{i,i-1} T_{i-1,i-1}
-#pragma unroll
-    for (int j = 0; j < 6; ++j) {
-        const int e = tid + kThreads * j;
-        const int i = 1 + (e >> 8), r = (e >> 4) & 15, c = e & 15;
-        const float* Y = Yf + ((i * (i - 1) / 2 + i - 1) * 16 + r) * kYStride;
-        const float* Tc = Tf + (16 * (i - 1)) * kAStride + 16 * (i - 1) + c;
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-            a0 = fmaf(Y[k], Tc[k * kAStride], a0);
-            a1 = fmaf(Y[k + 1], Tc[(k + 1) * kAStride], a1);
-        }
-        Tf[(16 * i + r) * kAStride + 16 * (i - 1) + c] = -(a0 + a1);
-    }
-    __syncthreads();
-    // distance 2: T_{i,i-2} = -(Y_{i,i-2} T_{i-2,i-2} + Y_{i,i-1} T_{i-1,i-2})
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int e = tid + kThreads * j;
-        const int i = 2 + (e >> 8), r = (e >> 4) & 15, c = e & 15;
-        const int jj = i - 2;
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int mm = 0; mm < 2; ++mm) {
-            const int m = jj + mm;
-            const float* Y = Yf + ((i * (i - 1) / 2 + m) * 16 + r) * kYStride;
-            const float* Tc = Tf + (16 * m) * kAStride + 16 * jj + c;
-#pragma unroll
-            for (int k = 0; k < 16; k += 2) {
-                a0 = fmaf(Y[k], Tc[k * kAStride], a0);
-                a1 = fmaf(Y[k + 1], Tc[(k + 1) * kAStride], a1);
-            }
-        }
-        Tf[(16 * i + r) * kAStride + 16 * jj + c] = -(a0 + a1);
-    }
-    __syncthreads();
-    // distance 3: T_30 = -(Y_30 T_00 + Y_31 T_10 + Y_32 T_20)
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int e = tid + kThreads * j;
-        const int r = (e >> 4) & 15, c = e & 15;
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int m = 0; m < 3; ++m) {
-            const float* Y = Yf + ((3 + m) * 16 + r) * kYStride;
-            const float* Tc = Tf + (16 * m) * kAStride + c;
-#pragma unroll
-            for (int k = 0; k < 16; k += 2) {
-                a0 = fmaf(Y[k], Tc[k * kAStride], a0);
-                a1 = fmaf(Y[k + 1], Tc[(k + 1) * kAStride], a1);
-            }
-        }
-        Tf[(48 + r) * kAStride + c] = -(a0 + a1);
-    }
-    __syncthreads();
+    tc::named_bar_sync(kBarIntra, 128);
+    const int lane = tid & 31;
+    if (warp == 1) offdiag_row<1>(Ao, Tt, lane);
+    else if (warp == 2) offdiag_row<2>(Ao, Tt, lane);
+    else if (warp == 3) offdiag_row<3>(Ao, Tt, lane);
+    tc::named_bar_sync(kBarIntra, 128);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -258,15 +327,14 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = tc::smem_u32(sm);
-    float* Af = reinterpret_cast<float*>(sm + kAF32);
-    float* Tf = reinterpret_cast<float*>(sm + kTF32);
-    float* Yf = reinterpret_cast<float*>(sm + kYF32);
-    float* gS = reinterpret_cast<float*>(sm + kGF32);
-    float* betaS = reinterpret_cast<float*>(sm + kBeta);
-    float* wtot = reinterpret_cast<float*>(sm + kWTot);
-    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + kBars);
-    uint64_t* bar_mma = bar_tma + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_tma + 3);
+    float* Ad = reinterpret_cast<float*>(sm + kADiag);
+    __nv_bfloat16* Ao = reinterpret_cast<__nv_bfloat16*>(sm + kAOff);
+    float* Tt = reinterpret_cast<float*>(sm + kTF);
+    float* gbuf = reinterpret_cast<float*>(sm + kGBuf);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+    int* abort_flag = reinterpret_cast<int*>(sm + kMisc);
+    float* wtot = reinterpret_cast<float*>(sm + kMisc + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc + 8);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -280,26 +348,22 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc::prefetch_tmap(&tm_q);
         tc::prefetch_tmap(&tm_k);
         tc::prefetch_tmap(&tm_v);
-        tc::mbar_init(&bar_tma[0], 1);
-        tc::mbar_init(&bar_tma[1], 1);
-        tc::mbar_init(bar_mma, 1);
+        for (int i = 0; i < kNumBars; ++i) tc::mbar_init(&bars[i], 1);
+        *abort_flag = 0;
         tc::fence_mbar_init();
     }
     if (warp == 0) {
         tc::tmem_alloc(tmem_slot, kTmemCols);
         tc::tmem_relinquish();
     }
-    // blockdiag(TW, TU) starts all zero; per chunk only the lower 16x16
-    // tiles of TW (box0 rows 0..63) and TU (box1 rows 64..127) are written.
-    {
-        uint4 z = make_uint4(0, 0, 0, 0);
-        for (int i = tid; i < 2048; i += kThreads)
-            *reinterpret_cast<uint4*>(sm + kBD + 16 * i) = z;
-    }
-    // initial state: row tid of S (64 columns of this CTA's half)
-    float S[kNV];
-    {
-        const float* src = p.h0 ? p.h0 + ((size_t)bh * kD + tid) * kD + j0
+    // TW | TU start all zero; per chunk only their lower 16x16 tiles change.
+    for (int i = tid; i < 1024; i += kThreads)
+        *reinterpret_cast<uint4*>(sm + kTWU + 16 * i) = make_uint4(0, 0, 0, 0);
+
+    float S[kNV];   // state rows (state warpgroup)
+    if (tid >= 128) {
+        const int row = tid - 128;
+        const float* src = p.h0 ? p.h0 + ((size_t)bh * kD + row) * kD + j0
                                 : nullptr;
 #pragma unroll
         for (int j = 0; j < kNV; j += 4) {
@@ -307,310 +371,364 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                            : make_float4(0.f, 0.f, 0.f, 0.f);
             S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
         }
-        st_row_sw128(sm + kSBuf, tid, S);
+        st_row_sw128(sm + kSBuf, row, S);
     }
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
 
-    if (tid == 0 && nchunks > 0) {
-        tc::mbar_arrive_expect_tx(&bar_tma[0], kTmaBytes);
-        uint8_t* st = sm;
-        tc::tma_load_4d(st, &tm_k, &bar_tma[0], 0, h, 0, b);
-        tc::tma_load_4d(st + kHalfStride, &tm_k, &bar_tma[0], 64, h, 0, b);
-        tc::tma_load_4d(st + kOffQ, &tm_q, &bar_tma[0], 0, h, 0, b);
-        tc::tma_load_4d(st + kHalfStride + kOffQ, &tm_q, &bar_tma[0], 64, h,
-                        0, b);
-        tc::tma_load_4d(st + kOffV, &tm_v, &bar_tma[0], j0, h, 0, b);
-    }
+    auto issue_tma = [&](int c) {
+        const int s = c % kNS;
+        uint8_t* st = sm + s * kStage;
+        const int t0 = c * kC;
+        uint64_t* bar = &bars[kBarTma + s];
+        tc::mbar_arrive_expect_tx(bar, kTmaBytes);
+        tc::tma_load_4d(st, &tm_k, bar, 0, h, t0, b);
+        tc::tma_load_4d(st + kOffQ, &tm_q, bar, 0, h, t0, b);
+        tc::tma_load_4d(st + kHalf, &tm_k, bar, 64, h, t0, b);
+        tc::tma_load_4d(st + kHalf + kOffQ, &tm_q, bar, 64, h, t0, b);
+        tc::tma_load_4d(st + kOffV, &tm_v, bar, j0, h, t0, b);
+    };
+    if (tid == 0)
+        for (int c = 0; c < kNS && c < nchunks; ++c) issue_tma(c);
 
-    // gates of the next chunk, prefetched into registers (rows 0..63)
-    auto load_gates = [&](int c, float& la, float& et) {
-        const int t = c * kC + tid;
-        if (tid < kC && t < T) {
-            const size_t off = ((size_t)b * T + t) * p.H + h;
-            la = p.log_alpha[off];
-            et = p.eta[off];
-        } else {
+    if (tid < 128) {
+        // ==================================================== intra warpgroup
+        const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
+        bool failed = false, g_pending = false, wu_pending = false;
+        auto load_gates = [&](int c, float& la, float& et) {
+            const int t = c * kC + tid;
             la = 0.f;
             et = 0.f;
-        }
-    };
-    float la_cur, eta_cur;
-    load_gates(0, la_cur, eta_cur);
-
-    uint32_t ph_tma[2] = {0, 0};
-    uint32_t ph_mma = 0;
-    bool failed = false;
-    bool tma_pending[2] = {nchunks > 0, false};
-    bool mma_pending = false;
-
-    for (int c = 0; c < nchunks; ++c) {
-        const int s = c & 1;
-        uint8_t* st = sm + s * kStage;
-        const uint32_t sst = sbase + s * kStage;
-        const int t0 = c * kC;
-
-        if (!wait_all(&bar_tma[s], ph_tma[s])) { failed = true; break; }
-        ph_tma[s] ^= 1;
-        tma_pending[s] = false;
-        if (c + 1 < nchunks) {
-            if (tid == 0) {
-                uint8_t* nx = sm + (s ^ 1) * kStage;
-                const int tn = t0 + kC;
-                tc::mbar_arrive_expect_tx(&bar_tma[s ^ 1], kTmaBytes);
-                tc::tma_load_4d(nx, &tm_k, &bar_tma[s ^ 1], 0, h, tn, b);
-                tc::tma_load_4d(nx + kHalfStride, &tm_k, &bar_tma[s ^ 1], 64, h,
-                                tn, b);
-                tc::tma_load_4d(nx + kOffQ, &tm_q, &bar_tma[s ^ 1], 0, h, tn,
-                                b);
-                tc::tma_load_4d(nx + kHalfStride + kOffQ, &tm_q,
-                                &bar_tma[s ^ 1], 64, h, tn, b);
-                tc::tma_load_4d(nx + kOffV, &tm_v, &bar_tma[s ^ 1], j0, h, tn,
-                                b);
+            if (tid < kC && t < T) {
+                const size_t off = ((size_t)b * T + t) * p.H + h;
+                la = p.log_alpha[off];
+                et = p.eta[off];
             }
-            tma_pending[s ^ 1] = true;
-        }
-        float la_nxt, eta_nxt;
-        load_gates(c + 1, la_nxt, eta_nxt);
-
-        // ---- (1) G = [K; Q] K^T ----
-        tc::tc_fence_after();
-        if (tid == 0) {
+        };
+        auto issue_g = [&](int c) {
+            const uint32_t sst = sbase + (c % kNS) * kStage;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t off = (ks >> 2) * kHalfStride + (ks & 3) * 32;
+                const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
                 tc::mma_bf16(tmem + kColG, desc_k(sst + off), desc_k(sst + off),
                              kIdG, ks > 0);
             }
-            tc::mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        // in-chunk cumulative log decay (rows 0..63: warps 0 and 1)
-        float gpart = la_cur;
-        if (warp < 2) {
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, gpart, off);
-                if ((tid & 31) >= off) gpart += y;
+            tc::mma_commit(&bars[kBarG]);
+        };
+        float la_cur, eta_cur;
+        load_gates(0, la_cur, eta_cur);
+        if (nchunks > 0) {
+            if (wg_wait(&bars[kBarTma], 0, abort_flag, kBarIntra)) {
+                tc::tc_fence_after();
+                if (tid == 0) issue_g(0);
+                g_pending = true;
+            } else {
+                failed = true;
             }
-            if ((tid & 31) == 31) wtot[warp] = gpart;
         }
-        if (!wait_all(bar_mma, ph_mma)) { failed = true; break; }
-        ph_mma ^= 1;
-        mma_pending = false;
-        tc::tc_fence_after();
+        for (int c = 0; c < nchunks && !failed; ++c) {
+            float la_nxt, eta_nxt;
+            load_gates(c + 1, la_nxt, eta_nxt);
+            float* gb = gbuf + (c & 1) * kGBufStride;   // g2 | beta | bg
 
-        float x[kC];
-        tmem_ld64(tlane + kColG, x);        // KK^T row (tid<64) / QK^T row
-        if (tid < kC) {
-            const float g = gpart + (tid >= 32 ? wtot[0] : 0.f);
-            gS[tid] = g;
-            float diag = 0.f;
+            // P and gate buffers of chunk c-2 released by the state side
+            if (c >= 2 && !wg_wait(&bars[kBarSDone], (c - 2) & 1, abort_flag,
+                                   kBarIntra)) { failed = true; break; }
+            // cumulative log2-decay: warp scans on rows 0..31 and 32..63
+            float g2 = la_cur * kLog2e;
+            if (warp < 2) {
 #pragma unroll
-            for (int j = 0; j < kC; ++j) diag = (j == tid) ? x[j] : diag;
-            const float denom = diag + p.eps;
-            betaS[tid] = denom == 0.f ? 0.f : eta_cur / denom;
-        }
-        __syncthreads();
-        if (tid < kC) {
-            const int r = tid;
-            const float gr = gS[r];
-            const float br = betaS[r];
-            float* Ar = Af + r * kAStride;
-#pragma unroll
-            for (int i = 0; i < kC; i += 4) {
-                float4 v;
-                v.x = (i + 0 < r) ? br * __expf(gr - gS[i + 0]) * x[i + 0] : 0.f;
-                v.y = (i + 1 < r) ? br * __expf(gr - gS[i + 1]) * x[i + 1] : 0.f;
-                v.z = (i + 2 < r) ? br * __expf(gr - gS[i + 2]) * x[i + 2] : 0.f;
-                v.w = (i + 3 < r) ? br * __expf(gr - gS[i + 3]) * x[i + 3] : 0.f;
-                *reinterpret_cast<float4*>(Ar + i) = v;
-            }
-        } else {
-            const int r = tid - kC;
-            const float gr = gS[r];
-#pragma unroll
-            for (int i = 0; i < kC; ++i)
-                x[i] = (i <= r) ? __expf(gr - gS[i]) * x[i] : 0.f;
-            st_row_sw128(sm + kPBuf, r, x);
-        }
-        __syncthreads();
-
-        // ---- T = A^{-1} (blocked, fp32) ----
-        invert_unit_lower64(Af, Tf, Yf, tid);
-        // TW = T Diag(beta gamma) -> box0 rows 0..63, TU = T Diag(beta) ->
-        // box1 rows 64..127, lower 16x16 tiles only (the rest stays zero).
-        // Item = (row r, 8-column chunk q): 64 rows x 8 chunks.
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = tid + kThreads * j;
-            const int r = e >> 3, q = e & 7;
-            if ((q >> 1) <= (r >> 4)) {
-                const float* Tr = Tf + r * kAStride + 8 * q;
-                float vw[8], vu[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float tv = (8 * q + k <= r) ? Tr[k] : 0.f;
-                    const float bc = betaS[8 * q + k];
-                    vu[k] = tv * bc;
-                    vw[k] = vu[k] * __expf(gS[8 * q + k]);
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, g2, off);
+                    if ((tid & 31) >= off) g2 += y;
                 }
-                uint4 w4, u4;
-                w4.x = pack_bf16(vw[0], vw[1]); w4.y = pack_bf16(vw[2], vw[3]);
-                w4.z = pack_bf16(vw[4], vw[5]); w4.w = pack_bf16(vw[6], vw[7]);
-                u4.x = pack_bf16(vu[0], vu[1]); u4.y = pack_bf16(vu[2], vu[3]);
-                u4.z = pack_bf16(vu[4], vu[5]); u4.w = pack_bf16(vu[6], vu[7]);
-                *reinterpret_cast<uint4*>(sm + kBD + r * 128 +
-                                          ((q ^ (r & 7)) << 4)) = w4;
-                *reinterpret_cast<uint4*>(sm + kBD + 16384 + (64 + r) * 128 +
-                                          ((q ^ (r & 7)) << 4)) = u4;
+                if (tid == 31) *wtot = g2;
             }
-        }
-        tc::fence_proxy_async_smem();
-        __syncthreads();
-        tc::tc_fence_after();
-
-        // ---- (2) [W; U] = blockdiag(TW, TU) [K; V] ----
-        if (tid == 0) {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t a = sbase + kBD + (ks >> 2) * 16384 + (ks & 3) * 32;
-                uint64_t bdesc;
-                if (ks < 4)
-                    bdesc = desc_mn(sst + (ks & 3) * 2048, kHalfStride);
-                else
-                    bdesc = desc_mn(sst + kOffV + (ks & 3) * 2048, 0);
-                tc::mma_bf16(tmem + kColWU, desc_k(a), bdesc, kIdWU, ks > 0);
+            if (!wg_wait(&bars[kBarG], c & 1, abort_flag, kBarIntra)) {
+                failed = true; break;
             }
-            tc::mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        if (!wait_all(bar_mma, ph_mma)) { failed = true; break; }
-        ph_mma ^= 1;
-        mma_pending = false;
-        tc::tc_fence_after();
-
-        if (tid < kC) {
-            // W row tid -> bf16 into W_0 (cols 0..63) and W_1 (cols 64..127);
-            // U (lanes 64..127) stays in TMEM until U~ is formed.
-            tmem_ld64(tlane + kColWU, x);
-            st_row_sw128(st + kOffW, tid, x);
-            tmem_ld64(tlane + kColWU + 64, x);
-            st_row_sw128(st + kHalfStride + kOffW, tid, x);
-        }
-        tc::fence_proxy_async_smem();
-        tc::tc_fence_before();
-        __syncthreads();
-        tc::tc_fence_after();
-
-        // ---- (3) X = [Q; W] S ----
-        if (tid == 0) {
+            g_pending = false;
+            tc::tc_fence_after();
+            float x[kC];
+            tmem_ld64(tlane + kColG, x);     // K K^T row / Q K^T row
+            if (tid < kC) {
+                if (tid >= 32) g2 += *wtot;
+                float diag = 0.f;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t a = sst + (ks >> 2) * kHalfStride + kOffQ + (ks & 3) * 32;
-                tc::mma_bf16(tmem + kColX, desc_k(a),
-                             desc_mn(sbase + kSBuf + ks * 2048, 0), kIdX, ks > 0);
+                for (int j = 0; j < kC; ++j) diag = (j == tid) ? x[j] : diag;
+                const float denom = diag + p.eps;
+                const float beta = denom == 0.f ? 0.f : eta_cur / denom;
+                gb[tid] = g2;
+                gb[kC + tid] = beta;
+                gb[2 * kC + tid] = beta * tc::ex2(g2);
             }
-            tc::mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        if (!wait_all(bar_mma, ph_mma)) { failed = true; break; }
-        ph_mma ^= 1;
-        mma_pending = false;
-        tc::tc_fence_after();
+            tc::named_bar_sync(kBarIntra, 128);
+            // ---- A (warps 0, 1) and P (warps 2, 3) ----
+            if (warp < 2) {
+                const int r = tid, ti = r >> 4, rr = r & 15;
+                const float gr = gb[r], br = gb[kC + r];
+                const int mmax = warp == 0 ? 1 : 3;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    if (m > mmax) break;
+                    float v[16];
+#pragma unroll
+                    for (int cc = 0; cc < 16; ++cc) {
+                        const int i = 16 * m + cc;
+                        v[cc] = (i < r) ? br * tc::ex2(gr - gb[i]) * x[i] : 0.f;
+                    }
+                    if (m < ti) {
+                        __nv_bfloat16* dst =
+                            Ao + (tri(ti - 1) + m) * 256 + rr * 16;
+#pragma unroll
+                        for (int cc = 0; cc < 16; cc += 8) {
+                            uint4 u;
+                            u.x = tc::pack_bf16x2(v[cc + 0], v[cc + 1]);
+                            u.y = tc::pack_bf16x2(v[cc + 2], v[cc + 3]);
+                            u.z = tc::pack_bf16x2(v[cc + 4], v[cc + 5]);
+                            u.w = tc::pack_bf16x2(v[cc + 6], v[cc + 7]);
+                            *reinterpret_cast<uint4*>(dst + cc) = u;
+                        }
+                    } else if (m == ti) {
+                        float* dst = Ad + ti * kTileF + rr * 17;
+#pragma unroll
+                        for (int cc = 0; cc < 16; ++cc) dst[cc] = v[cc];
+                    }
+                }
+            } else {
+                const int r = tid - kC;
+                const float gr = gb[r];
+                const int imax = warp == 2 ? 32 : 64;
+#pragma unroll
+                for (int i = 0; i < kC; ++i)
+                    x[i] = (i < imax && i <= r) ? tc::ex2(gr - gb[i]) * x[i]
+                                                : 0.f;
+                st_row_sw128(sm + kPBuf + (c & 1) * 8192, r, x);
+            }
+            tc::named_bar_sync(kBarIntra, 128);
 
-        const float g_last = gS[kC - 1];
-        if (tid >= kC) {                           // Q S stays in TMEM
-            const int r = tid - kC;
-            float u[kNV];
-            tmem_ld64(tlane + kColWU, u);          // U row
-            tmem_ld64(tlane + kColX, x);           // W S row
-#pragma unroll
-            for (int j = 0; j < kNV; ++j) u[j] -= x[j];   // U~ row
-            st_row_sw128(sm + kUtBuf, r, u);
-            const float dec = __expf(g_last - gS[r]);
-#pragma unroll
-            for (int j = 0; j < kNV; ++j) u[j] *= dec;
-            st_row_sw128(sm + kUtsBuf, r, u);
-        }
-        tc::fence_proxy_async_smem();
-        tc::tc_fence_before();
-        __syncthreads();
-        tc::tc_fence_after();
+            // ---- T = A^{-1} ----
+            invert_tiles(Ad, Ao, Tt, tid);
 
-        // ---- (4) dS = K^T Diag(Gamma_C) U~ ; (5) OI = [P; -] U~ ----
-        if (tid == 0) {
+            // ---- TW = T Diag(beta gamma) | TU = T Diag(beta), lower tiles --
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tmem + kColDS, desc_mn(sst + ks * 2048, kHalfStride),
-                             desc_mn(sbase + kUtsBuf + ks * 2048, 0), kIdDS,
-                             ks > 0);
+            for (int j = 0; j < 4; ++j) {
+                const int e = tid + 128 * j;
+                const int r = e >> 3, qq = e & 7;
+                const int ti = r >> 4, tj = qq >> 1;
+                if (tj <= ti) {
+                    const float* tr = Tt + (tri(ti) + tj) * kTileF +
+                                      (r & 15) * 17 + (qq & 1) * 8;
+                    float vw[8], vu[8];
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tmem + kColOI, desc_k(sbase + kPBuf + ks * 32),
-                             desc_mn(sbase + kUtBuf + ks * 2048, 0), kIdOI,
-                             ks > 0);
-            tc::mma_commit(bar_mma);
-        }
-        mma_pending = true;
-        if (!wait_all(bar_mma, ph_mma)) { failed = true; break; }
-        ph_mma ^= 1;
-        mma_pending = false;
-        tc::tc_fence_after();
-
-        {
-            const float gC = __expf(g_last);
-            tmem_ld64(tlane + kColDS, x);          // dS row tid
-#pragma unroll
-            for (int j = 0; j < kNV; ++j) S[j] = fmaf(gC, S[j], x[j]);
-            st_row_sw128(sm + kSBuf, tid, S);
-        }
-        if (tid < kC) {
-            float qs[kNV];
-            tmem_ld64(tlane + kColX, qs);          // Q S row
-            tmem_ld64(tlane + kColOI, x);          // P U~ row
-            const float gam = __expf(gS[tid]);
-#pragma unroll
-            for (int j = 0; j < kNV; ++j) qs[j] *= gam;
-            const int t = t0 + tid;
-            if (t < T) {
-                __nv_bfloat16* dst =
-                    p.o + (((size_t)b * T + t) * p.H + h) * kD + j0;
-#pragma unroll
-                for (int j = 0; j < kNV; j += 8) {
-                    uint4 v;
-                    v.x = pack_bf16(qs[j + 0] + x[j + 0], qs[j + 1] + x[j + 1]);
-                    v.y = pack_bf16(qs[j + 2] + x[j + 2], qs[j + 3] + x[j + 3]);
-                    v.z = pack_bf16(qs[j + 4] + x[j + 4], qs[j + 5] + x[j + 5]);
-                    v.w = pack_bf16(qs[j + 6] + x[j + 6], qs[j + 7] + x[j + 7]);
-                    *reinterpret_cast<uint4*>(dst + j) = v;
+                    for (int k = 0; k < 8; ++k) {
+                        const float tv = tr[k];
+                        vu[k] = tv * gb[kC + 8 * qq + k];
+                        vw[k] = tv * gb[2 * kC + 8 * qq + k];
+                    }
+                    uint4 w4, u4;
+                    w4.x = tc::pack_bf16x2(vw[0], vw[1]);
+                    w4.y = tc::pack_bf16x2(vw[2], vw[3]);
+                    w4.z = tc::pack_bf16x2(vw[4], vw[5]);
+                    w4.w = tc::pack_bf16x2(vw[6], vw[7]);
+                    u4.x = tc::pack_bf16x2(vu[0], vu[1]);
+                    u4.y = tc::pack_bf16x2(vu[2], vu[3]);
+                    u4.z = tc::pack_bf16x2(vu[4], vu[5]);
+                    u4.w = tc::pack_bf16x2(vu[6], vu[7]);
+                    const int swz = (qq ^ (r & 7)) << 4;
+                    *reinterpret_cast<uint4*>(sm + kTWU + r * 128 + swz) = w4;
+                    *reinterpret_cast<uint4*>(sm + kTWU + 8192 + r * 128 + swz) =
+                        u4;
                 }
             }
+            tc::fence_proxy_async_smem();
+            // TMEM W/U of chunk c-1 consumed, W buffer free (state side)
+            if (c >= 1) {
+                if (!wg_wait(&bars[kBarWUFree], (c - 1) & 1, abort_flag,
+                             kBarIntra)) { failed = true; break; }
+            } else {
+                tc::named_bar_sync(kBarIntra, 128);
+            }
+            tc::tc_fence_after();
+            if (tid == 0) {
+                const uint32_t sst = sbase + (c % kNS) * kStage;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + kColW, desc_k(sbase + kTWU + ks * 32),
+                                 desc_mn(sst + ks * 2048, kHalf), kIdW, ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + kColU,
+                                 desc_k(sbase + kTWU + 8192 + ks * 32),
+                                 desc_mn(sst + kOffV + ks * 2048, 0), kIdN64,
+                                 ks > 0);
+                tc::mma_commit(&bars[kBarWU]);
+            }
+            wu_pending = true;
+            // the next chunk's G as soon as its tiles have landed
+            if (c + 1 < nchunks) {
+                const int s1 = (c + 1) % kNS;
+                if (!wg_wait(&bars[kBarTma + s1], ((c + 1) / kNS) & 1,
+                             abort_flag, kBarIntra)) { failed = true; break; }
+                tc::tc_fence_after();
+                if (tid == 0) issue_g(c + 1);
+                g_pending = true;
+            }
+            if (!wg_wait(&bars[kBarWU], c & 1, abort_flag, kBarIntra)) {
+                failed = true; break;
+            }
+            wu_pending = false;
+            tc::tc_fence_after();
+            if (warp < 2) {   // W row -> bf16 K-major operand (two halves)
+                tmem_ld64(tlane + kColW, x);
+                st_row_sw128(sm + kWBuf, tid, x);
+                tmem_ld64(tlane + kColW + 64, x);
+                st_row_sw128(sm + kWBuf + 8192, tid, x);
+            }
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            tc::named_bar_sync(kBarIntra, 128);
+            if (tid == 0) tc::mbar_arrive(&bars[kBarWReady]);
+            la_cur = la_nxt;
+            eta_cur = eta_nxt;
         }
-        la_cur = la_nxt;
-        eta_cur = eta_nxt;
-        tc::fence_proxy_async_smem();
-        tc::tc_fence_before();
-        __syncthreads();
-        tc::tc_fence_after();
+        if (failed && tid == 0) {   // let issued MMAs finish (bounded)
+            if (g_pending) tc::mbar_wait(&bars[kBarG], 0, 100000000ull);
+            if (wu_pending) tc::mbar_wait(&bars[kBarWU], 0, 100000000ull);
+        }
+    } else {
+        // ==================================================== state warpgroup
+        const int sw = warp - 4;                 // TMEM lane quarter
+        const uint32_t tlane = tmem + ((uint32_t)(sw * 32) << 16);
+        const int row = tid - 128;               // TMEM lane = key row
+        bool failed = false, x_pending = false, ds_pending = false;
+        for (int c = 0; c < nchunks && !failed; ++c) {
+            const int s = c % kNS;
+            const uint32_t sst = sbase + s * kStage;
+            const float* gb = gbuf + (c & 1) * kGBufStride;
+            if (!wg_wait(&bars[kBarWReady], c & 1, abort_flag, kBarState)) {
+                failed = true; break;
+            }
+            tc::tc_fence_after();
+            if (tid == 128) {   // W S first (critical path), then Q S
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16(
+                        tmem + kColWS,
+                        desc_k(sbase + kWBuf + (ks >> 2) * 8192 + (ks & 3) * 32),
+                        desc_mn(sbase + kSBuf + ks * 2048, 0), kIdN64, ks > 0);
+                tc::mma_commit(&bars[kBarX]);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16(
+                        tmem + kColQS,
+                        desc_k(sst + (ks >> 2) * kHalf + kOffQ + (ks & 3) * 32),
+                        desc_mn(sbase + kSBuf + ks * 2048, 0), kIdN64, ks > 0);
+            }
+            x_pending = true;
+            if (!wg_wait(&bars[kBarX], c & 1, abort_flag, kBarState)) {
+                failed = true; break;
+            }
+            x_pending = false;
+            tc::tc_fence_after();
+            const float g_last = gb[kC - 1];
+            if (sw < 2) {   // rows 0..63: U~ = U - W S
+                float u[kNV], x[kNV];
+                tmem_ld64(tlane + kColU, u);
+                tmem_ld64(tlane + kColWS, x);
+#pragma unroll
+                for (int j = 0; j < kNV; ++j) u[j] -= x[j];
+                st_row_sw128(sm + kUtBuf, row, u);
+                const float dec = tc::ex2(g_last - gb[row]);
+#pragma unroll
+                for (int j = 0; j < kNV; ++j) u[j] *= dec;
+                st_row_sw128(sm + kUtsBuf, row, u);
+            }
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            tc::named_bar_sync(kBarState, 128);
+            tc::tc_fence_after();
+            if (tid == 128) {
+                tc::mbar_arrive(&bars[kBarWUFree]);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + kColDS, desc_mn(sst + ks * 2048, kHalf),
+                                 desc_mn(sbase + kUtsBuf + ks * 2048, 0), kIdDS,
+                                 ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(
+                        tmem + kColOI,
+                        desc_k(sbase + kPBuf + (c & 1) * 8192 + ks * 32),
+                        desc_mn(sbase + kUtBuf + ks * 2048, 0), kIdN64, ks > 0);
+                tc::mma_commit(&bars[kBarDS]);
+            }
+            ds_pending = true;
+            if (!wg_wait(&bars[kBarDS], c & 1, abort_flag, kBarState)) {
+                failed = true; break;
+            }
+            ds_pending = false;
+            tc::tc_fence_after();
+            {
+                float x[kNV];
+                const float gC = tc::ex2(g_last);
+                tmem_ld64(tlane + kColDS, x);
+#pragma unroll
+                for (int j = 0; j < kNV; ++j) S[j] = fmaf(gC, S[j], x[j]);
+                st_row_sw128(sm + kSBuf, row, S);
+            }
+            if (sw < 2) {   // rows 0..63: o = gamma Q S + P U~
+                float qs[kNV], x[kNV];
+                tmem_ld64(tlane + kColQS, qs);
+                tmem_ld64(tlane + kColOI, x);
+                const float gam = tc::ex2(gb[row]);
+                const int t = c * kC + row;
+                if (t < T) {
+                    __nv_bfloat16* dst =
+                        p.o + (((size_t)b * T + t) * p.H + h) * kD + j0;
+#pragma unroll
+                    for (int j = 0; j < kNV; j += 8) {
+                        uint4 v;
+                        v.x = tc::pack_bf16x2(fmaf(gam, qs[j + 0], x[j + 0]),
+                                              fmaf(gam, qs[j + 1], x[j + 1]));
+                        v.y = tc::pack_bf16x2(fmaf(gam, qs[j + 2], x[j + 2]),
+                                              fmaf(gam, qs[j + 3], x[j + 3]));
+                        v.z = tc::pack_bf16x2(fmaf(gam, qs[j + 4], x[j + 4]),
+                                              fmaf(gam, qs[j + 5], x[j + 5]));
+                        v.w = tc::pack_bf16x2(fmaf(gam, qs[j + 6], x[j + 6]),
+                                              fmaf(gam, qs[j + 7], x[j + 7]));
+                        *reinterpret_cast<uint4*>(dst + j) = v;
+                    }
+                }
+            }
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            tc::named_bar_sync(kBarState, 128);
+            if (tid == 128) {
+                tc::mbar_arrive(&bars[kBarSDone]);
+                if (c + kNS < nchunks) issue_tma(c + kNS);
+            }
+        }
+        if (failed && tid == 128) {   // let issued MMAs finish (bounded)
+            if (x_pending) tc::mbar_wait(&bars[kBarX], 0, 100000000ull);
+            if (ds_pending) tc::mbar_wait(&bars[kBarDS], 0, 100000000ull);
+        }
     }
 
-    if (failed) {
+    __syncthreads();
+    const bool any_failed = *reinterpret_cast<volatile int*>(abort_flag) != 0;
+    if (any_failed) {
         if (tid == 0) {
             atomicOr(&g_fault_word, 1u);
-            // drain what may still be in flight, each wait bounded
-            if (mma_pending) tc::mbar_wait(bar_mma, ph_mma, 100000000ull);
-            for (int i = 0; i < 2; ++i)
-                if (tma_pending[i])
-                    tc::mbar_wait(&bar_tma[i], ph_tma[i], 100000000ull);
+            for (int s = 0; s < kNS; ++s)   // copies possibly in flight
+                tc::mbar_wait(&bars[kBarTma + s], 0, 100000000ull);
         }
-        __syncthreads();
-    } else if (p.hT) {
-        float* dst = p.hT + ((size_t)bh * kD + tid) * kD + j0;
+    } else if (tid >= 128 && p.hT) {
+        const int row = tid - 128;
+        float* dst = p.hT + ((size_t)bh * kD + row) * kD + j0;
 #pragma unroll
         for (int j = 0; j < kNV; j += 4)
             *reinterpret_cast<float4*>(dst + j) =

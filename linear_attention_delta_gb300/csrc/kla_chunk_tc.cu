@@ -15,17 +15,21 @@
 // Work decomposition: one CTA per (batch, head, half of dv), 256 threads in
 // two specialised warpgroups that run one chunk apart:
 //   * intra warpgroup (warps 0-3), chunk c+1:  G = [K;Q] K^T on the tensor
-//     cores, beta and the cumulative decay, the Gamma-masked A and P,
-//     T = A^{-1} (fp32 substitution on the 16x16 diagonal tiles, warp-level
-//     mma for the off-diagonal tiles), TW = T Diag(beta gamma) and
-//     TU = T Diag(beta), then W = TW K and U = TU V on the tensor cores and
-//     W as a bf16 operand in shared memory;
-//   * state warpgroup (warps 4-7), chunk c:  W S and Q S, U~ = U - W S,
-//     dS = K^T Diag(Gamma_C) U~ and P U~ on the tensor cores; the 128 x 64
-//     fp32 state slice lives in registers (one key row per thread), its bf16
-//     copy in shared memory is the MMA operand; o is written from registers.
-// The warpgroups hand over through mbarriers (W ready / U consumed / chunk
-// done).  q, k, v tiles arrive by TMA (128-byte swizzle) in a three-deep
+//     cores, beta and the cumulative decay, the Gamma-masked A, T = A^{-1}
+//     (fp32 substitution on the 16x16 diagonal tiles, warp-level mma for the
+//     off-diagonal tiles) written straight out as TW = T Diag(beta gamma) and
+//     TU = T Diag(beta), then W = TW K and U = TU V issued on the tensor
+//     cores;
+//   * state warpgroup (warps 4-7), chunk c:  W to a bf16 operand,
+//     P = Gamma o Q K^T (warps 6, 7, off the critical path), U~ = U - W S
+//     accumulated in TMEM by a negated-operand MMA onto U, Q S,
+//     dS = K^T Diag(Gamma_C) U~ and P U~ on the tensor cores;
+//     the 128 x 64 fp32 state slice lives in registers (one key row per
+//     thread), its bf16 copy in shared memory is the MMA operand; o is
+//     written from registers.
+// The warpgroups hand over through mbarriers (chunk handed over / chunk
+// done); G, W and U have two TMEM buffers each, so the intra side never waits
+// for the state side to finish reading them.  q, k, v tiles arrive by TMA (128-byte swizzle) in a three-deep
 // ring, refilled by the state warpgroup as it frees each stage.
 //
 // Every mbarrier wait is bounded (2 s) and also gives up when the other
@@ -63,8 +67,8 @@ constexpr int kStage = 40960;
 constexpr int kWBuf = kNS * kStage;          // W_0 | W_1   (K-major, 64 rows)
 constexpr int kSBuf = kWBuf + 16384;         // bf16 S, 128 x 64, MN-major
 constexpr int kTWU = kSBuf + 16384;          // TW (rows 0..63) | TU
-constexpr int kPBuf = kTWU + 16384;          // P, two buffers
-constexpr int kUtBuf = kPBuf + 16384;        // U~ bf16, MN-major
+constexpr int kPBuf = kTWU + 16384;          // P, 64 x 64 K-major
+constexpr int kUtBuf = kPBuf + 8192;         // U~ bf16, MN-major
 constexpr int kUtsBuf = kUtBuf + 8192;       // Diag(Gamma_C) U~ bf16
 constexpr int kTileF = 16 * 17;              // fp32 16x16 tile, row stride 17
 constexpr int kADiag = kUtsBuf + 8192;       // 4 fp32 diagonal tiles of A
@@ -85,31 +89,33 @@ constexpr uint32_t kTmaBytes = 2 * 16384 + 8192;
 constexpr int kBarTma = 0;     // kNS: stage full (TMA)
 constexpr int kBarG = 3;       // G MMA done
 constexpr int kBarWU = 4;      // W, U MMAs done
-constexpr int kBarX = 5;       // W S done
+constexpr int kBarX = 5;       // U~ = U - W S formed in TMEM
 constexpr int kBarDS = 6;      // Q S, dS, P U~ done
-constexpr int kBarWReady = 7;  // intra -> state: W (smem), U (TMEM), P, gates
-constexpr int kBarWUFree = 8;  // state -> intra: U read and W S done
+constexpr int kBarWReady = 7;  // intra -> state: gates, W/U issued, G done
+constexpr int kBarWUAck = 8;   // state -> intra: passed its W/U wait (keeps
+                               //   the W/U barrier from running a phase ahead)
 constexpr int kBarSDone = 9;   // state -> intra: chunk finished
 
-// ---- TMEM columns ----------------------------------------------------------
-constexpr uint32_t kColG = 0;      // 64: lanes 0..63 K K^T, 64..127 Q K^T
-constexpr uint32_t kColW = 64;     // 128: lanes 0..63 W
-constexpr uint32_t kColU = 192;    // 64: lanes 0..63 U
-constexpr uint32_t kColWS = 256;   // 64: lanes 0..63 W S
-constexpr uint32_t kColQS = 320;   // 64: lanes 0..63 Q S
-constexpr uint32_t kColDS = 384;   // 64: lane = key row
-constexpr uint32_t kColOI = 448;   // 64: lanes 0..63 P U~
+// ---- TMEM columns (two buffers, by chunk parity b) -------------------------
+// G[b]: lanes 0..63 K K^T, lanes 64..127 Q K^T; then P U~ (lanes 0..63).
+// W[b]: lanes 0..63 W (128 cols); then Q S in its first 64 columns.
+// U[b]: lanes 0..63 U, then U~ = U - W S; then dS (lane = key row).
+constexpr uint32_t kColG = 0;      // + 64 b
+constexpr uint32_t kColW = 128;    // + 128 b
+constexpr uint32_t kColU = 384;    // + 64 b
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kIdG = tc::idesc_bf16(128, 64, false, false);
 constexpr uint32_t kIdW = tc::idesc_bf16(128, 128, false, true);
 constexpr uint32_t kIdN64 = tc::idesc_bf16(128, 64, false, true);
 constexpr uint32_t kIdDS = tc::idesc_bf16(128, 64, true, true);
+constexpr uint32_t kIdNegW = tc::idesc_bf16(128, 64, false, true, true);
 
 constexpr int kBarIntra = 1;   // named barrier ids
 constexpr int kBarState = 2;
 constexpr int kBarW13 = 3;     // intra warps 1..3
 constexpr int kBarW23 = 4;     // intra warps 2..3
+constexpr int kBarState01 = 5; // state warps 4, 5
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -139,10 +145,8 @@ __device__ __forceinline__ void st_row_sw128(uint8_t* base, int row,
 
 // 64 consecutive TMEM columns of this thread's lane -> x[0..63].
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* x) {
-    tc::tmem_ld16(taddr + 0, *reinterpret_cast<float(*)[16]>(x + 0));
-    tc::tmem_ld16(taddr + 16, *reinterpret_cast<float(*)[16]>(x + 16));
-    tc::tmem_ld16(taddr + 32, *reinterpret_cast<float(*)[16]>(x + 32));
-    tc::tmem_ld16(taddr + 48, *reinterpret_cast<float(*)[16]>(x + 48));
+    tc::tmem_ld32(taddr + 0, x);
+    tc::tmem_ld32(taddr + 32, x + 32);
     tc::tmem_ld_wait();
 }
 
@@ -217,17 +221,43 @@ __device__ __forceinline__ void mm_tile_bf16(float (&acc)[2][4],
     }
 }
 
-// -acc (a 16x16 result in accumulator-fragment layout) -> fp32 tile.
-__device__ __forceinline__ void store_neg_tile(float* t,
-                                               const float (&acc)[2][4], int g,
-                                               int q) {
+// Byte offset of element (row, col) in a K-major bf16 operand with 128-byte
+// swizzled rows (64 columns per row).
+__device__ __forceinline__ int sw_off(int row, int col) {
+    return row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1);
+}
+
+// Tile (I, J) of T, given as -acc in accumulator-fragment layout: keep the
+// fp32 copy when later tiles need it (tf != nullptr) and write the bf16
+// operands TW = T Diag(beta gamma) (rows 0..63 of twu) and TU = T Diag(beta)
+// (rows 64..127).  gb = {g2[64], beta[64], beta*gamma[64]} of this chunk.
+__device__ __forceinline__ void store_t_tile(float* tf, uint8_t* twu,
+                                             const float* gb, int I, int J,
+                                             const float (&acc)[2][4], int g,
+                                             int q) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
         const int c = nt * 8 + 2 * q;
-        t[g * 17 + c] = -acc[nt][0];
-        t[g * 17 + c + 1] = -acc[nt][1];
-        t[(g + 8) * 17 + c] = -acc[nt][2];
-        t[(g + 8) * 17 + c + 1] = -acc[nt][3];
+        const int col = 16 * J + c;
+        const float t00 = -acc[nt][0], t01 = -acc[nt][1];
+        const float t10 = -acc[nt][2], t11 = -acc[nt][3];
+        if (tf) {
+            tf[g * 17 + c] = t00;
+            tf[g * 17 + c + 1] = t01;
+            tf[(g + 8) * 17 + c] = t10;
+            tf[(g + 8) * 17 + c + 1] = t11;
+        }
+        const float b0 = gb[64 + col], b1 = gb[64 + col + 1];
+        const float w0 = gb[128 + col], w1 = gb[128 + col + 1];
+        const int r0 = 16 * I + g, r1 = r0 + 8;
+        *reinterpret_cast<uint32_t*>(twu + sw_off(r0, col)) =
+            tc::pack_bf16x2(t00 * w0, t01 * w1);
+        *reinterpret_cast<uint32_t*>(twu + sw_off(r1, col)) =
+            tc::pack_bf16x2(t10 * w0, t11 * w1);
+        *reinterpret_cast<uint32_t*>(twu + 8192 + sw_off(r0, col)) =
+            tc::pack_bf16x2(t00 * b0, t01 * b1);
+        *reinterpret_cast<uint32_t*>(twu + 8192 + sw_off(r1, col)) =
+            tc::pack_bf16x2(t10 * b0, t11 * b1);
     }
 }
 
@@ -242,8 +272,10 @@ __device__ __forceinline__ void zero_acc(float (&acc)[2][4]) {
 //   Y_Im = T_II A_Im (m < I), kept in registers as A fragments;
 //   T_Ij = -sum_{m=j}^{I-1} Y_Im T_mj, for j = I-1, I-2, I-3 in turn, with
 //   barriers between the distances because T_mj comes from other warps.
+// Tiles of block row 3 are never read again, so only TW/TU receive them.
 template <int I>
 __device__ __forceinline__ void offdiag_row(const __nv_bfloat16* Ao, float* Tt,
+                                            uint8_t* twu, const float* gb,
                                             int lane) {
     const int g = lane >> 2, q = lane & 3;
     uint32_t ta[4];
@@ -259,11 +291,13 @@ __device__ __forceinline__ void offdiag_row(const __nv_bfloat16* Ao, float* Tt,
         ya[m][2] = tc::pack_bf16x2(acc[1][0], acc[1][1]);
         ya[m][3] = tc::pack_bf16x2(acc[1][2], acc[1][3]);
     }
+    float* keep = I < 3 ? Tt : nullptr;
     {   // distance 1
         float acc[2][4];
         zero_acc(acc);
         mm_tile_f32(acc, ya[I - 1], Tt + (tri(I - 1) + I - 1) * kTileF, g, q);
-        store_neg_tile(Tt + (tri(I) + I - 1) * kTileF, acc, g, q);
+        store_t_tile(keep ? keep + (tri(I) + I - 1) * kTileF : nullptr, twu,
+                     gb, I, I - 1, acc, g, q);
     }
     tc::named_bar_sync(kBarW13, 96);
     if constexpr (I >= 2) {   // distance 2
@@ -271,7 +305,8 @@ __device__ __forceinline__ void offdiag_row(const __nv_bfloat16* Ao, float* Tt,
         zero_acc(acc);
         mm_tile_f32(acc, ya[I - 2], Tt + (tri(I - 2) + I - 2) * kTileF, g, q);
         mm_tile_f32(acc, ya[I - 1], Tt + (tri(I - 1) + I - 2) * kTileF, g, q);
-        store_neg_tile(Tt + (tri(I) + I - 2) * kTileF, acc, g, q);
+        store_t_tile(keep ? keep + (tri(I) + I - 2) * kTileF : nullptr, twu,
+                     gb, I, I - 2, acc, g, q);
         tc::named_bar_sync(kBarW23, 64);
     }
     if constexpr (I == 3) {   // distance 3
@@ -280,18 +315,22 @@ __device__ __forceinline__ void offdiag_row(const __nv_bfloat16* Ao, float* Tt,
         mm_tile_f32(acc, ya[0], Tt + tri(0) * kTileF, g, q);
         mm_tile_f32(acc, ya[1], Tt + tri(1) * kTileF, g, q);
         mm_tile_f32(acc, ya[2], Tt + tri(2) * kTileF, g, q);
-        store_neg_tile(Tt + tri(3) * kTileF, acc, g, q);
+        store_t_tile(nullptr, twu, gb, 3, 0, acc, g, q);
     }
 }
 
-// T = A^{-1} (64x64 unit lower triangular) by the 128 intra threads.
+// T = A^{-1} (64x64 unit lower triangular), written out as TW | TU.
 // A: fp32 diagonal tiles (strictly lower part, zero above) and bf16 tiles
-// A_im (i > m) at tri(i-1) + m.  T: fp32 tiles (i >= j) at tri(i) + j.
-__device__ __forceinline__ void invert_tiles(const float* Ad,
-                                             const __nv_bfloat16* Ao,
-                                             float* Tt, int tid) {
-    const int warp = tid >> 5;
-    if (warp < 2) {   // T_ii = A_ii^{-1}: column substitution, fp32
+// A_im (i > m) at tri(i-1) + m.  T: fp32 tiles (i >= j) at tri(i) + j, kept
+// for the tiles that later tiles are built from.
+//
+// Diagonal tiles T_ii = A_ii^{-1} (fp32 column substitution): thread
+// (bb = tid / 16, cl = tid % 16) of intra warps 0 and 1, i.e. each of those
+// warps inverts the two diagonal tiles of the rows it has just built.
+__device__ __forceinline__ void invert_diag_tiles(const float* Ad, float* Tt,
+                                                  uint8_t* twu,
+                                                  const float* gb, int tid) {
+    {
         const int bb = tid >> 4, cl = tid & 15;
         const float* Ab = Ad + bb * kTileF;
         float t[16];
@@ -308,16 +347,35 @@ __device__ __forceinline__ void invert_tiles(const float* Ad,
             if (r > cl) t[r] = -(a0 + a1);
         }
         float* Tb = Tt + (tri(bb) + bb) * kTileF + cl;
+        const int col = 16 * bb + cl;
+        const float bc = gb[64 + col], wc = gb[128 + col];
+        __nv_bfloat16* tw = reinterpret_cast<__nv_bfloat16*>(twu);
+        __nv_bfloat16* tu = reinterpret_cast<__nv_bfloat16*>(twu + 8192);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Tb[r * 17] = t[r];
+        for (int r = 0; r < 16; ++r) {
+            Tb[r * 17] = t[r];
+            const int off = sw_off(16 * bb + r, col) >> 1;
+            tw[off] = __float2bfloat16_rn(t[r] * wc);
+            tu[off] = __float2bfloat16_rn(t[r] * bc);
+        }
     }
-    tc::named_bar_sync(kBarIntra, 128);
-    const int lane = tid & 31;
-    if (warp == 1) offdiag_row<1>(Ao, Tt, lane);
-    else if (warp == 2) offdiag_row<2>(Ao, Tt, lane);
-    else if (warp == 3) offdiag_row<3>(Ao, Tt, lane);
-    tc::named_bar_sync(kBarIntra, 128);
 }
+
+// Off-diagonal tiles, after every diagonal tile is in place (warps 1..3).
+__device__ __forceinline__ void invert_offdiag_tiles(const __nv_bfloat16* Ao,
+                                                     float* Tt, uint8_t* twu,
+                                                     const float* gb,
+                                                     int tid) {
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    if (warp == 1) offdiag_row<1>(Ao, Tt, twu, gb, lane);
+    else if (warp == 2) offdiag_row<2>(Ao, Tt, twu, gb, lane);
+    else if (warp == 3) offdiag_row<3>(Ao, Tt, twu, gb, lane);
+}
+
+__device__ __forceinline__ uint32_t col_g(int c) { return kColG + 64 * (c & 1); }
+__device__ __forceinline__ uint32_t col_w(int c) { return kColW + 128 * (c & 1); }
+__device__ __forceinline__ uint32_t col_u(int c) { return kColU + 64 * (c & 1); }
 
 __global__ void __launch_bounds__(kThreads, 1)
 kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -413,8 +471,8 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-                tc::mma_bf16(tmem + kColG, desc_k(sst + off), desc_k(sst + off),
-                             kIdG, ks > 0);
+                tc::mma_bf16(tmem + col_g(c), desc_k(sst + off),
+                             desc_k(sst + off), kIdG, ks > 0);
             }
             tc::mma_commit(&bars[kBarG]);
         };
@@ -432,11 +490,10 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int c = 0; c < nchunks && !failed; ++c) {
             float la_nxt, eta_nxt;
             load_gates(c + 1, la_nxt, eta_nxt);
+            // gate buffer of chunk c-2: released (state side waited for it
+            // before G(c) was issued, see the end of the previous iteration)
             float* gb = gbuf + (c & 1) * kGBufStride;   // g2 | beta | bg
 
-            // P and gate buffers of chunk c-2 released by the state side
-            if (c >= 2 && !wg_wait(&bars[kBarSDone], (c - 2) & 1, abort_flag,
-                                   kBarIntra)) { failed = true; break; }
             // cumulative log2-decay: warp scans on rows 0..31 and 32..63
             float g2 = la_cur * kLog2e;
             if (warp < 2) {
@@ -453,8 +510,8 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             g_pending = false;
             tc::tc_fence_after();
             float x[kC];
-            tmem_ld64(tlane + kColG, x);     // K K^T row / Q K^T row
-            if (tid < kC) {
+            if (warp < 2) {
+                tmem_ld64(tlane + col_g(c), x);     // K K^T row tid
                 if (tid >= 32) g2 += *wtot;
                 float diag = 0.f;
 #pragma unroll
@@ -465,8 +522,15 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 gb[kC + tid] = beta;
                 gb[2 * kC + tid] = beta * tc::ex2(g2);
             }
-            tc::named_bar_sync(kBarIntra, 128);
-            // ---- A (warps 0, 1) and P (warps 2, 3) ----
+            // TW | TU are still read by the W, U MMAs of chunk c-1
+            if (c >= 1) {
+                if (!wg_wait(&bars[kBarWU], (c - 1) & 1, abort_flag,
+                             kBarIntra)) { failed = true; break; }
+                wu_pending = false;
+            } else {
+                tc::named_bar_sync(kBarIntra, 128);
+            }
+            // ---- A (warps 0, 1), then each warp inverts its diagonal tiles
             if (warp < 2) {
                 const int r = tid, ti = r >> 4, rr = r & 15;
                 const float gr = gb[r], br = gb[kC + r];
@@ -498,100 +562,50 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         for (int cc = 0; cc < 16; ++cc) dst[cc] = v[cc];
                     }
                 }
-            } else {
-                const int r = tid - kC;
-                const float gr = gb[r];
-                const int imax = warp == 2 ? 32 : 64;
-#pragma unroll
-                for (int i = 0; i < kC; ++i)
-                    x[i] = (i < imax && i <= r) ? tc::ex2(gr - gb[i]) * x[i]
-                                                : 0.f;
-                st_row_sw128(sm + kPBuf + (c & 1) * 8192, r, x);
+                __syncwarp();
+                invert_diag_tiles(Ad, Tt, sm + kTWU, gb, tid);
             }
             tc::named_bar_sync(kBarIntra, 128);
 
-            // ---- T = A^{-1} ----
-            invert_tiles(Ad, Ao, Tt, tid);
-
-            // ---- TW = T Diag(beta gamma) | TU = T Diag(beta), lower tiles --
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int e = tid + 128 * j;
-                const int r = e >> 3, qq = e & 7;
-                const int ti = r >> 4, tj = qq >> 1;
-                if (tj <= ti) {
-                    const float* tr = Tt + (tri(ti) + tj) * kTileF +
-                                      (r & 15) * 17 + (qq & 1) * 8;
-                    float vw[8], vu[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float tv = tr[k];
-                        vu[k] = tv * gb[kC + 8 * qq + k];
-                        vw[k] = tv * gb[2 * kC + 8 * qq + k];
-                    }
-                    uint4 w4, u4;
-                    w4.x = tc::pack_bf16x2(vw[0], vw[1]);
-                    w4.y = tc::pack_bf16x2(vw[2], vw[3]);
-                    w4.z = tc::pack_bf16x2(vw[4], vw[5]);
-                    w4.w = tc::pack_bf16x2(vw[6], vw[7]);
-                    u4.x = tc::pack_bf16x2(vu[0], vu[1]);
-                    u4.y = tc::pack_bf16x2(vu[2], vu[3]);
-                    u4.z = tc::pack_bf16x2(vu[4], vu[5]);
-                    u4.w = tc::pack_bf16x2(vu[6], vu[7]);
-                    const int swz = (qq ^ (r & 7)) << 4;
-                    *reinterpret_cast<uint4*>(sm + kTWU + r * 128 + swz) = w4;
-                    *reinterpret_cast<uint4*>(sm + kTWU + 8192 + r * 128 + swz) =
-                        u4;
-                }
-            }
+            // ---- off-diagonal tiles of T = A^{-1}, written as TW | TU ----
+            invert_offdiag_tiles(Ao, Tt, sm + kTWU, gb, tid);
             tc::fence_proxy_async_smem();
-            // TMEM W/U of chunk c-1 consumed, W buffer free (state side)
-            if (c >= 1) {
-                if (!wg_wait(&bars[kBarWUFree], (c - 1) & 1, abort_flag,
-                             kBarIntra)) { failed = true; break; }
-            } else {
-                tc::named_bar_sync(kBarIntra, 128);
-            }
+            tc::named_bar_sync(kBarIntra, 128);
+            // the state side must have passed its wait on the W/U(c-1)
+            // phase before W/U(c) can complete
+            if (c >= 1 && !wg_wait(&bars[kBarWUAck], (c - 1) & 1, abort_flag,
+                                   kBarIntra)) { failed = true; break; }
             tc::tc_fence_after();
             if (tid == 0) {
                 const uint32_t sst = sbase + (c % kNS) * kStage;
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tmem + kColW, desc_k(sbase + kTWU + ks * 32),
+                    tc::mma_bf16(tmem + col_w(c), desc_k(sbase + kTWU + ks * 32),
                                  desc_mn(sst + ks * 2048, kHalf), kIdW, ks > 0);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tmem + kColU,
+                    tc::mma_bf16(tmem + col_u(c),
                                  desc_k(sbase + kTWU + 8192 + ks * 32),
                                  desc_mn(sst + kOffV + ks * 2048, 0), kIdN64,
                                  ks > 0);
                 tc::mma_commit(&bars[kBarWU]);
+                tc::mbar_arrive(&bars[kBarWReady]);
             }
             wu_pending = true;
-            // the next chunk's G as soon as its tiles have landed
+            // the next chunk's G, once its tiles have landed and chunk c-1
+            // (last user of that G buffer and of the gate buffer) is done
             if (c + 1 < nchunks) {
                 const int s1 = (c + 1) % kNS;
                 if (!wg_wait(&bars[kBarTma + s1], ((c + 1) / kNS) & 1,
                              abort_flag, kBarIntra)) { failed = true; break; }
+                if (c >= 1 && !wg_wait(&bars[kBarSDone], (c - 1) & 1,
+                                       abort_flag, kBarIntra)) {
+                    failed = true; break;
+                }
                 tc::tc_fence_after();
                 if (tid == 0) issue_g(c + 1);
                 g_pending = true;
             }
-            if (!wg_wait(&bars[kBarWU], c & 1, abort_flag, kBarIntra)) {
-                failed = true; break;
-            }
-            wu_pending = false;
-            tc::tc_fence_after();
-            if (warp < 2) {   // W row -> bf16 K-major operand (two halves)
-                tmem_ld64(tlane + kColW, x);
-                st_row_sw128(sm + kWBuf, tid, x);
-                tmem_ld64(tlane + kColW + 64, x);
-                st_row_sw128(sm + kWBuf + 8192, tid, x);
-            }
-            tc::fence_proxy_async_smem();
-            tc::tc_fence_before();
-            tc::named_bar_sync(kBarIntra, 128);
-            if (tid == 0) tc::mbar_arrive(&bars[kBarWReady]);
             la_cur = la_nxt;
             eta_cur = eta_nxt;
         }
@@ -609,24 +623,68 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             const int s = c % kNS;
             const uint32_t sst = sbase + s * kStage;
             const float* gb = gbuf + (c & 1) * kGBufStride;
-            if (!wg_wait(&bars[kBarWReady], c & 1, abort_flag, kBarState)) {
+            if (!wg_wait(&bars[kBarWReady], c & 1, abort_flag, kBarState) ||
+                !wg_wait(&bars[kBarWU], c & 1, abort_flag, kBarState)) {
                 failed = true; break;
             }
+            if (tid == 128) tc::mbar_arrive(&bars[kBarWUAck]);
             tc::tc_fence_after();
-            if (tid == 128) {   // W S first (critical path), then Q S
+            if (sw < 2) {   // W row -> bf16 K-major operand (two halves)
+                float x[kNV];
+                tmem_ld64(tlane + col_w(c), x);
+                st_row_sw128(sm + kWBuf, row, x);
+                tmem_ld64(tlane + col_w(c) + 64, x);
+                st_row_sw128(sm + kWBuf + 8192, row, x);
+                tc::fence_proxy_async_smem();
+                tc::tc_fence_before();
+                tc::named_bar_sync(kBarState01, 64);
+                tc::tc_fence_after();
+                if (tid == 128) {
+                    // U~ = U - W S into U's columns (critical path), then Q S
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(
-                        tmem + kColWS,
-                        desc_k(sbase + kWBuf + (ks >> 2) * 8192 + (ks & 3) * 32),
-                        desc_mn(sbase + kSBuf + ks * 2048, 0), kIdN64, ks > 0);
-                tc::mma_commit(&bars[kBarX]);
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_bf16(tmem + col_u(c),
+                                     desc_k(sbase + kWBuf + (ks >> 2) * 8192 +
+                                            (ks & 3) * 32),
+                                     desc_mn(sbase + kSBuf + ks * 2048, 0),
+                                     kIdNegW, true);
+                    tc::mma_commit(&bars[kBarX]);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(
-                        tmem + kColQS,
-                        desc_k(sst + (ks >> 2) * kHalf + kOffQ + (ks & 3) * 32),
-                        desc_mn(sbase + kSBuf + ks * 2048, 0), kIdN64, ks > 0);
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_bf16(tmem + col_w(c),
+                                     desc_k(sst + (ks >> 2) * kHalf + kOffQ +
+                                            (ks & 3) * 32),
+                                     desc_mn(sbase + kSBuf + ks * 2048, 0),
+                                     kIdN64, ks > 0);
+                }
+            } else {        // P row = Gamma o Q K^T, lower incl.
+                const int r = row - kC;
+                const float gr = gb[r];
+                uint8_t* prow = sm + kPBuf + r * 128;
+                const int jmax = (r >> 3) + 1;   // 8-column groups needed
+#pragma unroll 1
+                for (int j = 0; j < 8; ++j) {
+                    uint4 v = make_uint4(0, 0, 0, 0);
+                    if (__any_sync(0xffffffffu, j < jmax)) {
+                        float x[8];
+                        tc::tmem_ld8(tlane + col_g(c) + 8 * j, x);
+                        const float4 g0 = *reinterpret_cast<const float4*>(gb + 8 * j);
+                        const float4 g1 = *reinterpret_cast<const float4*>(gb + 8 * j + 4);
+                        tc::tmem_ld_wait();
+                        const float gi[8] = {g0.x, g0.y, g0.z, g0.w,
+                                             g1.x, g1.y, g1.z, g1.w};
+                        float e[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            e[k] = (8 * j + k <= r) ? tc::ex2(gr - gi[k]) * x[k]
+                                                    : 0.f;
+                        v.x = tc::pack_bf16x2(e[0], e[1]);
+                        v.y = tc::pack_bf16x2(e[2], e[3]);
+                        v.z = tc::pack_bf16x2(e[4], e[5]);
+                        v.w = tc::pack_bf16x2(e[6], e[7]);
+                    }
+                    *reinterpret_cast<uint4*>(prow + ((j ^ (r & 7)) << 4)) = v;
+                }
             }
             x_pending = true;
             if (!wg_wait(&bars[kBarX], c & 1, abort_flag, kBarState)) {
@@ -635,12 +693,9 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             x_pending = false;
             tc::tc_fence_after();
             const float g_last = gb[kC - 1];
-            if (sw < 2) {   // rows 0..63: U~ = U - W S
-                float u[kNV], x[kNV];
-                tmem_ld64(tlane + kColU, u);
-                tmem_ld64(tlane + kColWS, x);
-#pragma unroll
-                for (int j = 0; j < kNV; ++j) u[j] -= x[j];
+            if (sw < 2) {   // rows 0..63: U~ and Diag(Gamma_C) U~ as operands
+                float u[kNV];
+                tmem_ld64(tlane + col_u(c), u);
                 st_row_sw128(sm + kUtBuf, row, u);
                 const float dec = tc::ex2(g_last - gb[row]);
 #pragma unroll
@@ -652,18 +707,17 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             tc::named_bar_sync(kBarState, 128);
             tc::tc_fence_after();
             if (tid == 128) {
-                tc::mbar_arrive(&bars[kBarWUFree]);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tmem + kColDS, desc_mn(sst + ks * 2048, kHalf),
+                    tc::mma_bf16(tmem + col_u(c), desc_mn(sst + ks * 2048, kHalf),
                                  desc_mn(sbase + kUtsBuf + ks * 2048, 0), kIdDS,
                                  ks > 0);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(
-                        tmem + kColOI,
-                        desc_k(sbase + kPBuf + (c & 1) * 8192 + ks * 32),
-                        desc_mn(sbase + kUtBuf + ks * 2048, 0), kIdN64, ks > 0);
+                    tc::mma_bf16(tmem + col_g(c),
+                                 desc_k(sbase + kPBuf + ks * 32),
+                                 desc_mn(sbase + kUtBuf + ks * 2048, 0), kIdN64,
+                                 ks > 0);
                 tc::mma_commit(&bars[kBarDS]);
             }
             ds_pending = true;
@@ -675,15 +729,15 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             {
                 float x[kNV];
                 const float gC = tc::ex2(g_last);
-                tmem_ld64(tlane + kColDS, x);
+                tmem_ld64(tlane + col_u(c), x);
 #pragma unroll
                 for (int j = 0; j < kNV; ++j) S[j] = fmaf(gC, S[j], x[j]);
                 st_row_sw128(sm + kSBuf, row, S);
             }
             if (sw < 2) {   // rows 0..63: o = gamma Q S + P U~
                 float qs[kNV], x[kNV];
-                tmem_ld64(tlane + kColQS, qs);
-                tmem_ld64(tlane + kColOI, x);
+                tmem_ld64(tlane + col_w(c), qs);
+                tmem_ld64(tlane + col_g(c), x);
                 const float gam = tc::ex2(gb[row]);
                 const int t = c * kC + row;
                 if (t < T) {

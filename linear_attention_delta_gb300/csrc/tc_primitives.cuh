@@ -266,12 +266,14 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 }
 
 // Instruction descriptor: bf16 A and B, fp32 D, dense.  a_mn / b_mn select
-// MN-major (transposed) operands.
+// MN-major (transposed) operands; neg_a computes D (+)= (-A) B.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn,
-                                                  bool b_mn) {
+                                                  bool b_mn,
+                                                  bool neg_a = false) {
     return (1u << 4)                         // D format: f32
            | (1u << 7)                       // A format: bf16
            | (1u << 10)                      // B format: bf16
+           | ((neg_a ? 1u : 0u) << 13)       // negate A
            | ((a_mn ? 1u : 0u) << 15)        // A major
            | ((b_mn ? 1u : 0u) << 16)        // B major
            | ((uint32_t)(N >> 3) << 17)      // N / 8
@@ -303,6 +305,35 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
           "=r"(u[5]), "=r"(u[6]), "=r"(u[7]), "=r"(u[8]), "=r"(u[9]),
           "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]),
           "=r"(u[15])
+        : "r"(taddr));
+}
+
+// 32 lanes x 8 consecutive 32-bit columns per warp.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&r)[8]) {
+    uint32_t* u = reinterpret_cast<uint32_t*>(r);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]),
+          "=r"(u[5]), "=r"(u[6]), "=r"(u[7])
+        : "r"(taddr));
+}
+
+// 32 lanes x 32 consecutive 32-bit columns per warp.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* r) {
+    uint32_t* u = reinterpret_cast<uint32_t*>(r);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%32];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]),
+          "=r"(u[5]), "=r"(u[6]), "=r"(u[7]), "=r"(u[8]), "=r"(u[9]),
+          "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]),
+          "=r"(u[15]), "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]),
+          "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]), "=r"(u[24]),
+          "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]),
+          "=r"(u[30]), "=r"(u[31])
         : "r"(taddr));
 }
 

@@ -249,8 +249,9 @@ def max_over_ranks(x: float, world: int) -> float:
 
 # ------------------------------------------------------------ our arm
 
-def bench_prefill(w, steps, warmup, world, gpu_index):
-    inp = gen.prefill_inputs(w)
+def bench_prefill(w, steps, warmup, world, gpu_index, rule="kaczmarz",
+                  inp=None):
+    inp = gen.prefill_inputs(w) if inp is None else inp
     dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
            for k, v in inp.items()}
     o = torch.empty_like(dev["v"])
@@ -261,7 +262,8 @@ def bench_prefill(w, steps, warmup, world, gpu_index):
 
     def step():
         kla.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["log_alpha"],
-                      dev["eta"], dev["eps"], dev["h0"], C=w.C, o=o, hT=hT)
+                      dev["eta"], dev["eps"], dev["h0"], C=w.C, o=o, hT=hT,
+                      rule=rule)
 
     for _ in range(warmup):
         flush.zero_()
@@ -448,6 +450,15 @@ def run_ours(args):
                   "timed_steps": args.decode_steps,
                   "token_inputs": "50 distinct draws cycled"}
 
+    # The learned-step (gated DeltaNet) rule on the same kernels and inputs,
+    # timed beside KLA: the pages claim equal prefill latency for the two.
+    gdn = bench_prefill(w, args.steps, args.warmup, world, local,
+                        rule="given", inp=pf["inputs"])
+    gdn_line = {"rule": "beta = eta (gated DeltaNet step)",
+                "ms_per_step": round(gdn["ms"], 5),
+                "tokens_per_s": round(world * tokens / (gdn["ms"] * 1e-3), 1),
+                "kla_over_gdn_time": round(ms / gdn["ms"], 4)}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_prefill(pf["inputs"])
@@ -463,7 +474,7 @@ def run_ours(args):
                        "l2": "flushed between timed steps (512 MiB write)"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": pf["launches"], "clocks": pf["clocks"],
-            "decode": decode,
+            "decode": decode, "gdn_mode": gdn_line,
             "per_step_ms": [round(x, 5) for x in pf["per_step_ms"]]}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -68,6 +68,14 @@ typedef enum {
     KLA_ALGO_TC = 2      /* tcgen05 tensor-core kernel: bf16, dk=dv=128, C=64 */
 } kla_algo;
 
+/* How the write step beta_t is formed from eta_t.
+ *   KLA_STEP_KACZMARZ: beta_t = eta_t / (||k_t||^2 + eps)  (the KLA rule)
+ *   KLA_STEP_GIVEN:    beta_t = eta_t, eps ignored  (the learned scalar step of
+ *                      gated DeltaNet, the rule KLA replaces -- page section
+ *                      "Declaracion del Problema"; same recurrence and block
+ *                      solver otherwise, section "Implementacion") */
+typedef enum { KLA_STEP_KACZMARZ = 0, KLA_STEP_GIVEN = 1 } kla_step_rule;
+
 /* Opaque stream handle; ABI-compatible with cudaStream_t / CUstream. */
 typedef struct CUstream_st* kla_stream_t;
 
@@ -101,16 +109,17 @@ KLA_API kla_status kla_chunk_fwd(const void* q, const void* k, const void* v,
                          kla_dtype dtype, kla_stream_t stream);
 
 /*
- * kla_chunk_fwd_ex -- kla_chunk_fwd with an explicit kernel choice.
- * KLA_ALGO_TC returns KLA_ERR_UNSUPPORTED_SHAPE unless dtype == KLA_BF16,
- * dk == dv == 128, C == 64 and q, k, v, o are 16-byte aligned.
+ * kla_chunk_fwd_ex -- kla_chunk_fwd with an explicit kernel choice and step
+ * rule.  KLA_ALGO_TC returns KLA_ERR_UNSUPPORTED_SHAPE unless dtype ==
+ * KLA_BF16, dk == dv == 128, C == 64 and q, k, v, o, h0, hT are 16-byte
+ * aligned.  An unknown algo or rule is KLA_ERR_INVALID_ARG.
  */
 KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
                             const float* log_alpha, const float* eta,
                             float eps, const float* h0, void* o, float* hT,
                             int B, int T, int H, int dk, int dv, int C,
                             kla_dtype dtype, kla_algo algo,
-                            kla_stream_t stream);
+                            kla_step_rule rule, kla_stream_t stream);
 
 /*
  * kla_decode_step -- one new token for each of N sequences x H heads (the
@@ -123,13 +132,20 @@ KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
  *   S          [N, H, dk, dv]  fp32    (read, then overwritten with S_t)
  *   o          [N, H, dv]      dtype   (written) = S_t^T q
  *
- * Supported: dk, dv in {16, 32, 64, 128}; N, H >= 0.  o must not alias S or
- * any input.  Errors as for kla_chunk_fwd.
+ * Supported: dk, dv in {16, 32, 64, 128}; N, H >= 0.  S must be 16-byte
+ * aligned.  o must not alias S or any input.  Errors as for kla_chunk_fwd.
  */
 KLA_API kla_status kla_decode_step(const void* q, const void* k, const void* v,
                            const float* log_alpha, const float* eta, float eps,
                            float* S, void* o, int N, int H, int dk, int dv,
                            kla_dtype dtype, kla_stream_t stream);
+
+/* kla_decode_step_ex -- kla_decode_step with an explicit step rule. */
+KLA_API kla_status kla_decode_step_ex(const void* q, const void* k,
+                              const void* v, const float* log_alpha,
+                              const float* eta, float eps, float* S, void* o,
+                              int N, int H, int dk, int dv, kla_dtype dtype,
+                              kla_step_rule rule, kla_stream_t stream);
 
 /*
  * kla_device_status -- synchronises `stream`, then reads and clears the

@@ -27,11 +27,14 @@ extern "C" kla_status kla_chunk_fwd_ex(const void* q, const void* k,
                                        const float* h0, void* o, float* hT,
                                        int B, int T, int H, int dk, int dv,
                                        int C, kla_dtype dtype, kla_algo algo,
+                                       kla_step_rule rule,
                                        kla_stream_t stream) {
     if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || C <= 0)
         return KLA_ERR_INVALID_ARG;
     if (dtype != KLA_F32 && dtype != KLA_BF16) return KLA_ERR_INVALID_ARG;
     if (algo != KLA_ALGO_AUTO && algo != KLA_ALGO_SIMT && algo != KLA_ALGO_TC)
+        return KLA_ERR_INVALID_ARG;
+    if (rule != KLA_STEP_KACZMARZ && rule != KLA_STEP_GIVEN)
         return KLA_ERR_INVALID_ARG;
     if (!(eps >= 0.f) || !std::isfinite(eps)) return KLA_ERR_INVALID_ARG;
     if (!supported_dim(dk) || !supported_dim(dv) || !supported_chunk(C))
@@ -65,7 +68,8 @@ extern "C" kla_status kla_chunk_fwd_ex(const void* q, const void* k,
         return from_cuda(cudaMemsetAsync(hT, 0, bytes, s));
     }
 
-    kla::FwdArgs a{q, k, v, log_alpha, eta, eps, h0, o, hT,
+    kla::FwdArgs a{q, k, v, log_alpha, eta, eps,
+                   rule == KLA_STEP_GIVEN ? 1 : 0, h0, o, hT,
                    B, T, H, dk, dv, C, dtype};
     const bool tc_ok = kla::chunk_tc_eligible(a);
     if (algo == KLA_ALGO_TC) {
@@ -85,15 +89,19 @@ extern "C" kla_status kla_chunk_fwd(const void* q, const void* k,
                                     int C, kla_dtype dtype,
                                     kla_stream_t stream) {
     return kla_chunk_fwd_ex(q, k, v, log_alpha, eta, eps, h0, o, hT, B, T, H,
-                            dk, dv, C, dtype, KLA_ALGO_AUTO, stream);
+                            dk, dv, C, dtype, KLA_ALGO_AUTO, KLA_STEP_KACZMARZ,
+                            stream);
 }
 
-extern "C" kla_status kla_decode_step(const void* q, const void* k,
-                                      const void* v, const float* log_alpha,
-                                      const float* eta, float eps, float* S,
-                                      void* o, int N, int H, int dk, int dv,
-                                      kla_dtype dtype, kla_stream_t stream) {
+extern "C" kla_status kla_decode_step_ex(const void* q, const void* k,
+                                         const void* v, const float* log_alpha,
+                                         const float* eta, float eps, float* S,
+                                         void* o, int N, int H, int dk, int dv,
+                                         kla_dtype dtype, kla_step_rule rule,
+                                         kla_stream_t stream) {
     if (N < 0 || H < 0 || dk <= 0 || dv <= 0) return KLA_ERR_INVALID_ARG;
+    if (rule != KLA_STEP_KACZMARZ && rule != KLA_STEP_GIVEN)
+        return KLA_ERR_INVALID_ARG;
     if (dtype != KLA_F32 && dtype != KLA_BF16) return KLA_ERR_INVALID_ARG;
     if (!(eps >= 0.f) || !std::isfinite(eps)) return KLA_ERR_INVALID_ARG;
     if (!supported_dim(dk) || !supported_dim(dv))
@@ -108,9 +116,20 @@ extern "C" kla_status kla_decode_step(const void* q, const void* k,
         !aligned(S, 16))
         return KLA_ERR_INVALID_ARG;
     if (o == (void*)S || o == q || o == k || o == v) return KLA_ERR_INVALID_ARG;
-    kla::DecodeArgs a{q, k, v, log_alpha, eta, eps, S, o, N, H, dk, dv, dtype};
+    kla::DecodeArgs a{q, k, v, log_alpha, eta, eps,
+                      rule == KLA_STEP_GIVEN ? 1 : 0, S, o, N, H, dk, dv,
+                      dtype};
     return from_cuda(
         kla::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" kla_status kla_decode_step(const void* q, const void* k,
+                                      const void* v, const float* log_alpha,
+                                      const float* eta, float eps, float* S,
+                                      void* o, int N, int H, int dk, int dv,
+                                      kla_dtype dtype, kla_stream_t stream) {
+    return kla_decode_step_ex(q, k, v, log_alpha, eta, eps, S, o, N, H, dk, dv,
+                              dtype, KLA_STEP_KACZMARZ, stream);
 }
 
 extern "C" kla_status kla_device_status(kla_stream_t stream) {

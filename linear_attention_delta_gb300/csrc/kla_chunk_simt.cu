@@ -119,7 +119,7 @@ kla_chunk_simt_kernel(FwdArgs a) {
                 n = fmaf(x, x, n);
             }
             const float denom = n + a.eps;
-            bs[tid] = denom == 0.f ? 0.f : bs[tid] / denom;
+            if (!a.gdn) bs[tid] = denom == 0.f ? 0.f : bs[tid] / denom;
         }
         if (tid == 32) {
             float acc = 0.f;

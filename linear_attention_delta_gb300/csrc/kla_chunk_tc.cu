@@ -126,6 +126,7 @@ struct TcParams {
     __nv_bfloat16* o;
     float* hT;
     float eps;
+    int gdn;
     int T, H;
 };
 
@@ -517,7 +518,8 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int j = 0; j < kC; ++j) diag = (j == tid) ? x[j] : diag;
                 const float denom = diag + p.eps;
-                const float beta = denom == 0.f ? 0.f : eta_cur / denom;
+                const float beta =
+                    p.gdn ? eta_cur : (denom == 0.f ? 0.f : eta_cur / denom);
                 gb[tid] = g2;
                 gb[kC + tid] = beta;
                 gb[2 * kC + tid] = beta * tc::ex2(g2);
@@ -856,7 +858,7 @@ cudaError_t launch_chunk_tc(const FwdArgs& a, cudaStream_t stream) {
         attr_set = true;
     }
     TcParams p{a.log_alpha, a.eta, a.h0,
-               static_cast<__nv_bfloat16*>(a.o), a.hT, a.eps, a.T, a.H};
+               static_cast<__nv_bfloat16*>(a.o), a.hT, a.eps, a.gdn, a.T, a.H};
     dim3 grid((unsigned)((long)a.B * a.H), kD / kNV);
     kla_chunk_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
     return cudaGetLastError();

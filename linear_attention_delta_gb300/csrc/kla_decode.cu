@@ -112,7 +112,8 @@ kla_decode_kernel(DecodeArgs a) {
 
     const float alpha = expf(a.log_alpha[head]);
     const float denom = nk_s + a.eps;
-    const float beta = denom == 0.f ? 0.f : a.eta[head] / denom;
+    const float beta =
+        a.gdn ? a.eta[head] : (denom == 0.f ? 0.f : a.eta[head] / denom);
     const float bqk = beta * qk_s;
 
     const T* vp = static_cast<const T*>(a.v) + (size_t)head * dv + j0 + 4 * cg;

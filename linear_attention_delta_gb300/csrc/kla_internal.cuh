@@ -30,6 +30,7 @@ struct FwdArgs {
     const float* log_alpha;
     const float* eta;
     float eps;
+    int gdn;           // 1: beta = eta (learned step), 0: Kaczmarz step
     const float* h0;   // may be null
     void* o;
     float* hT;         // may be null
@@ -44,6 +45,7 @@ struct DecodeArgs {
     const float* log_alpha;
     const float* eta;
     float eps;
+    int gdn;
     float* S;
     void* o;
     int N, H, dk, dv;

@@ -21,6 +21,7 @@ STATUS_NAMES = {0: "KLA_OK", -1: "KLA_ERR_INVALID_ARG",
                 -4: "KLA_ERR_TIMEOUT", -5: "KLA_ERR_NOT_IMPLEMENTED"}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 ALGOS = {"auto": 0, "simt": 1, "tc": 2}
+RULES = {"kaczmarz": 0, "given": 1}
 
 # name -> (restype, argtypes) of every symbol include/kla.h declares
 _VP, _FP, _F, _I = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, \
@@ -29,9 +30,11 @@ SIGNATURES = {
     "kla_chunk_fwd": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP, _FP,
                            _I, _I, _I, _I, _I, _I, _I, _VP]),
     "kla_chunk_fwd_ex": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP, _FP,
-                              _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
+                              _I, _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
     "kla_decode_step": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
                              _I, _I, _I, _I, _I, _VP]),
+    "kla_decode_step_ex": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
+                                _I, _I, _I, _I, _I, _I, _VP]),
     "kla_device_status": (_I, [_VP]),
     "kla_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -93,12 +96,13 @@ def _check_cuda(name, t, dtype=None):
 
 def chunk_fwd(q, k, v, log_alpha, eta, eps: float = 1e-6, h0=None,
               C: int = 64, algo: str = "auto", o=None, hT=None,
-              want_state: bool = True, stream=None):
+              want_state: bool = True, stream=None, rule: str = "kaczmarz"):
     """KLA forward pass (``kla_chunk_fwd_ex``).
 
     q, k [B,T,H,dk]; v [B,T,H,dv] (fp32 or bf16, same dtype); log_alpha, eta
     [B,T,H] fp32; h0 [B,H,dk,dv] fp32 or None.  Returns (o, hT); hT is None
     when ``want_state`` is False.  ``o``/``hT`` may be passed preallocated.
+    ``rule="given"`` uses eta as the step directly (gated DeltaNet).
     """
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_cuda(n, t, q.dtype)
@@ -117,14 +121,14 @@ def chunk_fwd(q, k, v, log_alpha, eta, eps: float = 1e-6, h0=None,
     st = load_library().kla_chunk_fwd_ex(
         _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(eta), float(eps),
         _ptr(h0), _ptr(o), _ptr(hT), B, T, H, dk, dv, int(C),
-        DTYPES[q.dtype], ALGOS[algo], _stream(stream))
+        DTYPES[q.dtype], ALGOS[algo], RULES[rule], _stream(stream))
     if st != KLA_OK:
         raise KlaError("kla_chunk_fwd_ex", st)
     return o, hT
 
 
 def decode_step(q, k, v, log_alpha, eta, S, eps: float = 1e-6, o=None,
-                stream=None):
+                stream=None, rule: str = "kaczmarz"):
     """One KLA decode token (``kla_decode_step``); S [N,H,dk,dv] fp32 is
     updated in place.  Returns o [N,H,dv]."""
     for n, t in (("q", q), ("k", k), ("v", v)):
@@ -136,11 +140,12 @@ def decode_step(q, k, v, log_alpha, eta, S, eps: float = 1e-6, o=None,
     dv = v.shape[-1]
     if o is None:
         o = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
-    st = load_library().kla_decode_step(
+    st = load_library().kla_decode_step_ex(
         _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(eta), float(eps),
-        _ptr(S), _ptr(o), N, H, dk, dv, DTYPES[q.dtype], _stream(stream))
+        _ptr(S), _ptr(o), N, H, dk, dv, DTYPES[q.dtype], RULES[rule],
+        _stream(stream))
     if st != KLA_OK:
-        raise KlaError("kla_decode_step", st)
+        raise KlaError("kla_decode_step_ex", st)
     return o
 
 

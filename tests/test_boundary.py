@@ -30,7 +30,8 @@ def lib():
 def test_header_declares_expected_entry_points():
     syms = declared_symbols()
     for name in ("kla_chunk_fwd", "kla_chunk_fwd_ex", "kla_decode_step",
-                 "kla_device_status", "kla_status_string"):
+                 "kla_decode_step_ex", "kla_device_status",
+                 "kla_status_string"):
         assert name in syms
 
 
@@ -56,9 +57,9 @@ P = ctypes.c_void_p(0x1000)      # never dereferenced: calls fail validation
 
 
 def fwd(lib, *, q=P, k=P, v=P, la=P, eta=P, eps=1e-6, h0=None, o=P, hT=None,
-        B=1, T=8, H=1, dk=16, dv=16, C=16, dtype=1, algo=0):
+        B=1, T=8, H=1, dk=16, dv=16, C=16, dtype=1, algo=0, rule=0):
     return lib.kla_chunk_fwd_ex(q, k, v, la, eta, eps, h0, o, hT, B, T, H, dk,
-                                dv, C, dtype, algo, None)
+                                dv, C, dtype, algo, rule, None)
 
 
 def dec(lib, *, q=P, k=P, v=P, la=P, eta=P, eps=1e-6, S=P, o=P, N=1, H=1,
@@ -76,6 +77,7 @@ def test_fwd_rejects_bad_arguments_on_host(lib):
     assert fwd(lib, C=0) == INVALID
     assert fwd(lib, dtype=7) == INVALID
     assert fwd(lib, algo=9) == INVALID
+    assert fwd(lib, rule=2) == INVALID
     assert fwd(lib, eps=-1.0) == INVALID
     assert fwd(lib, eps=float("nan")) == INVALID
     assert fwd(lib, eps=float("inf")) == INVALID

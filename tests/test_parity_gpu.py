@@ -243,3 +243,55 @@ def test_tensor_core_zero_initial_state_and_no_hT():
     assert hT is None
     o_ref, _ = oracle_fwd(inp)
     assert rel_err(o, o_ref) <= 2e-2
+
+
+# ---------------------------------------------------------------- GDN mode
+
+def _gdn_as_kla_eta(inp, b):
+    """The learned-step recurrence with step b equals KLA with
+    eta = b (||k||^2 + eps) (pinned on the CPU by test_gdn_reduction)."""
+    k = inp["k"].double().numpy()
+    return b * (np.sum(k * k, -1) + inp["eps"])
+
+
+@pytest.mark.parametrize("algo,w,sizes", [
+    ("tc", gen.LAYER_1B, dict(B=1, T=200, H=2)),
+    ("simt", gen.LAYER_1B, dict(B=1, T=200, H=2)),
+    ("simt", gen.TINY, dict(B=2, T=50, H=2)),
+])
+def test_given_step_mode_against_oracle(algo, w, sizes):
+    inp = gen.prefill_inputs(w, **sizes)
+    rng = np.random.default_rng(5)
+    b = rng.uniform(0.0, 0.5, inp["eta"].shape).astype(np.float32)
+    d = to_dev(inp)
+    o, hT = kla.chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"],
+                          torch.from_numpy(b).cuda(), d["eps"], d["h0"],
+                          C=inp["C"], algo=algo, rule="given")
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle.kla_fwd(inp["q"], inp["k"], inp["v"],
+                                  inp["log_alpha"],
+                                  _gdn_as_kla_eta(inp, b.astype(np.float64)),
+                                  inp["eps"], inp["h0"])
+    tol = TOL[inp["q"].dtype]
+    assert rel_err(o, o_ref) <= tol and rel_err(hT, h_ref) <= tol
+
+
+def test_given_step_decode():
+    from dataclasses import replace
+    w = replace(gen.DECODE, B=4, H=2)
+    d = gen.decode_inputs(w, steps=3)
+    S = d["S0"].cuda()
+    S_ref = d["S0"].double().numpy()
+    rng = np.random.default_rng(6)
+    for t in range(3):
+        b = rng.uniform(0.0, 0.5, (4, 2)).astype(np.float32)
+        args = [d[n][t] for n in ("q", "k", "v", "log_alpha")]
+        o = kla.decode_step(*[a.cuda() for a in args],
+                            torch.from_numpy(b).cuda(), S, eps=d["eps"],
+                            rule="given")
+        k = d["k"][t].double().numpy()
+        eta_kla = b * (np.sum(k * k, -1) + d["eps"])
+        o_ref, S_ref = oracle.kla_decode_step(*args, eta_kla, d["eps"], S_ref)
+        assert rel_err(o, o_ref) <= 2e-2
+    torch.cuda.synchronize()
+    assert rel_err(S, S_ref) <= 1e-4

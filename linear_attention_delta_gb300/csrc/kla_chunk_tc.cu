@@ -91,9 +91,7 @@ constexpr int kBarG = 3;       // G MMA done
 constexpr int kBarWU = 4;      // W, U MMAs done
 constexpr int kBarX = 5;       // U~ = U - W S formed in TMEM
 constexpr int kBarDS = 6;      // Q S, dS, P U~ done
-constexpr int kBarWReady = 7;  // intra -> state: gates, W/U issued, G done
-constexpr int kBarWUAck = 8;   // state -> intra: passed its W/U wait (keeps
-                               //   the W/U barrier from running a phase ahead)
+constexpr int kBarWReady = 7;  // intra -> state: gates and TW | TU written
 constexpr int kBarSDone = 9;   // state -> intra: chunk finished
 
 // ---- TMEM columns (two buffers, by chunk parity b) -------------------------
@@ -456,7 +454,7 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (tid < 128) {
         // ==================================================== intra warpgroup
         const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
-        bool failed = false, g_pending = false, wu_pending = false;
+        bool failed = false, g_pending = false;
         auto load_gates = [&](int c, float& la, float& et) {
             const int t = c * kC + tid;
             la = 0.f;
@@ -528,7 +526,6 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (c >= 1) {
                 if (!wg_wait(&bars[kBarWU], (c - 1) & 1, abort_flag,
                              kBarIntra)) { failed = true; break; }
-                wu_pending = false;
             } else {
                 tc::named_bar_sync(kBarIntra, 128);
             }
@@ -566,20 +563,62 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
                 __syncwarp();
                 invert_diag_tiles(Ad, Tt, sm + kTWU, gb, tid);
+                tc::fence_proxy_async_smem();
             }
             tc::named_bar_sync(kBarIntra, 128);
 
-            // ---- off-diagonal tiles of T = A^{-1}, written as TW | TU ----
-            invert_offdiag_tiles(Ao, Tt, sm + kTWU, gb, tid);
-            tc::fence_proxy_async_smem();
-            tc::named_bar_sync(kBarIntra, 128);
-            // the state side must have passed its wait on the W/U(c-1)
-            // phase before W/U(c) can complete
-            if (c >= 1 && !wg_wait(&bars[kBarWUAck], (c - 1) & 1, abort_flag,
-                                   kBarIntra)) { failed = true; break; }
+            if (warp == 0) {
+                // Warp 0 has no off-diagonal tile: it issues the next chunk's
+                // G once its tiles have landed and chunk c-1 (last user of
+                // that G buffer and of the gate buffer) is done.
+                if (c + 1 < nchunks) {
+                    const int s1 = (c + 1) % kNS;
+                    bool ok = tc::mbar_wait_or_abort(&bars[kBarTma + s1],
+                                                     ((c + 1) / kNS) & 1,
+                                                     abort_flag);
+                    if (ok && c >= 1)
+                        ok = tc::mbar_wait_or_abort(&bars[kBarSDone],
+                                                    (c - 1) & 1, abort_flag);
+                    if (__all_sync(0xffffffffu, ok)) {
+                        tc::tc_fence_after();
+                        if (tid == 0) issue_g(c + 1);
+                        g_pending = true;
+                    } else {
+                        *reinterpret_cast<volatile int*>(abort_flag) = 1;
+                    }
+                }
+            } else {
+                // ---- off-diagonal tiles of T = A^{-1}, as TW | TU ----
+                invert_offdiag_tiles(Ao, Tt, sm + kTWU, gb, tid);
+                tc::fence_proxy_async_smem();
+                tc::named_bar_sync(kBarW13, 96);
+                // chunk handed over: the state side issues W, U itself
+                if (tid == 32) tc::mbar_arrive(&bars[kBarWReady]);
+            }
+            la_cur = la_nxt;
+            eta_cur = eta_nxt;
+        }
+        if (failed && tid == 0) {   // let issued MMAs finish (bounded)
+            if (g_pending) tc::mbar_wait(&bars[kBarG], 0, 100000000ull);
+        }
+    } else {
+        // ==================================================== state warpgroup
+        const int sw = warp - 4;                 // TMEM lane quarter
+        const uint32_t tlane = tmem + ((uint32_t)(sw * 32) << 16);
+        const int row = tid - 128;               // TMEM lane = key row
+        bool failed = false, x_pending = false, ds_pending = false;
+        bool wu_pending = false;
+        for (int c = 0; c < nchunks && !failed; ++c) {
+            const int s = c % kNS;
+            const uint32_t sst = sbase + s * kStage;
+            const float* gb = gbuf + (c & 1) * kGBufStride;
+            if (!wg_wait(&bars[kBarWReady], c & 1, abort_flag, kBarState)) {
+                failed = true; break;
+            }
             tc::tc_fence_after();
-            if (tid == 0) {
-                const uint32_t sst = sbase + (c % kNS) * kStage;
+            if (tid == 224) {
+                // W = [TW; -] K (B: K, MN-major, key halves kHalf apart) and
+                // U = [TU; -] V
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     tc::mma_bf16(tmem + col_w(c), desc_k(sbase + kTWU + ks * 32),
@@ -591,47 +630,17 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                  desc_mn(sst + kOffV + ks * 2048, 0), kIdN64,
                                  ks > 0);
                 tc::mma_commit(&bars[kBarWU]);
-                tc::mbar_arrive(&bars[kBarWReady]);
             }
             wu_pending = true;
-            // the next chunk's G, once its tiles have landed and chunk c-1
-            // (last user of that G buffer and of the gate buffer) is done
-            if (c + 1 < nchunks) {
-                const int s1 = (c + 1) % kNS;
-                if (!wg_wait(&bars[kBarTma + s1], ((c + 1) / kNS) & 1,
-                             abort_flag, kBarIntra)) { failed = true; break; }
-                if (c >= 1 && !wg_wait(&bars[kBarSDone], (c - 1) & 1,
-                                       abort_flag, kBarIntra)) {
-                    failed = true; break;
-                }
+            bool wu_ok = true;
+            if (sw < 2) {   // warps 4, 5 agree before their pair barrier
+                const bool ok =
+                    tc::mbar_wait_or_abort(&bars[kBarWU], c & 1, abort_flag);
+                wu_ok = !tc::named_bar_or(kBarState01, 64, !ok);
+                if (!wu_ok) *reinterpret_cast<volatile int*>(abort_flag) = 1;
                 tc::tc_fence_after();
-                if (tid == 0) issue_g(c + 1);
-                g_pending = true;
             }
-            la_cur = la_nxt;
-            eta_cur = eta_nxt;
-        }
-        if (failed && tid == 0) {   // let issued MMAs finish (bounded)
-            if (g_pending) tc::mbar_wait(&bars[kBarG], 0, 100000000ull);
-            if (wu_pending) tc::mbar_wait(&bars[kBarWU], 0, 100000000ull);
-        }
-    } else {
-        // ==================================================== state warpgroup
-        const int sw = warp - 4;                 // TMEM lane quarter
-        const uint32_t tlane = tmem + ((uint32_t)(sw * 32) << 16);
-        const int row = tid - 128;               // TMEM lane = key row
-        bool failed = false, x_pending = false, ds_pending = false;
-        for (int c = 0; c < nchunks && !failed; ++c) {
-            const int s = c % kNS;
-            const uint32_t sst = sbase + s * kStage;
-            const float* gb = gbuf + (c & 1) * kGBufStride;
-            if (!wg_wait(&bars[kBarWReady], c & 1, abort_flag, kBarState) ||
-                !wg_wait(&bars[kBarWU], c & 1, abort_flag, kBarState)) {
-                failed = true; break;
-            }
-            if (tid == 128) tc::mbar_arrive(&bars[kBarWUAck]);
-            tc::tc_fence_after();
-            if (sw < 2) {   // W row -> bf16 K-major operand (two halves)
+            if (sw < 2 && wu_ok) {   // W row -> bf16 K-major operand
                 float x[kNV];
                 tmem_ld64(tlane + col_w(c), x);
                 st_row_sw128(sm + kWBuf, row, x);
@@ -768,6 +777,8 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 if (c + kNS < nchunks) issue_tma(c + kNS);
             }
         }
+        if (failed && tid == 224 && wu_pending)
+            tc::mbar_wait(&bars[kBarWU], 0, 100000000ull);
         if (failed && tid == 128) {   // let issued MMAs finish (bounded)
             if (x_pending) tc::mbar_wait(&bars[kBarX], 0, 100000000ull);
             if (ds_pending) tc::mbar_wait(&bars[kBarDS], 0, 100000000ull);

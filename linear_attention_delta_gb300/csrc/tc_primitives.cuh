@@ -69,6 +69,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Slow path of the waits below, kept out of line so that the many wait sites
+// of a kernel share one copy of the spin loop: polls until the phase with
+// the given parity completes (true), `limit_ns` nanoseconds pass or *abort
+// (when given) becomes non-zero (false).
+__device__ __noinline__ bool mbar_spin(uint32_t bar, uint32_t parity,
+                                       const volatile int* abort,
+                                       uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (abort && *abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // Wait for the phase with the given parity to complete, giving up after
 // `limit_ns` nanoseconds.  Returns false on time-out (the caller records the
 // fault and stops issuing work).
@@ -76,13 +93,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           uint64_t limit_ns = 2000000000ull) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(a, parity)) return true;
-        if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
+    return mbar_spin(a, parity, nullptr, limit_ns);
 }
 
 // As mbar_wait, but also gives up as soon as *abort becomes non-zero (another
@@ -92,14 +103,7 @@ __device__ __forceinline__ bool mbar_wait_or_abort(
     uint64_t limit_ns = 2000000000ull) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(a, parity)) return true;
-        if (*abort) return false;
-        if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
+    return mbar_spin(a, parity, abort, limit_ns);
 }
 
 // ------------------------------------------------------------ named barriers
@@ -173,6 +177,17 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap,
             smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0),
         "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// Prefetch the tile at the given coordinates into L2 (no shared memory, no
+// completion); out-of-range parts of the box are skipped by the hardware.
+__device__ __forceinline__ void tma_prefetch_4d(const void* tmap, int c0,
+                                                int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, "
+        "%4}];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
 

@@ -363,6 +363,68 @@ def bench_decode(w, steps, warmup, distinct=50):
     return ms / steps
 
 
+def bench_long_context(world, gpu_index, hbm):
+    """The pages' own efficiency points at layer scale: the 131072-token
+    prefill (KLA and the learned-step rule on the same kernels), and decode
+    steps from the state of a 32768-token prefill."""
+    w = gen.LONG_131K
+    inp = gen.prefill_inputs(w)
+    pf = bench_prefill(w, 3, 3, world, gpu_index, inp=inp)
+    gd = bench_prefill(w, 3, 3, world, gpu_index, rule="given", inp=inp)
+    del inp
+    gbs = prefill_bytes(w) / (pf["ms"] * 1e-3) / 1e9
+    prefill = {"workload": w.name, "ms": round(pf["ms"], 4),
+               "tokens_per_s": round(world * w.B * w.T / (pf["ms"] * 1e-3), 1),
+               "hbm_gbs": round(gbs, 1), "roofline_frac": round(gbs / hbm, 4),
+               "gdn_ms": round(gd["ms"], 4),
+               "kla_over_gdn_time": round(pf["ms"] / gd["ms"], 4),
+               "timed_steps": 3}
+
+    hw = gen.HANDOFF_32K
+    hin = gen.prefill_inputs(hw)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
+           for k, v in hin.items()}
+    del hin
+    S = torch.empty((hw.B, hw.H, hw.dk, hw.dv), dtype=torch.float32,
+                    device="cuda")
+    o = torch.empty_like(dev["v"])
+    e0, e1 = (torch.cuda.Event(enable_timing=True),
+              torch.cuda.Event(enable_timing=True))
+    kla.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["eta"],
+                  dev["eps"], None, C=hw.C, o=o, hT=S)   # warm-up
+    e0.record()
+    kla.chunk_fwd(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["eta"],
+                  dev["eps"], None, C=hw.C, o=o, hT=S)
+    e1.record()
+    torch.cuda.synchronize()
+    prefill_ms = e0.elapsed_time(e1)
+    del dev, o
+    steps, distinct = 200, 20
+    d = gen.decode_inputs(hw, steps=distinct, seed=gen.SEEDS[hw.name] + 100)
+    toks = [[d[n][i].cuda() for n in ("q", "k", "v", "log_alpha", "eta")]
+            for i in range(distinct)]
+    od = torch.empty((hw.B, hw.H, hw.dv), dtype=toks[0][0].dtype,
+                     device="cuda")
+    for i in range(10):                       # warm-up on a copy
+        kla.decode_step(*toks[i % distinct], S.clone(), eps=d["eps"], o=od)
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(steps):
+        kla.decode_step(*toks[i % distinct], S, eps=d["eps"], o=od)
+    e1.record()
+    torch.cuda.synchronize()
+    dms = e0.elapsed_time(e1) / steps
+    if kla.device_status() != 0:
+        raise RuntimeError("device-side timeout in the long-context points")
+    handoff = {"workload": hw.name, "prefill_ms": round(prefill_ms, 4),
+               "decode_sequences": hw.B, "decode_steps": steps,
+               "decode_steps_per_s": round(1e3 / dms, 1),
+               "decode_ms_per_step": round(dms, 5),
+               "note": "state carried from the 32768-token prefill; "
+                       "4 MiB of state (L2-resident), so launch-bound"}
+    return {"prefill_131k": prefill, "decode_after_32k": handoff}
+
+
 def cpu_baseline_prefill(inp, budget_s=30.0):
     """The fp64 oracle, as it stands, on the host cores: the whole workload,
     repeated until ~10 s have passed (never past the budget)."""
@@ -459,6 +521,10 @@ def run_ours(args):
                 "tokens_per_s": round(world * tokens / (gdn["ms"] * 1e-3), 1),
                 "kla_over_gdn_time": round(ms / gdn["ms"], 4)}
 
+    longctx = None
+    if not args.no_long:
+        longctx = bench_long_context(world, local, hbm)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_prefill(pf["inputs"])
@@ -475,6 +541,7 @@ def run_ours(args):
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": pf["launches"], "clocks": pf["clocks"],
             "decode": decode, "gdn_mode": gdn_line,
+            "long_context": longctx,
             "per_step_ms": [round(x, 5) for x in pf["per_step_ms"]]}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -534,6 +601,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-long", action="store_true",
+                    help="skip the 131K-prefill / 32K-decode points")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="run one kernel alone (profiler captures)")
     args = ap.parse_args()

@@ -67,8 +67,16 @@ DECODE = Workload("decode-bf16-N256-H16-d128-steps1000", B=256, T=1000, H=16,
                   k_norm=(0.5, 2.0), alpha_shift=2.0, h0_std=0.02,
                   decode=True)
 
+# The pages' own efficiency points: a 131K-token prefill, and decode at a
+# 32K-token context (state carried from the prefill into the decode steps).
+LONG_131K = replace(LONG_CTX, name="longctx-bf16-B1-T131072-H16-d128-C64",
+                    T=131072)
+HANDOFF_32K = replace(LAYER_1B, name="handoff-bf16-B4-T32768-H16-d128-C64",
+                      T=32768, h0_std=0.0)
+
 # Seeds: 1000 + position in this list.
-WORKLOADS = [TINY, LAYER_340M, LAYER_1B, LONG_CTX, DECODE]
+WORKLOADS = [TINY, LAYER_340M, LAYER_1B, LONG_CTX, DECODE, LONG_131K,
+             HANDOFF_32K]
 SEEDS = {w.name: 1000 + i for i, w in enumerate(WORKLOADS)}
 SEEDS[TINY_UNRELAXED.name] = SEEDS[TINY.name]
 

@@ -216,6 +216,51 @@ def test_prefill_then_decode_handoff():
     assert rel_err(S, h_ref) <= 2e-2
 
 
+# ---------------------------------------------------------------- the pages' points
+
+def test_long_prefill_131k_sampled_heads():
+    """The 131072-token prefill (one sequence, 16 heads) on the GPU; four
+    heads are followed by the oracle over every token (o and the final state
+    of those heads compared element by element)."""
+    inp = gen.prefill_inputs(gen.LONG_131K)
+    o, hT = run_fwd(inp)
+    hs = slice(5, 9)
+    sub = {k: (v[:, :, hs].contiguous()
+               if k in ("q", "k", "v", "log_alpha", "eta") else v)
+           for k, v in inp.items()}
+    assert sub["h0"] is None
+    o_ref, h_ref = oracle_fwd(sub)
+    assert rel_err(o[:, :, hs], o_ref) <= 2e-2
+    assert rel_err(hT[:, hs], h_ref) <= 2e-2
+
+
+def test_decode_after_32k_prefill():
+    """Four sequences prefilled over 32768 tokens, then 40 decode steps from
+    the prefill's final state; sequence 0 (all 16 heads) is followed by the
+    oracle through the prefill and every decode step."""
+    w = gen.HANDOFF_32K
+    inp = gen.prefill_inputs(w)
+    _, S = run_fwd(inp)
+    sub = {k: (v[:1].contiguous() if isinstance(v, torch.Tensor) else v)
+           for k, v in inp.items()}
+    _, S_ref = oracle_fwd(sub)
+    steps = 40
+    d = gen.decode_inputs(w, steps=steps, seed=gen.SEEDS[w.name] + 100)
+    dd = to_dev(d)
+    worst = 0.0
+    for t in range(steps):
+        o = kla.decode_step(dd["q"][t], dd["k"][t], dd["v"][t],
+                            dd["log_alpha"][t], dd["eta"][t], S,
+                            eps=d["eps"])
+        o_ref, S_ref = oracle.kla_decode_step(
+            d["q"][t, :1], d["k"][t, :1], d["v"][t, :1],
+            d["log_alpha"][t, :1], d["eta"][t, :1], d["eps"], S_ref)
+        worst = max(worst, rel_err(o[:1], o_ref))
+    torch.cuda.synchronize()
+    assert worst <= 2e-2
+    assert rel_err(S[:1], S_ref) <= 2e-2
+
+
 # ---------------------------------------------------------------- kernel paths
 
 @pytest.mark.parametrize("T", [64, 65, 128, 200, 1000])

@@ -8,7 +8,8 @@ Two independent implementations of the same definition are provided, both in
 fp64:
 
 * ``kla_fwd`` / ``kla_decode_step`` -- the C recurrence in ``kla_oracle.c``
-  (OpenMP over (batch, head)), used at every size;
+  (OpenMP over (batch, head)), used at every size; ``kla_bwd`` -- its
+  reverse mode (gradients of every input), derived token by token;
 * ``kla_fwd_np`` / ``kla_decode_step_np`` -- a NumPy loop over tokens,
   vectorised over (batch, head), for small cases.
 
@@ -60,6 +61,13 @@ def _load():
                                                ctypes.c_long, ctypes.c_long,
                                                ctypes.c_int]
         lib.oracle_kla_decode_step.restype = ctypes.c_int
+        lib.oracle_kla_bwd.argtypes = [dp, dp, dp, dp, dp, ctypes.c_double,
+                                       ctypes.c_int, dp, dp, dp,
+                                       dp, dp, dp, dp, dp, dp,
+                                       ctypes.c_long, ctypes.c_long,
+                                       ctypes.c_long, ctypes.c_long,
+                                       ctypes.c_long, ctypes.c_int]
+        lib.oracle_kla_bwd.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -129,6 +137,38 @@ def kla_decode_step(q, k, v, log_alpha, eta, eps, S, n_threads: int = 0):
     if rc != 0:
         raise RuntimeError(f"oracle_kla_decode_step failed with {rc}")
     return o, S
+
+
+def kla_bwd(q, k, v, log_alpha, eta, eps, h0, dout, dhT=None,
+            given: bool = False, n_threads: int = 0) -> dict:
+    """Reverse mode of the forward pass in fp64 (C): the gradients of
+    L = sum(dout * o) + sum(dhT * hT) with respect to every input.
+
+    ``given=True`` differentiates the learned-step rule beta_t = eta_t
+    instead of the Kaczmarz step.  Shapes as in ``kla_fwd``; dout like o,
+    dhT like hT (None: zero).  Returns a dict with dq, dk, dv, dlog_alpha,
+    deta and dh0 (fp64 NumPy arrays).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    la, et, do = _f64(log_alpha), _f64(eta), _f64(dout)
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    assert q.shape == k.shape and v.shape[:3] == (B, T, H)
+    assert la.shape == (B, T, H) and et.shape == (B, T, H)
+    assert do.shape == v.shape
+    h0a = None if h0 is None else _f64(h0)
+    dhTa = None if dhT is None else _f64(dhT)
+    out = dict(dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v),
+               dlog_alpha=np.zeros_like(la), deta=np.zeros_like(et),
+               dh0=np.zeros((B, H, dk, dv)))
+    rc = _load().oracle_kla_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(et), float(eps),
+        int(bool(given)), _ptr(h0a), _ptr(do), _ptr(dhTa), _ptr(out["dq"]),
+        _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dlog_alpha"]),
+        _ptr(out["deta"]), _ptr(out["dh0"]), B, T, H, dk, dv, int(n_threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_kla_bwd failed ({rc})")
+    return out
 
 
 def kla_fwd_np(q, k, v, log_alpha, eta, eps, h0=None):

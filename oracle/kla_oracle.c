@@ -150,6 +150,204 @@ int oracle_kla_decode_step(const double* q, const double* k, const double* v,
     return failed ? -2 : 0;
 }
 
+/* ------------------------------------------------------------ backward
+ *
+ * Reverse mode of the recurrence above: given dL/do_t for every token and
+ * dL/dS_T (dhT, may be NULL), the gradients with respect to q, k, v,
+ * log_alpha, eta and h0.  `given` selects the step rule: 0 = Kaczmarz
+ * (beta_t = eta_t/(||k_t||^2+eps), so k_t also receives the gradient that
+ * flows through its norm), 1 = the learned step of gated DeltaNet
+ * (beta_t = eta_t).  Each token is differentiated by hand, in the order of
+ * its forward formulas, from the state before it (S_{t-1}) and after it
+ * (S_t):
+ *
+ *   o   = S_t^T q                    dS_t += q do^T,      dq = S_t do
+ *   S_t = S~ + beta k e^T            dbeta = k^T dS_t e,  dk = beta dS_t e,
+ *                                    de = beta dS_t^T k,  dS~ = dS_t
+ *   e   = v - S~^T k                 dv = de,  dS~ -= k de^T,  dk -= S~ de
+ *   beta = eta/(n+eps), n = ||k||^2  deta = dbeta/(n+eps),
+ *                                    dk += 2 k (-dbeta beta/(n+eps))
+ *   S~  = alpha S_{t-1}              dalpha = <dS~, S_{t-1}>,
+ *                                    dlog_alpha = alpha dalpha,
+ *                                    dS_{t-1} = alpha dS~
+ *
+ * (beta := 0 when n + eps == 0: then deta and the norm term are 0.)  The
+ * states are recomputed forward from checkpoints kept every 64 tokens.
+ */
+
+/* Forward step on S in place (either rule), without the read-out. */
+static void kla_token_rule(double* S, const double* k, const double* v,
+                           double log_alpha, double eta, double eps,
+                           int given, long dk, long dv, double* e)
+{
+    const double alpha = exp(log_alpha);
+    double nrm = 0.0;
+    for (long i = 0; i < dk; ++i) nrm += k[i] * k[i];
+    const double denom = nrm + eps;
+    const double beta = given ? eta : (denom == 0.0 ? 0.0 : eta / denom);
+    for (long i = 0; i < dk * dv; ++i) S[i] *= alpha;
+    for (long j = 0; j < dv; ++j) e[j] = v[j];
+    for (long i = 0; i < dk; ++i)
+        for (long j = 0; j < dv; ++j) e[j] -= S[i * dv + j] * k[i];
+    for (long i = 0; i < dk; ++i)
+        for (long j = 0; j < dv; ++j) S[i * dv + j] += beta * k[i] * e[j];
+}
+
+/* One token backward.  Sp = S_{t-1}, St = S_t; dS holds dL/dS_t on entry
+ * (including this token's later uses) and dL/dS_{t-1} on return. */
+static void kla_token_bwd(const double* Sp, const double* St,
+                          const double* q, const double* k, const double* v,
+                          double log_alpha, double eta, double eps, int given,
+                          const double* dout, double* dS, double* dq,
+                          double* dk_out, double* dv_out, double* dla,
+                          double* deta, long dk, long dv, double* e,
+                          double* de, double* tk)
+{
+    const double alpha = exp(log_alpha);
+    double nrm = 0.0;
+    for (long i = 0; i < dk; ++i) nrm += k[i] * k[i];
+    const double denom = nrm + eps;
+    const double beta = given ? eta : (denom == 0.0 ? 0.0 : eta / denom);
+
+    /* e = v - S~^T k, S~ = alpha S_{t-1} */
+    for (long j = 0; j < dv; ++j) e[j] = v[j];
+    for (long i = 0; i < dk; ++i)
+        for (long j = 0; j < dv; ++j) e[j] -= alpha * Sp[i * dv + j] * k[i];
+
+    /* read-out */
+    for (long i = 0; i < dk; ++i) {
+        double acc = 0.0;
+        for (long j = 0; j < dv; ++j) {
+            dS[i * dv + j] += q[i] * dout[j];
+            acc += St[i * dv + j] * dout[j];
+        }
+        dq[i] = acc;
+    }
+
+    /* write */
+    double dbeta = 0.0;
+    for (long i = 0; i < dk; ++i) {
+        double acc = 0.0;
+        for (long j = 0; j < dv; ++j) acc += dS[i * dv + j] * e[j];
+        tk[i] = acc;                       /* (dS_t e)_i */
+        dbeta += k[i] * acc;
+        dk_out[i] = beta * acc;
+    }
+    for (long j = 0; j < dv; ++j) {
+        double acc = 0.0;
+        for (long i = 0; i < dk; ++i) acc += dS[i * dv + j] * k[i];
+        de[j] = beta * acc;
+        dv_out[j] = de[j];
+    }
+
+    /* residual: dS~ = dS_t - k de^T, dk -= S~ de */
+    for (long i = 0; i < dk; ++i) {
+        double acc = 0.0;
+        for (long j = 0; j < dv; ++j) {
+            dS[i * dv + j] -= k[i] * de[j];
+            acc += Sp[i * dv + j] * de[j];
+        }
+        dk_out[i] -= alpha * acc;
+    }
+
+    /* step size */
+    if (given) {
+        *deta = dbeta;
+    } else if (denom != 0.0) {
+        *deta = dbeta / denom;
+        const double dn = -dbeta * beta / denom;
+        for (long i = 0; i < dk; ++i) dk_out[i] += 2.0 * dn * k[i];
+    } else {
+        *deta = 0.0;
+    }
+
+    /* decay */
+    double dalpha = 0.0;
+    for (long i = 0; i < dk * dv; ++i) dalpha += dS[i] * Sp[i];
+    *dla = dalpha * alpha;
+    for (long i = 0; i < dk * dv; ++i) dS[i] *= alpha;
+}
+
+/* Backward pass for every (b, h).  dout [B,T,H,dv]; dhT [B,H,dk,dv] or NULL;
+ * outputs dq, dk [B,T,H,dk], dv [B,T,H,dv], dla, deta [B,T,H],
+ * dh0 [B,H,dk,dv] (may be NULL).  Returns 0, -1 (bad argument) or -2 (no
+ * scratch memory). */
+int oracle_kla_bwd(const double* q, const double* k, const double* v,
+                   const double* log_alpha, const double* eta, double eps,
+                   int given, const double* h0, const double* dout,
+                   const double* dhT, double* dq, double* dk_out,
+                   double* dv_out, double* dla, double* deta, double* dh0,
+                   long B, long T, long H, long dk, long dv, int n_threads)
+{
+    if (!q || !k || !v || !log_alpha || !eta || !dout || !dq || !dk_out ||
+        !dv_out || !dla || !deta)
+        return -1;
+    if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0) return -1;
+    const long seg = 64;
+    const long nseg = (T + seg - 1) / seg;
+    const long sz = dk * dv;
+    int failed = 0;
+    const long pairs = B * H;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+#endif
+    for (long p = 0; p < pairs; ++p) {
+        const long b = p / H, h = p % H;
+        double* ck = (double*)malloc(sizeof(double) * (size_t)((nseg + 1) * sz));
+        double* sb = (double*)malloc(sizeof(double) * (size_t)((seg + 1) * sz));
+        double* dS = (double*)malloc(sizeof(double) * (size_t)sz);
+        double* e = (double*)malloc(sizeof(double) * (size_t)dv);
+        double* de = (double*)malloc(sizeof(double) * (size_t)dv);
+        double* tk = (double*)malloc(sizeof(double) * (size_t)dk);
+        if (!ck || !sb || !dS || !e || !de || !tk) {
+            free(ck); free(sb); free(dS); free(e); free(de); free(tk);
+            failed |= 1;
+            continue;
+        }
+        /* forward: checkpoints at t = 0, 64, 128, ... */
+        double* S = sb;
+        if (h0) memcpy(S, h0 + p * sz, sizeof(double) * (size_t)sz);
+        else memset(S, 0, sizeof(double) * (size_t)sz);
+        for (long t = 0; t < T; ++t) {
+            if (t % seg == 0)
+                memcpy(ck + (t / seg) * sz, S, sizeof(double) * (size_t)sz);
+            const long row = (b * T + t) * H + h;
+            kla_token_rule(S, k + row * dk, v + row * dv, log_alpha[row],
+                           eta[row], eps, given, dk, dv, e);
+        }
+        /* backward, segment by segment */
+        if (dhT) memcpy(dS, dhT + p * sz, sizeof(double) * (size_t)sz);
+        else memset(dS, 0, sizeof(double) * (size_t)sz);
+        for (long s = nseg - 1; s >= 0; --s) {
+            const long t0 = s * seg;
+            const long t1 = (t0 + seg < T) ? t0 + seg : T;
+            memcpy(sb, ck + s * sz, sizeof(double) * (size_t)sz);
+            for (long t = t0; t < t1; ++t) {
+                const long row = (b * T + t) * H + h;
+                memcpy(sb + (t - t0 + 1) * sz, sb + (t - t0) * sz,
+                       sizeof(double) * (size_t)sz);
+                kla_token_rule(sb + (t - t0 + 1) * sz, k + row * dk,
+                               v + row * dv, log_alpha[row], eta[row], eps,
+                               given, dk, dv, e);
+            }
+            for (long t = t1 - 1; t >= t0; --t) {
+                const long row = (b * T + t) * H + h;
+                kla_token_bwd(sb + (t - t0) * sz, sb + (t - t0 + 1) * sz,
+                              q + row * dk, k + row * dk, v + row * dv,
+                              log_alpha[row], eta[row], eps, given,
+                              dout + row * dv, dS, dq + row * dk,
+                              dk_out + row * dk, dv_out + row * dv,
+                              dla + row, deta + row, dk, dv, e, de, tk);
+            }
+        }
+        if (dh0) memcpy(dh0 + p * sz, dS, sizeof(double) * (size_t)sz);
+        free(ck); free(sb); free(dS); free(e); free(de); free(tk);
+    }
+    (void)n_threads;
+    return failed ? -2 : 0;
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int oracle_max_threads(void)
 {

@@ -434,3 +434,118 @@ def test_decode_oracle_shapes_and_state_untouched():
                                       rng.uniform(0, 1, (N, H)), 1e-6, S)
     assert o.shape == (N, H, dv) and S_new.shape == S.shape
     assert np.array_equal(S, S_copy)
+
+
+# ---------------------------------------------------------------- backward
+
+def _bwd_case(seed, B=1, T=70, H=2, dk=4, dv=3, with_h0=True, eps=1e-3):
+    """Random inputs plus upstream gradients for L = <dout, o> + <dhT, hT>.
+    T = 70 crosses the oracle's 64-token checkpoint boundary."""
+    rng = np.random.default_rng(seed)
+    q, k, v, la, et, eps, S0 = _rand(rng, B, T, H, dk, dv, eps=eps)
+    if not with_h0:
+        S0 = None
+    dout = rng.standard_normal((B, T, H, dv))
+    dhT = rng.standard_normal((B, H, dk, dv))
+    return dict(q=q, k=k, v=v, la=la, eta=et, h0=S0), eps, dout, dhT, rng
+
+
+def _loss(x, eps, dout, dhT, given):
+    """L through the (pinned) forward oracle.  The learned-step rule
+    beta = b is the Kaczmarz forward with eta = b (||k||^2 + eps), a
+    function of (b, k), so its finite differences carry that chain rule."""
+    eta = x["eta"]
+    if given:
+        eta = x["eta"] * (np.sum(x["k"] ** 2, axis=-1) + eps)
+    o, hT = oracle.kla_fwd(x["q"], x["k"], x["v"], x["la"], eta, eps,
+                           x["h0"])
+    return float(np.sum(o * dout) + np.sum(hT * dhT))
+
+
+_GRAD = dict(q="dq", k="dk", v="dv", la="dlog_alpha", eta="deta",
+             h0="dh0")
+
+
+@pytest.mark.parametrize("given", [False, True], ids=["kaczmarz", "given"])
+@pytest.mark.parametrize("with_h0", [True, False])
+def test_backward_matches_finite_differences(given, with_h0):
+    """Directional central differences of L (through the forward oracle)
+    along random directions of every input equal <grad, direction>."""
+    x, eps, dout, dhT, rng = _bwd_case(30 + 2 * given + with_h0,
+                                       with_h0=with_h0)
+    g = oracle.kla_bwd(x["q"], x["k"], x["v"], x["la"], x["eta"], eps,
+                       x["h0"], dout, dhT, given=given)
+    for name, val in x.items():
+        if val is None:
+            continue
+        for _ in range(2):
+            u = rng.standard_normal(val.shape)
+            h = 1e-6
+            xp, xm = dict(x), dict(x)
+            xp[name], xm[name] = val + h * u, val - h * u
+            fd = (_loss(xp, eps, dout, dhT, given) -
+                  _loss(xm, eps, dout, dhT, given)) / (2 * h)
+            an = float(np.sum(g[_GRAD[name]] * u))
+            assert abs(fd - an) <= 1e-7 * max(1.0, abs(an)), (name, fd, an)
+
+
+def _torch_forward(q, k, v, la, eta, eps, h0, given):
+    """The recurrence in plain PyTorch fp64 (token loop), for autograd."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    S = (h0.clone() if h0 is not None else
+         torch.zeros(B, H, dk, dv, dtype=torch.float64))
+    outs = []
+    for t in range(T):
+        kt, vt, qt = k[:, t], v[:, t], q[:, t]
+        St = torch.exp(la[:, t])[..., None, None] * S
+        if given:
+            beta = eta[:, t]
+        else:
+            beta = eta[:, t] / ((kt * kt).sum(-1) + eps)
+        e = vt - torch.einsum("bhij,bhi->bhj", St, kt)
+        S = St + beta[..., None, None] * kt[..., :, None] * e[..., None, :]
+        outs.append(torch.einsum("bhij,bhi->bhj", S, qt))
+    return torch.stack(outs, 1), S
+
+
+@pytest.mark.parametrize("given", [False, True], ids=["kaczmarz", "given"])
+def test_backward_matches_autograd(given):
+    """Reverse mode of an independent PyTorch fp64 forward (autograd)."""
+    x, eps, dout, dhT, _ = _bwd_case(40 + given, T=20, H=3, dk=5, dv=4)
+    g = oracle.kla_bwd(x["q"], x["k"], x["v"], x["la"], x["eta"], eps,
+                       x["h0"], dout, dhT, given=given)
+    tx = {n: torch.tensor(a, requires_grad=True) for n, a in x.items()}
+    o, hT = _torch_forward(tx["q"], tx["k"], tx["v"], tx["la"], tx["eta"],
+                           eps, tx["h0"], given)
+    loss = (o * torch.tensor(dout)).sum() + (hT * torch.tensor(dhT)).sum()
+    loss.backward()
+    for n, t in tx.items():
+        assert _rel(g[_GRAD[n]], t.grad.numpy()) < 1e-11, n
+
+
+def test_backward_closed_form_without_writes():
+    """eta = 0 and alpha = 1: S_t = h0 for every t, o_t = h0^T q_t.  Then
+    dq_t = h0 dout_t, dh0 = dhT + sum_t q_t dout_t^T, dv = dk = 0,
+    dlog_alpha_t = <D_t, h0> and deta_t = k_t^T D_t (v_t - h0^T k_t) /
+    (||k_t||^2 + eps), with D_t = dhT + sum_{s >= t} q_s dout_s^T."""
+    x, eps, dout, dhT, _ = _bwd_case(50, T=12, H=2, dk=4, dv=3)
+    x["eta"] = np.zeros_like(x["eta"])
+    x["la"] = np.zeros_like(x["la"])
+    g = oracle.kla_bwd(x["q"], x["k"], x["v"], x["la"], x["eta"], eps,
+                       x["h0"], dout, dhT)
+    q, k, v, h0 = x["q"], x["k"], x["v"], x["h0"]
+    B, T, H, _ = q.shape
+    D = dhT.copy()
+    for t in range(T - 1, -1, -1):
+        D = D + np.einsum("bhi,bhj->bhij", q[:, t], dout[:, t])
+        assert _rel(g["dq"][:, t],
+                    np.einsum("bhij,bhj->bhi", h0, dout[:, t])) < 1e-13
+        assert _rel(g["dlog_alpha"][:, t],
+                    np.einsum("bhij,bhij->bh", D, h0)) < 1e-12
+        e = v[:, t] - np.einsum("bhij,bhi->bhj", h0, k[:, t])
+        de = np.einsum("bhi,bhij,bhj->bh", k[:, t], D, e) / (
+            np.sum(k[:, t] ** 2, -1) + eps)
+        assert _rel(g["deta"][:, t], de) < 1e-12
+    assert _rel(g["dh0"], D) < 1e-13
+    assert np.max(np.abs(g["dv"])) == 0.0 and np.max(np.abs(g["dk"])) == 0.0

@@ -38,6 +38,8 @@
 #ifndef KLA_H
 #define KLA_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -146,6 +148,57 @@ KLA_API kla_status kla_decode_step_ex(const void* q, const void* k,
                               const float* eta, float eps, float* S, void* o,
                               int N, int H, int dk, int dv, kla_dtype dtype,
                               kla_step_rule rule, kla_stream_t stream);
+
+/*
+ * kla_chunk_bwd_workspace_size -- bytes of device workspace kla_chunk_bwd
+ * needs for these sizes: two fp32 tensors [B, H, ceil(T/C), dk, dv] (the
+ * state at every chunk start and the gradient of the loss with respect to
+ * the state at every chunk end).  Writes 0 for an empty problem.  Errors:
+ * KLA_ERR_INVALID_ARG (null `bytes`, negative size, C <= 0).
+ */
+KLA_API kla_status kla_chunk_bwd_workspace_size(int B, int T, int H, int dk,
+                                                int dv, int C, size_t* bytes);
+
+/*
+ * kla_chunk_bwd -- backward pass of kla_chunk_fwd_ex: given the gradients of
+ * a loss L with respect to o (o_grad) and to the final state (hT_grad,
+ * NULL = zero), writes the gradients with respect to every input.  The
+ * forward pass is recomputed (it need not have been run); the result equals
+ * the reverse mode of the token-by-token recurrence above up to
+ * floating-point rounding, for either step rule (with KLA_STEP_KACZMARZ, k
+ * also receives the gradient through ||k||^2 in beta).  The chunkwise form
+ * differentiated is that of the page's section "Implementacion"; the page
+ * gives no backward pass of its own.
+ *
+ *   q, k, v, log_alpha, eta, eps, h0, B, T, H, dk, dv, C, dtype, rule:
+ *                  as for kla_chunk_fwd_ex (read)
+ *   o_grad         [B, T, H, dv]  dtype   (read)
+ *   hT_grad        [B, H, dk, dv] fp32    (read) or NULL
+ *   q_grad, k_grad [B, T, H, dk]  dtype   (written)
+ *   v_grad         [B, T, H, dv]  dtype   (written)
+ *   log_alpha_grad, eta_grad  [B, T, H] fp32 (written)
+ *   h0_grad        [B, H, dk, dv] fp32    (written) or NULL
+ *   workspace      device memory of at least
+ *                  kla_chunk_bwd_workspace_size(...) bytes, 16-byte aligned,
+ *                  owned by the caller; its contents on entry do not matter
+ *                  and are garbage on return
+ *
+ * Runs on the CUDA cores in fp32 (three launches).  Supported shapes as for
+ * kla_chunk_fwd.  Outputs must not alias inputs, each other or the
+ * workspace.  Errors: KLA_ERR_INVALID_ARG (null required pointer, negative
+ * size, bad enum, eps < 0 or not finite, workspace too small or misaligned),
+ * KLA_ERR_UNSUPPORTED_SHAPE, KLA_ERR_CUDA.
+ */
+KLA_API kla_status kla_chunk_bwd(const void* q, const void* k, const void* v,
+                                 const float* log_alpha, const float* eta,
+                                 float eps, const float* h0,
+                                 const void* o_grad, const float* hT_grad,
+                                 void* q_grad, void* k_grad, void* v_grad,
+                                 float* log_alpha_grad, float* eta_grad,
+                                 float* h0_grad, int B, int T, int H, int dk,
+                                 int dv, int C, kla_dtype dtype,
+                                 kla_step_rule rule, void* workspace,
+                                 size_t workspace_bytes, kla_stream_t stream);
 
 /*
  * kla_device_status -- synchronises `stream`, then reads and clears the

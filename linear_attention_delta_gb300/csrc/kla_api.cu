@@ -132,6 +132,87 @@ extern "C" kla_status kla_decode_step(const void* q, const void* k,
                               dtype, KLA_STEP_KACZMARZ, stream);
 }
 
+extern "C" kla_status kla_chunk_bwd_workspace_size(int B, int T, int H,
+                                                   int dk, int dv, int C,
+                                                   size_t* bytes) {
+    if (!bytes || B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || C <= 0)
+        return KLA_ERR_INVALID_ARG;
+    *bytes = sizeof(float) *
+             kla::chunk_bwd_workspace_floats(B, T, H, dk, dv, C);
+    return KLA_OK;
+}
+
+extern "C" kla_status kla_chunk_bwd(
+    const void* q, const void* k, const void* v, const float* log_alpha,
+    const float* eta, float eps, const float* h0, const void* o_grad,
+    const float* hT_grad, void* q_grad, void* k_grad, void* v_grad,
+    float* log_alpha_grad, float* eta_grad, float* h0_grad, int B, int T,
+    int H, int dk, int dv, int C, kla_dtype dtype, kla_step_rule rule,
+    void* workspace, size_t workspace_bytes, kla_stream_t stream) {
+    if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || C <= 0)
+        return KLA_ERR_INVALID_ARG;
+    if (dtype != KLA_F32 && dtype != KLA_BF16) return KLA_ERR_INVALID_ARG;
+    if (rule != KLA_STEP_KACZMARZ && rule != KLA_STEP_GIVEN)
+        return KLA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return KLA_ERR_INVALID_ARG;
+    if (!supported_dim(dk) || !supported_dim(dv) || !supported_chunk(C))
+        return KLA_ERR_UNSUPPORTED_SHAPE;
+    const long long nch = ((long long)T + C - 1) / C;
+    if ((long long)B * H > 0x7fffffffLL ||
+        (long long)B * H * nch > 0x7fffffffLL)
+        return KLA_ERR_UNSUPPORTED_SHAPE;
+    const bool empty = (long long)B * H == 0;
+    if (!empty && T > 0) {
+        if (!q || !k || !v || !log_alpha || !eta || !o_grad || !q_grad ||
+            !k_grad || !v_grad || !log_alpha_grad || !eta_grad || !workspace)
+            return KLA_ERR_INVALID_ARG;
+        const size_t elt = dtype == KLA_BF16 ? 2 : 4;
+        if (!aligned(q, elt) || !aligned(k, elt) || !aligned(v, elt) ||
+            !aligned(o_grad, elt) || !aligned(q_grad, elt) ||
+            !aligned(k_grad, elt) || !aligned(v_grad, elt) ||
+            !aligned(log_alpha, 4) || !aligned(eta, 4) ||
+            !aligned(log_alpha_grad, 4) || !aligned(eta_grad, 4) ||
+            !aligned(workspace, 16))
+            return KLA_ERR_INVALID_ARG;
+        const void* ins[] = {q, k, v, log_alpha, eta, h0, o_grad, hT_grad};
+        const void* outs[] = {q_grad, k_grad, v_grad, log_alpha_grad,
+                              eta_grad, h0_grad, workspace};
+        for (const void* out : outs) {
+            if (!out) continue;
+            for (const void* in : ins)
+                if (in == out) return KLA_ERR_INVALID_ARG;
+            int same = 0;
+            for (const void* o2 : outs) same += (o2 == out);
+            if (same > 1) return KLA_ERR_INVALID_ARG;
+        }
+        if (workspace_bytes <
+            sizeof(float) * kla::chunk_bwd_workspace_floats(B, T, H, dk, dv,
+                                                            C))
+            return KLA_ERR_INVALID_ARG;
+    }
+    if ((h0 && !aligned(h0, 4)) || (hT_grad && !aligned(hT_grad, 4)) ||
+        (h0_grad && !aligned(h0_grad, 4)))
+        return KLA_ERR_INVALID_ARG;
+    if (empty) return KLA_OK;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (T == 0) {   // L depends on h0 only through hT = h0
+        if (!h0_grad) return KLA_OK;
+        const size_t bytes = sizeof(float) * (size_t)B * H * dk * dv;
+        if (hT_grad)
+            return from_cuda(cudaMemcpyAsync(h0_grad, hT_grad, bytes,
+                                             cudaMemcpyDeviceToDevice, s));
+        return from_cuda(cudaMemsetAsync(h0_grad, 0, bytes, s));
+    }
+    const size_t half = kla::chunk_bwd_workspace_floats(B, T, H, dk, dv, C) / 2;
+    float* ws = static_cast<float*>(workspace);
+    kla::BwdArgs a{q, k, v, log_alpha, eta, eps,
+                   rule == KLA_STEP_GIVEN ? 1 : 0, h0, o_grad, hT_grad,
+                   q_grad, k_grad, v_grad, log_alpha_grad, eta_grad, h0_grad,
+                   ws, ws + half, B, T, H, dk, dv, C, dtype};
+    return from_cuda(kla::launch_chunk_bwd(a, s));
+}
+
 extern "C" kla_status kla_device_status(kla_stream_t stream) {
     unsigned int word = 0;
     cudaError_t e = kla::read_and_clear_fault(

@@ -1,0 +1,621 @@
+// Chunkwise KLA backward pass on CUDA cores, all arithmetic in fp32, for every
+// supported (dk, dv, C) and both I/O types.
+//
+// Per chunk (rows r, i = 0..C-1; g = in-chunk cumulative log decay,
+// gamma_r = exp(g_r), Gamma_ri = exp(g_r - g_i), lambda_t = exp(g_C - g_t),
+// beta, A = I + strict_lower(Diag(beta)(Gamma o K K^T)), T = A^{-1},
+// P = lower_incl(Gamma o Q K^T) as in the forward; S = the state the chunk
+// starts from, dS' = dL/dS at its end):
+//   X   = V - Diag(gamma) K S,   F = Diag(beta) X,   U~ = T F
+//   dU~ = P^T dO + Diag(lambda) K dS'
+//   dF  = T^T dU~,   dX = Diag(beta) dF = dV
+//   dS  = gamma_C dS' + Q^T Diag(gamma) dO - K^T Diag(gamma) dX
+//   dP  = dO U~^T (lower incl.),   dA = -dF U~^T (strictly lower)
+//   dQ  = Diag(gamma) dO S^T + (Gamma o dP) K
+//   dK  = Diag(lambda) U~ dS'^T - Diag(gamma) dX S^T + (Gamma o dP)^T Q
+//         + (D + D^T) K + 2 Diag(dn) K,      D = Diag(beta) (Gamma o dA)
+//   dbeta_r = sum_j dF_rj X_rj + sum_{i<r} dA_ri Gamma_ri k_r.k_i
+//   deta = dbeta / (||k||^2 + eps),  dn = -dbeta beta / (||k||^2 + eps)
+//          (learned-step rule: deta = dbeta, dn = 0)
+//   dg_r = dgamma_r gamma_r + sum_i dGamma_ri Gamma_ri
+//          - sum_r' dGamma_r'r Gamma_r'r - dlambda_r lambda_r
+//          (+ sum_t dlambda_t lambda_t + <dS', S> gamma_C on the last row),
+//   dlog_alpha_j = sum_{r >= j} dg_r.
+// This differentiates the chunkwise form of the forward pass (the gated
+// DeltaNet block solver with B = Diag(beta); gist.science/es/paper/2605.08587,
+// section "Implementacion").
+//
+// Three launches: the CUDA-core forward writes the state at every chunk start
+// (ckpt); kla_bwd_state_kernel walks the chunks in reverse (one CTA per
+// (batch, head, dv tile): the recurrence for dS is column-separable) and
+// writes dS' of every chunk (dsck) and dh0; kla_bwd_grad_kernel then forms
+// every gradient of one chunk's tokens per CTA, all chunks in parallel.
+#include "kla_internal.cuh"
+
+namespace kla {
+namespace {
+
+constexpr int kBwdThreads = 256;
+constexpr int kBwdMaxC = 64;
+
+__device__ __forceinline__ void load_chunk_qk(const BwdArgs& a, int b, int h,
+                                              int t0, int DK, int LDK,
+                                              float* Qs, float* Ks,
+                                              float* gs, float* bs) {
+    const int C = a.C, T = a.T, H = a.H;
+    for (int idx = threadIdx.x; idx < C * DK; idx += kBwdThreads) {
+        const int r = idx / DK, c = idx % DK;
+        const int t = t0 + r;
+        float qv = 0.f, kv = 0.f;
+        if (t < T) {
+            const size_t off = (((size_t)b * T + t) * H + h) * DK + c;
+            if (a.dtype == KLA_BF16) {
+                qv = to_f32(static_cast<const __nv_bfloat16*>(a.q)[off]);
+                kv = to_f32(static_cast<const __nv_bfloat16*>(a.k)[off]);
+            } else {
+                qv = static_cast<const float*>(a.q)[off];
+                kv = static_cast<const float*>(a.k)[off];
+            }
+        }
+        Qs[r * LDK + c] = qv;
+        Ks[r * LDK + c] = kv;
+    }
+    if (threadIdx.x < C) {
+        const int t = t0 + threadIdx.x;
+        const size_t off = ((size_t)b * T + t) * H + h;
+        gs[threadIdx.x] = t < T ? a.log_alpha[off] : 0.f;
+        bs[threadIdx.x] = t < T ? a.eta[off] : 0.f;
+    }
+}
+
+// beta (raw eta in bs on entry), ||k||^2 (nrm, may be null), the cumulative
+// log decay in gs, gamma and lambda.  Ends with a barrier.
+template <int DK>
+__device__ __forceinline__ void chunk_gates(const BwdArgs& a, const float* Ks,
+                                            int LDK, float* gs, float* bs,
+                                            float* gam, float* lam,
+                                            float* nrm) {
+    const int C = a.C, tid = threadIdx.x;
+    if (tid < C) {
+        float n = 0.f;
+        for (int c = 0; c < DK; ++c) {
+            const float x = Ks[tid * LDK + c];
+            n = fmaf(x, x, n);
+        }
+        if (nrm) nrm[tid] = n;
+        const float denom = n + a.eps;
+        if (!a.gdn) bs[tid] = denom == 0.f ? 0.f : bs[tid] / denom;
+    }
+    if (tid == 32) {
+        float acc = 0.f;
+        for (int r = 0; r < C; ++r) {
+            acc += gs[r];
+            gs[r] = acc;
+        }
+    }
+    __syncthreads();
+    if (tid < C) {
+        gam[tid] = expf(gs[tid]);
+        lam[tid] = expf(gs[C - 1] - gs[tid]);
+    }
+}
+
+// A (unit lower, strictly lower part beta_r Gamma_ri k_r.k_i) and
+// P = Gamma o Q K^T (lower incl.), row stride ldc.
+template <int DK>
+__device__ __forceinline__ void build_a_p(int C, const float* Qs,
+                                          const float* Ks, int LDK,
+                                          const float* gs, const float* bs,
+                                          float* As, float* Ps, int ldc) {
+    for (int idx = threadIdx.x; idx < C * C; idx += kBwdThreads) {
+        const int r = idx / C, i = idx % C;
+        float av = (i == r) ? 1.f : 0.f;
+        float pv = 0.f;
+        if (i <= r) {
+            float kk = 0.f, qk = 0.f;
+#pragma unroll 8
+            for (int c = 0; c < DK; ++c) {
+                const float ki = Ks[i * LDK + c];
+                kk = fmaf(Ks[r * LDK + c], ki, kk);
+                qk = fmaf(Qs[r * LDK + c], ki, qk);
+            }
+            const float dec = expf(gs[r] - gs[i]);
+            pv = dec * qk;
+            if (i < r) av = bs[r] * dec * kk;
+        }
+        As[r * ldc + i] = av;
+        Ps[r * ldc + i] = pv;
+    }
+}
+
+template <typename IO>
+__device__ __forceinline__ float ld_io(const void* p, size_t off) {
+    return to_f32(static_cast<const IO*>(p)[off]);
+}
+
+// ------------------------------------------------------------------ dS
+template <int DK, int DVT>
+struct StateSmem {
+    static constexpr int LDK = DK + 1;
+    static constexpr int LDV = DVT + 1;
+    static constexpr int LDC = kBwdMaxC + 1;
+    static constexpr int Q = 0;
+    static constexpr int K = Q + kBwdMaxC * LDK;
+    static constexpr int DO = K + kBwdMaxC * LDK;
+    static constexpr int W = DO + kBwdMaxC * LDV;
+    static constexpr int DS = W + kBwdMaxC * LDV;
+    static constexpr int A = DS + DK * LDV;
+    static constexpr int P = A + kBwdMaxC * LDC;
+    static constexpr int G = P + kBwdMaxC * LDC;
+    static constexpr int BETA = G + kBwdMaxC;
+    static constexpr int GAM = BETA + kBwdMaxC;
+    static constexpr int LAM = GAM + kBwdMaxC;
+    static constexpr int TOTAL = LAM + kBwdMaxC;
+    static constexpr size_t BYTES = sizeof(float) * (size_t)TOTAL;
+};
+
+template <int DK, int DVT, typename IO>
+__global__ void __launch_bounds__(kBwdThreads)
+kla_bwd_state_kernel(BwdArgs a) {
+    using L = StateSmem<DK, DVT>;
+    extern __shared__ float sm[];
+    float* Qs = sm + L::Q;
+    float* Ks = sm + L::K;
+    float* Ds = sm + L::DO;
+    float* Ws = sm + L::W;
+    float* dS = sm + L::DS;
+    float* As = sm + L::A;
+    float* Ps = sm + L::P;
+    float* gs = sm + L::G;
+    float* bs = sm + L::BETA;
+    float* gam = sm + L::GAM;
+    float* lam = sm + L::LAM;
+
+    const int bh = blockIdx.x;
+    const int b = bh / a.H, h = bh % a.H;
+    const int j0 = blockIdx.y * DVT;
+    const int tid = threadIdx.x;
+    const int C = a.C, T = a.T, H = a.H, dv = a.dv;
+    const int nch = (T + C - 1) / C;
+
+    for (int idx = tid; idx < DK * DVT; idx += kBwdThreads) {
+        const int c = idx / DVT, j = idx % DVT;
+        dS[c * L::LDV + j] =
+            a.dhT ? a.dhT[((size_t)bh * DK + c) * dv + j0 + j] : 0.f;
+    }
+
+    for (int ch = nch - 1; ch >= 0; --ch) {
+        const int t0 = ch * C;
+        load_chunk_qk(a, b, h, t0, DK, L::LDK, Qs, Ks, gs, bs);
+        for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
+            const int r = idx / DVT, j = idx % DVT;
+            const int t = t0 + r;
+            Ds[r * L::LDV + j] =
+                t < T ? ld_io<IO>(a.dout, (((size_t)b * T + t) * H + h) * dv +
+                                              j0 + j)
+                      : 0.f;
+        }
+        __syncthreads();
+        chunk_gates<DK>(a, Ks, L::LDK, gs, bs, gam, lam, nullptr);
+        build_a_p<DK>(C, Qs, Ks, L::LDK, gs, bs, As, Ps, L::LDC);
+        {   // dL/dS at the end of this chunk
+            float* out = a.dsck + ((size_t)bh * nch + ch) * DK * dv + j0;
+            for (int idx = tid; idx < DK * DVT; idx += kBwdThreads) {
+                const int c = idx / DVT, j = idx % DVT;
+                out[(size_t)c * dv + j] = dS[c * L::LDV + j];
+            }
+        }
+        __syncthreads();
+
+        // dU~ = P^T dO + Diag(lambda) K dS'
+        for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
+            const int r = idx / DVT, j = idx % DVT;
+            float kds = 0.f;
+#pragma unroll 8
+            for (int c = 0; c < DK; ++c)
+                kds = fmaf(Ks[r * L::LDK + c], dS[c * L::LDV + j], kds);
+            float w = lam[r] * kds;
+            for (int i = r; i < C; ++i)
+                w = fmaf(Ps[i * L::LDC + r], Ds[i * L::LDV + j], w);
+            Ws[r * L::LDV + j] = w;
+        }
+        __syncthreads();
+
+        // dF = A^{-T} dU~: back substitution, one thread per column
+        if (tid < DVT) {
+            for (int r = C - 1; r >= 0; --r) {
+                float x = Ws[r * L::LDV + tid];
+                for (int i = r + 1; i < C; ++i)
+                    x = fmaf(-As[i * L::LDC + r], Ws[i * L::LDV + tid], x);
+                Ws[r * L::LDV + tid] = x;
+            }
+        }
+        __syncthreads();
+
+        // dS = gamma_C dS' + Q^T Diag(gamma) dO - K^T Diag(gamma beta) dF
+        const float gC = gam[C - 1];
+        for (int idx = tid; idx < DK * DVT; idx += kBwdThreads) {
+            const int c = idx / DVT, j = idx % DVT;
+            float acc = gC * dS[c * L::LDV + j];
+            for (int r = 0; r < C; ++r)
+                acc = fmaf(gam[r],
+                           Qs[r * L::LDK + c] * Ds[r * L::LDV + j] -
+                               Ks[r * L::LDK + c] * bs[r] * Ws[r * L::LDV + j],
+                           acc);
+            dS[c * L::LDV + j] = acc;
+        }
+        __syncthreads();
+    }
+
+    if (a.dh0) {
+        for (int idx = tid; idx < DK * DVT; idx += kBwdThreads) {
+            const int c = idx / DVT, j = idx % DVT;
+            a.dh0[((size_t)bh * DK + c) * dv + j0 + j] = dS[c * L::LDV + j];
+        }
+    }
+}
+
+// ------------------------------------------------------------- gradients
+template <int DK, int DVT>
+struct GradSmem {
+    static constexpr int LDK = DK + 1;
+    static constexpr int LDV = DVT + 1;
+    static constexpr int LDC = kBwdMaxC + 1;
+    static constexpr int Q = 0;
+    static constexpr int K = Q + kBwdMaxC * LDK;
+    static constexpr int A = K + kBwdMaxC * LDK;       // later dGamma Gamma
+    static constexpr int P = A + kBwdMaxC * LDC;
+    static constexpr int DP = P + kBwdMaxC * LDC;      // later Gamma o dP
+    static constexpr int DA = DP + kBwdMaxC * LDC;     // later D
+    static constexpr int ST = DA + kBwdMaxC * LDC;     // S tile
+    static constexpr int DST = ST + DK * LDV;          // dS' tile
+    static constexpr int X = DST + DK * LDV;           // V, then X
+    static constexpr int DO = X + kBwdMaxC * LDV;
+    static constexpr int U = DO + kBwdMaxC * LDV;      // F, then U~
+    static constexpr int W = U + kBwdMaxC * LDV;       // dU~, then dF
+    static constexpr int KS = W + kBwdMaxC * LDV;
+    static constexpr int G = KS + kBwdMaxC * LDV;
+    static constexpr int BETA = G + kBwdMaxC;
+    static constexpr int GAM = BETA + kBwdMaxC;
+    static constexpr int LAM = GAM + kBwdMaxC;
+    static constexpr int NRM = LAM + kBwdMaxC;
+    static constexpr int DB = NRM + kBwdMaxC;          // dbeta, later dn
+    static constexpr int DGAM = DB + kBwdMaxC;
+    static constexpr int DLAM = DGAM + kBwdMaxC;
+    static constexpr int DG = DLAM + kBwdMaxC;
+    static constexpr int DGC = DG + kBwdMaxC;          // <dS', S>
+    static constexpr int TOTAL = DGC + 4;
+    static constexpr size_t BYTES = sizeof(float) * (size_t)TOTAL;
+};
+
+template <int DK, int DVT, typename IO>
+__global__ void __launch_bounds__(kBwdThreads)
+kla_bwd_grad_kernel(BwdArgs a) {
+    using L = GradSmem<DK, DVT>;
+    constexpr int kAcc = kBwdMaxC * DK / kBwdThreads;  // owned (r, c) pairs
+    extern __shared__ float sm[];
+    float* Qs = sm + L::Q;
+    float* Ks = sm + L::K;
+    float* As = sm + L::A;
+    float* Ps = sm + L::P;
+    float* dP = sm + L::DP;
+    float* dA = sm + L::DA;
+    float* St = sm + L::ST;
+    float* dSt = sm + L::DST;
+    float* Xs = sm + L::X;
+    float* Ds = sm + L::DO;
+    float* Us = sm + L::U;
+    float* Ws = sm + L::W;
+    float* KS = sm + L::KS;
+    float* gs = sm + L::G;
+    float* bs = sm + L::BETA;
+    float* gam = sm + L::GAM;
+    float* lam = sm + L::LAM;
+    float* nrm = sm + L::NRM;
+    float* db = sm + L::DB;
+    float* dgam = sm + L::DGAM;
+    float* dlam = sm + L::DLAM;
+    float* dg = sm + L::DG;
+    float* dgc = sm + L::DGC;
+
+    const int C = a.C, T = a.T, H = a.H, dv = a.dv;
+    const int nch = (T + C - 1) / C;
+    const long blk = blockIdx.x;
+    const int bh = (int)(blk / nch), ch = (int)(blk % nch);
+    const int b = bh / H, h = bh % H;
+    const int t0 = ch * C;
+    const int tid = threadIdx.x;
+    const float* Sg = a.ckpt + ((size_t)bh * nch + ch) * DK * dv;
+    const float* dSg = a.dsck + ((size_t)bh * nch + ch) * DK * dv;
+
+    load_chunk_qk(a, b, h, t0, DK, L::LDK, Qs, Ks, gs, bs);
+    for (int idx = tid; idx < C * L::LDC; idx += kBwdThreads) {
+        dP[idx] = 0.f;
+        dA[idx] = 0.f;
+    }
+    if (tid < kBwdMaxC) {
+        db[tid] = 0.f;
+        dgam[tid] = 0.f;
+        dlam[tid] = 0.f;
+    }
+    if (tid == 0) dgc[0] = 0.f;
+    __syncthreads();
+    chunk_gates<DK>(a, Ks, L::LDK, gs, bs, gam, lam, nrm);
+    build_a_p<DK>(C, Qs, Ks, L::LDK, gs, bs, As, Ps, L::LDC);
+    __syncthreads();
+
+    float dq_acc[kAcc], dk_acc[kAcc];
+#pragma unroll
+    for (int m = 0; m < kAcc; ++m) dq_acc[m] = dk_acc[m] = 0.f;
+
+    for (int j0 = 0; j0 < dv; j0 += DVT) {
+        float sdot = 0.f;
+        for (int idx = tid; idx < DK * DVT; idx += kBwdThreads) {
+            const int c = idx / DVT, j = idx % DVT;
+            const float sv = Sg[(size_t)c * dv + j0 + j];
+            const float dsv = dSg[(size_t)c * dv + j0 + j];
+            St[c * L::LDV + j] = sv;
+            dSt[c * L::LDV + j] = dsv;
+            sdot = fmaf(sv, dsv, sdot);
+        }
+        atomicAdd(dgc, sdot);
+        for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
+            const int r = idx / DVT, j = idx % DVT;
+            const int t = t0 + r;
+            const size_t off = (((size_t)b * T + t) * H + h) * dv + j0 + j;
+            Xs[r * L::LDV + j] = t < T ? ld_io<IO>(a.v, off) : 0.f;
+            Ds[r * L::LDV + j] = t < T ? ld_io<IO>(a.dout, off) : 0.f;
+        }
+        __syncthreads();
+
+        // K S, X = V - Diag(gamma) K S, F = Diag(beta) X; dgamma from Q S
+        for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
+            const int r = idx / DVT, j = idx % DVT;
+            float ks = 0.f, qs = 0.f;
+#pragma unroll 8
+            for (int c = 0; c < DK; ++c) {
+                const float sv = St[c * L::LDV + j];
+                ks = fmaf(Ks[r * L::LDK + c], sv, ks);
+                qs = fmaf(Qs[r * L::LDK + c], sv, qs);
+            }
+            KS[r * L::LDV + j] = ks;
+            const float x = fmaf(-gam[r], ks, Xs[r * L::LDV + j]);
+            Xs[r * L::LDV + j] = x;
+            Us[r * L::LDV + j] = bs[r] * x;
+            atomicAdd(&dgam[r], Ds[r * L::LDV + j] * qs);
+        }
+        __syncthreads();
+
+        // U~ = A^{-1} F: forward substitution, one thread per column
+        if (tid < DVT) {
+            for (int r = 0; r < C; ++r) {
+                float x = Us[r * L::LDV + tid];
+                for (int i = 0; i < r; ++i)
+                    x = fmaf(-As[r * L::LDC + i], Us[i * L::LDV + tid], x);
+                Us[r * L::LDV + tid] = x;
+            }
+        }
+        __syncthreads();
+
+        // dU~ = P^T dO + Diag(lambda) K dS';  dlambda_r = (K dS')_r . U~_r
+        for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
+            const int r = idx / DVT, j = idx % DVT;
+            float kds = 0.f;
+#pragma unroll 8
+            for (int c = 0; c < DK; ++c)
+                kds = fmaf(Ks[r * L::LDK + c], dSt[c * L::LDV + j], kds);
+            float w = lam[r] * kds;
+            for (int i = r; i < C; ++i)
+                w = fmaf(Ps[i * L::LDC + r], Ds[i * L::LDV + j], w);
+            Ws[r * L::LDV + j] = w;
+            atomicAdd(&dlam[r], kds * Us[r * L::LDV + j]);
+        }
+        __syncthreads();
+
+        // dF = A^{-T} dU~: back substitution, one thread per column
+        if (tid < DVT) {
+            for (int r = C - 1; r >= 0; --r) {
+                float x = Ws[r * L::LDV + tid];
+                for (int i = r + 1; i < C; ++i)
+                    x = fmaf(-As[i * L::LDC + r], Ws[i * L::LDV + tid], x);
+                Ws[r * L::LDV + tid] = x;
+            }
+        }
+        __syncthreads();
+
+        // dV = dX = Diag(beta) dF; dbeta from F = Diag(beta) X; dgamma from X
+        for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
+            const int r = idx / DVT, j = idx % DVT;
+            const int t = t0 + r;
+            const float df = Ws[r * L::LDV + j];
+            const float dx = bs[r] * df;
+            if (t < T)
+                static_cast<IO*>(a.dv_)[(((size_t)b * T + t) * H + h) * dv +
+                                        j0 + j] = from_f32<IO>(dx);
+            atomicAdd(&db[r], df * Xs[r * L::LDV + j]);
+            atomicAdd(&dgam[r], -dx * KS[r * L::LDV + j]);
+        }
+        // dP = dO U~^T (i <= r), dA = -dF U~^T (i < r)
+        for (int idx = tid; idx < C * C; idx += kBwdThreads) {
+            const int r = idx / C, i = idx % C;
+            if (i > r) continue;
+            float sp = 0.f, sa = 0.f;
+#pragma unroll 8
+            for (int j = 0; j < DVT; ++j) {
+                const float ui = Us[i * L::LDV + j];
+                sp = fmaf(Ds[r * L::LDV + j], ui, sp);
+                sa = fmaf(Ws[r * L::LDV + j], ui, sa);
+            }
+            dP[r * L::LDC + i] += sp;
+            if (i < r) dA[r * L::LDC + i] -= sa;
+        }
+        // owned (r, c): dQ += gamma_r dO S^T; dK += lambda_r U~ dS'^T -
+        // gamma_r beta_r dF S^T
+#pragma unroll
+        for (int m = 0; m < kAcc; ++m) {
+            const int idx = tid + m * kBwdThreads;
+            const int r = idx / DK, c = idx % DK;
+            if (r >= C) continue;
+            float sdo = 0.f, su = 0.f, sf = 0.f;
+#pragma unroll 8
+            for (int j = 0; j < DVT; ++j) {
+                const float sv = St[c * L::LDV + j];
+                sdo = fmaf(Ds[r * L::LDV + j], sv, sdo);
+                sf = fmaf(Ws[r * L::LDV + j], sv, sf);
+                su = fmaf(Us[r * L::LDV + j], dSt[c * L::LDV + j], su);
+            }
+            dq_acc[m] = fmaf(gam[r], sdo, dq_acc[m]);
+            dk_acc[m] += lam[r] * su - gam[r] * bs[r] * sf;
+        }
+        __syncthreads();
+    }
+
+    // dGamma o Gamma (into A), Gamma o dP (into dP), D (into dA), and the
+    // A-part of dbeta
+    for (int idx = tid; idx < C * C; idx += kBwdThreads) {
+        const int r = idx / C, i = idx % C;
+        float dgg = 0.f, dpt = 0.f, dd = 0.f;
+        if (i <= r) {
+            float qk = 0.f, kk = 0.f;
+#pragma unroll 8
+            for (int c = 0; c < DK; ++c) {
+                const float ki = Ks[i * L::LDK + c];
+                qk = fmaf(Qs[r * L::LDK + c], ki, qk);
+                kk = fmaf(Ks[r * L::LDK + c], ki, kk);
+            }
+            const float gmm = expf(gs[r] - gs[i]);
+            const float dpv = dP[r * L::LDC + i];
+            float dgm = dpv * qk;
+            dpt = gmm * dpv;
+            if (i < r) {
+                const float dav = dA[r * L::LDC + i];
+                dgm = fmaf(dav * bs[r], kk, dgm);
+                dd = bs[r] * gmm * dav;
+                atomicAdd(&db[r], dav * gmm * kk);
+            }
+            dgg = dgm * gmm;
+        }
+        As[r * L::LDC + i] = dgg;
+        dP[r * L::LDC + i] = dpt;
+        dA[r * L::LDC + i] = dd;
+    }
+    __syncthreads();
+
+    // per row: dg, deta, dn (dn replaces dbeta in db)
+    if (tid < C) {
+        const int r = tid;
+        float g = dgam[r] * gam[r] - dlam[r] * lam[r];
+        for (int i = 0; i <= r; ++i) g += As[r * L::LDC + i];
+        for (int rr = r; rr < C; ++rr) g -= As[rr * L::LDC + r];
+        if (r == C - 1) {
+            for (int t = 0; t < C; ++t) g = fmaf(dlam[t], lam[t], g);
+            g = fmaf(dgc[0], gam[C - 1], g);
+        }
+        dg[r] = g;
+        const float dbeta = db[r];
+        float deta, dn = 0.f;
+        if (a.gdn) {
+            deta = dbeta;
+        } else {
+            const float denom = nrm[r] + a.eps;
+            deta = denom == 0.f ? 0.f : dbeta / denom;
+            if (denom != 0.f) dn = -dbeta * bs[r] / denom;
+        }
+        const int t = t0 + r;
+        if (t < T) a.deta[((size_t)b * T + t) * H + h] = deta;
+        db[r] = dn;
+    }
+    __syncthreads();
+    if (tid < C) {   // dlog_alpha_j = sum_{r >= j} dg_r
+        float acc = 0.f;
+        for (int r = tid; r < C; ++r) acc += dg[r];
+        const int t = t0 + tid;
+        if (t < T) a.dlog_alpha[((size_t)b * T + t) * H + h] = acc;
+    }
+
+    // dQ += (Gamma o dP) K;  dK += (Gamma o dP)^T Q + (D + D^T) K + 2 dn k
+#pragma unroll
+    for (int m = 0; m < kAcc; ++m) {
+        const int idx = tid + m * kBwdThreads;
+        const int r = idx / DK, c = idx % DK;
+        if (r >= C) continue;
+        float q_acc = dq_acc[m], k_acc = dk_acc[m];
+        for (int i = 0; i <= r; ++i) {
+            q_acc = fmaf(dP[r * L::LDC + i], Ks[i * L::LDK + c], q_acc);
+            k_acc = fmaf(dA[r * L::LDC + i], Ks[i * L::LDK + c], k_acc);
+        }
+        for (int rr = r; rr < C; ++rr) {
+            k_acc = fmaf(dP[rr * L::LDC + r], Qs[rr * L::LDK + c], k_acc);
+            k_acc = fmaf(dA[rr * L::LDC + r], Ks[rr * L::LDK + c], k_acc);
+        }
+        k_acc = fmaf(2.f * db[r], Ks[r * L::LDK + c], k_acc);
+        const int t = t0 + r;
+        if (t < T) {
+            const size_t off = (((size_t)b * T + t) * H + h) * DK + c;
+            static_cast<IO*>(a.dq)[off] = from_f32<IO>(q_acc);
+            static_cast<IO*>(a.dk_)[off] = from_f32<IO>(k_acc);
+        }
+    }
+}
+
+template <int DK, int DVT, typename IO>
+cudaError_t launch_shape(const BwdArgs& a, cudaStream_t stream) {
+    using LS = StateSmem<DK, DVT>;
+    using LG = GradSmem<DK, DVT>;
+    auto ks = kla_bwd_state_kernel<DK, DVT, IO>;
+    auto kg = kla_bwd_grad_kernel<DK, DVT, IO>;
+    cudaError_t e = cudaFuncSetAttribute(
+        ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LS::BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)LG::BYTES);
+    if (e != cudaSuccess) return e;
+    const long bhs = (long)a.B * a.H;
+    const long nch = (a.T + a.C - 1) / a.C;
+    ks<<<dim3((unsigned)bhs, (unsigned)(a.dv / DVT)), kBwdThreads, LS::BYTES,
+         stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    kg<<<(unsigned)(bhs * nch), kBwdThreads, LG::BYTES, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t launch_dtype(const BwdArgs& a, cudaStream_t stream) {
+#define KLA_BWD_DK(DKV)                                                     \
+    if (a.dk == DKV) {                                                      \
+        if (a.dv == 16) return launch_shape<DKV, 16, IO>(a, stream);        \
+        return launch_shape<DKV, 32, IO>(a, stream);                        \
+    }
+    KLA_BWD_DK(16)
+    KLA_BWD_DK(32)
+    KLA_BWD_DK(64)
+    KLA_BWD_DK(128)
+#undef KLA_BWD_DK
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+size_t chunk_bwd_workspace_floats(int B, int T, int H, int dk, int dv,
+                                  int C) {
+    if (C <= 0) return 0;
+    const size_t nch = (size_t)(T + C - 1) / C;
+    return 2 * (size_t)B * H * nch * dk * dv;
+}
+
+cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t stream) {
+    if ((long)a.B * a.H == 0 || a.T == 0) return cudaSuccess;
+    if (a.C > kBwdMaxC) return cudaErrorInvalidValue;
+    // 1. states at every chunk start (CUDA-core forward, o not written)
+    FwdArgs f{a.q, a.k, a.v, a.log_alpha, a.eta, a.eps, a.gdn, a.h0,
+              nullptr, nullptr, a.B, a.T, a.H, a.dk, a.dv, a.C, a.dtype};
+    f.ckpt = a.ckpt;
+    cudaError_t e = launch_chunk_simt(f, stream);
+    if (e != cudaSuccess) return e;
+    // 2 and 3. dS' per chunk and dh0, then the gradients
+    if (a.dtype == KLA_BF16) return launch_dtype<__nv_bfloat16>(a, stream);
+    return launch_dtype<float>(a, stream);
+}
+
+}  // namespace kla

@@ -130,6 +130,14 @@ kla_chunk_simt_kernel(FwdArgs a) {
         }
         __syncthreads();
         if (tid < C) kd[tid] = expf(gs[C - 1] - gs[tid]);
+        if (a.ckpt) {   // the state this chunk starts from
+            float* ck = a.ckpt + ((size_t)bh * ((T + C - 1) / C) + t0 / C) *
+                                     DK * dv + j0;
+            for (int idx = tid; idx < DK * DVT; idx += kSimtThreads) {
+                const int c = idx / DVT, j = idx % DVT;
+                ck[(size_t)c * dv + j] = Ss[c * L::LDV + j];
+            }
+        }
 
         // ---- A (strictly lower part scaled by beta) and P = Gamma o QK^T ----
         for (int idx = tid; idx < C * C; idx += kSimtThreads) {
@@ -180,8 +188,9 @@ kla_chunk_simt_kernel(FwdArgs a) {
         }
         __syncthreads();
 
-        // ---- O = Diag(gamma) Q S + P U~ ----
-        for (int idx = tid; idx < C * DVT; idx += kSimtThreads) {
+        // ---- O = Diag(gamma) Q S + P U~ (skipped when only the states are
+        // wanted) ----
+        for (int idx = tid; o && idx < C * DVT; idx += kSimtThreads) {
             const int r = idx / DVT, j = idx % DVT;
             const int t = t0 + r;
             float qs = 0.f;

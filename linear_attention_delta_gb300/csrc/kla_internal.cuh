@@ -36,6 +36,32 @@ struct FwdArgs {
     float* hT;         // may be null
     int B, T, H, dk, dv, C;
     kla_dtype dtype;
+    // may be null: the state at the start of every chunk, fp32
+    // [B, H, ceil(T / C), dk, dv] (written by the CUDA-core kernel only)
+    float* ckpt = nullptr;
+};
+
+struct BwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* log_alpha;
+    const float* eta;
+    float eps;
+    int gdn;
+    const float* h0;     // may be null
+    const void* dout;    // like o
+    const float* dhT;    // may be null (zero)
+    void* dq;            // like q
+    void* dk_;           // like k
+    void* dv_;           // like v
+    float* dlog_alpha;   // [B, T, H]
+    float* deta;         // [B, T, H]
+    float* dh0;          // may be null
+    float* ckpt;         // workspace: state at every chunk start
+    float* dsck;         // workspace: dL/dS at every chunk end
+    int B, T, H, dk, dv, C;
+    kla_dtype dtype;
 };
 
 struct DecodeArgs {
@@ -59,6 +85,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_simt(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_tc(const FwdArgs& a, cudaStream_t stream);
 bool chunk_tc_eligible(const FwdArgs& a);
+// Backward pass: the checkpointing forward, the reverse state-gradient
+// recurrence and the per-chunk gradients (CUDA cores, fp32).
+cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t stream);
+size_t chunk_bwd_workspace_floats(int B, int T, int H, int dk, int dv, int C);
 
 // Device fault word of the tensor-core kernels (bounded waits that gave up).
 // read_and_clear_fault synchronises the stream first.

@@ -35,6 +35,12 @@ SIGNATURES = {
                              _I, _I, _I, _I, _I, _VP]),
     "kla_decode_step_ex": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
                                 _I, _I, _I, _I, _I, _I, _VP]),
+    "kla_chunk_bwd_workspace_size": (_I, [_I, _I, _I, _I, _I, _I,
+                                         ctypes.POINTER(ctypes.c_size_t)]),
+    "kla_chunk_bwd": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP, _FP,
+                           _VP, _VP, _VP, _FP, _FP, _FP,
+                           _I, _I, _I, _I, _I, _I, _I, _I,
+                           _VP, ctypes.c_size_t, _VP]),
     "kla_device_status": (_I, [_VP]),
     "kla_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -147,6 +153,62 @@ def decode_step(q, k, v, log_alpha, eta, S, eps: float = 1e-6, o=None,
     if st != KLA_OK:
         raise KlaError("kla_decode_step_ex", st)
     return o
+
+
+def chunk_bwd_workspace_size(B: int, T: int, H: int, dk: int, dv: int,
+                             C: int = 64) -> int:
+    """Bytes of workspace ``chunk_bwd`` needs (``kla_chunk_bwd_workspace_size``)."""
+    n = ctypes.c_size_t(0)
+    st = load_library().kla_chunk_bwd_workspace_size(B, T, H, dk, dv, int(C),
+                                                     ctypes.byref(n))
+    if st != KLA_OK:
+        raise KlaError("kla_chunk_bwd_workspace_size", st)
+    return int(n.value)
+
+
+def chunk_bwd(q, k, v, log_alpha, eta, o_grad, hT_grad=None, eps=1e-6,
+              h0=None, C: int = 64, rule: str = "kaczmarz", workspace=None,
+              want_h0_grad: bool = True, stream=None):
+    """Backward pass (``kla_chunk_bwd``): gradients of a loss with respect to
+    every input of ``chunk_fwd``, given dL/do (``o_grad``, like o) and dL/dhT
+    (``hT_grad``, fp32 [B,H,dk,dv] or None).  Returns a dict with q_grad,
+    k_grad, v_grad (input dtype), log_alpha_grad, eta_grad and h0_grad (fp32;
+    None unless ``want_h0_grad``).  ``workspace`` may be passed preallocated
+    (uint8 CUDA tensor of at least ``chunk_bwd_workspace_size`` bytes).
+    """
+    for n, t in (("q", q), ("k", k), ("v", v), ("o_grad", o_grad)):
+        _check_cuda(n, t, q.dtype)
+    _check_cuda("log_alpha", log_alpha, torch.float32)
+    _check_cuda("eta", eta, torch.float32)
+    for n, t in (("h0", h0), ("hT_grad", hT_grad)):
+        if t is not None:
+            _check_cuda(n, t, torch.float32)
+    if q.dtype not in DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    nbytes = chunk_bwd_workspace_size(B, T, H, dk, dv, C)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8,
+                                device=q.device)
+    _check_cuda("workspace", workspace)
+    out = dict(q_grad=torch.empty_like(q), k_grad=torch.empty_like(k),
+               v_grad=torch.empty_like(v),
+               log_alpha_grad=torch.empty_like(log_alpha),
+               eta_grad=torch.empty_like(eta),
+               h0_grad=(torch.empty((B, H, dk, dv), dtype=torch.float32,
+                                    device=q.device)
+                        if want_h0_grad else None))
+    st = load_library().kla_chunk_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(eta), float(eps),
+        _ptr(h0), _ptr(o_grad), _ptr(hT_grad), _ptr(out["q_grad"]),
+        _ptr(out["k_grad"]), _ptr(out["v_grad"]), _ptr(out["log_alpha_grad"]),
+        _ptr(out["eta_grad"]), _ptr(out["h0_grad"]), B, T, H, dk, dv, int(C),
+        DTYPES[q.dtype], RULES[rule], _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != KLA_OK:
+        raise KlaError("kla_chunk_bwd", st)
+    return out
 
 
 def device_status(stream=None) -> int:

@@ -30,7 +30,8 @@ def lib():
 def test_header_declares_expected_entry_points():
     syms = declared_symbols()
     for name in ("kla_chunk_fwd", "kla_chunk_fwd_ex", "kla_decode_step",
-                 "kla_decode_step_ex", "kla_device_status",
+                 "kla_decode_step_ex", "kla_chunk_bwd",
+                 "kla_chunk_bwd_workspace_size", "kla_device_status",
                  "kla_status_string"):
         assert name in syms
 
@@ -128,3 +129,46 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises(TypeError):
         kla.decode_step(x[0], x[0], x[0], la[0], la[0],
                         torch.zeros(4, 1, 16, 16))
+
+
+def bwd(lib, *, ws_bytes=1 << 20, ws=ctypes.c_void_p(0x9000), B=1, T=8, H=1,
+        dk=16, dv=16, C=16, dtype=1, rule=0, eps=1e-6, **ptrs):
+    names = ["q", "k", "v", "la", "eta", "h0", "g_o", "g_hT", "g_q", "g_k",
+             "g_v", "g_la", "g_eta", "g_h0"]
+    defaults = {n: ctypes.c_void_p(0x10000 * (i + 1)) for i, n in
+                enumerate(names)}
+    defaults["h0"] = defaults["g_hT"] = defaults["g_h0"] = None
+    defaults.update(ptrs)
+    p = [defaults[n] for n in names]
+    return lib.kla_chunk_bwd(p[0], p[1], p[2], p[3], p[4], eps, p[5], p[6],
+                             p[7], p[8], p[9], p[10], p[11], p[12], p[13],
+                             B, T, H, dk, dv, C, dtype, rule, ws, ws_bytes,
+                             None)
+
+
+def test_bwd_workspace_size(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.kla_chunk_bwd_workspace_size(2, 100, 3, 16, 32, 16,
+                                            ctypes.byref(n)) == OK
+    assert n.value == 2 * 4 * 2 * 3 * 7 * 16 * 32    # ceil(100/16) = 7
+    assert lib.kla_chunk_bwd_workspace_size(2, 100, 3, 16, 32, 0,
+                                            ctypes.byref(n)) == INVALID
+    assert lib.kla_chunk_bwd_workspace_size(2, 100, 3, 16, 32, 16,
+                                            None) == INVALID
+
+
+def test_bwd_rejects_bad_arguments_on_host(lib):
+    assert bwd(lib, q=None) == INVALID
+    assert bwd(lib, g_o=None) == INVALID
+    assert bwd(lib, g_q=None) == INVALID
+    assert bwd(lib, ws=None) == INVALID
+    assert bwd(lib, ws_bytes=16) == INVALID                   # too small
+    assert bwd(lib, ws=ctypes.c_void_p(0x9008)) == INVALID    # misaligned
+    assert bwd(lib, rule=5) == INVALID
+    assert bwd(lib, dtype=3) == INVALID
+    assert bwd(lib, eps=-1.0) == INVALID
+    assert bwd(lib, g_q=ctypes.c_void_p(0x10000)) == INVALID  # aliases q
+    assert bwd(lib, g_k=ctypes.c_void_p(0x90000)) == INVALID  # aliases g_q
+    assert bwd(lib, dk=24) == UNSUPPORTED
+    assert bwd(lib, C=48) == UNSUPPORTED
+    assert bwd(lib, B=0, q=None, k=None) == OK                 # empty: no-op

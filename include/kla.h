@@ -201,6 +201,35 @@ KLA_API kla_status kla_chunk_bwd(const void* q, const void* k, const void* v,
                                  size_t workspace_bytes, kla_stream_t stream);
 
 /*
+ * kla_chunk_bwd_noalloc -- kla_chunk_bwd for callers that cannot allocate
+ * device memory: a plain C program or plug-in that links only this library
+ * and owns no device allocator, a hook running inside a framework's own
+ * allocator (which must not be re-entered), or a process whose device-memory
+ * budget is fixed in advance.  The paper has no counterpart; it is an
+ * addition of this library.
+ *
+ * Arguments and results are those of kla_chunk_bwd without the workspace:
+ * its scratch is a fixed 32 MiB array inside the library (every GPU that
+ * loads the library holds it until the process exits).  A problem whose
+ * kla_chunk_bwd_workspace_size exceeds 32 MiB is rejected with
+ * KLA_ERR_UNSUPPORTED_SHAPE before anything is launched.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current; a failure returns KLA_ERR_CUDA); make that first call
+ * before any stream capture.  Every call shares the one array and leaves its
+ * contents behind; nothing in it has to start at zero.  Calls that overlap
+ * on the GPU (on different streams, or from different host threads, on the
+ * same device) race on the array: serialise them.
+ */
+KLA_API kla_status kla_chunk_bwd_noalloc(
+    const void* q, const void* k, const void* v, const float* log_alpha,
+    const float* eta, float eps, const float* h0, const void* o_grad,
+    const float* hT_grad, void* q_grad, void* k_grad, void* v_grad,
+    float* log_alpha_grad, float* eta_grad, float* h0_grad, int B, int T,
+    int H, int dk, int dv, int C, kla_dtype dtype, kla_step_rule rule,
+    kla_stream_t stream);
+
+/*
  * kla_device_status -- synchronises `stream`, then reads and clears the
  * library's device-side fault word.  Returns KLA_ERR_TIMEOUT if a bounded
  * wait inside a kernel gave up since the last call (the kernel then skipped

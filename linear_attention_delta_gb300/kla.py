@@ -41,6 +41,9 @@ SIGNATURES = {
                            _VP, _VP, _VP, _FP, _FP, _FP,
                            _I, _I, _I, _I, _I, _I, _I, _I,
                            _VP, ctypes.c_size_t, _VP]),
+    "kla_chunk_bwd_noalloc": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
+                                   _FP, _VP, _VP, _VP, _FP, _FP, _FP,
+                                   _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
     "kla_device_status": (_I, [_VP]),
     "kla_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -208,6 +211,43 @@ def chunk_bwd(q, k, v, log_alpha, eta, o_grad, hT_grad=None, eps=1e-6,
         workspace.numel() * workspace.element_size(), _stream(stream))
     if st != KLA_OK:
         raise KlaError("kla_chunk_bwd", st)
+    return out
+
+
+def chunk_bwd_noalloc(q, k, v, log_alpha, eta, o_grad, hT_grad=None,
+                      eps=1e-6, h0=None, C: int = 64, rule: str = "kaczmarz",
+                      want_h0_grad: bool = True, stream=None):
+    """``kla_chunk_bwd_noalloc``: as ``chunk_bwd``, with the library's fixed
+    32 MiB device array as scratch instead of a workspace (for callers that
+    cannot allocate device memory; larger problems raise).  The gradient
+    tensors are still allocated here, by torch; a C caller passes its own.
+    """
+    for n, t in (("q", q), ("k", k), ("v", v), ("o_grad", o_grad)):
+        _check_cuda(n, t, q.dtype)
+    _check_cuda("log_alpha", log_alpha, torch.float32)
+    _check_cuda("eta", eta, torch.float32)
+    for n, t in (("h0", h0), ("hT_grad", hT_grad)):
+        if t is not None:
+            _check_cuda(n, t, torch.float32)
+    if q.dtype not in DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    out = dict(q_grad=torch.empty_like(q), k_grad=torch.empty_like(k),
+               v_grad=torch.empty_like(v),
+               log_alpha_grad=torch.empty_like(log_alpha),
+               eta_grad=torch.empty_like(eta),
+               h0_grad=(torch.empty((B, H, dk, dv), dtype=torch.float32,
+                                    device=q.device)
+                        if want_h0_grad else None))
+    st = load_library().kla_chunk_bwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(eta), float(eps),
+        _ptr(h0), _ptr(o_grad), _ptr(hT_grad), _ptr(out["q_grad"]),
+        _ptr(out["k_grad"]), _ptr(out["v_grad"]), _ptr(out["log_alpha_grad"]),
+        _ptr(out["eta_grad"]), _ptr(out["h0_grad"]), B, T, H, dk, dv, int(C),
+        DTYPES[q.dtype], RULES[rule], _stream(stream))
+    if st != KLA_OK:
+        raise KlaError("kla_chunk_bwd_noalloc", st)
     return out
 
 

@@ -73,6 +73,22 @@ def prefill_flops(w) -> int:
     return w.B * w.T * w.H * per
 
 
+def backward_flops(w) -> int:
+    """Algorithmic FLOPs of one backward pass, counted as three forward
+    passes: the forward recompute that gives the chunk-start states, plus the
+    reverse mode, in which every forward contraction C = A B yields two
+    (dA = dC B^T, dB = A^T dC)."""
+    return 3 * prefill_flops(w)
+
+
+def fp32_alu_peak_tflops(sm_max_mhz=None) -> tuple:
+    """Peak fp32 FMA rate of the CUDA cores: SMs x 128 FP32 lanes x 2 FLOPs
+    x the maximum SM clock (NVML's, else 2070 MHz)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    mhz = float(sm_max_mhz) if sm_max_mhz else 2070.0
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, sms, mhz
+
+
 def decode_bytes(w) -> int:
     heads = w.B * w.H
     esz = 2 if w.dtype == "bf16" else 4
@@ -363,6 +379,47 @@ def bench_decode(w, steps, warmup, distinct=50):
     return ms / steps
 
 
+def bench_backward(w, inp, steps, warmup, world):
+    """kla_chunk_bwd on the forward's inputs with seeded upstream
+    gradients; the workspace is allocated once, outside the timed region;
+    L2 is flushed between timed steps."""
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
+           for k, v in inp.items()}
+    rng = np.random.default_rng(gen.SEEDS[w.name] + 200)
+    do = torch.from_numpy(rng.standard_normal(tuple(dev["v"].shape)).astype(
+        np.float32)).to(dev["v"].dtype).cuda()
+    dhT = torch.from_numpy(rng.standard_normal(
+        (w.B, w.H, w.dk, w.dv)).astype(np.float32)).cuda()
+    nbytes = kla.chunk_bwd_workspace_size(w.B, w.T, w.H, w.dk, w.dv, w.C)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kla.chunk_bwd(dev["q"], dev["k"], dev["v"], dev["log_alpha"],
+                      dev["eta"], do, dhT, eps=dev["eps"], h0=dev["h0"],
+                      C=w.C, workspace=ws)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev])),
+                        world)
+    return ms, nbytes
+
+
 def bench_long_context(world, gpu_index, hbm):
     """The pages' own efficiency points at layer scale: the 131072-token
     prefill (KLA and the learned-step rule on the same kernels), and decode
@@ -521,6 +578,26 @@ def run_ours(args):
                 "tokens_per_s": round(world * tokens / (gdn["ms"] * 1e-3), 1),
                 "kla_over_gdn_time": round(ms / gdn["ms"], 4)}
 
+    backward = None
+    if not args.no_backward:
+        bms, ws_bytes = bench_backward(w, pf["inputs"], 3, 3, world)
+        alu_peak, sms, mhz = fp32_alu_peak_tflops(
+            (pf["clocks"] or {}).get("sm_max_mhz"))
+        bflops = backward_flops(w)
+        ach = bflops / (bms * 1e-3) / 1e12
+        backward = {"workload": w.name, "ms": round(bms, 4),
+                    "tokens_per_s": round(world * tokens / (bms * 1e-3), 1),
+                    "kernels": "kla_chunk_bwd: CUDA-core fp32, 3 launches",
+                    "workspace_bytes": ws_bytes,
+                    "roofline": {"bound": "alu", "achieved": round(ach, 2),
+                                 "peak": round(alu_peak, 1),
+                                 "unit": "TFLOP/s",
+                                 "frac": round(ach / alu_peak, 4),
+                                 "flops_per_launch": bflops,
+                                 "peak_source": f"{sms} SMs x 128 FP32 lanes"
+                                                f" x 2 x {mhz:.0f} MHz"},
+                    "timed_steps": 3}
+
     longctx = None
     if not args.no_long:
         longctx = bench_long_context(world, local, hbm)
@@ -541,7 +618,7 @@ def run_ours(args):
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": pf["launches"], "clocks": pf["clocks"],
             "decode": decode, "gdn_mode": gdn_line,
-            "long_context": longctx,
+            "long_context": longctx, "backward": backward,
             "per_step_ms": [round(x, 5) for x in pf["per_step_ms"]]}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -601,6 +678,7 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-long", action="store_true",
                     help="skip the 131K-prefill / 32K-decode points")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,

@@ -25,8 +25,8 @@
 // DeltaNet block solver with B = Diag(beta); gist.science/es/paper/2605.08587,
 // section "Implementacion").
 //
-// Three launches: the CUDA-core forward writes the state at every chunk start
-// (ckpt); kla_bwd_state_kernel walks the chunks in reverse (one CTA per
+// Three launches: a forward pass writes the state at every chunk start
+// (ckpt; the tensor-core kernel where it applies, else the CUDA-core one); kla_bwd_state_kernel walks the chunks in reverse (one CTA per
 // (batch, head, dv tile): the recurrence for dS is column-separable) and
 // writes dS' of every chunk (dsck) and dh0; kla_bwd_grad_kernel then forms
 // every gradient of one chunk's tokens per CTA, all chunks in parallel.
@@ -128,6 +128,60 @@ __device__ __forceinline__ void build_a_p(int C, const float* Qs,
     }
 }
 
+// Tm = A^{-1} for the unit lower-triangular C x C matrix A (C = 16, 32 or
+// 64; row stride ldc), in 16 x 16 tiles: the diagonal tiles by column
+// substitution (one thread per column), then the tiles below them by
+// distance, T_IJ = -T_II (sum_{m=J}^{I-1} A_Im T_mJ), with the sum parked in
+// the (otherwise unused) upper tile (J, I).  Only the lower triangle of Tm
+// is meaningful on return.  Ends with a barrier.
+__device__ __forceinline__ void invert_unit_lower(const float* A, float* Tm,
+                                                  int C, int ldc) {
+    const int tid = threadIdx.x, nb = C / 16;
+    if (tid < nb * 16) {
+        const int bb = tid / 16, cl = tid % 16;
+        const float* Ab = A + (16 * bb) * ldc + 16 * bb;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = (r == cl) ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < 16; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < r; ++i) acc = fmaf(Ab[r * ldc + i], x[i], acc);
+            if (r > cl) x[r] = -acc;
+        }
+        float* Tb = Tm + (16 * bb) * ldc + 16 * bb + cl;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Tb[r * ldc] = x[r];
+    }
+    __syncthreads();
+    for (int d = 1; d < nb; ++d) {
+        for (int idx = tid; idx < (nb - d) * 256; idx += kBwdThreads) {
+            const int J = idx / 256, I = J + d, r = (idx % 256) / 16,
+                      c = idx % 16;
+            float acc = 0.f;
+            for (int m = J; m < I; ++m)
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    acc = fmaf(A[(16 * I + r) * ldc + 16 * m + k],
+                               Tm[(16 * m + k) * ldc + 16 * J + c], acc);
+            Tm[(16 * J + r) * ldc + 16 * I + c] = acc;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < (nb - d) * 256; idx += kBwdThreads) {
+            const int J = idx / 256, I = J + d, r = (idx % 256) / 16,
+                      c = idx % 16;
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                acc = fmaf(Tm[(16 * I + r) * ldc + 16 * I + k],
+                           Tm[(16 * J + k) * ldc + 16 * I + c], acc);
+            Tm[(16 * I + r) * ldc + 16 * J + c] = -acc;
+        }
+        __syncthreads();
+    }
+}
+
 template <typename IO>
 __device__ __forceinline__ float ld_io(const void* p, size_t off) {
     return to_f32(static_cast<const IO*>(p)[off]);
@@ -150,7 +204,9 @@ struct StateSmem {
     static constexpr int BETA = G + kBwdMaxC;
     static constexpr int GAM = BETA + kBwdMaxC;
     static constexpr int LAM = GAM + kBwdMaxC;
-    static constexpr int TOTAL = LAM + kBwdMaxC;
+    static constexpr int TM = LAM + kBwdMaxC;           // A^{-1}
+    static constexpr int W2 = TM + kBwdMaxC * LDC;      // dF
+    static constexpr int TOTAL = W2 + kBwdMaxC * LDV;
     static constexpr size_t BYTES = sizeof(float) * (size_t)TOTAL;
 };
 
@@ -170,6 +226,8 @@ kla_bwd_state_kernel(BwdArgs a) {
     float* bs = sm + L::BETA;
     float* gam = sm + L::GAM;
     float* lam = sm + L::LAM;
+    float* Tm = sm + L::TM;
+    float* W2 = sm + L::W2;
 
     const int bh = blockIdx.x;
     const int b = bh / a.H, h = bh % a.H;
@@ -206,6 +264,7 @@ kla_bwd_state_kernel(BwdArgs a) {
             }
         }
         __syncthreads();
+        invert_unit_lower(As, Tm, C, L::LDC);
 
         // dU~ = P^T dO + Diag(lambda) K dS'
         for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
@@ -221,14 +280,13 @@ kla_bwd_state_kernel(BwdArgs a) {
         }
         __syncthreads();
 
-        // dF = A^{-T} dU~: back substitution, one thread per column
-        if (tid < DVT) {
-            for (int r = C - 1; r >= 0; --r) {
-                float x = Ws[r * L::LDV + tid];
-                for (int i = r + 1; i < C; ++i)
-                    x = fmaf(-As[i * L::LDC + r], Ws[i * L::LDV + tid], x);
-                Ws[r * L::LDV + tid] = x;
-            }
+        // dF = T^T dU~
+        for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
+            const int r = idx / DVT, j = idx % DVT;
+            float x = 0.f;
+            for (int i = r; i < C; ++i)
+                x = fmaf(Tm[i * L::LDC + r], Ws[i * L::LDV + j], x);
+            W2[r * L::LDV + j] = x;
         }
         __syncthreads();
 
@@ -240,7 +298,7 @@ kla_bwd_state_kernel(BwdArgs a) {
             for (int r = 0; r < C; ++r)
                 acc = fmaf(gam[r],
                            Qs[r * L::LDK + c] * Ds[r * L::LDV + j] -
-                               Ks[r * L::LDK + c] * bs[r] * Ws[r * L::LDV + j],
+                               Ks[r * L::LDK + c] * bs[r] * W2[r * L::LDV + j],
                            acc);
             dS[c * L::LDV + j] = acc;
         }
@@ -284,7 +342,8 @@ struct GradSmem {
     static constexpr int DLAM = DGAM + kBwdMaxC;
     static constexpr int DG = DLAM + kBwdMaxC;
     static constexpr int DGC = DG + kBwdMaxC;          // <dS', S>
-    static constexpr int TOTAL = DGC + 4;
+    static constexpr int TM = DGC + 4;                 // A^{-1}
+    static constexpr int TOTAL = TM + kBwdMaxC * LDC;
     static constexpr size_t BYTES = sizeof(float) * (size_t)TOTAL;
 };
 
@@ -317,6 +376,7 @@ kla_bwd_grad_kernel(BwdArgs a) {
     float* dlam = sm + L::DLAM;
     float* dg = sm + L::DG;
     float* dgc = sm + L::DGC;
+    float* Tm = sm + L::TM;
 
     const int C = a.C, T = a.T, H = a.H, dv = a.dv;
     const int nch = (T + C - 1) / C;
@@ -343,6 +403,7 @@ kla_bwd_grad_kernel(BwdArgs a) {
     chunk_gates<DK>(a, Ks, L::LDK, gs, bs, gam, lam, nrm);
     build_a_p<DK>(C, Qs, Ks, L::LDK, gs, bs, As, Ps, L::LDC);
     __syncthreads();
+    invert_unit_lower(As, Tm, C, L::LDC);
 
     float dq_acc[kAcc], dk_acc[kAcc];
 #pragma unroll
@@ -381,19 +442,18 @@ kla_bwd_grad_kernel(BwdArgs a) {
             KS[r * L::LDV + j] = ks;
             const float x = fmaf(-gam[r], ks, Xs[r * L::LDV + j]);
             Xs[r * L::LDV + j] = x;
-            Us[r * L::LDV + j] = bs[r] * x;
+            Ws[r * L::LDV + j] = bs[r] * x;                 // F
             atomicAdd(&dgam[r], Ds[r * L::LDV + j] * qs);
         }
         __syncthreads();
 
-        // U~ = A^{-1} F: forward substitution, one thread per column
-        if (tid < DVT) {
-            for (int r = 0; r < C; ++r) {
-                float x = Us[r * L::LDV + tid];
-                for (int i = 0; i < r; ++i)
-                    x = fmaf(-As[r * L::LDC + i], Us[i * L::LDV + tid], x);
-                Us[r * L::LDV + tid] = x;
-            }
+        // U~ = T F
+        for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
+            const int r = idx / DVT, j = idx % DVT;
+            float x = 0.f;
+            for (int i = 0; i <= r; ++i)
+                x = fmaf(Tm[r * L::LDC + i], Ws[i * L::LDV + j], x);
+            Us[r * L::LDV + j] = x;
         }
         __syncthreads();
 
@@ -412,29 +472,23 @@ kla_bwd_grad_kernel(BwdArgs a) {
         }
         __syncthreads();
 
-        // dF = A^{-T} dU~: back substitution, one thread per column
-        if (tid < DVT) {
-            for (int r = C - 1; r >= 0; --r) {
-                float x = Ws[r * L::LDV + tid];
-                for (int i = r + 1; i < C; ++i)
-                    x = fmaf(-As[i * L::LDC + r], Ws[i * L::LDV + tid], x);
-                Ws[r * L::LDV + tid] = x;
-            }
-        }
-        __syncthreads();
-
-        // dV = dX = Diag(beta) dF; dbeta from F = Diag(beta) X; dgamma from X
+        // dF = T^T dU~ (into the K S slots, once used); dV = dX =
+        // Diag(beta) dF; dbeta from F = Diag(beta) X; dgamma from X
         for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
             const int r = idx / DVT, j = idx % DVT;
             const int t = t0 + r;
-            const float df = Ws[r * L::LDV + j];
+            float df = 0.f;
+            for (int i = r; i < C; ++i)
+                df = fmaf(Tm[i * L::LDC + r], Ws[i * L::LDV + j], df);
             const float dx = bs[r] * df;
             if (t < T)
                 static_cast<IO*>(a.dv_)[(((size_t)b * T + t) * H + h) * dv +
                                         j0 + j] = from_f32<IO>(dx);
             atomicAdd(&db[r], df * Xs[r * L::LDV + j]);
             atomicAdd(&dgam[r], -dx * KS[r * L::LDV + j]);
+            KS[r * L::LDV + j] = df;
         }
+        __syncthreads();
         // dP = dO U~^T (i <= r), dA = -dF U~^T (i < r)
         for (int idx = tid; idx < C * C; idx += kBwdThreads) {
             const int r = idx / C, i = idx % C;
@@ -444,7 +498,7 @@ kla_bwd_grad_kernel(BwdArgs a) {
             for (int j = 0; j < DVT; ++j) {
                 const float ui = Us[i * L::LDV + j];
                 sp = fmaf(Ds[r * L::LDV + j], ui, sp);
-                sa = fmaf(Ws[r * L::LDV + j], ui, sa);
+                sa = fmaf(KS[r * L::LDV + j], ui, sa);
             }
             dP[r * L::LDC + i] += sp;
             if (i < r) dA[r * L::LDC + i] -= sa;
@@ -461,7 +515,7 @@ kla_bwd_grad_kernel(BwdArgs a) {
             for (int j = 0; j < DVT; ++j) {
                 const float sv = St[c * L::LDV + j];
                 sdo = fmaf(Ds[r * L::LDV + j], sv, sdo);
-                sf = fmaf(Ws[r * L::LDV + j], sv, sf);
+                sf = fmaf(KS[r * L::LDV + j], sv, sf);
                 su = fmaf(Us[r * L::LDV + j], dSt[c * L::LDV + j], su);
             }
             dq_acc[m] = fmaf(gam[r], sdo, dq_acc[m]);
@@ -607,11 +661,13 @@ size_t chunk_bwd_workspace_floats(int B, int T, int H, int dk, int dv,
 cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t stream) {
     if ((long)a.B * a.H == 0 || a.T == 0) return cudaSuccess;
     if (a.C > kBwdMaxC) return cudaErrorInvalidValue;
-    // 1. states at every chunk start (CUDA-core forward, o not written)
+    // 1. states at every chunk start (a forward pass, o not written; the
+    // tensor-core kernel where it applies)
     FwdArgs f{a.q, a.k, a.v, a.log_alpha, a.eta, a.eps, a.gdn, a.h0,
               nullptr, nullptr, a.B, a.T, a.H, a.dk, a.dv, a.C, a.dtype};
     f.ckpt = a.ckpt;
-    cudaError_t e = launch_chunk_simt(f, stream);
+    cudaError_t e = chunk_tc_eligible(f) ? launch_chunk_tc(f, stream)
+                                         : launch_chunk_simt(f, stream);
     if (e != cudaSuccess) return e;
     // 2 and 3. dS' per chunk and dh0, then the gradients
     if (a.dtype == KLA_BF16) return launch_dtype<__nv_bfloat16>(a, stream);

@@ -141,8 +141,9 @@ struct TcParams {
     const float* log_alpha;
     const float* eta;
     const float* h0;
-    __nv_bfloat16* o;
+    __nv_bfloat16* o;      // may be null (only the states are wanted)
     float* hT;
+    float* ckpt;           // may be null: the state at every chunk start
     float eps;
     int gdn;
     int T, H;
@@ -800,13 +801,14 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             const float gam = gbuf[(cc & 3) * kGBufStride + 3 * kC + r];
             const int t = cc * kC + r;
             __nv_bfloat16* dst = p.o + (((size_t)b * T + t) * p.H + h) * kD + j0;
+            const bool store = t < T && p.o != nullptr;
 #pragma unroll 1
             for (int jj = 0; jj < 4; ++jj) {   // 16 columns a step
                 float qs[16], x[16];
                 tc::tmem_ld16(tlane + col_ks(cc) + 16 * jj, qs);
                 tc::tmem_ld16(tlane + kColOI + 16 * jj, x);
                 tc::tmem_ld_wait();
-                if (t >= T) continue;
+                if (!store) continue;
 #pragma unroll
                 for (int j = 0; j < 16; j += 8) {
                     uint4 v;
@@ -827,6 +829,14 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             const uint32_t sst = sbase + s * kStage;
             const float* gb = gbuf + (c & 3) * kGBufStride;
             const uint32_t tu = sbase + kTU + (c & 1) * kTUStride;
+            if (p.ckpt) {   // the state chunk c starts from (fp32)
+                float* dst = p.ckpt + (((size_t)bh * nchunks + c) * kD + row) *
+                                          kD + j0;
+#pragma unroll
+                for (int j = 0; j < kNV; j += 4)
+                    *reinterpret_cast<float4*>(dst + j) =
+                        make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+            }
             bool ok = true;
             if (sw < 2)   // the stage of chunk c (warps 6, 7 do not read it)
                 ok = team_wait(&bars[kBarTma + s], (c / kNS) & 1, abort_flag,
@@ -1062,7 +1072,8 @@ cudaError_t launch_chunk_tc(const FwdArgs& a, cudaStream_t stream) {
         attr_set = true;
     }
     TcParams p{a.log_alpha, a.eta, a.h0,
-               static_cast<__nv_bfloat16*>(a.o), a.hT, a.eps, a.gdn, a.T, a.H};
+               static_cast<__nv_bfloat16*>(a.o), a.hT, a.ckpt, a.eps, a.gdn,
+               a.T, a.H};
     dim3 grid((unsigned)((long)a.B * a.H), kD / kNV);
     kla_chunk_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
     return cudaGetLastError();

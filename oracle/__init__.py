@@ -68,6 +68,13 @@ def _load():
                                        ctypes.c_long, ctypes.c_long,
                                        ctypes.c_long, ctypes.c_int]
         lib.oracle_kla_bwd.restype = ctypes.c_int
+        lib.oracle_pkla_fwd.argtypes = [dp, dp, dp, dp, dp, ctypes.c_double,
+                                        ctypes.c_int, ctypes.c_double,
+                                        ctypes.c_double, dp, dp, dp, dp, dp,
+                                        ctypes.c_long, ctypes.c_long,
+                                        ctypes.c_long, ctypes.c_long,
+                                        ctypes.c_long, ctypes.c_int]
+        lib.oracle_pkla_fwd.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -169,6 +176,29 @@ def kla_bwd(q, k, v, log_alpha, eta, eps, h0, dout, dhT=None,
     if rc != 0:
         raise RuntimeError(f"oracle_kla_bwd failed ({rc})")
     return out
+
+
+def pkla_fwd(q, k, v, log_alpha, eta, eps, h0=None, A0=None, x=1.5,
+             delta=1e-6, given=False, n_threads: int = 0):
+    """The diagonal-preconditioned recurrence (write key P_t k_t, P_t from
+    the running key second moments squashed into [1/x, x]), fp64 (C).
+    Returns (o, hT, A_T, kw) with kw the write keys [B,T,H,dk]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    la, et = _f64(log_alpha), _f64(eta)
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    o = np.zeros((B, T, H, dv))
+    hT = np.zeros((B, H, dk, dv))
+    kw = np.zeros((B, T, H, dk))
+    A = np.zeros((B, H, dk)) if A0 is None else _f64(A0).copy()
+    h0a = None if h0 is None else _f64(h0)
+    rc = _load().oracle_pkla_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(et), float(eps),
+        int(bool(given)), float(x), float(delta), _ptr(h0a), _ptr(A),
+        _ptr(o), _ptr(hT), _ptr(kw), B, T, H, dk, dv, int(n_threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_pkla_fwd failed ({rc})")
+    return o, hT, A, kw
 
 
 def kla_fwd_np(q, k, v, log_alpha, eta, eps, h0=None):

@@ -348,6 +348,116 @@ int oracle_kla_bwd(const double* q, const double* k, const double* v,
     return failed ? -2 : 0;
 }
 
+/* ------------------------------------------------------------ preconditioned
+ *
+ * The diagonal-preconditioned delta rule of the adjacent page (gist.science
+ * "preconditioned DeltaNet", section "Aproximacion Diagonal"): the running
+ * second moments of the keys, A_t = A_{t-1} + k_t (.) k_t (per key
+ * dimension), give the preconditioner P_t ~ Diag(A_t)^{-1}, squashed in log
+ * space into [1/x, x] (x ~ 1.5), and applied to the write key (ATK):
+ *
+ *   z_i     = mean_j log(A_t,j + delta) - log(A_t,i + delta)
+ *   P_t,i   = exp(log(x) tanh(z_i / log(x)))     (slope 1 at z = 0)
+ *   kw_t    = P_t (.) k_t                         write key
+ *   e_t     = v_t - S~^T k_t                      residual, read key k_t
+ *   S_t     = S~ + beta_t kw_t e_t^T,   o_t = S_t^T q_t
+ *   beta_t  = eta_t (given) or eta_t / (k_t . kw_t + eps) (Kaczmarz: at
+ *             eta = 1, eps = 0 the write makes S_t^T k_t = v_t exactly)
+ *
+ * The page names a squash "in log space" onto [1/x, x] without the function
+ * or a reference level; tanh with unit slope, centred on the mean log second
+ * moment over the key dimensions, and the floor delta inside the log are
+ * this library's reading.  A [B, H, dk] carries A_t (in/out, may be NULL on
+ * input: zero).  Returns 0, -1 or -2 as the functions above.
+ */
+static void precond_key(double* A, const double* k, double* kw, long dk,
+                        double x, double delta)
+{
+    double mean = 0.0;
+    for (long i = 0; i < dk; ++i) {
+        A[i] += k[i] * k[i];
+        mean += log(A[i] + delta);
+    }
+    mean /= (double)dk;
+    const double lx = log(x);
+    for (long i = 0; i < dk; ++i) {
+        const double z = mean - log(A[i] + delta);
+        kw[i] = exp(lx * tanh(z / lx)) * k[i];
+    }
+}
+
+static void pkla_token(double* S, const double* q, const double* k,
+                       const double* kw, const double* v, double log_alpha,
+                       double eta, double eps, int given, double* o, long dk,
+                       long dv, double* e)
+{
+    const double alpha = exp(log_alpha);
+    double kkw = 0.0;
+    for (long i = 0; i < dk; ++i) kkw += k[i] * kw[i];
+    const double denom = kkw + eps;
+    const double beta = given ? eta : (denom == 0.0 ? 0.0 : eta / denom);
+    for (long i = 0; i < dk * dv; ++i) S[i] *= alpha;
+    for (long j = 0; j < dv; ++j) e[j] = v[j];
+    for (long i = 0; i < dk; ++i)
+        for (long j = 0; j < dv; ++j) e[j] -= S[i * dv + j] * k[i];
+    for (long i = 0; i < dk; ++i)
+        for (long j = 0; j < dv; ++j) S[i * dv + j] += beta * kw[i] * e[j];
+    if (o) {
+        for (long j = 0; j < dv; ++j) o[j] = 0.0;
+        for (long i = 0; i < dk; ++i)
+            for (long j = 0; j < dv; ++j) o[j] += S[i * dv + j] * q[i];
+    }
+}
+
+/* Forward pass over T tokens.  kw_out [B,T,H,dk] (may be NULL) receives the
+ * write keys; A [B,H,dk] (may be NULL) holds A_0 on entry (NULL: zero) and
+ * A_T on return. */
+int oracle_pkla_fwd(const double* q, const double* k, const double* v,
+                    const double* log_alpha, const double* eta, double eps,
+                    int given, double x, double delta, const double* h0,
+                    double* A, double* o, double* hT, double* kw_out,
+                    long B, long T, long H, long dk, long dv, int n_threads)
+{
+    if (!q || !k || !v || !log_alpha || !eta || !o) return -1;
+    if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || !(x > 1.0))
+        return -1;
+    int failed = 0;
+    const long pairs = B * H;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+#endif
+    for (long p = 0; p < pairs; ++p) {
+        const long b = p / H, h = p % H;
+        double* S = (double*)malloc(sizeof(double) * (size_t)(dk * dv));
+        double* e = (double*)malloc(sizeof(double) * (size_t)dv);
+        double* Ad = (double*)malloc(sizeof(double) * (size_t)dk);
+        double* kw = (double*)malloc(sizeof(double) * (size_t)dk);
+        if (!S || !e || !Ad || !kw) {
+            free(S); free(e); free(Ad); free(kw);
+            failed |= 1;
+            continue;
+        }
+        if (h0) memcpy(S, h0 + p * dk * dv, sizeof(double) * (size_t)(dk * dv));
+        else memset(S, 0, sizeof(double) * (size_t)(dk * dv));
+        if (A) memcpy(Ad, A + p * dk, sizeof(double) * (size_t)dk);
+        else memset(Ad, 0, sizeof(double) * (size_t)dk);
+        for (long t = 0; t < T; ++t) {
+            const long row = (b * T + t) * H + h;
+            precond_key(Ad, k + row * dk, kw, dk, x, delta);
+            if (kw_out) memcpy(kw_out + row * dk, kw, sizeof(double) * (size_t)dk);
+            pkla_token(S, q + row * dk, k + row * dk, kw, v + row * dv,
+                       log_alpha[row], eta[row], eps, given, o + row * dv,
+                       dk, dv, e);
+        }
+        if (hT) memcpy(hT + p * dk * dv, S, sizeof(double) * (size_t)(dk * dv));
+        if (A) memcpy(A + p * dk, Ad, sizeof(double) * (size_t)dk);
+        free(S); free(e); free(Ad); free(kw);
+    }
+    (void)n_threads;
+    return failed ? -2 : 0;
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int oracle_max_threads(void)
 {

@@ -549,3 +549,69 @@ def test_backward_closed_form_without_writes():
         assert _rel(g["deta"][:, t], de) < 1e-12
     assert _rel(g["dh0"], D) < 1e-13
     assert np.max(np.abs(g["dv"])) == 0.0 and np.max(np.abs(g["dk"])) == 0.0
+
+
+# ---------------------------------------------------------------- preconditioned
+
+def _pcase(seed, B=1, T=30, H=2, dk=6, dv=4):
+    rng = np.random.default_rng(seed)
+    q, k, v, la, et, eps, S0 = _rand(rng, B, T, H, dk, dv)
+    # anisotropic keys, so that the preconditioner is far from the identity
+    k = k * rng.uniform(0.2, 3.0, (1, 1, 1, dk))
+    return q, k, v, la, et, eps, S0, rng
+
+
+@pytest.mark.parametrize("given", [False, True])
+def test_precond_reduces_to_plain_rule_as_x_tends_to_one(given):
+    """x -> 1 squashes P_t onto the identity: write key = read key, and the
+    recurrence is the (pinned) plain one."""
+    q, k, v, la, et, eps, S0, _ = _pcase(70 + given)
+    o, hT, _, kw = oracle.pkla_fwd(q, k, v, la, et, eps, S0, x=1.0 + 1e-12,
+                                   given=given)
+    assert _rel(kw, k) < 1e-11
+    eta = et * (np.sum(k ** 2, -1) + eps) if given else et
+    o_ref, h_ref = oracle.kla_fwd(q, k, v, la, eta, eps, S0)
+    assert _rel(o, o_ref) < 1e-9 and _rel(hT, h_ref) < 1e-9
+
+
+def test_precond_kaczmarz_step_is_an_exact_projection():
+    """eta = 1, eps = 0: the preconditioned write still satisfies
+    S_t^T k_t = v_t after every token (an oblique projection): with q = k the
+    read-out returns v."""
+    q, k, v, la, _, _, S0, _ = _pcase(72)
+    o, _, _, _ = oracle.pkla_fwd(k, k, v, la, np.ones(la.shape), 0.0, S0)
+    assert _rel(o, v) < 1e-12
+
+
+def test_precond_gain_properties():
+    """P_t in [1/x, x]; a larger second moment gives a smaller gain; scaling
+    every key leaves P unchanged (the squash is centred on the mean log
+    second moment); equal second moments give P = 1."""
+    q, k, v, la, et, eps, S0, rng = _pcase(73, T=40, dk=8)
+    x = 1.5
+    _, _, A, kw = oracle.pkla_fwd(q, k, v, la, et, eps, S0, x=x, delta=0.0)
+    P = kw / k
+    assert P.min() >= 1 / x - 1e-12 and P.max() <= x + 1e-12
+    Acum = np.cumsum(k ** 2, axis=1)
+    order_A = np.argsort(Acum[0, -1, 0])
+    assert np.all(np.diff(P[0, -1, 0][order_A]) <= 1e-12)
+    _, _, _, kw2 = oracle.pkla_fwd(q, 3.0 * k, v, la, et, eps, S0, x=x,
+                                   delta=0.0)
+    assert _rel(kw2, 3.0 * kw) < 1e-12
+    kiso = np.ones_like(k) * rng.choice([-1.0, 1.0], k.shape)
+    _, _, _, kw3 = oracle.pkla_fwd(q, kiso, v, la, et, eps, S0, x=x,
+                                   delta=0.0)
+    assert _rel(kw3, kiso) < 1e-12
+
+
+def test_precond_segments_resume_with_second_moments():
+    """[0, T) equals [0, T1) then [T1, T) started from hT and A_T of the
+    first segment (A_t is part of the carried context)."""
+    q, k, v, la, et, eps, S0, _ = _pcase(74, T=25)
+    o, hT, A, _ = oracle.pkla_fwd(q, k, v, la, et, eps, S0)
+    o1, h1, A1, _ = oracle.pkla_fwd(q[:, :9], k[:, :9], v[:, :9], la[:, :9],
+                                    et[:, :9], eps, S0)
+    o2, h2, A2, _ = oracle.pkla_fwd(q[:, 9:], k[:, 9:], v[:, 9:], la[:, 9:],
+                                    et[:, 9:], eps, h1, A0=A1)
+    assert _rel(np.concatenate([o1, o2], 1), o) < 1e-13
+    assert _rel(h2, hT) < 1e-13 and _rel(A2, A) < 1e-14

@@ -150,6 +150,70 @@ KLA_API kla_status kla_decode_step_ex(const void* q, const void* k,
                               kla_step_rule rule, kla_stream_t stream);
 
 /*
+ * Diagonal-preconditioned variant (the adjacent preconditioned-DeltaNet page,
+ * section "Aproximacion Diagonal": P_t = Diag(A_t)^{-1} from the running key
+ * second moments A_t = A_{t-1} + k_t (.) k_t, squashed in log space onto
+ * [1/x, x], applied to the write key).  The recurrence becomes
+ *     e_t = v_t - S~^T k_t,   S_t = S~ + beta_t kw_t e_t^T,   o_t = S_t^T q_t
+ * with the write key kw_t = P_t (.) k_t, and with the Kaczmarz rule
+ * beta_t = eta_t / (k_t . kw_t + eps) (an oblique projection: S_t^T k_t = v_t
+ * at eta = 1, eps = 0); KLA_STEP_GIVEN keeps beta_t = eta_t (the page's
+ * preconditioned gated DeltaNet).  A prefill is kla_precond_keys followed by
+ * kla_chunk_fwd_kw; a decode step is kla_precond_keys with T = 1 followed by
+ * kla_decode_step_kw, A carried from one call to the next.
+ *
+ * kla_precond_keys -- write keys and second moments.  Per (b, h) and key
+ * dimension i:
+ *     A_t,i  = A_{t-1},i + k_t,i^2                      (A_0 = A0 or 0)
+ *     z_i    = mean_j log(A_t,j + delta) - log(A_t,i + delta)
+ *     kw_t,i = exp(log(x) tanh(z_i / log(x))) k_t,i
+ * The page fixes neither the squash nor its reference level; tanh with unit
+ * slope, centred on the mean log second moment (so that P is invariant to the
+ * scale of the keys), and the floor delta are this library's reading.
+ *
+ *   k        [B, T, H, dk]  dtype  (read)
+ *   A0       [B, H, dk]     fp32   (read) or NULL (zero)
+ *   k_write  [B, T, H, dk]  dtype  (written); must not alias k
+ *   AT       [B, H, dk]     fp32   (written: A_T) or NULL; may alias A0
+ *   x > 1 (the page uses about 1.5), delta >= 0
+ * Supported dk as for kla_chunk_fwd.  Errors: KLA_ERR_INVALID_ARG,
+ * KLA_ERR_UNSUPPORTED_SHAPE, KLA_ERR_CUDA.
+ */
+KLA_API kla_status kla_precond_keys(const void* k, const float* A0,
+                                    void* k_write, float* AT, int B, int T,
+                                    int H, int dk, float x, float delta,
+                                    kla_dtype dtype, kla_stream_t stream);
+
+/*
+ * kla_chunk_fwd_kw -- kla_chunk_fwd_ex with separate write keys k_write
+ * ([B, T, H, dk], dtype, read; e.g. from kla_precond_keys): the chunkwise
+ * form with A = I + strict_lower(Diag(beta)(Gamma o K Kw^T)),
+ * P = Gamma o Q Kw^T and the state written along Kw, the residual read along
+ * K.  Runs on the CUDA-core kernel.  k_write must not alias o.  Errors as
+ * for kla_chunk_fwd_ex (NULL k_write is KLA_ERR_INVALID_ARG).
+ */
+KLA_API kla_status kla_chunk_fwd_kw(const void* q, const void* k,
+                                    const void* k_write, const void* v,
+                                    const float* log_alpha, const float* eta,
+                                    float eps, const float* h0, void* o,
+                                    float* hT, int B, int T, int H, int dk,
+                                    int dv, int C, kla_dtype dtype,
+                                    kla_step_rule rule, kla_stream_t stream);
+
+/*
+ * kla_decode_step_kw -- kla_decode_step_ex with a separate write key
+ * k_write [N, H, dk] (dtype, read).  Errors as for kla_decode_step (NULL
+ * k_write is KLA_ERR_INVALID_ARG).
+ */
+KLA_API kla_status kla_decode_step_kw(const void* q, const void* k,
+                                      const void* k_write, const void* v,
+                                      const float* log_alpha,
+                                      const float* eta, float eps, float* S,
+                                      void* o, int N, int H, int dk, int dv,
+                                      kla_dtype dtype, kla_step_rule rule,
+                                      kla_stream_t stream);
+
+/*
  * kla_chunk_bwd_workspace_size -- bytes of device workspace kla_chunk_bwd
  * needs for these sizes: two fp32 tensors [B, H, ceil(T/C), dk, dv] (the
  * state at every chunk start and the gradient of the loss with respect to

@@ -21,14 +21,14 @@ kla_status from_cuda(cudaError_t e) {
 
 }  // namespace
 
-extern "C" kla_status kla_chunk_fwd_ex(const void* q, const void* k,
-                                       const void* v, const float* log_alpha,
-                                       const float* eta, float eps,
-                                       const float* h0, void* o, float* hT,
-                                       int B, int T, int H, int dk, int dv,
-                                       int C, kla_dtype dtype, kla_algo algo,
-                                       kla_step_rule rule,
-                                       kla_stream_t stream) {
+// Forward pass with optional separate write keys kw (null: the keys).
+static kla_status chunk_fwd_impl(const void* q, const void* k, const void* kw,
+                                 const void* v, const float* log_alpha,
+                                 const float* eta, float eps, const float* h0,
+                                 void* o, float* hT, int B, int T, int H,
+                                 int dk, int dv, int C, kla_dtype dtype,
+                                 kla_algo algo, kla_step_rule rule,
+                                 kla_stream_t stream) {
     if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || C <= 0)
         return KLA_ERR_INVALID_ARG;
     if (dtype != KLA_F32 && dtype != KLA_BF16) return KLA_ERR_INVALID_ARG;
@@ -47,10 +47,12 @@ extern "C" kla_status kla_chunk_fwd_ex(const void* q, const void* k,
         if (!q || !k || !v || !log_alpha || !eta || !o)
             return KLA_ERR_INVALID_ARG;
         if (!aligned(q, elt) || !aligned(k, elt) || !aligned(v, elt) ||
-            !aligned(o, elt) || !aligned(log_alpha, 4) || !aligned(eta, 4))
+            !aligned(o, elt) || !aligned(log_alpha, 4) || !aligned(eta, 4) ||
+            (kw && !aligned(kw, elt)))
             return KLA_ERR_INVALID_ARG;
         if (o == q || o == k || o == v || o == (const void*)log_alpha ||
-            o == (const void*)eta || o == (const void*)h0 || o == (void*)hT)
+            o == (const void*)eta || o == (const void*)h0 || o == (void*)hT ||
+            (kw && o == kw))
             return KLA_ERR_INVALID_ARG;
     }
     if ((h0 && !aligned(h0, 4)) || (hT && !aligned(hT, 4)))
@@ -71,7 +73,8 @@ extern "C" kla_status kla_chunk_fwd_ex(const void* q, const void* k,
     kla::FwdArgs a{q, k, v, log_alpha, eta, eps,
                    rule == KLA_STEP_GIVEN ? 1 : 0, h0, o, hT,
                    B, T, H, dk, dv, C, dtype};
-    const bool tc_ok = kla::chunk_tc_eligible(a);
+    a.kw = kw;
+    const bool tc_ok = !kw && kla::chunk_tc_eligible(a);
     if (algo == KLA_ALGO_TC) {
         if (!tc_ok) return KLA_ERR_UNSUPPORTED_SHAPE;
         return from_cuda(kla::launch_chunk_tc(a, s));
@@ -79,6 +82,55 @@ extern "C" kla_status kla_chunk_fwd_ex(const void* q, const void* k,
     if (algo == KLA_ALGO_AUTO && tc_ok)
         return from_cuda(kla::launch_chunk_tc(a, s));
     return from_cuda(kla::launch_chunk_simt(a, s));
+}
+
+extern "C" kla_status kla_chunk_fwd_ex(const void* q, const void* k,
+                                       const void* v, const float* log_alpha,
+                                       const float* eta, float eps,
+                                       const float* h0, void* o, float* hT,
+                                       int B, int T, int H, int dk, int dv,
+                                       int C, kla_dtype dtype, kla_algo algo,
+                                       kla_step_rule rule,
+                                       kla_stream_t stream) {
+    return chunk_fwd_impl(q, k, nullptr, v, log_alpha, eta, eps, h0, o, hT, B,
+                          T, H, dk, dv, C, dtype, algo, rule, stream);
+}
+
+extern "C" kla_status kla_chunk_fwd_kw(const void* q, const void* k,
+                                       const void* k_write, const void* v,
+                                       const float* log_alpha,
+                                       const float* eta, float eps,
+                                       const float* h0, void* o, float* hT,
+                                       int B, int T, int H, int dk, int dv,
+                                       int C, kla_dtype dtype,
+                                       kla_step_rule rule,
+                                       kla_stream_t stream) {
+    if (!k_write && (long long)B * H > 0 && T > 0) return KLA_ERR_INVALID_ARG;
+    return chunk_fwd_impl(q, k, k_write, v, log_alpha, eta, eps, h0, o, hT, B,
+                          T, H, dk, dv, C, dtype, KLA_ALGO_SIMT, rule, stream);
+}
+
+extern "C" kla_status kla_precond_keys(const void* k, const float* A0,
+                                       void* k_write, float* AT, int B, int T,
+                                       int H, int dk, float x, float delta,
+                                       kla_dtype dtype, kla_stream_t stream) {
+    if (B < 0 || T < 0 || H < 0 || dk <= 0) return KLA_ERR_INVALID_ARG;
+    if (dtype != KLA_F32 && dtype != KLA_BF16) return KLA_ERR_INVALID_ARG;
+    if (!(x > 1.f) || !std::isfinite(x) || !(delta >= 0.f) ||
+        !std::isfinite(delta))
+        return KLA_ERR_INVALID_ARG;
+    if (!supported_dim(dk)) return KLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H > 0x7fffffffLL) return KLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H == 0) return KLA_OK;
+    const size_t elt = dtype == KLA_BF16 ? 2 : 4;
+    if (T > 0 && (!k || !k_write || !aligned(k, elt) ||
+                  !aligned(k_write, elt) || k == k_write))
+        return KLA_ERR_INVALID_ARG;
+    if ((A0 && !aligned(A0, 4)) || (AT && !aligned(AT, 4)))
+        return KLA_ERR_INVALID_ARG;
+    kla::PrecondArgs a{k, A0, k_write, AT, B, T, H, dk, x, delta, dtype};
+    return from_cuda(
+        kla::launch_precond_keys(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 extern "C" kla_status kla_chunk_fwd(const void* q, const void* k,
@@ -93,12 +145,11 @@ extern "C" kla_status kla_chunk_fwd(const void* q, const void* k,
                             stream);
 }
 
-extern "C" kla_status kla_decode_step_ex(const void* q, const void* k,
-                                         const void* v, const float* log_alpha,
-                                         const float* eta, float eps, float* S,
-                                         void* o, int N, int H, int dk, int dv,
-                                         kla_dtype dtype, kla_step_rule rule,
-                                         kla_stream_t stream) {
+static kla_status decode_impl(const void* q, const void* k, const void* kw,
+                              const void* v, const float* log_alpha,
+                              const float* eta, float eps, float* S, void* o,
+                              int N, int H, int dk, int dv, kla_dtype dtype,
+                              kla_step_rule rule, kla_stream_t stream) {
     if (N < 0 || H < 0 || dk <= 0 || dv <= 0) return KLA_ERR_INVALID_ARG;
     if (rule != KLA_STEP_KACZMARZ && rule != KLA_STEP_GIVEN)
         return KLA_ERR_INVALID_ARG;
@@ -113,14 +164,38 @@ extern "C" kla_status kla_decode_step_ex(const void* q, const void* k,
     const size_t elt = dtype == KLA_BF16 ? 2 : 4;
     if (!aligned(q, elt) || !aligned(k, elt) || !aligned(v, elt) ||
         !aligned(o, elt) || !aligned(log_alpha, 4) || !aligned(eta, 4) ||
-        !aligned(S, 16))
+        !aligned(S, 16) || (kw && !aligned(kw, elt)))
         return KLA_ERR_INVALID_ARG;
-    if (o == (void*)S || o == q || o == k || o == v) return KLA_ERR_INVALID_ARG;
+    if (o == (void*)S || o == q || o == k || o == v || (kw && o == kw))
+        return KLA_ERR_INVALID_ARG;
     kla::DecodeArgs a{q, k, v, log_alpha, eta, eps,
                       rule == KLA_STEP_GIVEN ? 1 : 0, S, o, N, H, dk, dv,
                       dtype};
+    a.kw = kw;
     return from_cuda(
         kla::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" kla_status kla_decode_step_ex(const void* q, const void* k,
+                                         const void* v, const float* log_alpha,
+                                         const float* eta, float eps, float* S,
+                                         void* o, int N, int H, int dk, int dv,
+                                         kla_dtype dtype, kla_step_rule rule,
+                                         kla_stream_t stream) {
+    return decode_impl(q, k, nullptr, v, log_alpha, eta, eps, S, o, N, H, dk,
+                       dv, dtype, rule, stream);
+}
+
+extern "C" kla_status kla_decode_step_kw(const void* q, const void* k,
+                                         const void* k_write, const void* v,
+                                         const float* log_alpha,
+                                         const float* eta, float eps, float* S,
+                                         void* o, int N, int H, int dk, int dv,
+                                         kla_dtype dtype, kla_step_rule rule,
+                                         kla_stream_t stream) {
+    if (!k_write && (long long)N * H > 0) return KLA_ERR_INVALID_ARG;
+    return decode_impl(q, k, k_write, v, log_alpha, eta, eps, S, o, N, H, dk,
+                       dv, dtype, rule, stream);
 }
 
 extern "C" kla_status kla_decode_step(const void* q, const void* k,

@@ -45,7 +45,8 @@ struct SimtSmem {
     static constexpr int G = P + kSimtMaxC * LDC;      // cumulative log decay
     static constexpr int BETA = G + kSimtMaxC;
     static constexpr int KDEC = BETA + kSimtMaxC;      // exp(g_last - g_r)
-    static constexpr int TOTAL = KDEC + kSimtMaxC;
+    static constexpr int KW = KDEC + kSimtMaxC;        // write keys, if any
+    static constexpr int TOTAL = KW + kSimtMaxC * LDK;
     static constexpr size_t BYTES = sizeof(float) * (size_t)TOTAL;
 };
 
@@ -64,6 +65,8 @@ kla_chunk_simt_kernel(FwdArgs a) {
     float* gs = sm + L::G;
     float* bs = sm + L::BETA;
     float* kd = sm + L::KDEC;
+    // write keys: a separate tensor when given, else the keys themselves
+    float* KWs = a.kw ? sm + L::KW : Ks;
 
     const int bh = blockIdx.x;
     const int b = bh / a.H, h = bh % a.H;
@@ -73,6 +76,7 @@ kla_chunk_simt_kernel(FwdArgs a) {
     const IO* q = static_cast<const IO*>(a.q);
     const IO* k = static_cast<const IO*>(a.k);
     const IO* v = static_cast<const IO*>(a.v);
+    const IO* kwp = static_cast<const IO*>(a.kw);
     IO* o = static_cast<IO*>(a.o);
 
     // initial state slice
@@ -95,6 +99,10 @@ kla_chunk_simt_kernel(FwdArgs a) {
             }
             Qs[r * L::LDK + c] = qv;
             Ks[r * L::LDK + c] = kv;
+            if (kwp)
+                KWs[r * L::LDK + c] =
+                    t < T ? to_f32(kwp[(((size_t)b * T + t) * H + h) * DK + c])
+                          : 0.f;
         }
         for (int idx = tid; idx < C * DVT; idx += kSimtThreads) {
             const int r = idx / DVT, j = idx % DVT;
@@ -112,12 +120,10 @@ kla_chunk_simt_kernel(FwdArgs a) {
         __syncthreads();
 
         // ---- beta_r and the in-chunk cumulative log decay ----
-        if (tid < C) {
+        if (tid < C) {   // n = k . (write key), ||k||^2 without write keys
             float n = 0.f;
-            for (int c = 0; c < DK; ++c) {
-                const float x = Ks[tid * L::LDK + c];
-                n = fmaf(x, x, n);
-            }
+            for (int c = 0; c < DK; ++c)
+                n = fmaf(Ks[tid * L::LDK + c], KWs[tid * L::LDK + c], n);
             const float denom = n + a.eps;
             if (!a.gdn) bs[tid] = denom == 0.f ? 0.f : bs[tid] / denom;
         }
@@ -148,7 +154,7 @@ kla_chunk_simt_kernel(FwdArgs a) {
                 float kk = 0.f, qk = 0.f;
 #pragma unroll 8
                 for (int c = 0; c < DK; ++c) {
-                    const float ki = Ks[i * L::LDK + c];
+                    const float ki = KWs[i * L::LDK + c];   // write key i
                     kk = fmaf(Ks[r * L::LDK + c], ki, kk);
                     qk = fmaf(Qs[r * L::LDK + c], ki, qk);
                 }
@@ -212,7 +218,7 @@ kla_chunk_simt_kernel(FwdArgs a) {
             const int c = idx / DVT, j = idx % DVT;
             float acc = gC * Ss[c * L::LDV + j];
             for (int r = 0; r < C; ++r)
-                acc = fmaf(kd[r] * Ks[r * L::LDK + c], Us[r * L::LDV + j],
+                acc = fmaf(kd[r] * KWs[r * L::LDK + c], Us[r * L::LDV + j],
                            acc);
             Ss[c * L::LDV + j] = acc;
         }

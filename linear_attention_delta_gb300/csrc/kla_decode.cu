@@ -59,6 +59,7 @@ kla_decode_kernel(DecodeArgs a) {
             S + (size_t)(rs + i * Sh::RS) * dv));
 
     __shared__ float ks[DK];
+    __shared__ float kws[DK];   // write key (= ks without separate keys)
     __shared__ float qs[DK];
     __shared__ float4 red_a[Sh::RS][Sh::CG];
     __shared__ float4 red_b[Sh::RS][Sh::CG];
@@ -66,8 +67,11 @@ kla_decode_kernel(DecodeArgs a) {
 
     const T* qp = static_cast<const T*>(a.q) + (size_t)head * DK;
     const T* kp = static_cast<const T*>(a.k) + (size_t)head * DK;
+    const T* kwp = a.kw ? static_cast<const T*>(a.kw) + (size_t)head * DK
+                        : kp;
     for (int i = tid; i < DK; i += Sh::NT) {
         ks[i] = to_f32(kp[i]);
+        kws[i] = to_f32(kwp[i]);
         qs[i] = to_f32(qp[i]);
     }
     __syncthreads();
@@ -75,8 +79,8 @@ kla_decode_kernel(DecodeArgs a) {
     if (tid < 32) {
         float nk = 0.f, qk = 0.f;
         for (int i = tid; i < DK; i += 32) {
-            nk = fmaf(ks[i], ks[i], nk);
-            qk = fmaf(qs[i], ks[i], qk);
+            nk = fmaf(ks[i], kws[i], nk);     // k . (write key)
+            qk = fmaf(qs[i], kws[i], qk);
         }
         nk = warp_sum(nk);
         qk = warp_sum(qk);
@@ -134,7 +138,7 @@ kla_decode_kernel(DecodeArgs a) {
 #pragma unroll
     for (int i = 0; i < Sh::ROWS; ++i) {
         const int r = rs + i * Sh::RS;
-        const float bk = beta * ks[r];
+        const float bk = beta * kws[r];
         float4 n;
         n.x = fmaf(alpha, s[i].x, bk * e.x);
         n.y = fmaf(alpha, s[i].y, bk * e.y);

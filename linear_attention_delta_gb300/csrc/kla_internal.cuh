@@ -37,8 +37,21 @@ struct FwdArgs {
     int B, T, H, dk, dv, C;
     kla_dtype dtype;
     // may be null: the state at the start of every chunk, fp32
-    // [B, H, ceil(T / C), dk, dv] (written by the CUDA-core kernel only)
+    // [B, H, ceil(T / C), dk, dv]
     float* ckpt = nullptr;
+    // may be null: separate write keys [B, T, H, dk] (the CUDA-core kernel
+    // only); null means the write key is k
+    const void* kw = nullptr;
+};
+
+struct PrecondArgs {
+    const void* k;      // [B, T, H, dk]
+    const float* A0;    // [B, H, dk] or null (zero)
+    void* kw;           // [B, T, H, dk] write keys
+    float* AT;          // [B, H, dk] or null
+    int B, T, H, dk;
+    float x, delta;
+    kla_dtype dtype;
 };
 
 struct BwdArgs {
@@ -76,6 +89,7 @@ struct DecodeArgs {
     void* o;
     int N, H, dk, dv;
     kla_dtype dtype;
+    const void* kw = nullptr;   // separate write keys [N, H, dk] or null
 };
 
 // Each returns cudaSuccess or the launch error.  Shapes are validated by the
@@ -88,6 +102,7 @@ bool chunk_tc_eligible(const FwdArgs& a);
 // Backward pass: the checkpointing forward, the reverse state-gradient
 // recurrence and the per-chunk gradients (CUDA cores, fp32).
 cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_precond_keys(const PrecondArgs& a, cudaStream_t stream);
 size_t chunk_bwd_workspace_floats(int B, int T, int H, int dk, int dv, int C);
 
 // Device fault word of the tensor-core kernels (bounded waits that gave up).

@@ -44,6 +44,12 @@ SIGNATURES = {
     "kla_chunk_bwd_noalloc": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
                                    _FP, _VP, _VP, _VP, _FP, _FP, _FP,
                                    _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
+    "kla_precond_keys": (_I, [_VP, _FP, _VP, _FP, _I, _I, _I, _I, _F, _F,
+                              _I, _VP]),
+    "kla_chunk_fwd_kw": (_I, [_VP, _VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
+                              _FP, _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
+    "kla_decode_step_kw": (_I, [_VP, _VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
+                                _I, _I, _I, _I, _I, _I, _VP]),
     "kla_device_status": (_I, [_VP]),
     "kla_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -249,6 +255,77 @@ def chunk_bwd_noalloc(q, k, v, log_alpha, eta, o_grad, hT_grad=None,
     if st != KLA_OK:
         raise KlaError("kla_chunk_bwd_noalloc", st)
     return out
+
+
+def precond_keys(k, A0=None, x: float = 1.5, delta: float = 1e-6,
+                 k_write=None, AT=None, want_AT: bool = True, stream=None):
+    """Write keys of the diagonal-preconditioned variant
+    (``kla_precond_keys``).  k [B,T,H,dk]; A0 [B,H,dk] fp32 or None.
+    Returns (k_write, A_T); A_T is None unless ``want_AT``."""
+    _check_cuda("k", k)
+    if A0 is not None:
+        _check_cuda("A0", A0, torch.float32)
+    if k.dtype not in DTYPES:
+        raise TypeError(f"unsupported dtype {k.dtype}")
+    B, T, H, dk = k.shape
+    if k_write is None:
+        k_write = torch.empty_like(k)
+    if AT is None and want_AT:
+        AT = torch.empty((B, H, dk), dtype=torch.float32, device=k.device)
+    st = load_library().kla_precond_keys(
+        _ptr(k), _ptr(A0), _ptr(k_write), _ptr(AT), B, T, H, dk, float(x),
+        float(delta), DTYPES[k.dtype], _stream(stream))
+    if st != KLA_OK:
+        raise KlaError("kla_precond_keys", st)
+    return k_write, AT
+
+
+def chunk_fwd_kw(q, k, k_write, v, log_alpha, eta, eps: float = 1e-6,
+                 h0=None, C: int = 64, o=None, hT=None, want_state=True,
+                 stream=None, rule: str = "kaczmarz"):
+    """Forward pass with separate write keys (``kla_chunk_fwd_kw``); see
+    ``chunk_fwd`` for the other arguments."""
+    for n, t in (("q", q), ("k", k), ("k_write", k_write), ("v", v)):
+        _check_cuda(n, t, q.dtype)
+    _check_cuda("log_alpha", log_alpha, torch.float32)
+    _check_cuda("eta", eta, torch.float32)
+    if h0 is not None:
+        _check_cuda("h0", h0, torch.float32)
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and want_state:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    st = load_library().kla_chunk_fwd_kw(
+        _ptr(q), _ptr(k), _ptr(k_write), _ptr(v), _ptr(log_alpha), _ptr(eta),
+        float(eps), _ptr(h0), _ptr(o), _ptr(hT), B, T, H, dk, dv, int(C),
+        DTYPES[q.dtype], RULES[rule], _stream(stream))
+    if st != KLA_OK:
+        raise KlaError("kla_chunk_fwd_kw", st)
+    return o, hT
+
+
+def decode_step_kw(q, k, k_write, v, log_alpha, eta, S, eps: float = 1e-6,
+                   o=None, stream=None, rule: str = "kaczmarz"):
+    """One decode token with a separate write key (``kla_decode_step_kw``);
+    S [N,H,dk,dv] fp32 is updated in place.  Returns o [N,H,dv]."""
+    for n, t in (("q", q), ("k", k), ("k_write", k_write), ("v", v)):
+        _check_cuda(n, t, q.dtype)
+    _check_cuda("log_alpha", log_alpha, torch.float32)
+    _check_cuda("eta", eta, torch.float32)
+    _check_cuda("S", S, torch.float32)
+    N, H, dk = k.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    st = load_library().kla_decode_step_kw(
+        _ptr(q), _ptr(k), _ptr(k_write), _ptr(v), _ptr(log_alpha), _ptr(eta),
+        float(eps), _ptr(S), _ptr(o), N, H, dk, dv, DTYPES[q.dtype],
+        RULES[rule], _stream(stream))
+    if st != KLA_OK:
+        raise KlaError("kla_decode_step_kw", st)
+    return o
 
 
 def device_status(stream=None) -> int:

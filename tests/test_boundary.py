@@ -172,3 +172,25 @@ def test_bwd_rejects_bad_arguments_on_host(lib):
     assert bwd(lib, dk=24) == UNSUPPORTED
     assert bwd(lib, C=48) == UNSUPPORTED
     assert bwd(lib, B=0, q=None, k=None) == OK                 # empty: no-op
+
+
+def test_precond_entry_points_reject_bad_arguments_on_host(lib):
+    P, Q = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000)
+    pk = lib.kla_precond_keys
+    assert pk(P, None, Q, None, 1, 8, 2, 16, 1.0, 1e-6, 1, None) == INVALID
+    assert pk(P, None, Q, None, 1, 8, 2, 16, 1.5, -1.0, 1, None) == INVALID
+    assert pk(P, None, P, None, 1, 8, 2, 16, 1.5, 1e-6, 1, None) == INVALID
+    assert pk(P, None, None, None, 1, 8, 2, 16, 1.5, 1e-6, 1, None) == INVALID
+    assert pk(P, None, Q, None, 1, 8, 2, 24, 1.5, 1e-6, 1, None) == UNSUPPORTED
+    assert pk(None, None, None, None, 0, 8, 2, 16, 1.5, 1e-6, 1, None) == OK
+    fk = lib.kla_chunk_fwd_kw
+    ptrs = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(10)]
+    q, k, kw, v, la, eta, h0, o, hT = ptrs[:9]
+    assert fk(q, k, None, v, la, eta, 1e-6, None, o, None, 1, 8, 1, 16, 16,
+              16, 1, 0, None) == INVALID                  # no write keys
+    assert fk(q, k, o, v, la, eta, 1e-6, None, o, None, 1, 8, 1, 16, 16,
+              16, 1, 0, None) == INVALID                  # o aliases k_write
+    dk_ = lib.kla_decode_step_kw
+    S = ctypes.c_void_p(0x40000)
+    assert dk_(q, k, None, v, la, eta, 1e-6, S, o, 1, 1, 16, 16, 1, 0,
+               None) == INVALID

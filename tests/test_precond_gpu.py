@@ -1,0 +1,133 @@
+"""Parity of the diagonal-preconditioned variant (kla_precond_keys,
+kla_chunk_fwd_kw, kla_decode_step_kw; through the C ABI) with the oracle's
+preconditioned recurrence.
+
+Metric per tensor: err = max|x - x_ref| / max|x_ref|; fp32 I/O <= 1e-4,
+bf16 I/O <= 2e-2.
+"""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_attention_delta_gb300 import inputs as gen
+from linear_attention_delta_gb300 import kla
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+X, DELTA = 1.5, 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    kla.load_library()
+    yield
+    assert kla.device_status() == 0
+
+
+def rel_err(x, ref):
+    x = x.detach().double().cpu().numpy() if hasattr(x, "detach") else x
+    return float(np.max(np.abs(x - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def aniso(inp, seed):
+    """Per-dimension key scales, so that the preconditioner matters."""
+    rng = np.random.default_rng(seed)
+    dk = inp["k"].shape[-1]
+    s = torch.from_numpy(rng.uniform(0.3, 3.0, dk).astype(np.float32))
+    inp = dict(inp)
+    inp["k"] = (inp["k"].float() * s).to(inp["k"].dtype)
+    return inp
+
+
+def dev(inp):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
+            for k, v in inp.items()}
+
+
+@pytest.mark.parametrize("w,sizes", [
+    (gen.TINY, dict(T=50)),
+    (gen.LAYER_1B, dict(B=2, T=300, H=2)),
+])
+def test_write_keys_and_second_moments(w, sizes):
+    inp = aniso(gen.prefill_inputs(w, **sizes), 1)
+    B, T, H, dk = inp["k"].shape
+    A0 = torch.from_numpy(np.random.default_rng(2).uniform(
+        0, 5, (B, H, dk)).astype(np.float32))
+    d = dev(inp)
+    kw, AT = kla.precond_keys(d["k"], A0.cuda(), x=X, delta=DELTA)
+    torch.cuda.synchronize()
+    _, _, A_ref, kw_ref = oracle.pkla_fwd(inp["q"], inp["k"], inp["v"],
+                                          inp["log_alpha"], inp["eta"],
+                                          inp["eps"], None, A0=A0, x=X,
+                                          delta=DELTA)
+    tol = TOL[inp["k"].dtype]
+    assert rel_err(kw, kw_ref) <= tol
+    assert rel_err(AT, A_ref) <= 1e-5
+
+
+@pytest.mark.parametrize("rule", ["kaczmarz", "given"])
+@pytest.mark.parametrize("C,T", [(16, 64), (16, 50), (64, 130)])
+def test_forward_fp32(rule, C, T):
+    w = replace(gen.TINY, h0_std=0.3)
+    inp = aniso(gen.prefill_inputs(w, B=2, T=T, H=2), 3)
+    d = dev(inp)
+    kw, _ = kla.precond_keys(d["k"], x=X, delta=DELTA)
+    o, hT = kla.chunk_fwd_kw(d["q"], d["k"], kw, d["v"], d["log_alpha"],
+                             d["eta"], d["eps"], d["h0"], C=C, rule=rule)
+    torch.cuda.synchronize()
+    o_ref, h_ref, _, _ = oracle.pkla_fwd(inp["q"], inp["k"], inp["v"],
+                                         inp["log_alpha"], inp["eta"],
+                                         inp["eps"], inp["h0"], x=X,
+                                         delta=DELTA, given=(rule == "given"))
+    assert rel_err(o, o_ref) <= 1e-4 and rel_err(hT, h_ref) <= 1e-4
+
+
+@pytest.mark.parametrize("rule", ["kaczmarz", "given"])
+def test_forward_bf16_d128(rule):
+    inp = aniso(gen.prefill_inputs(gen.LAYER_1B, B=1, T=400, H=2), 4)
+    d = dev(inp)
+    kw, _ = kla.precond_keys(d["k"], x=X, delta=DELTA)
+    o, hT = kla.chunk_fwd_kw(d["q"], d["k"], kw, d["v"], d["log_alpha"],
+                             d["eta"], d["eps"], d["h0"], C=64, rule=rule)
+    torch.cuda.synchronize()
+    o_ref, h_ref, _, _ = oracle.pkla_fwd(inp["q"], inp["k"], inp["v"],
+                                         inp["log_alpha"], inp["eta"],
+                                         inp["eps"], inp["h0"], x=X,
+                                         delta=DELTA, given=(rule == "given"))
+    assert rel_err(o, o_ref) <= 2e-2 and rel_err(hT, h_ref) <= 2e-2
+
+
+def test_prefill_then_decode_handoff():
+    """Prefill of 100 tokens (write keys + two-key forward), then 20 decode
+    steps (write key of one token + two-key decode step), the second moments
+    and the state carried across; equals the oracle over all 120 tokens."""
+    inp = aniso(gen.prefill_inputs(gen.LAYER_1B, B=2, T=120, H=2), 5)
+    o_ref, h_ref, A_ref, _ = oracle.pkla_fwd(
+        inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["eta"],
+        inp["eps"], inp["h0"], x=X, delta=DELTA)
+    d = dev(inp)
+    sl = slice(0, 100)
+    cut = {n: d[n][:, sl].contiguous()
+           for n in ("q", "k", "v", "log_alpha", "eta")}
+    kw, A = kla.precond_keys(cut["k"], x=X, delta=DELTA)
+    o, S = kla.chunk_fwd_kw(cut["q"], cut["k"], kw, cut["v"],
+                            cut["log_alpha"], cut["eta"], d["eps"], d["h0"],
+                            C=64)
+    outs = [o]
+    for t in range(100, 120):
+        tok = {n: d[n][:, t].contiguous()
+               for n in ("q", "k", "v", "log_alpha", "eta")}
+        kwt, A = kla.precond_keys(tok["k"][:, None].contiguous(), A, x=X,
+                                  delta=DELTA, AT=A)
+        outs.append(kla.decode_step_kw(
+            tok["q"], tok["k"], kwt[:, 0].contiguous(), tok["v"],
+            tok["log_alpha"], tok["eta"], S, eps=d["eps"])[:, None])
+    torch.cuda.synchronize()
+    assert rel_err(torch.cat(outs, 1), o_ref) <= 2e-2
+    assert rel_err(S, h_ref) <= 2e-2
+    assert rel_err(A, A_ref) <= 1e-5

@@ -420,6 +420,52 @@ def bench_backward(w, inp, steps, warmup, world):
     return ms, nbytes
 
 
+def bench_precond(w, inp, steps, warmup, world):
+    """The diagonal-preconditioned variant on the forward's inputs: the
+    write-key scan plus the two-key forward (CUDA-core kernel), beside the
+    plain forward on the same CUDA-core kernel."""
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
+         for k, v in inp.items()}
+    o = torch.empty_like(d["v"])
+    hT = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32,
+                     device="cuda")
+    kw = torch.empty_like(d["k"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def plain():
+        kla.chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["eta"],
+                      d["eps"], d["h0"], C=w.C, o=o, hT=hT, algo="simt")
+
+    def keys():
+        kla.precond_keys(d["k"], k_write=kw, want_AT=False)
+
+    def fwd_kw():
+        kla.chunk_fwd_kw(d["q"], d["k"], kw, d["v"], d["log_alpha"],
+                         d["eta"], d["eps"], d["h0"], C=w.C, o=o, hT=hT)
+
+    def timed(fn):
+        for _ in range(warmup):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = (torch.cuda.Event(enable_timing=True),
+                      torch.cuda.Event(enable_timing=True))
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return max_over_ranks(float(np.mean(ts)), world)
+
+    t_plain, t_keys, t_fwd = timed(plain), timed(keys), timed(fwd_kw)
+    if kla.device_status() != 0:
+        raise RuntimeError("device-side timeout in the preconditioned bench")
+    return t_plain, t_keys, t_fwd
+
+
 def bench_long_context(world, gpu_index, hbm):
     """The pages' own efficiency points at layer scale: the 131072-token
     prefill (KLA and the learned-step rule on the same kernels), and decode
@@ -598,6 +644,29 @@ def run_ours(args):
                                                 f" x 2 x {mhz:.0f} MHz"},
                     "timed_steps": 3}
 
+    precond = None
+    if not args.no_precond:
+        t_plain, t_keys, t_fwd = bench_precond(w, pf["inputs"], 3, 2, world)
+        alu_peak, sms, mhz = fp32_alu_peak_tflops(
+            (pf["clocks"] or {}).get("sm_max_mhz"))
+        ach = prefill_flops(w) / ((t_keys + t_fwd) * 1e-3) / 1e12
+        precond = {"workload": w.name,
+                   "variant": "diagonal preconditioner on the write key "
+                              "(x = 1.5), Kaczmarz step",
+                   "write_keys_ms": round(t_keys, 4),
+                   "forward_ms": round(t_fwd, 4),
+                   "tokens_per_s": round(world * tokens /
+                                         ((t_keys + t_fwd) * 1e-3), 1),
+                   "plain_same_kernel_ms": round(t_plain, 4),
+                   "overhead_vs_plain": round((t_keys + t_fwd) / t_plain, 4),
+                   "kernels": "kla_precond_keys + kla_chunk_fwd_kw "
+                              "(CUDA-core fp32)",
+                   "roofline": {"bound": "alu", "achieved": round(ach, 2),
+                                "peak": round(alu_peak, 1),
+                                "unit": "TFLOP/s",
+                                "frac": round(ach / alu_peak, 4)},
+                   "timed_steps": 3}
+
     longctx = None
     if not args.no_long:
         longctx = bench_long_context(world, local, hbm)
@@ -619,6 +688,7 @@ def run_ours(args):
             "gpu_launches": pf["launches"], "clocks": pf["clocks"],
             "decode": decode, "gdn_mode": gdn_line,
             "long_context": longctx, "backward": backward,
+            "preconditioned": precond,
             "per_step_ms": [round(x, 5) for x in pf["per_step_ms"]]}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -679,6 +749,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-precond", action="store_true")
     ap.add_argument("--no-long", action="store_true",
                     help="skip the 131K-prefill / 32K-decode points")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,

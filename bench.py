@@ -548,6 +548,65 @@ def cpu_baseline_prefill(inp, budget_s=30.0):
                        f"(fp64 C recurrence, OpenMP over batch x head)")
 
 
+def oracle_rate(fn, units, unit, sample, budget_s=3.0):
+    """The oracle call `fn` (a bounded sample of a workload worth `units`
+    of `unit`), as it stands, repeated on the host cores until `budget_s`
+    have passed (at least once)."""
+    import oracle
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return dict(value=n * units / el, unit=unit, cores=oracle.max_threads(),
+                kind="oracle", sample=f"{sample} x{n}")
+
+
+def extra_cpu_baselines(pf_inputs):
+    """Oracle timings beside the decode, backward, preconditioned and
+    131K-prefill lines, each on a bounded sample of its workload."""
+    import oracle
+    out = {}
+    dw = gen.DECODE
+    d = gen.decode_inputs(dw, steps=1)
+    args = [d[n][0] for n in ("q", "k", "v", "log_alpha", "eta")]
+    S0 = d["S0"].double().numpy()
+    out["decode"] = oracle_rate(
+        lambda: oracle.kla_decode_step(*args, d["eps"], S0), 1, "steps/s",
+        f"one full decode step ({dw.B} x {dw.H} heads, fp64 C)")
+    w = gen.LAYER_1B
+    sub = {k: (v[:1] if isinstance(v, torch.Tensor) else v)
+           for k, v in pf_inputs.items()}
+    rng = np.random.default_rng(gen.SEEDS[w.name] + 200)
+    do = rng.standard_normal(tuple(sub["v"].shape))
+    dhT = rng.standard_normal((1, w.H, w.dk, w.dv))
+    out["backward"] = oracle_rate(
+        lambda: oracle.kla_bwd(sub["q"], sub["k"], sub["v"],
+                               sub["log_alpha"], sub["eta"], sub["eps"],
+                               sub["h0"], do, dhT),
+        w.T, "tokens/s",
+        f"sequence 0 of {w.name} (all {w.H} heads), reverse mode, fp64 C")
+    out["preconditioned"] = oracle_rate(
+        lambda: oracle.pkla_fwd(sub["q"], sub["k"], sub["v"],
+                                sub["log_alpha"], sub["eta"], sub["eps"],
+                                sub["h0"]),
+        w.T, "tokens/s",
+        f"sequence 0 of {w.name} (all {w.H} heads), preconditioned, fp64 C")
+    lw = gen.LONG_131K
+    lt = 8192
+    li = gen.prefill_inputs(lw, T=lt)
+    out["prefill_131k"] = oracle_rate(
+        lambda: oracle.kla_fwd(li["q"], li["k"], li["v"], li["log_alpha"],
+                               li["eta"], li["eps"], li["h0"]),
+        lt, "tokens/s",
+        f"the first {lt} tokens of {lw.name} (all heads; the recurrence "
+        f"costs the same per token at any position), fp64 C")
+    return out
+
+
 def run_only(args):
     """A single kernel on its workload, for profiler captures: warm-up
     launches then `--steps` launches, no other GPU work besides input setup
@@ -674,6 +733,15 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_prefill(pf["inputs"])
+        extra = extra_cpu_baselines(pf["inputs"])
+        if decode is not None:
+            decode["cpu_baseline"] = extra["decode"]
+        if backward is not None:
+            backward["cpu_baseline"] = extra["backward"]
+        if precond is not None:
+            precond["cpu_baseline"] = extra["preconditioned"]
+        if longctx is not None:
+            longctx["prefill_131k"]["cpu_baseline"] = extra["prefill_131k"]
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

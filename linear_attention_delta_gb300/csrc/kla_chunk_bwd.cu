@@ -101,30 +101,50 @@ __device__ __forceinline__ void chunk_gates(const BwdArgs& a, const float* Ks,
 }
 
 // A (unit lower, strictly lower part beta_r Gamma_ri k_r.k_i) and
-// P = Gamma o Q K^T (lower incl.), row stride ldc.
+// P = Gamma o Q K^T (lower incl.), row stride ldc; 4 x 4 tiles per thread.
 template <int DK>
 __device__ __forceinline__ void build_a_p(int C, const float* Qs,
                                           const float* Ks, int LDK,
                                           const float* gs, const float* bs,
                                           float* As, float* Ps, int ldc) {
-    for (int idx = threadIdx.x; idx < C * C; idx += kBwdThreads) {
-        const int r = idx / C, i = idx % C;
-        float av = (i == r) ? 1.f : 0.f;
-        float pv = 0.f;
-        if (i <= r) {
-            float kk = 0.f, qk = 0.f;
-#pragma unroll 8
+    const int nrt = C / 4;
+    for (int tile = threadIdx.x; tile < nrt * nrt; tile += kBwdThreads) {
+        const int r0 = (tile / nrt) * 4, i0 = (tile % nrt) * 4;
+        float kk[4][4] = {}, qk[4][4] = {};
+        if (i0 <= r0 + 3) {
+#pragma unroll 4
             for (int c = 0; c < DK; ++c) {
-                const float ki = Ks[i * LDK + c];
-                kk = fmaf(Ks[r * LDK + c], ki, kk);
-                qk = fmaf(Qs[r * LDK + c], ki, qk);
+                float kr[4], qr[4], ki[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    kr[x] = Ks[(r0 + x) * LDK + c];
+                    qr[x] = Qs[(r0 + x) * LDK + c];
+                    ki[x] = Ks[(i0 + x) * LDK + c];
+                }
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                    for (int ii = 0; ii < 4; ++ii) {
+                        kk[rr][ii] = fmaf(kr[rr], ki[ii], kk[rr][ii]);
+                        qk[rr][ii] = fmaf(qr[rr], ki[ii], qk[rr][ii]);
+                    }
             }
-            const float dec = expf(gs[r] - gs[i]);
-            pv = dec * qk;
-            if (i < r) av = bs[r] * dec * kk;
         }
-        As[r * ldc + i] = av;
-        Ps[r * ldc + i] = pv;
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+                const int r = r0 + rr, i = i0 + ii;
+                float av = (i == r) ? 1.f : 0.f;
+                float pv = 0.f;
+                if (i <= r) {
+                    const float dec = expf(gs[r] - gs[i]);
+                    pv = dec * qk[rr][ii];
+                    if (i < r) av = bs[r] * dec * kk[rr][ii];
+                }
+                As[r * ldc + i] = av;
+                Ps[r * ldc + i] = pv;
+            }
     }
 }
 
@@ -266,41 +286,97 @@ kla_bwd_state_kernel(BwdArgs a) {
         __syncthreads();
         invert_unit_lower(As, Tm, C, L::LDC);
 
-        // dU~ = P^T dO + Diag(lambda) K dS'
-        for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
-            const int r = idx / DVT, j = idx % DVT;
-            float kds = 0.f;
-#pragma unroll 8
-            for (int c = 0; c < DK; ++c)
-                kds = fmaf(Ks[r * L::LDK + c], dS[c * L::LDV + j], kds);
-            float w = lam[r] * kds;
-            for (int i = r; i < C; ++i)
-                w = fmaf(Ps[i * L::LDC + r], Ds[i * L::LDV + j], w);
-            Ws[r * L::LDV + j] = w;
+        constexpr int NCQ = DVT / 4;
+        constexpr int LDK = L::LDK, LDV = L::LDV, LDC = L::LDC;
+        // dU~ = P^T dO + Diag(lambda) K dS' (2 x 4 tiles)
+        for (int tile = tid; tile < (C / 2) * NCQ; tile += kBwdThreads) {
+            const int r0 = (tile / NCQ) * 2, q0 = (tile % NCQ) * 4;
+            float kd[2][4] = {}, pd[2][4] = {};
+#pragma unroll 4
+            for (int c = 0; c < DK; ++c) {
+                const float k0 = Ks[r0 * LDK + c], k1 = Ks[(r0 + 1) * LDK + c];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float dsv = dS[c * LDV + q0 + jj];
+                    kd[0][jj] = fmaf(k0, dsv, kd[0][jj]);
+                    kd[1][jj] = fmaf(k1, dsv, kd[1][jj]);
+                }
+            }
+            for (int i = r0; i < C; ++i) {
+                const float p0 = Ps[i * LDC + r0];
+                const float p1 = i > r0 ? Ps[i * LDC + r0 + 1] : 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float d = Ds[i * LDV + q0 + jj];
+                    pd[0][jj] = fmaf(p0, d, pd[0][jj]);
+                    pd[1][jj] = fmaf(p1, d, pd[1][jj]);
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    Ws[(r0 + rr) * LDV + q0 + jj] =
+                        fmaf(lam[r0 + rr], kd[rr][jj], pd[rr][jj]);
         }
         __syncthreads();
 
-        // dF = T^T dU~
-        for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
-            const int r = idx / DVT, j = idx % DVT;
-            float x = 0.f;
-            for (int i = r; i < C; ++i)
-                x = fmaf(Tm[i * L::LDC + r], Ws[i * L::LDV + j], x);
-            W2[r * L::LDV + j] = x;
+        // dF = T^T dU~ (2 x 4 tiles)
+        for (int tile = tid; tile < (C / 2) * NCQ; tile += kBwdThreads) {
+            const int r0 = (tile / NCQ) * 2, q0 = (tile % NCQ) * 4;
+            float df[2][4] = {};
+            for (int i = r0; i < C; ++i) {
+                const float t0v = Tm[i * LDC + r0];
+                const float t1v = i > r0 ? Tm[i * LDC + r0 + 1] : 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float w = Ws[i * LDV + q0 + jj];
+                    df[0][jj] = fmaf(t0v, w, df[0][jj]);
+                    df[1][jj] = fmaf(t1v, w, df[1][jj]);
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    W2[(r0 + rr) * LDV + q0 + jj] = df[rr][jj];
         }
         __syncthreads();
 
         // dS = gamma_C dS' + Q^T Diag(gamma) dO - K^T Diag(gamma beta) dF
+        // (4 x 4 tiles of the DK x DVT slice)
         const float gC = gam[C - 1];
-        for (int idx = tid; idx < DK * DVT; idx += kBwdThreads) {
-            const int c = idx / DVT, j = idx % DVT;
-            float acc = gC * dS[c * L::LDV + j];
-            for (int r = 0; r < C; ++r)
-                acc = fmaf(gam[r],
-                           Qs[r * L::LDK + c] * Ds[r * L::LDV + j] -
-                               Ks[r * L::LDK + c] * bs[r] * W2[r * L::LDV + j],
-                           acc);
-            dS[c * L::LDV + j] = acc;
+        for (int tile = tid; tile < (DK / 4) * NCQ; tile += kBwdThreads) {
+            const int c0 = (tile / NCQ) * 4, q0 = (tile % NCQ) * 4;
+            float acc[4][4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    acc[x][jj] = gC * dS[(c0 + x) * LDV + q0 + jj];
+            for (int r = 0; r < C; ++r) {
+                const float gr = gam[r], gbr = gam[r] * bs[r];
+                float qv[4], kv[4], d[4], w[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    qv[x] = gr * Qs[r * LDK + c0 + x];
+                    kv[x] = gbr * Ks[r * LDK + c0 + x];
+                    d[x] = Ds[r * LDV + q0 + x];
+                    w[x] = W2[r * LDV + q0 + x];
+                }
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        acc[x][jj] = fmaf(qv[x], d[jj],
+                                          fmaf(-kv[x], w[jj], acc[x][jj]));
+            }
+            // all reads of dS happen in this tile's own entries
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    dS[(c0 + x) * LDV + q0 + jj] = acc[x][jj];
         }
         __syncthreads();
     }
@@ -351,7 +427,9 @@ template <int DK, int DVT, typename IO>
 __global__ void __launch_bounds__(kBwdThreads)
 kla_bwd_grad_kernel(BwdArgs a) {
     using L = GradSmem<DK, DVT>;
-    constexpr int kAcc = kBwdMaxC * DK / kBwdThreads;  // owned (r, c) pairs
+    constexpr int LDK = L::LDK, LDV = L::LDV, LDC = L::LDC;
+    constexpr int NCC = DK / 16;      // owned columns of a C x DK tile
+    constexpr int NCQ = DVT / 4;      // column quads of a C x DVT matrix
     extern __shared__ float sm[];
     float* Qs = sm + L::Q;
     float* Ks = sm + L::K;
@@ -388,8 +466,8 @@ kla_bwd_grad_kernel(BwdArgs a) {
     const float* Sg = a.ckpt + ((size_t)bh * nch + ch) * DK * dv;
     const float* dSg = a.dsck + ((size_t)bh * nch + ch) * DK * dv;
 
-    load_chunk_qk(a, b, h, t0, DK, L::LDK, Qs, Ks, gs, bs);
-    for (int idx = tid; idx < C * L::LDC; idx += kBwdThreads) {
+    load_chunk_qk(a, b, h, t0, DK, LDK, Qs, Ks, gs, bs);
+    for (int idx = tid; idx < C * LDC; idx += kBwdThreads) {
         dP[idx] = 0.f;
         dA[idx] = 0.f;
     }
@@ -400,14 +478,19 @@ kla_bwd_grad_kernel(BwdArgs a) {
     }
     if (tid == 0) dgc[0] = 0.f;
     __syncthreads();
-    chunk_gates<DK>(a, Ks, L::LDK, gs, bs, gam, lam, nrm);
-    build_a_p<DK>(C, Qs, Ks, L::LDK, gs, bs, As, Ps, L::LDC);
+    chunk_gates<DK>(a, Ks, LDK, gs, bs, gam, lam, nrm);
+    build_a_p<DK>(C, Qs, Ks, LDK, gs, bs, As, Ps, LDC);
     __syncthreads();
-    invert_unit_lower(As, Tm, C, L::LDC);
+    invert_unit_lower(As, Tm, C, LDC);
 
-    float dq_acc[kAcc], dk_acc[kAcc];
+    // owned 4 x NCC tile of the C x DK gradients dQ, dK: rows 4 rg + rr,
+    // columns cg + 16 cc
+    const int cg = tid % 16, rg = tid / 16;
+    float dq_acc[4][NCC], dk_acc[4][NCC];
 #pragma unroll
-    for (int m = 0; m < kAcc; ++m) dq_acc[m] = dk_acc[m] = 0.f;
+    for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+        for (int cc = 0; cc < NCC; ++cc) dq_acc[rr][cc] = dk_acc[rr][cc] = 0.f;
 
     for (int j0 = 0; j0 < dv; j0 += DVT) {
         float sdot = 0.f;
@@ -415,8 +498,8 @@ kla_bwd_grad_kernel(BwdArgs a) {
             const int c = idx / DVT, j = idx % DVT;
             const float sv = Sg[(size_t)c * dv + j0 + j];
             const float dsv = dSg[(size_t)c * dv + j0 + j];
-            St[c * L::LDV + j] = sv;
-            dSt[c * L::LDV + j] = dsv;
+            St[c * LDV + j] = sv;
+            dSt[c * LDV + j] = dsv;
             sdot = fmaf(sv, dsv, sdot);
         }
         atomicAdd(dgc, sdot);
@@ -424,134 +507,261 @@ kla_bwd_grad_kernel(BwdArgs a) {
             const int r = idx / DVT, j = idx % DVT;
             const int t = t0 + r;
             const size_t off = (((size_t)b * T + t) * H + h) * dv + j0 + j;
-            Xs[r * L::LDV + j] = t < T ? ld_io<IO>(a.v, off) : 0.f;
-            Ds[r * L::LDV + j] = t < T ? ld_io<IO>(a.dout, off) : 0.f;
+            Xs[r * LDV + j] = t < T ? ld_io<IO>(a.v, off) : 0.f;
+            Ds[r * LDV + j] = t < T ? ld_io<IO>(a.dout, off) : 0.f;
         }
         __syncthreads();
 
-        // K S, X = V - Diag(gamma) K S, F = Diag(beta) X; dgamma from Q S
-        for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
-            const int r = idx / DVT, j = idx % DVT;
-            float ks = 0.f, qs = 0.f;
-#pragma unroll 8
+        // K S, Q S (2 x 4 tiles): X = V - Diag(gamma) K S, F = Diag(beta) X
+        // (into W), dgamma += dO . Q S
+        for (int tile = tid; tile < (C / 2) * NCQ; tile += kBwdThreads) {
+            const int r0 = (tile / NCQ) * 2, q0 = (tile % NCQ) * 4;
+            float ks[2][4] = {}, qs[2][4] = {};
+#pragma unroll 4
             for (int c = 0; c < DK; ++c) {
-                const float sv = St[c * L::LDV + j];
-                ks = fmaf(Ks[r * L::LDK + c], sv, ks);
-                qs = fmaf(Qs[r * L::LDK + c], sv, qs);
+                const float k0 = Ks[r0 * LDK + c], k1 = Ks[(r0 + 1) * LDK + c];
+                const float x0 = Qs[r0 * LDK + c], x1 = Qs[(r0 + 1) * LDK + c];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float sv = St[c * LDV + q0 + jj];
+                    ks[0][jj] = fmaf(k0, sv, ks[0][jj]);
+                    ks[1][jj] = fmaf(k1, sv, ks[1][jj]);
+                    qs[0][jj] = fmaf(x0, sv, qs[0][jj]);
+                    qs[1][jj] = fmaf(x1, sv, qs[1][jj]);
+                }
             }
-            KS[r * L::LDV + j] = ks;
-            const float x = fmaf(-gam[r], ks, Xs[r * L::LDV + j]);
-            Xs[r * L::LDV + j] = x;
-            Ws[r * L::LDV + j] = bs[r] * x;                 // F
-            atomicAdd(&dgam[r], Ds[r * L::LDV + j] * qs);
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = r0 + rr;
+                float dgp = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int j = q0 + jj;
+                    KS[r * LDV + j] = ks[rr][jj];
+                    const float x = fmaf(-gam[r], ks[rr][jj], Xs[r * LDV + j]);
+                    Xs[r * LDV + j] = x;
+                    Ws[r * LDV + j] = bs[r] * x;
+                    dgp = fmaf(Ds[r * LDV + j], qs[rr][jj], dgp);
+                }
+                atomicAdd(&dgam[r], dgp);
+            }
         }
         __syncthreads();
 
         // U~ = T F
-        for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
-            const int r = idx / DVT, j = idx % DVT;
-            float x = 0.f;
-            for (int i = 0; i <= r; ++i)
-                x = fmaf(Tm[r * L::LDC + i], Ws[i * L::LDV + j], x);
-            Us[r * L::LDV + j] = x;
-        }
-        __syncthreads();
-
-        // dU~ = P^T dO + Diag(lambda) K dS';  dlambda_r = (K dS')_r . U~_r
-        for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
-            const int r = idx / DVT, j = idx % DVT;
-            float kds = 0.f;
-#pragma unroll 8
-            for (int c = 0; c < DK; ++c)
-                kds = fmaf(Ks[r * L::LDK + c], dSt[c * L::LDV + j], kds);
-            float w = lam[r] * kds;
-            for (int i = r; i < C; ++i)
-                w = fmaf(Ps[i * L::LDC + r], Ds[i * L::LDV + j], w);
-            Ws[r * L::LDV + j] = w;
-            atomicAdd(&dlam[r], kds * Us[r * L::LDV + j]);
-        }
-        __syncthreads();
-
-        // dF = T^T dU~ (into the K S slots, once used); dV = dX =
-        // Diag(beta) dF; dbeta from F = Diag(beta) X; dgamma from X
-        for (int idx = tid; idx < C * DVT; idx += kBwdThreads) {
-            const int r = idx / DVT, j = idx % DVT;
-            const int t = t0 + r;
-            float df = 0.f;
-            for (int i = r; i < C; ++i)
-                df = fmaf(Tm[i * L::LDC + r], Ws[i * L::LDV + j], df);
-            const float dx = bs[r] * df;
-            if (t < T)
-                static_cast<IO*>(a.dv_)[(((size_t)b * T + t) * H + h) * dv +
-                                        j0 + j] = from_f32<IO>(dx);
-            atomicAdd(&db[r], df * Xs[r * L::LDV + j]);
-            atomicAdd(&dgam[r], -dx * KS[r * L::LDV + j]);
-            KS[r * L::LDV + j] = df;
-        }
-        __syncthreads();
-        // dP = dO U~^T (i <= r), dA = -dF U~^T (i < r)
-        for (int idx = tid; idx < C * C; idx += kBwdThreads) {
-            const int r = idx / C, i = idx % C;
-            if (i > r) continue;
-            float sp = 0.f, sa = 0.f;
-#pragma unroll 8
-            for (int j = 0; j < DVT; ++j) {
-                const float ui = Us[i * L::LDV + j];
-                sp = fmaf(Ds[r * L::LDV + j], ui, sp);
-                sa = fmaf(KS[r * L::LDV + j], ui, sa);
-            }
-            dP[r * L::LDC + i] += sp;
-            if (i < r) dA[r * L::LDC + i] -= sa;
-        }
-        // owned (r, c): dQ += gamma_r dO S^T; dK += lambda_r U~ dS'^T -
-        // gamma_r beta_r dF S^T
+        for (int tile = tid; tile < (C / 2) * NCQ; tile += kBwdThreads) {
+            const int r0 = (tile / NCQ) * 2, q0 = (tile % NCQ) * 4;
+            float u[2][4] = {};
+            for (int i = 0; i <= r0 + 1; ++i) {
+                const float t0v = i <= r0 ? Tm[r0 * LDC + i] : 0.f;
+                const float t1v = Tm[(r0 + 1) * LDC + i];
 #pragma unroll
-        for (int m = 0; m < kAcc; ++m) {
-            const int idx = tid + m * kBwdThreads;
-            const int r = idx / DK, c = idx % DK;
-            if (r >= C) continue;
-            float sdo = 0.f, su = 0.f, sf = 0.f;
-#pragma unroll 8
-            for (int j = 0; j < DVT; ++j) {
-                const float sv = St[c * L::LDV + j];
-                sdo = fmaf(Ds[r * L::LDV + j], sv, sdo);
-                sf = fmaf(KS[r * L::LDV + j], sv, sf);
-                su = fmaf(Us[r * L::LDV + j], dSt[c * L::LDV + j], su);
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float f = Ws[i * LDV + q0 + jj];
+                    u[0][jj] = fmaf(t0v, f, u[0][jj]);
+                    u[1][jj] = fmaf(t1v, f, u[1][jj]);
+                }
             }
-            dq_acc[m] = fmaf(gam[r], sdo, dq_acc[m]);
-            dk_acc[m] += lam[r] * su - gam[r] * bs[r] * sf;
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    Us[(r0 + rr) * LDV + q0 + jj] = u[rr][jj];
+        }
+        __syncthreads();
+
+        // dU~ = P^T dO + Diag(lambda) K dS' (into W); dlambda_r = (K dS')_r.U~_r
+        for (int tile = tid; tile < (C / 2) * NCQ; tile += kBwdThreads) {
+            const int r0 = (tile / NCQ) * 2, q0 = (tile % NCQ) * 4;
+            float kd[2][4] = {}, pd[2][4] = {};
+#pragma unroll 4
+            for (int c = 0; c < DK; ++c) {
+                const float k0 = Ks[r0 * LDK + c], k1 = Ks[(r0 + 1) * LDK + c];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float dsv = dSt[c * LDV + q0 + jj];
+                    kd[0][jj] = fmaf(k0, dsv, kd[0][jj]);
+                    kd[1][jj] = fmaf(k1, dsv, kd[1][jj]);
+                }
+            }
+            for (int i = r0; i < C; ++i) {
+                const float p0 = Ps[i * LDC + r0];
+                const float p1 = i > r0 ? Ps[i * LDC + r0 + 1] : 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float d = Ds[i * LDV + q0 + jj];
+                    pd[0][jj] = fmaf(p0, d, pd[0][jj]);
+                    pd[1][jj] = fmaf(p1, d, pd[1][jj]);
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = r0 + rr;
+                float dlp = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int j = q0 + jj;
+                    Ws[r * LDV + j] = fmaf(lam[r], kd[rr][jj], pd[rr][jj]);
+                    dlp = fmaf(kd[rr][jj], Us[r * LDV + j], dlp);
+                }
+                atomicAdd(&dlam[r], dlp);
+            }
+        }
+        __syncthreads();
+
+        // dF = T^T dU~ (into the K S slots, once read); dV = dX =
+        // Diag(beta) dF; dbeta from F = Diag(beta) X; dgamma from X
+        for (int tile = tid; tile < (C / 2) * NCQ; tile += kBwdThreads) {
+            const int r0 = (tile / NCQ) * 2, q0 = (tile % NCQ) * 4;
+            float df[2][4] = {};
+            for (int i = r0; i < C; ++i) {
+                const float t0v = Tm[i * LDC + r0];
+                const float t1v = i > r0 ? Tm[i * LDC + r0 + 1] : 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float w = Ws[i * LDV + q0 + jj];
+                    df[0][jj] = fmaf(t0v, w, df[0][jj]);
+                    df[1][jj] = fmaf(t1v, w, df[1][jj]);
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = r0 + rr;
+                const int t = t0 + r;
+                float dbp = 0.f, dgp = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int j = q0 + jj;
+                    const float dx = bs[r] * df[rr][jj];
+                    if (t < T)
+                        static_cast<IO*>(a.dv_)[(((size_t)b * T + t) * H + h) *
+                                                    dv + j0 + j] =
+                            from_f32<IO>(dx);
+                    dbp = fmaf(df[rr][jj], Xs[r * LDV + j], dbp);
+                    dgp = fmaf(-dx, KS[r * LDV + j], dgp);
+                    KS[r * LDV + j] = df[rr][jj];
+                }
+                atomicAdd(&db[r], dbp);
+                atomicAdd(&dgam[r], dgp);
+            }
+        }
+        __syncthreads();
+
+        // dP = dO U~^T (i <= r), dA = -dF U~^T (i < r): 4 x 4 tiles
+        {
+            const int nrt = C / 4;
+            for (int tile = tid; tile < nrt * nrt; tile += kBwdThreads) {
+                const int r0 = (tile / nrt) * 4, i0 = (tile % nrt) * 4;
+                if (i0 > r0 + 3) continue;
+                float ap[4][4] = {}, aa[4][4] = {};
+#pragma unroll 4
+                for (int j = 0; j < DVT; ++j) {
+                    float d[4], f[4], u[4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        d[x] = Ds[(r0 + x) * LDV + j];
+                        f[x] = KS[(r0 + x) * LDV + j];
+                        u[x] = Us[(i0 + x) * LDV + j];
+                    }
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                        for (int ii = 0; ii < 4; ++ii) {
+                            ap[rr][ii] = fmaf(d[rr], u[ii], ap[rr][ii]);
+                            aa[rr][ii] = fmaf(f[rr], u[ii], aa[rr][ii]);
+                        }
+                }
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                    for (int ii = 0; ii < 4; ++ii) {
+                        const int r = r0 + rr, i = i0 + ii;
+                        if (i <= r) dP[r * LDC + i] += ap[rr][ii];
+                        if (i < r) dA[r * LDC + i] -= aa[rr][ii];
+                    }
+            }
+        }
+        // owned (r, c): dQ += gamma_r dO S^T;
+        // dK += lambda_r U~ dS'^T - gamma_r beta_r dF S^T
+#pragma unroll 2
+        for (int j = 0; j < DVT; ++j) {
+            float d[4], u[4], f[4];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                const int r = 4 * rg + rr;
+                const bool in = r < C;
+                d[rr] = in ? gam[r] * Ds[r * LDV + j] : 0.f;
+                u[rr] = in ? lam[r] * Us[r * LDV + j] : 0.f;
+                f[rr] = in ? gam[r] * bs[r] * KS[r * LDV + j] : 0.f;
+            }
+#pragma unroll
+            for (int cc = 0; cc < NCC; ++cc) {
+                const int c = cg + 16 * cc;
+                const float sv = St[c * LDV + j], dsv = dSt[c * LDV + j];
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) {
+                    dq_acc[rr][cc] = fmaf(d[rr], sv, dq_acc[rr][cc]);
+                    dk_acc[rr][cc] =
+                        fmaf(u[rr], dsv, fmaf(-f[rr], sv, dk_acc[rr][cc]));
+                }
+            }
         }
         __syncthreads();
     }
 
     // dGamma o Gamma (into A), Gamma o dP (into dP), D (into dA), and the
-    // A-part of dbeta
-    for (int idx = tid; idx < C * C; idx += kBwdThreads) {
-        const int r = idx / C, i = idx % C;
-        float dgg = 0.f, dpt = 0.f, dd = 0.f;
-        if (i <= r) {
-            float qk = 0.f, kk = 0.f;
-#pragma unroll 8
+    // A-part of dbeta: 4 x 4 tiles of the lower triangle
+    {
+        const int nrt = C / 4;
+        for (int tile = tid; tile < nrt * nrt; tile += kBwdThreads) {
+            const int r0 = (tile / nrt) * 4, i0 = (tile % nrt) * 4;
+            if (i0 > r0 + 3) continue;
+            float qk[4][4] = {}, kk[4][4] = {};
+#pragma unroll 4
             for (int c = 0; c < DK; ++c) {
-                const float ki = Ks[i * L::LDK + c];
-                qk = fmaf(Qs[r * L::LDK + c], ki, qk);
-                kk = fmaf(Ks[r * L::LDK + c], ki, kk);
+                float qr[4], kr[4], ki[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    qr[x] = Qs[(r0 + x) * LDK + c];
+                    kr[x] = Ks[(r0 + x) * LDK + c];
+                    ki[x] = Ks[(i0 + x) * LDK + c];
+                }
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                    for (int ii = 0; ii < 4; ++ii) {
+                        qk[rr][ii] = fmaf(qr[rr], ki[ii], qk[rr][ii]);
+                        kk[rr][ii] = fmaf(kr[rr], ki[ii], kk[rr][ii]);
+                    }
             }
-            const float gmm = expf(gs[r] - gs[i]);
-            const float dpv = dP[r * L::LDC + i];
-            float dgm = dpv * qk;
-            dpt = gmm * dpv;
-            if (i < r) {
-                const float dav = dA[r * L::LDC + i];
-                dgm = fmaf(dav * bs[r], kk, dgm);
-                dd = bs[r] * gmm * dav;
-                atomicAdd(&db[r], dav * gmm * kk);
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                const int r = r0 + rr;
+                float dbp = 0.f;
+#pragma unroll
+                for (int ii = 0; ii < 4; ++ii) {
+                    const int i = i0 + ii;
+                    float dgg = 0.f, dpt = 0.f, dd = 0.f;
+                    if (i <= r) {
+                        const float gmm = expf(gs[r] - gs[i]);
+                        const float dpv = dP[r * LDC + i];
+                        float dgm = dpv * qk[rr][ii];
+                        dpt = gmm * dpv;
+                        if (i < r) {
+                            const float dav = dA[r * LDC + i];
+                            dgm = fmaf(dav * bs[r], kk[rr][ii], dgm);
+                            dd = bs[r] * gmm * dav;
+                            dbp = fmaf(dav * gmm, kk[rr][ii], dbp);
+                        }
+                        dgg = dgm * gmm;
+                    }
+                    As[r * LDC + i] = dgg;
+                    dP[r * LDC + i] = dpt;
+                    dA[r * LDC + i] = dd;
+                }
+                atomicAdd(&db[r], dbp);
             }
-            dgg = dgm * gmm;
         }
-        As[r * L::LDC + i] = dgg;
-        dP[r * L::LDC + i] = dpt;
-        dA[r * L::LDC + i] = dd;
     }
     __syncthreads();
 
@@ -559,8 +769,8 @@ kla_bwd_grad_kernel(BwdArgs a) {
     if (tid < C) {
         const int r = tid;
         float g = dgam[r] * gam[r] - dlam[r] * lam[r];
-        for (int i = 0; i <= r; ++i) g += As[r * L::LDC + i];
-        for (int rr = r; rr < C; ++rr) g -= As[rr * L::LDC + r];
+        for (int i = 0; i <= r; ++i) g += As[r * LDC + i];
+        for (int rr = r; rr < C; ++rr) g -= As[rr * LDC + r];
         if (r == C - 1) {
             for (int t = 0; t < C; ++t) g = fmaf(dlam[t], lam[t], g);
             g = fmaf(dgc[0], gam[C - 1], g);
@@ -588,26 +798,41 @@ kla_bwd_grad_kernel(BwdArgs a) {
     }
 
     // dQ += (Gamma o dP) K;  dK += (Gamma o dP)^T Q + (D + D^T) K + 2 dn k
+    for (int i = 0; i < C; ++i) {
+        float kv[NCC], qv[NCC];
 #pragma unroll
-    for (int m = 0; m < kAcc; ++m) {
-        const int idx = tid + m * kBwdThreads;
-        const int r = idx / DK, c = idx % DK;
-        if (r >= C) continue;
-        float q_acc = dq_acc[m], k_acc = dk_acc[m];
-        for (int i = 0; i <= r; ++i) {
-            q_acc = fmaf(dP[r * L::LDC + i], Ks[i * L::LDK + c], q_acc);
-            k_acc = fmaf(dA[r * L::LDC + i], Ks[i * L::LDK + c], k_acc);
+        for (int cc = 0; cc < NCC; ++cc) {
+            kv[cc] = Ks[i * LDK + cg + 16 * cc];
+            qv[cc] = Qs[i * LDK + cg + 16 * cc];
         }
-        for (int rr = r; rr < C; ++rr) {
-            k_acc = fmaf(dP[rr * L::LDC + r], Qs[rr * L::LDK + c], k_acc);
-            k_acc = fmaf(dA[rr * L::LDC + r], Ks[rr * L::LDK + c], k_acc);
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            const int r = 4 * rg + rr;
+            if (r >= C) continue;
+            const float dp = i <= r ? dP[r * LDC + i] : 0.f;
+            const float dd = i < r ? dA[r * LDC + i] : 0.f;
+            const float dpT = i >= r ? dP[i * LDC + r] : 0.f;
+            const float ddT = i > r ? dA[i * LDC + r] : 0.f;
+#pragma unroll
+            for (int cc = 0; cc < NCC; ++cc) {
+                dq_acc[rr][cc] = fmaf(dp, kv[cc], dq_acc[rr][cc]);
+                dk_acc[rr][cc] = fmaf(dd + ddT, kv[cc],
+                                      fmaf(dpT, qv[cc], dk_acc[rr][cc]));
+            }
         }
-        k_acc = fmaf(2.f * db[r], Ks[r * L::LDK + c], k_acc);
+    }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+        const int r = 4 * rg + rr;
         const int t = t0 + r;
-        if (t < T) {
+        if (r >= C || t >= T) continue;
+#pragma unroll
+        for (int cc = 0; cc < NCC; ++cc) {
+            const int c = cg + 16 * cc;
             const size_t off = (((size_t)b * T + t) * H + h) * DK + c;
-            static_cast<IO*>(a.dq)[off] = from_f32<IO>(q_acc);
-            static_cast<IO*>(a.dk_)[off] = from_f32<IO>(k_acc);
+            static_cast<IO*>(a.dq)[off] = from_f32<IO>(dq_acc[rr][cc]);
+            static_cast<IO*>(a.dk_)[off] = from_f32<IO>(
+                fmaf(2.f * db[r], Ks[r * LDK + c], dk_acc[rr][cc]));
         }
     }
 }

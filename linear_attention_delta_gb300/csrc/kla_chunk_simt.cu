@@ -9,20 +9,24 @@
 // Per chunk (rows r, i = 0..C-1; g = in-chunk cumulative log decay,
 // gamma_r = exp(g_r), Gamma_ri = exp(g_r - g_i) for r >= i):
 //   beta_r = eta_r / (||k_r||^2 + eps)                    Kaczmarz step
-//   A = I + strict_lower(Diag(beta) (Gamma o K K^T))      C x C, unit lower
-//   [U | W] = A^{-1} [Diag(beta) V | Diag(beta gamma) K]  forward substitution
-//   U~ = U - W S                                          chunk residuals
+//   A  = I + strict_lower(Diag(beta) (Gamma o K K^T)),    T = A^{-1}
+//   U~ = T Diag(beta) (V - Diag(gamma) K S)               chunk residuals
 //   O  = Diag(gamma) Q S + lower_incl(Gamma o Q K^T) U~
 //   S  = gamma_C S + (Diag(Gamma_{C,.}) K)^T U~
 // This is the gated-DeltaNet block solver with B = Diag(beta) as the only
-// change (gist.science/es/paper/2605.08587, section "Implementacion").  The
-// decay-aware W = A^{-1} B Diag(gamma) K follows from the recurrence with a
-// per-token scalar decay; only exponents g_r - g_i with r >= i (and g_r,
-// g_C - g_i) are ever exponentiated, so no factor exceeds 1.
+// change (gist.science/es/paper/2605.08587, section "Implementacion"), with
+// U - W S (U = T B V, W = T B Diag(gamma) K) regrouped as T B times the
+// residual.  Only exponents g_r - g_i with r >= i (and g_r, g_C - g_i) are
+// ever exponentiated, so no factor exceeds 1.  T comes from a blocked
+// inverse (16 x 16 tiles); every product is register-tiled.  With separate
+// write keys kw (the diagonal-preconditioned variant) K K^T and Q K^T become
+// K Kw^T and Q Kw^T, ||k||^2 becomes k . kw and the state is written along
+// Kw; the residual is still read along K.
 //
 // A ragged last chunk is padded in-kernel with k = q = v = 0, eta = 0,
 // log_alpha = 0: such a step has beta = 0 and alpha = 1, an exact identity.
 #include "kla_internal.cuh"
+#include "simt_blocks.cuh"
 
 namespace kla {
 namespace {
@@ -37,16 +41,20 @@ struct SimtSmem {
     static constexpr int LDC = kSimtMaxC + 1;
     static constexpr int Q = 0;
     static constexpr int K = Q + kSimtMaxC * LDK;
-    static constexpr int W = K + kSimtMaxC * LDK;
-    static constexpr int U = W + kSimtMaxC * LDK;
-    static constexpr int S = U + kSimtMaxC * LDV;
-    static constexpr int A = S + DK * LDV;
+    static constexpr int KW = K + kSimtMaxC * LDK;     // write keys, if any
+    static constexpr int S = KW + kSimtMaxC * LDK;     // DK x DVT state slice
+    static constexpr int X = S + DK * LDV;             // V, then the residual
+    static constexpr int F = X + kSimtMaxC * LDV;      // Diag(beta) X
+    static constexpr int U = F + kSimtMaxC * LDV;      // U~
+    static constexpr int QS = U + kSimtMaxC * LDV;     // Q S
+    static constexpr int A = QS + kSimtMaxC * LDV;
     static constexpr int P = A + kSimtMaxC * LDC;
-    static constexpr int G = P + kSimtMaxC * LDC;      // cumulative log decay
+    static constexpr int TM = P + kSimtMaxC * LDC;     // A^{-1}
+    static constexpr int G = TM + kSimtMaxC * LDC;     // cumulative log decay
     static constexpr int BETA = G + kSimtMaxC;
-    static constexpr int KDEC = BETA + kSimtMaxC;      // exp(g_last - g_r)
-    static constexpr int KW = KDEC + kSimtMaxC;        // write keys, if any
-    static constexpr int TOTAL = KW + kSimtMaxC * LDK;
+    static constexpr int GAM = BETA + kSimtMaxC;       // exp(g_r)
+    static constexpr int KDEC = GAM + kSimtMaxC;       // exp(g_last - g_r)
+    static constexpr int TOTAL = KDEC + kSimtMaxC;
     static constexpr size_t BYTES = sizeof(float) * (size_t)TOTAL;
 };
 
@@ -54,19 +62,25 @@ template <int DK, int DVT, typename IO>
 __global__ void __launch_bounds__(kSimtThreads)
 kla_chunk_simt_kernel(FwdArgs a) {
     using L = SimtSmem<DK, DVT>;
+    constexpr int LDK = L::LDK, LDV = L::LDV, LDC = L::LDC;
+    constexpr int NCQ = DVT / 4;
     extern __shared__ float sm[];
     float* Qs = sm + L::Q;
     float* Ks = sm + L::K;
-    float* Ws = sm + L::W;
-    float* Us = sm + L::U;
-    float* Ss = sm + L::S;
-    float* As = sm + L::A;
-    float* Ps = sm + L::P;
-    float* gs = sm + L::G;
-    float* bs = sm + L::BETA;
-    float* kd = sm + L::KDEC;
     // write keys: a separate tensor when given, else the keys themselves
     float* KWs = a.kw ? sm + L::KW : Ks;
+    float* Ss = sm + L::S;
+    float* Xs = sm + L::X;
+    float* Fs = sm + L::F;
+    float* Us = sm + L::U;
+    float* QSs = sm + L::QS;
+    float* As = sm + L::A;
+    float* Ps = sm + L::P;
+    float* Tm = sm + L::TM;
+    float* gs = sm + L::G;
+    float* bs = sm + L::BETA;
+    float* gam = sm + L::GAM;
+    float* kd = sm + L::KDEC;
 
     const int bh = blockIdx.x;
     const int b = bh / a.H, h = bh % a.H;
@@ -82,7 +96,7 @@ kla_chunk_simt_kernel(FwdArgs a) {
     // initial state slice
     for (int idx = tid; idx < DK * DVT; idx += kSimtThreads) {
         const int c = idx / DVT, j = idx % DVT;
-        Ss[c * L::LDV + j] =
+        Ss[c * LDV + j] =
             a.h0 ? a.h0[((size_t)bh * DK + c) * dv + j0 + j] : 0.f;
     }
 
@@ -91,23 +105,21 @@ kla_chunk_simt_kernel(FwdArgs a) {
         for (int idx = tid; idx < C * DK; idx += kSimtThreads) {
             const int r = idx / DK, c = idx % DK;
             const int t = t0 + r;
-            float qv = 0.f, kv = 0.f;
+            float qv = 0.f, kv = 0.f, wv = 0.f;
             if (t < T) {
                 const size_t off = (((size_t)b * T + t) * H + h) * DK + c;
                 qv = to_f32(q[off]);
                 kv = to_f32(k[off]);
+                if (kwp) wv = to_f32(kwp[off]);
             }
-            Qs[r * L::LDK + c] = qv;
-            Ks[r * L::LDK + c] = kv;
-            if (kwp)
-                KWs[r * L::LDK + c] =
-                    t < T ? to_f32(kwp[(((size_t)b * T + t) * H + h) * DK + c])
-                          : 0.f;
+            Qs[r * LDK + c] = qv;
+            Ks[r * LDK + c] = kv;
+            if (kwp) KWs[r * LDK + c] = wv;
         }
         for (int idx = tid; idx < C * DVT; idx += kSimtThreads) {
             const int r = idx / DVT, j = idx % DVT;
             const int t = t0 + r;
-            Us[r * L::LDV + j] =
+            Xs[r * LDV + j] =
                 t < T ? to_f32(v[(((size_t)b * T + t) * H + h) * dv + j0 + j])
                       : 0.f;
         }
@@ -123,7 +135,7 @@ kla_chunk_simt_kernel(FwdArgs a) {
         if (tid < C) {   // n = k . (write key), ||k||^2 without write keys
             float n = 0.f;
             for (int c = 0; c < DK; ++c)
-                n = fmaf(Ks[tid * L::LDK + c], KWs[tid * L::LDK + c], n);
+                n = fmaf(Ks[tid * LDK + c], KWs[tid * LDK + c], n);
             const float denom = n + a.eps;
             if (!a.gdn) bs[tid] = denom == 0.f ? 0.f : bs[tid] / denom;
         }
@@ -135,92 +147,137 @@ kla_chunk_simt_kernel(FwdArgs a) {
             }
         }
         __syncthreads();
-        if (tid < C) kd[tid] = expf(gs[C - 1] - gs[tid]);
+        if (tid < C) {
+            gam[tid] = expf(gs[tid]);
+            kd[tid] = expf(gs[C - 1] - gs[tid]);
+        }
         if (a.ckpt) {   // the state this chunk starts from
             float* ck = a.ckpt + ((size_t)bh * ((T + C - 1) / C) + t0 / C) *
                                      DK * dv + j0;
             for (int idx = tid; idx < DK * DVT; idx += kSimtThreads) {
                 const int c = idx / DVT, j = idx % DVT;
-                ck[(size_t)c * dv + j] = Ss[c * L::LDV + j];
+                ck[(size_t)c * dv + j] = Ss[c * LDV + j];
             }
         }
 
-        // ---- A (strictly lower part scaled by beta) and P = Gamma o QK^T ----
-        for (int idx = tid; idx < C * C; idx += kSimtThreads) {
-            const int r = idx / C, i = idx % C;
-            float av = (i == r) ? 1.f : 0.f;
-            float pv = 0.f;
-            if (i <= r) {
-                float kk = 0.f, qk = 0.f;
-#pragma unroll 8
-                for (int c = 0; c < DK; ++c) {
-                    const float ki = KWs[i * L::LDK + c];   // write key i
-                    kk = fmaf(Ks[r * L::LDK + c], ki, kk);
-                    qk = fmaf(Qs[r * L::LDK + c], ki, qk);
+        // ---- A, P, T = A^{-1} ----
+        build_a_p<DK, kSimtThreads>(C, Qs, Ks, KWs, LDK, gs, bs, As, Ps, LDC);
+        __syncthreads();
+        invert_unit_lower<kSimtThreads>(As, Tm, C, LDC);
+
+        // ---- K S and Q S (2 x 4 tiles): X = V - Diag(gamma) K S,
+        // F = Diag(beta) X ----
+        for (int tile = tid; tile < (C / 2) * NCQ; tile += kSimtThreads) {
+            const int r0 = (tile / NCQ) * 2, q0 = (tile % NCQ) * 4;
+            float ks[2][4] = {}, qs[2][4] = {};
+#pragma unroll 4
+            for (int c = 0; c < DK; ++c) {
+                const float k0 = Ks[r0 * LDK + c], k1 = Ks[(r0 + 1) * LDK + c];
+                const float x0 = Qs[r0 * LDK + c], x1 = Qs[(r0 + 1) * LDK + c];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float sv = Ss[c * LDV + q0 + jj];
+                    ks[0][jj] = fmaf(k0, sv, ks[0][jj]);
+                    ks[1][jj] = fmaf(k1, sv, ks[1][jj]);
+                    qs[0][jj] = fmaf(x0, sv, qs[0][jj]);
+                    qs[1][jj] = fmaf(x1, sv, qs[1][jj]);
                 }
-                const float dec = expf(gs[r] - gs[i]);
-                pv = dec * qk;
-                if (i < r) av = bs[r] * dec * kk;
             }
-            As[r * L::LDC + i] = av;
-            Ps[r * L::LDC + i] = pv;
-        }
-        __syncthreads();
-
-        // ---- forward substitution: one thread per right-hand-side column --
-        if (tid < DVT + DK) {
-            const bool is_u = tid < DVT;
-            const int col = is_u ? tid : tid - DVT;
-            float* X = is_u ? Us : Ws;
-            const int ld = is_u ? L::LDV : L::LDK;
-            for (int r = 0; r < C; ++r) {
-                float x = is_u ? bs[r] * Us[r * L::LDV + col]
-                               : bs[r] * expf(gs[r]) * Ks[r * L::LDK + col];
-                for (int i = 0; i < r; ++i)
-                    x = fmaf(-As[r * L::LDC + i], X[i * ld + col], x);
-                X[r * ld + col] = x;
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = r0 + rr;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int j = q0 + jj;
+                    const float x = fmaf(-gam[r], ks[rr][jj], Xs[r * LDV + j]);
+                    Fs[r * LDV + j] = bs[r] * x;
+                    QSs[r * LDV + j] = qs[rr][jj];
+                }
             }
         }
         __syncthreads();
 
-        // ---- U~ = U - W S ----
-        for (int idx = tid; idx < C * DVT; idx += kSimtThreads) {
-            const int r = idx / DVT, j = idx % DVT;
-            float acc = Us[r * L::LDV + j];
-#pragma unroll 8
-            for (int c = 0; c < DK; ++c)
-                acc = fmaf(-Ws[r * L::LDK + c], Ss[c * L::LDV + j], acc);
-            Us[r * L::LDV + j] = acc;
+        // ---- U~ = T F ----
+        for (int tile = tid; tile < (C / 2) * NCQ; tile += kSimtThreads) {
+            const int r0 = (tile / NCQ) * 2, q0 = (tile % NCQ) * 4;
+            float u[2][4] = {};
+            for (int i = 0; i <= r0 + 1; ++i) {
+                const float t0v = i <= r0 ? Tm[r0 * LDC + i] : 0.f;
+                const float t1v = Tm[(r0 + 1) * LDC + i];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float f = Fs[i * LDV + q0 + jj];
+                    u[0][jj] = fmaf(t0v, f, u[0][jj]);
+                    u[1][jj] = fmaf(t1v, f, u[1][jj]);
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    Us[(r0 + rr) * LDV + q0 + jj] = u[rr][jj];
         }
         __syncthreads();
 
         // ---- O = Diag(gamma) Q S + P U~ (skipped when only the states are
         // wanted) ----
-        for (int idx = tid; o && idx < C * DVT; idx += kSimtThreads) {
-            const int r = idx / DVT, j = idx % DVT;
-            const int t = t0 + r;
-            float qs = 0.f;
-#pragma unroll 8
-            for (int c = 0; c < DK; ++c)
-                qs = fmaf(Qs[r * L::LDK + c], Ss[c * L::LDV + j], qs);
-            float acc = expf(gs[r]) * qs;
-            for (int i = 0; i <= r; ++i)
-                acc = fmaf(Ps[r * L::LDC + i], Us[i * L::LDV + j], acc);
-            if (t < T)
-                o[(((size_t)b * T + t) * H + h) * dv + j0 + j] =
-                    from_f32<IO>(acc);
+        for (int tile = tid; o && tile < (C / 2) * NCQ; tile += kSimtThreads) {
+            const int r0 = (tile / NCQ) * 2, q0 = (tile % NCQ) * 4;
+            float acc[2][4];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    acc[rr][jj] = gam[r0 + rr] * QSs[(r0 + rr) * LDV + q0 + jj];
+            for (int i = 0; i <= r0 + 1; ++i) {
+                const float p0 = i <= r0 ? Ps[r0 * LDC + i] : 0.f;
+                const float p1 = Ps[(r0 + 1) * LDC + i];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float u = Us[i * LDV + q0 + jj];
+                    acc[0][jj] = fmaf(p0, u, acc[0][jj]);
+                    acc[1][jj] = fmaf(p1, u, acc[1][jj]);
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int t = t0 + r0 + rr;
+                if (t >= T) continue;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    o[(((size_t)b * T + t) * H + h) * dv + j0 + q0 + jj] =
+                        from_f32<IO>(acc[rr][jj]);
+            }
         }
-        __syncthreads();
 
-        // ---- S = gamma_C S + (Diag(Gamma_C) K)^T U~ ----
-        const float gC = expf(gs[C - 1]);
-        for (int idx = tid; idx < DK * DVT; idx += kSimtThreads) {
-            const int c = idx / DVT, j = idx % DVT;
-            float acc = gC * Ss[c * L::LDV + j];
-            for (int r = 0; r < C; ++r)
-                acc = fmaf(kd[r] * KWs[r * L::LDK + c], Us[r * L::LDV + j],
-                           acc);
-            Ss[c * L::LDV + j] = acc;
+        // ---- S = gamma_C S + (Diag(Gamma_C) Kw)^T U~ (4 x 4 tiles) ----
+        const float gC = gam[C - 1];
+        for (int tile = tid; tile < (DK / 4) * NCQ; tile += kSimtThreads) {
+            const int c0 = (tile / NCQ) * 4, q0 = (tile % NCQ) * 4;
+            float acc[4][4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    acc[x][jj] = gC * Ss[(c0 + x) * LDV + q0 + jj];
+            for (int r = 0; r < C; ++r) {
+                float kv[4], u[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    kv[x] = kd[r] * KWs[r * LDK + c0 + x];
+                    u[x] = Us[r * LDV + q0 + x];
+                }
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        acc[x][jj] = fmaf(kv[x], u[jj], acc[x][jj]);
+            }
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    Ss[(c0 + x) * LDV + q0 + jj] = acc[x][jj];
         }
         __syncthreads();
     }
@@ -228,7 +285,7 @@ kla_chunk_simt_kernel(FwdArgs a) {
     if (a.hT) {
         for (int idx = tid; idx < DK * DVT; idx += kSimtThreads) {
             const int c = idx / DVT, j = idx % DVT;
-            a.hT[((size_t)bh * DK + c) * dv + j0 + j] = Ss[c * L::LDV + j];
+            a.hT[((size_t)bh * DK + c) * dv + j0 + j] = Ss[c * LDV + j];
         }
     }
 }

@@ -10,50 +10,149 @@
 // "preconditioned DeltaNet" page, section "Aproximacion Diagonal"; the tanh
 // squash centred on the mean log second moment is this library's reading).
 //
-// One CTA per (batch, head), one thread per key dimension, tokens in order
-// (A_t is a running sum); the mean over the key dimensions is a block
-// reduction per token.
+// The running sum is a prefix sum over tokens, so the sequence is split:
+// one cluster of kClusterCtas CTAs per (batch, head), each CTA taking one
+// contiguous slice of the tokens and each of its warps one sub-slice.  Pass 1
+// sums k^2 over every sub-slice; the sums that precede a warp (earlier warps
+// of the CTA from shared memory, earlier CTAs of the cluster from their
+// shared memory over the cluster's distributed shared memory) give its
+// starting A; pass 2 walks its tokens in order.  A lane holds dk / 32 key
+// dimensions (one when dk = 16), so the mean over the key dimensions is a
+// warp reduction.  No global scratch, one launch.
+#include <cooperative_groups.h>
+
 #include "kla_internal.cuh"
 
 namespace kla {
 namespace {
 
-constexpr int kPrecondThreads = 128;   // >= dk, a multiple of 32
+namespace cg = cooperative_groups;
 
-template <typename IO>
-__global__ void __launch_bounds__(kPrecondThreads)
-kla_precond_keys_kernel(PrecondArgs a) {
-    __shared__ float part[kPrecondThreads / 32];
-    const int bh = blockIdx.x;
+constexpr int kClusterCtas = 8;
+constexpr int kPrecondWarps = 32;
+constexpr int kPrecondThreads = kPrecondWarps * 32;
+constexpr int kTokBatch = 4;   // tokens loaded ahead of their use
+
+template <int DK, typename IO>
+__global__ void __cluster_dims__(kClusterCtas, 1, 1)
+    __launch_bounds__(kPrecondThreads, 1)
+    kla_precond_keys_kernel(PrecondArgs a) {
+    constexpr int DPL = DK >= 32 ? DK / 32 : 1;   // dimensions per lane
+    constexpr int LANES = DK / DPL;               // lanes holding dimensions
+    __shared__ float wsum[kPrecondWarps][DK];     // sum of k^2 per sub-slice
+    __shared__ float ctot[DK];                    // ... per CTA slice
+    __shared__ float base[DK];                    // A before this CTA's slice
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int bh = blockIdx.x / kClusterCtas;
     const int b = bh / a.H, h = bh % a.H;
-    const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
-    const int dk = a.dk, T = a.T, H = a.H;
-    const int nwarps = (dk + 31) / 32;
-    const bool live = i < dk;
-    const float lx = logf(a.x);
-    float A = (live && a.A0) ? a.A0[(size_t)bh * dk + i] : 0.f;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = a.T, H = a.H;
+    const bool live = lane < LANES;
+    const int d0 = lane * DPL;
+
+    // this warp's tokens [t_lo, t_hi)
+    const int per_cta = (T + kClusterCtas - 1) / kClusterCtas;
+    const int per_warp = (per_cta + kPrecondWarps - 1) / kPrecondWarps;
+    const int c_lo = min(T, rank * per_cta);
+    const int c_hi = min(T, c_lo + per_cta);
+    const int t_lo = min(c_hi, c_lo + warp * per_warp);
+    const int t_hi = min(c_hi, t_lo + per_warp);
+
     const IO* k = static_cast<const IO*>(a.k);
     IO* kw = static_cast<IO*>(a.kw);
+    auto row = [&](int t) {
+        return (((size_t)b * T + t) * H + h) * DK + d0;
+    };
 
-    for (int t = 0; t < T; ++t) {
-        const size_t off = (((size_t)b * T + t) * H + h) * dk + i;
-        const float kv = live ? to_f32(k[off]) : 0.f;
-        A = fmaf(kv, kv, A);
-        const float l = live ? logf(A + a.delta) : 0.f;
-        float s = l;
+    // ---- pass 1: sum of k^2 over the sub-slice ----
+    float sq[DPL] = {};
+    for (int t = t_lo; t < t_hi; t += kTokBatch) {
+        float kv[kTokBatch][DPL];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0 && warp < nwarps) part[warp] = s;
-        __syncthreads();
-        float tot = 0.f;
-        for (int w = 0; w < nwarps; ++w) tot += part[w];
-        __syncthreads();
-        if (live) {
-            const float z = tot / (float)dk - l;
-            kw[off] = from_f32<IO>(expf(lx * tanhf(z / lx)) * kv);
+        for (int u = 0; u < kTokBatch; ++u)
+#pragma unroll
+            for (int d = 0; d < DPL; ++d)
+                kv[u][d] = (live && t + u < t_hi) ? to_f32(k[row(t + u) + d])
+                                                  : 0.f;
+#pragma unroll
+        for (int u = 0; u < kTokBatch; ++u)
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) sq[d] = fmaf(kv[u][d], kv[u][d], sq[d]);
+    }
+    if (live) {
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) wsum[warp][d0 + d] = sq[d];
+    }
+    __syncthreads();
+    if (tid < DK) {
+        float s = 0.f;
+        for (int w = 0; w < kPrecondWarps; ++w) s += wsum[w][tid];
+        ctot[tid] = s;
+    }
+    cluster.sync();   // every CTA's slice total is visible cluster-wide
+    if (tid < DK) {
+        float s = a.A0 ? a.A0[(size_t)bh * DK + tid] : 0.f;
+        for (int r = 0; r < rank; ++r) s += cluster.map_shared_rank(ctot, r)[tid];
+        base[tid] = s;
+        if (rank == kClusterCtas - 1 && a.AT)
+            a.AT[(size_t)bh * DK + tid] = s + ctot[tid];
+    }
+    cluster.sync();   // remote reads done (no CTA leaves while read); base set
+
+    // ---- pass 2: the sub-slice's tokens in order ----
+    float A[DPL];
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) {
+        float s = live ? base[d0 + d] : 0.f;
+        for (int w = 0; w < warp; ++w) s += live ? wsum[w][d0 + d] : 0.f;
+        A[d] = s;
+    }
+    const float lx = logf(a.x);
+    const float inv_dk = 1.f / (float)DK;
+    for (int t = t_lo; t < t_hi; t += kTokBatch) {
+        float kv[kTokBatch][DPL];
+#pragma unroll
+        for (int u = 0; u < kTokBatch; ++u)
+#pragma unroll
+            for (int d = 0; d < DPL; ++d)
+                kv[u][d] = (live && t + u < t_hi) ? to_f32(k[row(t + u) + d])
+                                                  : 0.f;
+#pragma unroll
+        for (int u = 0; u < kTokBatch; ++u) {
+            if (t + u >= t_hi) break;   // warp-uniform
+            float l[DPL], s = 0.f;
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) {
+                A[d] = fmaf(kv[u][d], kv[u][d], A[d]);
+                l[d] = live ? logf(A[d] + a.delta) : 0.f;
+                s += l[d];
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (live) {
+                const float mean = s * inv_dk;
+#pragma unroll
+                for (int d = 0; d < DPL; ++d)
+                    kw[row(t + u) + d] = from_f32<IO>(
+                        expf(lx * tanhf((mean - l[d]) / lx)) * kv[u][d]);
+            }
         }
     }
-    if (live && a.AT) a.AT[(size_t)bh * dk + i] = A;
+}
+
+template <int DK>
+cudaError_t launch_dk(const PrecondArgs& a, cudaStream_t stream) {
+    const unsigned grid = (unsigned)((long)a.B * a.H * kClusterCtas);
+    if (a.dtype == KLA_BF16)
+        kla_precond_keys_kernel<DK, __nv_bfloat16>
+            <<<grid, kPrecondThreads, 0, stream>>>(a);
+    else
+        kla_precond_keys_kernel<DK, float>
+            <<<grid, kPrecondThreads, 0, stream>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -61,14 +160,14 @@ kla_precond_keys_kernel(PrecondArgs a) {
 cudaError_t launch_precond_keys(const PrecondArgs& a, cudaStream_t stream) {
     const long bhs = (long)a.B * a.H;
     if (bhs == 0) return cudaSuccess;
-    if (a.dk > kPrecondThreads) return cudaErrorInvalidValue;
-    if (a.dtype == KLA_BF16)
-        kla_precond_keys_kernel<__nv_bfloat16>
-            <<<(unsigned)bhs, kPrecondThreads, 0, stream>>>(a);
-    else
-        kla_precond_keys_kernel<float>
-            <<<(unsigned)bhs, kPrecondThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    if (bhs * kClusterCtas > 0x7fffffffL) return cudaErrorInvalidValue;
+    switch (a.dk) {
+        case 16: return launch_dk<16>(a, stream);
+        case 32: return launch_dk<32>(a, stream);
+        case 64: return launch_dk<64>(a, stream);
+        case 128: return launch_dk<128>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace kla

@@ -51,7 +51,11 @@ def dev(inp):
 
 @pytest.mark.parametrize("w,sizes", [
     (gen.TINY, dict(T=50)),
+    (gen.TINY, dict(T=0)),
+    (replace(gen.TINY, dk=32, dv=32), dict(T=777)),
+    (replace(gen.TINY, dk=64), dict(B=1, T=1029, H=3)),
     (gen.LAYER_1B, dict(B=2, T=300, H=2)),
+    (gen.LAYER_1B, dict(B=1, T=4100, H=2)),
 ])
 def test_write_keys_and_second_moments(w, sizes):
     inp = aniso(gen.prefill_inputs(w, **sizes), 1)
@@ -66,6 +70,9 @@ def test_write_keys_and_second_moments(w, sizes):
                                           inp["eps"], None, A0=A0, x=X,
                                           delta=DELTA)
     tol = TOL[inp["k"].dtype]
+    if T == 0:
+        assert torch.equal(AT.cpu(), A0)
+        return
     assert rel_err(kw, kw_ref) <= tol
     assert rel_err(AT, A_ref) <= 1e-5
 

@@ -40,6 +40,8 @@
 
 #include <mutex>
 
+#include <atomic>
+
 #include "kla_internal.cuh"
 #include "tc_primitives.cuh"
 
@@ -141,9 +143,9 @@ struct TcParams {
     const float* log_alpha;
     const float* eta;
     const float* h0;
-    __nv_bfloat16* o;      // may be null (only the states are wanted)
+    __nv_bfloat16* o;      // null in checkpoint mode
     float* hT;
-    float* ckpt;           // may be null: the state at every chunk start
+    float* ckpt;           // checkpoint mode: the state at every chunk start
     float eps;
     int gdn;
     int T, H;
@@ -452,6 +454,10 @@ __device__ __forceinline__ void unpack_bf16x2(uint32_t u, float& lo, float& hi) 
     hi = __uint_as_float(u & 0xffff0000u);
 }
 
+// kCkpt: write the state at every chunk start (p.ckpt) instead of o; the
+// two modes are separate instantiations so that neither carries the other's
+// code.
+template <bool kCkpt>
 __global__ void __launch_bounds__(kThreads, 1)
 kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -797,11 +803,12 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         uint32_t last_par = 0;
         // o of chunk cc = gamma Q S + P U~ (warps 6, 7: lanes 64..127)
         auto write_o = [&](int cc) {
+            if constexpr (kCkpt) return;   // only the states are wanted
             const int r = row - kC;
             const float gam = gbuf[(cc & 3) * kGBufStride + 3 * kC + r];
             const int t = cc * kC + r;
             __nv_bfloat16* dst = p.o + (((size_t)b * T + t) * p.H + h) * kD + j0;
-            const bool store = t < T && p.o != nullptr;
+            const bool store = t < T;
 #pragma unroll 1
             for (int jj = 0; jj < 4; ++jj) {   // 16 columns a step
                 float qs[16], x[16];
@@ -829,7 +836,7 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             const uint32_t sst = sbase + s * kStage;
             const float* gb = gbuf + (c & 3) * kGBufStride;
             const uint32_t tu = sbase + kTU + (c & 1) * kTUStride;
-            if (p.ckpt) {   // the state chunk c starts from (fp32)
+            if constexpr (kCkpt) {   // the state chunk c starts from (fp32)
                 float* dst = p.ckpt + (((size_t)bh * nchunks + c) * kD + row) *
                                           kD + j0;
 #pragma unroll
@@ -1063,19 +1070,27 @@ cudaError_t launch_chunk_tc(const FwdArgs& a, cudaStream_t stream) {
         !make_map(&mk, a.k, a.B, a.T, a.H) ||
         !make_map(&mv, a.v, a.B, a.T, a.H))
         return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(
-            kla_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-            kSmemBytes);
+    // exactly one of o (the forward) and ckpt (the backward's checkpoints)
+    if ((a.o == nullptr) == (a.ckpt == nullptr)) return cudaErrorInvalidValue;
+    const bool ckpt = a.ckpt != nullptr;
+    auto kern = ckpt ? kla_chunk_tc_kernel<true> : kla_chunk_tc_kernel<false>;
+    // the shared-memory opt-in, once per (instantiation, device)
+    static std::atomic<unsigned long long> attr_done[2];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (!bit || !(attr_done[ckpt].load() & bit)) {
+        e = cudaFuncSetAttribute(
+            kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_done[ckpt].fetch_or(bit);
     }
     TcParams p{a.log_alpha, a.eta, a.h0,
                static_cast<__nv_bfloat16*>(a.o), a.hT, a.ckpt, a.eps, a.gdn,
                a.T, a.H};
     dim3 grid((unsigned)((long)a.B * a.H), kD / kNV);
-    kla_chunk_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
     return cudaGetLastError();
 }
 

@@ -37,7 +37,8 @@ struct FwdArgs {
     int B, T, H, dk, dv, C;
     kla_dtype dtype;
     // may be null: the state at the start of every chunk, fp32
-    // [B, H, ceil(T / C), dk, dv]
+    // [B, H, ceil(T / C), dk, dv] (the tensor-core kernel takes exactly one
+    // of o and ckpt)
     float* ckpt = nullptr;
     // may be null: separate write keys [B, T, H, dk] (the CUDA-core kernel
     // only); null means the write key is k

@@ -737,11 +737,13 @@ kla_bwd_grad_kernel(BwdArgs a) {
     }
 }
 
-template <int DK, int DVT, typename IO>
+// DVS: dv columns per CTA of the reverse state recurrence; DVT: dv columns
+// per step of the gradient kernel.
+template <int DK, int DVS, int DVT, typename IO>
 cudaError_t launch_shape(const BwdArgs& a, cudaStream_t stream) {
-    using LS = StateSmem<DK, DVT>;
+    using LS = StateSmem<DK, DVS>;
     using LG = GradSmem<DK, DVT>;
-    auto ks = kla_bwd_state_kernel<DK, DVT, IO>;
+    auto ks = kla_bwd_state_kernel<DK, DVS, IO>;
     auto kg = kla_bwd_grad_kernel<DK, DVT, IO>;
     cudaError_t e = cudaFuncSetAttribute(
         ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LS::BYTES);
@@ -751,7 +753,7 @@ cudaError_t launch_shape(const BwdArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const long bhs = (long)a.B * a.H;
     const long nch = (a.T + a.C - 1) / a.C;
-    ks<<<dim3((unsigned)bhs, (unsigned)(a.dv / DVT)), kBwdThreads, LS::BYTES,
+    ks<<<dim3((unsigned)bhs, (unsigned)(a.dv / DVS)), kBwdThreads, LS::BYTES,
          stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -761,10 +763,20 @@ cudaError_t launch_shape(const BwdArgs& a, cudaStream_t stream) {
 
 template <typename IO>
 cudaError_t launch_dtype(const BwdArgs& a, cudaStream_t stream) {
+    // The reverse state recurrence is one CTA per (batch, head, dv slice),
+    // sequential over the chunks: 64-column slices when 32-column ones
+    // would need more than one wave of CTAs (one CTA per SM).
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const bool wide = a.dv >= 64 && (long)a.B * a.H * (a.dv / 32) > sms;
 #define KLA_BWD_DK(DKV)                                                     \
     if (a.dk == DKV) {                                                      \
-        if (a.dv == 16) return launch_shape<DKV, 16, IO>(a, stream);        \
-        return launch_shape<DKV, 32, IO>(a, stream);                        \
+        if (a.dv == 16) return launch_shape<DKV, 16, 16, IO>(a, stream);    \
+        if (wide) return launch_shape<DKV, 64, 32, IO>(a, stream);          \
+        return launch_shape<DKV, 32, 32, IO>(a, stream);                    \
     }
     KLA_BWD_DK(16)
     KLA_BWD_DK(32)

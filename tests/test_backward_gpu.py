@@ -94,6 +94,16 @@ def test_fp32_head_dims(dk, dv):
     check(inp, do, dhT, 32)
 
 
+def test_fp32_many_heads_wide_state_slices():
+    """B*H = 80 heads of dk = dv = 64: more (head, 32-column) slices than a
+    GB300 has SMs, so the reverse state recurrence runs 64-column slices."""
+    from dataclasses import replace
+    w = replace(gen.TINY, dk=64, dv=64, h0_std=0.3)
+    inp = gen.prefill_inputs(w, B=2, T=70, H=40)
+    do, dhT = upstream(inp, 41)
+    check(inp, do, dhT, 32)
+
+
 @pytest.mark.parametrize("rule", ["kaczmarz", "given"])
 def test_bf16_d128(rule):
     inp = gen.prefill_inputs(gen.LAYER_1B, B=1, T=200, H=2)

@@ -422,8 +422,9 @@ def bench_backward(w, inp, steps, warmup, world):
 
 def bench_precond(w, inp, steps, warmup, world):
     """The diagonal-preconditioned variant on the forward's inputs: the
-    write-key scan plus the two-key forward (CUDA-core kernel), beside the
-    plain forward on the same CUDA-core kernel."""
+    write-key scan plus the two-key forward (the tensor-core kernel's
+    write-key mode for bf16 d128 C64, else the CUDA-core kernel), beside the
+    plain forward on the same path."""
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
          for k, v in inp.items()}
     o = torch.empty_like(d["v"])
@@ -434,7 +435,7 @@ def bench_precond(w, inp, steps, warmup, world):
 
     def plain():
         kla.chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["eta"],
-                      d["eps"], d["h0"], C=w.C, o=o, hT=hT, algo="simt")
+                      d["eps"], d["h0"], C=w.C, o=o, hT=hT)
 
     def keys():
         kla.precond_keys(d["k"], k_write=kw, want_AT=False)
@@ -705,26 +706,30 @@ def run_ours(args):
 
     precond = None
     if not args.no_precond:
-        t_plain, t_keys, t_fwd = bench_precond(w, pf["inputs"], 3, 2, world)
-        alu_peak, sms, mhz = fp32_alu_peak_tflops(
-            (pf["clocks"] or {}).get("sm_max_mhz"))
-        ach = prefill_flops(w) / ((t_keys + t_fwd) * 1e-3) / 1e12
+        t_plain, t_keys, t_fwd = bench_precond(w, pf["inputs"], 10, 3, world)
+        esz = 2 if w.dtype == "bf16" else 4
+        kw_bytes = esz * w.B * w.T * w.H * w.dk        # the write keys
+        fwd_bytes = prefill_bytes(w) + kw_bytes        # + kw read once
+        fwd_gbs = fwd_bytes / (t_fwd * 1e-3) / 1e9
         precond = {"workload": w.name,
                    "variant": "diagonal preconditioner on the write key "
                               "(x = 1.5), Kaczmarz step",
                    "write_keys_ms": round(t_keys, 4),
+                   "write_keys_gbs": round(2 * kw_bytes / (t_keys * 1e-3)
+                                           / 1e9, 1),
                    "forward_ms": round(t_fwd, 4),
                    "tokens_per_s": round(world * tokens /
                                          ((t_keys + t_fwd) * 1e-3), 1),
-                   "plain_same_kernel_ms": round(t_plain, 4),
+                   "plain_forward_ms": round(t_plain, 4),
                    "overhead_vs_plain": round((t_keys + t_fwd) / t_plain, 4),
                    "kernels": "kla_precond_keys + kla_chunk_fwd_kw "
-                              "(CUDA-core fp32)",
-                   "roofline": {"bound": "alu", "achieved": round(ach, 2),
-                                "peak": round(alu_peak, 1),
-                                "unit": "TFLOP/s",
-                                "frac": round(ach / alu_peak, 4)},
-                   "timed_steps": 3}
+                              "(tensor-core kernel, write-key mode)",
+                   "roofline": {"bound": "hbm", "kernel": "two-key forward",
+                                "achieved": round(fwd_gbs, 1),
+                                "peak": hbm, "unit": "GB/s",
+                                "frac": round(fwd_gbs / hbm, 4),
+                                "algorithmic_bytes_per_launch": fwd_bytes},
+                   "timed_steps": 10}
 
     longctx = None
     if not args.no_long:

@@ -189,8 +189,11 @@ KLA_API kla_status kla_precond_keys(const void* k, const float* A0,
  * ([B, T, H, dk], dtype, read; e.g. from kla_precond_keys): the chunkwise
  * form with A = I + strict_lower(Diag(beta)(Gamma o K Kw^T)),
  * P = Gamma o Q Kw^T and the state written along Kw, the residual read along
- * K.  Runs on the CUDA-core kernel.  k_write must not alias o.  Errors as
- * for kla_chunk_fwd_ex (NULL k_write is KLA_ERR_INVALID_ARG).
+ * K.  Runs on the tensor-core kernel (its write-key mode) where
+ * kla_chunk_fwd_ex's KLA_ALGO_AUTO would (bf16, dk = dv = 128, C = 64,
+ * 16-byte-aligned tensors, k_write included), else on the CUDA-core kernel.
+ * k_write must not alias o.  Errors as for kla_chunk_fwd_ex (NULL k_write is
+ * KLA_ERR_INVALID_ARG).
  */
 KLA_API kla_status kla_chunk_fwd_kw(const void* q, const void* k,
                                     const void* k_write, const void* v,

@@ -74,7 +74,7 @@ static kla_status chunk_fwd_impl(const void* q, const void* k, const void* kw,
                    rule == KLA_STEP_GIVEN ? 1 : 0, h0, o, hT,
                    B, T, H, dk, dv, C, dtype};
     a.kw = kw;
-    const bool tc_ok = !kw && kla::chunk_tc_eligible(a);
+    const bool tc_ok = kla::chunk_tc_eligible(a);
     if (algo == KLA_ALGO_TC) {
         if (!tc_ok) return KLA_ERR_UNSUPPORTED_SHAPE;
         return from_cuda(kla::launch_chunk_tc(a, s));
@@ -107,7 +107,7 @@ extern "C" kla_status kla_chunk_fwd_kw(const void* q, const void* k,
                                        kla_stream_t stream) {
     if (!k_write && (long long)B * H > 0 && T > 0) return KLA_ERR_INVALID_ARG;
     return chunk_fwd_impl(q, k, k_write, v, log_alpha, eta, eps, h0, o, hT, B,
-                          T, H, dk, dv, C, dtype, KLA_ALGO_SIMT, rule, stream);
+                          T, H, dk, dv, C, dtype, KLA_ALGO_AUTO, rule, stream);
 }
 
 extern "C" kla_status kla_precond_keys(const void* k, const float* A0,

@@ -66,6 +66,13 @@ constexpr int kOffQ = 8192;
 constexpr int kHalf = 16384;
 constexpr int kOffV = 32768;
 constexpr int kStage = 40960;
+// With separate write keys (the preconditioned variant) a stage also holds
+// KW_0 | KW_1 (64 rows x 128 B each, like K_h) and the ring is two deep, in
+// the same 120 KB.
+constexpr int kOffKW = 40960;
+constexpr int kStageKW = 57344;
+constexpr int kNSKW = 2;
+static_assert(kNSKW * kStageKW <= kNS * kStage, "write-key ring");
 constexpr int kSBuf = kNS * kStage;          // bf16 S, 128 x 64, MN-major
 constexpr int kTU = kSBuf + 16384;           // 2 x {TU | P}, by chunk parity
 constexpr int kTUStride = 16384;             // TU, P: 64 x 64 K-major each
@@ -100,6 +107,7 @@ static_assert(kBars % 8 == 0, "mbarrier alignment");
 static_assert(kTU % 1024 == 0 && kUtBuf % 1024 == 0 &&
               kUtsBuf % 1024 == 0 && kSBuf % 1024 == 0, "operand alignment");
 constexpr uint32_t kTmaBytes = 2 * 16384 + 8192;
+constexpr uint32_t kTmaBytesKW = kTmaBytes + 16384;
 
 // mbarrier slots (all with one arrival per phase)
 constexpr int kBarTma = 0;       // kNS: stage full (TMA)
@@ -454,14 +462,19 @@ __device__ __forceinline__ void unpack_bf16x2(uint32_t u, float& lo, float& hi) 
     hi = __uint_as_float(u & 0xffff0000u);
 }
 
-// kCkpt: write the state at every chunk start (p.ckpt) instead of o; the
-// two modes are separate instantiations so that neither carries the other's
-// code.
-template <bool kCkpt>
+// kCkpt: write the state at every chunk start (p.ckpt) instead of o.
+// kKW: separate write keys (tm_kw): G = [K;Q] Kw^T (so beta's denominator is
+// k . kw, A uses K Kw^T and P uses Q Kw^T) and dS = Kw^T Diag(Gamma_C) U~;
+// the residual still reads K S.  The modes are separate instantiations so
+// that none carries another's code.
+template <bool kCkpt, bool kKW>
 __global__ void __launch_bounds__(kThreads, 1)
 kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, TcParams p) {
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_kw, TcParams p) {
+    constexpr int NS = kKW ? kNSKW : kNS;            // ring depth
+    constexpr int STAGE = kKW ? kStageKW : kStage;   // bytes per stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -485,6 +498,7 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc::prefetch_tmap(&tm_q);
         tc::prefetch_tmap(&tm_k);
         tc::prefetch_tmap(&tm_v);
+        if constexpr (kKW) tc::prefetch_tmap(&tm_kw);
         for (int i = 0; i < kNumBars; ++i) tc::mbar_init(&bars[i], 1);
         *abort_flag = 0;
         *tma_issued = 0;
@@ -520,11 +534,15 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t tmem = *tmem_slot;
 
     auto issue_tma = [&](int c) {
-        const int s = c % kNS;
-        uint8_t* st = sm + s * kStage;
+        const int s = c % NS;
+        uint8_t* st = sm + s * STAGE;
         const int t0 = c * kC;
         uint64_t* bar = &bars[kBarTma + s];
-        tc::mbar_arrive_expect_tx(bar, kTmaBytes);
+        tc::mbar_arrive_expect_tx(bar, kKW ? kTmaBytesKW : kTmaBytes);
+        if constexpr (kKW) {
+            tc::tma_load_4d(st + kOffKW, &tm_kw, bar, 0, h, t0, b);
+            tc::tma_load_4d(st + kOffKW + 8192, &tm_kw, bar, 64, h, t0, b);
+        }
         tc::tma_load_4d(st, &tm_k, bar, 0, h, t0, b);
         tc::tma_load_4d(st + kOffQ, &tm_q, bar, 0, h, t0, b);
         tc::tma_load_4d(st + kHalf, &tm_k, bar, 64, h, t0, b);
@@ -539,22 +557,28 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc::tma_prefetch_4d(&tm_k, 64, h, t0, b);
         tc::tma_prefetch_4d(&tm_q, 64, h, t0, b);
         tc::tma_prefetch_4d(&tm_v, j0, h, t0, b);
+        if constexpr (kKW) {
+            tc::tma_prefetch_4d(&tm_kw, 0, h, t0, b);
+            tc::tma_prefetch_4d(&tm_kw, 64, h, t0, b);
+        }
     };
-    // G = [K; Q] K^T of chunk c into G[c & 1]
+    // G = [K; Q] K^T (or [K; Q] Kw^T) of chunk c into G[c & 1]
     auto issue_g = [&](int c) {
-        const uint32_t sst = sbase + (c % kNS) * kStage;
+        const uint32_t sst = sbase + (c % NS) * STAGE;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-            tc::mma_bf16(tmem + col_g(c), desc_k(sst + off), desc_k(sst + off),
-                         kIdG, ks > 0);
+            const uint32_t offb =
+                kKW ? kOffKW + (ks >> 2) * 8192 + (ks & 3) * 32 : off;
+            tc::mma_bf16(tmem + col_g(c), desc_k(sst + off),
+                         desc_k(sst + offb), kIdG, ks > 0);
         }
         tc::mma_commit(&bars[kBarG + (c & 1)]);
     };
     if (tid == 0) {
-        for (int c = 0; c < kNS && c < nchunks; ++c) issue_tma(c);
-        *tma_issued = nchunks < kNS ? nchunks : kNS;
-        for (int c = kNS; c < kNS + kPrefetch && c < nchunks; ++c)
+        for (int c = 0; c < NS && c < nchunks; ++c) issue_tma(c);
+        *tma_issued = nchunks < NS ? nchunks : NS;
+        for (int c = NS; c < NS + kPrefetch && c < nchunks; ++c)
             prefetch_l2(c);
     }
 
@@ -705,8 +729,8 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const bool gok =
                     tc::mbar_wait_or_abort(&bars[kBarPDone + ((c + 1) & 1)],
                                            ((c - 1) >> 1) & 1, abort_flag) &&
-                    tc::mbar_wait_or_abort(&bars[kBarTma + (c + 1) % kNS],
-                                           ((c + 1) / kNS) & 1, abort_flag);
+                    tc::mbar_wait_or_abort(&bars[kBarTma + (c + 1) % NS],
+                                           ((c + 1) / NS) & 1, abort_flag);
                 if (gok) {
                     tc::tc_fence_after();
                     issue_g(c + 1);
@@ -832,8 +856,8 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
         };
         for (int c = 0; c < nchunks && !failed; ++c) {
-            const int s = c % kNS;
-            const uint32_t sst = sbase + s * kStage;
+            const int s = c % NS;
+            const uint32_t sst = sbase + s * STAGE;
             const float* gb = gbuf + (c & 3) * kGBufStride;
             const uint32_t tu = sbase + kTU + (c & 1) * kTUStride;
             if constexpr (kCkpt) {   // the state chunk c starts from (fp32)
@@ -846,7 +870,7 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
             bool ok = true;
             if (sw < 2)   // the stage of chunk c (warps 6, 7 do not read it)
-                ok = team_wait(&bars[kBarTma + s], (c / kNS) & 1, abort_flag,
+                ok = team_wait(&bars[kBarTma + s], (c / NS) & 1, abort_flag,
                                kBarState01, 64);
             tc::tc_fence_after();
             if (ok && tid == 128) {   // [K; Q] S: K S lanes 0..63, Q S 64..127
@@ -868,7 +892,7 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 if (ok) {
                     tc::tc_fence_after();
                     const float gam = gb[3 * kC + row];
-                    uint8_t* vrow = sm + s * kStage + kOffV + row * 128;
+                    uint8_t* vrow = sm + s * STAGE + kOffV + row * 128;
 #pragma unroll 1
                     for (int jj = 0; jj < 4; ++jj) {   // 16 columns a step
                         float x[16];
@@ -945,7 +969,9 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (tid == 128) {   // dS = K^T Diag(Gamma_C) U~, then P U~
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tmem + kColDS, desc_mn(sst + ks * 2048, kHalf),
+                    tc::mma_bf16(tmem + kColDS,
+                                 kKW ? desc_mn(sst + kOffKW + ks * 2048, 8192)
+                                     : desc_mn(sst + ks * 2048, kHalf),
                                  desc_mn(sbase + kUtsBuf + ks * 2048, 0), kIdDS,
                                  ks > 0);
                 tc::mma_commit(&bars[kBarDS]);
@@ -972,11 +998,11 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             tc::fence_proxy_async_smem();
             tc::tc_fence_before();
             tc::named_bar_sync(kBarState, 128);
-            if (tid == 224 && c + kNS < nchunks) {
-                issue_tma(c + kNS);
-                *reinterpret_cast<volatile int*>(tma_issued) = c + kNS + 1;
-                if (c + kNS + kPrefetch < nchunks)
-                    prefetch_l2(c + kNS + kPrefetch);
+            if (tid == 224 && c + NS < nchunks) {
+                issue_tma(c + NS);
+                *reinterpret_cast<volatile int*>(tma_issued) = c + NS + 1;
+                if (c + NS + kPrefetch < nchunks)
+                    prefetch_l2(c + NS + kPrefetch);
             }
         }
         if (!failed && sw >= 2 && nchunks > 0) {   // o of the last chunk
@@ -997,10 +1023,10 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (any_failed) {
         if (tid == 0) {
             atomicOr(&g_fault_word, 1u);
-            // copies possibly in flight: the last kNS chunks issued
+            // copies possibly in flight: the last NS chunks issued
             const int n = *reinterpret_cast<volatile int*>(tma_issued);
-            for (int c = n - kNS < 0 ? 0 : n - kNS; c < n; ++c)
-                tc::mbar_wait(&bars[kBarTma + c % kNS], (c / kNS) & 1,
+            for (int c = n - NS < 0 ? 0 : n - NS; c < n; ++c)
+                tc::mbar_wait(&bars[kBarTma + c % NS], (c / NS) & 1,
                               100000000ull);
         }
     } else if (tid >= 128 && p.hT) {
@@ -1059,38 +1085,43 @@ bool chunk_tc_eligible(const FwdArgs& a) {
     return a.dtype == KLA_BF16 && a.dk == kD && a.dv == kD && a.C == kC &&
            aligned16(a.q) && aligned16(a.k) && aligned16(a.v) &&
            aligned16(a.o) && (!a.h0 || aligned16(a.h0)) &&
-           (!a.hT || aligned16(a.hT)) && get_encoder();
+           (!a.hT || aligned16(a.hT)) && aligned16(a.kw) && get_encoder();
 }
 
 cudaError_t launch_chunk_tc(const FwdArgs& a, cudaStream_t stream) {
     if ((long)a.B * a.H == 0 || a.T == 0) return cudaSuccess;
     if (!get_encoder()) return cudaErrorNotSupported;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mkw;
     if (!make_map(&mq, a.q, a.B, a.T, a.H) ||
         !make_map(&mk, a.k, a.B, a.T, a.H) ||
-        !make_map(&mv, a.v, a.B, a.T, a.H))
+        !make_map(&mv, a.v, a.B, a.T, a.H) ||
+        !make_map(&mkw, a.kw ? a.kw : a.k, a.B, a.T, a.H))
         return cudaErrorInvalidValue;
-    // exactly one of o (the forward) and ckpt (the backward's checkpoints)
+    // exactly one of o (the forward) and ckpt (the backward's checkpoints);
+    // write keys only in the forward
     if ((a.o == nullptr) == (a.ckpt == nullptr)) return cudaErrorInvalidValue;
-    const bool ckpt = a.ckpt != nullptr;
-    auto kern = ckpt ? kla_chunk_tc_kernel<true> : kla_chunk_tc_kernel<false>;
+    if (a.kw && a.ckpt) return cudaErrorInvalidValue;
+    const int mode = a.ckpt ? 1 : a.kw ? 2 : 0;
+    auto kern = mode == 1   ? kla_chunk_tc_kernel<true, false>
+                : mode == 2 ? kla_chunk_tc_kernel<false, true>
+                            : kla_chunk_tc_kernel<false, false>;
     // the shared-memory opt-in, once per (instantiation, device)
-    static std::atomic<unsigned long long> attr_done[2];
+    static std::atomic<unsigned long long> attr_done[3];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
-    if (!bit || !(attr_done[ckpt].load() & bit)) {
+    if (!bit || !(attr_done[mode].load() & bit)) {
         e = cudaFuncSetAttribute(
             kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_done[ckpt].fetch_or(bit);
+        attr_done[mode].fetch_or(bit);
     }
     TcParams p{a.log_alpha, a.eta, a.h0,
                static_cast<__nv_bfloat16*>(a.o), a.hT, a.ckpt, a.eps, a.gdn,
                a.T, a.H};
     dim3 grid((unsigned)((long)a.B * a.H), kD / kNV);
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mkw, p);
     return cudaGetLastError();
 }
 

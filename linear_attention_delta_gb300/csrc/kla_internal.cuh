@@ -40,8 +40,8 @@ struct FwdArgs {
     // [B, H, ceil(T / C), dk, dv] (the tensor-core kernel takes exactly one
     // of o and ckpt)
     float* ckpt = nullptr;
-    // may be null: separate write keys [B, T, H, dk] (the CUDA-core kernel
-    // only); null means the write key is k
+    // may be null: separate write keys [B, T, H, dk]; null means the write
+    // key is k
     const void* kw = nullptr;
 };
 

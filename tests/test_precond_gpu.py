@@ -95,8 +95,11 @@ def test_forward_fp32(rule, C, T):
 
 
 @pytest.mark.parametrize("rule", ["kaczmarz", "given"])
-def test_forward_bf16_d128(rule):
-    inp = aniso(gen.prefill_inputs(gen.LAYER_1B, B=1, T=400, H=2), 4)
+@pytest.mark.parametrize("T", [50, 128, 400])
+def test_forward_bf16_d128(rule, T):
+    """bf16, dk = dv = 128, C = 64: the tensor-core kernel's write-key mode
+    (one chunk, whole chunks, a ragged tail)."""
+    inp = aniso(gen.prefill_inputs(gen.LAYER_1B, B=1, T=T, H=2), 4)
     d = dev(inp)
     kw, _ = kla.precond_keys(d["k"], x=X, delta=DELTA)
     o, hT = kla.chunk_fwd_kw(d["q"], d["k"], kw, d["v"], d["log_alpha"],
@@ -138,3 +141,37 @@ def test_prefill_then_decode_handoff():
     assert rel_err(torch.cat(outs, 1), o_ref) <= 2e-2
     assert rel_err(S, h_ref) <= 2e-2
     assert rel_err(A, A_ref) <= 1e-5
+
+
+def test_write_keys_equal_to_keys_give_the_plain_forward():
+    """With k_write = k the write-key mode computes exactly what the plain
+    forward does (same operands, same order): bit-identical o and state."""
+    inp = gen.prefill_inputs(gen.LAYER_1B, B=2, T=300, H=3)
+    d = dev(inp)
+    o1, h1 = kla.chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["eta"],
+                           d["eps"], d["h0"], C=64)
+    o2, h2 = kla.chunk_fwd_kw(d["q"], d["k"], d["k"], d["v"],
+                              d["log_alpha"], d["eta"], d["eps"], d["h0"],
+                              C=64)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_forward_full_size_sampled_heads():
+    """The 1B layer (B4 T4096 H16) through write keys and the two-key
+    forward on the GPU; heads (b=2, h=7..8) follow the oracle over all 4096
+    tokens."""
+    inp = aniso(gen.prefill_inputs(gen.LAYER_1B), 6)
+    d = dev(inp)
+    kw, _ = kla.precond_keys(d["k"], x=X, delta=DELTA)
+    o, hT = kla.chunk_fwd_kw(d["q"], d["k"], kw, d["v"], d["log_alpha"],
+                             d["eta"], d["eps"], d["h0"], C=64)
+    torch.cuda.synchronize()
+    tok = np.s_[2:3, :, 7:9]
+    st = np.s_[2:3, 7:9]
+    o_ref, h_ref, _, _ = oracle.pkla_fwd(
+        inp["q"][tok], inp["k"][tok], inp["v"][tok], inp["log_alpha"][tok],
+        inp["eta"][tok], inp["eps"], inp["h0"][st], x=X, delta=DELTA)
+    assert rel_err(o[tok], o_ref) <= 2e-2
+    assert rel_err(hT[st], h_ref) <= 2e-2
+

@@ -124,6 +124,58 @@ KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
                             kla_step_rule rule, kla_stream_t stream);
 
 /*
+ * kla_chunk_fwd_host_workspace_size -- bytes of device workspace
+ * kla_chunk_fwd_host needs for these sizes: two buffers of every per-token
+ * tensor for one segment of the sequence (at most 8 segments of whole
+ * chunks) and two fp32 states [B, H, dk, dv].  Writes 0 when B * H == 0.
+ * Errors: KLA_ERR_INVALID_ARG (null `bytes`, negative size, bad dtype),
+ * KLA_ERR_UNSUPPORTED_SHAPE (dk, dv or C outside the supported set).
+ */
+KLA_API kla_status kla_chunk_fwd_host_workspace_size(int B, int T, int H,
+                                                     int dk, int dv, int C,
+                                                     kla_dtype dtype,
+                                                     size_t* bytes);
+
+/*
+ * kla_chunk_fwd_host -- kla_chunk_fwd_ex from host memory to host memory:
+ * q, k, v, log_alpha, eta, h0 are read from, and o, hT written to, host
+ * buffers with the layouts of kla_chunk_fwd.  The pages have no counterpart;
+ * it is the library's way of overlapping the host<->device copies with the
+ * kernels.  The sequence is cut into segments of whole chunks (at most 8);
+ * while the kernel runs segment i on `stream`, a copy stream of the library
+ * brings segment i+1's inputs to the device and another takes segment
+ * i-1's o back.  Each segment's kernel starts from the fp32 state the
+ * previous one ended with, so o and hT are bit-identical to those of
+ * kla_chunk_fwd_ex on device copies of the same inputs.
+ *
+ *   q .. hT, eps, B .. C, dtype, algo, rule: as for kla_chunk_fwd_ex, host
+ *                  pointers (page-locked memory for the copies to overlap;
+ *                  pageable memory works, without the overlap)
+ *   workspace      device memory of at least
+ *                  kla_chunk_fwd_host_workspace_size(...) bytes, 256-byte
+ *                  aligned, owned by the caller; contents on entry do not
+ *                  matter
+ *
+ * Asynchronous: returns once everything is enqueued; o and hT are valid
+ * after `stream` has been synchronised (all copies are ordered before any
+ * later work on `stream`), and the host inputs must stay unchanged until
+ * then.  The library's two copy streams and a few events per device are
+ * created on the first call on that device and kept; calls on one device are
+ * enqueued one at a time.  Calls that share a workspace must be ordered by
+ * the caller (the same stream does it).  Errors: as for kla_chunk_fwd_ex,
+ * plus KLA_ERR_INVALID_ARG for a missing, small or misaligned workspace.
+ */
+KLA_API kla_status kla_chunk_fwd_host(const void* q, const void* k,
+                                      const void* v, const float* log_alpha,
+                                      const float* eta, float eps,
+                                      const float* h0, void* o, float* hT,
+                                      int B, int T, int H, int dk, int dv,
+                                      int C, kla_dtype dtype, kla_algo algo,
+                                      kla_step_rule rule, void* workspace,
+                                      size_t workspace_bytes,
+                                      kla_stream_t stream);
+
+/*
  * kla_decode_step -- one new token for each of N sequences x H heads (the
  * recurrence above for a single t), updating the recurrent state in place.
  *

@@ -50,6 +50,11 @@ SIGNATURES = {
                               _FP, _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
     "kla_decode_step_kw": (_I, [_VP, _VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
                                 _I, _I, _I, _I, _I, _I, _VP]),
+    "kla_chunk_fwd_host_workspace_size": (
+        _I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
+    "kla_chunk_fwd_host": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP, _FP,
+                                _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                                _VP, ctypes.c_size_t, _VP]),
     "kla_device_status": (_I, [_VP]),
     "kla_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -139,6 +144,65 @@ def chunk_fwd(q, k, v, log_alpha, eta, eps: float = 1e-6, h0=None,
         DTYPES[q.dtype], ALGOS[algo], RULES[rule], _stream(stream))
     if st != KLA_OK:
         raise KlaError("kla_chunk_fwd_ex", st)
+    return o, hT
+
+
+def _check_host(name, t, dtype=None):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise TypeError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def chunk_fwd_host_workspace_size(B, T, H, dk, dv, C, dtype) -> int:
+    """Bytes of device workspace ``chunk_fwd_host`` needs."""
+    n = ctypes.c_size_t(0)
+    st = load_library().kla_chunk_fwd_host_workspace_size(
+        B, T, H, dk, dv, int(C), DTYPES[dtype], ctypes.byref(n))
+    if st != KLA_OK:
+        raise KlaError("kla_chunk_fwd_host_workspace_size", st)
+    return n.value
+
+
+def chunk_fwd_host(q, k, v, log_alpha, eta, eps: float = 1e-6, h0=None,
+                   C: int = 64, algo: str = "auto", o=None, hT=None,
+                   want_state: bool = True, workspace=None, stream=None,
+                   rule: str = "kaczmarz"):
+    """KLA forward pass from host tensors to host tensors
+    (``kla_chunk_fwd_host``): the copies to and from the device overlap with
+    the kernels.  Inputs as for ``chunk_fwd`` but on the host (page-locked
+    for the overlap); ``o``/``hT`` are returned on the host (page-locked when
+    allocated here) and are valid once ``stream`` (default: the current one)
+    has been synchronised.  ``workspace``: a device uint8 tensor of at least
+    ``chunk_fwd_host_workspace_size`` bytes, allocated here when None."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_host(n, t, q.dtype)
+    _check_host("log_alpha", log_alpha, torch.float32)
+    _check_host("eta", eta, torch.float32)
+    if h0 is not None:
+        _check_host("h0", h0, torch.float32)
+    if q.dtype not in DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype).pin_memory()
+    if hT is None and want_state:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32).pin_memory()
+    need = chunk_fwd_host_workspace_size(B, T, H, dk, dv, C, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8,
+                                device="cuda")
+    _check_cuda("workspace", workspace, torch.uint8)
+    st = load_library().kla_chunk_fwd_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(eta), float(eps),
+        _ptr(h0), _ptr(o), _ptr(hT), B, T, H, dk, dv, int(C),
+        DTYPES[q.dtype], ALGOS[algo], RULES[rule], _ptr(workspace),
+        workspace.numel(), _stream(stream))
+    if st != KLA_OK:
+        raise KlaError("kla_chunk_fwd_host", st)
     return o, hT
 
 

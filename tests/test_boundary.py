@@ -194,3 +194,49 @@ def test_precond_entry_points_reject_bad_arguments_on_host(lib):
     S = ctypes.c_void_p(0x40000)
     assert dk_(q, k, None, v, la, eta, 1e-6, S, o, 1, 1, 16, 16, 1, 0,
                None) == INVALID
+
+
+HP = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(6)]   # distinct
+
+
+def host_fwd(lib, *, q=HP[0], k=HP[1], v=HP[2], la=HP[3], eta=HP[4],
+             eps=1e-6, h0=None, o=HP[5], hT=None, B=1, T=64, H=1, dk=16,
+             dv=16, C=16, dtype=0, algo=0, rule=0,
+             ws=ctypes.c_void_p(0x10000), ws_bytes=1 << 40):
+    return lib.kla_chunk_fwd_host(q, k, v, la, eta, eps, h0, o, hT, B, T, H,
+                                  dk, dv, C, dtype, algo, rule, ws, ws_bytes,
+                                  None)
+
+
+def test_host_fwd_workspace_size(lib):
+    n = ctypes.c_size_t(123)
+    assert lib.kla_chunk_fwd_host_workspace_size(
+        4, 4096, 16, 128, 128, 64, 1, ctypes.byref(n)) == OK
+    # two slots of one segment (512 tokens: q, k, v, o bf16, two fp32
+    # gates) and two fp32 states
+    rows = 4 * 512 * 16
+    assert n.value == 2 * rows * (4 * 128 * 2 + 8) + 2 * 4 * 16 * 128 * 128 * 4
+    assert lib.kla_chunk_fwd_host_workspace_size(
+        0, 64, 3, 16, 16, 16, 0, ctypes.byref(n)) == OK and n.value == 0
+    assert lib.kla_chunk_fwd_host_workspace_size(
+        1, 64, 1, 24, 16, 16, 0, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.kla_chunk_fwd_host_workspace_size(
+        1, 64, 1, 16, 16, 16, 0, None) == INVALID
+    assert lib.kla_chunk_fwd_host_workspace_size(
+        1, -1, 1, 16, 16, 16, 0, ctypes.byref(n)) == INVALID
+
+
+def test_host_fwd_rejects_bad_arguments_on_host(lib):
+    assert host_fwd(lib, ws=None) == INVALID
+    assert host_fwd(lib, ws=ctypes.c_void_p(0x10008)) == INVALID   # alignment
+    assert host_fwd(lib, ws_bytes=16) == INVALID
+    assert host_fwd(lib, q=None) == INVALID
+    assert host_fwd(lib, o=None) == INVALID
+    assert host_fwd(lib, q=HP[5]) == INVALID            # o aliases q
+    assert host_fwd(lib, algo=7) == INVALID
+    assert host_fwd(lib, rule=9) == INVALID
+    assert host_fwd(lib, eps=-1.0) == INVALID
+    assert host_fwd(lib, eps=float("inf")) == INVALID
+    assert host_fwd(lib, dk=24) == UNSUPPORTED
+    assert host_fwd(lib, C=48) == UNSUPPORTED
+    assert host_fwd(lib, B=0) == OK                     # empty: nothing to do

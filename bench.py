@@ -466,6 +466,51 @@ def bench_precond(w, inp, steps, warmup, world):
     return t_plain, t_keys, t_fwd
 
 
+def seq_segments(w) -> int:
+    """The split kla_chunk_fwd_seq picks for segments = 0 (the same rule)."""
+    sms = torch.cuda.get_device_properties(
+        torch.cuda.current_device()).multi_processor_count
+    P = 1
+    while (2 * P <= 8 and 4 * w.B * w.H * 2 * P <= sms and
+           w.T % (2 * P * w.C) == 0):
+        P *= 2
+    return P
+
+
+def bench_seq(w, inp, steps, warmup, world, rule="kaczmarz"):
+    """The sequence-split forward (kla_chunk_fwd_seq, segments chosen by the
+    library), inputs resident on the device; CUDA events around each call."""
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
+         for k, v in inp.items()}
+    o = torch.empty_like(d["v"])
+    hT = torch.empty((w.B, w.H, w.dk, w.dv), dtype=torch.float32,
+                     device="cuda")
+    ws = torch.empty(max(1, kla.chunk_fwd_seq_workspace_size(
+        w.B, w.T, w.H, w.dk, w.dv, w.C, d["q"].dtype, 0)), dtype=torch.uint8,
+        device="cuda")
+
+    def call():
+        kla.chunk_fwd_seq(d["q"], d["k"], d["v"], d["log_alpha"], d["eta"],
+                          d["eps"], d["h0"], C=w.C, segments=0, o=o, hT=hT,
+                          workspace=ws, rule=rule)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        e0, e1 = (torch.cuda.Event(enable_timing=True),
+                  torch.cuda.Event(enable_timing=True))
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    if kla.device_status() != 0:
+        raise RuntimeError("device-side timeout in the split prefill")
+    return max_over_ranks(float(np.mean(ts)), world), seq_segments(w)
+
+
 def bench_long_context(world, gpu_index, hbm):
     """The pages' own efficiency points at layer scale: the 131072-token
     prefill (KLA and the learned-step rule on the same kernels), and decode
@@ -474,13 +519,27 @@ def bench_long_context(world, gpu_index, hbm):
     inp = gen.prefill_inputs(w)
     pf = bench_prefill(w, 3, 3, world, gpu_index, inp=inp)
     gd = bench_prefill(w, 3, 3, world, gpu_index, rule="given", inp=inp)
+    split_ms, split_p = bench_seq(w, inp, 3, 3, world)
+    split_gd_ms, _ = bench_seq(w, inp, 3, 3, world, rule="given")
     del inp
     gbs = prefill_bytes(w) / (pf["ms"] * 1e-3) / 1e9
+    sgbs = prefill_bytes(w) / (split_ms * 1e-3) / 1e9
     prefill = {"workload": w.name, "ms": round(pf["ms"], 4),
                "tokens_per_s": round(world * w.B * w.T / (pf["ms"] * 1e-3), 1),
                "hbm_gbs": round(gbs, 1), "roofline_frac": round(gbs / hbm, 4),
                "gdn_ms": round(gd["ms"], 4),
                "kla_over_gdn_time": round(pf["ms"] / gd["ms"], 4),
+               "split": {"entry": "kla_chunk_fwd_seq", "segments": split_p,
+                         "ms": round(split_ms, 4),
+                         "tokens_per_s": round(world * w.B * w.T /
+                                               (split_ms * 1e-3), 1),
+                         "hbm_gbs": round(sgbs, 1),
+                         "roofline_frac": round(sgbs / hbm, 4),
+                         "gdn_ms": round(split_gd_ms, 4),
+                         "kla_over_gdn_time": round(split_ms / split_gd_ms,
+                                                    4),
+                         "speedup_vs_single_launch": round(pf["ms"] /
+                                                           split_ms, 3)},
                "timed_steps": 3}
 
     hw = gen.HANDOFF_32K

@@ -124,6 +124,66 @@ KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
                             kla_step_rule rule, kla_stream_t stream);
 
 /*
+ * kla_chunk_fwd_seq_workspace_size -- bytes of device workspace
+ * kla_chunk_fwd_seq needs: fp32 start and end states of the 2 x B x P
+ * segment runs (4 tensors [B, P, H, 128, 128]), O_hom [B, T, H, 128] bf16,
+ * the bf16 start states [B, P, H, 128, 128] and a [64, H, 128] bf16 zero
+ * tile; 0 when there is nothing to split.  segments = 0 picks P as
+ * kla_chunk_fwd_seq does (for the current device).  Errors:
+ * KLA_ERR_INVALID_ARG (null `bytes`, negative size or segments),
+ * KLA_ERR_UNSUPPORTED_SHAPE (not bf16 with dk = dv = 128 and C = 64, P > 8,
+ * or T not a multiple of 64 P).
+ */
+KLA_API kla_status kla_chunk_fwd_seq_workspace_size(int B, int T, int H,
+                                                    int dk, int dv, int C,
+                                                    kla_dtype dtype,
+                                                    int segments,
+                                                    size_t* bytes);
+
+/*
+ * kla_chunk_fwd_seq -- kla_chunk_fwd_ex (tensor-core kernel) for a few long
+ * sequences, split into P segments per sequence so that more SMs work on
+ * each.  The recurrence is linear in the state: segment s maps its start
+ * state S_s to Phi_s S_s + B_s and gives the outputs O0_s + O_hom,s S_s,
+ * with B_s, O0_s from the segment run from a zero state and Phi_s, O_hom,s
+ * from the run from the identity with V = 0.  Both runs are the forward
+ * kernel over the B P segments (at the same time, on `stream` and on a
+ * second stream of the library); a small kernel chains S_{s+1} =
+ * Phi_s S_s + B_s and a tensor-core kernel adds O_hom,s S_s to o of every
+ * segment after the first.  The pages have no counterpart: it reorders the
+ * sums of the chunkwise form, so o and hT equal kla_chunk_fwd_ex's up to
+ * rounding (O_hom and S_s enter the last product in bf16), not bit for
+ * bit.
+ *
+ *   q .. hT, eps, B .. C, dtype, rule: as for kla_chunk_fwd_ex (device
+ *                  memory, 16-byte aligned)
+ *   segments       P >= 1, or 0 to take the most segments (up to 8, T a
+ *                  multiple of 64 P) for which the two runs' 4 B H P CTAs
+ *                  fit on the device's SMs at once; P = 1 is
+ *                  kla_chunk_fwd_ex with KLA_ALGO_TC
+ *   workspace      device memory of at least
+ *                  kla_chunk_fwd_seq_workspace_size(...) bytes, 256-byte
+ *                  aligned, owned by the caller; contents on entry do not
+ *                  matter
+ *
+ * Asynchronous on `stream`; all of the call's work is ordered before later
+ * work on `stream`.  The library's second stream and its two events per
+ * device are created on the first call on that device and kept; calls on
+ * one device are enqueued one at a time.  Errors: as for kla_chunk_fwd_ex,
+ * plus KLA_ERR_UNSUPPORTED_SHAPE (as for the workspace size) and
+ * KLA_ERR_INVALID_ARG for a missing, small or misaligned workspace.
+ */
+KLA_API kla_status kla_chunk_fwd_seq(const void* q, const void* k,
+                                     const void* v, const float* log_alpha,
+                                     const float* eta, float eps,
+                                     const float* h0, void* o, float* hT,
+                                     int B, int T, int H, int dk, int dv,
+                                     int C, kla_dtype dtype,
+                                     kla_step_rule rule, int segments,
+                                     void* workspace, size_t workspace_bytes,
+                                     kla_stream_t stream);
+
+/*
  * kla_chunk_fwd_host_workspace_size -- bytes of device workspace
  * kla_chunk_fwd_host needs for these sizes: two buffers of every per-token
  * tensor for one segment of the sequence (at most 8 segments of whole

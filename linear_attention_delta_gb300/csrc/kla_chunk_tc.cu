@@ -1094,7 +1094,8 @@ cudaError_t launch_chunk_tc(const FwdArgs& a, cudaStream_t stream) {
     CUtensorMap mq, mk, mv, mkw;
     if (!make_map(&mq, a.q, a.B, a.T, a.H) ||
         !make_map(&mk, a.k, a.B, a.T, a.H) ||
-        !make_map(&mv, a.v, a.B, a.T, a.H) ||
+        !(a.v_zero ? make_map(&mv, a.v, 1, kC, a.H)
+                   : make_map(&mv, a.v, a.B, a.T, a.H)) ||
         !make_map(&mkw, a.kw ? a.kw : a.k, a.B, a.T, a.H))
         return cudaErrorInvalidValue;
     // exactly one of o (the forward) and ckpt (the backward's checkpoints);

@@ -43,6 +43,9 @@ struct FwdArgs {
     // may be null: separate write keys [B, T, H, dk]; null means the write
     // key is k
     const void* kw = nullptr;
+    // tensor-core kernel only: v is a zeroed [1, 64, H, dv] tile standing
+    // for an all-zero V (every other load falls outside it and reads zeros)
+    bool v_zero = false;
 };
 
 struct PrecondArgs {
@@ -105,6 +108,8 @@ bool chunk_tc_eligible(const FwdArgs& a);
 cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_precond_keys(const PrecondArgs& a, cudaStream_t stream);
 size_t chunk_bwd_workspace_floats(int B, int T, int H, int dk, int dv, int C);
+// SM count of the current device (cached per device).
+int device_sm_count();
 
 // Device fault word of the tensor-core kernels (bounded waits that gave up).
 // read_and_clear_fault synchronises the stream first.

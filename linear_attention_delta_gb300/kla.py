@@ -50,6 +50,12 @@ SIGNATURES = {
                               _FP, _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
     "kla_decode_step_kw": (_I, [_VP, _VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
                                 _I, _I, _I, _I, _I, _I, _VP]),
+    "kla_chunk_fwd_seq_workspace_size": (
+        _I, [_I, _I, _I, _I, _I, _I, _I, _I,
+             ctypes.POINTER(ctypes.c_size_t)]),
+    "kla_chunk_fwd_seq": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP, _FP,
+                               _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                               _VP, ctypes.c_size_t, _VP]),
     "kla_chunk_fwd_host_workspace_size": (
         _I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     "kla_chunk_fwd_host": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP, _FP,
@@ -144,6 +150,55 @@ def chunk_fwd(q, k, v, log_alpha, eta, eps: float = 1e-6, h0=None,
         DTYPES[q.dtype], ALGOS[algo], RULES[rule], _stream(stream))
     if st != KLA_OK:
         raise KlaError("kla_chunk_fwd_ex", st)
+    return o, hT
+
+
+def chunk_fwd_seq_workspace_size(B, T, H, dk, dv, C, dtype,
+                                 segments: int = 0) -> int:
+    """Bytes of device workspace ``chunk_fwd_seq`` needs."""
+    n = ctypes.c_size_t(0)
+    st = load_library().kla_chunk_fwd_seq_workspace_size(
+        B, T, H, dk, dv, int(C), DTYPES[dtype], int(segments), ctypes.byref(n))
+    if st != KLA_OK:
+        raise KlaError("kla_chunk_fwd_seq_workspace_size", st)
+    return n.value
+
+
+def chunk_fwd_seq(q, k, v, log_alpha, eta, eps: float = 1e-6, h0=None,
+                  C: int = 64, segments: int = 0, o=None, hT=None,
+                  want_state: bool = True, workspace=None, stream=None,
+                  rule: str = "kaczmarz"):
+    """KLA forward pass split along the sequence (``kla_chunk_fwd_seq``):
+    for a few long sequences (bf16, dk = dv = 128, C = 64).  Arguments as
+    for ``chunk_fwd``; ``segments`` = 0 picks the split; ``workspace``: a
+    device uint8 tensor of ``chunk_fwd_seq_workspace_size`` bytes, allocated
+    here when None."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(n, t, q.dtype)
+    _check_cuda("log_alpha", log_alpha, torch.float32)
+    _check_cuda("eta", eta, torch.float32)
+    if h0 is not None:
+        _check_cuda("h0", h0, torch.float32)
+    if q.dtype not in DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and want_state:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    need = chunk_fwd_seq_workspace_size(B, T, H, dk, dv, C, q.dtype, segments)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8,
+                                device=q.device)
+    _check_cuda("workspace", workspace, torch.uint8)
+    st = load_library().kla_chunk_fwd_seq(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(eta), float(eps),
+        _ptr(h0), _ptr(o), _ptr(hT), B, T, H, dk, dv, int(C),
+        DTYPES[q.dtype], RULES[rule], int(segments), _ptr(workspace),
+        workspace.numel(), _stream(stream))
+    if st != KLA_OK:
+        raise KlaError("kla_chunk_fwd_seq", st)
     return o, hT
 
 

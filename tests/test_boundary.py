@@ -240,3 +240,38 @@ def test_host_fwd_rejects_bad_arguments_on_host(lib):
     assert host_fwd(lib, dk=24) == UNSUPPORTED
     assert host_fwd(lib, C=48) == UNSUPPORTED
     assert host_fwd(lib, B=0) == OK                     # empty: nothing to do
+
+
+def test_seq_fwd_workspace_size_and_host_checks(lib):
+    n = ctypes.c_size_t(7)
+    # B1 T131072 H16, two segments
+    assert lib.kla_chunk_fwd_seq_workspace_size(
+        1, 131072, 16, 128, 128, 64, 1, 2, ctypes.byref(n)) == OK
+    st = 1 * 2 * 16 * 128 * 128
+    assert n.value == (4 * st * 4 + 131072 * 16 * 128 * 2 + st * 2
+                       + 64 * 16 * 128 * 2)
+    # one segment: nothing to split, no workspace
+    assert lib.kla_chunk_fwd_seq_workspace_size(
+        1, 4096, 16, 128, 128, 64, 1, 1, ctypes.byref(n)) == OK
+    assert n.value == 0
+    for args in ((1, 4096, 16, 64, 64, 64, 1, 2),      # not d128
+                 (1, 4096, 16, 128, 128, 64, 0, 2),    # not bf16
+                 (1, 4096, 16, 128, 128, 32, 1, 2),    # not C64
+                 (1, 4160, 16, 128, 128, 64, 1, 2),    # T not a multiple of 128
+                 (1, 4096, 16, 128, 128, 64, 1, 16)):  # P > 8
+        assert lib.kla_chunk_fwd_seq_workspace_size(
+            *args, ctypes.byref(n)) == UNSUPPORTED, args
+    assert lib.kla_chunk_fwd_seq_workspace_size(
+        1, 4096, 16, 128, 128, 64, 1, -1, ctypes.byref(n)) == INVALID
+    call = lambda **kw: lib.kla_chunk_fwd_seq(
+        kw.get("q", HP[0]), HP[1], HP[2], HP[3], HP[4], kw.get("eps", 1e-6),
+        None, kw.get("o", HP[5]), None, 1, 4096, 16, 128, 128, 64, 1,
+        kw.get("rule", 0), 2, kw.get("ws", ctypes.c_void_p(0x10000)),
+        kw.get("ws_bytes", 1 << 40), None)
+    assert call(q=None) == INVALID
+    assert call(q=HP[5]) == INVALID          # o aliases q
+    assert call(rule=5) == INVALID
+    assert call(eps=float("nan")) == INVALID
+    assert call(ws=None) == INVALID
+    assert call(ws_bytes=1024) == INVALID
+    assert call(ws=ctypes.c_void_p(0x10010)) == INVALID

@@ -180,6 +180,22 @@ add_segment_start(__nv_bfloat16* __restrict__ o,
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t row_stride = (size_t)H * kD;
     auto tok = [&](int r) { return (size_t)b * T + (size_t)s * tseg + r; };
+    const int g = lane >> 2, q = lane & 3;
+    const int ra = warp * 16 + g;
+
+    // this thread's o entries first, so that their loads are in flight
+    // while the tiles come in and the products run
+    uint32_t old[2][kD / 8];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int r = r_base + ra + 8 * half;
+        const __nv_bfloat16* orow = o + tok(r) * row_stride + (size_t)h * kD;
+#pragma unroll
+        for (int nt = 0; nt < kD / 8; ++nt)
+            old[half][nt] = r < tseg ? *reinterpret_cast<const uint32_t*>(
+                                           orow + 8 * nt + 2 * q)
+                                     : 0u;
+    }
 
     for (int i = tid; i < kRows * (kD / 8); i += 256) {
         const int r = i / (kD / 8), c8 = i % (kD / 8);
@@ -198,8 +214,6 @@ add_segment_start(__nv_bfloat16* __restrict__ o,
     }
     __syncthreads();
 
-    const int g = lane >> 2, q = lane & 3;
-    const int ra = warp * 16 + g;
     float acc[kD / 8][4];
 #pragma unroll
     for (int nt = 0; nt < kD / 8; ++nt)
@@ -226,11 +240,11 @@ add_segment_start(__nv_bfloat16* __restrict__ o,
         __nv_bfloat16* orow = o + tok(r) * row_stride + (size_t)h * kD;
 #pragma unroll
         for (int nt = 0; nt < kD / 8; ++nt) {
-            __nv_bfloat162* p =
-                reinterpret_cast<__nv_bfloat162*>(orow + 8 * nt + 2 * q);
-            const float2 old = __bfloat1622float2(*p);
-            *p = __floats2bfloat162_rn(old.x + acc[nt][2 * half],
-                                       old.y + acc[nt][2 * half + 1]);
+            const float2 o0 = __bfloat1622float2(
+                *reinterpret_cast<const __nv_bfloat162*>(&old[half][nt]));
+            *reinterpret_cast<__nv_bfloat162*>(orow + 8 * nt + 2 * q) =
+                __floats2bfloat162_rn(o0.x + acc[nt][2 * half],
+                                      o0.y + acc[nt][2 * half + 1]);
         }
     }
 }

@@ -18,7 +18,10 @@
 // shared memory over the cluster's distributed shared memory) give its
 // starting A; pass 2 walks its tokens in order.  A lane holds dk / 32 key
 // dimensions (one when dk = 16), so the mean over the key dimensions is a
-// warp reduction.  No global scratch, one launch.
+// warp reduction.  No global scratch, one launch.  The logarithm and the
+// exponentials are the hardware approximations (__logf, __expf, a few ulp:
+// they move kw by a few 1e-6 relative, far inside the 1e-4 bound), with
+// tanh written through the exponential.
 #include <cooperative_groups.h>
 
 #include "kla_internal.cuh"
@@ -110,6 +113,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1)
         A[d] = s;
     }
     const float lx = logf(a.x);
+    const float inv_lx = 1.f / lx;
     const float inv_dk = 1.f / (float)DK;
     for (int t = t_lo; t < t_hi; t += kTokBatch) {
         float kv[kTokBatch][DPL];
@@ -126,7 +130,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1)
 #pragma unroll
             for (int d = 0; d < DPL; ++d) {
                 A[d] = fmaf(kv[u][d], kv[u][d], A[d]);
-                l[d] = live ? logf(A[d] + a.delta) : 0.f;
+                l[d] = live ? __logf(A[d] + a.delta) : 0.f;
                 s += l[d];
             }
 #pragma unroll
@@ -135,9 +139,15 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1)
             if (live) {
                 const float mean = s * inv_dk;
 #pragma unroll
-                for (int d = 0; d < DPL; ++d)
-                    kw[row(t + u) + d] = from_f32<IO>(
-                        expf(lx * tanhf((mean - l[d]) / lx)) * kv[u][d]);
+                for (int d = 0; d < DPL; ++d) {
+                    // tanh(y) = 1 - 2 / (e^{2y} + 1), 2y kept in [-40, 40]
+                    // (tanh is +-1 to fp32 there)
+                    const float y2 = fminf(fmaxf(2.f * (mean - l[d]) * inv_lx,
+                                                 -40.f), 40.f);
+                    const float th = 1.f - __fdividef(2.f, __expf(y2) + 1.f);
+                    kw[row(t + u) + d] = from_f32<IO>(__expf(lx * th) *
+                                                      kv[u][d]);
+                }
             }
         }
     }

@@ -18,6 +18,11 @@
 // column group of the tile and dk/RS rows (row r = slice + i*RS), so a warp
 // reads whole 512-byte row segments.  Every state load is issued before any
 // reduction so that each CTA keeps its whole tile in flight.
+//
+// Each step is launched as a programmatic dependent of the previous kernel
+// on the stream: its CTAs may be scheduled while the previous grid's last
+// CTAs run, and every CTA waits for that grid (and its memory) before it
+// touches memory, so the ordering is that of plain stream order.
 #include "kla_internal.cuh"
 
 namespace kla {
@@ -50,6 +55,11 @@ kla_decode_kernel(DecodeArgs a) {
     const int cg = tid % Sh::CG;
     const int rs = tid / Sh::CG;
 
+    // launched as a programmatic dependent of the previous kernel on the
+    // stream: wait for it (and its memory) before touching memory, and let
+    // the next one be scheduled as this grid's last CTAs start
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     float* S = a.S + (size_t)head * DK * dv + j0 + 4 * cg;
 
     float4 s[Sh::ROWS];
@@ -154,8 +164,17 @@ cudaError_t launch_shape(const DecodeArgs& a, cudaStream_t stream) {
     const long heads = (long)a.N * a.H;
     if (heads == 0) return cudaSuccess;
     dim3 grid((unsigned)heads, (unsigned)(a.dv / DVT));
-    kla_decode_kernel<DK, DVT, T><<<grid, Sh::NT, 0, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(Sh::NT);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kla_decode_kernel<DK, DVT, T>, a);
 }
 
 template <typename T>

@@ -576,14 +576,38 @@ def bench_long_context(world, gpu_index, hbm):
     e1.record()
     torch.cuda.synchronize()
     dms = e0.elapsed_time(e1) / steps
+    # the same steps from a CUDA graph: `distinct` decode steps (fixed token
+    # buffers) captured once and replayed, one graph launch per `distinct`
+    # steps instead of one kernel launch per step
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):               # warm-up off the capture
+        kla.decode_step(*toks[0], S.clone(), eps=d["eps"], o=od)
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(graph):
+        for i in range(distinct):
+            kla.decode_step(*toks[i], S, eps=d["eps"], o=od)
+    graph.replay()                              # warm-up
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(steps // distinct):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    gms = e0.elapsed_time(e1) / (steps // distinct * distinct)
     if kla.device_status() != 0:
         raise RuntimeError("device-side timeout in the long-context points")
     handoff = {"workload": hw.name, "prefill_ms": round(prefill_ms, 4),
                "decode_sequences": hw.B, "decode_steps": steps,
                "decode_steps_per_s": round(1e3 / dms, 1),
                "decode_ms_per_step": round(dms, 5),
+               "graph_decode_ms_per_step": round(gms, 5),
+               "graph_steps_per_replay": distinct,
                "note": "state carried from the 32768-token prefill; "
-                       "4 MiB of state (L2-resident), so launch-bound"}
+                       "4 MiB of state (L2-resident), so launch-bound: "
+                       "one kernel launch per step, and the same steps "
+                       "replayed from a CUDA graph"}
     return {"prefill_131k": prefill, "decode_after_32k": handoff}
 
 

@@ -105,6 +105,19 @@ def test_hand_worked_example():
                                atol=1e-15)
 
 
+def test_golden_worked_example_fixture():
+    """tests/golden/kla_worked_example_2x2.txt: three tokens worked by hand
+    (decay, a half step and a relaxed step included); both oracles reproduce
+    every output and the final state."""
+    from golden.fixtures import worked_example_2x2
+    g = worked_example_2x2()
+    args = [g[n] for n in ("q", "k", "v", "log_alpha", "eta")]
+    for fwd in (oracle.kla_fwd, oracle.kla_fwd_np):
+        o, hT = fwd(*args, g["eps"], None)
+        np.testing.assert_allclose(o, g["o"], rtol=0, atol=1e-6)
+        np.testing.assert_allclose(hT, g["hT"], rtol=0, atol=1e-6)
+
+
 # --------------------------------------------------------------------------
 # Unrelaxed case (eta = 1, eps = 0): the three properties the page states
 # (section "Propiedades Clave": orthogonal projection, exact line search,

@@ -340,3 +340,28 @@ def test_given_step_decode():
         assert rel_err(o, o_ref) <= 2e-2
     torch.cuda.synchronize()
     assert rel_err(S, S_ref) <= 1e-4
+
+
+def test_golden_worked_example_through_the_library():
+    """tests/golden/kla_worked_example_2x2.txt through the C ABI (fp32,
+    CUDA-core kernel), zero-padded to dk = dv = 16: the padded key and value
+    dims change nothing, so the first two columns must be the hand-worked
+    values and the rest zero."""
+    from golden.fixtures import worked_example_2x2
+    g = worked_example_2x2()
+    pad = lambda x: np.concatenate(
+        [x, np.zeros(x.shape[:-1] + (14,))], -1).astype(np.float32)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    o, hT = kla.chunk_fwd(dev(pad(g["q"])), dev(pad(g["k"])),
+                          dev(pad(g["v"])),
+                          dev(g["log_alpha"].astype(np.float32)),
+                          dev(g["eta"].astype(np.float32)), g["eps"], None,
+                          C=16, algo="simt")
+    torch.cuda.synchronize()
+    o, hT = o.cpu().double().numpy(), hT.cpu().double().numpy()
+    np.testing.assert_allclose(o[..., :2], g["o"], rtol=0, atol=1e-6)
+    assert np.all(o[..., 2:] == 0)
+    np.testing.assert_allclose(hT[:, :, :2, :2], g["hT"], rtol=0, atol=1e-6)
+    hT[:, :, :2, :2] = 0
+    assert np.all(hT == 0)
+

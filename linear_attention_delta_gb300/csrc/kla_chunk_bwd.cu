@@ -30,6 +30,8 @@
 // (batch, head, dv tile): the recurrence for dS is column-separable) and
 // writes dS' of every chunk (dsck) and dh0; kla_bwd_grad_kernel then forms
 // every gradient of one chunk's tokens per CTA, all chunks in parallel.
+#include <type_traits>
+
 #include "kla_internal.cuh"
 #include "simt_blocks.cuh"
 
@@ -285,6 +287,249 @@ kla_bwd_state_kernel(BwdArgs a) {
         for (int idx = tid; idx < DK * DVT; idx += kBwdThreads) {
             const int c = idx / DVT, j = idx % DVT;
             a.dh0[((size_t)bh * DK + c) * dv + j0 + j] = dS[c * L::LDV + j];
+        }
+    }
+}
+
+// ------------------------------------- reverse state recurrence, tensor cores
+// The bf16 case with dk = 128, 64-column dv slices and C = 64: the same
+// per-chunk algebra as kla_bwd_state_kernel, its products on the tensor
+// cores (mma.sync m16n8k8 with tf32 operands rounded to nearest and fp32
+// accumulation; tf32's 2^-11 relative rounding sits far inside the bf16
+// bound): A and P (their lower 16 x 8 tiles), dU~ = P^T dO + Diag(lambda)
+// K dS', dF = T^T dU~ and dS = gamma_C dS' + Q^T Diag(gamma) dO
+// - K^T Diag(gamma beta) dF.  Row strides of 136 and 72 floats make every
+// fragment load conflict-free.
+constexpr int kTcDK = 128, kTcDV = 64, kTcC = 64;
+
+struct StateTcSmem {
+    static constexpr int LDK = kTcDK + 8;
+    static constexpr int LDV = kTcDV + 8;
+    static constexpr int LDC = kTcC + 8;
+    static constexpr int Q = 0;
+    static constexpr int K = Q + kTcC * LDK;
+    static constexpr int DO = K + kTcC * LDK;
+    static constexpr int W = DO + kTcC * LDV;      // dU~
+    static constexpr int W2 = W + kTcC * LDV;      // dF
+    static constexpr int DS = W2 + kTcC * LDV;     // dS, key dim x dv
+    static constexpr int A = DS + kTcDK * LDV;
+    static constexpr int P = A + kTcC * LDC;
+    static constexpr int TM = P + kTcC * LDC;      // A^{-1}
+    static constexpr int G = TM + kTcC * LDC;
+    static constexpr int BETA = G + kTcC;
+    static constexpr int GAM = BETA + kTcC;
+    static constexpr int LAM = GAM + kTcC;
+    static constexpr int TOTAL = LAM + kTcC;
+    static constexpr size_t BYTES = sizeof(float) * (size_t)TOTAL;
+};
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// d += a b for one 16 x 8 tile (a: 16 x 8 row fragment, b: 8 x 8 column
+// fragment; rows g, g + 8 and columns 2q, 2q + 1 of d per lane)
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(kBwdThreads)
+kla_bwd_state_tc_kernel(BwdArgs a) {
+    using L = StateTcSmem;
+    constexpr int LDK = L::LDK, LDV = L::LDV, LDC = L::LDC, C = kTcC;
+    extern __shared__ float sm[];
+    float* Qs = sm + L::Q;
+    float* Ks = sm + L::K;
+    float* Ds = sm + L::DO;
+    float* Ws = sm + L::W;
+    float* W2 = sm + L::W2;
+    float* dS = sm + L::DS;
+    float* As = sm + L::A;
+    float* Ps = sm + L::P;
+    float* Tm = sm + L::TM;
+    float* gs = sm + L::G;
+    float* bs = sm + L::BETA;
+    float* gam = sm + L::GAM;
+    float* lam = sm + L::LAM;
+
+    const int bh = blockIdx.x;
+    const int b = bh / a.H, h = bh % a.H;
+    const int j0 = blockIdx.y * kTcDV;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int T = a.T, H = a.H, dv = a.dv;
+    const int nch = (T + C - 1) / C;
+
+    for (int idx = tid; idx < kTcDK * kTcDV; idx += kBwdThreads) {
+        const int c = idx / kTcDV, j = idx % kTcDV;
+        dS[c * LDV + j] =
+            a.dhT ? a.dhT[((size_t)bh * kTcDK + c) * dv + j0 + j] : 0.f;
+    }
+    // P's tiles above the diagonal are never written: zero once
+    for (int idx = tid; idx < C * LDC; idx += kBwdThreads) Ps[idx] = 0.f;
+
+    for (int ch = nch - 1; ch >= 0; --ch) {
+        const int t0 = ch * C;
+        load_chunk_qk(a, b, h, t0, kTcDK, LDK, Qs, Ks, gs, bs);
+        for (int idx = tid; idx < C * kTcDV; idx += kBwdThreads) {
+            const int r = idx / kTcDV, j = idx % kTcDV;
+            const int t = t0 + r;
+            Ds[r * LDV + j] =
+                t < T ? ld_io<IO>(a.dout, (((size_t)b * T + t) * H + h) * dv +
+                                              j0 + j)
+                      : 0.f;
+        }
+        __syncthreads();
+        chunk_gates<kTcDK>(a, Ks, LDK, gs, bs, gam, lam, nullptr);
+        __syncthreads();
+
+        // A = I + strict_lower(Diag(beta)(Gamma o K K^T)) and
+        // P = lower_incl(Gamma o Q K^T): the 20 lower 16 x 8 tiles of each
+        for (int tt = warp; tt < 40; tt += kBwdThreads / 32) {
+            const bool isP = tt >= 20;
+            const int ti = isP ? tt - 20 : tt;
+            int rb = 0, base = 0;            // row block rb has 2 rb + 2 tiles
+            while (ti >= base + 2 * rb + 2) {
+                base += 2 * rb + 2;
+                ++rb;
+            }
+            const int r0 = 16 * rb, n0 = 8 * (ti - base);
+            const float* X = isP ? Qs : Ks;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int k0 = 0; k0 < kTcDK; k0 += 8) {
+                uint32_t af[4];
+                af[0] = to_tf32(X[(r0 + g) * LDK + k0 + q]);
+                af[1] = to_tf32(X[(r0 + g + 8) * LDK + k0 + q]);
+                af[2] = to_tf32(X[(r0 + g) * LDK + k0 + q + 4]);
+                af[3] = to_tf32(X[(r0 + g + 8) * LDK + k0 + q + 4]);
+                mma_tf32(acc, af, to_tf32(Ks[(n0 + g) * LDK + k0 + q]),
+                         to_tf32(Ks[(n0 + g) * LDK + k0 + q + 4]));
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = r0 + g + 8 * (e >> 1), i = n0 + 2 * q + (e & 1);
+                const float dec = i <= r ? expf(gs[r] - gs[i]) : 0.f;
+                if (isP)
+                    Ps[r * LDC + i] = i <= r ? dec * acc[e] : 0.f;
+                else
+                    As[r * LDC + i] = i < r ? bs[r] * dec * acc[e]
+                                            : (i == r ? 1.f : 0.f);
+            }
+        }
+        {   // dL/dS at the end of this chunk
+            float* out = a.dsck + ((size_t)bh * nch + ch) * kTcDK * dv + j0;
+            for (int idx = tid; idx < kTcDK * kTcDV; idx += kBwdThreads) {
+                const int c = idx / kTcDV, j = idx % kTcDV;
+                out[(size_t)c * dv + j] = dS[c * LDV + j];
+            }
+        }
+        __syncthreads();
+        invert_unit_lower<kBwdThreads>(As, Tm, C, LDC);   // ends with a barrier
+
+        // dU~ = P^T dO + Diag(lambda) K dS': 32 tiles, 4 per warp
+        for (int tt = warp; tt < 32; tt += kBwdThreads / 32) {
+            const int r0 = 16 * (tt / 8), n0 = 8 * (tt % 8);
+            float kd[4] = {0.f, 0.f, 0.f, 0.f}, pd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int k0 = 0; k0 < kTcDK; k0 += 8) {
+                uint32_t af[4];
+                af[0] = to_tf32(Ks[(r0 + g) * LDK + k0 + q]);
+                af[1] = to_tf32(Ks[(r0 + g + 8) * LDK + k0 + q]);
+                af[2] = to_tf32(Ks[(r0 + g) * LDK + k0 + q + 4]);
+                af[3] = to_tf32(Ks[(r0 + g + 8) * LDK + k0 + q + 4]);
+                mma_tf32(kd, af, to_tf32(dS[(k0 + q) * LDV + n0 + g]),
+                         to_tf32(dS[(k0 + q + 4) * LDV + n0 + g]));
+            }
+            for (int k0 = r0; k0 < C; k0 += 8) {   // P[i][r] = 0 for i < r
+                uint32_t af[4];
+                af[0] = to_tf32(Ps[(k0 + q) * LDC + r0 + g]);
+                af[1] = to_tf32(Ps[(k0 + q) * LDC + r0 + g + 8]);
+                af[2] = to_tf32(Ps[(k0 + q + 4) * LDC + r0 + g]);
+                af[3] = to_tf32(Ps[(k0 + q + 4) * LDC + r0 + g + 8]);
+                mma_tf32(pd, af, to_tf32(Ds[(k0 + q) * LDV + n0 + g]),
+                         to_tf32(Ds[(k0 + q + 4) * LDV + n0 + g]));
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = r0 + g + 8 * (e >> 1), j = n0 + 2 * q + (e & 1);
+                Ws[r * LDV + j] = fmaf(lam[r], kd[e], pd[e]);
+            }
+        }
+        __syncthreads();
+
+        // dF = T^T dU~ (T lower triangular; its upper part holds scratch)
+        for (int tt = warp; tt < 32; tt += kBwdThreads / 32) {
+            const int r0 = 16 * (tt / 8), n0 = 8 * (tt % 8);
+            const int ra = r0 + g, rb = r0 + g + 8;
+            float df[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k0 = r0; k0 < C; k0 += 8) {
+                const int i0 = k0 + q, i1 = k0 + q + 4;
+                uint32_t af[4];
+                af[0] = to_tf32(i0 >= ra ? Tm[i0 * LDC + ra] : 0.f);
+                af[1] = to_tf32(i0 >= rb ? Tm[i0 * LDC + rb] : 0.f);
+                af[2] = to_tf32(i1 >= ra ? Tm[i1 * LDC + ra] : 0.f);
+                af[3] = to_tf32(i1 >= rb ? Tm[i1 * LDC + rb] : 0.f);
+                mma_tf32(df, af, to_tf32(Ws[i0 * LDV + n0 + g]),
+                         to_tf32(Ws[i1 * LDV + n0 + g]));
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = r0 + g + 8 * (e >> 1), j = n0 + 2 * q + (e & 1);
+                W2[r * LDV + j] = df[e];
+            }
+        }
+        __syncthreads();
+
+        // dS = gamma_C dS' + Q^T Diag(gamma) dO - K^T Diag(gamma beta) dF:
+        // 64 tiles, 8 per warp; each thread reads and writes only its own
+        // entries of dS
+        const float gC = gam[C - 1];
+        for (int tt = warp; tt < 64; tt += kBwdThreads / 32) {
+            const int c0 = 16 * (tt / 8), n0 = 8 * (tt % 8);
+            float acc[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                acc[e] = gC * dS[(c0 + g + 8 * (e >> 1)) * LDV + n0 + 2 * q +
+                                 (e & 1)];
+#pragma unroll 2
+            for (int k0 = 0; k0 < C; k0 += 8) {
+                const int r0 = k0 + q, r1 = k0 + q + 4;
+                uint32_t af[4];
+                af[0] = to_tf32(Qs[r0 * LDK + c0 + g]);
+                af[1] = to_tf32(Qs[r0 * LDK + c0 + g + 8]);
+                af[2] = to_tf32(Qs[r1 * LDK + c0 + g]);
+                af[3] = to_tf32(Qs[r1 * LDK + c0 + g + 8]);
+                mma_tf32(acc, af, to_tf32(gam[r0] * Ds[r0 * LDV + n0 + g]),
+                         to_tf32(gam[r1] * Ds[r1 * LDV + n0 + g]));
+                af[0] = to_tf32(Ks[r0 * LDK + c0 + g]);
+                af[1] = to_tf32(Ks[r0 * LDK + c0 + g + 8]);
+                af[2] = to_tf32(Ks[r1 * LDK + c0 + g]);
+                af[3] = to_tf32(Ks[r1 * LDK + c0 + g + 8]);
+                mma_tf32(acc, af,
+                         to_tf32(-gam[r0] * bs[r0] * W2[r0 * LDV + n0 + g]),
+                         to_tf32(-gam[r1] * bs[r1] * W2[r1 * LDV + n0 + g]));
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                dS[(c0 + g + 8 * (e >> 1)) * LDV + n0 + 2 * q + (e & 1)] =
+                    acc[e];
+        }
+        __syncthreads();
+    }
+
+    if (a.dh0) {
+        for (int idx = tid; idx < kTcDK * kTcDV; idx += kBwdThreads) {
+            const int c = idx / kTcDV, j = idx % kTcDV;
+            a.dh0[((size_t)bh * kTcDK + c) * dv + j0 + j] = dS[c * LDV + j];
         }
     }
 }
@@ -753,8 +998,24 @@ cudaError_t launch_shape(const BwdArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const long bhs = (long)a.B * a.H;
     const long nch = (a.T + a.C - 1) / a.C;
-    ks<<<dim3((unsigned)bhs, (unsigned)(a.dv / DVS)), kBwdThreads, LS::BYTES,
-         stream>>>(a);
+    if constexpr (DK == kTcDK && DVS == kTcDV &&
+                  std::is_same<IO, __nv_bfloat16>::value) {
+        if (a.C == kTcC) {   // the reverse recurrence on the tensor cores
+            auto kt = kla_bwd_state_tc_kernel<IO>;
+            e = cudaFuncSetAttribute(
+                kt, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                (int)StateTcSmem::BYTES);
+            if (e != cudaSuccess) return e;
+            kt<<<dim3((unsigned)bhs, (unsigned)(a.dv / DVS)), kBwdThreads,
+                 StateTcSmem::BYTES, stream>>>(a);
+        } else {
+            ks<<<dim3((unsigned)bhs, (unsigned)(a.dv / DVS)), kBwdThreads,
+                 LS::BYTES, stream>>>(a);
+        }
+    } else {
+        ks<<<dim3((unsigned)bhs, (unsigned)(a.dv / DVS)), kBwdThreads,
+             LS::BYTES, stream>>>(a);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     kg<<<(unsigned)(bhs * nch), kBwdThreads, LG::BYTES, stream>>>(a);
@@ -771,7 +1032,12 @@ cudaError_t launch_dtype(const BwdArgs& a, cudaStream_t stream) {
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const bool wide = a.dv >= 64 && (long)a.B * a.H * (a.dv / 32) > sms;
+    // bf16, dk = 128, C = 64: 64-column slices always (the tensor-core
+    // reverse recurrence)
+    const bool tc = std::is_same<IO, __nv_bfloat16>::value && a.dk == kTcDK &&
+                    a.C == kTcC && a.dv % kTcDV == 0;
+    const bool wide =
+        tc || (a.dv >= 64 && (long)a.B * a.H * (a.dv / 32) > sms);
 #define KLA_BWD_DK(DKV)                                                     \
     if (a.dk == DKV) {                                                      \
         if (a.dv == 16) return launch_shape<DKV, 16, 16, IO>(a, stream);    \

@@ -340,6 +340,16 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The tensor-core recurrence applies: bf16, dk = 128, C = 64, dv a multiple
+// of 64, and q, k, dO 16-byte aligned (its tile loads are 16 bytes wide).
+__host__ __forceinline__ bool state_tc_ok(const BwdArgs& a) {
+    auto al16 = [](const void* p) {
+        return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+    };
+    return a.dtype == KLA_BF16 && a.dk == kTcDK && a.C == kTcC &&
+           a.dv % kTcDV == 0 && al16(a.q) && al16(a.k) && al16(a.dout);
+}
+
 template <typename IO>
 __global__ void __launch_bounds__(kBwdThreads)
 kla_bwd_state_tc_kernel(BwdArgs a) {
@@ -376,18 +386,67 @@ kla_bwd_state_tc_kernel(BwdArgs a) {
     // P's tiles above the diagonal are never written: zero once
     for (int idx = tid; idx < C * LDC; idx += kBwdThreads) Ps[idx] = 0.f;
 
+    // The tiles of a chunk (q, k: 64 x 128, dO: 64 x 64, bf16) and its gates
+    // are loaded into registers, 16 bytes a load, while the previous chunk
+    // computes, and stored to shared memory when it is done.
+    const uint4* q4 = static_cast<const uint4*>(a.q);
+    const uint4* k4 = static_cast<const uint4*>(a.k);
+    const uint4* d4 = static_cast<const uint4*>(a.dout);
+    uint4 pq[4], pk[4], pd[2];
+    float pla = 0.f, peta = 0.f;
+    auto fetch = [&](int c) {
+        const int t0c = c * C;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {   // row tid / 16 + 16 m, 8 dims at 8 (tid % 16)
+            const int r = tid / 16 + 16 * m, t = t0c + r;
+            const size_t e = ((((size_t)b * T + t) * H + h) * kTcDK) / 8 +
+                             tid % 16;
+            pq[m] = t < T ? q4[e] : make_uint4(0, 0, 0, 0);
+            pk[m] = t < T ? k4[e] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {   // row tid / 8 + 32 m, dv 8 (tid % 8)
+            const int r = tid / 8 + 32 * m, t = t0c + r;
+            const size_t e =
+                ((((size_t)b * T + t) * H + h) * dv + j0) / 8 + tid % 8;
+            pd[m] = t < T ? d4[e] : make_uint4(0, 0, 0, 0);
+        }
+        if (tid < C) {
+            const int t = t0c + tid;
+            const size_t off = ((size_t)b * T + t) * H + h;
+            pla = t < T ? a.log_alpha[off] : 0.f;
+            peta = t < T ? a.eta[off] : 0.f;
+        }
+    };
+    auto unpack8 = [](uint4 u, float* dst) {   // 8 bf16 -> 8 fp32
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+        reinterpret_cast<float4*>(dst)[0] = make_float4(f[0], f[1], f[2], f[3]);
+        reinterpret_cast<float4*>(dst)[1] = make_float4(f[4], f[5], f[6], f[7]);
+    };
+    fetch(nch - 1);
+
     for (int ch = nch - 1; ch >= 0; --ch) {
-        const int t0 = ch * C;
-        load_chunk_qk(a, b, h, t0, kTcDK, LDK, Qs, Ks, gs, bs);
-        for (int idx = tid; idx < C * kTcDV; idx += kBwdThreads) {
-            const int r = idx / kTcDV, j = idx % kTcDV;
-            const int t = t0 + r;
-            Ds[r * LDV + j] =
-                t < T ? ld_io<IO>(a.dout, (((size_t)b * T + t) * H + h) * dv +
-                                              j0 + j)
-                      : 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int r = tid / 16 + 16 * m, c8 = tid % 16;
+            unpack8(pq[m], Qs + r * LDK + 8 * c8);
+            unpack8(pk[m], Ks + r * LDK + 8 * c8);
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+            unpack8(pd[m], Ds + (tid / 8 + 32 * m) * LDV + 8 * (tid % 8));
+        if (tid < C) {
+            gs[tid] = pla;
+            bs[tid] = peta;
         }
         __syncthreads();
+        if (ch > 0) fetch(ch - 1);   // in flight during this chunk
         chunk_gates<kTcDK>(a, Ks, LDK, gs, bs, gam, lam, nullptr);
         __syncthreads();
 
@@ -1000,7 +1059,7 @@ cudaError_t launch_shape(const BwdArgs& a, cudaStream_t stream) {
     const long nch = (a.T + a.C - 1) / a.C;
     if constexpr (DK == kTcDK && DVS == kTcDV &&
                   std::is_same<IO, __nv_bfloat16>::value) {
-        if (a.C == kTcC) {   // the reverse recurrence on the tensor cores
+        if (state_tc_ok(a)) {   // the reverse recurrence on the tensor cores
             auto kt = kla_bwd_state_tc_kernel<IO>;
             e = cudaFuncSetAttribute(
                 kt, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1032,10 +1091,9 @@ cudaError_t launch_dtype(const BwdArgs& a, cudaStream_t stream) {
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    // bf16, dk = 128, C = 64: 64-column slices always (the tensor-core
-    // reverse recurrence)
-    const bool tc = std::is_same<IO, __nv_bfloat16>::value && a.dk == kTcDK &&
-                    a.C == kTcC && a.dv % kTcDV == 0;
+    // where the tensor-core reverse recurrence applies: 64-column slices
+    // always
+    const bool tc = std::is_same<IO, __nv_bfloat16>::value && state_tc_ok(a);
     const bool wide =
         tc || (a.dv >= 64 && (long)a.B * a.H * (a.dv / 32) > sms);
 #define KLA_BWD_DK(DKV)                                                     \

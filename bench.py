@@ -775,7 +775,9 @@ def run_ours(args):
         ach = bflops / (bms * 1e-3) / 1e12
         backward = {"workload": w.name, "ms": round(bms, 4),
                     "tokens_per_s": round(world * tokens / (bms * 1e-3), 1),
-                    "kernels": "kla_chunk_bwd: CUDA-core fp32, 3 launches",
+                    "kernels": "kla_chunk_bwd: tcgen05 checkpoints, tf32 "
+                               "mma.sync reverse recurrence, CUDA-core fp32 "
+                               "gradients; 3 launches",
                     "workspace_bytes": ws_bytes,
                     "roofline": {"bound": "alu", "achieved": round(ach, 2),
                                  "peak": round(alu_peak, 1),

@@ -33,22 +33,41 @@ struct Pipe {
 std::mutex g_pipe_mu;   // also serialises the enqueue of whole calls
 Pipe g_pipe[kMaxDevices];
 
+// Releases whatever a failed init_pipe created (so that a retry starts
+// clean).
+void release_pipe(Pipe& p) {
+    cudaEvent_t* ev[] = {&p.start, &p.fin, &p.in_done[0], &p.in_done[1],
+                         &p.comp_done[0], &p.comp_done[1], &p.out_done[0],
+                         &p.out_done[1]};
+    for (cudaEvent_t* e : ev)
+        if (*e) { cudaEventDestroy(*e); *e = nullptr; }
+    if (p.in) { cudaStreamDestroy(p.in); p.in = nullptr; }
+    if (p.out) { cudaStreamDestroy(p.out); p.out = nullptr; }
+}
+
 cudaError_t init_pipe(Pipe& p, int dev) {
+    static_assert(kSlots == 2, "release_pipe lists two slots");
     int pitch = 0;
     cudaError_t e = cudaDeviceGetAttribute(&pitch, cudaDevAttrMaxPitch, dev);
     if (e != cudaSuccess) return e;
     p.max_pitch = (size_t)(unsigned)pitch;
     const unsigned sf = cudaStreamNonBlocking;
     const unsigned ef = cudaEventDisableTiming;
-    if ((e = cudaStreamCreateWithFlags(&p.in, sf)) != cudaSuccess) return e;
-    if ((e = cudaStreamCreateWithFlags(&p.out, sf)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&p.start, ef)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&p.fin, ef)) != cudaSuccess) return e;
-    for (int j = 0; j < kSlots; ++j) {
-        if ((e = cudaEventCreateWithFlags(&p.in_done[j], ef)) != cudaSuccess ||
-            (e = cudaEventCreateWithFlags(&p.comp_done[j], ef)) != cudaSuccess ||
-            (e = cudaEventCreateWithFlags(&p.out_done[j], ef)) != cudaSuccess)
-            return e;
+    if ((e = cudaStreamCreateWithFlags(&p.in, sf)) == cudaSuccess &&
+        (e = cudaStreamCreateWithFlags(&p.out, sf)) == cudaSuccess &&
+        (e = cudaEventCreateWithFlags(&p.start, ef)) == cudaSuccess &&
+        (e = cudaEventCreateWithFlags(&p.fin, ef)) == cudaSuccess) {
+        for (int j = 0; j < kSlots && e == cudaSuccess; ++j) {
+            if ((e = cudaEventCreateWithFlags(&p.in_done[j], ef)) ==
+                    cudaSuccess &&
+                (e = cudaEventCreateWithFlags(&p.comp_done[j], ef)) ==
+                    cudaSuccess)
+                e = cudaEventCreateWithFlags(&p.out_done[j], ef);
+        }
+    }
+    if (e != cudaSuccess) {
+        release_pipe(p);
+        return e;
     }
     p.ready = true;
     return cudaSuccess;

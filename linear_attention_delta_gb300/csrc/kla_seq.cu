@@ -270,8 +270,15 @@ cudaError_t init_aux(Aux& a) {
         e = cudaFuncSetAttribute(add_segment_start,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kAddSmem);
-    a.ready = e == cudaSuccess;
-    return e;
+    if (e != cudaSuccess) {   // release what was made, so a retry starts clean
+        if (a.join) cudaEventDestroy(a.join);
+        if (a.fork) cudaEventDestroy(a.fork);
+        if (a.s) cudaStreamDestroy(a.s);
+        a = Aux{};
+        return e;
+    }
+    a.ready = true;
+    return cudaSuccess;
 }
 
 bool aligned16(const void* p) {

@@ -362,8 +362,12 @@ KLA_API kla_status kla_chunk_bwd_workspace_size(int B, int T, int H, int dk,
  *                  owned by the caller; its contents on entry do not matter
  *                  and are garbage on return
  *
- * Runs on the CUDA cores in fp32 (three launches).  Supported shapes as for
- * kla_chunk_fwd.  Outputs must not alias inputs, each other or the
+ * Three launches: the forward pass writing the state at every chunk start
+ * (the tensor-core kernel where kla_chunk_fwd_ex's KLA_ALGO_AUTO would use
+ * it); the reverse recurrence of dL/dS over the chunks (on the tensor cores
+ * with tf32 operands for bf16, dk = 128, C = 64 and 16-byte-aligned q, k,
+ * o_grad; else on the CUDA cores in fp32); the per-chunk gradients (CUDA
+ * cores, fp32).  Supported shapes as for kla_chunk_fwd.  Outputs must not alias inputs, each other or the
  * workspace.  Errors: KLA_ERR_INVALID_ARG (null required pointer, negative
  * size, bad enum, eps < 0 or not finite, workspace too small or misaligned),
  * KLA_ERR_UNSUPPORTED_SHAPE, KLA_ERR_CUDA.

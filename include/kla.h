@@ -248,6 +248,11 @@ KLA_API kla_status kla_chunk_fwd_host(const void* q, const void* k,
  *
  * Supported: dk, dv in {16, 32, 64, 128}; N, H >= 0.  S must be 16-byte
  * aligned.  o must not alias S or any input.  Errors as for kla_chunk_fwd.
+ * The step is launched as a programmatic dependent of the previous kernel on
+ * `stream`: its blocks may be scheduled while that kernel's last blocks run,
+ * but each waits for that kernel, and its memory, before touching memory,
+ * so the ordering is that of plain stream order.  It allocates, synchronises
+ * and reads back nothing, so steps can be recorded in a CUDA graph.
  */
 KLA_API kla_status kla_decode_step(const void* q, const void* k, const void* v,
                            const float* log_alpha, const float* eta, float eps,

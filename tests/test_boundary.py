@@ -129,6 +129,24 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises(TypeError):
         kla.decode_step(x[0], x[0], x[0], la[0], la[0],
                         torch.zeros(4, 1, 16, 16))
+    with pytest.raises(TypeError):
+        kla.chunk_fwd_seq(x, x, x, la, la)
+    with pytest.raises(TypeError):
+        kla.chunk_fwd_kw(x, x, x, x, la, la)
+    with pytest.raises(TypeError):
+        kla.precond_keys(x)
+
+
+def test_host_binding_checks_its_inputs_before_any_device_call():
+    import torch
+    x = torch.zeros(1, 4, 1, 16)
+    la = torch.zeros(1, 4, 1)
+    with pytest.raises(ValueError):          # not contiguous
+        kla.chunk_fwd_host(x.transpose(1, 3), x, x, la, la)
+    with pytest.raises(TypeError):           # gates must be fp32
+        kla.chunk_fwd_host(x, x, x, la.double(), la)
+    with pytest.raises(TypeError):           # q, k, v share one dtype
+        kla.chunk_fwd_host(x, x.double(), x, la, la)
 
 
 def bwd(lib, *, ws_bytes=1 << 20, ws=ctypes.c_void_p(0x9000), B=1, T=8, H=1,

@@ -23,6 +23,8 @@
 // they move kw by a few 1e-6 relative, far inside the 1e-4 bound), with
 // tanh written through the exponential.
 #include <cooperative_groups.h>
+#include <cstdint>
+#include <type_traits>
 
 #include "kla_internal.cuh"
 
@@ -36,7 +38,47 @@ constexpr int kPrecondWarps = 32;
 constexpr int kPrecondThreads = kPrecondWarps * 32;
 constexpr int kTokBatch = 4;   // tokens loaded ahead of their use
 
-template <int DK, typename IO>
+// A lane's DPL consecutive key dimensions: one 16-byte (fp32) or 8-byte
+// (bf16) access when VEC (DPL == 4, tensors 16-byte aligned), else DPL
+// scalar ones.
+template <bool VEC, int DPL, typename IO>
+__device__ __forceinline__ void ld_dims(const IO* p, float (&x)[DPL]) {
+    if constexpr (VEC && DPL == 4) {
+        if constexpr (std::is_same<IO, float>::value) {
+            const float4 v = *reinterpret_cast<const float4*>(p);
+            x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+        } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(p);
+            x[0] = __uint_as_float(v.x << 16);
+            x[1] = __uint_as_float(v.x & 0xffff0000u);
+            x[2] = __uint_as_float(v.y << 16);
+            x[3] = __uint_as_float(v.y & 0xffff0000u);
+        }
+    } else {
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) x[d] = to_f32(p[d]);
+    }
+}
+
+template <bool VEC, int DPL, typename IO>
+__device__ __forceinline__ void st_dims(IO* p, const float (&x)[DPL]) {
+    if constexpr (VEC && DPL == 4) {
+        if constexpr (std::is_same<IO, float>::value) {
+            *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+        } else {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(x[2], x[3]);
+            *reinterpret_cast<uint2*>(p) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                           *reinterpret_cast<const uint32_t*>(&hi));
+        }
+    } else {
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) p[d] = from_f32<IO>(x[d]);
+    }
+}
+
+template <int DK, typename IO, bool VEC>
 __global__ void __cluster_dims__(kClusterCtas, 1, 1)
     __launch_bounds__(kPrecondThreads, 1)
     kla_precond_keys_kernel(PrecondArgs a) {
@@ -63,22 +105,26 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1)
     const int t_lo = min(c_hi, c_lo + warp * per_warp);
     const int t_hi = min(c_hi, t_lo + per_warp);
 
-    const IO* k = static_cast<const IO*>(a.k);
-    IO* kw = static_cast<IO*>(a.kw);
-    auto row = [&](int t) {
-        return (((size_t)b * T + t) * H + h) * DK + d0;
-    };
+    // this lane's dimensions of the warp's first token; a token is H DK
+    // elements further
+    const size_t tstride = (size_t)H * DK;
+    const size_t first = (((size_t)b * T + t_lo) * H + h) * DK + d0;
+    const IO* kb = static_cast<const IO*>(a.k) + first;
+    IO* wb = static_cast<IO*>(a.kw) + first;
 
     // ---- pass 1: sum of k^2 over the sub-slice ----
     float sq[DPL] = {};
     for (int t = t_lo; t < t_hi; t += kTokBatch) {
         float kv[kTokBatch][DPL];
 #pragma unroll
-        for (int u = 0; u < kTokBatch; ++u)
+        for (int u = 0; u < kTokBatch; ++u) {
+            if (live && t + u < t_hi) {
+                ld_dims<VEC>(kb + (size_t)(t + u - t_lo) * tstride, kv[u]);
+            } else {
 #pragma unroll
-            for (int d = 0; d < DPL; ++d)
-                kv[u][d] = (live && t + u < t_hi) ? to_f32(k[row(t + u) + d])
-                                                  : 0.f;
+                for (int d = 0; d < DPL; ++d) kv[u][d] = 0.f;
+            }
+        }
 #pragma unroll
         for (int u = 0; u < kTokBatch; ++u)
 #pragma unroll
@@ -118,11 +164,14 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1)
     for (int t = t_lo; t < t_hi; t += kTokBatch) {
         float kv[kTokBatch][DPL];
 #pragma unroll
-        for (int u = 0; u < kTokBatch; ++u)
+        for (int u = 0; u < kTokBatch; ++u) {
+            if (live && t + u < t_hi) {
+                ld_dims<VEC>(kb + (size_t)(t + u - t_lo) * tstride, kv[u]);
+            } else {
 #pragma unroll
-            for (int d = 0; d < DPL; ++d)
-                kv[u][d] = (live && t + u < t_hi) ? to_f32(k[row(t + u) + d])
-                                                  : 0.f;
+                for (int d = 0; d < DPL; ++d) kv[u][d] = 0.f;
+            }
+        }
 #pragma unroll
         for (int u = 0; u < kTokBatch; ++u) {
             if (t + u >= t_hi) break;   // warp-uniform
@@ -138,6 +187,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1)
                 s += __shfl_xor_sync(0xffffffffu, s, o);
             if (live) {
                 const float mean = s * inv_dk;
+                float w[DPL];
 #pragma unroll
                 for (int d = 0; d < DPL; ++d) {
                     // tanh(y) = 1 - 2 / (e^{2y} + 1), 2y kept in [-40, 40]
@@ -145,24 +195,33 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1)
                     const float y2 = fminf(fmaxf(2.f * (mean - l[d]) * inv_lx,
                                                  -40.f), 40.f);
                     const float th = 1.f - __fdividef(2.f, __expf(y2) + 1.f);
-                    kw[row(t + u) + d] = from_f32<IO>(__expf(lx * th) *
-                                                      kv[u][d]);
+                    w[d] = __expf(lx * th) * kv[u][d];
                 }
+                st_dims<VEC>(wb + (size_t)(t + u - t_lo) * tstride, w);
             }
         }
     }
 }
 
-template <int DK>
-cudaError_t launch_dk(const PrecondArgs& a, cudaStream_t stream) {
+template <int DK, typename IO>
+cudaError_t launch_io(const PrecondArgs& a, cudaStream_t stream) {
     const unsigned grid = (unsigned)((long)a.B * a.H * kClusterCtas);
-    if (a.dtype == KLA_BF16)
-        kla_precond_keys_kernel<DK, __nv_bfloat16>
+    auto al16 = [](const void* p) {
+        return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+    };
+    if (DK == 128 && al16(a.k) && al16(a.kw))
+        kla_precond_keys_kernel<DK, IO, true>
             <<<grid, kPrecondThreads, 0, stream>>>(a);
     else
-        kla_precond_keys_kernel<DK, float>
+        kla_precond_keys_kernel<DK, IO, false>
             <<<grid, kPrecondThreads, 0, stream>>>(a);
     return cudaGetLastError();
+}
+
+template <int DK>
+cudaError_t launch_dk(const PrecondArgs& a, cudaStream_t stream) {
+    if (a.dtype == KLA_BF16) return launch_io<DK, __nv_bfloat16>(a, stream);
+    return launch_io<DK, float>(a, stream);
 }
 
 }  // namespace

@@ -293,3 +293,23 @@ def test_seq_fwd_workspace_size_and_host_checks(lib):
     assert call(ws=None) == INVALID
     assert call(ws_bytes=1024) == INVALID
     assert call(ws=ctypes.c_void_p(0x10010)) == INVALID
+
+
+def declared_arities():
+    """Entry point -> number of parameters, parsed from include/kla.h."""
+    text = open(HEADER).read()
+    out = {}
+    for m in re.finditer(r"KLA_API\s+[\w\s\*]+?\b(kla_\w+)\s*\(([^)]*)\)",
+                         text):
+        params = [p for p in m.group(2).split(",") if p.strip()]
+        if len(params) == 1 and params[0].strip() == "void":
+            params = []
+        out[m.group(1)] = len(params)
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    arities = declared_arities()
+    assert set(arities) == set(declared_symbols())
+    for name, n in arities.items():
+        assert len(kla.SIGNATURES[name][1]) == n, name

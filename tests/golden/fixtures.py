@@ -28,3 +28,19 @@ def worked_example_2x2():
                 log_alpha=np.log(alpha).reshape(1, len(toks), 1),
                 eta=eta.reshape(1, len(toks), 1), eps=0.0,
                 o=shape(o), hT=np.array(state).reshape(1, 1, 2, 2))
+
+
+def precond_squash_2d():
+    """x, delta, A0 [1, 1, 2], k [1, 1, 1, 2], expected write key kw
+    [1, 1, 1, 2] and A_T [1, 1, 2] of precond_squash_2d.txt (float64)."""
+    vals = {}
+    with open(os.path.join(HERE, "precond_squash_2d.txt")) as f:
+        for line in f:
+            parts = line.split()
+            if not parts or parts[0].startswith("#"):
+                continue
+            vals[parts[0]] = np.array([float(x) for x in parts[1:]])
+    return dict(x=float(vals["x"][0]), delta=float(vals["delta"][0]),
+                A0=vals["A0"].reshape(1, 1, 2), k=vals["k"].reshape(1, 1, 1, 2),
+                kw=vals["kw"].reshape(1, 1, 1, 2),
+                AT=vals["AT"].reshape(1, 1, 2))

@@ -628,3 +628,75 @@ def test_precond_segments_resume_with_second_moments():
                                     et[:, 9:], eps, h1, A0=A1)
     assert _rel(np.concatenate([o1, o2], 1), o) < 1e-13
     assert _rel(h2, hT) < 1e-13 and _rel(A2, A) < 1e-14
+
+
+def test_precond_golden_squash_value():
+    """tests/golden/precond_squash_2d.txt: the gain worked by hand for
+    A_1 = (1, 4), x = 1.5 (adjacent page "preconditioned DeltaNet", section
+    "Aproximacion Diagonal"; the squash is this library's reading, slope 1
+    at z = 0, stated in the fixture).  The oracle's write key and second
+    moments match the hand values to 1e-12."""
+    from golden.fixtures import precond_squash_2d
+    g = precond_squash_2d()
+    k = g["k"]
+    z = np.zeros((1, 1, 1))
+    _, _, A, kw = oracle.pkla_fwd(np.zeros_like(k), k, np.zeros((1, 1, 1, 1)),
+                                  z, np.ones((1, 1, 1)), 1e-6, None,
+                                  A0=g["A0"], x=g["x"], delta=g["delta"])
+    np.testing.assert_allclose(kw, g["kw"], rtol=1e-12, atol=0)
+    np.testing.assert_allclose(A, g["AT"], rtol=0, atol=1e-15)
+
+
+def _gain(A_t, x, delta=0.0):
+    """P_t of the oracle for the second moments A_t [dk] (one token with
+    k = 1 and A_0 = A_t - 1, so that kw = P_t)."""
+    dk = A_t.shape[0]
+    k = np.ones((1, 1, 1, dk))
+    _, _, _, kw = oracle.pkla_fwd(np.zeros_like(k), k, np.zeros((1, 1, 1, 1)),
+                                  np.zeros((1, 1, 1)), np.ones((1, 1, 1)),
+                                  1e-6, None, A0=(A_t - 1.0).reshape(1, 1, dk),
+                                  x=x, delta=delta)
+    return kw.reshape(dk)
+
+
+def test_precond_gain_is_inverse_second_moment_to_first_order():
+    """Near equal second moments the squash is the identity in log space
+    (slope 1 at z = 0), so the gain is P_t proportional to Diag(A_t)^{-1}
+    to first order, as the page's P_t ~ Diag(A_t)^{-1} says: ln(P_i A_i) is
+    the same for every i up to O(z^3) terms, and ln P_i / z_i -> 1 with z_i
+    the log of the geometric mean of A over A_i."""
+    rng = np.random.default_rng(75)
+    dk = 8
+    for s in (1e-3, 1e-4):
+        lnA = rng.standard_normal(dk) * s
+        A_t = 2.0 * np.exp(lnA)
+        P = _gain(A_t, 1.5)
+        z = np.mean(lnA) - lnA
+        # ln x tanh(z / ln x) = z - z^3 / (3 ln^2 x) + ...: the departures
+        # from the first-order law are third order in z
+        zm, l2x = np.max(np.abs(z)), np.log(1.5) ** 2
+        lnPA = np.log(P) + np.log(A_t)
+        assert np.ptp(lnPA) < zm ** 3 / l2x + 1e-13, (s, np.ptp(lnPA))
+        slope = np.log(P) / z
+        assert np.max(np.abs(slope - 1.0)) < zm ** 2 / l2x + 1e-8, (s, slope)
+
+
+def test_precond_pins_reject_other_slopes():
+    """The two pins above tell the reading apart from plausible mistakes in
+    the squash: gains computed (here, on the CPU) with the slope ln x at
+    z = 0, exp(ln x tanh(z)), or with slope 2, exp(ln x tanh(2 z / ln x)),
+    miss the hand value and the first-order law P ~ Diag(A)^{-1}."""
+    from golden.fixtures import precond_squash_2d
+    g = precond_squash_2d()
+    lx = np.log(g["x"])
+    z0 = np.log(2.0)          # A_1 = (1, 4): z_0 = ln 2
+    planted = {"tanh(z)": lambda z: np.exp(lx * np.tanh(z)),
+               "tanh(2z/ln x)": lambda z: np.exp(lx * np.tanh(2 * z / lx))}
+    for name, gain in planted.items():
+        assert abs(gain(z0) - g["kw"][0, 0, 0, 0]) > 1e-3, name
+        s = 1e-4
+        z = np.array([s, -s])
+        P = gain(z)
+        A_t = np.exp(-z)              # log-centred second moments
+        lnPA = np.log(P) + np.log(A_t)
+        assert np.ptp(lnPA) > 1e-5, name

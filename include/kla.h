@@ -100,7 +100,9 @@ typedef struct CUstream_st* kla_stream_t;
  *
  * Supported: dk, dv in {16, 32, 64, 128}; C in {16, 32, 64}; any T >= 0
  * (a ragged last chunk is handled in-kernel); B, H >= 0.  T == 0 copies h0
- * (or zeros) to hT.  o must not alias any input; hT may alias h0.
+ * (or zeros) to hT.  o must not overlap any input or hT, and hT must not
+ * overlap any input other than h0, which it may equal exactly (byte ranges
+ * from the sizes; KLA_ERR_INVALID_ARG otherwise).
  * Errors: KLA_ERR_INVALID_ARG (null required pointer, negative size,
  * eps < 0 or not finite, bad dtype), KLA_ERR_UNSUPPORTED_SHAPE, KLA_ERR_CUDA.
  */
@@ -148,7 +150,8 @@ KLA_API kla_status kla_chunk_fwd_seq_workspace_size(int B, int T, int H,
  * with B_s, O0_s from the segment run from a zero state and Phi_s, O_hom,s
  * from the run from the identity with V = 0.  Both runs are the forward
  * kernel over the B P segments (at the same time, on `stream` and on a
- * second stream of the library); a small kernel chains S_{s+1} =
+ * second stream of the library; with B = 1 the second run skips segment 0,
+ * whose Phi and O_hom are not needed); a small kernel chains S_{s+1} =
  * Phi_s S_s + B_s and a tensor-core kernel adds O_hom,s S_s to o of every
  * segment after the first.  The pages have no counterpart: it reorders the
  * sums of the chunkwise form, so o and hT equal kla_chunk_fwd_ex's up to
@@ -247,7 +250,8 @@ KLA_API kla_status kla_chunk_fwd_host(const void* q, const void* k,
  *   o          [N, H, dv]      dtype   (written) = S_t^T q
  *
  * Supported: dk, dv in {16, 32, 64, 128}; N, H >= 0.  S must be 16-byte
- * aligned.  o must not alias S or any input.  Errors as for kla_chunk_fwd.
+ * aligned.  o and S must not overlap each other or any input (byte
+ * ranges).  Errors as for kla_chunk_fwd.
  * The step is launched as a programmatic dependent of the previous kernel on
  * `stream`: its blocks may be scheduled while that kernel's last blocks run,
  * but each waits for that kernel, and its memory, before touching memory,
@@ -290,8 +294,9 @@ KLA_API kla_status kla_decode_step_ex(const void* q, const void* k,
  *
  *   k        [B, T, H, dk]  dtype  (read)
  *   A0       [B, H, dk]     fp32   (read) or NULL (zero)
- *   k_write  [B, T, H, dk]  dtype  (written); must not alias k
- *   AT       [B, H, dk]     fp32   (written: A_T) or NULL; may alias A0
+ *   k_write  [B, T, H, dk]  dtype  (written); must not overlap k, A0, AT
+ *   AT       [B, H, dk]     fp32   (written: A_T) or NULL; may equal A0
+ *            exactly, must not overlap it or k otherwise
  *   x > 1 (the page uses about 1.5), delta >= 0
  * Supported dk as for kla_chunk_fwd.  Errors: KLA_ERR_INVALID_ARG,
  * KLA_ERR_UNSUPPORTED_SHAPE, KLA_ERR_CUDA.
@@ -309,7 +314,7 @@ KLA_API kla_status kla_precond_keys(const void* k, const float* A0,
  * K.  Runs on the tensor-core kernel (its write-key mode) where
  * kla_chunk_fwd_ex's KLA_ALGO_AUTO would (bf16, dk = dv = 128, C = 64,
  * 16-byte-aligned tensors, k_write included), else on the CUDA-core kernel.
- * k_write must not alias o.  Errors as for kla_chunk_fwd_ex (NULL k_write is
+ * k_write must not overlap o.  Errors as for kla_chunk_fwd_ex (NULL k_write is
  * KLA_ERR_INVALID_ARG).
  */
 KLA_API kla_status kla_chunk_fwd_kw(const void* q, const void* k,
@@ -372,10 +377,13 @@ KLA_API kla_status kla_chunk_bwd_workspace_size(int B, int T, int H, int dk,
  * it); the reverse recurrence of dL/dS over the chunks (on the tensor cores
  * with tf32 operands for bf16, dk = 128, C = 64 and 16-byte-aligned q, k,
  * o_grad; else on the CUDA cores in fp32); the per-chunk gradients (CUDA
- * cores, fp32).  Supported shapes as for kla_chunk_fwd.  Outputs must not alias inputs, each other or the
- * workspace.  Errors: KLA_ERR_INVALID_ARG (null required pointer, negative
- * size, bad enum, eps < 0 or not finite, workspace too small or misaligned),
- * KLA_ERR_UNSUPPORTED_SHAPE, KLA_ERR_CUDA.
+ * cores, fp32).  Supported shapes as for kla_chunk_fwd.  No output may
+ * overlap an input, another output or the workspace, and the workspace may
+ * overlap no input (byte ranges from the sizes).  Errors:
+ * KLA_ERR_INVALID_ARG (null required pointer, negative size, bad enum,
+ * eps < 0 or not finite, overlapping buffers, workspace too small or
+ * misaligned), KLA_ERR_UNSUPPORTED_SHAPE, KLA_ERR_CUDA; the argument checks
+ * come before those on the workspace.
  */
 KLA_API kla_status kla_chunk_bwd(const void* q, const void* k, const void* v,
                                  const float* log_alpha, const float* eta,
@@ -398,13 +406,18 @@ KLA_API kla_status kla_chunk_bwd(const void* q, const void* k, const void* v,
  *
  * Arguments and results are those of kla_chunk_bwd without the workspace:
  * its scratch is a fixed 32 MiB array inside the library (every GPU that
- * loads the library holds it until the process exits).  A problem whose
- * kla_chunk_bwd_workspace_size exceeds 32 MiB is rejected with
- * KLA_ERR_UNSUPPORTED_SHAPE before anything is launched.
+ * loads the library holds it until the process exits).  The argument checks
+ * of kla_chunk_bwd run first (KLA_ERR_INVALID_ARG, KLA_ERR_UNSUPPORTED_SHAPE);
+ * then a problem whose kla_chunk_bwd_workspace_size exceeds 32 MiB (for
+ * dk = dv = 128: B * H * ceil(T / C) > 256) is rejected with
+ * KLA_ERR_UNSUPPORTED_SHAPE.  Either way nothing is launched.
  *
- * The first call on a device looks up the array's device address (with that
- * device current; a failure returns KLA_ERR_CUDA); make that first call
- * before any stream capture.  Every call shares the one array and leaves its
+ * Every call made outside a stream capture looks up the array's device
+ * address on the current device (a failure returns KLA_ERR_CUDA), so an
+ * address from before a cudaDeviceReset is never reused; a call made while
+ * `stream` is being captured uses the address of the last such lookup on
+ * that device, so the first call on a device must come before any capture
+ * (else KLA_ERR_CUDA).  Every call shares the one array and leaves its
  * contents behind; nothing in it has to start at zero.  Calls that overlap
  * on the GPU (on different streams, or from different host threads, on the
  * same device) race on the array: serialise them.

@@ -19,6 +19,33 @@ kla_status from_cuda(cudaError_t e) {
     return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
 }
 
+// A buffer of the call: start and length in bytes (null or empty: none).
+struct Span {
+    const void* p;
+    size_t n;
+};
+
+// True when the byte ranges of a and b share at least one byte.
+bool overlap(Span a, Span b) {
+    if (!a.p || !b.p || a.n == 0 || b.n == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p);
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
+// True when any written span overlaps any read span, or two written spans
+// overlap each other.
+template <size_t NI, size_t NO>
+bool any_overlap(const Span (&ins)[NI], const Span (&outs)[NO]) {
+    for (size_t i = 0; i < NO; ++i) {
+        for (size_t j = 0; j < NI; ++j)
+            if (overlap(outs[i], ins[j])) return true;
+        for (size_t j = i + 1; j < NO; ++j)
+            if (overlap(outs[i], outs[j])) return true;
+    }
+    return false;
+}
+
 }  // namespace
 
 // Forward pass with optional separate write keys kw (null: the keys).
@@ -50,10 +77,24 @@ static kla_status chunk_fwd_impl(const void* q, const void* k, const void* kw,
             !aligned(o, elt) || !aligned(log_alpha, 4) || !aligned(eta, 4) ||
             (kw && !aligned(kw, elt)))
             return KLA_ERR_INVALID_ARG;
-        if (o == q || o == k || o == v || o == (const void*)log_alpha ||
-            o == (const void*)eta || o == (const void*)h0 || o == (void*)hT ||
-            (kw && o == kw))
+        // o must not overlap any input or hT (hT may alias h0 exactly: the
+        // state is read before it is written)
+        const size_t tok = (size_t)B * T * H;
+        const size_t st = sizeof(float) * (size_t)B * H * dk * dv;
+        const Span ins[] = {{q, tok * dk * elt}, {k, tok * dk * elt},
+                            {v, tok * dv * elt}, {log_alpha, tok * 4},
+                            {eta, tok * 4}, {kw, tok * dk * elt}, {h0, st}};
+        const Span outs[] = {{o, tok * dv * elt}};
+        if (any_overlap(ins, outs) || overlap({o, tok * dv * elt}, {hT, st}))
             return KLA_ERR_INVALID_ARG;
+        if (hT && (const void*)hT != (const void*)h0) {
+            const Span ins2[] = {{q, tok * dk * elt}, {k, tok * dk * elt},
+                                 {v, tok * dv * elt}, {log_alpha, tok * 4},
+                                 {eta, tok * 4}, {kw, tok * dk * elt},
+                                 {h0, st}};
+            const Span outs2[] = {{hT, st}};
+            if (any_overlap(ins2, outs2)) return KLA_ERR_INVALID_ARG;
+        }
     }
     if ((h0 && !aligned(h0, 4)) || (hT && !aligned(hT, 4)))
         return KLA_ERR_INVALID_ARG;
@@ -124,10 +165,22 @@ extern "C" kla_status kla_precond_keys(const void* k, const float* A0,
     if ((long long)B * H == 0) return KLA_OK;
     const size_t elt = dtype == KLA_BF16 ? 2 : 4;
     if (T > 0 && (!k || !k_write || !aligned(k, elt) ||
-                  !aligned(k_write, elt) || k == k_write))
+                  !aligned(k_write, elt)))
         return KLA_ERR_INVALID_ARG;
     if ((A0 && !aligned(A0, 4)) || (AT && !aligned(AT, 4)))
         return KLA_ERR_INVALID_ARG;
+    {   // k_write must not overlap k, A0 or AT; AT may equal A0 exactly
+        const size_t kb = (size_t)B * T * H * dk * elt;
+        const size_t ab = sizeof(float) * (size_t)B * H * dk;
+        const Span ins[] = {{k, kb}, {A0, ab}};
+        const Span outs[] = {{T > 0 ? k_write : nullptr, kb}};
+        if (any_overlap(ins, outs) || overlap({T > 0 ? k_write : nullptr, kb},
+                                              {AT, ab}))
+            return KLA_ERR_INVALID_ARG;
+        if ((const void*)AT != (const void*)A0 &&
+            (overlap({AT, ab}, {A0, ab}) || overlap({AT, ab}, {k, kb})))
+            return KLA_ERR_INVALID_ARG;
+    }
     kla::PrecondArgs a{k, A0, k_write, AT, B, T, H, dk, x, delta, dtype};
     return from_cuda(
         kla::launch_precond_keys(a, reinterpret_cast<cudaStream_t>(stream)));
@@ -166,8 +219,16 @@ static kla_status decode_impl(const void* q, const void* k, const void* kw,
         !aligned(o, elt) || !aligned(log_alpha, 4) || !aligned(eta, 4) ||
         !aligned(S, 16) || (kw && !aligned(kw, elt)))
         return KLA_ERR_INVALID_ARG;
-    if (o == (void*)S || o == q || o == k || o == v || (kw && o == kw))
-        return KLA_ERR_INVALID_ARG;
+    {   // o must not overlap S or any input; S is updated in place and
+        // must not overlap the token inputs either
+        const size_t nh = (size_t)N * H;
+        const Span ins[] = {{q, nh * dk * elt}, {k, nh * dk * elt},
+                            {v, nh * dv * elt}, {log_alpha, nh * 4},
+                            {eta, nh * 4}, {kw, nh * dk * elt}};
+        const Span outs[] = {{o, nh * dv * elt},
+                             {S, sizeof(float) * nh * dk * dv}};
+        if (any_overlap(ins, outs)) return KLA_ERR_INVALID_ARG;
+    }
     kla::DecodeArgs a{q, k, v, log_alpha, eta, eps,
                       rule == KLA_STEP_GIVEN ? 1 : 0, S, o, N, H, dk, dv,
                       dtype};
@@ -217,6 +278,51 @@ extern "C" kla_status kla_chunk_bwd_workspace_size(int B, int T, int H,
     return KLA_OK;
 }
 
+namespace kla {
+
+// Every check of kla_chunk_bwd except those on the workspace.
+kla_status check_chunk_bwd_args(const BwdArgs& a) {
+    const int B = a.B, T = a.T, H = a.H, dk = a.dk, dv = a.dv, C = a.C;
+    if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || C <= 0)
+        return KLA_ERR_INVALID_ARG;
+    if (a.dtype != KLA_F32 && a.dtype != KLA_BF16) return KLA_ERR_INVALID_ARG;
+    if (!(a.eps >= 0.f) || !std::isfinite(a.eps)) return KLA_ERR_INVALID_ARG;
+    if (!supported_dim(dk) || !supported_dim(dv) || !supported_chunk(C))
+        return KLA_ERR_UNSUPPORTED_SHAPE;
+    const long long nch = ((long long)T + C - 1) / C;
+    if ((long long)B * H > 0x7fffffffLL ||
+        (long long)B * H * nch > 0x7fffffffLL)
+        return KLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H > 0 && T > 0) {
+        if (!a.q || !a.k || !a.v || !a.log_alpha || !a.eta || !a.dout ||
+            !a.dq || !a.dk_ || !a.dv_ || !a.dlog_alpha || !a.deta)
+            return KLA_ERR_INVALID_ARG;
+        const size_t elt = a.dtype == KLA_BF16 ? 2 : 4;
+        if (!aligned(a.q, elt) || !aligned(a.k, elt) || !aligned(a.v, elt) ||
+            !aligned(a.dout, elt) || !aligned(a.dq, elt) ||
+            !aligned(a.dk_, elt) || !aligned(a.dv_, elt) ||
+            !aligned(a.log_alpha, 4) || !aligned(a.eta, 4) ||
+            !aligned(a.dlog_alpha, 4) || !aligned(a.deta, 4))
+            return KLA_ERR_INVALID_ARG;
+        const size_t tok = (size_t)B * T * H;
+        const size_t st = sizeof(float) * (size_t)B * H * dk * dv;
+        const Span ins[] = {{a.q, tok * dk * elt}, {a.k, tok * dk * elt},
+                            {a.v, tok * dv * elt}, {a.log_alpha, tok * 4},
+                            {a.eta, tok * 4}, {a.h0, st},
+                            {a.dout, tok * dv * elt}, {a.dhT, st}};
+        const Span outs[] = {{a.dq, tok * dk * elt}, {a.dk_, tok * dk * elt},
+                             {a.dv_, tok * dv * elt}, {a.dlog_alpha, tok * 4},
+                             {a.deta, tok * 4}, {a.dh0, st}};
+        if (any_overlap(ins, outs)) return KLA_ERR_INVALID_ARG;
+    }
+    if ((a.h0 && !aligned(a.h0, 4)) || (a.dhT && !aligned(a.dhT, 4)) ||
+        (a.dh0 && !aligned(a.dh0, 4)))
+        return KLA_ERR_INVALID_ARG;
+    return KLA_OK;
+}
+
+}  // namespace kla
+
 extern "C" kla_status kla_chunk_bwd(
     const void* q, const void* k, const void* v, const float* log_alpha,
     const float* eta, float eps, const float* h0, const void* o_grad,
@@ -224,50 +330,34 @@ extern "C" kla_status kla_chunk_bwd(
     float* log_alpha_grad, float* eta_grad, float* h0_grad, int B, int T,
     int H, int dk, int dv, int C, kla_dtype dtype, kla_step_rule rule,
     void* workspace, size_t workspace_bytes, kla_stream_t stream) {
-    if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || C <= 0)
-        return KLA_ERR_INVALID_ARG;
-    if (dtype != KLA_F32 && dtype != KLA_BF16) return KLA_ERR_INVALID_ARG;
     if (rule != KLA_STEP_KACZMARZ && rule != KLA_STEP_GIVEN)
         return KLA_ERR_INVALID_ARG;
-    if (!(eps >= 0.f) || !std::isfinite(eps)) return KLA_ERR_INVALID_ARG;
-    if (!supported_dim(dk) || !supported_dim(dv) || !supported_chunk(C))
-        return KLA_ERR_UNSUPPORTED_SHAPE;
-    const long long nch = ((long long)T + C - 1) / C;
-    if ((long long)B * H > 0x7fffffffLL ||
-        (long long)B * H * nch > 0x7fffffffLL)
-        return KLA_ERR_UNSUPPORTED_SHAPE;
+    kla::BwdArgs a{q, k, v, log_alpha, eta, eps,
+                   rule == KLA_STEP_GIVEN ? 1 : 0, h0, o_grad, hT_grad,
+                   q_grad, k_grad, v_grad, log_alpha_grad, eta_grad, h0_grad,
+                   nullptr, nullptr, B, T, H, dk, dv, C, dtype};
+    const kla_status st = kla::check_chunk_bwd_args(a);
+    if (st != KLA_OK) return st;
     const bool empty = (long long)B * H == 0;
     if (!empty && T > 0) {
-        if (!q || !k || !v || !log_alpha || !eta || !o_grad || !q_grad ||
-            !k_grad || !v_grad || !log_alpha_grad || !eta_grad || !workspace)
-            return KLA_ERR_INVALID_ARG;
+        if (!workspace || !aligned(workspace, 16)) return KLA_ERR_INVALID_ARG;
+        const size_t need =
+            sizeof(float) * kla::chunk_bwd_workspace_floats(B, T, H, dk, dv, C);
+        if (workspace_bytes < need) return KLA_ERR_INVALID_ARG;
         const size_t elt = dtype == KLA_BF16 ? 2 : 4;
-        if (!aligned(q, elt) || !aligned(k, elt) || !aligned(v, elt) ||
-            !aligned(o_grad, elt) || !aligned(q_grad, elt) ||
-            !aligned(k_grad, elt) || !aligned(v_grad, elt) ||
-            !aligned(log_alpha, 4) || !aligned(eta, 4) ||
-            !aligned(log_alpha_grad, 4) || !aligned(eta_grad, 4) ||
-            !aligned(workspace, 16))
-            return KLA_ERR_INVALID_ARG;
-        const void* ins[] = {q, k, v, log_alpha, eta, h0, o_grad, hT_grad};
-        const void* outs[] = {q_grad, k_grad, v_grad, log_alpha_grad,
-                              eta_grad, h0_grad, workspace};
-        for (const void* out : outs) {
-            if (!out) continue;
-            for (const void* in : ins)
-                if (in == out) return KLA_ERR_INVALID_ARG;
-            int same = 0;
-            for (const void* o2 : outs) same += (o2 == out);
-            if (same > 1) return KLA_ERR_INVALID_ARG;
-        }
-        if (workspace_bytes <
-            sizeof(float) * kla::chunk_bwd_workspace_floats(B, T, H, dk, dv,
-                                                            C))
-            return KLA_ERR_INVALID_ARG;
+        const size_t tok = (size_t)B * T * H;
+        const size_t st = sizeof(float) * (size_t)B * H * dk * dv;
+        const Span bufs[] = {{q, tok * dk * elt}, {k, tok * dk * elt},
+                             {v, tok * dv * elt}, {log_alpha, tok * 4},
+                             {eta, tok * 4}, {h0, st},
+                             {o_grad, tok * dv * elt}, {hT_grad, st},
+                             {q_grad, tok * dk * elt}, {k_grad, tok * dk * elt},
+                             {v_grad, tok * dv * elt},
+                             {log_alpha_grad, tok * 4}, {eta_grad, tok * 4},
+                             {h0_grad, st}};
+        const Span ws[] = {{workspace, need}};
+        if (any_overlap(bufs, ws)) return KLA_ERR_INVALID_ARG;
     }
-    if ((h0 && !aligned(h0, 4)) || (hT_grad && !aligned(hT_grad, 4)) ||
-        (h0_grad && !aligned(h0_grad, 4)))
-        return KLA_ERR_INVALID_ARG;
     if (empty) return KLA_OK;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -281,10 +371,8 @@ extern "C" kla_status kla_chunk_bwd(
     }
     const size_t half = kla::chunk_bwd_workspace_floats(B, T, H, dk, dv, C) / 2;
     float* ws = static_cast<float*>(workspace);
-    kla::BwdArgs a{q, k, v, log_alpha, eta, eps,
-                   rule == KLA_STEP_GIVEN ? 1 : 0, h0, o_grad, hT_grad,
-                   q_grad, k_grad, v_grad, log_alpha_grad, eta_grad, h0_grad,
-                   ws, ws + half, B, T, H, dk, dv, C, dtype};
+    a.ckpt = ws;
+    a.dsck = ws + half;
     return from_cuda(kla::launch_chunk_bwd(a, s));
 }
 

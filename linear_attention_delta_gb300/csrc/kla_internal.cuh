@@ -108,6 +108,9 @@ bool chunk_tc_eligible(const FwdArgs& a);
 cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_precond_keys(const PrecondArgs& a, cudaStream_t stream);
 size_t chunk_bwd_workspace_floats(int B, int T, int H, int dk, int dv, int C);
+// Every argument check of kla_chunk_bwd except those on the workspace and
+// the step rule (a.ckpt, a.dsck are not looked at).
+kla_status check_chunk_bwd_args(const BwdArgs& a);
 // SM count of the current device (cached per device).
 int device_sm_count();
 

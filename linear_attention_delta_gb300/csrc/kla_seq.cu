@@ -11,7 +11,9 @@
 // [B P, T / P, H, d]); they run at the same time on two streams.  A small
 // kernel then chains the start states, S_{s+1} = Phi_s S_s + B_s, and a
 // tensor-core kernel adds O_hom,s S_s to the outputs of every segment after
-// the first (whose run started from the true initial state).
+// the first (whose run started from the true initial state).  With one
+// sequence the homogeneous run skips the first segment, whose Phi and O_hom
+// are never used.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -382,6 +384,20 @@ extern "C" kla_status kla_chunk_fwd_seq(
     kla::FwdArgs hom{q, k, zero, log_alpha, eta, eps, gdn, eye, ohom, phi,
                      B * P, tseg, H, kD, kD, kC, KLA_BF16};
     hom.v_zero = true;
+    if (B == 1) {
+        // segment 0 starts from the true initial state, so its homogeneous
+        // run (Phi_0, O_hom,0) is never used: run segments 1 .. P-1 only,
+        // which are contiguous when there is one sequence
+        const size_t tok = (size_t)tseg * H;
+        hom.q = static_cast<const __nv_bfloat16*>(q) + tok * kD;
+        hom.k = static_cast<const __nv_bfloat16*>(k) + tok * kD;
+        hom.log_alpha = log_alpha + tok;
+        hom.eta = eta + tok;
+        hom.h0 = eye + (size_t)H * kD * kD;
+        hom.o = ohom + tok * kD;
+        hom.hT = phi + (size_t)H * kD * kD;
+        hom.B = P - 1;
+    }
     if (!kla::chunk_tc_eligible(zs)) return KLA_ERR_UNSUPPORTED_SHAPE;
     KLA_TRY(kla::launch_chunk_tc(zs, s));
     KLA_TRY(kla::launch_chunk_tc(hom, A.s));

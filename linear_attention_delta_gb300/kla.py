@@ -356,24 +356,37 @@ def chunk_bwd_noalloc(q, k, v, log_alpha, eta, o_grad, hT_grad=None,
             _check_cuda(n, t, torch.float32)
     if q.dtype not in DTYPES:
         raise TypeError(f"unsupported dtype {q.dtype}")
+    for n, t in (("k", k), ("v", v), ("o_grad", o_grad),
+                 ("log_alpha", log_alpha), ("eta", eta), ("h0", h0),
+                 ("hT_grad", hT_grad)):
+        if t is not None and t.device != q.device:
+            raise ValueError(f"{n} is on {t.device}, q on {q.device}")
     B, T, H, dk = k.shape
     dv = v.shape[-1]
-    out = dict(q_grad=torch.empty_like(q), k_grad=torch.empty_like(k),
-               v_grad=torch.empty_like(v),
-               log_alpha_grad=torch.empty_like(log_alpha),
-               eta_grad=torch.empty_like(eta),
-               h0_grad=(torch.empty((B, H, dk, dv), dtype=torch.float32,
-                                    device=q.device)
-                        if want_h0_grad else None))
-    st = load_library().kla_chunk_bwd_noalloc(
+    # the library takes the array of the current device and launches there
+    with torch.cuda.device(q.device):
+        out = dict(q_grad=torch.empty_like(q), k_grad=torch.empty_like(k),
+                   v_grad=torch.empty_like(v),
+                   log_alpha_grad=torch.empty_like(log_alpha),
+                   eta_grad=torch.empty_like(eta),
+                   h0_grad=(torch.empty((B, H, dk, dv), dtype=torch.float32,
+                                        device=q.device)
+                            if want_h0_grad else None))
+        st = _bwd_noalloc_call(q, k, v, log_alpha, eta, o_grad, hT_grad, eps,
+                               h0, C, rule, out, B, T, H, dk, dv, stream)
+    if st != KLA_OK:
+        raise KlaError("kla_chunk_bwd_noalloc", st)
+    return out
+
+
+def _bwd_noalloc_call(q, k, v, log_alpha, eta, o_grad, hT_grad, eps, h0, C,
+                      rule, out, B, T, H, dk, dv, stream):
+    return load_library().kla_chunk_bwd_noalloc(
         _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(eta), float(eps),
         _ptr(h0), _ptr(o_grad), _ptr(hT_grad), _ptr(out["q_grad"]),
         _ptr(out["k_grad"]), _ptr(out["v_grad"]), _ptr(out["log_alpha_grad"]),
         _ptr(out["eta_grad"]), _ptr(out["h0_grad"]), B, T, H, dk, dv, int(C),
         DTYPES[q.dtype], RULES[rule], _stream(stream))
-    if st != KLA_OK:
-        raise KlaError("kla_chunk_bwd_noalloc", st)
-    return out
 
 
 def precond_keys(k, A0=None, x: float = 1.5, delta: float = 1e-6,

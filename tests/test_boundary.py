@@ -313,3 +313,42 @@ def test_binding_signatures_match_the_header():
     assert set(arities) == set(declared_symbols())
     for name, n in arities.items():
         assert len(kla.SIGNATURES[name][1]) == n, name
+
+
+def _bufs(n):
+    """n distinct fake device addresses 4 GiB apart (never dereferenced)."""
+    return [0x10000 + (i << 32) for i in range(n)]
+
+
+def test_overlapping_buffers_are_refused_on_host(lib):
+    """o (and every other written buffer) may not share a byte with an input,
+    checked on byte ranges from the sizes rather than start pointers: an o
+    that starts inside q, an hT that starts inside h0 without being h0, a
+    decode o that runs into S, a gradient that starts inside o_grad."""
+    V = ctypes.c_void_p
+    q, k, v, la, eta, o, h0, hT = _bufs(8)
+    B, T, H, d = 1, 64, 2, 16
+    qbytes = B * T * H * d * 2                       # bf16
+    # o starting on the last element of q
+    assert fwd(lib, q=V(q), k=V(k), v=V(v), la=V(la), eta=V(eta),
+               o=V(q + qbytes - 2), B=B, T=T, H=H, dk=d, dv=d) == INVALID
+    # hT starting 4 bytes into h0: refused (hT == h0 exactly is allowed)
+    assert fwd(lib, q=V(q), k=V(k), v=V(v), la=V(la), eta=V(eta), o=V(o),
+               h0=V(h0), hT=V(h0 + 4), B=B, T=T, H=H, dk=d, dv=d) == INVALID
+    # hT inside k
+    assert fwd(lib, q=V(q), k=V(k), v=V(v), la=V(la), eta=V(eta), o=V(o),
+               hT=V(k + 64), B=B, T=T, H=H, dk=d, dv=d) == INVALID
+    # decode: o running into S, S running into v
+    N, Hd = 2, 2
+    S = h0
+    assert dec(lib, q=V(q), k=V(k), v=V(v), la=V(la), eta=V(eta), S=V(S),
+               o=V(S - 16), N=N, H=Hd) == INVALID
+    assert dec(lib, q=V(q), k=V(k), v=V(v), la=V(la), eta=V(eta),
+               S=V(v + 16), o=V(o), N=N, H=Hd) == INVALID
+    # backward: k_grad starting inside o_grad
+    b = _bufs(12)
+    st = lib.kla_chunk_bwd(V(b[0]), V(b[1]), V(b[2]), V(b[3]), V(b[4]), 1e-6,
+                           None, V(b[5]), None, V(b[6]), V(b[5] + 32),
+                           V(b[8]), V(b[9]), V(b[10]), None, 1, 64, 2, 16, 16,
+                           16, 1, 0, V(b[11]), 1 << 20, None)
+    assert st == INVALID

@@ -678,6 +678,18 @@ def extra_cpu_baselines(pf_inputs):
                                 sub["h0"]),
         w.T, "tokens/s",
         f"sequence 0 of {w.name} (all {w.H} heads), preconditioned, fp64 C")
+    c1w = gen.LAYER_340M
+    c1 = gen.prefill_inputs(c1w, B=1)
+    out["c1"] = oracle_rate(
+        lambda: oracle.kla_fwd(c1["q"], c1["k"], c1["v"], c1["log_alpha"],
+                               c1["eta"], c1["eps"], c1["h0"]),
+        c1w.T, "tokens/s", f"sequence 0 of {c1w.name} (all heads), fp64 C")
+    c3w = gen.LONG_CTX
+    c3 = gen.prefill_inputs(c3w, T=4096)
+    out["c3"] = oracle_rate(
+        lambda: oracle.kla_fwd(c3["q"], c3["k"], c3["v"], c3["log_alpha"],
+                               c3["eta"], c3["eps"], c3["h0"]),
+        4096, "tokens/s", f"the first 4096 tokens of {c3w.name}, fp64 C")
     lw = gen.LONG_131K
     lt = 8192
     li = gen.prefill_inputs(lw, T=lt)
@@ -707,6 +719,25 @@ def run_only(args):
                           "ms_per_launch": round(ms, 5)}))
 
 
+def sig(x, n=4):
+    """x rounded to n significant digits (keeps the printed line short)."""
+    if x is None or x == 0 or not np.isfinite(x):
+        return x
+    return float(f"{x:.{n}g}")
+
+
+def prefill_point(w, world, gpu_index, hbm, steps=5, warmup=3, inp=None,
+                  rule="kaczmarz"):
+    """Forward pass of workload `w`: ms per call, tokens/s over all ranks and
+    the HBM roofline fraction of the path (algorithmic bytes / time)."""
+    pf = bench_prefill(w, steps, warmup, world, gpu_index, rule=rule,
+                       inp=inp)
+    gbs = prefill_bytes(w) / (pf["ms"] * 1e-3) / 1e9
+    return pf, {"ms": sig(pf["ms"]),
+                "tps": sig(world * w.B * w.T / (pf["ms"] * 1e-3)),
+                "frac": sig(gbs / hbm, 3)}
+
+
 def run_ours(args):
     world, rank, local = dist_setup()
     hbm, tf_burst, tf_sus, peak_src = peaks()
@@ -716,139 +747,104 @@ def run_ours(args):
     ms = pf["ms"]
     tokens = w.B * w.T
     value = world * tokens / (ms * 1e-3)
-
     nbytes = prefill_bytes(w)
     achieved = nbytes / (ms * 1e-3) / 1e9
     flops = prefill_flops(w)
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1),
-                "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4),
-                "traffic": profiled_traffic("kla_chunk_tc"),
-                "kernel": "kla_chunk_fwd (tensor-core path)"
-                if w.dtype == "bf16" else "kla_chunk_fwd",
-                "algorithmic_bytes_per_launch": nbytes,
-                "tensor_view": {"flops_per_launch": flops,
-                                "achieved_tflops": round(
-                                    flops / (ms * 1e-3) / 1e12, 2),
-                                "peak_tflops": tf_burst,
-                                "frac": round(flops / (ms * 1e-3) / 1e12
-                                              / tf_burst, 4)},
-                "peak_source": peak_src}
+    path = kla.forward_path(w.B, w.T, w.H, w.dk, w.dv, w.C, torch.bfloat16)
+    roofline = {"bound": "hbm", "achieved": sig(achieved, 5), "peak": hbm,
+                "unit": "GB/s", "frac": sig(achieved / hbm, 4),
+                "traffic": profiled_traffic(path["traffic_key"]),
+                "tc_frac": sig(flops / (ms * 1e-3) / 1e12 / tf_burst, 3),
+                "src": peak_src}
+    inputs = pf["inputs"]
 
-    e2e_ms, h2d, d2h = bench_prefill_e2e(w, pf["inputs"], max(3, args.steps
-                                                              // 2), 2)
-    e2e = {"value": round(world * tokens / (e2e_ms * 1e-3), 1),
+    e2e_ms, h2d, d2h = bench_prefill_e2e(w, inputs, max(3, args.steps // 2),
+                                         2)
+    e2e = {"value": sig(world * tokens / (e2e_ms * 1e-3), 5),
            "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+           "d2h_bytes_per_step": d2h}
 
-    decode = None
+    extra = {}
+    # the learned-step (gated DeltaNet) rule on the same kernels and inputs:
+    # the pages claim equal prefill latency for the two
+    gdn = bench_prefill(w, args.steps, args.warmup, world, local,
+                        rule="given", inp=inputs)
+    extra["gdn_ratio"] = sig(ms / gdn["ms"], 4)
+
     if not args.no_decode:
         dw = gen.DECODE
         dms = bench_decode(dw, args.decode_steps, 20)
-        dbytes = decode_bytes(dw)
-        gbs = dbytes / (dms * 1e-3) / 1e9
-        decode = {"workload": dw.name, "steps_per_s": round(1e3 / dms, 1),
-                  "ms_per_step": round(dms, 5), "hbm_gbs": round(gbs, 1),
-                  "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
-                               "peak": hbm, "unit": "GB/s",
-                               "frac": round(gbs / hbm, 4),
-                               "bytes_per_step": dbytes,
-                               "traffic": profiled_traffic("kla_decode")},
-                  "timed_steps": args.decode_steps,
-                  "token_inputs": "50 distinct draws cycled"}
+        gbs = decode_bytes(dw) / (dms * 1e-3) / 1e9
+        extra["decode"] = {"sps": sig(1e3 / dms, 5), "ms": sig(dms),
+                           "gbs": sig(gbs), "frac": sig(gbs / hbm, 3)}
 
-    # The learned-step (gated DeltaNet) rule on the same kernels and inputs,
-    # timed beside KLA: the pages claim equal prefill latency for the two.
-    gdn = bench_prefill(w, args.steps, args.warmup, world, local,
-                        rule="given", inp=pf["inputs"])
-    gdn_line = {"rule": "beta = eta (gated DeltaNet step)",
-                "ms_per_step": round(gdn["ms"], 5),
-                "tokens_per_s": round(world * tokens / (gdn["ms"] * 1e-3), 1),
-                "kla_over_gdn_time": round(ms / gdn["ms"], 4)}
+    if not args.no_configs:
+        _, extra["c1"] = prefill_point(gen.LAYER_340M, world, local, hbm)
+        c3w = gen.LONG_CTX
+        c3in = gen.prefill_inputs(c3w)
+        _, c3 = prefill_point(c3w, world, local, hbm, steps=3, inp=c3in)
+        sms, sp = bench_seq(c3w, c3in, 3, 3, world)
+        c3["split_ms"] = sig(sms)
+        c3["split_frac"] = sig(prefill_bytes(c3w) / (sms * 1e-3) / 1e9 / hbm,
+                               3)
+        extra["c3"] = c3
+        del c3in
 
-    backward = None
     if not args.no_backward:
-        bms, ws_bytes = bench_backward(w, pf["inputs"], 3, 3, world)
-        alu_peak, sms, mhz = fp32_alu_peak_tflops(
-            (pf["clocks"] or {}).get("sm_max_mhz"))
+        bms, ws_bytes = bench_backward(w, inputs, 3, 3, world)
         bflops = backward_flops(w)
         ach = bflops / (bms * 1e-3) / 1e12
-        backward = {"workload": w.name, "ms": round(bms, 4),
-                    "tokens_per_s": round(world * tokens / (bms * 1e-3), 1),
-                    "kernels": "kla_chunk_bwd: tcgen05 checkpoints, tf32 "
-                               "mma.sync reverse recurrence, CUDA-core fp32 "
-                               "gradients; 3 launches",
-                    "workspace_bytes": ws_bytes,
-                    "roofline": {"bound": "alu", "achieved": round(ach, 2),
-                                 "peak": round(alu_peak, 1),
-                                 "unit": "TFLOP/s",
-                                 "frac": round(ach / alu_peak, 4),
-                                 "flops_per_launch": bflops,
-                                 "peak_source": f"{sms} SMs x 128 FP32 lanes"
-                                                f" x 2 x {mhz:.0f} MHz"},
-                    "timed_steps": 3}
+        extra["bwd"] = {"ms": sig(bms), "tps": sig(world * tokens /
+                                                    (bms * 1e-3)),
+                        "tflops": sig(ach), "frac": sig(ach / tf_sus, 3)}
 
-    precond = None
     if not args.no_precond:
-        t_plain, t_keys, t_fwd = bench_precond(w, pf["inputs"], 10, 3, world)
-        esz = 2 if w.dtype == "bf16" else 4
-        kw_bytes = esz * w.B * w.T * w.H * w.dk        # the write keys
-        fwd_bytes = prefill_bytes(w) + kw_bytes        # + kw read once
-        fwd_gbs = fwd_bytes / (t_fwd * 1e-3) / 1e9
-        precond = {"workload": w.name,
-                   "variant": "diagonal preconditioner on the write key "
-                              "(x = 1.5), Kaczmarz step",
-                   "write_keys_ms": round(t_keys, 4),
-                   "write_keys_gbs": round(2 * kw_bytes / (t_keys * 1e-3)
-                                           / 1e9, 1),
-                   "forward_ms": round(t_fwd, 4),
-                   "tokens_per_s": round(world * tokens /
-                                         ((t_keys + t_fwd) * 1e-3), 1),
-                   "plain_forward_ms": round(t_plain, 4),
-                   "overhead_vs_plain": round((t_keys + t_fwd) / t_plain, 4),
-                   "kernels": "kla_precond_keys + kla_chunk_fwd_kw "
-                              "(tensor-core kernel, write-key mode)",
-                   "roofline": {"bound": "hbm", "kernel": "two-key forward",
-                                "achieved": round(fwd_gbs, 1),
-                                "peak": hbm, "unit": "GB/s",
-                                "frac": round(fwd_gbs / hbm, 4),
-                                "algorithmic_bytes_per_launch": fwd_bytes},
-                   "timed_steps": 10}
+        t_plain, t_keys, t_fwd = bench_precond(w, inputs, 10, 3, world)
+        extra["pkla"] = {"keys_ms": sig(t_keys), "fwd_ms": sig(t_fwd),
+                         "ratio": sig((t_keys + t_fwd) / t_plain, 3)}
 
-    longctx = None
     if not args.no_long:
-        longctx = bench_long_context(world, local, hbm)
+        lc = bench_long_context(world, local, hbm)
+        p131, h32 = lc["prefill_131k"], lc["decode_after_32k"]
+        extra["l131k"] = {"ms": p131["ms"], "frac": sig(p131["roofline_frac"],
+                                                        3),
+                          "split_ms": p131["split"]["ms"],
+                          "split_frac": sig(p131["split"]["roofline_frac"],
+                                            3),
+                          "gdn_ratio": p131["kla_over_gdn_time"]}
+        extra["h32k"] = {"prefill_ms": h32["prefill_ms"],
+                         "dec_ms": h32["decode_ms_per_step"],
+                         "graph_ms": h32["graph_decode_ms_per_step"]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_prefill(pf["inputs"])
-        extra = extra_cpu_baselines(pf["inputs"])
-        if decode is not None:
-            decode["cpu_baseline"] = extra["decode"]
-        if backward is not None:
-            backward["cpu_baseline"] = extra["backward"]
-        if precond is not None:
-            precond["cpu_baseline"] = extra["preconditioned"]
-        if longctx is not None:
-            longctx["prefill_131k"]["cpu_baseline"] = extra["prefill_131k"]
+        cpu = cpu_baseline_prefill(inputs)
+        cpu["value"] = sig(cpu["value"], 5)
+        ob = extra_cpu_baselines(inputs)
+        for key, name in (("decode", "decode"), ("bwd", "backward"),
+                          ("pkla", "preconditioned"),
+                          ("l131k", "prefill_131k"), ("c1", "c1"),
+                          ("c3", "c3")):
+            if key in extra and name in ob:
+                extra[key]["cpu"] = sig(ob[name]["value"], 4)
 
-    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+    clk = pf["clocks"] or {}
+    line = {"metric": METRIC, "value": sig(value, 6), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "ms_per_step": sig(ms, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded; 1B-layer distributions)",
-            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H,
-                       "dk": w.dk, "dv": w.dv, "C": w.C,
-                       "state": "fp32", "parallelism": f"replicas x{world}",
-                       "l2": "flushed between timed steps (512 MiB write)"},
+            "data": "synthetic",
+            "config": {"workload": w.name, "l2": "flushed per step",
+                       "path": path["name"], "parallelism":
+                       f"replicas x{world}"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": pf["launches"], "clocks": pf["clocks"],
-            "decode": decode, "gdn_mode": gdn_line,
-            "long_context": longctx, "backward": backward,
-            "preconditioned": precond,
-            "per_step_ms": [round(x, 5) for x in pf["per_step_ms"]]}
+            "gpu_launches": pf["launches"] * path["launches"],
+            "clocks": {"sm_mhz": clk.get("sm_mhz"),
+                       "sm_max_mhz": clk.get("sm_max_mhz"),
+                       "reasons": clk.get("reasons", [])}}
+    line.update(extra)
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        print(json.dumps(line, separators=(",", ":")), flush=True)
 
 
 # ------------------------------------------------------------ reference arm
@@ -909,6 +905,8 @@ def main():
     ap.add_argument("--no-precond", action="store_true")
     ap.add_argument("--no-long", action="store_true",
                     help="skip the 131K-prefill / 32K-decode points")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the 340M-layer and 65K-context lines")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="run one kernel alone (profiler captures)")
     args = ap.parse_args()

@@ -21,8 +21,11 @@
  *
  * Conventions for every entry point below:
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The
- *     library keeps no pointer after a call returns and allocates no device
- *     memory.
+ *     library keeps no pointer after a call returns.  It allocates no device
+ *     memory, with two exceptions stated at the entry points: the forward
+ *     pass without a workspace argument takes stream-ordered scratch for its
+ *     tensor-core path (kla_chunk_fwd_ws avoids that), and
+ *     kla_chunk_bwd_noalloc owns a fixed device array.
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream).
  *     A status other than KLA_OK means nothing was launched (argument errors
  *     are detected on the host before any launch) or that the launch itself
@@ -63,11 +66,15 @@ typedef enum {
  * internal accumulation are always fp32. */
 typedef enum { KLA_F32 = 0, KLA_BF16 = 1 } kla_dtype;
 
-/* Forward-pass kernel selection for kla_chunk_fwd_ex. */
+/* Forward-pass kernel selection for kla_chunk_fwd_ex / kla_chunk_fwd_ws. */
 typedef enum {
     KLA_ALGO_AUTO = 0,   /* tensor-core path when eligible, else CUDA cores */
     KLA_ALGO_SIMT = 1,   /* fp32 CUDA-core chunkwise kernel (any supported shape) */
-    KLA_ALGO_TC = 2      /* tcgen05 tensor-core kernel: bf16, dk=dv=128, C=64 */
+    KLA_ALGO_TC = 2,     /* tcgen05 tensor cores, two kernels: a chunk-parallel
+                            pre-pass and the sequential state pass (bf16,
+                            dk = dv = 128, C = 64; needs a workspace) */
+    KLA_ALGO_TC_FUSED = 3 /* tcgen05 tensor cores, one fused kernel per
+                            (batch, head, dv half) (same shapes; no workspace) */
 } kla_algo;
 
 /* How the write step beta_t is formed from eta_t.
@@ -114,9 +121,17 @@ KLA_API kla_status kla_chunk_fwd(const void* q, const void* k, const void* v,
 
 /*
  * kla_chunk_fwd_ex -- kla_chunk_fwd with an explicit kernel choice and step
- * rule.  KLA_ALGO_TC returns KLA_ERR_UNSUPPORTED_SHAPE unless dtype ==
- * KLA_BF16, dk == dv == 128, C == 64 and q, k, v, o, h0, hT are 16-byte
- * aligned.  An unknown algo or rule is KLA_ERR_INVALID_ARG.
+ * rule.  KLA_ALGO_TC and KLA_ALGO_TC_FUSED return KLA_ERR_UNSUPPORTED_SHAPE
+ * unless dtype == KLA_BF16, dk == dv == 128, C == 64 and q, k, v, o, h0, hT
+ * are 16-byte aligned.  An unknown algo or rule is KLA_ERR_INVALID_ARG.
+ *
+ * KLA_ALGO_AUTO takes the fused tensor-core kernel where it is eligible.
+ * The two-kernel tensor-core path (KLA_ALGO_TC) writes per-chunk
+ * intermediates between its two kernels:
+ * kla_chunk_fwd and kla_chunk_fwd_ex take that scratch
+ * (kla_chunk_fwd_workspace_size bytes) with cudaMallocAsync on `stream` from
+ * the device's current memory pool and release it with cudaFreeAsync after
+ * the kernels, both stream-ordered; a failure there is KLA_ERR_CUDA.
  */
 KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
                             const float* log_alpha, const float* eta,
@@ -124,6 +139,40 @@ KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
                             int B, int T, int H, int dk, int dv, int C,
                             kla_dtype dtype, kla_algo algo,
                             kla_step_rule rule, kla_stream_t stream);
+
+/*
+ * kla_chunk_fwd_workspace_size -- bytes of device workspace kla_chunk_fwd_ws
+ * needs with this algorithm: for bf16, dk = dv = 128, C = 64 and KLA_ALGO_TC,
+ * the pre-pass records of the two-kernel tensor-core path,
+ * 16,640 bytes per (batch, head, chunk of 64 tokens); 0 otherwise (those
+ * paths need none).  Errors: KLA_ERR_INVALID_ARG (null `bytes`, negative
+ * size, bad enum), KLA_ERR_UNSUPPORTED_SHAPE (dk, dv or C outside the set).
+ */
+KLA_API kla_status kla_chunk_fwd_workspace_size(int B, int T, int H, int dk,
+                                                int dv, int C,
+                                                kla_dtype dtype,
+                                                kla_algo algo, size_t* bytes);
+
+/*
+ * kla_chunk_fwd_ws -- kla_chunk_fwd_ex with a caller-provided workspace, so
+ * that the library allocates nothing: device memory of at least
+ * kla_chunk_fwd_workspace_size(...) bytes, 16-byte aligned, overlapping no
+ * argument, owned by the caller; its contents on entry do not matter.  Calls
+ * that share a workspace must be ordered (the same stream does it).  When
+ * the size is 0 the workspace may be NULL; when the call takes another path
+ * (e.g. misaligned tensors) the workspace is not touched.  Errors: as for
+ * kla_chunk_fwd_ex, plus KLA_ERR_INVALID_ARG for a missing, small,
+ * misaligned or overlapping workspace.
+ */
+KLA_API kla_status kla_chunk_fwd_ws(const void* q, const void* k,
+                                    const void* v, const float* log_alpha,
+                                    const float* eta, float eps,
+                                    const float* h0, void* o, float* hT,
+                                    int B, int T, int H, int dk, int dv, int C,
+                                    kla_dtype dtype, kla_algo algo,
+                                    kla_step_rule rule, void* workspace,
+                                    size_t workspace_bytes,
+                                    kla_stream_t stream);
 
 /*
  * kla_chunk_fwd_seq_workspace_size -- bytes of device workspace
@@ -163,7 +212,7 @@ KLA_API kla_status kla_chunk_fwd_seq_workspace_size(int B, int T, int H,
  *   segments       P >= 1, or 0 to take the most segments (up to 8, T a
  *                  multiple of 64 P) for which the two runs' 4 B H P CTAs
  *                  fit on the device's SMs at once; P = 1 is
- *                  kla_chunk_fwd_ex with KLA_ALGO_TC
+ *                  kla_chunk_fwd_ex with KLA_ALGO_TC_FUSED
  *   workspace      device memory of at least
  *                  kla_chunk_fwd_seq_workspace_size(...) bytes, 256-byte
  *                  aligned, owned by the caller; contents on entry do not
@@ -190,7 +239,9 @@ KLA_API kla_status kla_chunk_fwd_seq(const void* q, const void* k,
  * kla_chunk_fwd_host_workspace_size -- bytes of device workspace
  * kla_chunk_fwd_host needs for these sizes: two buffers of every per-token
  * tensor for one segment of the sequence (at most 8 segments of whole
- * chunks) and two fp32 states [B, H, dk, dv].  Writes 0 when B * H == 0.
+ * chunks), two fp32 states [B, H, dk, dv] and the forward's workspace for
+ * one segment (kla_chunk_fwd_workspace_size with KLA_ALGO_AUTO).  Writes 0
+ * when B * H == 0.
  * Errors: KLA_ERR_INVALID_ARG (null `bytes`, negative size, bad dtype),
  * KLA_ERR_UNSUPPORTED_SHAPE (dk, dv or C outside the supported set).
  */
@@ -438,6 +489,20 @@ KLA_API kla_status kla_chunk_bwd_noalloc(
  * synchronisation failed, else KLA_OK.
  */
 KLA_API kla_status kla_device_status(kla_stream_t stream);
+
+/*
+ * kla_selftest_wait_timeout -- exercises the device-side timeout path
+ * without faulting anything: launches one CTA of the tensor-core state-pass
+ * kernel on `stream` whose copy-issuing thread issues nothing and whose
+ * waits give up after 1 ms.  Its first waits (on barriers nothing will
+ * arrive on, with no copy or tensor-core operation in flight) run out, the
+ * CTA takes its abort path (TMEM freed, return) and sets the fault word, so
+ * that the next kla_device_status on `stream` returns KLA_ERR_TIMEOUT (and
+ * the one after that KLA_OK).  The pages have no counterpart; it is a test
+ * hook of this library.  Errors: KLA_ERR_CUDA (launch failed or no tensor
+ * map support).
+ */
+KLA_API kla_status kla_selftest_wait_timeout(kla_stream_t stream);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 KLA_API const char* kla_status_string(kla_status status);

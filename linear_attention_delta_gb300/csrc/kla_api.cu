@@ -48,18 +48,35 @@ bool any_overlap(const Span (&ins)[NI], const Span (&outs)[NO]) {
 
 }  // namespace
 
-// Forward pass with optional separate write keys kw (null: the keys).
+// Whether KLA_ALGO_AUTO takes the two-kernel tensor-core path where it is
+// eligible (else the fused kernel): the faster of the two on GB300.
+constexpr bool kAutoTwoKernel = false;
+
+// Bytes of workspace the two-kernel tensor-core path needs for these sizes
+// (0 when the shape or the algorithm does not take that path).
+static size_t fwd_workspace_bytes(int B, int T, int H, int dk, int dv, int C,
+                                  kla_dtype dtype, kla_algo algo) {
+    if (dtype != KLA_BF16 || dk != 128 || dv != 128 || C != 64) return 0;
+    if (algo != KLA_ALGO_TC && !(algo == KLA_ALGO_AUTO && kAutoTwoKernel))
+        return 0;
+    return kla::chunk_tc2_workspace_bytes(B, T, H);
+}
+
+// Forward pass with optional separate write keys kw (null: the keys) and an
+// optional caller workspace (null: stream-ordered scratch when needed).
 static kla_status chunk_fwd_impl(const void* q, const void* k, const void* kw,
                                  const void* v, const float* log_alpha,
                                  const float* eta, float eps, const float* h0,
                                  void* o, float* hT, int B, int T, int H,
                                  int dk, int dv, int C, kla_dtype dtype,
                                  kla_algo algo, kla_step_rule rule,
+                                 void* workspace, size_t workspace_bytes,
                                  kla_stream_t stream) {
     if (B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || C <= 0)
         return KLA_ERR_INVALID_ARG;
     if (dtype != KLA_F32 && dtype != KLA_BF16) return KLA_ERR_INVALID_ARG;
-    if (algo != KLA_ALGO_AUTO && algo != KLA_ALGO_SIMT && algo != KLA_ALGO_TC)
+    if (algo != KLA_ALGO_AUTO && algo != KLA_ALGO_SIMT &&
+        algo != KLA_ALGO_TC && algo != KLA_ALGO_TC_FUSED)
         return KLA_ERR_INVALID_ARG;
     if (rule != KLA_STEP_KACZMARZ && rule != KLA_STEP_GIVEN)
         return KLA_ERR_INVALID_ARG;
@@ -115,14 +132,75 @@ static kla_status chunk_fwd_impl(const void* q, const void* k, const void* kw,
                    rule == KLA_STEP_GIVEN ? 1 : 0, h0, o, hT,
                    B, T, H, dk, dv, C, dtype};
     a.kw = kw;
+    const bool tc2_ok = kla::chunk_tc2_eligible(a);
     const bool tc_ok = kla::chunk_tc_eligible(a);
-    if (algo == KLA_ALGO_TC) {
+    if ((algo == KLA_ALGO_TC || (algo == KLA_ALGO_AUTO && kAutoTwoKernel)) &&
+        tc2_ok) {
+        const size_t need = kla::chunk_tc2_workspace_bytes(B, T, H);
+        if (workspace) {
+            if (workspace_bytes < need || !aligned(workspace, 16))
+                return KLA_ERR_INVALID_ARG;
+            const Span bufs[] = {{q, (size_t)B * T * H * dk * 2},
+                                 {k, (size_t)B * T * H * dk * 2},
+                                 {v, (size_t)B * T * H * dv * 2},
+                                 {o, (size_t)B * T * H * dv * 2},
+                                 {log_alpha, (size_t)B * T * H * 4},
+                                 {eta, (size_t)B * T * H * 4},
+                                 {h0, sizeof(float) * B * H * dk * dv},
+                                 {hT, sizeof(float) * B * H * dk * dv}};
+            const Span ws[] = {{workspace, need}};
+            if (any_overlap(bufs, ws)) return KLA_ERR_INVALID_ARG;
+            return from_cuda(kla::launch_chunk_tc2(a, workspace, s));
+        }
+        // stream-ordered scratch from the device's current memory pool
+        void* scratch = nullptr;
+        if (cudaMallocAsync(&scratch, need, s) != cudaSuccess)
+            return KLA_ERR_CUDA;
+        const cudaError_t e = kla::launch_chunk_tc2(a, scratch, s);
+        const cudaError_t f = cudaFreeAsync(scratch, s);
+        return from_cuda(e != cudaSuccess ? e : f);
+    }
+    if (algo == KLA_ALGO_TC || algo == KLA_ALGO_TC_FUSED) {
         if (!tc_ok) return KLA_ERR_UNSUPPORTED_SHAPE;
         return from_cuda(kla::launch_chunk_tc(a, s));
     }
     if (algo == KLA_ALGO_AUTO && tc_ok)
         return from_cuda(kla::launch_chunk_tc(a, s));
     return from_cuda(kla::launch_chunk_simt(a, s));
+}
+
+extern "C" kla_status kla_chunk_fwd_workspace_size(int B, int T, int H,
+                                                   int dk, int dv, int C,
+                                                   kla_dtype dtype,
+                                                   kla_algo algo,
+                                                   size_t* bytes) {
+    if (!bytes || B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || C <= 0)
+        return KLA_ERR_INVALID_ARG;
+    if (dtype != KLA_F32 && dtype != KLA_BF16) return KLA_ERR_INVALID_ARG;
+    if (algo != KLA_ALGO_AUTO && algo != KLA_ALGO_SIMT &&
+        algo != KLA_ALGO_TC && algo != KLA_ALGO_TC_FUSED)
+        return KLA_ERR_INVALID_ARG;
+    if (!supported_dim(dk) || !supported_dim(dv) || !supported_chunk(C))
+        return KLA_ERR_UNSUPPORTED_SHAPE;
+    *bytes = fwd_workspace_bytes(B, T, H, dk, dv, C, dtype, algo);
+    return KLA_OK;
+}
+
+extern "C" kla_status kla_chunk_fwd_ws(const void* q, const void* k,
+                                       const void* v, const float* log_alpha,
+                                       const float* eta, float eps,
+                                       const float* h0, void* o, float* hT,
+                                       int B, int T, int H, int dk, int dv,
+                                       int C, kla_dtype dtype, kla_algo algo,
+                                       kla_step_rule rule, void* workspace,
+                                       size_t workspace_bytes,
+                                       kla_stream_t stream) {
+    if (!workspace && fwd_workspace_bytes(B, T, H, dk, dv, C, dtype, algo) &&
+        (long long)B * H > 0 && T > 0)
+        return KLA_ERR_INVALID_ARG;
+    return chunk_fwd_impl(q, k, nullptr, v, log_alpha, eta, eps, h0, o, hT, B,
+                          T, H, dk, dv, C, dtype, algo, rule, workspace,
+                          workspace_bytes, stream);
 }
 
 extern "C" kla_status kla_chunk_fwd_ex(const void* q, const void* k,
@@ -134,7 +212,8 @@ extern "C" kla_status kla_chunk_fwd_ex(const void* q, const void* k,
                                        kla_step_rule rule,
                                        kla_stream_t stream) {
     return chunk_fwd_impl(q, k, nullptr, v, log_alpha, eta, eps, h0, o, hT, B,
-                          T, H, dk, dv, C, dtype, algo, rule, stream);
+                          T, H, dk, dv, C, dtype, algo, rule, nullptr, 0,
+                          stream);
 }
 
 extern "C" kla_status kla_chunk_fwd_kw(const void* q, const void* k,
@@ -148,7 +227,8 @@ extern "C" kla_status kla_chunk_fwd_kw(const void* q, const void* k,
                                        kla_stream_t stream) {
     if (!k_write && (long long)B * H > 0 && T > 0) return KLA_ERR_INVALID_ARG;
     return chunk_fwd_impl(q, k, k_write, v, log_alpha, eta, eps, h0, o, hT, B,
-                          T, H, dk, dv, C, dtype, KLA_ALGO_AUTO, rule, stream);
+                          T, H, dk, dv, C, dtype, KLA_ALGO_AUTO, rule, nullptr,
+                          0, stream);
 }
 
 extern "C" kla_status kla_precond_keys(const void* k, const float* A0,
@@ -382,6 +462,11 @@ extern "C" kla_status kla_device_status(kla_stream_t stream) {
         reinterpret_cast<cudaStream_t>(stream), &word);
     if (e != cudaSuccess) return KLA_ERR_CUDA;
     return word ? KLA_ERR_TIMEOUT : KLA_OK;
+}
+
+extern "C" kla_status kla_selftest_wait_timeout(kla_stream_t stream) {
+    return from_cuda(kla::launch_state_selftest(
+        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 extern "C" const char* kla_status_string(kla_status status) {

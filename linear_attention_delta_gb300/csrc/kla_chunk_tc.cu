@@ -883,6 +883,7 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 tc::mma_commit(&bars[kBarKS]);
                 last_bar = kBarKS; last_par = c & 1;
             }
+            __syncwarp();   // the issuing lane rejoins before the waits
             if (sw < 2) {
                 // ---- residual X = V - Diag(gamma) K S, over V in the stage
                 ok = ok && tc::mbar_wait_or_abort(&bars[kBarAReady + (c & 3)],
@@ -936,6 +937,7 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     tc::mma_commit(&bars[kBarUT + (c & 1)]);
                     last_bar = kBarUT + (c & 1); last_par = (c >> 1) & 1;
                 }
+                __syncwarp();
                 ok = team_wait(&bars[kBarUT + (c & 1)], (c >> 1) & 1,
                                abort_flag, kBarState01, 64, ok);
                 if (ok) {   // rows 0..63: U~ and Diag(Gamma_C) U~ as operands
@@ -983,6 +985,7 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 tc::mma_commit(&bars[kBarOI + (c & 1)]);
                 last_bar = kBarOI + (c & 1); last_par = (c >> 1) & 1;
             }
+            __syncwarp();
             if (!team_wait(&bars[kBarDS], c & 1, abort_flag, kBarState, 128)) {
                 failed = true; break;
             }
@@ -1047,6 +1050,8 @@ kla_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
+}  // namespace
+
 bool get_encoder() {
     std::call_once(g_encode_once, [] {
         cudaDriverEntryPointQueryResult q;
@@ -1074,6 +1079,8 @@ bool make_map(CUtensorMap* m, const void* base, int B, int T, int H) {
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 bool aligned16(const void* ptr) {
     return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0;
@@ -1132,7 +1139,12 @@ cudaError_t read_and_clear_fault(cudaStream_t stream, unsigned int* word) {
     e = cudaMemcpyFromSymbol(word, g_fault_word, sizeof(unsigned int));
     if (e != cudaSuccess) return e;
     const unsigned int zero = 0;
-    return cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(unsigned int));
+    e = cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(unsigned int));
+    if (e != cudaSuccess) return e;
+    unsigned int w2 = 0;
+    e = read_and_clear_fault2(&w2);
+    *word |= w2;
+    return e;
 }
 
 }  // namespace kla

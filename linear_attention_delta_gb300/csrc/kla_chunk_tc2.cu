@@ -1,0 +1,999 @@
+// Two-kernel tensor-core forward pass for bf16 q/k/v/o, dk = dv = 128,
+// chunk C = 64, fp32 state: a chunk-parallel pre-pass and a sequential
+// state pass.
+//
+// Per (batch, head) and chunk (rows r, i; g = in-chunk cumulative log decay,
+// gamma_r = exp(g_r), Gamma_ri = exp(g_r - g_i), Gamma_C,r = exp(g_C - g_r)),
+// the gated-DeltaNet block solver with B = Diag(beta) as the only change
+// (gist.science/es/paper/2605.08587, section "Implementacion"):
+//   beta_r = eta_r / (||k_r||^2 + eps)
+//   A   = I + strict_lower(Diag(beta) (Gamma o K K^T)),   T = A^{-1}
+//   TU  = T Diag(beta),     P = lower_incl(Gamma o Q K^T),   PTU = P TU
+//   W   = TU Diag(gamma) K,           U = TU V
+//   Q'  = Diag(gamma) Q - PTU Diag(gamma) K
+//   U~  = U - W S                     (the new values of the chunk)
+//   O   = Diag(gamma) Q S + P U~ = Q' S + PTU V
+//   S  <- gamma_C S + K^T Diag(Gamma_C) U~
+// Only the last three lines involve the state; everything else depends on
+// the chunk's own inputs.
+//
+// Pre-pass (kla_prep_kernel): one CTA per chunk-head, all in parallel.  G =
+// [K; Q] K^T on the tensor cores (tcgen05, TMEM accumulator); beta from its
+// diagonal; A in fp32 and P in bf16; T = A^{-1} by blocks (fp32
+// substitution on the 16x16 diagonal blocks, tf32 warp-level MMAs for the
+// rest); PTU = P TU on the tensor cores; TU and PTU written to global
+// memory (one bulk copy) as the exact shared-memory image of a 128-row
+// K-major bf16 tensor-core operand [TU; PTU], followed by g.
+//
+// State pass (kla_state_kernel): one CTA per (batch, head, 64 columns of
+// dv), walking the chunks in order.  A helper warpgroup prepares chunk c+1
+// while the chain warpgroup runs chunk c:
+//   helper: K_gamma = Diag(gamma) K; [-W; -PTU K_gamma] = -[TU; PTU] K_gamma
+//           and [U; PTU V] = [TU; PTU] V on the tensor cores; -W and Q'
+//           written over K and Q in the stage, Diag(Gamma_C) K over TU and
+//           PTU;
+//   chain:  [U~; O] = [U; PTU V] + [-W; Q'] S   (one MMA group of 8),
+//           U~ to shared memory, dS = (Diag(Gamma_C) K)^T U~  (4 MMAs),
+//           S <- gamma_C S + dS in registers (fp32, one key row per thread),
+//           o from the lower half of the first accumulator, written through
+//           shared memory by a TMA store.
+// So only two dependent tensor-core round trips remain per chunk.
+//
+// Every wait on an mbarrier is bounded; a CTA that gives up raises its abort
+// flag, records the fault in the library's fault word, lets its own copies
+// and MMAs finish (bounded), frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "kla_internal.cuh"
+#include "tc_primitives.cuh"
+
+namespace kla {
+
+namespace {
+
+__device__ unsigned int g_fault_word2 = 0;
+
+constexpr int kC = 64;
+constexpr int kD = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Record of one chunk-head written by the pre-pass (bytes): the 128-row
+// K-major operand [TU; PTU] (128-byte swizzled rows) and g (log2 units).
+constexpr int kRecTU = 0;
+constexpr int kRecPTU = 8192;
+constexpr int kRecG = 16384;
+constexpr int kRecBytes = 16640;
+
+// Byte offset of element (row, col) of a 64-column bf16 tile stored as
+// 128-byte swizzled rows (the layout TMA writes with 128-byte swizzle and the
+// tensor cores read from a 1024-byte-aligned base).
+__host__ __device__ constexpr int swz(int row, int col) {
+    return row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1);
+}
+
+__device__ __forceinline__ uint64_t desc_k(uint32_t addr) {
+    return tc::sdesc_sw128(addr, 16, 1024);
+}
+__device__ __forceinline__ uint64_t desc_mn(uint32_t addr, uint32_t lbo) {
+    return tc::sdesc_sw128(addr, lbo, 1024);
+}
+
+// ===================================================================
+// Pre-pass
+// ===================================================================
+
+constexpr int kPrepThreads = 128;
+constexpr int kLd = 68;                       // fp32 tile row stride
+constexpr int kTileBytes = 64 * kLd * 4;      // 17408
+// shared memory map (from a 1024-aligned base)
+constexpr int kPKQ = 0;          // K_0 | Q_0 | K_1 | Q_1 (TMA), 32 KB; after G
+                                 // the record image [TU | P, then PTU | g]
+constexpr int kPL = 32768;       // L (strictly lower part of A), fp32
+constexpr int kPT = kPL + kTileBytes;        // T = A^{-1}, fp32
+constexpr int kPY = kPT + kTileBytes;        // 4 warps x 16 x 8 fp32 scratch
+constexpr int kPG = kPY + 4 * 16 * 8 * 4;    // g2[64]
+constexpr int kPBeta = kPG + 256;            // beta[64]
+constexpr int kPBars = kPBeta + 256;         // 3 mbarriers
+constexpr int kPMisc = kPBars + 24;          // TMEM slot, warp total, flag
+constexpr int kPSmem = kPMisc + 16 + 1024;
+static_assert(kRecBytes <= kPL, "pre-pass map");
+static_assert(kPSmem <= 232448, "pre-pass shared memory");
+
+struct PrepParams {
+    const float* log_alpha;
+    const float* eta;
+    uint8_t* rec;        // [B, H, nchunks, kRecBytes]
+    float eps;
+    int gdn;
+    int T, H, nchunks;
+};
+
+// acc (16 x 8, fragment layout) += A (16 x 16 fp32 tile, row stride kLd) x
+// B[:, n0 .. n0 + 7] (16 x 8 of a fp32 tile, row stride kLd), tf32 MMAs.
+__device__ __forceinline__ void mm16x8(float (&acc)[4], const float* A,
+                                       const float* B, int n0, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+        uint32_t a[4];
+        a[0] = tc::to_tf32(A[g * kLd + 8 * kk + t]);
+        a[1] = tc::to_tf32(A[(g + 8) * kLd + 8 * kk + t]);
+        a[2] = tc::to_tf32(A[g * kLd + 8 * kk + t + 4]);
+        a[3] = tc::to_tf32(A[(g + 8) * kLd + 8 * kk + t + 4]);
+        const uint32_t b0 = tc::to_tf32(B[(8 * kk + t) * kLd + n0 + g]);
+        const uint32_t b1 = tc::to_tf32(B[(8 * kk + t + 4) * kLd + n0 + g]);
+        tc::mma_m16n8k8_tf32(acc, a, b0, b1);
+    }
+}
+
+// One 16 x 8 slab of an off-diagonal block of T = A^{-1} (A = I + L):
+//   T_IJ[:, n0..n0+7] = -T_II sum_{m=J}^{I-1} L_Im T_mJ[:, n0..n0+7].
+// The sum is formed in registers, passed through this warp's scratch Y
+// (16 x 8, row stride 8) and multiplied by T_II.
+__device__ void offdiag_slab(const float* L, float* T, float* Y, int I, int J,
+                             int n0, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int m = J; m < I; ++m)
+        mm16x8(acc, L + 16 * I * kLd + 16 * m, T + 16 * m * kLd + 16 * J, n0,
+               lane);
+    Y[g * 8 + 2 * t] = acc[0];
+    Y[g * 8 + 2 * t + 1] = acc[1];
+    Y[(g + 8) * 8 + 2 * t] = acc[2];
+    Y[(g + 8) * 8 + 2 * t + 1] = acc[3];
+    __syncwarp();
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    const float* Tii = T + 16 * I * kLd + 16 * I;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+        uint32_t a[4];
+        a[0] = tc::to_tf32(Tii[g * kLd + 8 * kk + t]);
+        a[1] = tc::to_tf32(Tii[(g + 8) * kLd + 8 * kk + t]);
+        a[2] = tc::to_tf32(Tii[g * kLd + 8 * kk + t + 4]);
+        a[3] = tc::to_tf32(Tii[(g + 8) * kLd + 8 * kk + t + 4]);
+        const uint32_t b0 = tc::to_tf32(Y[(8 * kk + t) * 8 + g]);
+        const uint32_t b1 = tc::to_tf32(Y[(8 * kk + t + 4) * 8 + g]);
+        tc::mma_m16n8k8_tf32(d, a, b0, b1);
+    }
+    __syncwarp();
+    float* dst = T + 16 * I * kLd + 16 * J + n0;
+    dst[g * kLd + 2 * t] = -d[0];
+    dst[g * kLd + 2 * t + 1] = -d[1];
+    dst[(g + 8) * kLd + 2 * t] = -d[2];
+    dst[(g + 8) * kLd + 2 * t + 1] = -d[3];
+}
+
+__global__ void __launch_bounds__(kPrepThreads)
+kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
+                const __grid_constant__ CUtensorMap tm_k, PrepParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = tc::smem_u32(sm);
+    float* Lt = reinterpret_cast<float*>(sm + kPL);
+    float* Tt = reinterpret_cast<float*>(sm + kPT);
+    float* g2s = reinterpret_cast<float*>(sm + kPG);
+    float* betas = reinterpret_cast<float*>(sm + kPBeta);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPBars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kPMisc);
+    float* wtot = reinterpret_cast<float*>(sm + kPMisc + 4);
+    int* failed_flag = reinterpret_cast<int*>(sm + kPMisc + 8);
+    uint8_t* out = sm + kPKQ;   // record image, over the consumed K / Q
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x % p.nchunks;
+    const int bh = blockIdx.x / p.nchunks;
+    const int b = bh / p.H, h = bh % p.H;
+    const int t0 = c * kC;
+    constexpr uint64_t kLimit = 2000000000ull;
+
+    if (tid == 0) {
+        tc::prefetch_tmap(&tm_q);
+        tc::prefetch_tmap(&tm_k);
+        for (int i = 0; i < 3; ++i) tc::mbar_init(&bars[i], 1);
+        *failed_flag = 0;
+        tc::fence_mbar_init();
+        tc::mbar_arrive_expect_tx(&bars[0], 32768);
+        tc::tma_load_4d(sm + kPKQ, &tm_k, &bars[0], 0, h, t0, b);
+        tc::tma_load_4d(sm + kPKQ + 8192, &tm_q, &bars[0], 0, h, t0, b);
+        tc::tma_load_4d(sm + kPKQ + 16384, &tm_k, &bars[0], 64, h, t0, b);
+        tc::tma_load_4d(sm + kPKQ + 24576, &tm_q, &bars[0], 64, h, t0, b);
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, 128);
+        tc::tmem_relinquish();
+    }
+    // gates of this chunk: cumulative log2 decay (two warp scans)
+    float la = 0.f, et = 0.f;
+    if (tid < kC && t0 + tid < p.T) {
+        const size_t off = ((size_t)b * p.T + t0 + tid) * p.H + h;
+        la = p.log_alpha[off];
+        et = p.eta[off];
+    }
+    float g2 = la * kLog2e;
+    if (tid < kC) {
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, g2, off);
+            if (lane >= off) g2 += y;
+        }
+        if (tid == 31) *wtot = g2;
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (tid >= 32 && tid < kC) g2 += *wtot;
+    if (tid < kC) g2s[tid] = g2;
+
+    // G = [K; Q] K^T: lanes 0..63 K K^T, lanes 64..127 Q K^T (columns 0..63)
+    if (tid == 0) {
+        if (tc::mbar_wait(&bars[0], 0, kLimit)) {
+            tc::tc_fence_after();
+            constexpr uint32_t idG = tc::idesc_bf16(128, 64, false, false);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                tc::mma_bf16(tmem, desc_k(sbase + kPKQ + off),
+                             desc_k(sbase + kPKQ + off), idG, ks > 0);
+            }
+            tc::mma_commit(&bars[1]);
+        } else {
+            *reinterpret_cast<volatile int*>(failed_flag) = 1;
+        }
+    }
+    __syncthreads();   // g2s complete; the issuing lane rejoined
+    bool ok = *reinterpret_cast<volatile int*>(failed_flag) == 0;
+    ok = ok && tc::mbar_wait(&bars[1], 0, kLimit);
+    ok = !__syncthreads_or(!ok);
+    if (!ok) {
+        if (tid == 0) {
+            atomicOr(&g_fault_word2, 1u);
+            tc::mbar_wait(&bars[0], 0, 100000000ull);   // copies in flight
+            tc::mbar_wait(&bars[1], 0, 100000000ull);   // the MMAs, if issued
+        }
+        __syncthreads();
+        if (warp == 0) tc::tmem_dealloc(tmem, 128);
+        return;
+    }
+    tc::tc_fence_after();
+    {
+        float x[64];
+        const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
+        tc::tmem_ld32(ta, x);
+        tc::tmem_ld32(ta + 32, x + 32);
+        tc::tmem_ld_wait();
+        if (tid < kC) {
+            // A row r = tid: beta_r Gamma_ri (K K^T)_ri for i < r (fp32;
+            // float4 stores: rows 68 floats apart put the 8 rows of a
+            // quarter warp in 8 different bank groups)
+            const int r = tid;
+            float* Lr = Lt + r * kLd;
+#pragma unroll
+            for (int i = 0; i < 64; i += 4)
+                *reinterpret_cast<float4*>(Lr + i) =
+                    make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+            const float denom = Lr[r] + p.eps;   // ||k_r||^2 + eps
+            const float br = p.gdn ? et : (denom == 0.f ? 0.f : et / denom);
+            betas[r] = br;
+#pragma unroll
+            for (int i = 0; i < 64; i += 4) {
+                const float4 gi = *reinterpret_cast<const float4*>(g2s + i);
+                float4 a;
+                a.x = i + 0 < r ? br * tc::ex2(g2 - gi.x) * x[i + 0] : 0.f;
+                a.y = i + 1 < r ? br * tc::ex2(g2 - gi.y) * x[i + 1] : 0.f;
+                a.z = i + 2 < r ? br * tc::ex2(g2 - gi.z) * x[i + 2] : 0.f;
+                a.w = i + 3 < r ? br * tc::ex2(g2 - gi.w) * x[i + 3] : 0.f;
+                *reinterpret_cast<float4*>(Lr + i) = a;
+            }
+        } else {
+            // P row r = tid - 64: Gamma_ri (Q K^T)_ri for i <= r, as bf16
+            // operand rows behind TU in the record image
+            const int r = tid - kC;
+            const float gr = g2s[r];
+#pragma unroll
+            for (int i = 0; i < 64; i += 8) {
+                const float4 ga = *reinterpret_cast<const float4*>(g2s + i);
+                const float4 gb = *reinterpret_cast<const float4*>(g2s + i + 4);
+                const float gi[8] = {ga.x, ga.y, ga.z, ga.w,
+                                     gb.x, gb.y, gb.z, gb.w};
+                float e[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    e[k] = i + k <= r ? tc::ex2(gr - gi[k]) * x[i + k] : 0.f;
+                uint4 v;
+                v.x = tc::pack_bf16x2(e[0], e[1]);
+                v.y = tc::pack_bf16x2(e[2], e[3]);
+                v.z = tc::pack_bf16x2(e[4], e[5]);
+                v.w = tc::pack_bf16x2(e[6], e[7]);
+                *reinterpret_cast<uint4*>(out + kRecPTU + swz(r, i)) = v;
+            }
+        }
+    }
+    __syncthreads();
+    // diagonal blocks T_bb = (I + L_bb)^{-1}: thread (bb, cl) solves column
+    // cl by substitution (threads 0..63); the others zero T above the
+    // diagonal blocks
+    if (tid < kC) {
+        const int bb = tid >> 4, cl = tid & 15;
+        const float* Lb = Lt + 16 * bb * kLd + 16 * bb;
+        float xv[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) xv[r] = (r == cl) ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < 16; ++r) {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < r; i += 2) {
+                a0 = fmaf(Lb[r * kLd + i], xv[i], a0);
+                if (i + 1 < r) a1 = fmaf(Lb[r * kLd + i + 1], xv[i + 1], a1);
+            }
+            if (r > cl) xv[r] = -(a0 + a1);
+        }
+        float* Tb = Tt + 16 * bb * kLd + 16 * bb + cl;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Tb[r * kLd] = xv[r];
+    } else {
+        // blocks (I, J) with I < J
+        for (int e = tid - kC; e < 6 * 256; e += kC) {
+            const int blk = e >> 8, w = e & 255;
+            const int I = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+            const int J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            Tt[(16 * I + (w >> 4)) * kLd + 16 * J + (w & 15)] = 0.f;
+        }
+    }
+    __syncthreads();
+    float* Y = reinterpret_cast<float*>(sm + kPY) + warp * 128;
+    // level 1: (1,0), (2,1), (3,2); 6 slabs of 8 columns on 4 warps
+    for (int job = warp; job < 6; job += 4) {
+        const int I = (job >> 1) + 1;
+        offdiag_slab(Lt, Tt, Y, I, I - 1, 8 * (job & 1), lane);
+        __syncwarp();
+    }
+    __syncthreads();
+    // level 2: (2,0), (3,1)
+    offdiag_slab(Lt, Tt, Y, 2 + (warp >> 1), warp >> 1, 8 * (warp & 1), lane);
+    __syncthreads();
+    // level 3: (3,0)
+    if (warp < 2) offdiag_slab(Lt, Tt, Y, 3, 0, 8 * warp, lane);
+    __syncthreads();
+
+    // TU = T Diag(beta) as bf16 operand rows: thread -> (row, 32 columns)
+    {
+        const int r = tid >> 1, c0 = 32 * (tid & 1);
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+            uint4 v;
+            const float4 ta =
+                *reinterpret_cast<const float4*>(Tt + r * kLd + c0 + j);
+            const float4 tb =
+                *reinterpret_cast<const float4*>(Tt + r * kLd + c0 + j + 4);
+            const float4 ba = *reinterpret_cast<const float4*>(betas + c0 + j);
+            const float4 bb =
+                *reinterpret_cast<const float4*>(betas + c0 + j + 4);
+            v.x = tc::pack_bf16x2(ta.x * ba.x, ta.y * ba.y);
+            v.y = tc::pack_bf16x2(ta.z * ba.z, ta.w * ba.w);
+            v.z = tc::pack_bf16x2(tb.x * bb.x, tb.y * bb.y);
+            v.w = tc::pack_bf16x2(tb.z * bb.z, tb.w * bb.w);
+            *reinterpret_cast<uint4*>(out + kRecTU + swz(r, c0 + j)) = v;
+        }
+    }
+    if (tid < kC) reinterpret_cast<float*>(out + kRecG)[tid] = g2s[tid];
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    // PTU = P TU on the tensor cores: [TU; P] TU, lanes 64..127 (TMEM
+    // columns 64..127); TU is K-major as the A rows and MN-major as B
+    if (tid == 0) {
+        tc::tc_fence_after();
+        constexpr uint32_t idP = tc::idesc_bf16(128, 64, false, true);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            tc::mma_bf16(tmem + 64, desc_k(sbase + kPKQ + kRecTU + ks * 32),
+                         desc_mn(sbase + kPKQ + kRecTU + ks * 2048, 0), idP,
+                         ks > 0);
+        tc::mma_commit(&bars[2]);
+    }
+    __syncwarp();
+    ok = tc::mbar_wait(&bars[2], 0, kLimit);
+    if (!__syncthreads_or(!ok)) {
+        tc::tc_fence_after();
+        if (tid >= kC) {   // PTU rows over P
+            const int r = tid - kC;
+            float x[64];
+            const uint32_t ta = tmem + 64 + ((uint32_t)(warp * 32) << 16);
+            tc::tmem_ld32(ta, x);
+            tc::tmem_ld32(ta + 32, x + 32);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint4 v;
+                v.x = tc::pack_bf16x2(x[8 * j + 0], x[8 * j + 1]);
+                v.y = tc::pack_bf16x2(x[8 * j + 2], x[8 * j + 3]);
+                v.z = tc::pack_bf16x2(x[8 * j + 4], x[8 * j + 5]);
+                v.w = tc::pack_bf16x2(x[8 * j + 6], x[8 * j + 7]);
+                *reinterpret_cast<uint4*>(out + kRecPTU + swz(r, 8 * j)) = v;
+            }
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {   // the record, one bulk copy
+            tc::bulk_store(p.rec + ((size_t)bh * p.nchunks + c) * kRecBytes,
+                           out, kRecBytes);
+            tc::tma_store_commit();
+            tc::tma_store_wait_read<0>();
+        }
+    } else if (tid == 0) {
+        atomicOr(&g_fault_word2, 1u);
+        tc::mbar_wait(&bars[2], 0, 100000000ull);
+    }
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+}
+
+// ===================================================================
+// State pass
+// ===================================================================
+
+constexpr int kNV = 64;              // dv columns per CTA
+constexpr int kNS = 3;               // stages of the TMA ring
+// stage map (bytes from the stage base, 1024-aligned)
+constexpr int kSK0 = 0;              // K_0, later -W_0     } [-W_0; Q'_0]
+constexpr int kSQ0 = 8192;           // Q_0, later Q'_0     }
+constexpr int kSK1 = 16384;          // K_1, later -W_1     } [-W_1; Q'_1]
+constexpr int kSQ1 = 24576;          // Q_1, later Q'_1     }
+constexpr int kSV = 32768;           // V (64 tokens x 64 columns)
+constexpr int kSTU = 40960;          // [TU; PTU], later [KG_0 | KG_1] with
+                                     // KG = Diag(Gamma_C) K
+constexpr int kSG = kSTU + kRecG;    // g (log2), 64 floats
+constexpr int kStage = 58368;
+constexpr int kSKg = kNS * kStage;   // Diag(gamma) K: [Kg_0 | Kg_1]
+constexpr int kSS = kSKg + 16384;    // S bf16, 128 x 64, MN-major
+constexpr int kSUt = kSS + 16384;    // U~ bf16, 64 x 64, MN-major
+constexpr int kSO = kSUt + 8192;     // o of a chunk, bf16 (TMA store image)
+constexpr int kSBars = kSO + 8192;
+// mbarriers: full[3] (TMA), empty[3] (chain done with the stage), ready[3]
+// (helper done with the stage), hmma (helper MMAs), c1 (chain MMA group 1),
+// c2 (dS), accfree[2] (accumulator of a chunk parity read out)
+constexpr int kBFull = 0, kBEmpty = 3, kBReady = 6, kBHmma = 9, kBC1 = 10,
+              kBC2 = 11, kBAccFree = 12, kNumBars = 14;
+constexpr int kSMisc = kSBars + 8 * kNumBars;   // abort, TMEM slot, issued
+constexpr int kSSmem = kSMisc + 16 + 1024;
+static_assert(kSG + 256 <= kStage && kStage % 1024 == 0, "stage map");
+static_assert(kSSmem <= 232448, "state-pass shared memory");
+constexpr uint32_t kStageTx = 4 * 8192 + 8192 + kRecBytes;
+
+// TMEM columns
+constexpr uint32_t kColH = 0;        // helper: [W; PTU Kg] (128 columns)
+constexpr uint32_t kColAcc = 128;    // + 64 (c & 1): [U; PTU V], then [U~; O]
+constexpr uint32_t kColDS = 256;     // dS
+constexpr uint32_t kTmemCols = 512;
+
+constexpr int kChainThreads = 128, kHelperThreads = 128;
+constexpr int kStateThreads = kChainThreads + kHelperThreads + 32;
+constexpr int kBarHelper = 1, kBarChain = 2, kBarChainLo = 3,
+              kBarChainHi = 4;
+
+struct StateParams {
+    const float* h0;
+    __nv_bfloat16* o;     // null in checkpoint mode
+    float* hT;
+    float* ckpt;          // checkpoint mode: the state at every chunk start
+    const uint8_t* rec;   // records of the pre-pass
+    int T, H, nchunks;
+    uint64_t wait_ns;     // limit of every mbarrier wait
+    int no_issue;         // self-test: the producer issues nothing
+};
+
+// Write 64 fp32 values as one 128-byte swizzled bf16 row.
+__device__ __forceinline__ void st_row(uint8_t* base, int row,
+                                       const float* x) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint4 v;
+        v.x = tc::pack_bf16x2(x[8 * j + 0], x[8 * j + 1]);
+        v.y = tc::pack_bf16x2(x[8 * j + 2], x[8 * j + 3]);
+        v.z = tc::pack_bf16x2(x[8 * j + 4], x[8 * j + 5]);
+        v.w = tc::pack_bf16x2(x[8 * j + 6], x[8 * j + 7]);
+        *reinterpret_cast<uint4*>(base + row * 128 + ((j ^ (row & 7)) << 4)) =
+            v;
+    }
+}
+
+__device__ __forceinline__ void unpack2(uint32_t u, float& lo, float& hi) {
+    lo = __uint_as_float(u << 16);
+    hi = __uint_as_float(u & 0xffff0000u);
+}
+
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) {
+    return *reinterpret_cast<__nv_bfloat162*>(&u);
+}
+__device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v) {
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 8 bf16 times s (packed bf16 multiplies; s is rounded to bf16 first)
+__device__ __forceinline__ uint4 scale8(uint4 u, __nv_bfloat162 s) {
+    uint4 r;
+    r.x = as_u32(__hmul2(as_bf2(u.x), s));
+    r.y = as_u32(__hmul2(as_bf2(u.y), s));
+    r.z = as_u32(__hmul2(as_bf2(u.z), s));
+    r.w = as_u32(__hmul2(as_bf2(u.w), s));
+    return r;
+}
+
+template <bool kCkpt>
+__global__ void __launch_bounds__(kStateThreads, 1)
+kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
+                 const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v,
+                 const __grid_constant__ CUtensorMap tm_o, StateParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = tc::smem_u32(sm);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSBars);
+    int* abort_flag = reinterpret_cast<int*>(sm + kSMisc);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kSMisc + 4);
+    int* issued = reinterpret_cast<int*>(sm + kSMisc + 8);
+    volatile int* vabort = abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int bh = blockIdx.x;
+    const int b = bh / p.H, h = bh % p.H;
+    const int j0 = blockIdx.y * kNV;
+    const int T = p.T, nchunks = p.nchunks;
+
+    if (tid == 0) {
+        for (int i = 0; i < kNumBars; ++i) tc::mbar_init(&bars[i], 1);
+        *abort_flag = 0;
+        *issued = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    float S[kNV];
+    if (tid < kChainThreads) {   // S rows (key dims) of this column slice
+        const float* src =
+            p.h0 ? p.h0 + ((size_t)bh * kD + tid) * kD + j0 : nullptr;
+#pragma unroll
+        for (int j = 0; j < kNV; j += 4) {
+            const float4 v = src ? *reinterpret_cast<const float4*>(src + j)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
+        }
+        st_row(sm + kSS, tid, S);
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (tid >= kChainThreads + kHelperThreads) {
+        // ========================================================= producer
+        if (tid == kChainThreads + kHelperThreads && !p.no_issue) {
+            tc::prefetch_tmap(&tm_q);
+            tc::prefetch_tmap(&tm_k);
+            tc::prefetch_tmap(&tm_v);
+            const uint8_t* rec0 = p.rec + (size_t)bh * nchunks * kRecBytes;
+            auto prefetch = [&](int c) {
+                const int t0 = c * kC;
+                tc::tma_prefetch_4d(&tm_k, 0, h, t0, b);
+                tc::tma_prefetch_4d(&tm_q, 0, h, t0, b);
+                tc::tma_prefetch_4d(&tm_k, 64, h, t0, b);
+                tc::tma_prefetch_4d(&tm_q, 64, h, t0, b);
+                tc::tma_prefetch_4d(&tm_v, j0, h, t0, b);
+                tc::bulk_prefetch_l2(rec0 + (size_t)c * kRecBytes, kRecBytes);
+            };
+            for (int c = kNS; c < 2 * kNS && c < nchunks; ++c) prefetch(c);
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c % kNS;
+                if (c >= kNS &&
+                    !tc::mbar_wait_or_abort(&bars[kBEmpty + s],
+                                            ((c / kNS) - 1) & 1, vabort,
+                                            p.wait_ns)) {
+                    *vabort = 1;
+                    break;
+                }
+                uint8_t* st = sm + s * kStage;
+                uint64_t* bar = &bars[kBFull + s];
+                const int t0 = c * kC;
+                tc::mbar_arrive_expect_tx(bar, kStageTx);
+                tc::tma_load_4d(st + kSK0, &tm_k, bar, 0, h, t0, b);
+                tc::tma_load_4d(st + kSQ0, &tm_q, bar, 0, h, t0, b);
+                tc::tma_load_4d(st + kSK1, &tm_k, bar, 64, h, t0, b);
+                tc::tma_load_4d(st + kSQ1, &tm_q, bar, 64, h, t0, b);
+                tc::tma_load_4d(st + kSV, &tm_v, bar, j0, h, t0, b);
+                tc::bulk_load(st + kSTU, rec0 + (size_t)c * kRecBytes,
+                              kRecBytes, bar);
+                *reinterpret_cast<volatile int*>(issued) = c + 1;
+                if (c + 2 * kNS < nchunks) prefetch(c + 2 * kNS);
+            }
+        }
+    } else if (tid >= kChainThreads) {
+        // =========================================================== helper
+        const int hl = tid - kChainThreads;          // TMEM lane
+        const uint32_t tl = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+        // [-W; -PTU Kg]: the negation rides on the instruction (negate A)
+        constexpr uint32_t idA = tc::idesc_bf16(128, 128, false, true, true);
+        constexpr uint32_t idB = tc::idesc_bf16(128, kNV, false, true);
+        int committed = -1;
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c % kNS;
+            uint8_t* st = sm + s * kStage;
+            const uint32_t sst = sbase + s * kStage;
+            bool ok = tc::mbar_wait_or_abort(&bars[kBFull + s], (c / kNS) & 1,
+                                             vabort, p.wait_ns);
+            if (ok && c >= 2)   // accumulator of this parity read out
+                ok = tc::mbar_wait_or_abort(&bars[kBAccFree + (c & 1)],
+                                            ((c - 2) >> 1) & 1, vabort, p.wait_ns);
+            if (tc::named_bar_or(kBarHelper, kHelperThreads, !ok)) {
+                *vabort = 1;
+                break;
+            }
+            // Diag(gamma) K into Kg; Diag(Gamma_C) K kept in registers
+            const float* g2 = reinterpret_cast<const float*>(st + kSG);
+            const int r = hl & 63, hh = hl >> 6;
+            const __nv_bfloat162 gam = __float2bfloat162_rn(tc::ex2(g2[r]));
+            const __nv_bfloat162 gamC =
+                __float2bfloat162_rn(tc::ex2(g2[kC - 1] - g2[r]));
+            // (16-byte chunk (j + r) mod 8 at step j: the 8 rows a quarter
+            // warp touches at once sit in 8 different bank groups; a chunk
+            // keeps its swizzled position, the scaling is per row)
+            {
+                const uint8_t* krow = st + (hh ? kSK1 : kSK0) + r * 128;
+                uint8_t* grow = sm + kSKg + hh * 8192 + r * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int cj = ((j + r) & 7) << 4;
+                    const uint4 u = *reinterpret_cast<const uint4*>(krow + cj);
+                    *reinterpret_cast<uint4*>(grow + cj) = scale8(u, gam);
+                }
+            }
+            tc::fence_proxy_async_smem();
+            tc::named_bar_sync(kBarHelper, kHelperThreads);
+            if (hl == 0) {
+                tc::tc_fence_after();
+                // [-W; -PTU Kg] = -[TU; PTU] Kg    (M 128, N 128, K 64)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + kColH, desc_k(sst + kSTU + ks * 32),
+                                 desc_mn(sbase + kSKg + ks * 2048, 8192), idA,
+                                 ks > 0);
+                // [U; PTU V] = [TU; PTU] V       (M 128, N 64, K 64)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + kColAcc + 64 * (c & 1),
+                                 desc_k(sst + kSTU + ks * 32),
+                                 desc_mn(sst + kSV + ks * 2048, 0), idB,
+                                 ks > 0);
+                tc::mma_commit(&bars[kBHmma]);
+            }
+            __syncwarp();   // the issuing lane rejoins before the waits
+            committed = c;
+            if (tc::named_bar_or(kBarHelper, kHelperThreads,
+                                 !tc::mbar_wait_or_abort(&bars[kBHmma], c & 1,
+                                                         vabort, p.wait_ns))) {
+                *vabort = 1;
+                break;
+            }
+            tc::tc_fence_after();
+            if (hl < kC) {
+                // Diag(Gamma_C) K row hl over [TU; PTU] (read by the
+                // finished MMAs), then -W row hl over K (both halves)
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const uint8_t* krow = st + (half ? kSK1 : kSK0) + hl * 128;
+                    uint8_t* grow = st + kSTU + half * 8192 + hl * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int cj = ((j + hl) & 7) << 4;
+                        *reinterpret_cast<uint4*>(grow + cj) = scale8(
+                            *reinterpret_cast<const uint4*>(krow + cj), gamC);
+                    }
+                }
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    float x[64];
+                    tc::tmem_ld32(tl + kColH + 64 * half, x);
+                    tc::tmem_ld32(tl + kColH + 64 * half + 32, x + 32);
+                    tc::tmem_ld_wait();
+                    st_row(st + (half ? kSK1 : kSK0), hl, x);
+                }
+            } else {
+                // Q' row = gamma_r Q_r + (-PTU Kg)_r over Q (in place; packed
+                // bf16 fma, the TMEM values rounded to bf16 first)
+                const int rq = hl - kC;
+                const __nv_bfloat162 gq =
+                    __float2bfloat162_rn(tc::ex2(g2[rq]));
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    float x[64];
+                    tc::tmem_ld32(tl + kColH + 64 * half, x);
+                    tc::tmem_ld32(tl + kColH + 64 * half + 32, x + 32);
+                    tc::tmem_ld_wait();
+                    uint8_t* qrow = st + (half ? kSQ1 : kSQ0) + rq * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint4* pq = reinterpret_cast<uint4*>(
+                            qrow + ((j ^ (rq & 7)) << 4));
+                        uint4 u = *pq;
+                        const float* xj = x + 8 * j;
+                        u.x = as_u32(__hfma2(gq, as_bf2(u.x), as_bf2(
+                            tc::pack_bf16x2(xj[0], xj[1]))));
+                        u.y = as_u32(__hfma2(gq, as_bf2(u.y), as_bf2(
+                            tc::pack_bf16x2(xj[2], xj[3]))));
+                        u.z = as_u32(__hfma2(gq, as_bf2(u.z), as_bf2(
+                            tc::pack_bf16x2(xj[4], xj[5]))));
+                        u.w = as_u32(__hfma2(gq, as_bf2(u.w), as_bf2(
+                            tc::pack_bf16x2(xj[6], xj[7]))));
+                        *pq = u;
+                    }
+                }
+            }
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            tc::named_bar_sync(kBarHelper, kHelperThreads);
+            if (hl == 0) tc::mbar_arrive(&bars[kBReady + s]);
+        }
+        if (*vabort && hl == 0 && committed >= 0)   // drain own MMAs
+            tc::mbar_wait(&bars[kBHmma], committed & 1, 100000000ull);
+    } else {
+        // ============================================================ chain
+        const int row = tid;                      // TMEM lane
+        const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+        constexpr uint32_t idN = tc::idesc_bf16(128, kNV, false, true);
+        constexpr uint32_t idDS = tc::idesc_bf16(128, kNV, true, true);
+        int last_c1 = -1, last_c2 = -1;
+        bool failed = false;
+        for (int c = 0; c < nchunks && !failed; ++c) {
+            const int s = c % kNS;
+            const uint8_t* st = sm + s * kStage;
+            const uint32_t sst = sbase + s * kStage;
+            const uint32_t acc = tmem + kColAcc + 64 * (c & 1);
+            if constexpr (kCkpt) {   // the state chunk c starts from (fp32)
+                float* dst = p.ckpt +
+                             (((size_t)bh * nchunks + c) * kD + row) * kD + j0;
+#pragma unroll
+                for (int j = 0; j < kNV; j += 4)
+                    *reinterpret_cast<float4*>(dst + j) =
+                        make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+            }
+            if (tc::named_bar_or(kBarChain, kChainThreads,
+                                 !tc::mbar_wait_or_abort(&bars[kBReady + s],
+                                                         (c / kNS) & 1,
+                                                         vabort, p.wait_ns))) {
+                failed = true;
+                break;
+            }
+            tc::tc_fence_after();
+            if (tid == 0) {   // [U~; O] = [U; PTU V] + [-W; Q'] S
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16(acc,
+                                 desc_k(sst + (ks >> 2) * 16384 +
+                                        (ks & 3) * 32),
+                                 desc_mn(sbase + kSS + ks * 2048, 0), idN,
+                                 true);
+                tc::mma_commit(&bars[kBC1]);
+                last_c1 = c;
+            }
+            __syncwarp();
+            const float* g2 = reinterpret_cast<const float*>(st + kSG);
+            bool ok = tc::mbar_wait_or_abort(&bars[kBC1], c & 1, vabort, p.wait_ns);
+            if (warp < 2) {
+                // U~ row (token) to shared memory, then dS = KG^T U~
+                if (ok) {
+                    tc::tc_fence_after();
+                    float x[64];
+                    tc::tmem_ld32(tl + (acc - tmem), x);
+                    tc::tmem_ld32(tl + (acc - tmem) + 32, x + 32);
+                    tc::tmem_ld_wait();
+                    st_row(sm + kSUt, row, x);
+                    tc::fence_proxy_async_smem();
+                }
+                tc::tc_fence_before();
+                ok = !tc::named_bar_or(kBarChainLo, 64, !ok);
+                if (ok && tid == 0) {
+                    tc::tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma_bf16(tmem + kColDS,
+                                     desc_mn(sst + kSTU + ks * 2048, 8192),
+                                     desc_mn(sbase + kSUt + ks * 2048, 0),
+                                     idDS, ks > 0);
+                    tc::mma_commit(&bars[kBC2]);
+                    last_c2 = c;
+                }
+                __syncwarp();
+            } else if (ok && !kCkpt) {
+                // o of the chunk (row - 64 = token) through shared memory
+                // and one TMA store (rows past T are clipped by the copy);
+                // the image is free once the previous store has read it
+                if (tid == kC) tc::tma_store_wait_read<0>();
+                tc::tc_fence_after();
+                float x[64];
+                tc::tmem_ld32(tl + (acc - tmem), x);
+                tc::tmem_ld32(tl + (acc - tmem) + 32, x + 32);
+                tc::tmem_ld_wait();
+                tc::named_bar_sync(kBarChainHi, 64);
+                st_row(sm + kSO, row - kC, x);
+                tc::fence_proxy_async_smem();
+                tc::named_bar_sync(kBarChainHi, 64);
+                if (tid == kC) {
+                    tc::tma_store_4d(&tm_o, sm + kSO, j0, h, c * kC, b);
+                    tc::tma_store_commit();
+                }
+            }
+            ok = ok && tc::mbar_wait_or_abort(&bars[kBC2], c & 1, vabort, p.wait_ns);
+            if (tc::named_bar_or(kBarChain, kChainThreads, !ok)) {
+                failed = true;
+                break;
+            }
+            tc::tc_fence_after();
+            {   // S <- gamma_C S + dS
+                const float gC = tc::ex2(g2[kC - 1]);
+                float x[64];
+                tc::tmem_ld32(tl + kColDS, x);
+                tc::tmem_ld32(tl + kColDS + 32, x + 32);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < kNV; ++j) S[j] = fmaf(gC, S[j], x[j]);
+                st_row(sm + kSS, row, S);
+            }
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            tc::named_bar_sync(kBarChain, kChainThreads);
+            if (tid == 0) {
+                tc::mbar_arrive(&bars[kBEmpty + s]);
+                tc::mbar_arrive(&bars[kBAccFree + (c & 1)]);
+            }
+        }
+        if (failed) {
+            *vabort = 1;
+            if (tid == 0) {   // drain own MMAs
+                if (last_c1 >= 0)
+                    tc::mbar_wait(&bars[kBC1], last_c1 & 1, 100000000ull);
+                if (last_c2 >= 0)
+                    tc::mbar_wait(&bars[kBC2], last_c2 & 1, 100000000ull);
+            }
+        }
+    }
+
+    if (tid == kC && !kCkpt) tc::tma_store_wait_all<0>();   // o written
+    __syncthreads();
+    if (*vabort) {
+        if (tid == 0) {
+            atomicOr(&g_fault_word2, 1u);
+            const int n = *reinterpret_cast<volatile int*>(issued);
+            for (int c = n - kNS < 0 ? 0 : n - kNS; c < n; ++c)
+                tc::mbar_wait(&bars[kBFull + c % kNS], (c / kNS) & 1,
+                              100000000ull);
+        }
+    } else if (tid < kChainThreads && p.hT) {
+        float* dst = p.hT + ((size_t)bh * kD + tid) * kD + j0;
+#pragma unroll
+        for (int j = 0; j < kNV; j += 4)
+            *reinterpret_cast<float4*>(dst + j) =
+                make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------- host side
+
+bool aligned16(const void* ptr) {
+    return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0;
+}
+
+// [1, 64, H, 128] map standing for an all-zero V: every load of the kernel
+// falls outside it (and reads zeros) except the first chunk of sequence 0,
+// which reads the zero tile itself.
+bool make_v_map(CUtensorMap* m, const FwdArgs& a) {
+    return a.v_zero ? make_map(m, a.v, 1, kC, a.H)
+                    : make_map(m, a.v, a.B, a.T, a.H);
+}
+
+cudaError_t set_smem(const void* kern, int bytes, std::atomic<unsigned long long>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done.load() & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit);
+    return e;
+}
+
+std::atomic<unsigned long long> g_prep_attr{0}, g_state_attr[2];
+
+}  // namespace
+
+size_t chunk_tc2_workspace_bytes(int B, int T, int H) {
+    const size_t nch = ((size_t)T + kC - 1) / kC;
+    return (size_t)B * H * nch * kRecBytes;
+}
+
+bool chunk_tc2_eligible(const FwdArgs& a) {
+    return a.dtype == KLA_BF16 && a.dk == kD && a.dv == kD && a.C == kC &&
+           !a.kw && aligned16(a.q) && aligned16(a.k) && aligned16(a.v) &&
+           (!a.o || aligned16(a.o)) && (!a.h0 || aligned16(a.h0)) &&
+           (!a.hT || aligned16(a.hT)) && get_encoder();
+}
+
+cudaError_t launch_chunk_tc2(const FwdArgs& a, void* workspace,
+                             cudaStream_t stream) {
+    if ((long)a.B * a.H == 0 || a.T == 0) return cudaSuccess;
+    if (!get_encoder()) return cudaErrorNotSupported;
+    if ((a.o == nullptr) == (a.ckpt == nullptr)) return cudaErrorInvalidValue;
+    if (!workspace || !aligned16(workspace)) return cudaErrorInvalidValue;
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map(&mq, a.q, a.B, a.T, a.H) ||
+        !make_map(&mk, a.k, a.B, a.T, a.H) || !make_v_map(&mv, a) ||
+        !make_map(&mo, a.o ? a.o : a.q, a.B, a.T, a.H))
+        return cudaErrorInvalidValue;
+    const int nchunks = (a.T + kC - 1) / kC;
+    const long nprep = (long)a.B * a.H * nchunks;
+    if (nprep > 0x7fffffffL) return cudaErrorInvalidValue;
+    cudaError_t e = set_smem((const void*)kla_prep_kernel, kPSmem, g_prep_attr);
+    if (e != cudaSuccess) return e;
+    uint8_t* rec = static_cast<uint8_t*>(workspace);
+    PrepParams pp{a.log_alpha, a.eta, rec, a.eps, a.gdn, a.T, a.H, nchunks};
+    kla_prep_kernel<<<(unsigned)nprep, kPrepThreads, kPSmem, stream>>>(mq, mk,
+                                                                      pp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    auto kern = a.ckpt ? kla_state_kernel<true> : kla_state_kernel<false>;
+    e = set_smem((const void*)kern, kSSmem, g_state_attr[a.ckpt ? 1 : 0]);
+    if (e != cudaSuccess) return e;
+    StateParams sp{a.h0, static_cast<__nv_bfloat16*>(a.o), a.hT, a.ckpt, rec,
+                   a.T, a.H, nchunks, 2000000000ull, 0};
+    dim3 grid((unsigned)((long)a.B * a.H), kD / kNV);
+    kern<<<grid, kStateThreads, kSSmem, stream>>>(mq, mk, mv, mo, sp);
+    return cudaGetLastError();
+}
+
+namespace {
+// Device memory the self-test's tensor maps point at; never read (the
+// self-test's producer issues no copy).
+__device__ __align__(1024) uint8_t g_selftest_tile[64 * kD * 2];
+}  // namespace
+
+cudaError_t launch_state_selftest(cudaStream_t stream) {
+    if (!get_encoder()) return cudaErrorNotSupported;
+    void* base = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&base, g_selftest_tile);
+    if (e != cudaSuccess) return e;
+    CUtensorMap m;
+    if (!make_map(&m, base, 1, kC, 1)) return cudaErrorInvalidValue;
+    e = set_smem((const void*)kla_state_kernel<false>, kSSmem, g_state_attr[0]);
+    if (e != cudaSuccess) return e;
+    // one CTA, one chunk; its waits give up after 1 ms
+    StateParams sp{nullptr, static_cast<__nv_bfloat16*>(base), nullptr,
+                   nullptr, static_cast<const uint8_t*>(base), kC, 1, 1,
+                   1000000ull, 1};
+    kla_state_kernel<false><<<dim3(1, 1), kStateThreads, kSSmem, stream>>>(
+        m, m, m, m, sp);
+    return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_fault2(unsigned int* word) {
+    cudaError_t e = cudaMemcpyFromSymbol(word, g_fault_word2,
+                                         sizeof(unsigned int));
+    if (e != cudaSuccess) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_fault_word2, &zero, sizeof(unsigned int));
+}
+
+}  // namespace kla

@@ -7,7 +7,9 @@
 // per tensor alternate between segments.  Each segment's kernel starts from
 // the fp32 state the previous one ended with, exactly as the state is
 // carried from chunk to chunk inside one launch, so the result is that of
-// kla_chunk_fwd_ex on the whole sequence.
+// kla_chunk_fwd_ex on the whole sequence.  The forward's own workspace (the
+// pre-pass records of the two-kernel tensor-core path) is part of this
+// call's workspace, so nothing is allocated.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -84,13 +86,16 @@ void segments(int T, int C, int* tseg, int* nseg) {
 }
 
 // Byte layout of the workspace: per slot q | k | v | log_alpha | eta | o,
-// then two fp32 states.
+// then two fp32 states, then the forward's own workspace for one segment
+// (the segments' kernels run one after another on the caller's stream).
 struct Layout {
-    size_t q, k, v, g, o, slot, state, total;
+    size_t q, k, v, g, o, slot, state, fwd, total;
 };
 
-Layout layout(int B, int tseg, int H, int dk, int dv, size_t esz) {
+Layout layout(int B, int tseg, int H, int dk, int dv, int C,
+              kla_dtype dtype) {
     Layout L;
+    const size_t esz = dtype == KLA_BF16 ? 2 : 4;
     const size_t rows = (size_t)B * tseg * H;
     L.q = round_up(rows * dk * esz);
     L.k = L.q;
@@ -99,7 +104,11 @@ Layout layout(int B, int tseg, int H, int dk, int dv, size_t esz) {
     L.o = L.v;
     L.slot = L.q + L.k + L.v + 2 * L.g + L.o;
     L.state = round_up((size_t)B * H * dk * dv * sizeof(float));
-    L.total = kSlots * L.slot + 2 * L.state;
+    size_t fwd = 0;
+    kla_chunk_fwd_workspace_size(B, tseg, H, dk, dv, C, dtype, KLA_ALGO_AUTO,
+                                 &fwd);
+    L.fwd = round_up(fwd);
+    L.total = kSlots * L.slot + 2 * L.state + L.fwd;
     return L;
 }
 
@@ -143,9 +152,8 @@ extern "C" kla_status kla_chunk_fwd_host_workspace_size(
     if (!valid_sizes(dk, dv, C)) return KLA_ERR_UNSUPPORTED_SHAPE;
     int tseg = 0, nseg = 0;
     segments(T, C, &tseg, &nseg);
-    const size_t esz = dtype == KLA_BF16 ? 2 : 4;
     *bytes = (long long)B * H == 0 ? 0
-                                   : layout(B, tseg, H, dk, dv, esz).total;
+                                   : layout(B, tseg, H, dk, dv, C, dtype).total;
     return KLA_OK;
 }
 
@@ -159,7 +167,8 @@ extern "C" kla_status kla_chunk_fwd_host(
     kla_status st =
         kla_chunk_fwd_host_workspace_size(B, T, H, dk, dv, C, dtype, &need);
     if (st != KLA_OK) return st;
-    if (algo != KLA_ALGO_AUTO && algo != KLA_ALGO_SIMT && algo != KLA_ALGO_TC)
+    if (algo != KLA_ALGO_AUTO && algo != KLA_ALGO_SIMT &&
+        algo != KLA_ALGO_TC && algo != KLA_ALGO_TC_FUSED)
         return KLA_ERR_INVALID_ARG;
     if (rule != KLA_STEP_KACZMARZ && rule != KLA_STEP_GIVEN)
         return KLA_ERR_INVALID_ARG;
@@ -184,10 +193,11 @@ extern "C" kla_status kla_chunk_fwd_host(
     int tseg = 0, nseg = 0;
     segments(T, C, &tseg, &nseg);
     const size_t esz = dtype == KLA_BF16 ? 2 : 4;
-    const Layout L = layout(B, tseg, H, dk, dv, esz);
+    const Layout L = layout(B, tseg, H, dk, dv, C, dtype);
     char* ws = static_cast<char*>(workspace);
     float* state[2] = {reinterpret_cast<float*>(ws + kSlots * L.slot),
                        reinterpret_cast<float*>(ws + kSlots * L.slot + L.state)};
+    void* fwd_ws = L.fwd ? ws + kSlots * L.slot + 2 * L.state : nullptr;
     const size_t state_bytes = (size_t)B * H * dk * dv * sizeof(float);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t mp = P.max_pitch;
@@ -258,10 +268,10 @@ extern "C" kla_status kla_chunk_fwd_host(
         if (i >= kSlots) KLA_TRY(cudaStreamWaitEvent(s, P.out_done[j], 0));
         const float* sin = i == 0 ? (h0 ? state[1] : nullptr)
                                   : state[(i - 1) % 2];
-        st = kla_chunk_fwd_ex(dq, dk_, dvv, reinterpret_cast<float*>(dla),
+        st = kla_chunk_fwd_ws(dq, dk_, dvv, reinterpret_cast<float*>(dla),
                               reinterpret_cast<float*>(det), eps, sin, dout,
                               state[i % 2], B, tn, H, dk, dv, C, dtype, algo,
-                              rule, stream);
+                              rule, fwd_ws, L.fwd, stream);
         if (st != KLA_OK) return st;
         KLA_TRY(cudaEventRecord(P.comp_done[j], s));
 

@@ -1,6 +1,7 @@
 // Internal launchers of libkla.so (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -103,6 +104,19 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_simt(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_chunk_tc(const FwdArgs& a, cudaStream_t stream);
 bool chunk_tc_eligible(const FwdArgs& a);
+// Two-kernel tensor-core forward (chunk-parallel pre-pass, then the state
+// pass): bf16, dk = dv = 128, C = 64, no separate write keys.  The workspace
+// holds the pre-pass records: chunk_tc2_workspace_bytes(B, T, H) bytes,
+// 16-byte aligned.  Takes exactly one of a.o and a.ckpt.
+bool chunk_tc2_eligible(const FwdArgs& a);
+size_t chunk_tc2_workspace_bytes(int B, int T, int H);
+cudaError_t launch_chunk_tc2(const FwdArgs& a, void* workspace,
+                             cudaStream_t stream);
+cudaError_t read_and_clear_fault2(unsigned int* word);
+// One CTA of the state-pass kernel whose producer issues no copy and whose
+// waits give up after 1 ms: it takes the kernel's abort path and sets the
+// fault word.
+cudaError_t launch_state_selftest(cudaStream_t stream);
 // Backward pass: the checkpointing forward, the reverse state-gradient
 // recurrence and the per-chunk gradients (CUDA cores, fp32).
 cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t stream);
@@ -113,6 +127,12 @@ size_t chunk_bwd_workspace_floats(int B, int T, int H, int dk, int dv, int C);
 kla_status check_chunk_bwd_args(const BwdArgs& a);
 // SM count of the current device (cached per device).
 int device_sm_count();
+
+// cuTensorMapEncodeTiled from the driver (looked up once); false if absent.
+bool get_encoder();
+// Tensor map of a [B, T, H, 128] bf16 tensor with 128-byte swizzle and boxes
+// of 64 features x 1 head x 64 tokens x 1 batch (zero fill out of range).
+bool make_map(CUtensorMap* m, const void* base, int B, int T, int H);
 
 // Device fault word of the tensor-core kernels (bounded waits that gave up).
 // read_and_clear_fault synchronises the stream first.

@@ -321,7 +321,7 @@ extern "C" kla_status kla_chunk_fwd_seq(
     const int P = choose_segments(B, T, H, segments);
     if ((long long)B * H == 0 || T == 0 || P == 1)   // nothing to split
         return kla_chunk_fwd_ex(q, k, v, log_alpha, eta, eps, h0, o, hT, B, T,
-                                H, dk, dv, C, dtype, KLA_ALGO_TC, rule,
+                                H, dk, dv, C, dtype, KLA_ALGO_TC_FUSED, rule,
                                 stream);
     if (!q || !k || !v || !log_alpha || !eta || !o) return KLA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||

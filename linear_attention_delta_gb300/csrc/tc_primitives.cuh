@@ -73,7 +73,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // of a kernel share one copy of the spin loop: polls until the phase with
 // the given parity completes (true), `limit_ns` nanoseconds pass or *abort
 // (when given) becomes non-zero (false).
-__device__ __noinline__ bool mbar_spin(uint32_t bar, uint32_t parity,
+static __device__ __noinline__ bool mbar_spin(uint32_t bar, uint32_t parity,
                                        const volatile int* abort,
                                        uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
@@ -379,6 +379,80 @@ __device__ __forceinline__ void tmem_st_wait() {
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
     const uint32_t chunk = (col >> 3) ^ (row & 7);       // 16-byte chunk
     return row * 128u + (chunk << 4) + ((col & 7u) << 1);
+}
+
+}  // namespace tc
+}  // namespace kla
+
+namespace kla {
+namespace tc {
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global to this CTA's shared memory, completing on `bar` (complete_tx).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src,
+                                          uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// fp32 -> tf32 (round to nearest, ties away), as a 32-bit register.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// Warp-level D = A * B + D, m16n8k8, tf32 operands, fp32 accumulate.
+// Fragments (g = lane / 4, t = lane % 4):
+//   a[0] = A[g][t]  a[1] = A[g+8][t]  a[2] = A[g][t+4]  a[3] = A[g+8][t+4]
+//   b0 = B[t][g]    b1 = B[t+4][g]
+//   d  = {D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1]}
+__device__ __forceinline__ void mma_m16n8k8_tf32(float (&d)[4],
+                                                 const uint32_t (&a)[4],
+                                                 uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+}  // namespace tc
+}  // namespace kla
+
+namespace kla {
+namespace tc {
+
+// Prefetch `bytes` (multiple of 16) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src,
+                                                 uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                     reinterpret_cast<uint64_t>(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+}  // namespace tc
+}  // namespace kla
+
+namespace kla {
+namespace tc {
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory to global memory, in the current bulk group
+// (commit with tma_store_commit, wait with tma_store_wait_read /
+// tma_store_wait_all).
+__device__ __forceinline__ void bulk_store(void* dst, const void* src,
+                                           uint32_t bytes) {
+    asm volatile(
+        "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+            reinterpret_cast<uint64_t>(dst)),
+        "r"(smem_u32(src)), "r"(bytes)
+        : "memory");
 }
 
 }  // namespace tc

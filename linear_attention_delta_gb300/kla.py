@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "KLA_OK", -1: "KLA_ERR_INVALID_ARG",
                 -2: "KLA_ERR_UNSUPPORTED_SHAPE", -3: "KLA_ERR_CUDA",
                 -4: "KLA_ERR_TIMEOUT", -5: "KLA_ERR_NOT_IMPLEMENTED"}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
-ALGOS = {"auto": 0, "simt": 1, "tc": 2}
+ALGOS = {"auto": 0, "simt": 1, "tc": 2, "tc_fused": 3}
 RULES = {"kaczmarz": 0, "given": 1}
 
 # name -> (restype, argtypes) of every symbol include/kla.h declares
@@ -31,6 +31,12 @@ SIGNATURES = {
                            _I, _I, _I, _I, _I, _I, _I, _VP]),
     "kla_chunk_fwd_ex": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP, _FP,
                               _I, _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
+    "kla_chunk_fwd_workspace_size": (
+        _I, [_I, _I, _I, _I, _I, _I, _I, _I,
+             ctypes.POINTER(ctypes.c_size_t)]),
+    "kla_chunk_fwd_ws": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP, _FP,
+                              _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                              _VP, ctypes.c_size_t, _VP]),
     "kla_decode_step": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
                              _I, _I, _I, _I, _I, _VP]),
     "kla_decode_step_ex": (_I, [_VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
@@ -62,6 +68,7 @@ SIGNATURES = {
                                 _I, _I, _I, _I, _I, _I, _I, _I, _I,
                                 _VP, ctypes.c_size_t, _VP]),
     "kla_device_status": (_I, [_VP]),
+    "kla_selftest_wait_timeout": (_I, [_VP]),
     "kla_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -120,15 +127,44 @@ def _check_cuda(name, t, dtype=None):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def chunk_fwd_workspace_size(B, T, H, dk, dv, C, dtype, algo="auto") -> int:
+    """Bytes of device workspace ``chunk_fwd`` needs
+    (``kla_chunk_fwd_workspace_size``); 0 for paths that need none."""
+    n = ctypes.c_size_t(0)
+    st = load_library().kla_chunk_fwd_workspace_size(
+        B, T, H, dk, dv, int(C), DTYPES[dtype], ALGOS[algo], ctypes.byref(n))
+    if st != KLA_OK:
+        raise KlaError("kla_chunk_fwd_workspace_size", st)
+    return n.value
+
+
+def forward_path(B, T, H, dk, dv, C, dtype, algo="auto") -> dict:
+    """Which forward kernels ``chunk_fwd`` launches for these sizes (with
+    16-byte-aligned tensors, as torch allocates them): the name of the
+    path, kernel launches per call and the kernel whose DRAM traffic
+    dominates."""
+    if chunk_fwd_workspace_size(B, T, H, dk, dv, C, dtype, algo) > 0:
+        return {"name": "prepass+state", "launches": 2,
+                "traffic_key": "kla_state_kernel"}
+    if dtype == torch.bfloat16 and dk == dv == 128 and C == 64 and \
+            algo in ("auto", "tc", "tc_fused"):
+        return {"name": "fused", "launches": 1,
+                "traffic_key": "kla_chunk_tc"}
+    return {"name": "simt", "launches": 1, "traffic_key": "kla_chunk_simt"}
+
+
 def chunk_fwd(q, k, v, log_alpha, eta, eps: float = 1e-6, h0=None,
               C: int = 64, algo: str = "auto", o=None, hT=None,
-              want_state: bool = True, stream=None, rule: str = "kaczmarz"):
-    """KLA forward pass (``kla_chunk_fwd_ex``).
+              want_state: bool = True, stream=None, rule: str = "kaczmarz",
+              workspace=None):
+    """KLA forward pass (``kla_chunk_fwd_ws``).
 
     q, k [B,T,H,dk]; v [B,T,H,dv] (fp32 or bf16, same dtype); log_alpha, eta
     [B,T,H] fp32; h0 [B,H,dk,dv] fp32 or None.  Returns (o, hT); hT is None
     when ``want_state`` is False.  ``o``/``hT`` may be passed preallocated.
     ``rule="given"`` uses eta as the step directly (gated DeltaNet).
+    ``workspace``: a device uint8 tensor of at least
+    ``chunk_fwd_workspace_size`` bytes, allocated here (by torch) when None.
     """
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_cuda(n, t, q.dtype)
@@ -144,12 +180,18 @@ def chunk_fwd(q, k, v, log_alpha, eta, eps: float = 1e-6, h0=None,
         o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     if hT is None and want_state:
         hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
-    st = load_library().kla_chunk_fwd_ex(
+    need = chunk_fwd_workspace_size(B, T, H, dk, dv, C, q.dtype, algo)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is not None:
+        _check_cuda("workspace", workspace, torch.uint8)
+    st = load_library().kla_chunk_fwd_ws(
         _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(eta), float(eps),
         _ptr(h0), _ptr(o), _ptr(hT), B, T, H, dk, dv, int(C),
-        DTYPES[q.dtype], ALGOS[algo], RULES[rule], _stream(stream))
+        DTYPES[q.dtype], ALGOS[algo], RULES[rule], _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _stream(stream))
     if st != KLA_OK:
-        raise KlaError("kla_chunk_fwd_ex", st)
+        raise KlaError("kla_chunk_fwd_ws", st)
     return o, hT
 
 
@@ -463,3 +505,9 @@ def decode_step_kw(q, k, k_write, v, log_alpha, eta, S, eps: float = 1e-6,
 def device_status(stream=None) -> int:
     """``kla_device_status``: sync the stream, read and clear the fault word."""
     return int(load_library().kla_device_status(_stream(stream)))
+
+
+def selftest_wait_timeout(stream=None) -> int:
+    """``kla_selftest_wait_timeout``: one kernel whose device-side waits give
+    up after 1 ms (nothing arrives on them); returns the launch status."""
+    return int(load_library().kla_selftest_wait_timeout(_stream(stream)))

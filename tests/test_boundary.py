@@ -231,9 +231,13 @@ def test_host_fwd_workspace_size(lib):
     assert lib.kla_chunk_fwd_host_workspace_size(
         4, 4096, 16, 128, 128, 64, 1, ctypes.byref(n)) == OK
     # two slots of one segment (512 tokens: q, k, v, o bf16, two fp32
-    # gates) and two fp32 states
+    # gates), two fp32 states and the forward's own workspace for one
+    # segment (none: the default path is the fused kernel)
     rows = 4 * 512 * 16
-    assert n.value == 2 * rows * (4 * 128 * 2 + 8) + 2 * 4 * 16 * 128 * 128 * 4
+    fwd = kla.chunk_fwd_workspace_size(4, 512, 16, 128, 128, 64,
+                                       kla.torch.bfloat16)
+    assert n.value == (2 * rows * (4 * 128 * 2 + 8) +
+                       2 * 4 * 16 * 128 * 128 * 4 + fwd)
     assert lib.kla_chunk_fwd_host_workspace_size(
         0, 64, 3, 16, 16, 16, 0, ctypes.byref(n)) == OK and n.value == 0
     assert lib.kla_chunk_fwd_host_workspace_size(
@@ -352,3 +356,26 @@ def test_overlapping_buffers_are_refused_on_host(lib):
                            V(b[8]), V(b[9]), V(b[10]), None, 1, 64, 2, 16, 16,
                            16, 1, 0, V(b[11]), 1 << 20, None)
     assert st == INVALID
+
+
+def test_forward_workspace_size_and_missing_workspace(lib):
+    """The two-kernel tensor-core path needs 16640 bytes per (batch, head,
+    64-token chunk); the other paths need none; kla_chunk_fwd_ws refuses a
+    missing workspace when one is needed, before any device call."""
+    assert kla.chunk_fwd_workspace_size(2, 200, 3, 128, 128, 64,
+                                        kla.torch.bfloat16, "tc") == \
+        2 * 3 * 4 * 16640
+    for algo in ("simt", "tc_fused"):
+        assert kla.chunk_fwd_workspace_size(2, 200, 3, 128, 128, 64,
+                                            kla.torch.bfloat16, algo) == 0
+    assert kla.chunk_fwd_workspace_size(2, 200, 3, 16, 16, 16,
+                                        kla.torch.float32) == 0
+    V = ctypes.c_void_p
+    b = _bufs(8)
+    st = lib.kla_chunk_fwd_ws(V(b[0]), V(b[1]), V(b[2]), V(b[3]), V(b[4]),
+                              1e-6, None, V(b[5]), None, 1, 64, 1, 128, 128,
+                              64, 1, 2, 0, None, 0, None)
+    assert st == INVALID
+    n = ctypes.c_size_t(0)
+    assert lib.kla_chunk_fwd_workspace_size(1, 64, 1, 128, 128, 64, 1, 7,
+                                            ctypes.byref(n)) == INVALID

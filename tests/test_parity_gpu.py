@@ -444,3 +444,54 @@ def test_golden_worked_example_through_the_library():
     hT[:, :, :2, :2] = 0
     assert np.all(hT == 0)
 
+
+
+def test_device_wait_timeout_is_reported_then_cleared():
+    """The bounded-wait path of the tensor-core state kernel: one CTA whose
+    copy-issuing thread issues nothing waits 1 ms on barriers nothing will
+    arrive on, takes its abort path and sets the fault word; the next
+    kla_device_status reports KLA_ERR_TIMEOUT, the one after KLA_OK, and a
+    forward pass afterwards is correct (the context stays usable)."""
+    assert kla.device_status() == 0
+    assert kla.selftest_wait_timeout() == 0
+    assert kla.device_status() == -4          # KLA_ERR_TIMEOUT
+    assert kla.device_status() == 0
+    check_fwd(gen.prefill_inputs(gen.LAYER_1B, B=1, T=130, H=2), "tc")
+
+
+def test_two_kernel_and_fused_tensor_core_paths_agree():
+    """The two tensor-core forward paths (pre-pass + state pass, and the
+    single fused kernel) on the same inputs: both within the bf16 bound of
+    the oracle, and within it of each other."""
+    inp = gen.prefill_inputs(gen.LAYER_1B, B=2, T=300, H=3)
+    o2, h2 = run_fwd(inp, "tc")
+    of, hf = run_fwd(inp, "tc_fused")
+    o_ref, h_ref = oracle_fwd(inp)
+    for o, h in ((o2, h2), (of, hf)):
+        assert rel_err(o, o_ref) <= 2e-2 and rel_err(h, h_ref) <= 2e-2
+    assert rel_err(o2, of.double().cpu().numpy()) <= 2e-2
+
+
+def test_forward_workspace_and_stream_ordered_scratch_agree():
+    """kla_chunk_fwd_ws with a caller workspace and kla_chunk_fwd_ex with
+    the library's stream-ordered scratch run the same kernels on the same
+    inputs: bit-identical o and hT (the kernels have no atomics)."""
+    import ctypes
+    inp = gen.prefill_inputs(gen.LAYER_1B, B=2, T=200, H=2)
+    d = to_dev(inp)
+    o_ws, h_ws = kla.chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"],
+                               d["eta"], d["eps"], d["h0"], C=64)
+    lib = kla.load_library()
+    P = lambda t: ctypes.c_void_p(0 if t is None else t.data_ptr())
+    o = torch.empty_like(o_ws)
+    hT = torch.empty_like(h_ws)
+    B, T, H, dk = inp["k"].shape
+    st = lib.kla_chunk_fwd_ex(P(d["q"]), P(d["k"]), P(d["v"]),
+                              P(d["log_alpha"]), P(d["eta"]),
+                              ctypes.c_float(inp["eps"]), P(d["h0"]), P(o),
+                              P(hT), B, T, H, dk, dk, 64, 1, 0, 0,
+                              ctypes.c_void_p(
+                                  torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ws) and torch.equal(hT, h_ws)

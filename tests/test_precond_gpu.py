@@ -144,12 +144,13 @@ def test_prefill_then_decode_handoff():
 
 
 def test_write_keys_equal_to_keys_give_the_plain_forward():
-    """With k_write = k the write-key mode computes exactly what the plain
-    forward does (same operands, same order): bit-identical o and state."""
+    """With k_write = k the write-key mode of the fused tensor-core kernel
+    computes exactly what its plain mode does (same operands, same order):
+    bit-identical o and state."""
     inp = gen.prefill_inputs(gen.LAYER_1B, B=2, T=300, H=3)
     d = dev(inp)
     o1, h1 = kla.chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["eta"],
-                           d["eps"], d["h0"], C=64)
+                           d["eps"], d["h0"], C=64, algo="tc_fused")
     o2, h2 = kla.chunk_fwd_kw(d["q"], d["k"], d["k"], d["v"],
                               d["log_alpha"], d["eta"], d["eps"], d["h0"],
                               C=64)

@@ -26,12 +26,12 @@
 // K-major bf16 tensor-core operand [TU; PTU], followed by g.
 //
 // State pass (kla_state_kernel): one CTA per (batch, head, 64 columns of
-// dv), walking the chunks in order.  A helper warpgroup prepares chunk c+1
-// while the chain warpgroup runs chunk c:
-//   helper: K_gamma = Diag(gamma) K; [-W; -PTU K_gamma] = -[TU; PTU] K_gamma
-//           and [U; PTU V] = [TU; PTU] V on the tensor cores; -W and Q'
-//           written over K and Q in the stage, Diag(Gamma_C) K over TU and
-//           PTU;
+// dv), walking the chunks in order.  Two helper warpgroups prepare the next
+// chunks (in turns) while the chain warpgroup runs chunk c:
+//   helper: K_gamma = Diag(gamma) K (in place of K); [-W; -PTU K_gamma] =
+//           -[TU; PTU] K_gamma and [U; PTU V] = [TU; PTU] V on the tensor
+//           cores; -W and Q' written over K_gamma and Q in the stage,
+//           Diag(Gamma_C) K over TU and PTU;
 //   chain:  [U~; O] = [U; PTU V] + [-W; Q'] S   (one MMA group of 8),
 //           U~ to shared memory, dS = (Diag(Gamma_C) K)^T U~  (4 MMAs),
 //           S <- gamma_C S + dS in registers (fp32, one key row per thread),
@@ -97,7 +97,8 @@ constexpr int kPT = kPL + kTileBytes;        // T = A^{-1}, fp32
 constexpr int kPY = kPT + kTileBytes;        // 4 warps x 16 x 8 fp32 scratch
 constexpr int kPG = kPY + 4 * 16 * 8 * 4;    // g2[64]
 constexpr int kPBeta = kPG + 256;            // beta[64]
-constexpr int kPBars = kPBeta + 256;         // 3 mbarriers
+constexpr int kPE = kPBeta + 256;            // column factors e_i[64]
+constexpr int kPBars = kPE + 256;            // 3 mbarriers
 constexpr int kPMisc = kPBars + 24;          // TMEM slot, warp total, flag
 constexpr int kPSmem = kPMisc + 16 + 1024;
 static_assert(kRecBytes <= kPL, "pre-pass map");
@@ -229,6 +230,14 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t tmem = *tmem_slot;
     if (tid >= 32 && tid < kC) g2 += *wtot;
     if (tid < kC) g2s[tid] = g2;
+    // Gamma_ri = 2^(g_r - g_m) e_i with g_m the g of the last column m of
+    // i's 16-column tile and e_i = 2^(g_m - g_i) <= 1: one ex2 per row and
+    // tile instead of one per element (a tile whose g spans more than 2^96
+    // takes the direct form, so that neither factor can overflow)
+    float* ecol = reinterpret_cast<float*>(sm + kPE);
+    if (tid < kC)
+        ecol[tid] = tc::ex2(__shfl_sync(0xffffffffu, g2, (lane & 16) | 15) -
+                            g2);
 
     // G = [K; Q] K^T: lanes 0..63 K K^T, lanes 64..127 Q K^T (columns 0..63)
     if (tid == 0) {
@@ -281,14 +290,25 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
             const float br = p.gdn ? et : (denom == 0.f ? 0.f : et / denom);
             betas[r] = br;
 #pragma unroll
-            for (int i = 0; i < 64; i += 4) {
-                const float4 gi = *reinterpret_cast<const float4*>(g2s + i);
-                float4 a;
-                a.x = i + 0 < r ? br * tc::ex2(g2 - gi.x) * x[i + 0] : 0.f;
-                a.y = i + 1 < r ? br * tc::ex2(g2 - gi.y) * x[i + 1] : 0.f;
-                a.z = i + 2 < r ? br * tc::ex2(g2 - gi.z) * x[i + 2] : 0.f;
-                a.w = i + 3 < r ? br * tc::ex2(g2 - gi.w) * x[i + 3] : 0.f;
-                *reinterpret_cast<float4*>(Lr + i) = a;
+            for (int m = 0; m < 4; ++m) {
+                const float gm = g2s[16 * m + 15];
+                const bool fact = fabsf(g2s[16 * m] - gm) <= 96.f;
+                const float bf = br * tc::ex2(g2 - gm);
+#pragma unroll
+                for (int i = 16 * m; i < 16 * m + 16; i += 4) {
+                    const float4 e = *reinterpret_cast<const float4*>(ecol + i);
+                    const float4 gi = *reinterpret_cast<const float4*>(g2s + i);
+                    float4 a;
+                    a.x = fact ? bf * e.x : br * tc::ex2(g2 - gi.x);
+                    a.y = fact ? bf * e.y : br * tc::ex2(g2 - gi.y);
+                    a.z = fact ? bf * e.z : br * tc::ex2(g2 - gi.z);
+                    a.w = fact ? bf * e.w : br * tc::ex2(g2 - gi.w);
+                    a.x = i + 0 < r ? a.x * x[i + 0] : 0.f;
+                    a.y = i + 1 < r ? a.y * x[i + 1] : 0.f;
+                    a.z = i + 2 < r ? a.z * x[i + 2] : 0.f;
+                    a.w = i + 3 < r ? a.w * x[i + 3] : 0.f;
+                    *reinterpret_cast<float4*>(Lr + i) = a;
+                }
             }
         } else {
             // P row r = tid - 64: Gamma_ri (Q K^T)_ri for i <= r, as bf16
@@ -296,21 +316,26 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
             const int r = tid - kC;
             const float gr = g2s[r];
 #pragma unroll
-            for (int i = 0; i < 64; i += 8) {
-                const float4 ga = *reinterpret_cast<const float4*>(g2s + i);
-                const float4 gb = *reinterpret_cast<const float4*>(g2s + i + 4);
-                const float gi[8] = {ga.x, ga.y, ga.z, ga.w,
-                                     gb.x, gb.y, gb.z, gb.w};
-                float e[8];
+            for (int m = 0; m < 4; ++m) {
+                const float gm = g2s[16 * m + 15];
+                const bool fact = fabsf(g2s[16 * m] - gm) <= 96.f;
+                const float f = tc::ex2(gr - gm);
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    e[k] = i + k <= r ? tc::ex2(gr - gi[k]) * x[i + k] : 0.f;
-                uint4 v;
-                v.x = tc::pack_bf16x2(e[0], e[1]);
-                v.y = tc::pack_bf16x2(e[2], e[3]);
-                v.z = tc::pack_bf16x2(e[4], e[5]);
-                v.w = tc::pack_bf16x2(e[6], e[7]);
-                *reinterpret_cast<uint4*>(out + kRecPTU + swz(r, i)) = v;
+                for (int i = 16 * m; i < 16 * m + 16; i += 8) {
+                    float e[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float gam =
+                            fact ? f * ecol[i + k] : tc::ex2(gr - g2s[i + k]);
+                        e[k] = i + k <= r ? gam * x[i + k] : 0.f;
+                    }
+                    uint4 v;
+                    v.x = tc::pack_bf16x2(e[0], e[1]);
+                    v.y = tc::pack_bf16x2(e[2], e[3]);
+                    v.z = tc::pack_bf16x2(e[4], e[5]);
+                    v.w = tc::pack_bf16x2(e[6], e[7]);
+                    *reinterpret_cast<uint4*>(out + kRecPTU + swz(r, i)) = v;
+                }
             }
         }
     }
@@ -452,16 +477,15 @@ constexpr int kSTU = 40960;          // [TU; PTU], later [KG_0 | KG_1] with
                                      // KG = Diag(Gamma_C) K
 constexpr int kSG = kSTU + kRecG;    // g (log2), 64 floats
 constexpr int kStage = 58368;
-constexpr int kSKg = kNS * kStage;   // Diag(gamma) K: [Kg_0 | Kg_1]
-constexpr int kSS = kSKg + 16384;    // S bf16, 128 x 64, MN-major
+constexpr int kSS = kNS * kStage;    // S bf16, 128 x 64, MN-major
 constexpr int kSUt = kSS + 16384;    // U~ bf16, 64 x 64, MN-major
 constexpr int kSO = kSUt + 8192;     // o of a chunk, bf16 (TMA store image)
 constexpr int kSBars = kSO + 8192;
-// mbarriers: full[3] (TMA), empty[3] (chain done with the stage), ready[3]
-// (helper done with the stage), hmma (helper MMAs), c1 (chain MMA group 1),
-// c2 (dS), accfree[2] (accumulator of a chunk parity read out)
-constexpr int kBFull = 0, kBEmpty = 3, kBReady = 6, kBHmma = 9, kBC1 = 10,
-              kBC2 = 11, kBAccFree = 12, kNumBars = 14;
+// mbarriers: full[3] (TMA), ready[3] (helper done with the stage), hmma[2]
+// (helper MMAs, by helper group), c1 (chain MMA group 1), c2 (dS),
+// accfree[2] (accumulator of a chunk parity read out)
+constexpr int kBFull = 0, kBReady = 3, kBHmma = 6, kBC1 = 8, kBC2 = 9,
+              kBAccFree = 10, kNumBars = 12;
 constexpr int kSMisc = kSBars + 8 * kNumBars;   // abort, TMEM slot, issued
 constexpr int kSSmem = kSMisc + 16 + 1024;
 static_assert(kSG + 256 <= kStage && kStage % 1024 == 0, "stage map");
@@ -469,15 +493,18 @@ static_assert(kSSmem <= 232448, "state-pass shared memory");
 constexpr uint32_t kStageTx = 4 * 8192 + 8192 + kRecBytes;
 
 // TMEM columns
-constexpr uint32_t kColH = 0;        // helper: [W; PTU Kg] (128 columns)
+constexpr uint32_t kColH = 0;        // helper group 0: [-W; -PTU Kg] (128)
 constexpr uint32_t kColAcc = 128;    // + 64 (c & 1): [U; PTU V], then [U~; O]
 constexpr uint32_t kColDS = 256;     // dS
+constexpr uint32_t kColH1 = 320;     // helper group 1: [-W; -PTU Kg] (128)
 constexpr uint32_t kTmemCols = 512;
 
-constexpr int kChainThreads = 128, kHelperThreads = 128;
-constexpr int kStateThreads = kChainThreads + kHelperThreads + 32;
-constexpr int kBarHelper = 1, kBarChain = 2, kBarChainLo = 3,
-              kBarChainHi = 4;
+// Two helper warpgroups take the chunks in turns (group c & 1), so each has
+// two chain periods for one chunk.
+constexpr int kChainThreads = 128, kHelperThreads = 128, kHelperGroups = 2;
+constexpr int kStateThreads = kChainThreads + kHelperGroups * kHelperThreads;
+constexpr int kBarChain = 2, kBarChainLo = 3, kBarChainHi = 4,
+              kBarHelper0 = 5;   // + helper group
 
 struct StateParams {
     const float* h0;
@@ -505,9 +532,20 @@ __device__ __forceinline__ void st_row(uint8_t* base, int row,
     }
 }
 
-__device__ __forceinline__ void unpack2(uint32_t u, float& lo, float& hi) {
-    lo = __uint_as_float(u << 16);
-    hi = __uint_as_float(u & 0xffff0000u);
+// Write 32 fp32 values as 16-byte chunks 4 hf .. 4 hf + 3 (the columns
+// 32 hf .. 32 hf + 31) of a 128-byte swizzled bf16 row.
+__device__ __forceinline__ void st_half_row(uint8_t* base, int row, int hf,
+                                            const float* x) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint4 v;
+        v.x = tc::pack_bf16x2(x[8 * j + 0], x[8 * j + 1]);
+        v.y = tc::pack_bf16x2(x[8 * j + 2], x[8 * j + 3]);
+        v.z = tc::pack_bf16x2(x[8 * j + 4], x[8 * j + 5]);
+        v.w = tc::pack_bf16x2(x[8 * j + 6], x[8 * j + 7]);
+        *reinterpret_cast<uint4*>(base + row * 128 +
+                                  (((4 * hf + j) ^ (row & 7)) << 4)) = v;
+    }
 }
 
 __device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t u) {
@@ -547,7 +585,7 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H;
     const int j0 = blockIdx.y * kNV;
-    const int T = p.T, nchunks = p.nchunks;
+    const int nchunks = p.nchunks;
 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) tc::mbar_init(&bars[i], 1);
@@ -577,56 +615,57 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (tid >= kChainThreads + kHelperThreads) {
-        // ========================================================= producer
-        if (tid == kChainThreads + kHelperThreads && !p.no_issue) {
-            tc::prefetch_tmap(&tm_q);
-            tc::prefetch_tmap(&tm_k);
-            tc::prefetch_tmap(&tm_v);
-            const uint8_t* rec0 = p.rec + (size_t)bh * nchunks * kRecBytes;
-            auto prefetch = [&](int c) {
-                const int t0 = c * kC;
-                tc::tma_prefetch_4d(&tm_k, 0, h, t0, b);
-                tc::tma_prefetch_4d(&tm_q, 0, h, t0, b);
-                tc::tma_prefetch_4d(&tm_k, 64, h, t0, b);
-                tc::tma_prefetch_4d(&tm_q, 64, h, t0, b);
-                tc::tma_prefetch_4d(&tm_v, j0, h, t0, b);
-                tc::bulk_prefetch_l2(rec0 + (size_t)c * kRecBytes, kRecBytes);
-            };
-            for (int c = kNS; c < 2 * kNS && c < nchunks; ++c) prefetch(c);
-            for (int c = 0; c < nchunks; ++c) {
-                const int s = c % kNS;
-                if (c >= kNS &&
-                    !tc::mbar_wait_or_abort(&bars[kBEmpty + s],
-                                            ((c / kNS) - 1) & 1, vabort,
-                                            p.wait_ns)) {
-                    *vabort = 1;
-                    break;
-                }
-                uint8_t* st = sm + s * kStage;
-                uint64_t* bar = &bars[kBFull + s];
-                const int t0 = c * kC;
-                tc::mbar_arrive_expect_tx(bar, kStageTx);
-                tc::tma_load_4d(st + kSK0, &tm_k, bar, 0, h, t0, b);
-                tc::tma_load_4d(st + kSQ0, &tm_q, bar, 0, h, t0, b);
-                tc::tma_load_4d(st + kSK1, &tm_k, bar, 64, h, t0, b);
-                tc::tma_load_4d(st + kSQ1, &tm_q, bar, 64, h, t0, b);
-                tc::tma_load_4d(st + kSV, &tm_v, bar, j0, h, t0, b);
-                tc::bulk_load(st + kSTU, rec0 + (size_t)c * kRecBytes,
-                              kRecBytes, bar);
-                *reinterpret_cast<volatile int*>(issued) = c + 1;
-                if (c + 2 * kNS < nchunks) prefetch(c + 2 * kNS);
-            }
-        }
-    } else if (tid >= kChainThreads) {
-        // =========================================================== helper
-        const int hl = tid - kChainThreads;          // TMEM lane
-        const uint32_t tl = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    // Loads of chunk c into its stage (TMA tiles of K, Q, V and the record
+    // of the pre-pass), issued by chain thread 0: the first kNS at the start,
+    // then chunk c + kNS right after the chain has finished chunk c with
+    // that stage.  Chunks two rings ahead are prefetched into L2.
+    const uint8_t* rec0 = p.rec + (size_t)bh * nchunks * kRecBytes;
+    auto prefetch = [&](int c) {
+        const int t0 = c * kC;
+        tc::tma_prefetch_4d(&tm_k, 0, h, t0, b);
+        tc::tma_prefetch_4d(&tm_q, 0, h, t0, b);
+        tc::tma_prefetch_4d(&tm_k, 64, h, t0, b);
+        tc::tma_prefetch_4d(&tm_q, 64, h, t0, b);
+        tc::tma_prefetch_4d(&tm_v, j0, h, t0, b);
+        tc::bulk_prefetch_l2(rec0 + (size_t)c * kRecBytes, kRecBytes);
+    };
+    auto issue_loads = [&](int c) {
+        const int s = c % kNS;
+        uint8_t* st = sm + s * kStage;
+        uint64_t* bar = &bars[kBFull + s];
+        const int t0 = c * kC;
+        tc::mbar_arrive_expect_tx(bar, kStageTx);
+        tc::tma_load_4d(st + kSK0, &tm_k, bar, 0, h, t0, b);
+        tc::tma_load_4d(st + kSQ0, &tm_q, bar, 0, h, t0, b);
+        tc::tma_load_4d(st + kSK1, &tm_k, bar, 64, h, t0, b);
+        tc::tma_load_4d(st + kSQ1, &tm_q, bar, 64, h, t0, b);
+        tc::tma_load_4d(st + kSV, &tm_v, bar, j0, h, t0, b);
+        tc::bulk_load(st + kSTU, rec0 + (size_t)c * kRecBytes, kRecBytes,
+                      bar);
+        *reinterpret_cast<volatile int*>(issued) = c + 1;
+        if (c + 2 * kNS < nchunks) prefetch(c + 2 * kNS);
+    };
+    if (tid == 0 && !p.no_issue) {
+        tc::prefetch_tmap(&tm_q);
+        tc::prefetch_tmap(&tm_k);
+        tc::prefetch_tmap(&tm_v);
+        for (int c = kNS; c < 2 * kNS && c < nchunks; ++c) prefetch(c);
+        for (int c = 0; c < kNS && c < nchunks; ++c) issue_loads(c);
+    }
+
+    if (tid >= kChainThreads) {
+        // ========================================================== helpers
+        const int grp = (tid - kChainThreads) / kHelperThreads;
+        const int hl = (tid - kChainThreads) % kHelperThreads;  // TMEM lane
+        const int bar_id = kBarHelper0 + grp;
+        const uint32_t colH = grp ? kColH1 : kColH;
+        uint64_t* hbar = &bars[kBHmma + grp];
+        const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         // [-W; -PTU Kg]: the negation rides on the instruction (negate A)
         constexpr uint32_t idA = tc::idesc_bf16(128, 128, false, true, true);
         constexpr uint32_t idB = tc::idesc_bf16(128, kNV, false, true);
-        int committed = -1;
-        for (int c = 0; c < nchunks; ++c) {
+        int committed = -1, nmma = 0;
+        for (int c = grp; c < nchunks; c += kHelperGroups) {
             const int s = c % kNS;
             uint8_t* st = sm + s * kStage;
             const uint32_t sst = sbase + s * kStage;
@@ -634,40 +673,44 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
                                              vabort, p.wait_ns);
             if (ok && c >= 2)   // accumulator of this parity read out
                 ok = tc::mbar_wait_or_abort(&bars[kBAccFree + (c & 1)],
-                                            ((c - 2) >> 1) & 1, vabort, p.wait_ns);
-            if (tc::named_bar_or(kBarHelper, kHelperThreads, !ok)) {
+                                            ((c - 2) >> 1) & 1, vabort,
+                                            p.wait_ns);
+            if (tc::named_bar_or(bar_id, kHelperThreads, !ok)) {
                 *vabort = 1;
                 break;
             }
-            // Diag(gamma) K into Kg; Diag(Gamma_C) K kept in registers
+            // Diag(gamma) K in place of K (the operand of the next MMAs);
+            // Diag(Gamma_C) K kept in registers until TU, PTU are read.
+            // (16-byte chunk (j + r) mod 8 at step j: the 8 rows a quarter
+            // warp touches at once sit in 8 different bank groups; a chunk
+            // keeps its swizzled position, the scaling is per row)
             const float* g2 = reinterpret_cast<const float*>(st + kSG);
             const int r = hl & 63, hh = hl >> 6;
             const __nv_bfloat162 gam = __float2bfloat162_rn(tc::ex2(g2[r]));
             const __nv_bfloat162 gamC =
                 __float2bfloat162_rn(tc::ex2(g2[kC - 1] - g2[r]));
-            // (16-byte chunk (j + r) mod 8 at step j: the 8 rows a quarter
-            // warp touches at once sit in 8 different bank groups; a chunk
-            // keeps its swizzled position, the scaling is per row)
+            uint4 kG[8];
             {
-                const uint8_t* krow = st + (hh ? kSK1 : kSK0) + r * 128;
-                uint8_t* grow = sm + kSKg + hh * 8192 + r * 128;
+                uint8_t* krow = st + (hh ? kSK1 : kSK0) + r * 128;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int cj = ((j + r) & 7) << 4;
                     const uint4 u = *reinterpret_cast<const uint4*>(krow + cj);
-                    *reinterpret_cast<uint4*>(grow + cj) = scale8(u, gam);
+                    *reinterpret_cast<uint4*>(krow + cj) = scale8(u, gam);
+                    kG[j] = scale8(u, gamC);
                 }
             }
             tc::fence_proxy_async_smem();
-            tc::named_bar_sync(kBarHelper, kHelperThreads);
+            tc::named_bar_sync(bar_id, kHelperThreads);
             if (hl == 0) {
                 tc::tc_fence_after();
-                // [-W; -PTU Kg] = -[TU; PTU] Kg    (M 128, N 128, K 64)
+                // [-W; -PTU Kg] = -[TU; PTU] Kg    (M 128, N 128, K 64; the
+                // two 64-feature halves of Kg are 16 KB apart)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tmem + kColH, desc_k(sst + kSTU + ks * 32),
-                                 desc_mn(sbase + kSKg + ks * 2048, 8192), idA,
-                                 ks > 0);
+                    tc::mma_bf16(tmem + colH, desc_k(sst + kSTU + ks * 32),
+                                 desc_mn(sst + kSK0 + ks * 2048, kSK1 - kSK0),
+                                 idA, ks > 0);
                 // [U; PTU V] = [TU; PTU] V       (M 128, N 64, K 64)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
@@ -675,38 +718,33 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
                                  desc_k(sst + kSTU + ks * 32),
                                  desc_mn(sst + kSV + ks * 2048, 0), idB,
                                  ks > 0);
-                tc::mma_commit(&bars[kBHmma]);
+                tc::mma_commit(hbar);
             }
             __syncwarp();   // the issuing lane rejoins before the waits
-            committed = c;
-            if (tc::named_bar_or(kBarHelper, kHelperThreads,
-                                 !tc::mbar_wait_or_abort(&bars[kBHmma], c & 1,
+            committed = nmma++;
+            if (tc::named_bar_or(bar_id, kHelperThreads,
+                                 !tc::mbar_wait_or_abort(hbar, committed & 1,
                                                          vabort, p.wait_ns))) {
                 *vabort = 1;
                 break;
             }
             tc::tc_fence_after();
+            {   // Diag(Gamma_C) K over [TU; PTU] (read by the finished MMAs)
+                uint8_t* grow = st + kSTU + hh * 8192 + r * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<uint4*>(grow + (((j + r) & 7) << 4)) =
+                        kG[j];
+            }
             if (hl < kC) {
-                // Diag(Gamma_C) K row hl over [TU; PTU] (read by the
-                // finished MMAs), then -W row hl over K (both halves)
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const uint8_t* krow = st + (half ? kSK1 : kSK0) + hl * 128;
-                    uint8_t* grow = st + kSTU + half * 8192 + hl * 128;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int cj = ((j + hl) & 7) << 4;
-                        *reinterpret_cast<uint4*>(grow + cj) = scale8(
-                            *reinterpret_cast<const uint4*>(krow + cj), gamC);
-                    }
-                }
+                // -W row hl over Kg (both halves; read by the finished MMA)
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    float x[64];
-                    tc::tmem_ld32(tl + kColH + 64 * half, x);
-                    tc::tmem_ld32(tl + kColH + 64 * half + 32, x + 32);
+                for (int q4 = 0; q4 < 4; ++q4) {   // 32 columns at a time
+                    float x[32];
+                    tc::tmem_ld32(tl + colH + 32 * q4, x);
                     tc::tmem_ld_wait();
-                    st_row(st + (half ? kSK1 : kSK0), hl, x);
+                    st_half_row(st + ((q4 >> 1) ? kSK1 : kSK0), hl, q4 & 1,
+                                x);
                 }
             } else {
                 // Q' row = gamma_r Q_r + (-PTU Kg)_r over Q (in place; packed
@@ -715,16 +753,15 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const __nv_bfloat162 gq =
                     __float2bfloat162_rn(tc::ex2(g2[rq]));
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    float x[64];
-                    tc::tmem_ld32(tl + kColH + 64 * half, x);
-                    tc::tmem_ld32(tl + kColH + 64 * half + 32, x + 32);
+                for (int q4 = 0; q4 < 4; ++q4) {   // 32 columns at a time
+                    float x[32];
+                    tc::tmem_ld32(tl + colH + 32 * q4, x);
                     tc::tmem_ld_wait();
-                    uint8_t* qrow = st + (half ? kSQ1 : kSQ0) + rq * 128;
+                    uint8_t* qrow = st + ((q4 >> 1) ? kSQ1 : kSQ0) + rq * 128;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int j = 0; j < 4; ++j) {
                         uint4* pq = reinterpret_cast<uint4*>(
-                            qrow + ((j ^ (rq & 7)) << 4));
+                            qrow + (((4 * (q4 & 1) + j) ^ (rq & 7)) << 4));
                         uint4 u = *pq;
                         const float* xj = x + 8 * j;
                         u.x = as_u32(__hfma2(gq, as_bf2(u.x), as_bf2(
@@ -741,11 +778,11 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
             tc::fence_proxy_async_smem();
             tc::tc_fence_before();
-            tc::named_bar_sync(kBarHelper, kHelperThreads);
+            tc::named_bar_sync(bar_id, kHelperThreads);
             if (hl == 0) tc::mbar_arrive(&bars[kBReady + s]);
         }
         if (*vabort && hl == 0 && committed >= 0)   // drain own MMAs
-            tc::mbar_wait(&bars[kBHmma], committed & 1, 100000000ull);
+            tc::mbar_wait(hbar, committed & 1, 100000000ull);
     } else {
         // ============================================================ chain
         const int row = tid;                      // TMEM lane
@@ -793,11 +830,13 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
                 // U~ row (token) to shared memory, then dS = KG^T U~
                 if (ok) {
                     tc::tc_fence_after();
-                    float x[64];
-                    tc::tmem_ld32(tl + (acc - tmem), x);
-                    tc::tmem_ld32(tl + (acc - tmem) + 32, x + 32);
-                    tc::tmem_ld_wait();
-                    st_row(sm + kSUt, row, x);
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        float x[32];
+                        tc::tmem_ld32(tl + (acc - tmem) + 32 * hf, x);
+                        tc::tmem_ld_wait();
+                        st_half_row(sm + kSUt, row, hf, x);
+                    }
                     tc::fence_proxy_async_smem();
                 }
                 tc::tc_fence_before();
@@ -820,12 +859,14 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
                 // the image is free once the previous store has read it
                 if (tid == kC) tc::tma_store_wait_read<0>();
                 tc::tc_fence_after();
-                float x[64];
-                tc::tmem_ld32(tl + (acc - tmem), x);
-                tc::tmem_ld32(tl + (acc - tmem) + 32, x + 32);
-                tc::tmem_ld_wait();
                 tc::named_bar_sync(kBarChainHi, 64);
-                st_row(sm + kSO, row - kC, x);
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    float x[32];
+                    tc::tmem_ld32(tl + (acc - tmem) + 32 * hf, x);
+                    tc::tmem_ld_wait();
+                    st_half_row(sm + kSO, row - kC, hf, x);
+                }
                 tc::fence_proxy_async_smem();
                 tc::named_bar_sync(kBarChainHi, 64);
                 if (tid == kC) {
@@ -841,20 +882,23 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
             tc::tc_fence_after();
             {   // S <- gamma_C S + dS
                 const float gC = tc::ex2(g2[kC - 1]);
-                float x[64];
-                tc::tmem_ld32(tl + kColDS, x);
-                tc::tmem_ld32(tl + kColDS + 32, x + 32);
-                tc::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < kNV; ++j) S[j] = fmaf(gC, S[j], x[j]);
-                st_row(sm + kSS, row, S);
+                for (int hf = 0; hf < 2; ++hf) {
+                    float x[32];
+                    tc::tmem_ld32(tl + kColDS + 32 * hf, x);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        S[32 * hf + j] = fmaf(gC, S[32 * hf + j], x[j]);
+                    st_half_row(sm + kSS, row, hf, S + 32 * hf);
+                }
             }
             tc::fence_proxy_async_smem();
             tc::tc_fence_before();
             tc::named_bar_sync(kBarChain, kChainThreads);
             if (tid == 0) {
-                tc::mbar_arrive(&bars[kBEmpty + s]);
                 tc::mbar_arrive(&bars[kBAccFree + (c & 1)]);
+                if (c + kNS < nchunks) issue_loads(c + kNS);   // stage free
             }
         }
         if (failed) {

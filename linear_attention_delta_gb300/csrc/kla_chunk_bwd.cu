@@ -34,6 +34,7 @@
 
 #include "kla_internal.cuh"
 #include "simt_blocks.cuh"
+#include "tc_primitives.cuh"
 
 namespace kla {
 namespace {
@@ -1041,6 +1042,544 @@ kla_bwd_grad_kernel(BwdArgs a) {
     }
 }
 
+// ------------------------------------------ gradients, tensor cores (bf16)
+// The same per-chunk gradients for bf16 inputs with dk = 128, C = 64, every
+// product on the tensor cores: warp-level m16n8k16 MMAs with bf16 operands
+// (rounded from the fp32 shared-memory tiles as the fragments are loaded)
+// and fp32 accumulation.  The elementwise and row-reduction steps are those
+// of kla_bwd_grad_kernel.  Eight warps; a product's 16 x 8 output tiles are
+// dealt out to them, dq and dk stay in registers (warp w: rows 16 (w & 3)..,
+// columns 64 (w >> 2)..).
+
+// A fragment of the 16 x 16 block starting at `p`, element (m, k) at
+// p[m * sm + k * sk], optionally each row m scaled by rs[m] and/or masked
+// to the lower (k <= m, tri = 1) or upper (k >= m, tri = 2) triangle.
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const float* p,
+                                       int sm, int sk, int lane,
+                                       const float* rs = nullptr,
+                                       int tri = 0) {
+    const int g = lane >> 2, t = lane & 3;
+    float v[8];
+    const int ms[2] = {g, g + 8};
+    const int ks[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+#pragma unroll
+    for (int hm = 0; hm < 2; ++hm)
+#pragma unroll
+        for (int hk = 0; hk < 2; ++hk)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int m = ms[hm], k = ks[2 * hk + e];
+                float x = p[m * sm + k * sk];
+                if (tri == 1 && k > m) x = 0.f;
+                if (tri == 2 && k < m) x = 0.f;
+                if (rs) x *= rs[m];
+                v[4 * hk + 2 * hm + e] = x;
+            }
+    a[0] = tc::pack_bf16x2(v[0], v[1]);   // (g, 2t..2t+1)
+    a[1] = tc::pack_bf16x2(v[2], v[3]);   // (g+8, 2t..)
+    a[2] = tc::pack_bf16x2(v[4], v[5]);   // (g, 2t+8..)
+    a[3] = tc::pack_bf16x2(v[6], v[7]);   // (g+8, 2t+8..)
+}
+
+// B fragment of the 16 x 8 block starting at `p`, element (k, n) at
+// p[k * sk + n * sn].
+__device__ __forceinline__ void frag_b(uint32_t& b0, uint32_t& b1,
+                                       const float* p, int sk, int sn,
+                                       int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    b0 = tc::pack_bf16x2(p[(2 * t) * sk + g * sn], p[(2 * t + 1) * sk + g * sn]);
+    b1 = tc::pack_bf16x2(p[(2 * t + 8) * sk + g * sn],
+                         p[(2 * t + 9) * sk + g * sn]);
+}
+
+// acc += A B for one k-step (A 16 x 16, B 16 x 8).
+__device__ __forceinline__ void mma_step(float (&acc)[4],
+                                         const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    tc::mma_m16n8k16(acc, a, b0, b1);
+}
+
+// Lower 16 x 8 tiles (mt, nt) of a 64 x 64 matrix (8 nt <= 16 mt + 15):
+// tile index 0 .. 19 -> (mt, nt).
+__device__ __forceinline__ void lower_tile(int idx, int& mt, int& nt) {
+    mt = idx < 2 ? 0 : idx < 6 ? 1 : idx < 12 ? 2 : 3;
+    const int first = mt == 0 ? 0 : mt == 1 ? 2 : mt == 2 ? 6 : 12;
+    nt = idx - first;
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(kBwdThreads)
+kla_bwd_grad_mma_kernel(BwdArgs a) {
+    constexpr int DK = 128, DVT = 32;
+    using L = GradSmem<DK, DVT>;
+    constexpr int LDK = L::LDK, LDV = L::LDV, LDC = L::LDC;
+    extern __shared__ float sm[];
+    float* Qs = sm + L::Q;
+    float* Ks = sm + L::K;
+    float* As = sm + L::A;
+    float* Ps = sm + L::P;
+    float* dP = sm + L::DP;
+    float* dA = sm + L::DA;
+    float* St = sm + L::ST;
+    float* dSt = sm + L::DST;
+    float* Xs = sm + L::X;
+    float* Ds = sm + L::DO;
+    float* Us = sm + L::U;
+    float* Ws = sm + L::W;
+    float* KS = sm + L::KS;
+    float* gs = sm + L::G;
+    float* bs = sm + L::BETA;
+    float* gam = sm + L::GAM;
+    float* lam = sm + L::LAM;
+    float* nrm = sm + L::NRM;
+    float* db = sm + L::DB;
+    float* dgam = sm + L::DGAM;
+    float* dlam = sm + L::DLAM;
+    float* dg = sm + L::DG;
+    float* dgc = sm + L::DGC;
+    float* Tm = sm + L::TM;
+
+    const int C = a.C, T = a.T, H = a.H, dv = a.dv;   // C == 64
+    const int nch = (T + C - 1) / C;
+    const long blk = blockIdx.x;
+    const int bh = (int)(blk / nch), ch = (int)(blk % nch);
+    const int b = bh / H, h = bh % H;
+    const int t0 = ch * C;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const float* Sg = a.ckpt + ((size_t)bh * nch + ch) * DK * dv;
+    const float* dSg = a.dsck + ((size_t)bh * nch + ch) * DK * dv;
+
+    {   // q, k rows: 16-byte loads (8 bf16), all issued before the stores
+        uint4 qv[4], kv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = tid + u * kBwdThreads;   // 64 rows x 16 chunks
+            const int r = idx >> 4, c8 = idx & 15;
+            const int t = t0 + r;
+            qv[u] = kv[u] = make_uint4(0, 0, 0, 0);
+            if (t < T) {
+                const size_t off = (((size_t)b * T + t) * H + h) * DK + 8 * c8;
+                qv[u] = *reinterpret_cast<const uint4*>(
+                    static_cast<const IO*>(a.q) + off);
+                kv[u] = *reinterpret_cast<const uint4*>(
+                    static_cast<const IO*>(a.k) + off);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = tid + u * kBwdThreads;
+            const int r = idx >> 4, c8 = idx & 15;
+            const uint32_t qw[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+            const uint32_t kw[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                Qs[r * LDK + 8 * c8 + 2 * e] = __uint_as_float(qw[e] << 16);
+                Qs[r * LDK + 8 * c8 + 2 * e + 1] =
+                    __uint_as_float(qw[e] & 0xffff0000u);
+                Ks[r * LDK + 8 * c8 + 2 * e] = __uint_as_float(kw[e] << 16);
+                Ks[r * LDK + 8 * c8 + 2 * e + 1] =
+                    __uint_as_float(kw[e] & 0xffff0000u);
+            }
+        }
+        if (tid < C) {
+            const int t = t0 + tid;
+            const size_t off = ((size_t)b * T + t) * H + h;
+            gs[tid] = t < T ? a.log_alpha[off] : 0.f;
+            bs[tid] = t < T ? a.eta[off] : 0.f;
+        }
+    }
+    for (int idx = tid; idx < C * LDC; idx += kBwdThreads) {
+        dP[idx] = 0.f;
+        dA[idx] = 0.f;
+    }
+    if (tid < kBwdMaxC) {
+        db[tid] = 0.f;
+        dgam[tid] = 0.f;
+        dlam[tid] = 0.f;
+    }
+    if (tid == 0) dgc[0] = 0.f;
+    __syncthreads();
+    chunk_gates<DK>(a, Ks, LDK, gs, bs, gam, lam, nrm);
+    build_a_p<DK, kBwdThreads>(C, Qs, Ks, Ks, LDK, gs, bs, As, Ps, LDC);
+    __syncthreads();
+    invert_unit_lower<kBwdThreads>(As, Tm, C, LDC);   // lower part of Tm
+
+    // dq, dk of this warp's rows 16 mo .. and columns 64 co .. (fragments)
+    const int mo = warp & 3, co = 64 * (warp >> 2);
+    float dq[8][4], dk[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dq[nt][e] = dk[nt][e] = 0.f;
+    // row scales -gamma_r beta_r in dg (free until the per-row step)
+    if (tid < C) dg[tid] = -gam[tid] * bs[tid];
+    __syncthreads();
+    const float* sgd = gam + 16 * mo;   // row scales of this warp's rows
+    const float* sgb = dg + 16 * mo;
+    const float* sl = lam + 16 * mo;
+
+    for (int j0 = 0; j0 < dv; j0 += DVT) {
+        {   // S, dS' (128 x 32 fp32: 4 float4 each per thread), V, dO
+            // (64 x 32 bf16: one 16-byte load each): every load issued
+            // before the shared-memory stores
+            float4 sv[4], dsv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int idx = tid + u * kBwdThreads;   // 128 rows x 8
+                const int c = idx >> 3, j4 = idx & 7;
+                sv[u] = *reinterpret_cast<const float4*>(
+                    Sg + (size_t)c * dv + j0 + 4 * j4);
+                dsv[u] = *reinterpret_cast<const float4*>(
+                    dSg + (size_t)c * dv + j0 + 4 * j4);
+            }
+            const int r = tid >> 2, j8 = tid & 3;        // 64 rows x 4
+            const int t = t0 + r;
+            uint4 vv = make_uint4(0, 0, 0, 0), dov = make_uint4(0, 0, 0, 0);
+            if (t < T) {
+                const size_t off =
+                    (((size_t)b * T + t) * H + h) * dv + j0 + 8 * j8;
+                vv = *reinterpret_cast<const uint4*>(
+                    static_cast<const IO*>(a.v) + off);
+                dov = *reinterpret_cast<const uint4*>(
+                    static_cast<const IO*>(a.dout) + off);
+            }
+            float sdot = 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int idx = tid + u * kBwdThreads;
+                const int c = idx >> 3, j = 4 * (idx & 7);
+                const float s4[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
+                const float d4[4] = {dsv[u].x, dsv[u].y, dsv[u].z, dsv[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    St[c * LDV + j + e] = s4[e];
+                    dSt[c * LDV + j + e] = d4[e];
+                    sdot = fmaf(s4[e], d4[e], sdot);
+                }
+            }
+            atomicAdd(dgc, sdot);
+            const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+            const uint32_t dw[4] = {dov.x, dov.y, dov.z, dov.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                Xs[r * LDV + 8 * j8 + 2 * e] = __uint_as_float(vw[e] << 16);
+                Xs[r * LDV + 8 * j8 + 2 * e + 1] =
+                    __uint_as_float(vw[e] & 0xffff0000u);
+                Ds[r * LDV + 8 * j8 + 2 * e] = __uint_as_float(dw[e] << 16);
+                Ds[r * LDV + 8 * j8 + 2 * e + 1] =
+                    __uint_as_float(dw[e] & 0xffff0000u);
+            }
+        }
+        __syncthreads();
+
+        // K S, Q S: X = V - Diag(gamma) K S, F = Diag(beta) X (into W),
+        // dgamma += dO . Q S
+        for (int tile = warp; tile < 16; tile += 8) {
+            const int mt = tile >> 2, nt = tile & 3;
+            float ks[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < DK / 16; ++kk) {
+                uint32_t ak[4], aq[4], b0, b1;
+                frag_a(ak, Ks + 16 * mt * LDK + 16 * kk, LDK, 1, lane);
+                frag_a(aq, Qs + 16 * mt * LDK + 16 * kk, LDK, 1, lane);
+                frag_b(b0, b1, St + 16 * kk * LDV + 8 * nt, LDV, 1, lane);
+                mma_step(ks, ak, b0, b1);
+                mma_step(qs, aq, b0, b1);
+            }
+#pragma unroll
+            for (int hm = 0; hm < 2; ++hm) {
+                const int r = 16 * mt + g8 + 8 * hm;
+                float dgp = 0.f;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = 8 * nt + 2 * t4 + e;
+                    const float v = ks[2 * hm + e];
+                    KS[r * LDV + j] = v;
+                    const float x = fmaf(-gam[r], v, Xs[r * LDV + j]);
+                    Xs[r * LDV + j] = x;
+                    Ws[r * LDV + j] = bs[r] * x;
+                    dgp = fmaf(Ds[r * LDV + j], qs[2 * hm + e], dgp);
+                }
+                atomicAdd(&dgam[r], dgp);
+            }
+        }
+        __syncthreads();
+
+        // U~ = T F (T lower triangular)
+        for (int tile = warp; tile < 16; tile += 8) {
+            const int mt = tile >> 2, nt = tile & 3;
+            float u[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int kk = 0; kk <= mt; ++kk) {
+                uint32_t at[4], b0, b1;
+                frag_a(at, Tm + 16 * mt * LDC + 16 * kk, LDC, 1, lane, nullptr,
+                       kk == mt ? 1 : 0);
+                frag_b(b0, b1, Ws + 16 * kk * LDV + 8 * nt, LDV, 1, lane);
+                mma_step(u, at, b0, b1);
+            }
+#pragma unroll
+            for (int hm = 0; hm < 2; ++hm)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    Us[(16 * mt + g8 + 8 * hm) * LDV + 8 * nt + 2 * t4 + e] =
+                        u[2 * hm + e];
+        }
+        __syncthreads();
+
+        // dU~ = P^T dO + Diag(lambda) K dS' (into W); dlambda_r = (K dS')_r.U~_r
+        for (int tile = warp; tile < 16; tile += 8) {
+            const int mt = tile >> 2, nt = tile & 3;
+            float kd[4] = {0.f, 0.f, 0.f, 0.f}, pd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < DK / 16; ++kk) {
+                uint32_t ak[4], b0, b1;
+                frag_a(ak, Ks + 16 * mt * LDK + 16 * kk, LDK, 1, lane);
+                frag_b(b0, b1, dSt + 16 * kk * LDV + 8 * nt, LDV, 1, lane);
+                mma_step(kd, ak, b0, b1);
+            }
+            for (int kk = mt; kk < 4; ++kk) {   // P^T(r, i) = P(i, r), i >= r
+                uint32_t ap[4], b0, b1;
+                frag_a(ap, Ps + 16 * kk * LDC + 16 * mt, 1, LDC, lane);
+                frag_b(b0, b1, Ds + 16 * kk * LDV + 8 * nt, LDV, 1, lane);
+                mma_step(pd, ap, b0, b1);
+            }
+#pragma unroll
+            for (int hm = 0; hm < 2; ++hm) {
+                const int r = 16 * mt + g8 + 8 * hm;
+                float dlp = 0.f;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = 8 * nt + 2 * t4 + e;
+                    Ws[r * LDV + j] = fmaf(lam[r], kd[2 * hm + e], pd[2 * hm + e]);
+                    dlp = fmaf(kd[2 * hm + e], Us[r * LDV + j], dlp);
+                }
+                atomicAdd(&dlam[r], dlp);
+            }
+        }
+        __syncthreads();
+
+        // dF = T^T dU~ (into the K S slots, once read); dV = Diag(beta) dF;
+        // dbeta from F = Diag(beta) X; dgamma from X
+        for (int tile = warp; tile < 16; tile += 8) {
+            const int mt = tile >> 2, nt = tile & 3;
+            float df[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int kk = mt; kk < 4; ++kk) {   // T^T(r, i) = T(i, r), i >= r
+                uint32_t at[4], b0, b1;
+                frag_a(at, Tm + 16 * kk * LDC + 16 * mt, 1, LDC, lane, nullptr,
+                       kk == mt ? 2 : 0);
+                frag_b(b0, b1, Ws + 16 * kk * LDV + 8 * nt, LDV, 1, lane);
+                mma_step(df, at, b0, b1);
+            }
+#pragma unroll
+            for (int hm = 0; hm < 2; ++hm) {
+                const int r = 16 * mt + g8 + 8 * hm;
+                const int t = t0 + r;
+                float dbp = 0.f, dgp = 0.f;
+                float dx2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = 8 * nt + 2 * t4 + e;
+                    const float dfv = df[2 * hm + e];
+                    const float dx = bs[r] * dfv;
+                    dx2[e] = dx;
+                    dbp = fmaf(dfv, Xs[r * LDV + j], dbp);
+                    dgp = fmaf(-dx, KS[r * LDV + j], dgp);
+                    KS[r * LDV + j] = dfv;
+                }
+                if (t < T) {
+                    const size_t off = (((size_t)b * T + t) * H + h) * dv +
+                                       j0 + 8 * nt + 2 * t4;
+                    static_cast<IO*>(a.dv_)[off] = from_f32<IO>(dx2[0]);
+                    static_cast<IO*>(a.dv_)[off + 1] = from_f32<IO>(dx2[1]);
+                }
+                atomicAdd(&db[r], dbp);
+                atomicAdd(&dgam[r], dgp);
+            }
+        }
+        __syncthreads();
+
+        // dP += dO U~^T (i <= r), dA -= dF U~^T (i < r): lower tiles
+        for (int idx = warp; idx < 20; idx += 8) {
+            int mt, nt;
+            lower_tile(idx, mt, nt);
+            float ap[4] = {0.f, 0.f, 0.f, 0.f}, aa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < DVT / 16; ++kk) {
+                uint32_t ad[4], af[4], b0, b1;
+                frag_a(ad, Ds + 16 * mt * LDV + 16 * kk, LDV, 1, lane);
+                frag_a(af, KS + 16 * mt * LDV + 16 * kk, LDV, 1, lane);
+                // B(j, i) = U~(i, j)
+                frag_b(b0, b1, Us + 8 * nt * LDV + 16 * kk, 1, LDV, lane);
+                mma_step(ap, ad, b0, b1);
+                mma_step(aa, af, b0, b1);
+            }
+#pragma unroll
+            for (int hm = 0; hm < 2; ++hm)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = 16 * mt + g8 + 8 * hm;
+                    const int i = 8 * nt + 2 * t4 + e;
+                    if (i <= r) dP[r * LDC + i] += ap[2 * hm + e];
+                    if (i < r) dA[r * LDC + i] -= aa[2 * hm + e];
+                }
+        }
+        // dq += Diag(gamma) dO S^T; dk += Diag(lambda) U~ dS'^T
+        //                               - Diag(gamma beta) dF S^T
+#pragma unroll
+        for (int kk = 0; kk < DVT / 16; ++kk) {
+            uint32_t ad[4], au[4], af[4];
+            frag_a(ad, Ds + 16 * mo * LDV + 16 * kk, LDV, 1, lane, sgd);
+            frag_a(au, Us + 16 * mo * LDV + 16 * kk, LDV, 1, lane, sl);
+            frag_a(af, KS + 16 * mo * LDV + 16 * kk, LDV, 1, lane, sgb);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                const int c0 = co + 8 * nt;
+                uint32_t bs0, bs1, bd0, bd1;
+                // B(j, c) = S(c, j)
+                frag_b(bs0, bs1, St + c0 * LDV + 16 * kk, 1, LDV, lane);
+                frag_b(bd0, bd1, dSt + c0 * LDV + 16 * kk, 1, LDV, lane);
+                mma_step(dq[nt], ad, bs0, bs1);
+                mma_step(dk[nt], au, bd0, bd1);
+                mma_step(dk[nt], af, bs0, bs1);
+            }
+        }
+        __syncthreads();
+    }
+
+    // dGamma o Gamma (into A), Gamma o dP (into dP), D (into dA), and the
+    // A-part of dbeta, from Q K^T and K K^T of the lower tiles
+    for (int idx = warp; idx < 20; idx += 8) {
+        int mt, nt;
+        lower_tile(idx, mt, nt);
+        float qk[4] = {0.f, 0.f, 0.f, 0.f}, kk4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < DK / 16; ++kk) {
+            uint32_t aq[4], ak[4], b0, b1;
+            frag_a(aq, Qs + 16 * mt * LDK + 16 * kk, LDK, 1, lane);
+            frag_a(ak, Ks + 16 * mt * LDK + 16 * kk, LDK, 1, lane);
+            frag_b(b0, b1, Ks + 8 * nt * LDK + 16 * kk, 1, LDK, lane);   // K^T
+            mma_step(qk, aq, b0, b1);
+            mma_step(kk4, ak, b0, b1);
+        }
+#pragma unroll
+        for (int hm = 0; hm < 2; ++hm) {
+            const int r = 16 * mt + g8 + 8 * hm;
+            float dbp = 0.f;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int i = 8 * nt + 2 * t4 + e;
+                float dgg = 0.f, dpt = 0.f, dd = 0.f;
+                if (i <= r) {
+                    const float gmm = expf(gs[r] - gs[i]);
+                    const float dpv = dP[r * LDC + i];
+                    float dgm = dpv * qk[2 * hm + e];
+                    dpt = gmm * dpv;
+                    if (i < r) {
+                        const float dav = dA[r * LDC + i];
+                        dgm = fmaf(dav * bs[r], kk4[2 * hm + e], dgm);
+                        dd = bs[r] * gmm * dav;
+                        dbp = fmaf(dav * gmm, kk4[2 * hm + e], dbp);
+                    }
+                    dgg = dgm * gmm;
+                }
+                As[r * LDC + i] = dgg;
+                dP[r * LDC + i] = dpt;
+                dA[r * LDC + i] = dd;
+            }
+            atomicAdd(&db[r], dbp);
+        }
+    }
+    __syncthreads();
+
+    // per row: dg, deta, dn (dn replaces dbeta in db)
+    if (tid < C) {
+        const int r = tid;
+        float gsum = dgam[r] * gam[r] - dlam[r] * lam[r];
+        for (int i = 0; i <= r; ++i) gsum += As[r * LDC + i];
+        for (int rr = r; rr < C; ++rr) gsum -= As[rr * LDC + r];
+        if (r == C - 1) {
+            for (int t = 0; t < C; ++t) gsum = fmaf(dlam[t], lam[t], gsum);
+            gsum = fmaf(dgc[0], gam[C - 1], gsum);
+        }
+        dg[r] = gsum;
+        const float dbeta = db[r];
+        float deta, dn = 0.f;
+        if (a.gdn) {
+            deta = dbeta;
+        } else {
+            const float denom = nrm[r] + a.eps;
+            deta = denom == 0.f ? 0.f : dbeta / denom;
+            if (denom != 0.f) dn = -dbeta * bs[r] / denom;
+        }
+        const int t = t0 + r;
+        if (t < T) a.deta[((size_t)b * T + t) * H + h] = deta;
+        db[r] = dn;
+    }
+    __syncthreads();
+    if (tid < C) {   // dlog_alpha_j = sum_{r >= j} dg_r
+        float acc = 0.f;
+        for (int r = tid; r < C; ++r) acc += dg[r];
+        const int t = t0 + tid;
+        if (t < T) a.dlog_alpha[((size_t)b * T + t) * H + h] = acc;
+    }
+
+    // dq += (Gamma o dP) K;  dk += (Gamma o dP)^T Q + (D + D^T) K
+    for (int kk = 0; kk < 4; ++kk) {
+        uint32_t ap[4], apt[4], ad[4];
+        const bool low = kk <= mo, up = kk >= mo;
+        if (low) frag_a(ap, dP + 16 * mo * LDC + 16 * kk, LDC, 1, lane);
+        if (up) frag_a(apt, dP + 16 * kk * LDC + 16 * mo, 1, LDC, lane);
+        {   // (D + D^T)(r, i) = D(r, i) + D(i, r)
+            const int g = lane >> 2, t = lane & 3;
+            float v[8];
+            const int ms[2] = {g, g + 8};
+            const int ks[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+#pragma unroll
+            for (int hm = 0; hm < 2; ++hm)
+#pragma unroll
+                for (int hk = 0; hk < 2; ++hk)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int r = 16 * mo + ms[hm], i = 16 * kk + ks[2 * hk + e];
+                        v[4 * hk + 2 * hm + e] = dA[r * LDC + i] + dA[i * LDC + r];
+                    }
+            ad[0] = tc::pack_bf16x2(v[0], v[1]);
+            ad[1] = tc::pack_bf16x2(v[2], v[3]);
+            ad[2] = tc::pack_bf16x2(v[4], v[5]);
+            ad[3] = tc::pack_bf16x2(v[6], v[7]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            const int c0 = co + 8 * nt;
+            uint32_t bk0, bk1, bq0, bq1;
+            frag_b(bk0, bk1, Ks + 16 * kk * LDK + c0, LDK, 1, lane);
+            frag_b(bq0, bq1, Qs + 16 * kk * LDK + c0, LDK, 1, lane);
+            if (low) mma_step(dq[nt], ap, bk0, bk1);
+            if (up) mma_step(dk[nt], apt, bq0, bq1);
+            mma_step(dk[nt], ad, bk0, bk1);
+        }
+    }
+#pragma unroll
+    for (int hm = 0; hm < 2; ++hm) {
+        const int r = 16 * mo + g8 + 8 * hm;
+        const int t = t0 + r;
+        if (t >= T) continue;
+        const float dn2 = 2.f * db[r];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            const int c = co + 8 * nt + 2 * t4;
+            const size_t off = (((size_t)b * T + t) * H + h) * DK + c;
+            IO* q2 = static_cast<IO*>(a.dq) + off;
+            IO* k2 = static_cast<IO*>(a.dk_) + off;
+            q2[0] = from_f32<IO>(dq[nt][2 * hm]);
+            q2[1] = from_f32<IO>(dq[nt][2 * hm + 1]);
+            k2[0] = from_f32<IO>(fmaf(dn2, Ks[r * LDK + c], dk[nt][2 * hm]));
+            k2[1] = from_f32<IO>(
+                fmaf(dn2, Ks[r * LDK + c + 1], dk[nt][2 * hm + 1]));
+        }
+    }
+}
+
 // DVS: dv columns per CTA of the reverse state recurrence; DVT: dv columns
 // per step of the gradient kernel.
 template <int DK, int DVS, int DVT, typename IO>
@@ -1077,6 +1616,23 @@ cudaError_t launch_shape(const BwdArgs& a, cudaStream_t stream) {
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if constexpr (DK == kTcDK && DVT == 32 &&
+                  std::is_same<IO, __nv_bfloat16>::value) {
+        auto a16 = [](const void* p) {
+            return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+        };
+        // the per-chunk products on the tensor cores (16-byte loads of q,
+        // k, v, o_grad)
+        if (a.C == kTcC && a16(a.q) && a16(a.k) && a16(a.v) && a16(a.dout)) {
+            auto km = kla_bwd_grad_mma_kernel<IO>;
+            e = cudaFuncSetAttribute(
+                km, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                (int)LG::BYTES);
+            if (e != cudaSuccess) return e;
+            km<<<(unsigned)(bhs * nch), kBwdThreads, LG::BYTES, stream>>>(a);
+            return cudaGetLastError();
+        }
+    }
     kg<<<(unsigned)(bhs * nch), kBwdThreads, LG::BYTES, stream>>>(a);
     return cudaGetLastError();
 }

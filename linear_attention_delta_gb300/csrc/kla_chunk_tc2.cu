@@ -87,22 +87,32 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t addr, uint32_t lbo) {
 // ===================================================================
 
 constexpr int kPrepThreads = 128;
-constexpr int kLd = 68;                       // fp32 tile row stride
-constexpr int kTileBytes = 64 * kLd * 4;      // 17408
+// L and T are lower triangular in 16 x 16 blocks: only the 10 blocks (I, J)
+// with J <= I are stored, block bidx(I, J) = I (I + 1) / 2 + J, as 16 rows
+// of 20 floats (rows 80 bytes apart: the 8 rows a quarter warp reads or
+// writes at once fall in 8 different 4-bank groups).
+constexpr int kBs = 20;                       // packed block row stride
+constexpr int kBlk = 16 * kBs;                // floats per packed block
+constexpr int kPackBytes = 10 * kBlk * 4;     // 12800
+__host__ __device__ constexpr int bidx(int I, int J) {
+    return I * (I + 1) / 2 + J;
+}
 // shared memory map (from a 1024-aligned base)
 constexpr int kPKQ = 0;          // K_0 | Q_0 | K_1 | Q_1 (TMA), 32 KB; after G
-                                 // the record image [TU | P, then PTU | g]
-constexpr int kPL = 32768;       // L (strictly lower part of A), fp32
-constexpr int kPT = kPL + kTileBytes;        // T = A^{-1}, fp32
-constexpr int kPY = kPT + kTileBytes;        // 4 warps x 16 x 8 fp32 scratch
-constexpr int kPG = kPY + 4 * 16 * 8 * 4;    // g2[64]
+                                 // the record image [TU | P, then PTU | g],
+constexpr int kPL = kRecBytes;   // L (strictly lower part of A), packed, and
+constexpr int kPY = kPL + kPackBytes;   // 4 warps x 16 x 8 fp32 scratch
+constexpr int kPT = 32768;       // T = A^{-1}, packed
+constexpr int kPG = kPT + kPackBytes;        // g2[64]
 constexpr int kPBeta = kPG + 256;            // beta[64]
 constexpr int kPE = kPBeta + 256;            // column factors e_i[64]
 constexpr int kPBars = kPE + 256;            // 3 mbarriers
 constexpr int kPMisc = kPBars + 24;          // TMEM slot, warp total, flag
 constexpr int kPSmem = kPMisc + 16 + 1024;
-static_assert(kRecBytes <= kPL, "pre-pass map");
-static_assert(kPSmem <= 232448, "pre-pass shared memory");
+static_assert(kPY + 4 * 16 * 8 * 4 <= kPT, "pre-pass map");
+static_assert(kPL % 16 == 0 && kPT % 16 == 0, "float4 rows");
+// four CTAs per SM (the driver keeps 1 KB of each CTA's shared memory)
+static_assert(4 * (kPSmem + 1024) <= 233472, "pre-pass shared memory");
 
 struct PrepParams {
     const float* log_alpha;
@@ -113,20 +123,20 @@ struct PrepParams {
     int T, H, nchunks;
 };
 
-// acc (16 x 8, fragment layout) += A (16 x 16 fp32 tile, row stride kLd) x
-// B[:, n0 .. n0 + 7] (16 x 8 of a fp32 tile, row stride kLd), tf32 MMAs.
+// acc (16 x 8, fragment layout) += A (16 x 16 packed fp32 block) x
+// B[:, n0 .. n0 + 7] (16 x 8 of a packed fp32 block), tf32 MMAs.
 __device__ __forceinline__ void mm16x8(float (&acc)[4], const float* A,
                                        const float* B, int n0, int lane) {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
         uint32_t a[4];
-        a[0] = tc::to_tf32(A[g * kLd + 8 * kk + t]);
-        a[1] = tc::to_tf32(A[(g + 8) * kLd + 8 * kk + t]);
-        a[2] = tc::to_tf32(A[g * kLd + 8 * kk + t + 4]);
-        a[3] = tc::to_tf32(A[(g + 8) * kLd + 8 * kk + t + 4]);
-        const uint32_t b0 = tc::to_tf32(B[(8 * kk + t) * kLd + n0 + g]);
-        const uint32_t b1 = tc::to_tf32(B[(8 * kk + t + 4) * kLd + n0 + g]);
+        a[0] = tc::to_tf32(A[g * kBs + 8 * kk + t]);
+        a[1] = tc::to_tf32(A[(g + 8) * kBs + 8 * kk + t]);
+        a[2] = tc::to_tf32(A[g * kBs + 8 * kk + t + 4]);
+        a[3] = tc::to_tf32(A[(g + 8) * kBs + 8 * kk + t + 4]);
+        const uint32_t b0 = tc::to_tf32(B[(8 * kk + t) * kBs + n0 + g]);
+        const uint32_t b1 = tc::to_tf32(B[(8 * kk + t + 4) * kBs + n0 + g]);
         tc::mma_m16n8k8_tf32(acc, a, b0, b1);
     }
 }
@@ -140,7 +150,7 @@ __device__ void offdiag_slab(const float* L, float* T, float* Y, int I, int J,
     const int g = lane >> 2, t = lane & 3;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int m = J; m < I; ++m)
-        mm16x8(acc, L + 16 * I * kLd + 16 * m, T + 16 * m * kLd + 16 * J, n0,
+        mm16x8(acc, L + bidx(I, m) * kBlk, T + bidx(m, J) * kBlk, n0,
                lane);
     Y[g * 8 + 2 * t] = acc[0];
     Y[g * 8 + 2 * t + 1] = acc[1];
@@ -148,27 +158,27 @@ __device__ void offdiag_slab(const float* L, float* T, float* Y, int I, int J,
     Y[(g + 8) * 8 + 2 * t + 1] = acc[3];
     __syncwarp();
     float d[4] = {0.f, 0.f, 0.f, 0.f};
-    const float* Tii = T + 16 * I * kLd + 16 * I;
+    const float* Tii = T + bidx(I, I) * kBlk;
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
         uint32_t a[4];
-        a[0] = tc::to_tf32(Tii[g * kLd + 8 * kk + t]);
-        a[1] = tc::to_tf32(Tii[(g + 8) * kLd + 8 * kk + t]);
-        a[2] = tc::to_tf32(Tii[g * kLd + 8 * kk + t + 4]);
-        a[3] = tc::to_tf32(Tii[(g + 8) * kLd + 8 * kk + t + 4]);
+        a[0] = tc::to_tf32(Tii[g * kBs + 8 * kk + t]);
+        a[1] = tc::to_tf32(Tii[(g + 8) * kBs + 8 * kk + t]);
+        a[2] = tc::to_tf32(Tii[g * kBs + 8 * kk + t + 4]);
+        a[3] = tc::to_tf32(Tii[(g + 8) * kBs + 8 * kk + t + 4]);
         const uint32_t b0 = tc::to_tf32(Y[(8 * kk + t) * 8 + g]);
         const uint32_t b1 = tc::to_tf32(Y[(8 * kk + t + 4) * 8 + g]);
         tc::mma_m16n8k8_tf32(d, a, b0, b1);
     }
     __syncwarp();
-    float* dst = T + 16 * I * kLd + 16 * J + n0;
-    dst[g * kLd + 2 * t] = -d[0];
-    dst[g * kLd + 2 * t + 1] = -d[1];
-    dst[(g + 8) * kLd + 2 * t] = -d[2];
-    dst[(g + 8) * kLd + 2 * t + 1] = -d[3];
+    float* dst = T + bidx(I, J) * kBlk + n0;
+    dst[g * kBs + 2 * t] = -d[0];
+    dst[g * kBs + 2 * t + 1] = -d[1];
+    dst[(g + 8) * kBs + 2 * t] = -d[2];
+    dst[(g + 8) * kBs + 2 * t + 1] = -d[3];
 }
 
-__global__ void __launch_bounds__(kPrepThreads)
+__global__ void __launch_bounds__(kPrepThreads, 4)
 kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_k, PrepParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -277,20 +287,19 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc::tmem_ld32(ta + 32, x + 32);
         tc::tmem_ld_wait();
         if (tid < kC) {
-            // A row r = tid: beta_r Gamma_ri (K K^T)_ri for i < r (fp32;
-            // float4 stores: rows 68 floats apart put the 8 rows of a
-            // quarter warp in 8 different bank groups)
-            const int r = tid;
-            float* Lr = Lt + r * kLd;
+            // A row r = tid: beta_r Gamma_ri (K K^T)_ri for i < r (fp32),
+            // into the packed blocks (I, m), m <= I, of its block row I
+            const int r = tid, I = r >> 4;
+            float kk = 0.f;   // ||k_r||^2, the diagonal of K K^T
 #pragma unroll
-            for (int i = 0; i < 64; i += 4)
-                *reinterpret_cast<float4*>(Lr + i) =
-                    make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
-            const float denom = Lr[r] + p.eps;   // ||k_r||^2 + eps
+            for (int i = 0; i < 64; ++i) kk = i == r ? x[i] : kk;
+            const float denom = kk + p.eps;
             const float br = p.gdn ? et : (denom == 0.f ? 0.f : et / denom);
             betas[r] = br;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
+                if (m > I) break;
+                float* Lr = Lt + bidx(I, m) * kBlk + (r & 15) * kBs - 16 * m;
                 const float gm = g2s[16 * m + 15];
                 const bool fact = fabsf(g2s[16 * m] - gm) <= 96.f;
                 const float bf = br * tc::ex2(g2 - gm);
@@ -341,11 +350,10 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     __syncthreads();
     // diagonal blocks T_bb = (I + L_bb)^{-1}: thread (bb, cl) solves column
-    // cl by substitution (threads 0..63); the others zero T above the
-    // diagonal blocks
+    // cl by substitution (threads 0..63)
     if (tid < kC) {
         const int bb = tid >> 4, cl = tid & 15;
-        const float* Lb = Lt + 16 * bb * kLd + 16 * bb;
+        const float* Lb = Lt + bidx(bb, bb) * kBlk;
         float xv[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) xv[r] = (r == cl) ? 1.f : 0.f;
@@ -354,22 +362,14 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll
             for (int i = 0; i < r; i += 2) {
-                a0 = fmaf(Lb[r * kLd + i], xv[i], a0);
-                if (i + 1 < r) a1 = fmaf(Lb[r * kLd + i + 1], xv[i + 1], a1);
+                a0 = fmaf(Lb[r * kBs + i], xv[i], a0);
+                if (i + 1 < r) a1 = fmaf(Lb[r * kBs + i + 1], xv[i + 1], a1);
             }
             if (r > cl) xv[r] = -(a0 + a1);
         }
-        float* Tb = Tt + 16 * bb * kLd + 16 * bb + cl;
+        float* Tb = Tt + bidx(bb, bb) * kBlk + cl;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Tb[r * kLd] = xv[r];
-    } else {
-        // blocks (I, J) with I < J
-        for (int e = tid - kC; e < 6 * 256; e += kC) {
-            const int blk = e >> 8, w = e & 255;
-            const int I = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-            const int J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            Tt[(16 * I + (w >> 4)) * kLd + 16 * J + (w & 15)] = 0.f;
-        }
+        for (int r = 0; r < 16; ++r) Tb[r * kBs] = xv[r];
     }
     __syncthreads();
     float* Y = reinterpret_cast<float*>(sm + kPY) + warp * 128;
@@ -393,10 +393,14 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int j = 0; j < 32; j += 8) {
             uint4 v;
+            const int col = c0 + j, I = r >> 4, J = col >> 4;
+            const float* tr =
+                Tt + bidx(I, J) * kBlk + (r & 15) * kBs + (col & 15);
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);   // J > I
             const float4 ta =
-                *reinterpret_cast<const float4*>(Tt + r * kLd + c0 + j);
+                J <= I ? *reinterpret_cast<const float4*>(tr) : z;
             const float4 tb =
-                *reinterpret_cast<const float4*>(Tt + r * kLd + c0 + j + 4);
+                J <= I ? *reinterpret_cast<const float4*>(tr + 4) : z;
             const float4 ba = *reinterpret_cast<const float4*>(betas + c0 + j);
             const float4 bb =
                 *reinterpret_cast<const float4*>(betas + c0 + j + 4);
@@ -483,9 +487,10 @@ constexpr int kSO = kSUt + 8192;     // o of a chunk, bf16 (TMA store image)
 constexpr int kSBars = kSO + 8192;
 // mbarriers: full[3] (TMA), ready[3] (helper done with the stage), hmma[2]
 // (helper MMAs, by helper group), c1 (chain MMA group 1), c2 (dS),
-// accfree[2] (accumulator of a chunk parity read out)
+// accfree[3] (accumulator c mod 3 read out), empty[3] (the chain is done
+// with a stage)
 constexpr int kBFull = 0, kBReady = 3, kBHmma = 6, kBC1 = 8, kBC2 = 9,
-              kBAccFree = 10, kNumBars = 12;
+              kBAccFree = 10, kBEmpty = 13, kNumBars = 16;
 constexpr int kSMisc = kSBars + 8 * kNumBars;   // abort, TMEM slot, issued
 constexpr int kSSmem = kSMisc + 16 + 1024;
 static_assert(kSG + 256 <= kStage && kStage % 1024 == 0, "stage map");
@@ -494,10 +499,19 @@ constexpr uint32_t kStageTx = 4 * 8192 + 8192 + kRecBytes;
 
 // TMEM columns
 constexpr uint32_t kColH = 0;        // helper group 0: [-W; -PTU Kg] (128)
-constexpr uint32_t kColAcc = 128;    // + 64 (c & 1): [U; PTU V], then [U~; O]
+constexpr uint32_t kColAcc = 128;    // + 64 (c mod 3 < 2): [U; PTU V], then
+constexpr uint32_t kColAcc2 = 448;   // [U~; O]; c mod 3 = 2 here
 constexpr uint32_t kColDS = 256;     // dS
 constexpr uint32_t kColH1 = 320;     // helper group 1: [-W; -PTU Kg] (128)
 constexpr uint32_t kTmemCols = 512;
+
+// Three accumulators [U; PTU V] in turn: the helper of chunk c writes one
+// while the chain still reads those of chunks c - 1 and c - 2, so a helper
+// waits only for the chain of chunk c - 3.
+__device__ __forceinline__ uint32_t acc_col(int c) {
+    const int r = c % 3;
+    return r == 2 ? kColAcc2 : kColAcc + 64 * r;
+}
 
 // Two helper warpgroups take the chunks in turns (group c & 1), so each has
 // two chain periods for one chunk.
@@ -616,9 +630,10 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t tmem = *tmem_slot;
 
     // Loads of chunk c into its stage (TMA tiles of K, Q, V and the record
-    // of the pre-pass), issued by chain thread 0: the first kNS at the start,
-    // then chunk c + kNS right after the chain has finished chunk c with
-    // that stage.  Chunks two rings ahead are prefetched into L2.
+    // of the pre-pass): the first kNS by thread 0 at the start, then chunk
+    // c >= kNS by lane 0 of the helper group that prepares it, as soon as
+    // the chain has released the stage (chunk c - kNS done).  Chunks two
+    // rings ahead are prefetched into L2.
     const uint8_t* rec0 = p.rec + (size_t)bh * nchunks * kRecBytes;
     auto prefetch = [&](int c) {
         const int t0 = c * kC;
@@ -642,7 +657,7 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc::tma_load_4d(st + kSV, &tm_v, bar, j0, h, t0, b);
         tc::bulk_load(st + kSTU, rec0 + (size_t)c * kRecBytes, kRecBytes,
                       bar);
-        *reinterpret_cast<volatile int*>(issued) = c + 1;
+        atomicMax(issued, c + 1);
         if (c + 2 * kNS < nchunks) prefetch(c + 2 * kNS);
     };
     if (tid == 0 && !p.no_issue) {
@@ -669,11 +684,25 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
             const int s = c % kNS;
             uint8_t* st = sm + s * kStage;
             const uint32_t sst = sbase + s * kStage;
-            bool ok = tc::mbar_wait_or_abort(&bars[kBFull + s], (c / kNS) & 1,
-                                             vabort, p.wait_ns);
-            if (ok && c >= 2)   // accumulator of this parity read out
-                ok = tc::mbar_wait_or_abort(&bars[kBAccFree + (c & 1)],
-                                            ((c - 2) >> 1) & 1, vabort,
+            bool ok = true;
+            if (c >= kNS && hl == 0 && !p.no_issue) {
+                // this group's lane 0 loads the chunk once the chain is done
+                // with chunk c - kNS (the helpers wait for the data anyway;
+                // the chain's own thread would pay the issue on its path)
+                ok = tc::mbar_wait_or_abort(&bars[kBEmpty + s],
+                                            ((c - kNS) / kNS) & 1, vabort,
+                                            p.wait_ns);
+                if (ok)
+                    issue_loads(c);
+                else
+                    *vabort = 1;
+            }
+            __syncwarp();
+            ok = ok && tc::mbar_wait_or_abort(&bars[kBFull + s],
+                                              (c / kNS) & 1, vabort, p.wait_ns);
+            if (ok && c >= 3)   // accumulator of chunk c - 3 read out
+                ok = tc::mbar_wait_or_abort(&bars[kBAccFree + c % 3],
+                                            ((c - 3) / 3) & 1, vabort,
                                             p.wait_ns);
             if (tc::named_bar_or(bar_id, kHelperThreads, !ok)) {
                 *vabort = 1;
@@ -714,7 +743,7 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
                 // [U; PTU V] = [TU; PTU] V       (M 128, N 64, K 64)
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tmem + kColAcc + 64 * (c & 1),
+                    tc::mma_bf16(tmem + acc_col(c),
                                  desc_k(sst + kSTU + ks * 32),
                                  desc_mn(sst + kSV + ks * 2048, 0), idB,
                                  ks > 0);
@@ -795,7 +824,7 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
             const int s = c % kNS;
             const uint8_t* st = sm + s * kStage;
             const uint32_t sst = sbase + s * kStage;
-            const uint32_t acc = tmem + kColAcc + 64 * (c & 1);
+            const uint32_t acc = tmem + acc_col(c);
             if constexpr (kCkpt) {   // the state chunk c starts from (fp32)
                 float* dst = p.ckpt +
                              (((size_t)bh * nchunks + c) * kD + row) * kD + j0;
@@ -897,8 +926,9 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
             tc::tc_fence_before();
             tc::named_bar_sync(kBarChain, kChainThreads);
             if (tid == 0) {
-                tc::mbar_arrive(&bars[kBAccFree + (c & 1)]);
-                if (c + kNS < nchunks) issue_loads(c + kNS);   // stage free
+                tc::mbar_arrive(&bars[kBAccFree + c % 3]);
+                if (c + kNS < nchunks)   // stage free
+                    tc::mbar_arrive(&bars[kBEmpty + s]);
             }
         }
         if (failed) {

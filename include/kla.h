@@ -125,8 +125,8 @@ KLA_API kla_status kla_chunk_fwd(const void* q, const void* k, const void* v,
  * unless dtype == KLA_BF16, dk == dv == 128, C == 64 and q, k, v, o, h0, hT
  * are 16-byte aligned.  An unknown algo or rule is KLA_ERR_INVALID_ARG.
  *
- * KLA_ALGO_AUTO takes the fused tensor-core kernel where it is eligible.
- * The two-kernel tensor-core path (KLA_ALGO_TC) writes per-chunk
+ * KLA_ALGO_AUTO takes the two-kernel tensor-core path (KLA_ALGO_TC) where it
+ * is eligible, the faster one on GB300.  That path writes per-chunk
  * intermediates between its two kernels:
  * kla_chunk_fwd and kla_chunk_fwd_ex take that scratch
  * (kla_chunk_fwd_workspace_size bytes) with cudaMallocAsync on `stream` from
@@ -142,8 +142,8 @@ KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
 
 /*
  * kla_chunk_fwd_workspace_size -- bytes of device workspace kla_chunk_fwd_ws
- * needs with this algorithm: for bf16, dk = dv = 128, C = 64 and KLA_ALGO_TC,
- * the pre-pass records of the two-kernel tensor-core path,
+ * needs with this algorithm: for bf16, dk = dv = 128, C = 64 and KLA_ALGO_TC
+ * or KLA_ALGO_AUTO, the pre-pass records of the two-kernel tensor-core path,
  * 16,640 bytes per (batch, head, chunk of 64 tokens); 0 otherwise (those
  * paths need none).  Errors: KLA_ERR_INVALID_ARG (null `bytes`, negative
  * size, bad enum), KLA_ERR_UNSUPPORTED_SHAPE (dk, dv or C outside the set).

@@ -50,7 +50,7 @@ bool any_overlap(const Span (&ins)[NI], const Span (&outs)[NO]) {
 
 // Whether KLA_ALGO_AUTO takes the two-kernel tensor-core path where it is
 // eligible (else the fused kernel): the faster of the two on GB300.
-constexpr bool kAutoTwoKernel = false;
+constexpr bool kAutoTwoKernel = true;
 
 // Bytes of workspace the two-kernel tensor-core path needs for these sizes
 // (0 when the shape or the algorithm does not take that path).

@@ -88,22 +88,27 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t addr, uint32_t lbo) {
 
 constexpr int kPrepThreads = 128;
 // L and T are lower triangular in 16 x 16 blocks: only the 10 blocks (I, J)
-// with J <= I are stored, block bidx(I, J) = I (I + 1) / 2 + J, as 16 rows
-// of 20 floats (rows 80 bytes apart: the 8 rows a quarter warp reads or
-// writes at once fall in 8 different 4-bank groups).
+// with J <= I of L are stored, block bidx(I, J) = I (I + 1) / 2 + J, as 16
+// rows of 20 floats (rows 80 bytes apart: the 8 rows a quarter warp reads
+// or writes at once fall in 8 different 4-bank groups).  The diagonal
+// blocks T_II replace L_II once solved; the 6 blocks of T below them are
+// stored apart, block oidx(I, J) = I (I - 1) / 2 + J.
 constexpr int kBs = 20;                       // packed block row stride
 constexpr int kBlk = 16 * kBs;                // floats per packed block
 constexpr int kPackBytes = 10 * kBlk * 4;     // 12800
 __host__ __device__ constexpr int bidx(int I, int J) {
     return I * (I + 1) / 2 + J;
 }
+__host__ __device__ constexpr int oidx(int I, int J) {
+    return I * (I - 1) / 2 + J;
+}
 // shared memory map (from a 1024-aligned base)
 constexpr int kPKQ = 0;          // K_0 | Q_0 | K_1 | Q_1 (TMA), 32 KB; after G
                                  // the record image [TU | P, then PTU | g],
 constexpr int kPL = kRecBytes;   // L (strictly lower part of A), packed, and
 constexpr int kPY = kPL + kPackBytes;   // 4 warps x 16 x 8 fp32 scratch
-constexpr int kPT = 32768;       // T = A^{-1}, packed
-constexpr int kPG = kPT + kPackBytes;        // g2[64]
+constexpr int kPT = 32768;       // T below its diagonal blocks, packed
+constexpr int kPG = kPT + 6 * kBlk * 4;      // g2[64]
 constexpr int kPBeta = kPG + 256;            // beta[64]
 constexpr int kPE = kPBeta + 256;            // column factors e_i[64]
 constexpr int kPBars = kPE + 256;            // 3 mbarriers
@@ -111,8 +116,8 @@ constexpr int kPMisc = kPBars + 24;          // TMEM slot, warp total, flag
 constexpr int kPSmem = kPMisc + 16 + 1024;
 static_assert(kPY + 4 * 16 * 8 * 4 <= kPT, "pre-pass map");
 static_assert(kPL % 16 == 0 && kPT % 16 == 0, "float4 rows");
-// four CTAs per SM (the driver keeps 1 KB of each CTA's shared memory)
-static_assert(4 * (kPSmem + 1024) <= 233472, "pre-pass shared memory");
+// five CTAs per SM (the driver keeps 1 KB of each CTA's shared memory)
+static_assert(5 * (kPSmem + 1024) <= 233472, "pre-pass shared memory");
 
 struct PrepParams {
     const float* log_alpha;
@@ -145,12 +150,17 @@ __device__ __forceinline__ void mm16x8(float (&acc)[4], const float* A,
 //   T_IJ[:, n0..n0+7] = -T_II sum_{m=J}^{I-1} L_Im T_mJ[:, n0..n0+7].
 // The sum is formed in registers, passed through this warp's scratch Y
 // (16 x 8, row stride 8) and multiplied by T_II.
-__device__ void offdiag_slab(const float* L, float* T, float* Y, int I, int J,
+// Block (I, J) of T: the diagonal ones sit in L's storage, the others in To.
+__device__ __forceinline__ float* tblock(float* L, float* To, int I, int J) {
+    return I == J ? L + bidx(I, I) * kBlk : To + oidx(I, J) * kBlk;
+}
+
+__device__ void offdiag_slab(float* L, float* T, float* Y, int I, int J,
                              int n0, int lane) {
     const int g = lane >> 2, t = lane & 3;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int m = J; m < I; ++m)
-        mm16x8(acc, L + bidx(I, m) * kBlk, T + bidx(m, J) * kBlk, n0,
+        mm16x8(acc, L + bidx(I, m) * kBlk, tblock(L, T, m, J), n0,
                lane);
     Y[g * 8 + 2 * t] = acc[0];
     Y[g * 8 + 2 * t + 1] = acc[1];
@@ -158,7 +168,7 @@ __device__ void offdiag_slab(const float* L, float* T, float* Y, int I, int J,
     Y[(g + 8) * 8 + 2 * t + 1] = acc[3];
     __syncwarp();
     float d[4] = {0.f, 0.f, 0.f, 0.f};
-    const float* Tii = T + bidx(I, I) * kBlk;
+    const float* Tii = L + bidx(I, I) * kBlk;
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
         uint32_t a[4];
@@ -171,14 +181,14 @@ __device__ void offdiag_slab(const float* L, float* T, float* Y, int I, int J,
         tc::mma_m16n8k8_tf32(d, a, b0, b1);
     }
     __syncwarp();
-    float* dst = T + bidx(I, J) * kBlk + n0;
+    float* dst = T + oidx(I, J) * kBlk + n0;
     dst[g * kBs + 2 * t] = -d[0];
     dst[g * kBs + 2 * t + 1] = -d[1];
     dst[(g + 8) * kBs + 2 * t] = -d[2];
     dst[(g + 8) * kBs + 2 * t + 1] = -d[3];
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 4)
+__global__ void __launch_bounds__(kPrepThreads, 5)
 kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_k, PrepParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -367,7 +377,8 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
             if (r > cl) xv[r] = -(a0 + a1);
         }
-        float* Tb = Tt + bidx(bb, bb) * kBlk + cl;
+        __syncwarp();   // this warp's two blocks of L are read: T over them
+        float* Tb = Lt + bidx(bb, bb) * kBlk + cl;
 #pragma unroll
         for (int r = 0; r < 16; ++r) Tb[r * kBs] = xv[r];
     }
@@ -395,7 +406,7 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
             uint4 v;
             const int col = c0 + j, I = r >> 4, J = col >> 4;
             const float* tr =
-                Tt + bidx(I, J) * kBlk + (r & 15) * kBs + (col & 15);
+                tblock(Lt, Tt, I, J < I ? J : I) + (r & 15) * kBs + (col & 15);
             const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);   // J > I
             const float4 ta =
                 J <= I ? *reinterpret_cast<const float4*>(tr) : z;

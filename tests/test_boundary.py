@@ -232,7 +232,7 @@ def test_host_fwd_workspace_size(lib):
         4, 4096, 16, 128, 128, 64, 1, ctypes.byref(n)) == OK
     # two slots of one segment (512 tokens: q, k, v, o bf16, two fp32
     # gates), two fp32 states and the forward's own workspace for one
-    # segment (none: the default path is the fused kernel)
+    # segment (the pre-pass records of the default two-kernel path)
     rows = 4 * 512 * 16
     fwd = kla.chunk_fwd_workspace_size(4, 512, 16, 128, 128, 64,
                                        kla.torch.bfloat16)

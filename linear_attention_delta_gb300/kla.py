@@ -145,7 +145,7 @@ def forward_path(B, T, H, dk, dv, C, dtype, algo="auto") -> dict:
     dominates."""
     if chunk_fwd_workspace_size(B, T, H, dk, dv, C, dtype, algo) > 0:
         return {"name": "prepass+state", "launches": 2,
-                "traffic_key": "kla_state_kernel"}
+                "traffic_key": "kla_prep_kernel+kla_state_kernel"}
     if dtype == torch.bfloat16 and dk == dv == 128 and C == 64 and \
             algo in ("auto", "tc", "tc_fused"):
         return {"name": "fused", "launches": 1,

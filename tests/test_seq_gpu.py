@@ -78,11 +78,14 @@ def test_learned_step_rule():
 
 
 def test_one_segment_is_the_plain_forward():
+    """One segment runs the fused tensor-core kernel on the whole sequence
+    (the sequence path allocates nothing of its own), bit for bit."""
     inp = gen.prefill_inputs(gen.LAYER_1B, B=1, T=640, H=2)
     o1, h1 = run_seq(inp, 1)
     d = {n: (v.cuda() if isinstance(v, torch.Tensor) else v)
          for n, v in inp.items()}
-    o2, h2 = kla.chunk_fwd(*[d[n] for n in NAMES], d["eps"], d["h0"], C=64)
+    o2, h2 = kla.chunk_fwd(*[d[n] for n in NAMES], d["eps"], d["h0"], C=64,
+                           algo="tc_fused")
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(h1, h2)
 

@@ -178,8 +178,10 @@ KLA_API kla_status kla_chunk_fwd_ws(const void* q, const void* k,
  * kla_chunk_fwd_seq_workspace_size -- bytes of device workspace
  * kla_chunk_fwd_seq needs: fp32 start and end states of the 2 x B x P
  * segment runs (4 tensors [B, P, H, 128, 128]), O_hom [B, T, H, 128] bf16,
- * the bf16 start states [B, P, H, 128, 128] and a [64, H, 128] bf16 zero
- * tile; 0 when there is nothing to split.  segments = 0 picks P as
+ * the bf16 start states [B, P, H, 128, 128], a [64, H, 128] bf16 zero
+ * tile and the records of the two-kernel path's pre-pass (16,640 bytes per
+ * (batch, head, 64-token chunk)), each rounded up to 256 bytes; 0 when
+ * there is nothing to split.  segments = 0 picks P as
  * kla_chunk_fwd_seq does (for the current device).  Errors:
  * KLA_ERR_INVALID_ARG (null `bytes`, negative size or segments),
  * KLA_ERR_UNSUPPORTED_SHAPE (not bf16 with dk = dv = 128 and C = 64, P > 8,
@@ -197,10 +199,12 @@ KLA_API kla_status kla_chunk_fwd_seq_workspace_size(int B, int T, int H,
  * each.  The recurrence is linear in the state: segment s maps its start
  * state S_s to Phi_s S_s + B_s and gives the outputs O0_s + O_hom,s S_s,
  * with B_s, O0_s from the segment run from a zero state and Phi_s, O_hom,s
- * from the run from the identity with V = 0.  Both runs are the forward
- * kernel over the B P segments (at the same time, on `stream` and on a
- * second stream of the library; with B = 1 the second run skips segment 0,
- * whose Phi and O_hom are not needed); a small kernel chains S_{s+1} =
+ * from the run from the identity with V = 0.  Both runs are the two-kernel
+ * tensor-core forward over the B P segments: one pre-pass (its records
+ * depend on q, k and the gates only) serves the two state passes, which run
+ * at the same time on `stream` and on a second stream of the library (with
+ * B = 1 the second run skips segment 0, whose Phi and O_hom are not
+ * needed); a small kernel chains S_{s+1} =
  * Phi_s S_s + B_s and a tensor-core kernel adds O_hom,s S_s to o of every
  * segment after the first.  The pages have no counterpart: it reorders the
  * sums of the chunkwise form, so o and hT equal kla_chunk_fwd_ex's up to

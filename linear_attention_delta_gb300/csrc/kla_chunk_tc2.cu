@@ -1017,36 +1017,55 @@ bool chunk_tc2_eligible(const FwdArgs& a) {
            (!a.hT || aligned16(a.hT)) && get_encoder();
 }
 
-cudaError_t launch_chunk_tc2(const FwdArgs& a, void* workspace,
-                             cudaStream_t stream) {
+cudaError_t launch_prep_tc2(const FwdArgs& a, void* rec, cudaStream_t stream) {
     if ((long)a.B * a.H == 0 || a.T == 0) return cudaSuccess;
     if (!get_encoder()) return cudaErrorNotSupported;
-    if ((a.o == nullptr) == (a.ckpt == nullptr)) return cudaErrorInvalidValue;
-    if (!workspace || !aligned16(workspace)) return cudaErrorInvalidValue;
-    CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mq, a.q, a.B, a.T, a.H) ||
-        !make_map(&mk, a.k, a.B, a.T, a.H) || !make_v_map(&mv, a) ||
-        !make_map(&mo, a.o ? a.o : a.q, a.B, a.T, a.H))
+    if (!rec || !aligned16(rec)) return cudaErrorInvalidValue;
+    CUtensorMap mq, mk;
+    if (!make_map(&mq, a.q, a.B, a.T, a.H) || !make_map(&mk, a.k, a.B, a.T, a.H))
         return cudaErrorInvalidValue;
     const int nchunks = (a.T + kC - 1) / kC;
     const long nprep = (long)a.B * a.H * nchunks;
     if (nprep > 0x7fffffffL) return cudaErrorInvalidValue;
     cudaError_t e = set_smem((const void*)kla_prep_kernel, kPSmem, g_prep_attr);
     if (e != cudaSuccess) return e;
-    uint8_t* rec = static_cast<uint8_t*>(workspace);
-    PrepParams pp{a.log_alpha, a.eta, rec, a.eps, a.gdn, a.T, a.H, nchunks};
+    PrepParams pp{a.log_alpha, a.eta, static_cast<uint8_t*>(rec), a.eps, a.gdn,
+                  a.T, a.H, nchunks};
     kla_prep_kernel<<<(unsigned)nprep, kPrepThreads, kPSmem, stream>>>(mq, mk,
                                                                       pp);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_state_tc2(const FwdArgs& a, const void* rec,
+                             cudaStream_t stream) {
+    if ((long)a.B * a.H == 0 || a.T == 0) return cudaSuccess;
+    if (!get_encoder()) return cudaErrorNotSupported;
+    if ((a.o == nullptr) == (a.ckpt == nullptr)) return cudaErrorInvalidValue;
+    if (!rec || !aligned16(rec)) return cudaErrorInvalidValue;
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map(&mq, a.q, a.B, a.T, a.H) ||
+        !make_map(&mk, a.k, a.B, a.T, a.H) || !make_v_map(&mv, a) ||
+        !make_map(&mo, a.o ? a.o : a.q, a.B, a.T, a.H))
+        return cudaErrorInvalidValue;
+    const int nchunks = (a.T + kC - 1) / kC;
     auto kern = a.ckpt ? kla_state_kernel<true> : kla_state_kernel<false>;
-    e = set_smem((const void*)kern, kSSmem, g_state_attr[a.ckpt ? 1 : 0]);
+    cudaError_t e =
+        set_smem((const void*)kern, kSSmem, g_state_attr[a.ckpt ? 1 : 0]);
     if (e != cudaSuccess) return e;
-    StateParams sp{a.h0, static_cast<__nv_bfloat16*>(a.o), a.hT, a.ckpt, rec,
-                   a.T, a.H, nchunks, 2000000000ull, 0};
+    StateParams sp{a.h0, static_cast<__nv_bfloat16*>(a.o), a.hT, a.ckpt,
+                   static_cast<const uint8_t*>(rec), a.T, a.H, nchunks,
+                   2000000000ull, 0};
     dim3 grid((unsigned)((long)a.B * a.H), kD / kNV);
     kern<<<grid, kStateThreads, kSSmem, stream>>>(mq, mk, mv, mo, sp);
     return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_tc2(const FwdArgs& a, void* workspace,
+                             cudaStream_t stream) {
+    if ((a.o == nullptr) == (a.ckpt == nullptr)) return cudaErrorInvalidValue;
+    cudaError_t e = launch_prep_tc2(a, workspace, stream);
+    if (e != cudaSuccess) return e;
+    return launch_state_tc2(a, workspace, stream);
 }
 
 namespace {

@@ -48,7 +48,7 @@ size_t round_up(size_t n) { return (n + kAlign - 1) / kAlign * kAlign; }
 
 // Byte layout of the workspace.
 struct Layout {
-    size_t h0s, hts, eye, phi, ohom, sst, zero, total;
+    size_t h0s, hts, eye, phi, ohom, sst, zero, rec, total;
 };
 
 Layout layout(int B, int T, int H, int P) {
@@ -62,6 +62,9 @@ Layout layout(int B, int T, int H, int P) {
     L.ohom = off; off += round_up((size_t)B * T * H * kD * 2);
     L.sst = off; off += round_up((size_t)B * P * H * kD * kD * 2);
     L.zero = off; off += round_up((size_t)kC * H * kD * 2);
+    // pre-pass records of the two-kernel tensor-core path, shared by the
+    // two runs
+    L.rec = off; off += round_up(kla::chunk_tc2_workspace_bytes(B * P, T / P, H));
     L.total = off;
     return L;
 }
@@ -398,9 +401,22 @@ extern "C" kla_status kla_chunk_fwd_seq(
         hom.hT = phi + (size_t)H * kD * kD;
         hom.B = P - 1;
     }
-    if (!kla::chunk_tc_eligible(zs)) return KLA_ERR_UNSUPPORTED_SHAPE;
-    KLA_TRY(kla::launch_chunk_tc(zs, s));
-    KLA_TRY(kla::launch_chunk_tc(hom, A.s));
+    if (kla::chunk_tc2_eligible(zs)) {
+        // one pre-pass over all B P segments, then the two state passes;
+        // with B = 1 the homogeneous run starts at segment 1's records
+        char* rec = ws + L.rec;
+        const char* rec_hom =
+            rec + (B == 1 ? kla::chunk_tc2_workspace_bytes(1, tseg, H) : 0);
+        KLA_TRY(kla::launch_prep_tc2(zs, rec, s));
+        KLA_TRY(cudaEventRecord(A.fork, s));
+        KLA_TRY(cudaStreamWaitEvent(A.s, A.fork, 0));
+        KLA_TRY(kla::launch_state_tc2(zs, rec, s));
+        KLA_TRY(kla::launch_state_tc2(hom, rec_hom, A.s));
+    } else {
+        if (!kla::chunk_tc_eligible(zs)) return KLA_ERR_UNSUPPORTED_SHAPE;
+        KLA_TRY(kla::launch_chunk_tc(zs, s));
+        KLA_TRY(kla::launch_chunk_tc(hom, A.s));
+    }
     KLA_TRY(cudaEventRecord(A.join, A.s));
     KLA_TRY(cudaStreamWaitEvent(s, A.join, 0));
 

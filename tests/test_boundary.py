@@ -270,8 +270,9 @@ def test_seq_fwd_workspace_size_and_host_checks(lib):
     assert lib.kla_chunk_fwd_seq_workspace_size(
         1, 131072, 16, 128, 128, 64, 1, 2, ctypes.byref(n)) == OK
     st = 1 * 2 * 16 * 128 * 128
+    rec = 16 * (131072 // 64) * 16640    # pre-pass records, all chunks
     assert n.value == (4 * st * 4 + 131072 * 16 * 128 * 2 + st * 2
-                       + 64 * 16 * 128 * 2)
+                       + 64 * 16 * 128 * 2 + rec)
     # one segment: nothing to split, no workspace
     assert lib.kla_chunk_fwd_seq_workspace_size(
         1, 4096, 16, 128, 128, 64, 1, 1, ctypes.byref(n)) == OK

@@ -206,6 +206,9 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
     uint8_t* out = sm + kPKQ;   // record image, over the consumed K / Q
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the state pass may be scheduled once every pre-pass CTA has started;
+    // it waits for this grid's completion before it reads a record
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int c = blockIdx.x % p.nchunks;
     const int bh = blockIdx.x / p.nchunks;
     const int b = bh / p.H, h = bh % p.H;
@@ -225,7 +228,7 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc::tma_load_4d(sm + kPKQ + 24576, &tm_q, &bars[0], 64, h, t0, b);
     }
     if (warp == 0) {
-        tc::tmem_alloc(tmem_slot, 128);
+        tc::tmem_alloc(tmem_slot, 64);   // five CTAs per SM fit in TMEM
         tc::tmem_relinquish();
     }
     // gates of this chunk: cumulative log2 decay (two warp scans)
@@ -286,7 +289,7 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
             tc::mbar_wait(&bars[1], 0, 100000000ull);   // the MMAs, if issued
         }
         __syncthreads();
-        if (warp == 0) tc::tmem_dealloc(tmem, 128);
+        if (warp == 0) tc::tmem_dealloc(tmem, 64);
         return;
     }
     tc::tc_fence_after();
@@ -426,14 +429,15 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
-    // PTU = P TU on the tensor cores: [TU; P] TU, lanes 64..127 (TMEM
-    // columns 64..127); TU is K-major as the A rows and MN-major as B
+    // PTU = P TU on the tensor cores: [TU; P] TU, lanes 64..127, over G's
+    // columns (G was read out before the barriers above); TU is K-major as
+    // the A rows and MN-major as B
     if (tid == 0) {
         tc::tc_fence_after();
         constexpr uint32_t idP = tc::idesc_bf16(128, 64, false, true);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16(tmem + 64, desc_k(sbase + kPKQ + kRecTU + ks * 32),
+            tc::mma_bf16(tmem, desc_k(sbase + kPKQ + kRecTU + ks * 32),
                          desc_mn(sbase + kPKQ + kRecTU + ks * 2048, 0), idP,
                          ks > 0);
         tc::mma_commit(&bars[2]);
@@ -445,7 +449,7 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (tid >= kC) {   // PTU rows over P
             const int r = tid - kC;
             float x[64];
-            const uint32_t ta = tmem + 64 + ((uint32_t)(warp * 32) << 16);
+            const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
             tc::tmem_ld32(ta, x);
             tc::tmem_ld32(ta + 32, x + 32);
             tc::tmem_ld_wait();
@@ -473,7 +477,7 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc::mbar_wait(&bars[2], 0, 100000000ull);
     }
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+    if (warp == 0) tc::tmem_dealloc(tmem, 64);
 }
 
 // ===================================================================
@@ -639,6 +643,9 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // launched as a programmatic dependent of the pre-pass: everything above
+    // overlaps its last wave; the records are read only after this
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Loads of chunk c into its stage (TMA tiles of K, Q, V and the record
     // of the pre-pass): the first kNS by thread 0 at the start, then chunk
@@ -1037,7 +1044,7 @@ cudaError_t launch_prep_tc2(const FwdArgs& a, void* rec, cudaStream_t stream) {
 }
 
 cudaError_t launch_state_tc2(const FwdArgs& a, const void* rec,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, bool after_prep) {
     if ((long)a.B * a.H == 0 || a.T == 0) return cudaSuccess;
     if (!get_encoder()) return cudaErrorNotSupported;
     if ((a.o == nullptr) == (a.ckpt == nullptr)) return cudaErrorInvalidValue;
@@ -1055,9 +1062,17 @@ cudaError_t launch_state_tc2(const FwdArgs& a, const void* rec,
     StateParams sp{a.h0, static_cast<__nv_bfloat16*>(a.o), a.hT, a.ckpt,
                    static_cast<const uint8_t*>(rec), a.T, a.H, nchunks,
                    2000000000ull, 0};
-    dim3 grid((unsigned)((long)a.B * a.H), kD / kNV);
-    kern<<<grid, kStateThreads, kSSmem, stream>>>(mq, mk, mv, mo, sp);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((long)a.B * a.H), kD / kNV);
+    cfg.blockDim = dim3(kStateThreads);
+    cfg.dynamicSmemBytes = kSSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_prep ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, sp);
 }
 
 cudaError_t launch_chunk_tc2(const FwdArgs& a, void* workspace,
@@ -1065,7 +1080,7 @@ cudaError_t launch_chunk_tc2(const FwdArgs& a, void* workspace,
     if ((a.o == nullptr) == (a.ckpt == nullptr)) return cudaErrorInvalidValue;
     cudaError_t e = launch_prep_tc2(a, workspace, stream);
     if (e != cudaSuccess) return e;
-    return launch_state_tc2(a, workspace, stream);
+    return launch_state_tc2(a, workspace, stream, true);
 }
 
 namespace {

@@ -115,9 +115,12 @@ cudaError_t launch_chunk_tc2(const FwdArgs& a, void* workspace,
 // Its two launches apart: the pre-pass writes the records of a.q, a.k and
 // the gates (a.v, a.o, a.h0 unused); the state pass reads them.  Two state
 // passes may share one pre-pass when they differ only in v, h0, o, hT.
+// after_prep: the pre-pass is the launch right before on this stream; the
+// state pass is then launched as its programmatic dependent (its set-up
+// overlaps the pre-pass's last wave).
 cudaError_t launch_prep_tc2(const FwdArgs& a, void* rec, cudaStream_t stream);
 cudaError_t launch_state_tc2(const FwdArgs& a, const void* rec,
-                             cudaStream_t stream);
+                             cudaStream_t stream, bool after_prep);
 cudaError_t read_and_clear_fault2(unsigned int* word);
 // One CTA of the state-pass kernel whose producer issues no copy and whose
 // waits give up after 1 ms: it takes the kernel's abort path and sets the

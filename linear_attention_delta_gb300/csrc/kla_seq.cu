@@ -410,8 +410,8 @@ extern "C" kla_status kla_chunk_fwd_seq(
         KLA_TRY(kla::launch_prep_tc2(zs, rec, s));
         KLA_TRY(cudaEventRecord(A.fork, s));
         KLA_TRY(cudaStreamWaitEvent(A.s, A.fork, 0));
-        KLA_TRY(kla::launch_state_tc2(zs, rec, s));
-        KLA_TRY(kla::launch_state_tc2(hom, rec_hom, A.s));
+        KLA_TRY(kla::launch_state_tc2(zs, rec, s, true));
+        KLA_TRY(kla::launch_state_tc2(hom, rec_hom, A.s, false));
     } else {
         if (!kla::chunk_tc_eligible(zs)) return KLA_ERR_UNSUPPORTED_SHAPE;
         KLA_TRY(kla::launch_chunk_tc(zs, s));

@@ -140,22 +140,24 @@ def test_zero_keys_with_zero_eps():
     check_fwd(inp, "simt")
 
 
-def test_tensor_core_zero_keys_with_zero_eps():
+@pytest.mark.parametrize("algo", ["tc", "tc_fused"])
+def test_tensor_core_zero_keys_with_zero_eps(algo):
     """k = 0 with eps = 0 makes beta's denominator exactly 0; beta := 0 (no
-    write), as in the oracle.  Through the tensor-core kernel, with zero keys
-    on the first and the last row of a chunk, inside a chunk, on a run of
-    rows and on the last token of a ragged tail."""
+    write), as in the oracle.  Through both tensor-core paths, with zero
+    keys on the first and the last row of a chunk, inside a chunk, on a run
+    of rows and on the last token of a ragged tail."""
     inp = gen.prefill_inputs(gen.LAYER_1B, B=2, T=200, H=2)
     for t in (0, 5, 63, 64, 100, 101, 102, 127, 199):
         inp["k"][:, t] = 0.0
     inp["k"][1, 130:140, 1] = 0.0
     inp["eps"] = 0.0
-    check_fwd(inp, "tc")
+    check_fwd(inp, algo)
 
 
-def test_tensor_core_unrelaxed_projection():
+@pytest.mark.parametrize("algo", ["tc", "tc_fused"])
+def test_tensor_core_unrelaxed_projection(algo):
     """eta = 1, eps = 0, alpha = 1 (every write an exact projection,
-    S_t^T k_t = v_t): with q := k the bf16 tensor-core path returns each
+    S_t^T k_t = v_t): with q := k both bf16 tensor-core paths return each
     token's value, within the bf16 bound, over 3 chunks and a ragged tail."""
     from dataclasses import replace
     w = replace(gen.LAYER_1B, unrelaxed=True, eps=0.0, h0_std=0.0)
@@ -163,9 +165,9 @@ def test_tensor_core_unrelaxed_projection():
     assert float(inp["eps"]) == 0.0 and float(inp["eta"].min()) == 1.0
     assert float(inp["log_alpha"].abs().max()) == 0.0
     inp["q"] = inp["k"].clone()
-    o, _ = run_fwd(inp, "tc")
+    o, _ = run_fwd(inp, algo)
     assert rel_err(o, inp["v"].double().numpy()) <= 2e-2
-    check_fwd(inp, "tc")
+    check_fwd(inp, algo)
 
 
 def test_plain_c_entry_points_through_ctypes():
@@ -215,8 +217,14 @@ def test_plain_c_entry_points_through_ctypes():
 @pytest.mark.parametrize("w", [gen.LAYER_340M, gen.LAYER_1B, gen.LONG_CTX],
                          ids=lambda w: w.name)
 def test_full_size_against_oracle(w):
-    """The workloads at their full sizes, every element compared."""
+    """The workloads at their full sizes, every element compared (the
+    default path: the two-kernel tensor-core forward)."""
     check_fwd(gen.prefill_inputs(w))
+
+
+def test_full_size_fused_kernel_against_oracle():
+    """The fused tensor-core kernel on the full 1B layer, every element."""
+    check_fwd(gen.prefill_inputs(gen.LAYER_1B), "tc_fused")
 
 
 # ---------------------------------------------------------------- decode

@@ -1042,63 +1042,6 @@ kla_bwd_grad_kernel(BwdArgs a) {
     }
 }
 
-// ------------------------------------------ gradients, tensor cores (bf16)
-// The same per-chunk gradients for bf16 inputs with dk = 128, C = 64, every
-// product on the tensor cores: warp-level m16n8k16 MMAs with bf16 operands
-// (rounded from the fp32 shared-memory tiles as the fragments are loaded)
-// and fp32 accumulation.  The elementwise and row-reduction steps are those
-// of kla_bwd_grad_kernel.  Eight warps; a product's 16 x 8 output tiles are
-// dealt out to them, dq and dk stay in registers (warp w: rows 16 (w & 3)..,
-// columns 64 (w >> 2)..).
-
-// A fragment of the 16 x 16 block starting at `p`, element (m, k) at
-// p[m * sm + k * sk], optionally each row m scaled by rs[m] and/or masked
-// to the lower (k <= m, tri = 1) or upper (k >= m, tri = 2) triangle.
-__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const float* p,
-                                       int sm, int sk, int lane,
-                                       const float* rs = nullptr,
-                                       int tri = 0) {
-    const int g = lane >> 2, t = lane & 3;
-    float v[8];
-    const int ms[2] = {g, g + 8};
-    const int ks[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
-#pragma unroll
-    for (int hm = 0; hm < 2; ++hm)
-#pragma unroll
-        for (int hk = 0; hk < 2; ++hk)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int m = ms[hm], k = ks[2 * hk + e];
-                float x = p[m * sm + k * sk];
-                if (tri == 1 && k > m) x = 0.f;
-                if (tri == 2 && k < m) x = 0.f;
-                if (rs) x *= rs[m];
-                v[4 * hk + 2 * hm + e] = x;
-            }
-    a[0] = tc::pack_bf16x2(v[0], v[1]);   // (g, 2t..2t+1)
-    a[1] = tc::pack_bf16x2(v[2], v[3]);   // (g+8, 2t..)
-    a[2] = tc::pack_bf16x2(v[4], v[5]);   // (g, 2t+8..)
-    a[3] = tc::pack_bf16x2(v[6], v[7]);   // (g+8, 2t+8..)
-}
-
-// B fragment of the 16 x 8 block starting at `p`, element (k, n) at
-// p[k * sk + n * sn].
-__device__ __forceinline__ void frag_b(uint32_t& b0, uint32_t& b1,
-                                       const float* p, int sk, int sn,
-                                       int lane) {
-    const int g = lane >> 2, t = lane & 3;
-    b0 = tc::pack_bf16x2(p[(2 * t) * sk + g * sn], p[(2 * t + 1) * sk + g * sn]);
-    b1 = tc::pack_bf16x2(p[(2 * t + 8) * sk + g * sn],
-                         p[(2 * t + 9) * sk + g * sn]);
-}
-
-// acc += A B for one k-step (A 16 x 16, B 16 x 8).
-__device__ __forceinline__ void mma_step(float (&acc)[4],
-                                         const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    tc::mma_m16n8k16(acc, a, b0, b1);
-}
-
 // Lower 16 x 8 tiles (mt, nt) of a 64 x 64 matrix (8 nt <= 16 mt + 15):
 // tile index 0 .. 19 -> (mt, nt).
 __device__ __forceinline__ void lower_tile(int idx, int& mt, int& nt) {
@@ -1107,39 +1050,159 @@ __device__ __forceinline__ void lower_tile(int idx, int& mt, int& nt) {
     nt = idx - first;
 }
 
-template <typename IO>
-__global__ void __launch_bounds__(kBwdThreads)
-kla_bwd_grad_mma_kernel(BwdArgs a) {
-    constexpr int DK = 128, DVT = 32;
-    using L = GradSmem<DK, DVT>;
-    constexpr int LDK = L::LDK, LDV = L::LDV, LDC = L::LDC;
-    extern __shared__ float sm[];
-    float* Qs = sm + L::Q;
-    float* Ks = sm + L::K;
-    float* As = sm + L::A;
-    float* Ps = sm + L::P;
-    float* dP = sm + L::DP;
-    float* dA = sm + L::DA;
-    float* St = sm + L::ST;
-    float* dSt = sm + L::DST;
-    float* Xs = sm + L::X;
-    float* Ds = sm + L::DO;
-    float* Us = sm + L::U;
-    float* Ws = sm + L::W;
-    float* KS = sm + L::KS;
-    float* gs = sm + L::G;
-    float* bs = sm + L::BETA;
-    float* gam = sm + L::GAM;
-    float* lam = sm + L::LAM;
-    float* nrm = sm + L::NRM;
-    float* db = sm + L::DB;
-    float* dgam = sm + L::DGAM;
-    float* dlam = sm + L::DLAM;
-    float* dg = sm + L::DG;
-    float* dgc = sm + L::DGC;
-    float* Tm = sm + L::TM;
+// ------------------------------ gradients, tensor cores, bf16 operand tiles
+// The per-chunk gradients of kla_bwd_grad_kernel for bf16 inputs with
+// dk = 128, C = 64, every product on the tensor cores (warp-level m16n8k16
+// MMAs, bf16 operands, fp32 accumulation), every MMA operand kept once in
+// shared memory as a bf16 tile whose rows are 16-byte
+// aligned and 16 bytes apart modulo 128 (row strides of 136, 72 and 40
+// elements), read by ldmatrix: one instruction per 16 x 16 (or two 16 x 8)
+// fragment, transposed on the fly where the product needs the other
+// orientation, and no bank conflict.  fp32 tiles stay only where an
+// elementwise step needs them (X, K S, U~) and for the inverse; dP and dA
+// accumulate in registers over the dv steps.  Inputs are bf16, so q and k
+// go to shared memory unconverted, and K K^T, Q K^T (for A, P and the
+// decay and beta terms at the end) are tensor-core products of the exact
+// inputs.
+using bf16 = __nv_bfloat16;
 
-    const int C = a.C, T = a.T, H = a.H, dv = a.dv;   // C == 64
+namespace lm {
+constexpr int C = 64, DK = 128, DVT = 32;
+constexpr int LQ = DK + 8;    // q, k rows (bf16)
+constexpr int LC = C + 8;     // C x C bf16 tiles
+constexpr int LV = DVT + 8;   // C x DVT and DK x DVT bf16 tiles
+constexpr int LF = C + 1;     // C x C fp32 (inverse, final phase)
+constexpr int LX = DVT + 1;   // C x DVT fp32
+// byte offsets
+constexpr int QB = 0;
+constexpr int KB = QB + C * LQ * 2;
+constexpr int TB = KB + C * LQ * 2;          // T = A^{-1}, lower
+constexpr int PB = TB + C * LC * 2;          // P, lower incl.
+constexpr int F0 = PB + C * LC * 2;          // fp32: A, later dP
+constexpr int F1 = F0 + C * LF * 4;          // fp32: T, later D
+constexpr int F2 = F1 + C * LF * 4;          // fp32: dGamma o Gamma
+constexpr int SB = F2 + C * LF * 4;          // S (DK x DVT), later Gamma o dP
+constexpr int DSB = SB + DK * LV * 2;        // dS', later D + D^T
+constexpr int XF = DSB + DK * LV * 2;        // V, then X (fp32)
+constexpr int KSF = XF + C * LX * 4;         // K S (fp32)
+constexpr int UF = KSF + C * LX * 4;         // U~ (fp32)
+constexpr int FB = UF + C * LX * 4;          // F = Diag(beta) X
+constexpr int UB = FB + C * LV * 2;          // U~
+constexpr int ULB = UB + C * LV * 2;         // Diag(lambda) U~
+constexpr int DUB = ULB + C * LV * 2;        // dU~
+constexpr int DOB = DUB + C * LV * 2;        // dO
+constexpr int DOG = DOB + C * LV * 2;        // Diag(gamma) dO
+constexpr int DFB = DOG + C * LV * 2;        // dF
+constexpr int DFS = DFB + C * LV * 2;        // -Diag(gamma beta) dF
+constexpr int SMALL = DFS + C * LV * 2;      // fp32 vectors of C
+constexpr int NVEC = 11;   // gs bs gam lam nrm db dgam dlam dg gb dgc
+constexpr int BYTES = SMALL + NVEC * C * 4;
+static_assert(C * LC * 2 * 2 <= 2 * DK * LV * 2, "final tiles fit");
+static_assert(BYTES <= 232448, "shared memory");
+static_assert(QB % 16 == 0 && KB % 16 == 0 && TB % 16 == 0 && PB % 16 == 0 &&
+                  SB % 16 == 0 && DSB % 16 == 0 && FB % 16 == 0 &&
+                  UB % 16 == 0 && ULB % 16 == 0 && DUB % 16 == 0 &&
+                  DOB % 16 == 0 && DOG % 16 == 0 && DFB % 16 == 0 &&
+                  DFS % 16 == 0,
+              "ldmatrix rows are 16-byte aligned");
+
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], const void* p) {
+    asm volatile(
+        "ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+        : "r"(tc::smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], const void* p) {
+    asm volatile(
+        "ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, "
+        "[%4];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+        : "r"(tc::smem_u32(p)));
+}
+
+// A fragment (16 x 16) of the row-major tile at p (row stride ld elements):
+// A(m, k) = p[m ld + k].
+__device__ __forceinline__ void a_row(uint32_t (&a)[4], const bf16* p, int ld,
+                                      int lane) {
+    ldsm4(a, p + (lane & 15) * ld + (lane >> 4) * 8);
+}
+// A fragment of the transpose: A(m, k) = p[k ld + m].
+__device__ __forceinline__ void a_trn(uint32_t (&a)[4], const bf16* p, int ld,
+                                      int lane) {
+    const int i = lane >> 3;
+    ldsm4t(a, p + ((i >> 1) * 8 + (lane & 7)) * ld + (i & 1) * 8);
+}
+// B fragments of two adjacent 16 x 8 tiles (columns n .. n + 15) of the
+// row-major tile at p: B(k, n) = p[k ld + n]; b[0..1] the first, b[2..3]
+// the second.
+__device__ __forceinline__ void b_row2(uint32_t (&b)[4], const bf16* p, int ld,
+                                       int lane) {
+    const int i = lane >> 3;
+    ldsm4t(b, p + ((i & 1) * 8 + (lane & 7)) * ld + (i >> 1) * 8);
+}
+// The same for B(k, n) = p[n ld + k] (the tile holds B's columns as rows).
+__device__ __forceinline__ void b_col2(uint32_t (&b)[4], const bf16* p, int ld,
+                                       int lane) {
+    const int i = lane >> 3;
+    ldsm4(b, p + ((i >> 1) * 8 + (lane & 7)) * ld + (i & 1) * 8);
+}
+__device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4],
+                                    uint32_t b0, uint32_t b1) {
+    tc::mma_m16n8k16(d, a, b0, b1);
+}
+__device__ __forceinline__ float bf(const bf16* p, int i) {
+    return __bfloat162float(p[i]);
+}
+// Sum over the four lanes that share a fragment row (lane >> 2).
+__device__ __forceinline__ float quad_sum(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    return x;
+}
+}  // namespace lm
+
+template <typename IO>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+kla_bwd_grad_lm_kernel(BwdArgs a) {
+    using namespace lm;
+    extern __shared__ __align__(16) uint8_t smraw[];
+    bf16* Qb = reinterpret_cast<bf16*>(smraw + QB);
+    bf16* Kb = reinterpret_cast<bf16*>(smraw + KB);
+    bf16* Tb = reinterpret_cast<bf16*>(smraw + TB);
+    bf16* Pb = reinterpret_cast<bf16*>(smraw + PB);
+    float* F0f = reinterpret_cast<float*>(smraw + F0);
+    float* F1f = reinterpret_cast<float*>(smraw + F1);
+    float* F2f = reinterpret_cast<float*>(smraw + F2);
+    bf16* Sb = reinterpret_cast<bf16*>(smraw + SB);
+    bf16* dSb = reinterpret_cast<bf16*>(smraw + DSB);
+    float* Xf = reinterpret_cast<float*>(smraw + XF);
+    float* KSf = reinterpret_cast<float*>(smraw + KSF);
+    float* Uf = reinterpret_cast<float*>(smraw + UF);
+    bf16* Fb = reinterpret_cast<bf16*>(smraw + FB);
+    bf16* Ub = reinterpret_cast<bf16*>(smraw + UB);
+    bf16* Ulb = reinterpret_cast<bf16*>(smraw + ULB);
+    bf16* dUb = reinterpret_cast<bf16*>(smraw + DUB);
+    bf16* dOb = reinterpret_cast<bf16*>(smraw + DOB);
+    bf16* dOg = reinterpret_cast<bf16*>(smraw + DOG);
+    bf16* dFb = reinterpret_cast<bf16*>(smraw + DFB);
+    bf16* dFs = reinterpret_cast<bf16*>(smraw + DFS);
+    float* vec = reinterpret_cast<float*>(smraw + SMALL);
+    float* gs = vec;             // cumulative log decay
+    float* bs = vec + C;         // beta (eta on entry)
+    float* gam = vec + 2 * C;
+    float* lam = vec + 3 * C;
+    float* nrm = vec + 4 * C;
+    float* db = vec + 5 * C;     // dbeta, later dn
+    float* dgam = vec + 6 * C;
+    float* dlam = vec + 7 * C;
+    float* dg = vec + 8 * C;
+    float* gb = vec + 9 * C;     // -gamma beta
+    float* dgc = vec + 10 * C;   // <dS', S>
+    // the final phase's bf16 tiles over S and dS'
+    bf16* Gdp = Sb;              // Gamma o dP (C x C)
+    bf16* Ddt = dSb;             // D + D^T
+
+    const int T = a.T, H = a.H, dv = a.dv;
     const int nch = (T + C - 1) / C;
     const long blk = blockIdx.x;
     const int bh = (int)(blk / nch), ch = (int)(blk % nch);
@@ -1150,60 +1213,108 @@ kla_bwd_grad_mma_kernel(BwdArgs a) {
     const float* Sg = a.ckpt + ((size_t)bh * nch + ch) * DK * dv;
     const float* dSg = a.dsck + ((size_t)bh * nch + ch) * DK * dv;
 
-    {   // q, k rows: 16-byte loads (8 bf16), all issued before the stores
-        uint4 qv[4], kv[4];
+    {   // q, k rows (bf16, 16-byte loads straight to shared memory), gates
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int idx = tid + u * kBwdThreads;   // 64 rows x 16 chunks
             const int r = idx >> 4, c8 = idx & 15;
             const int t = t0 + r;
-            qv[u] = kv[u] = make_uint4(0, 0, 0, 0);
+            uint4 qv = make_uint4(0, 0, 0, 0), kv = make_uint4(0, 0, 0, 0);
             if (t < T) {
                 const size_t off = (((size_t)b * T + t) * H + h) * DK + 8 * c8;
-                qv[u] = *reinterpret_cast<const uint4*>(
+                qv = *reinterpret_cast<const uint4*>(
                     static_cast<const IO*>(a.q) + off);
-                kv[u] = *reinterpret_cast<const uint4*>(
+                kv = *reinterpret_cast<const uint4*>(
                     static_cast<const IO*>(a.k) + off);
             }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int idx = tid + u * kBwdThreads;
-            const int r = idx >> 4, c8 = idx & 15;
-            const uint32_t qw[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
-            const uint32_t kw[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                Qs[r * LDK + 8 * c8 + 2 * e] = __uint_as_float(qw[e] << 16);
-                Qs[r * LDK + 8 * c8 + 2 * e + 1] =
-                    __uint_as_float(qw[e] & 0xffff0000u);
-                Ks[r * LDK + 8 * c8 + 2 * e] = __uint_as_float(kw[e] << 16);
-                Ks[r * LDK + 8 * c8 + 2 * e + 1] =
-                    __uint_as_float(kw[e] & 0xffff0000u);
-            }
+            *reinterpret_cast<uint4*>(Qb + r * LQ + 8 * c8) = qv;
+            *reinterpret_cast<uint4*>(Kb + r * LQ + 8 * c8) = kv;
         }
         if (tid < C) {
             const int t = t0 + tid;
             const size_t off = ((size_t)b * T + t) * H + h;
             gs[tid] = t < T ? a.log_alpha[off] : 0.f;
             bs[tid] = t < T ? a.eta[off] : 0.f;
+            db[tid] = dgam[tid] = dlam[tid] = 0.f;
+        }
+        if (tid == 0) dgc[0] = 0.f;
+        // zero P (its upper part is never written) and the final phase's
+        // Gamma o dP happens over S later (cleared there)
+        for (int i = tid; i < C * LC / 2; i += kBwdThreads)
+            reinterpret_cast<uint32_t*>(Pb)[i] = 0u;
+    }
+    __syncthreads();
+    {   // ||k||^2 (four threads per row), beta, cumulative decay
+        const int r = tid >> 2, q4 = tid & 3;
+        float n = 0.f;
+#pragma unroll 8
+        for (int c = 32 * q4; c < 32 * q4 + 32; ++c) {
+            const float x = bf(Kb, r * LQ + c);
+            n = fmaf(x, x, n);
+        }
+        n = quad_sum(n);
+        if (q4 == 0) {
+            nrm[r] = n;
+            const float denom = n + a.eps;
+            if (!a.gdn) bs[r] = denom == 0.f ? 0.f : bs[r] / denom;
+        }
+        if (warp == 0) {   // inclusive scan of the 64 log decays
+            float x0 = gs[2 * lane], x1 = gs[2 * lane + 1];
+            float s = x0 + x1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, s, off);
+                if (lane >= off) s += y;
+            }
+            gs[2 * lane] = s - x1;
+            gs[2 * lane + 1] = s;
         }
     }
-    for (int idx = tid; idx < C * LDC; idx += kBwdThreads) {
-        dP[idx] = 0.f;
-        dA[idx] = 0.f;
-    }
-    if (tid < kBwdMaxC) {
-        db[tid] = 0.f;
-        dgam[tid] = 0.f;
-        dlam[tid] = 0.f;
-    }
-    if (tid == 0) dgc[0] = 0.f;
     __syncthreads();
-    chunk_gates<DK>(a, Ks, LDK, gs, bs, gam, lam, nrm);
-    build_a_p<DK, kBwdThreads>(C, Qs, Ks, Ks, LDK, gs, bs, As, Ps, LDC);
+    if (tid < C) {
+        gam[tid] = expf(gs[tid]);
+        lam[tid] = expf(gs[C - 1] - gs[tid]);
+        gb[tid] = -gam[tid] * bs[tid];
+    }
+    // A (unit lower, fp32, into F0) and P (bf16) from K K^T and Q K^T on the
+    // tensor cores: the 20 lower 16 x 8 tiles, dealt out to the warps
+    for (int idx = warp; idx < 20; idx += 8) {
+        int mt, nt;
+        lower_tile(idx, mt, nt);
+        float qk[4] = {0.f, 0.f, 0.f, 0.f}, kk[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < DK / 16; ++ks) {
+            uint32_t aq[4], ak[4], bk[4];
+            a_row(aq, Qb + 16 * mt * LQ + 16 * ks, LQ, lane);
+            a_row(ak, Kb + 16 * mt * LQ + 16 * ks, LQ, lane);
+            // K^T columns 8 nt .. 8 nt + 7 (and the next 8, unused)
+            b_col2(bk, Kb + 8 * nt * LQ + 16 * ks, LQ, lane);
+            mma(qk, aq, bk[0], bk[1]);
+            mma(kk, ak, bk[0], bk[1]);
+        }
+#pragma unroll
+        for (int hm = 0; hm < 2; ++hm) {
+            const int r = 16 * mt + g8 + 8 * hm;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int i = 8 * nt + 2 * t4 + e;
+                float av = i == r ? 1.f : 0.f, pv = 0.f;
+                if (i <= r) {
+                    const float dec = expf(gs[r] - gs[i]);
+                    pv = dec * qk[2 * hm + e];
+                    if (i < r) av = bs[r] * dec * kk[2 * hm + e];
+                }
+                F0f[r * LF + i] = av;
+                Pb[r * LC + i] = __float2bfloat16_rn(pv);
+            }
+        }
+    }
     __syncthreads();
-    invert_unit_lower<kBwdThreads>(As, Tm, C, LDC);   // lower part of Tm
+    invert_unit_lower<kBwdThreads>(F0f, F1f, C, LF);   // lower part of F1
+    for (int i = tid; i < C * C; i += kBwdThreads) {   // T (bf16, lower)
+        const int r = i >> 6, c = i & 63;
+        Tb[r * LC + c] = __float2bfloat16_rn(c <= r ? F1f[r * LF + c] : 0.f);
+    }
 
     // dq, dk of this warp's rows 16 mo .. and columns 64 co .. (fragments)
     const int mo = warp & 3, co = 64 * (warp >> 2);
@@ -1212,17 +1323,21 @@ kla_bwd_grad_mma_kernel(BwdArgs a) {
     for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) dq[nt][e] = dk[nt][e] = 0.f;
-    // row scales -gamma_r beta_r in dg (free until the per-row step)
-    if (tid < C) dg[tid] = -gam[tid] * bs[tid];
+    // dP, dA of this warp's lower tiles (idx = warp, warp + 8, warp + 16)
+    float dPa[3][4], dAa[3][4];
+#pragma unroll
+    for (int x = 0; x < 3; ++x)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dPa[x][e] = dAa[x][e] = 0.f;
+    // this warp's two 16 x 8 tiles of the C x DVT products: rows 16 (w >> 1),
+    // columns 16 (w & 1) .. + 15
+    const int pm = warp >> 1, pn = 16 * (warp & 1);
+    float sdot = 0.f;
     __syncthreads();
-    const float* sgd = gam + 16 * mo;   // row scales of this warp's rows
-    const float* sgb = dg + 16 * mo;
-    const float* sl = lam + 16 * mo;
 
     for (int j0 = 0; j0 < dv; j0 += DVT) {
-        {   // S, dS' (128 x 32 fp32: 4 float4 each per thread), V, dO
-            // (64 x 32 bf16: one 16-byte load each): every load issued
-            // before the shared-memory stores
+        {   // S, dS' (DK x DVT fp32 -> bf16), V (fp32), dO (bf16, and
+            // Diag(gamma) dO): every load issued before the stores
             float4 sv[4], dsv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -1244,222 +1359,284 @@ kla_bwd_grad_mma_kernel(BwdArgs a) {
                 dov = *reinterpret_cast<const uint4*>(
                     static_cast<const IO*>(a.dout) + off);
             }
-            float sdot = 0.f;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int idx = tid + u * kBwdThreads;
                 const int c = idx >> 3, j = 4 * (idx & 7);
-                const float s4[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
-                const float d4[4] = {dsv[u].x, dsv[u].y, dsv[u].z, dsv[u].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    St[c * LDV + j + e] = s4[e];
-                    dSt[c * LDV + j + e] = d4[e];
-                    sdot = fmaf(s4[e], d4[e], sdot);
-                }
+                sdot = fmaf(sv[u].x, dsv[u].x, sdot);
+                sdot = fmaf(sv[u].y, dsv[u].y, sdot);
+                sdot = fmaf(sv[u].z, dsv[u].z, sdot);
+                sdot = fmaf(sv[u].w, dsv[u].w, sdot);
+                uint2 s2, d2;
+                s2.x = tc::pack_bf16x2(sv[u].x, sv[u].y);
+                s2.y = tc::pack_bf16x2(sv[u].z, sv[u].w);
+                d2.x = tc::pack_bf16x2(dsv[u].x, dsv[u].y);
+                d2.y = tc::pack_bf16x2(dsv[u].z, dsv[u].w);
+                *reinterpret_cast<uint2*>(Sb + c * LV + j) = s2;
+                *reinterpret_cast<uint2*>(dSb + c * LV + j) = d2;
             }
-            atomicAdd(dgc, sdot);
+            *reinterpret_cast<uint4*>(dOb + r * LV + 8 * j8) = dov;
             const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
             const uint32_t dw[4] = {dov.x, dov.y, dov.z, dov.w};
+            const float gr = gam[r];
+            uint4 dg4;
+            uint32_t* dgw = &dg4.x;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                Xs[r * LDV + 8 * j8 + 2 * e] = __uint_as_float(vw[e] << 16);
-                Xs[r * LDV + 8 * j8 + 2 * e + 1] =
+                Xf[r * LX + 8 * j8 + 2 * e] = __uint_as_float(vw[e] << 16);
+                Xf[r * LX + 8 * j8 + 2 * e + 1] =
                     __uint_as_float(vw[e] & 0xffff0000u);
-                Ds[r * LDV + 8 * j8 + 2 * e] = __uint_as_float(dw[e] << 16);
-                Ds[r * LDV + 8 * j8 + 2 * e + 1] =
-                    __uint_as_float(dw[e] & 0xffff0000u);
+                dgw[e] = tc::pack_bf16x2(gr * __uint_as_float(dw[e] << 16),
+                                         gr * __uint_as_float(dw[e] & 0xffff0000u));
             }
+            *reinterpret_cast<uint4*>(dOg + r * LV + 8 * j8) = dg4;
         }
         __syncthreads();
 
-        // K S, Q S: X = V - Diag(gamma) K S, F = Diag(beta) X (into W),
+        // K S, Q S: X = V - Diag(gamma) K S, F = Diag(beta) X,
         // dgamma += dO . Q S
-        for (int tile = warp; tile < 16; tile += 8) {
-            const int mt = tile >> 2, nt = tile & 3;
-            float ks[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            float ks[2][4] = {}, qs[2][4] = {};
 #pragma unroll
             for (int kk = 0; kk < DK / 16; ++kk) {
-                uint32_t ak[4], aq[4], b0, b1;
-                frag_a(ak, Ks + 16 * mt * LDK + 16 * kk, LDK, 1, lane);
-                frag_a(aq, Qs + 16 * mt * LDK + 16 * kk, LDK, 1, lane);
-                frag_b(b0, b1, St + 16 * kk * LDV + 8 * nt, LDV, 1, lane);
-                mma_step(ks, ak, b0, b1);
-                mma_step(qs, aq, b0, b1);
+                uint32_t ak[4], aq[4], bs4[4];
+                a_row(ak, Kb + 16 * pm * LQ + 16 * kk, LQ, lane);
+                a_row(aq, Qb + 16 * pm * LQ + 16 * kk, LQ, lane);
+                b_row2(bs4, Sb + 16 * kk * LV + pn, LV, lane);
+                mma(ks[0], ak, bs4[0], bs4[1]);
+                mma(ks[1], ak, bs4[2], bs4[3]);
+                mma(qs[0], aq, bs4[0], bs4[1]);
+                mma(qs[1], aq, bs4[2], bs4[3]);
             }
 #pragma unroll
             for (int hm = 0; hm < 2; ++hm) {
-                const int r = 16 * mt + g8 + 8 * hm;
+                const int r = 16 * pm + g8 + 8 * hm;
                 float dgp = 0.f;
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int j = 8 * nt + 2 * t4 + e;
-                    const float v = ks[2 * hm + e];
-                    KS[r * LDV + j] = v;
-                    const float x = fmaf(-gam[r], v, Xs[r * LDV + j]);
-                    Xs[r * LDV + j] = x;
-                    Ws[r * LDV + j] = bs[r] * x;
-                    dgp = fmaf(Ds[r * LDV + j], qs[2 * hm + e], dgp);
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int j = pn + 8 * nt + 2 * t4;
+                    float xs[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float v = ks[nt][2 * hm + e];
+                        KSf[r * LX + j + e] = v;
+                        const float x = fmaf(-gam[r], v, Xf[r * LX + j + e]);
+                        Xf[r * LX + j + e] = x;
+                        xs[e] = bs[r] * x;
+                        dgp = fmaf(bf(dOb, r * LV + j + e), qs[nt][2 * hm + e],
+                                   dgp);
+                    }
+                    *reinterpret_cast<uint32_t*>(Fb + r * LV + j) =
+                        tc::pack_bf16x2(xs[0], xs[1]);
                 }
-                atomicAdd(&dgam[r], dgp);
+                dgp = quad_sum(dgp);
+                if (t4 == 0) atomicAdd(&dgam[r], dgp);
             }
         }
         __syncthreads();
 
         // U~ = T F (T lower triangular)
-        for (int tile = warp; tile < 16; tile += 8) {
-            const int mt = tile >> 2, nt = tile & 3;
-            float u[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int kk = 0; kk <= mt; ++kk) {
-                uint32_t at[4], b0, b1;
-                frag_a(at, Tm + 16 * mt * LDC + 16 * kk, LDC, 1, lane, nullptr,
-                       kk == mt ? 1 : 0);
-                frag_b(b0, b1, Ws + 16 * kk * LDV + 8 * nt, LDV, 1, lane);
-                mma_step(u, at, b0, b1);
+        {
+            float u[2][4] = {};
+            for (int kk = 0; kk <= pm; ++kk) {
+                uint32_t at[4], bf4[4];
+                a_row(at, Tb + 16 * pm * LC + 16 * kk, LC, lane);
+                b_row2(bf4, Fb + 16 * kk * LV + pn, LV, lane);
+                mma(u[0], at, bf4[0], bf4[1]);
+                mma(u[1], at, bf4[2], bf4[3]);
             }
 #pragma unroll
-            for (int hm = 0; hm < 2; ++hm)
+            for (int hm = 0; hm < 2; ++hm) {
+                const int r = 16 * pm + g8 + 8 * hm;
+                const float lr = lam[r];
 #pragma unroll
-                for (int e = 0; e < 2; ++e)
-                    Us[(16 * mt + g8 + 8 * hm) * LDV + 8 * nt + 2 * t4 + e] =
-                        u[2 * hm + e];
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int j = pn + 8 * nt + 2 * t4;
+                    const float u0 = u[nt][2 * hm], u1 = u[nt][2 * hm + 1];
+                    Uf[r * LX + j] = u0;
+                    Uf[r * LX + j + 1] = u1;
+                    *reinterpret_cast<uint32_t*>(Ub + r * LV + j) =
+                        tc::pack_bf16x2(u0, u1);
+                    *reinterpret_cast<uint32_t*>(Ulb + r * LV + j) =
+                        tc::pack_bf16x2(lr * u0, lr * u1);
+                }
+            }
         }
         __syncthreads();
 
-        // dU~ = P^T dO + Diag(lambda) K dS' (into W); dlambda_r = (K dS')_r.U~_r
-        for (int tile = warp; tile < 16; tile += 8) {
-            const int mt = tile >> 2, nt = tile & 3;
-            float kd[4] = {0.f, 0.f, 0.f, 0.f}, pd[4] = {0.f, 0.f, 0.f, 0.f};
+        // dU~ = P^T dO + Diag(lambda) K dS';  dlambda_r += (K dS')_r . U~_r
+        {
+            float kd[2][4] = {}, pd[2][4] = {};
 #pragma unroll
             for (int kk = 0; kk < DK / 16; ++kk) {
-                uint32_t ak[4], b0, b1;
-                frag_a(ak, Ks + 16 * mt * LDK + 16 * kk, LDK, 1, lane);
-                frag_b(b0, b1, dSt + 16 * kk * LDV + 8 * nt, LDV, 1, lane);
-                mma_step(kd, ak, b0, b1);
+                uint32_t ak[4], bd4[4];
+                a_row(ak, Kb + 16 * pm * LQ + 16 * kk, LQ, lane);
+                b_row2(bd4, dSb + 16 * kk * LV + pn, LV, lane);
+                mma(kd[0], ak, bd4[0], bd4[1]);
+                mma(kd[1], ak, bd4[2], bd4[3]);
             }
-            for (int kk = mt; kk < 4; ++kk) {   // P^T(r, i) = P(i, r), i >= r
-                uint32_t ap[4], b0, b1;
-                frag_a(ap, Ps + 16 * kk * LDC + 16 * mt, 1, LDC, lane);
-                frag_b(b0, b1, Ds + 16 * kk * LDV + 8 * nt, LDV, 1, lane);
-                mma_step(pd, ap, b0, b1);
+            for (int kk = pm; kk < C / 16; ++kk) {   // P^T(r, i) = P(i, r)
+                uint32_t ap[4], bo4[4];
+                a_trn(ap, Pb + 16 * kk * LC + 16 * pm, LC, lane);
+                b_row2(bo4, dOb + 16 * kk * LV + pn, LV, lane);
+                mma(pd[0], ap, bo4[0], bo4[1]);
+                mma(pd[1], ap, bo4[2], bo4[3]);
             }
 #pragma unroll
             for (int hm = 0; hm < 2; ++hm) {
-                const int r = 16 * mt + g8 + 8 * hm;
+                const int r = 16 * pm + g8 + 8 * hm;
+                const float lr = lam[r];
                 float dlp = 0.f;
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int j = 8 * nt + 2 * t4 + e;
-                    Ws[r * LDV + j] = fmaf(lam[r], kd[2 * hm + e], pd[2 * hm + e]);
-                    dlp = fmaf(kd[2 * hm + e], Us[r * LDV + j], dlp);
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int j = pn + 8 * nt + 2 * t4;
+                    const float k0 = kd[nt][2 * hm], k1 = kd[nt][2 * hm + 1];
+                    *reinterpret_cast<uint32_t*>(dUb + r * LV + j) =
+                        tc::pack_bf16x2(fmaf(lr, k0, pd[nt][2 * hm]),
+                                        fmaf(lr, k1, pd[nt][2 * hm + 1]));
+                    dlp = fmaf(k0, Uf[r * LX + j], dlp);
+                    dlp = fmaf(k1, Uf[r * LX + j + 1], dlp);
                 }
-                atomicAdd(&dlam[r], dlp);
+                dlp = quad_sum(dlp);
+                if (t4 == 0) atomicAdd(&dlam[r], dlp);
             }
         }
         __syncthreads();
 
-        // dF = T^T dU~ (into the K S slots, once read); dV = Diag(beta) dF;
-        // dbeta from F = Diag(beta) X; dgamma from X
-        for (int tile = warp; tile < 16; tile += 8) {
-            const int mt = tile >> 2, nt = tile & 3;
-            float df[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int kk = mt; kk < 4; ++kk) {   // T^T(r, i) = T(i, r), i >= r
-                uint32_t at[4], b0, b1;
-                frag_a(at, Tm + 16 * kk * LDC + 16 * mt, 1, LDC, lane, nullptr,
-                       kk == mt ? 2 : 0);
-                frag_b(b0, b1, Ws + 16 * kk * LDV + 8 * nt, LDV, 1, lane);
-                mma_step(df, at, b0, b1);
+        // dF = T^T dU~; dV = Diag(beta) dF; dbeta += dF . X;
+        // dgamma -= dX . K S
+        {
+            float df[2][4] = {};
+            for (int kk = pm; kk < C / 16; ++kk) {   // T^T(r, i) = T(i, r)
+                uint32_t at[4], bu4[4];
+                a_trn(at, Tb + 16 * kk * LC + 16 * pm, LC, lane);
+                b_row2(bu4, dUb + 16 * kk * LV + pn, LV, lane);
+                mma(df[0], at, bu4[0], bu4[1]);
+                mma(df[1], at, bu4[2], bu4[3]);
             }
 #pragma unroll
             for (int hm = 0; hm < 2; ++hm) {
-                const int r = 16 * mt + g8 + 8 * hm;
+                const int r = 16 * pm + g8 + 8 * hm;
                 const int t = t0 + r;
+                const float br = bs[r], gbr = gb[r];
                 float dbp = 0.f, dgp = 0.f;
-                float dx2[2];
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int j = 8 * nt + 2 * t4 + e;
-                    const float dfv = df[2 * hm + e];
-                    const float dx = bs[r] * dfv;
-                    dx2[e] = dx;
-                    dbp = fmaf(dfv, Xs[r * LDV + j], dbp);
-                    dgp = fmaf(-dx, KS[r * LDV + j], dgp);
-                    KS[r * LDV + j] = dfv;
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int j = pn + 8 * nt + 2 * t4;
+                    const float f0 = df[nt][2 * hm], f1 = df[nt][2 * hm + 1];
+                    const float x0 = br * f0, x1 = br * f1;
+                    dbp = fmaf(f0, Xf[r * LX + j], dbp);
+                    dbp = fmaf(f1, Xf[r * LX + j + 1], dbp);
+                    dgp = fmaf(-x0, KSf[r * LX + j], dgp);
+                    dgp = fmaf(-x1, KSf[r * LX + j + 1], dgp);
+                    *reinterpret_cast<uint32_t*>(dFb + r * LV + j) =
+                        tc::pack_bf16x2(f0, f1);
+                    *reinterpret_cast<uint32_t*>(dFs + r * LV + j) =
+                        tc::pack_bf16x2(gbr * f0, gbr * f1);
+                    if (t < T) {
+                        const size_t off =
+                            (((size_t)b * T + t) * H + h) * dv + j0 + j;
+                        static_cast<IO*>(a.dv_)[off] = from_f32<IO>(x0);
+                        static_cast<IO*>(a.dv_)[off + 1] = from_f32<IO>(x1);
+                    }
                 }
-                if (t < T) {
-                    const size_t off = (((size_t)b * T + t) * H + h) * dv +
-                                       j0 + 8 * nt + 2 * t4;
-                    static_cast<IO*>(a.dv_)[off] = from_f32<IO>(dx2[0]);
-                    static_cast<IO*>(a.dv_)[off + 1] = from_f32<IO>(dx2[1]);
+                dbp = quad_sum(dbp);
+                dgp = quad_sum(dgp);
+                if (t4 == 0) {
+                    atomicAdd(&db[r], dbp);
+                    atomicAdd(&dgam[r], dgp);
                 }
-                atomicAdd(&db[r], dbp);
-                atomicAdd(&dgam[r], dgp);
             }
         }
         __syncthreads();
 
-        // dP += dO U~^T (i <= r), dA -= dF U~^T (i < r): lower tiles
-        for (int idx = warp; idx < 20; idx += 8) {
+        // dP += dO U~^T, dA -= dF U~^T (this warp's lower tiles, registers)
+#pragma unroll
+        for (int x = 0; x < 3; ++x) {
+            const int idx = warp + 8 * x;
+            if (idx >= 20) break;
             int mt, nt;
             lower_tile(idx, mt, nt);
-            float ap[4] = {0.f, 0.f, 0.f, 0.f}, aa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kk = 0; kk < DVT / 16; ++kk) {
-                uint32_t ad[4], af[4], b0, b1;
-                frag_a(ad, Ds + 16 * mt * LDV + 16 * kk, LDV, 1, lane);
-                frag_a(af, KS + 16 * mt * LDV + 16 * kk, LDV, 1, lane);
-                // B(j, i) = U~(i, j)
-                frag_b(b0, b1, Us + 8 * nt * LDV + 16 * kk, 1, LDV, lane);
-                mma_step(ap, ad, b0, b1);
-                mma_step(aa, af, b0, b1);
+                uint32_t ad[4], af[4], bu[4];
+                a_row(ad, dOb + 16 * mt * LV + 16 * kk, LV, lane);
+                a_row(af, dFb + 16 * mt * LV + 16 * kk, LV, lane);
+                // B(j, i) = U~(i, j): U~ rows 8 nt .. (and the next 8, unused)
+                b_col2(bu, Ub + 8 * nt * LV + 16 * kk, LV, lane);
+                mma(dPa[x], ad, bu[0], bu[1]);
+                mma(dAa[x], af, bu[0], bu[1]);
             }
-#pragma unroll
-            for (int hm = 0; hm < 2; ++hm)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int r = 16 * mt + g8 + 8 * hm;
-                    const int i = 8 * nt + 2 * t4 + e;
-                    if (i <= r) dP[r * LDC + i] += ap[2 * hm + e];
-                    if (i < r) dA[r * LDC + i] -= aa[2 * hm + e];
-                }
         }
-        // dq += Diag(gamma) dO S^T; dk += Diag(lambda) U~ dS'^T
-        //                               - Diag(gamma beta) dF S^T
+        // dq += Diag(gamma) dO S^T;
+        // dk += Diag(lambda) U~ dS'^T - Diag(gamma beta) dF S^T
 #pragma unroll
         for (int kk = 0; kk < DVT / 16; ++kk) {
             uint32_t ad[4], au[4], af[4];
-            frag_a(ad, Ds + 16 * mo * LDV + 16 * kk, LDV, 1, lane, sgd);
-            frag_a(au, Us + 16 * mo * LDV + 16 * kk, LDV, 1, lane, sl);
-            frag_a(af, KS + 16 * mo * LDV + 16 * kk, LDV, 1, lane, sgb);
+            a_row(ad, dOg + 16 * mo * LV + 16 * kk, LV, lane);
+            a_row(au, Ulb + 16 * mo * LV + 16 * kk, LV, lane);
+            a_row(af, dFs + 16 * mo * LV + 16 * kk, LV, lane);
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                const int c0 = co + 8 * nt;
-                uint32_t bs0, bs1, bd0, bd1;
+            for (int np = 0; np < 4; ++np) {   // pairs of 8-column tiles
+                const int c0 = co + 16 * np;
+                uint32_t bs4[4], bd4[4];
                 // B(j, c) = S(c, j)
-                frag_b(bs0, bs1, St + c0 * LDV + 16 * kk, 1, LDV, lane);
-                frag_b(bd0, bd1, dSt + c0 * LDV + 16 * kk, 1, LDV, lane);
-                mma_step(dq[nt], ad, bs0, bs1);
-                mma_step(dk[nt], au, bd0, bd1);
-                mma_step(dk[nt], af, bs0, bs1);
+                b_col2(bs4, Sb + c0 * LV + 16 * kk, LV, lane);
+                b_col2(bd4, dSb + c0 * LV + 16 * kk, LV, lane);
+#pragma unroll
+                for (int hn = 0; hn < 2; ++hn) {
+                    mma(dq[2 * np + hn], ad, bs4[2 * hn], bs4[2 * hn + 1]);
+                    mma(dk[2 * np + hn], au, bd4[2 * hn], bd4[2 * hn + 1]);
+                    mma(dk[2 * np + hn], af, bs4[2 * hn], bs4[2 * hn + 1]);
+                }
             }
         }
         __syncthreads();
     }
+    {   // <dS', S> over the whole state
+        float s = sdot;
+#pragma unroll
+        for (int off = 16; off; off >>= 1)
+            s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) atomicAdd(dgc, s);
+    }
+    // dP (lower incl.) into F0, dA (strictly lower) into F1, zeros above
+    for (int i = tid; i < C * LF; i += kBwdThreads) F0f[i] = F1f[i] = 0.f;
+    for (int i = tid; i < C * LC / 2; i += kBwdThreads)
+        reinterpret_cast<uint32_t*>(Gdp)[i] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int x = 0; x < 3; ++x) {
+        const int idx = warp + 8 * x;
+        if (idx >= 20) break;
+        int mt, nt;
+        lower_tile(idx, mt, nt);
+#pragma unroll
+        for (int hm = 0; hm < 2; ++hm)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = 16 * mt + g8 + 8 * hm;
+                const int i = 8 * nt + 2 * t4 + e;
+                if (i <= r) F0f[r * LF + i] = dPa[x][2 * hm + e];
+                if (i < r) F1f[r * LF + i] = -dAa[x][2 * hm + e];
+            }
+    }
+    __syncthreads();
 
-    // dGamma o Gamma (into A), Gamma o dP (into dP), D (into dA), and the
+    // dGamma o Gamma (F2), Gamma o dP (bf16), D (over dA in F1) and the
     // A-part of dbeta, from Q K^T and K K^T of the lower tiles
     for (int idx = warp; idx < 20; idx += 8) {
         int mt, nt;
         lower_tile(idx, mt, nt);
         float qk[4] = {0.f, 0.f, 0.f, 0.f}, kk4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int kk = 0; kk < DK / 16; ++kk) {
-            uint32_t aq[4], ak[4], b0, b1;
-            frag_a(aq, Qs + 16 * mt * LDK + 16 * kk, LDK, 1, lane);
-            frag_a(ak, Ks + 16 * mt * LDK + 16 * kk, LDK, 1, lane);
-            frag_b(b0, b1, Ks + 8 * nt * LDK + 16 * kk, 1, LDK, lane);   // K^T
-            mma_step(qk, aq, b0, b1);
-            mma_step(kk4, ak, b0, b1);
+        for (int ks = 0; ks < DK / 16; ++ks) {
+            uint32_t aq[4], ak[4], bk[4];
+            a_row(aq, Qb + 16 * mt * LQ + 16 * ks, LQ, lane);
+            a_row(ak, Kb + 16 * mt * LQ + 16 * ks, LQ, lane);
+            b_col2(bk, Kb + 8 * nt * LQ + 16 * ks, LQ, lane);
+            mma(qk, aq, bk[0], bk[1]);
+            mma(kk4, ak, bk[0], bk[1]);
         }
 #pragma unroll
         for (int hm = 0; hm < 2; ++hm) {
@@ -1471,32 +1648,33 @@ kla_bwd_grad_mma_kernel(BwdArgs a) {
                 float dgg = 0.f, dpt = 0.f, dd = 0.f;
                 if (i <= r) {
                     const float gmm = expf(gs[r] - gs[i]);
-                    const float dpv = dP[r * LDC + i];
+                    const float dpv = F0f[r * LF + i];
                     float dgm = dpv * qk[2 * hm + e];
                     dpt = gmm * dpv;
                     if (i < r) {
-                        const float dav = dA[r * LDC + i];
+                        const float dav = F1f[r * LF + i];
                         dgm = fmaf(dav * bs[r], kk4[2 * hm + e], dgm);
                         dd = bs[r] * gmm * dav;
                         dbp = fmaf(dav * gmm, kk4[2 * hm + e], dbp);
                     }
                     dgg = dgm * gmm;
                 }
-                As[r * LDC + i] = dgg;
-                dP[r * LDC + i] = dpt;
-                dA[r * LDC + i] = dd;
+                F2f[r * LF + i] = dgg;
+                Gdp[r * LC + i] = __float2bfloat16_rn(dpt);
+                F1f[r * LF + i] = dd;
             }
-            atomicAdd(&db[r], dbp);
+            dbp = quad_sum(dbp);
+            if (t4 == 0) atomicAdd(&db[r], dbp);
         }
     }
     __syncthreads();
 
-    // per row: dg, deta, dn (dn replaces dbeta in db)
+    // per row: dg, deta, dn (dn replaces dbeta in db); D + D^T (bf16)
     if (tid < C) {
         const int r = tid;
         float gsum = dgam[r] * gam[r] - dlam[r] * lam[r];
-        for (int i = 0; i <= r; ++i) gsum += As[r * LDC + i];
-        for (int rr = r; rr < C; ++rr) gsum -= As[rr * LDC + r];
+        for (int i = 0; i <= r; ++i) gsum += F2f[r * LF + i];
+        for (int rr = r; rr < C; ++rr) gsum -= F2f[rr * LF + r];
         if (r == C - 1) {
             for (int t = 0; t < C; ++t) gsum = fmaf(dlam[t], lam[t], gsum);
             gsum = fmaf(dgc[0], gam[C - 1], gsum);
@@ -1515,6 +1693,11 @@ kla_bwd_grad_mma_kernel(BwdArgs a) {
         if (t < T) a.deta[((size_t)b * T + t) * H + h] = deta;
         db[r] = dn;
     }
+    for (int i = tid; i < C * C; i += kBwdThreads) {
+        const int r = i >> 6, c = i & 63;
+        Ddt[r * LC + c] =
+            __float2bfloat16_rn(F1f[r * LF + c] + F1f[c * LF + r]);
+    }
     __syncthreads();
     if (tid < C) {   // dlog_alpha_j = sum_{r >= j} dg_r
         float acc = 0.f;
@@ -1524,39 +1707,24 @@ kla_bwd_grad_mma_kernel(BwdArgs a) {
     }
 
     // dq += (Gamma o dP) K;  dk += (Gamma o dP)^T Q + (D + D^T) K
-    for (int kk = 0; kk < 4; ++kk) {
+    for (int kk = 0; kk < C / 16; ++kk) {
         uint32_t ap[4], apt[4], ad[4];
         const bool low = kk <= mo, up = kk >= mo;
-        if (low) frag_a(ap, dP + 16 * mo * LDC + 16 * kk, LDC, 1, lane);
-        if (up) frag_a(apt, dP + 16 * kk * LDC + 16 * mo, 1, LDC, lane);
-        {   // (D + D^T)(r, i) = D(r, i) + D(i, r)
-            const int g = lane >> 2, t = lane & 3;
-            float v[8];
-            const int ms[2] = {g, g + 8};
-            const int ks[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+        if (low) a_row(ap, Gdp + 16 * mo * LC + 16 * kk, LC, lane);
+        if (up) a_trn(apt, Gdp + 16 * kk * LC + 16 * mo, LC, lane);
+        a_row(ad, Ddt + 16 * mo * LC + 16 * kk, LC, lane);
 #pragma unroll
-            for (int hm = 0; hm < 2; ++hm)
+        for (int np = 0; np < 4; ++np) {
+            const int c0 = co + 16 * np;
+            uint32_t bk4[4], bq4[4];
+            b_row2(bk4, Kb + 16 * kk * LQ + c0, LQ, lane);
+            b_row2(bq4, Qb + 16 * kk * LQ + c0, LQ, lane);
 #pragma unroll
-                for (int hk = 0; hk < 2; ++hk)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int r = 16 * mo + ms[hm], i = 16 * kk + ks[2 * hk + e];
-                        v[4 * hk + 2 * hm + e] = dA[r * LDC + i] + dA[i * LDC + r];
-                    }
-            ad[0] = tc::pack_bf16x2(v[0], v[1]);
-            ad[1] = tc::pack_bf16x2(v[2], v[3]);
-            ad[2] = tc::pack_bf16x2(v[4], v[5]);
-            ad[3] = tc::pack_bf16x2(v[6], v[7]);
-        }
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            const int c0 = co + 8 * nt;
-            uint32_t bk0, bk1, bq0, bq1;
-            frag_b(bk0, bk1, Ks + 16 * kk * LDK + c0, LDK, 1, lane);
-            frag_b(bq0, bq1, Qs + 16 * kk * LDK + c0, LDK, 1, lane);
-            if (low) mma_step(dq[nt], ap, bk0, bk1);
-            if (up) mma_step(dk[nt], apt, bq0, bq1);
-            mma_step(dk[nt], ad, bk0, bk1);
+            for (int hn = 0; hn < 2; ++hn) {
+                if (low) mma(dq[2 * np + hn], ap, bk4[2 * hn], bk4[2 * hn + 1]);
+                if (up) mma(dk[2 * np + hn], apt, bq4[2 * hn], bq4[2 * hn + 1]);
+                mma(dk[2 * np + hn], ad, bk4[2 * hn], bk4[2 * hn + 1]);
+            }
         }
     }
 #pragma unroll
@@ -1573,9 +1741,9 @@ kla_bwd_grad_mma_kernel(BwdArgs a) {
             IO* k2 = static_cast<IO*>(a.dk_) + off;
             q2[0] = from_f32<IO>(dq[nt][2 * hm]);
             q2[1] = from_f32<IO>(dq[nt][2 * hm + 1]);
-            k2[0] = from_f32<IO>(fmaf(dn2, Ks[r * LDK + c], dk[nt][2 * hm]));
+            k2[0] = from_f32<IO>(fmaf(dn2, bf(Kb, r * LQ + c), dk[nt][2 * hm]));
             k2[1] = from_f32<IO>(
-                fmaf(dn2, Ks[r * LDK + c + 1], dk[nt][2 * hm + 1]));
+                fmaf(dn2, bf(Kb, r * LQ + c + 1), dk[nt][2 * hm + 1]));
         }
     }
 }
@@ -1624,12 +1792,11 @@ cudaError_t launch_shape(const BwdArgs& a, cudaStream_t stream) {
         // the per-chunk products on the tensor cores (16-byte loads of q,
         // k, v, o_grad)
         if (a.C == kTcC && a16(a.q) && a16(a.k) && a16(a.v) && a16(a.dout)) {
-            auto km = kla_bwd_grad_mma_kernel<IO>;
+            auto km = kla_bwd_grad_lm_kernel<IO>;
             e = cudaFuncSetAttribute(
-                km, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                (int)LG::BYTES);
+                km, cudaFuncAttributeMaxDynamicSharedMemorySize, lm::BYTES);
             if (e != cudaSuccess) return e;
-            km<<<(unsigned)(bhs * nch), kBwdThreads, LG::BYTES, stream>>>(a);
+            km<<<(unsigned)(bhs * nch), kBwdThreads, lm::BYTES, stream>>>(a);
             return cudaGetLastError();
         }
     }

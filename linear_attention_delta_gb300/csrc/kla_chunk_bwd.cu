@@ -26,10 +26,14 @@
 // section "Implementacion").
 //
 // Three launches: a forward pass writes the state at every chunk start
-// (ckpt; the tensor-core kernel where it applies, else the CUDA-core one); kla_bwd_state_kernel walks the chunks in reverse (one CTA per
-// (batch, head, dv tile): the recurrence for dS is column-separable) and
-// writes dS' of every chunk (dsck) and dh0; kla_bwd_grad_kernel then forms
-// every gradient of one chunk's tokens per CTA, all chunks in parallel.
+// (ckpt; the tensor-core kernel where it applies, else the CUDA-core one);
+// the reverse recurrence walks the chunks backwards (one CTA per (batch,
+// head, dv tile): the recurrence for dS is column-separable) and writes dS'
+// of every chunk (dsck) and dh0; the gradient kernel then forms every
+// gradient of one chunk's tokens per CTA, all chunks in parallel.  For bf16
+// with dk = 128 and C = 64 the last two run on the tensor cores
+// (kla_bwd_state_lm_kernel, kla_bwd_grad_lm_kernel), else on the CUDA cores
+// in fp32 (kla_bwd_state_kernel, kla_bwd_grad_kernel).
 #include <type_traits>
 
 #include "kla_internal.cuh"
@@ -293,53 +297,9 @@ kla_bwd_state_kernel(BwdArgs a) {
 }
 
 // ------------------------------------- reverse state recurrence, tensor cores
-// The bf16 case with dk = 128, 64-column dv slices and C = 64: the same
-// per-chunk algebra as kla_bwd_state_kernel, its products on the tensor
-// cores (mma.sync m16n8k8 with tf32 operands rounded to nearest and fp32
-// accumulation; tf32's 2^-11 relative rounding sits far inside the bf16
-// bound): A and P (their lower 16 x 8 tiles), dU~ = P^T dO + Diag(lambda)
-// K dS', dF = T^T dU~ and dS = gamma_C dS' + Q^T Diag(gamma) dO
-// - K^T Diag(gamma beta) dF.  Row strides of 136 and 72 floats make every
-// fragment load conflict-free.
+// The bf16 case with dk = 128, 64-column dv slices and C = 64 runs on the
+// tensor cores (kla_bwd_state_lm_kernel, below the gradient kernels).
 constexpr int kTcDK = 128, kTcDV = 64, kTcC = 64;
-
-struct StateTcSmem {
-    static constexpr int LDK = kTcDK + 8;
-    static constexpr int LDV = kTcDV + 8;
-    static constexpr int LDC = kTcC + 8;
-    static constexpr int Q = 0;
-    static constexpr int K = Q + kTcC * LDK;
-    static constexpr int DO = K + kTcC * LDK;
-    static constexpr int W = DO + kTcC * LDV;      // dU~
-    static constexpr int W2 = W + kTcC * LDV;      // dF
-    static constexpr int DS = W2 + kTcC * LDV;     // dS, key dim x dv
-    static constexpr int A = DS + kTcDK * LDV;
-    static constexpr int P = A + kTcC * LDC;
-    static constexpr int TM = P + kTcC * LDC;      // A^{-1}
-    static constexpr int G = TM + kTcC * LDC;
-    static constexpr int BETA = G + kTcC;
-    static constexpr int GAM = BETA + kTcC;
-    static constexpr int LAM = GAM + kTcC;
-    static constexpr int TOTAL = LAM + kTcC;
-    static constexpr size_t BYTES = sizeof(float) * (size_t)TOTAL;
-};
-
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-// d += a b for one 16 x 8 tile (a: 16 x 8 row fragment, b: 8 x 8 column
-// fragment; rows g, g + 8 and columns 2q, 2q + 1 of d per lane)
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
-                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 
 // The tensor-core recurrence applies: bf16, dk = 128, C = 64, dv a multiple
 // of 64, and q, k, dO 16-byte aligned (its tile loads are 16 bytes wide).
@@ -349,249 +309,6 @@ __host__ __forceinline__ bool state_tc_ok(const BwdArgs& a) {
     };
     return a.dtype == KLA_BF16 && a.dk == kTcDK && a.C == kTcC &&
            a.dv % kTcDV == 0 && al16(a.q) && al16(a.k) && al16(a.dout);
-}
-
-template <typename IO>
-__global__ void __launch_bounds__(kBwdThreads)
-kla_bwd_state_tc_kernel(BwdArgs a) {
-    using L = StateTcSmem;
-    constexpr int LDK = L::LDK, LDV = L::LDV, LDC = L::LDC, C = kTcC;
-    extern __shared__ float sm[];
-    float* Qs = sm + L::Q;
-    float* Ks = sm + L::K;
-    float* Ds = sm + L::DO;
-    float* Ws = sm + L::W;
-    float* W2 = sm + L::W2;
-    float* dS = sm + L::DS;
-    float* As = sm + L::A;
-    float* Ps = sm + L::P;
-    float* Tm = sm + L::TM;
-    float* gs = sm + L::G;
-    float* bs = sm + L::BETA;
-    float* gam = sm + L::GAM;
-    float* lam = sm + L::LAM;
-
-    const int bh = blockIdx.x;
-    const int b = bh / a.H, h = bh % a.H;
-    const int j0 = blockIdx.y * kTcDV;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, q = lane & 3;
-    const int T = a.T, H = a.H, dv = a.dv;
-    const int nch = (T + C - 1) / C;
-
-    for (int idx = tid; idx < kTcDK * kTcDV; idx += kBwdThreads) {
-        const int c = idx / kTcDV, j = idx % kTcDV;
-        dS[c * LDV + j] =
-            a.dhT ? a.dhT[((size_t)bh * kTcDK + c) * dv + j0 + j] : 0.f;
-    }
-    // P's tiles above the diagonal are never written: zero once
-    for (int idx = tid; idx < C * LDC; idx += kBwdThreads) Ps[idx] = 0.f;
-
-    // The tiles of a chunk (q, k: 64 x 128, dO: 64 x 64, bf16) and its gates
-    // are loaded into registers, 16 bytes a load, while the previous chunk
-    // computes, and stored to shared memory when it is done.
-    const uint4* q4 = static_cast<const uint4*>(a.q);
-    const uint4* k4 = static_cast<const uint4*>(a.k);
-    const uint4* d4 = static_cast<const uint4*>(a.dout);
-    uint4 pq[4], pk[4], pd[2];
-    float pla = 0.f, peta = 0.f;
-    auto fetch = [&](int c) {
-        const int t0c = c * C;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {   // row tid / 16 + 16 m, 8 dims at 8 (tid % 16)
-            const int r = tid / 16 + 16 * m, t = t0c + r;
-            const size_t e = ((((size_t)b * T + t) * H + h) * kTcDK) / 8 +
-                             tid % 16;
-            pq[m] = t < T ? q4[e] : make_uint4(0, 0, 0, 0);
-            pk[m] = t < T ? k4[e] : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {   // row tid / 8 + 32 m, dv 8 (tid % 8)
-            const int r = tid / 8 + 32 * m, t = t0c + r;
-            const size_t e =
-                ((((size_t)b * T + t) * H + h) * dv + j0) / 8 + tid % 8;
-            pd[m] = t < T ? d4[e] : make_uint4(0, 0, 0, 0);
-        }
-        if (tid < C) {
-            const int t = t0c + tid;
-            const size_t off = ((size_t)b * T + t) * H + h;
-            pla = t < T ? a.log_alpha[off] : 0.f;
-            peta = t < T ? a.eta[off] : 0.f;
-        }
-    };
-    auto unpack8 = [](uint4 u, float* dst) {   // 8 bf16 -> 8 fp32
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-        float f[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
-        reinterpret_cast<float4*>(dst)[0] = make_float4(f[0], f[1], f[2], f[3]);
-        reinterpret_cast<float4*>(dst)[1] = make_float4(f[4], f[5], f[6], f[7]);
-    };
-    fetch(nch - 1);
-
-    for (int ch = nch - 1; ch >= 0; --ch) {
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int r = tid / 16 + 16 * m, c8 = tid % 16;
-            unpack8(pq[m], Qs + r * LDK + 8 * c8);
-            unpack8(pk[m], Ks + r * LDK + 8 * c8);
-        }
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-            unpack8(pd[m], Ds + (tid / 8 + 32 * m) * LDV + 8 * (tid % 8));
-        if (tid < C) {
-            gs[tid] = pla;
-            bs[tid] = peta;
-        }
-        __syncthreads();
-        if (ch > 0) fetch(ch - 1);   // in flight during this chunk
-        chunk_gates<kTcDK>(a, Ks, LDK, gs, bs, gam, lam, nullptr);
-        __syncthreads();
-
-        // A = I + strict_lower(Diag(beta)(Gamma o K K^T)) and
-        // P = lower_incl(Gamma o Q K^T): the 20 lower 16 x 8 tiles of each
-        for (int tt = warp; tt < 40; tt += kBwdThreads / 32) {
-            const bool isP = tt >= 20;
-            const int ti = isP ? tt - 20 : tt;
-            int rb = 0, base = 0;            // row block rb has 2 rb + 2 tiles
-            while (ti >= base + 2 * rb + 2) {
-                base += 2 * rb + 2;
-                ++rb;
-            }
-            const int r0 = 16 * rb, n0 = 8 * (ti - base);
-            const float* X = isP ? Qs : Ks;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-            for (int k0 = 0; k0 < kTcDK; k0 += 8) {
-                uint32_t af[4];
-                af[0] = to_tf32(X[(r0 + g) * LDK + k0 + q]);
-                af[1] = to_tf32(X[(r0 + g + 8) * LDK + k0 + q]);
-                af[2] = to_tf32(X[(r0 + g) * LDK + k0 + q + 4]);
-                af[3] = to_tf32(X[(r0 + g + 8) * LDK + k0 + q + 4]);
-                mma_tf32(acc, af, to_tf32(Ks[(n0 + g) * LDK + k0 + q]),
-                         to_tf32(Ks[(n0 + g) * LDK + k0 + q + 4]));
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = r0 + g + 8 * (e >> 1), i = n0 + 2 * q + (e & 1);
-                const float dec = i <= r ? expf(gs[r] - gs[i]) : 0.f;
-                if (isP)
-                    Ps[r * LDC + i] = i <= r ? dec * acc[e] : 0.f;
-                else
-                    As[r * LDC + i] = i < r ? bs[r] * dec * acc[e]
-                                            : (i == r ? 1.f : 0.f);
-            }
-        }
-        {   // dL/dS at the end of this chunk
-            float* out = a.dsck + ((size_t)bh * nch + ch) * kTcDK * dv + j0;
-            for (int idx = tid; idx < kTcDK * kTcDV; idx += kBwdThreads) {
-                const int c = idx / kTcDV, j = idx % kTcDV;
-                out[(size_t)c * dv + j] = dS[c * LDV + j];
-            }
-        }
-        __syncthreads();
-        invert_unit_lower<kBwdThreads>(As, Tm, C, LDC);   // ends with a barrier
-
-        // dU~ = P^T dO + Diag(lambda) K dS': 32 tiles, 4 per warp
-        for (int tt = warp; tt < 32; tt += kBwdThreads / 32) {
-            const int r0 = 16 * (tt / 8), n0 = 8 * (tt % 8);
-            float kd[4] = {0.f, 0.f, 0.f, 0.f}, pd[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-            for (int k0 = 0; k0 < kTcDK; k0 += 8) {
-                uint32_t af[4];
-                af[0] = to_tf32(Ks[(r0 + g) * LDK + k0 + q]);
-                af[1] = to_tf32(Ks[(r0 + g + 8) * LDK + k0 + q]);
-                af[2] = to_tf32(Ks[(r0 + g) * LDK + k0 + q + 4]);
-                af[3] = to_tf32(Ks[(r0 + g + 8) * LDK + k0 + q + 4]);
-                mma_tf32(kd, af, to_tf32(dS[(k0 + q) * LDV + n0 + g]),
-                         to_tf32(dS[(k0 + q + 4) * LDV + n0 + g]));
-            }
-            for (int k0 = r0; k0 < C; k0 += 8) {   // P[i][r] = 0 for i < r
-                uint32_t af[4];
-                af[0] = to_tf32(Ps[(k0 + q) * LDC + r0 + g]);
-                af[1] = to_tf32(Ps[(k0 + q) * LDC + r0 + g + 8]);
-                af[2] = to_tf32(Ps[(k0 + q + 4) * LDC + r0 + g]);
-                af[3] = to_tf32(Ps[(k0 + q + 4) * LDC + r0 + g + 8]);
-                mma_tf32(pd, af, to_tf32(Ds[(k0 + q) * LDV + n0 + g]),
-                         to_tf32(Ds[(k0 + q + 4) * LDV + n0 + g]));
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = r0 + g + 8 * (e >> 1), j = n0 + 2 * q + (e & 1);
-                Ws[r * LDV + j] = fmaf(lam[r], kd[e], pd[e]);
-            }
-        }
-        __syncthreads();
-
-        // dF = T^T dU~ (T lower triangular; its upper part holds scratch)
-        for (int tt = warp; tt < 32; tt += kBwdThreads / 32) {
-            const int r0 = 16 * (tt / 8), n0 = 8 * (tt % 8);
-            const int ra = r0 + g, rb = r0 + g + 8;
-            float df[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int k0 = r0; k0 < C; k0 += 8) {
-                const int i0 = k0 + q, i1 = k0 + q + 4;
-                uint32_t af[4];
-                af[0] = to_tf32(i0 >= ra ? Tm[i0 * LDC + ra] : 0.f);
-                af[1] = to_tf32(i0 >= rb ? Tm[i0 * LDC + rb] : 0.f);
-                af[2] = to_tf32(i1 >= ra ? Tm[i1 * LDC + ra] : 0.f);
-                af[3] = to_tf32(i1 >= rb ? Tm[i1 * LDC + rb] : 0.f);
-                mma_tf32(df, af, to_tf32(Ws[i0 * LDV + n0 + g]),
-                         to_tf32(Ws[i1 * LDV + n0 + g]));
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = r0 + g + 8 * (e >> 1), j = n0 + 2 * q + (e & 1);
-                W2[r * LDV + j] = df[e];
-            }
-        }
-        __syncthreads();
-
-        // dS = gamma_C dS' + Q^T Diag(gamma) dO - K^T Diag(gamma beta) dF:
-        // 64 tiles, 8 per warp; each thread reads and writes only its own
-        // entries of dS
-        const float gC = gam[C - 1];
-        for (int tt = warp; tt < 64; tt += kBwdThreads / 32) {
-            const int c0 = 16 * (tt / 8), n0 = 8 * (tt % 8);
-            float acc[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                acc[e] = gC * dS[(c0 + g + 8 * (e >> 1)) * LDV + n0 + 2 * q +
-                                 (e & 1)];
-#pragma unroll 2
-            for (int k0 = 0; k0 < C; k0 += 8) {
-                const int r0 = k0 + q, r1 = k0 + q + 4;
-                uint32_t af[4];
-                af[0] = to_tf32(Qs[r0 * LDK + c0 + g]);
-                af[1] = to_tf32(Qs[r0 * LDK + c0 + g + 8]);
-                af[2] = to_tf32(Qs[r1 * LDK + c0 + g]);
-                af[3] = to_tf32(Qs[r1 * LDK + c0 + g + 8]);
-                mma_tf32(acc, af, to_tf32(gam[r0] * Ds[r0 * LDV + n0 + g]),
-                         to_tf32(gam[r1] * Ds[r1 * LDV + n0 + g]));
-                af[0] = to_tf32(Ks[r0 * LDK + c0 + g]);
-                af[1] = to_tf32(Ks[r0 * LDK + c0 + g + 8]);
-                af[2] = to_tf32(Ks[r1 * LDK + c0 + g]);
-                af[3] = to_tf32(Ks[r1 * LDK + c0 + g + 8]);
-                mma_tf32(acc, af,
-                         to_tf32(-gam[r0] * bs[r0] * W2[r0 * LDV + n0 + g]),
-                         to_tf32(-gam[r1] * bs[r1] * W2[r1 * LDV + n0 + g]));
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                dS[(c0 + g + 8 * (e >> 1)) * LDV + n0 + 2 * q + (e & 1)] =
-                    acc[e];
-        }
-        __syncthreads();
-    }
-
-    if (a.dh0) {
-        for (int idx = tid; idx < kTcDK * kTcDV; idx += kBwdThreads) {
-            const int c = idx / kTcDV, j = idx % kTcDV;
-            a.dh0[((size_t)bh * kTcDK + c) * dv + j0 + j] = dS[c * LDV + j];
-        }
-    }
 }
 
 // ------------------------------------------------------------- gradients
@@ -1748,6 +1465,347 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
     }
 }
 
+// ------------------------- reverse state recurrence, bf16 operand tiles
+// kla_bwd_state_kernel's per-chunk algebra for bf16, dk = 128, C = 64 and
+// 64-column dv slices, every product on the tensor cores: A and P from
+// K K^T and Q K^T of the exact bf16 inputs, dU~ = P^T dO + Diag(lambda) K dS',
+// dF = T^T dU~ and dS = gamma_C dS' + Q^T Diag(gamma) dO
+// - K^T Diag(gamma beta) dF as m16n8k16 MMAs (bf16 operands, fp32
+// accumulation) whose operands are bf16 tiles read by ldmatrix, in the
+// layout of kla_bwd_grad_lm_kernel.  dS itself stays in fp32 registers for
+// the whole walk (warp w owns key rows 16 w .. 16 w + 15, all 64 columns of
+// the slice) and is copied to shared memory in bf16, as the operand of
+// K dS', once per chunk.
+namespace sm2 {
+constexpr int C = 64, DK = 128, DV = 64;
+constexpr int LQ = DK + 8, LC = C + 8, LV = DV + 8, LF = C + 1;
+constexpr int QB = 0;
+constexpr int KB = QB + C * LQ * 2;
+constexpr int DOB = KB + C * LQ * 2;   // dO
+constexpr int DOG = DOB + C * LV * 2;  // Diag(gamma) dO
+constexpr int PB = DOG + C * LV * 2;
+constexpr int TB = PB + C * LC * 2;
+constexpr int DSB = TB + C * LC * 2;   // dS' (DK x DV)
+constexpr int DUB = DSB + DK * LV * 2;
+constexpr int DFS = DUB + C * LV * 2;  // -Diag(gamma beta) dF
+constexpr int AF = DFS + C * LV * 2;   // A (fp32)
+constexpr int TF = AF + C * LF * 4;    // A^{-1} (fp32)
+constexpr int VEC = TF + C * LF * 4;   // gs, bs, gam, lam
+constexpr int BYTES = VEC + 4 * C * 4;
+static_assert(BYTES <= 232448, "shared memory");
+static_assert(KB % 16 == 0 && DOB % 16 == 0 && DOG % 16 == 0 &&
+                  PB % 16 == 0 && TB % 16 == 0 && DSB % 16 == 0 &&
+                  DUB % 16 == 0 && DFS % 16 == 0,
+              "ldmatrix rows are 16-byte aligned");
+}  // namespace sm2
+
+template <typename IO>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+kla_bwd_state_lm_kernel(BwdArgs a) {
+    using namespace sm2;
+    using lm::a_row;
+    using lm::a_trn;
+    using lm::b_row2;
+    using lm::mma;
+    extern __shared__ __align__(16) uint8_t smraw[];
+    bf16* Qb = reinterpret_cast<bf16*>(smraw + QB);
+    bf16* Kb = reinterpret_cast<bf16*>(smraw + KB);
+    bf16* dOb = reinterpret_cast<bf16*>(smraw + DOB);
+    bf16* dOg = reinterpret_cast<bf16*>(smraw + DOG);
+    bf16* Pb = reinterpret_cast<bf16*>(smraw + PB);
+    bf16* Tb = reinterpret_cast<bf16*>(smraw + TB);
+    bf16* dSb = reinterpret_cast<bf16*>(smraw + DSB);
+    bf16* dUb = reinterpret_cast<bf16*>(smraw + DUB);
+    bf16* dFs = reinterpret_cast<bf16*>(smraw + DFS);
+    float* Af = reinterpret_cast<float*>(smraw + AF);
+    float* Tf = reinterpret_cast<float*>(smraw + TF);
+    float* gs = reinterpret_cast<float*>(smraw + VEC);
+    float* bs = gs + C;
+    float* gam = gs + 2 * C;
+    float* lam = gs + 3 * C;
+
+    const int bh = blockIdx.x;
+    const int b = bh / a.H, h = bh % a.H;
+    const int j0 = blockIdx.y * DV;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int T = a.T, H = a.H, dv = a.dv;
+    const int nch = (T + C - 1) / C;
+
+    // dS of this warp's key rows 16 warp + g8 (+ 8), columns 8 nt + 2 t4
+    // (+ 1): fragment layout, 8 column tiles
+    float dS[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = 16 * warp + g8 + 8 * (e >> 1);
+            const int j = 8 * nt + 2 * t4 + (e & 1);
+            dS[nt][e] =
+                a.dhT ? a.dhT[((size_t)bh * DK + c) * dv + j0 + j] : 0.f;
+        }
+    for (int i = tid; i < C * LC / 2; i += kBwdThreads)   // P's upper part
+        reinterpret_cast<uint32_t*>(Pb)[i] = 0u;
+
+    // The tiles of a chunk (q, k: 64 x 128, dO: 64 x 64, bf16) and its gates
+    // are loaded into registers, 16 bytes a load, while the previous chunk
+    // computes, and stored to shared memory (unconverted) when it is done.
+    const uint4* q4 = static_cast<const uint4*>(a.q);
+    const uint4* k4 = static_cast<const uint4*>(a.k);
+    const uint4* d4 = static_cast<const uint4*>(a.dout);
+    uint4 pq[4], pk[4], pd[2];
+    float pla = 0.f, peta = 0.f;
+    auto fetch = [&](int c) {
+        const int t0c = c * C;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {   // row tid / 16 + 16 m, dims 8 (tid % 16)
+            const int r = tid / 16 + 16 * m, t = t0c + r;
+            const size_t e =
+                ((((size_t)b * T + t) * H + h) * DK) / 8 + tid % 16;
+            pq[m] = t < T ? q4[e] : make_uint4(0, 0, 0, 0);
+            pk[m] = t < T ? k4[e] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {   // row tid / 8 + 32 m, dv 8 (tid % 8)
+            const int r = tid / 8 + 32 * m, t = t0c + r;
+            const size_t e =
+                ((((size_t)b * T + t) * H + h) * dv + j0) / 8 + tid % 8;
+            pd[m] = t < T ? d4[e] : make_uint4(0, 0, 0, 0);
+        }
+        if (tid < C) {
+            const int t = t0c + tid;
+            const size_t off = ((size_t)b * T + t) * H + h;
+            pla = t < T ? a.log_alpha[off] : 0.f;
+            peta = t < T ? a.eta[off] : 0.f;
+        }
+    };
+    fetch(nch - 1);
+    // this warp's tiles of the C x DV products: rows 16 (w >> 1), columns
+    // 32 (w & 1) .. + 31 (four 16 x 8 tiles)
+    const int pm = warp >> 1, pn = 32 * (warp & 1);
+
+    for (int ch = nch - 1; ch >= 0; --ch) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int r = tid / 16 + 16 * m, c8 = tid % 16;
+            *reinterpret_cast<uint4*>(Qb + r * LQ + 8 * c8) = pq[m];
+            *reinterpret_cast<uint4*>(Kb + r * LQ + 8 * c8) = pk[m];
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+            *reinterpret_cast<uint4*>(dOb + (tid / 8 + 32 * m) * LV +
+                                      8 * (tid % 8)) = pd[m];
+        if (tid < C) {
+            gs[tid] = pla;
+            bs[tid] = peta;
+        }
+        {   // dL/dS at the end of this chunk: to the workspace (fp32) and,
+            // in bf16, to shared memory as an operand
+            float* out = a.dsck + ((size_t)bh * nch + ch) * DK * dv + j0;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int hm = 0; hm < 2; ++hm) {
+                    const int c = 16 * warp + g8 + 8 * hm;
+                    const int j = 8 * nt + 2 * t4;
+                    *reinterpret_cast<float2*>(out + (size_t)c * dv + j) =
+                        make_float2(dS[nt][2 * hm], dS[nt][2 * hm + 1]);
+                    *reinterpret_cast<uint32_t*>(dSb + c * LV + j) =
+                        tc::pack_bf16x2(dS[nt][2 * hm], dS[nt][2 * hm + 1]);
+                }
+        }
+        __syncthreads();
+        if (ch > 0) fetch(ch - 1);   // in flight during this chunk
+        {   // ||k||^2 (four threads per row), beta, cumulative decay
+            const int r = tid >> 2, q4i = tid & 3;
+            float n = 0.f;
+#pragma unroll 8
+            for (int c = 32 * q4i; c < 32 * q4i + 32; ++c) {
+                const float x = lm::bf(Kb, r * LQ + c);
+                n = fmaf(x, x, n);
+            }
+            n = lm::quad_sum(n);
+            if (q4i == 0 && !a.gdn) {
+                const float denom = n + a.eps;
+                bs[r] = denom == 0.f ? 0.f : bs[r] / denom;
+            }
+            if (warp == 0) {   // inclusive scan of the 64 log decays
+                const float x0 = gs[2 * lane], x1 = gs[2 * lane + 1];
+                float s = x0 + x1;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, s, off);
+                    if (lane >= off) s += y;
+                }
+                gs[2 * lane] = s - x1;
+                gs[2 * lane + 1] = s;
+            }
+        }
+        __syncthreads();
+        if (tid < C) {
+            gam[tid] = expf(gs[tid]);
+            lam[tid] = expf(gs[C - 1] - gs[tid]);
+        }
+        // A (fp32) and P (bf16) from K K^T and Q K^T: the 20 lower tiles
+        for (int idx = warp; idx < 20; idx += 8) {
+            int mt, nt;
+            lower_tile(idx, mt, nt);
+            float qk[4] = {0.f, 0.f, 0.f, 0.f}, kk[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < DK / 16; ++ks) {
+                uint32_t aq[4], ak[4], bk[4];
+                a_row(aq, Qb + 16 * mt * LQ + 16 * ks, LQ, lane);
+                a_row(ak, Kb + 16 * mt * LQ + 16 * ks, LQ, lane);
+                lm::b_col2(bk, Kb + 8 * nt * LQ + 16 * ks, LQ, lane);
+                mma(qk, aq, bk[0], bk[1]);
+                mma(kk, ak, bk[0], bk[1]);
+            }
+#pragma unroll
+            for (int hm = 0; hm < 2; ++hm) {
+                const int r = 16 * mt + g8 + 8 * hm;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int i = 8 * nt + 2 * t4 + e;
+                    float av = i == r ? 1.f : 0.f, pv = 0.f;
+                    if (i <= r) {
+                        const float dec = expf(gs[r] - gs[i]);
+                        pv = dec * qk[2 * hm + e];
+                        if (i < r) av = bs[r] * dec * kk[2 * hm + e];
+                    }
+                    Af[r * LF + i] = av;
+                    Pb[r * LC + i] = __float2bfloat16_rn(pv);
+                }
+            }
+        }
+        __syncthreads();
+        {   // Diag(gamma) dO (bf16)
+            const int r = tid >> 2, c16 = 16 * (tid & 3);
+            const float gr = gam[r];
+#pragma unroll
+            for (int u = 0; u < 16; u += 2) {
+                const float x0 = lm::bf(dOb, r * LV + c16 + u);
+                const float x1 = lm::bf(dOb, r * LV + c16 + u + 1);
+                *reinterpret_cast<uint32_t*>(dOg + r * LV + c16 + u) =
+                    tc::pack_bf16x2(gr * x0, gr * x1);
+            }
+        }
+        invert_unit_lower<kBwdThreads>(Af, Tf, C, LF);   // ends with a barrier
+        for (int i = tid; i < C * C; i += kBwdThreads) {   // T (bf16, lower)
+            const int r = i >> 6, c = i & 63;
+            Tb[r * LC + c] = __float2bfloat16_rn(c <= r ? Tf[r * LF + c] : 0.f);
+        }
+        __syncthreads();
+
+        // dU~ = P^T dO + Diag(lambda) K dS'
+        {
+            float kd[4][4] = {}, pd4[4][4] = {};
+#pragma unroll
+            for (int kk = 0; kk < DK / 16; ++kk) {
+                uint32_t ak[4], b0[4], b1[4];
+                a_row(ak, Kb + 16 * pm * LQ + 16 * kk, LQ, lane);
+                b_row2(b0, dSb + 16 * kk * LV + pn, LV, lane);
+                b_row2(b1, dSb + 16 * kk * LV + pn + 16, LV, lane);
+                mma(kd[0], ak, b0[0], b0[1]);
+                mma(kd[1], ak, b0[2], b0[3]);
+                mma(kd[2], ak, b1[0], b1[1]);
+                mma(kd[3], ak, b1[2], b1[3]);
+            }
+            for (int kk = pm; kk < C / 16; ++kk) {   // P^T(r, i) = P(i, r)
+                uint32_t ap[4], b0[4], b1[4];
+                a_trn(ap, Pb + 16 * kk * LC + 16 * pm, LC, lane);
+                b_row2(b0, dOb + 16 * kk * LV + pn, LV, lane);
+                b_row2(b1, dOb + 16 * kk * LV + pn + 16, LV, lane);
+                mma(pd4[0], ap, b0[0], b0[1]);
+                mma(pd4[1], ap, b0[2], b0[3]);
+                mma(pd4[2], ap, b1[0], b1[1]);
+                mma(pd4[3], ap, b1[2], b1[3]);
+            }
+#pragma unroll
+            for (int hm = 0; hm < 2; ++hm) {
+                const int r = 16 * pm + g8 + 8 * hm;
+                const float lr = lam[r];
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int j = pn + 8 * nt + 2 * t4;
+                    *reinterpret_cast<uint32_t*>(dUb + r * LV + j) =
+                        tc::pack_bf16x2(
+                            fmaf(lr, kd[nt][2 * hm], pd4[nt][2 * hm]),
+                            fmaf(lr, kd[nt][2 * hm + 1], pd4[nt][2 * hm + 1]));
+                }
+            }
+        }
+        __syncthreads();
+
+        // dF = T^T dU~, stored as -Diag(gamma beta) dF
+        {
+            float df[4][4] = {};
+            for (int kk = pm; kk < C / 16; ++kk) {   // T^T(r, i) = T(i, r)
+                uint32_t at[4], b0[4], b1[4];
+                a_trn(at, Tb + 16 * kk * LC + 16 * pm, LC, lane);
+                b_row2(b0, dUb + 16 * kk * LV + pn, LV, lane);
+                b_row2(b1, dUb + 16 * kk * LV + pn + 16, LV, lane);
+                mma(df[0], at, b0[0], b0[1]);
+                mma(df[1], at, b0[2], b0[3]);
+                mma(df[2], at, b1[0], b1[1]);
+                mma(df[3], at, b1[2], b1[3]);
+            }
+#pragma unroll
+            for (int hm = 0; hm < 2; ++hm) {
+                const int r = 16 * pm + g8 + 8 * hm;
+                const float s = -gam[r] * bs[r];
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int j = pn + 8 * nt + 2 * t4;
+                    *reinterpret_cast<uint32_t*>(dFs + r * LV + j) =
+                        tc::pack_bf16x2(s * df[nt][2 * hm],
+                                        s * df[nt][2 * hm + 1]);
+                }
+            }
+        }
+        __syncthreads();
+
+        // dS = gamma_C dS' + Q^T Diag(gamma) dO - K^T Diag(gamma beta) dF
+        {
+            const float gC = gam[C - 1];
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dS[nt][e] *= gC;
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk) {
+                uint32_t aq[4], ak[4];
+                a_trn(aq, Qb + 16 * kk * LQ + 16 * warp, LQ, lane);   // Q^T
+                a_trn(ak, Kb + 16 * kk * LQ + 16 * warp, LQ, lane);   // K^T
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t bo[4], bf4[4];
+                    b_row2(bo, dOg + 16 * kk * LV + 16 * np, LV, lane);
+                    b_row2(bf4, dFs + 16 * kk * LV + 16 * np, LV, lane);
+                    mma(dS[2 * np], aq, bo[0], bo[1]);
+                    mma(dS[2 * np + 1], aq, bo[2], bo[3]);
+                    mma(dS[2 * np], ak, bf4[0], bf4[1]);
+                    mma(dS[2 * np + 1], ak, bf4[2], bf4[3]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    if (a.dh0) {
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int hm = 0; hm < 2; ++hm) {
+                const int c = 16 * warp + g8 + 8 * hm;
+                const int j = 8 * nt + 2 * t4;
+                *reinterpret_cast<float2*>(a.dh0 +
+                                           ((size_t)bh * DK + c) * dv + j0 +
+                                           j) =
+                    make_float2(dS[nt][2 * hm], dS[nt][2 * hm + 1]);
+            }
+    }
+}
+
 // DVS: dv columns per CTA of the reverse state recurrence; DVT: dv columns
 // per step of the gradient kernel.
 template <int DK, int DVS, int DVT, typename IO>
@@ -1767,13 +1825,12 @@ cudaError_t launch_shape(const BwdArgs& a, cudaStream_t stream) {
     if constexpr (DK == kTcDK && DVS == kTcDV &&
                   std::is_same<IO, __nv_bfloat16>::value) {
         if (state_tc_ok(a)) {   // the reverse recurrence on the tensor cores
-            auto kt = kla_bwd_state_tc_kernel<IO>;
+            auto kt = kla_bwd_state_lm_kernel<IO>;
             e = cudaFuncSetAttribute(
-                kt, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                (int)StateTcSmem::BYTES);
+                kt, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2::BYTES);
             if (e != cudaSuccess) return e;
             kt<<<dim3((unsigned)bhs, (unsigned)(a.dv / DVS)), kBwdThreads,
-                 StateTcSmem::BYTES, stream>>>(a);
+                 sm2::BYTES, stream>>>(a);
         } else {
             ks<<<dim3((unsigned)bhs, (unsigned)(a.dv / DVS)), kBwdThreads,
                  LS::BYTES, stream>>>(a);

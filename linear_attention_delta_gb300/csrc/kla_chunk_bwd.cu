@@ -870,6 +870,27 @@ __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4],
 __device__ __forceinline__ float bf(const bf16* p, int i) {
     return __bfloat162float(p[i]);
 }
+// 16-byte asynchronous copy global -> shared (zeros when !valid; src must
+// still point into the tensor).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src,
+                                           bool valid) {
+    asm volatile(
+        "cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+            tc::smem_u32(dst)),
+        "l"(src), "r"(valid ? 16 : 0)
+        : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+// staging of one dv step in the fp32 scratch (S | dS' fp32, V | dO bf16)
+constexpr int STG_DS = DK * DVT * 4, STG_V = 2 * DK * DVT * 4,
+              STG_DO = STG_V + C * DVT * 2, STG_END = STG_DO + C * DVT * 2;
+static_assert(F0 + STG_END <= SB, "staging fits in the fp32 scratch");
+
 // Sum over the four lanes that share a fragment row (lane >> 2).
 __device__ __forceinline__ float quad_sum(float x) {
     x += __shfl_xor_sync(0xffffffffu, x, 1);
@@ -1052,30 +1073,75 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
     float sdot = 0.f;
     __syncthreads();
 
+    // Steps after the first are staged one step ahead by cp.async in the
+    // fp32 scratch, which the dv steps leave free; each thread copies and
+    // later reads back the same 16-byte pieces, so no barrier guards the
+    // staging area.
+    uint8_t* stage = smraw + F0;
+    auto stage_issue = [&](int jn) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = tid + u * kBwdThreads;   // 128 rows x 8
+            const int c = idx >> 3, j4 = idx & 7;
+            cp_async16(stage + (c * DVT + 4 * j4) * 4,
+                       Sg + (size_t)c * dv + jn + 4 * j4, true);
+            cp_async16(stage + STG_DS + (c * DVT + 4 * j4) * 4,
+                       dSg + (size_t)c * dv + jn + 4 * j4, true);
+        }
+        const int r = tid >> 2, j8 = tid & 3;        // 64 rows x 4
+        const int t = t0 + r;
+        const size_t off =
+            (((size_t)b * T + (t < T ? t : t0)) * H + h) * dv + jn + 8 * j8;
+        cp_async16(stage + STG_V + (r * DVT + 8 * j8) * 2,
+                   static_cast<const IO*>(a.v) + off, t < T);
+        cp_async16(stage + STG_DO + (r * DVT + 8 * j8) * 2,
+                   static_cast<const IO*>(a.dout) + off, t < T);
+        cp_async_commit();
+    };
+
     for (int j0 = 0; j0 < dv; j0 += DVT) {
         {   // S, dS' (DK x DVT fp32 -> bf16), V (fp32), dO (bf16, and
-            // Diag(gamma) dO): every load issued before the stores
+            // Diag(gamma) dO): from global memory for the first step (every
+            // load issued before the stores), from the staging area after
             float4 sv[4], dsv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int idx = tid + u * kBwdThreads;   // 128 rows x 8
-                const int c = idx >> 3, j4 = idx & 7;
-                sv[u] = *reinterpret_cast<const float4*>(
-                    Sg + (size_t)c * dv + j0 + 4 * j4);
-                dsv[u] = *reinterpret_cast<const float4*>(
-                    dSg + (size_t)c * dv + j0 + 4 * j4);
-            }
             const int r = tid >> 2, j8 = tid & 3;        // 64 rows x 4
             const int t = t0 + r;
             uint4 vv = make_uint4(0, 0, 0, 0), dov = make_uint4(0, 0, 0, 0);
-            if (t < T) {
-                const size_t off =
-                    (((size_t)b * T + t) * H + h) * dv + j0 + 8 * j8;
+            if (j0 == 0) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int idx = tid + u * kBwdThreads;   // 128 rows x 8
+                    const int c = idx >> 3, j4 = idx & 7;
+                    sv[u] = *reinterpret_cast<const float4*>(
+                        Sg + (size_t)c * dv + j0 + 4 * j4);
+                    dsv[u] = *reinterpret_cast<const float4*>(
+                        dSg + (size_t)c * dv + j0 + 4 * j4);
+                }
+                if (t < T) {
+                    const size_t off =
+                        (((size_t)b * T + t) * H + h) * dv + j0 + 8 * j8;
+                    vv = *reinterpret_cast<const uint4*>(
+                        static_cast<const IO*>(a.v) + off);
+                    dov = *reinterpret_cast<const uint4*>(
+                        static_cast<const IO*>(a.dout) + off);
+                }
+            } else {
+                cp_async_wait_all();
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int idx = tid + u * kBwdThreads;
+                    const int c = idx >> 3, j4 = idx & 7;
+                    sv[u] = *reinterpret_cast<const float4*>(
+                        stage + (c * DVT + 4 * j4) * 4);
+                    dsv[u] = *reinterpret_cast<const float4*>(
+                        stage + STG_DS + (c * DVT + 4 * j4) * 4);
+                }
                 vv = *reinterpret_cast<const uint4*>(
-                    static_cast<const IO*>(a.v) + off);
+                    stage + STG_V + (r * DVT + 8 * j8) * 2);
                 dov = *reinterpret_cast<const uint4*>(
-                    static_cast<const IO*>(a.dout) + off);
+                    stage + STG_DO + (r * DVT + 8 * j8) * 2);
             }
+            if (j0 + DVT < dv) stage_issue(j0 + DVT);   // next step in flight
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int idx = tid + u * kBwdThreads;

@@ -891,6 +891,88 @@ constexpr int STG_DS = DK * DVT * 4, STG_V = 2 * DK * DVT * 4,
               STG_DO = STG_V + C * DVT * 2, STG_END = STG_DO + C * DVT * 2;
 static_assert(F0 + STG_END <= SB, "staging fits in the fp32 scratch");
 
+// acc (16 x 8) += A (16 x 16 fp32 block, row stride la) x B[:, 0..7] (16 x 8
+// of an fp32 block, row stride lb): two tf32 m16n8k8 MMAs.
+__device__ __forceinline__ void mm16x8_tf32(float (&acc)[4], const float* A,
+                                            int la, const float* B, int lb,
+                                            int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+        uint32_t a[4];
+        a[0] = tc::to_tf32(A[g * la + 8 * kk + t]);
+        a[1] = tc::to_tf32(A[(g + 8) * la + 8 * kk + t]);
+        a[2] = tc::to_tf32(A[g * la + 8 * kk + t + 4]);
+        a[3] = tc::to_tf32(A[(g + 8) * la + 8 * kk + t + 4]);
+        tc::mma_m16n8k8_tf32(acc, a, tc::to_tf32(B[(8 * kk + t) * lb + g]),
+                             tc::to_tf32(B[(8 * kk + t + 4) * lb + g]));
+    }
+}
+
+// T = A^{-1} for the unit lower-triangular 64 x 64 A (fp32, row stride la;
+// only its strict lower part is read), into the lower part of Tm (row
+// stride lt; the 16 x 16 blocks above the diagonal are left as they were).
+// The diagonal blocks by fp32 column substitution (threads 0..63), the
+// blocks below them in three levels, T_IJ = -T_II (sum_{m=J}^{I-1} A_Im
+// T_mJ) for 8-column slabs on the tensor cores (tf32 operands, fp32
+// accumulation), the sum passed through Y (16 x 8 floats per warp).  All 256
+// threads take part; ends with a barrier.
+__device__ __forceinline__ void invert_lower64(const float* A, int la,
+                                               float* Tm, int lt, float* Y) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
+    if (tid < 64) {
+        const int bb = tid >> 4, cl = tid & 15;
+        const float* Ab = A + 16 * bb * la + 16 * bb;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = r == cl ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < 16; ++r) {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < r; i += 2) {
+                a0 = fmaf(Ab[r * la + i], x[i], a0);
+                if (i + 1 < r) a1 = fmaf(Ab[r * la + i + 1], x[i + 1], a1);
+            }
+            if (r > cl) x[r] = -(a0 + a1);
+        }
+        float* Tb = Tm + 16 * bb * lt + 16 * bb + cl;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Tb[r * lt] = x[r];
+    }
+    __syncthreads();
+    float* Yw = Y + warp * 128;
+    auto slab = [&](int I, int J, int n0) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int m = J; m < I; ++m)
+            mm16x8_tf32(acc, A + 16 * I * la + 16 * m, la,
+                        Tm + 16 * m * lt + 16 * J + n0, lt, lane);
+        Yw[g * 8 + 2 * t] = acc[0];
+        Yw[g * 8 + 2 * t + 1] = acc[1];
+        Yw[(g + 8) * 8 + 2 * t] = acc[2];
+        Yw[(g + 8) * 8 + 2 * t + 1] = acc[3];
+        __syncwarp();
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mm16x8_tf32(d, Tm + 16 * I * lt + 16 * I, lt, Yw, 8, lane);
+        __syncwarp();
+        float* dst = Tm + 16 * I * lt + 16 * J + n0;
+        dst[g * lt + 2 * t] = -d[0];
+        dst[g * lt + 2 * t + 1] = -d[1];
+        dst[(g + 8) * lt + 2 * t] = -d[2];
+        dst[(g + 8) * lt + 2 * t + 1] = -d[3];
+    };
+    // level 1: (1,0), (2,1), (3,2) -- two 8-column slabs each
+    if (warp < 6) slab((warp >> 1) + 1, warp >> 1, 8 * (warp & 1));
+    __syncthreads();
+    // level 2: (2,0), (3,1)
+    if (warp < 4) slab(2 + (warp >> 1), warp >> 1, 8 * (warp & 1));
+    __syncthreads();
+    // level 3: (3,0)
+    if (warp < 2) slab(3, 0, 8 * warp);
+    __syncthreads();
+}
+
 // Sum over the four lanes that share a fragment row (lane >> 2).
 __device__ __forceinline__ float quad_sum(float x) {
     x += __shfl_xor_sync(0xffffffffu, x, 1);
@@ -1048,7 +1130,7 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
         }
     }
     __syncthreads();
-    invert_unit_lower<kBwdThreads>(F0f, F1f, C, LF);   // lower part of F1
+    invert_lower64(F0f, LF, F1f, LF, Xf);   // lower part of F1 (X free yet)
     for (int i = tid; i < C * C; i += kBwdThreads) {   // T (bf16, lower)
         const int r = i >> 6, c = i & 63;
         Tb[r * LC + c] = __float2bfloat16_rn(c <= r ? F1f[r * LF + c] : 0.f);
@@ -1755,7 +1837,8 @@ kla_bwd_state_lm_kernel(BwdArgs a) {
                     tc::pack_bf16x2(gr * x0, gr * x1);
             }
         }
-        invert_unit_lower<kBwdThreads>(Af, Tf, C, LF);   // ends with a barrier
+        // T = A^{-1} (ends with a barrier; dU~'s tile is free scratch here)
+        lm::invert_lower64(Af, LF, Tf, LF, reinterpret_cast<float*>(dUb));
         for (int i = tid; i < C * C; i += kBwdThreads) {   // T (bf16, lower)
             const int r = i >> 6, c = i & 63;
             Tb[r * LC + c] = __float2bfloat16_rn(c <= r ? Tf[r * LF + c] : 0.f);

@@ -979,6 +979,58 @@ __device__ __forceinline__ float quad_sum(float x) {
     x += __shfl_xor_sync(0xffffffffu, x, 2);
     return x;
 }
+
+// ||k_r||^2 from a bf16 row (row stride LQ), four threads per row, 32
+// dimensions each (16-byte loads); the sum ends in all four.
+__device__ __forceinline__ float row_norm2(const bf16* Kb, int r, int q4) {
+    float n = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint4 v = *reinterpret_cast<const uint4*>(Kb + r * LQ + 32 * q4 +
+                                                        8 * u);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float lo = __uint_as_float(w[e] << 16);
+            const float hi = __uint_as_float(w[e] & 0xffff0000u);
+            n = fmaf(lo, lo, n);
+            n = fmaf(hi, hi, n);
+        }
+    }
+    return quad_sum(n);
+}
+
+// Q K^T and K K^T on this warp's lower 16 x 8 tiles of the C x C products
+// (tile indices warp, warp + 8, warp + 16 below 20: three tiles for warps
+// 0..3, two for the others), the tiles' MMA chains interleaved.
+__device__ __forceinline__ void qk_kk_tiles(float (&qk)[3][4],
+                                            float (&kk)[3][4], int (&mt)[3],
+                                            int (&nt)[3], const bf16* Qb,
+                                            const bf16* Kb, int warp,
+                                            int lane) {
+    const int n = warp < 4 ? 3 : 2;
+#pragma unroll
+    for (int x = 0; x < 3; ++x) {
+        lower_tile(x < n ? warp + 8 * x : warp, mt[x], nt[x]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qk[x][e] = kk[x][e] = 0.f;
+    }
+#pragma unroll
+    for (int ks = 0; ks < DK / 16; ++ks) {
+#pragma unroll
+        for (int x = 0; x < 3; ++x) {
+            if (x < n) {
+                uint32_t aq[4], ak[4], bk[4];
+                a_row(aq, Qb + 16 * mt[x] * LQ + 16 * ks, LQ, lane);
+                a_row(ak, Kb + 16 * mt[x] * LQ + 16 * ks, LQ, lane);
+                // K^T columns 8 nt .. 8 nt + 7 (and the next 8, unused)
+                b_col2(bk, Kb + 8 * nt[x] * LQ + 16 * ks, LQ, lane);
+                mma(qk[x], aq, bk[0], bk[1]);
+                mma(kk[x], ak, bk[0], bk[1]);
+            }
+        }
+    }
+}
 }  // namespace lm
 
 template <typename IO>
@@ -1066,13 +1118,7 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
     __syncthreads();
     {   // ||k||^2 (four threads per row), beta, cumulative decay
         const int r = tid >> 2, q4 = tid & 3;
-        float n = 0.f;
-#pragma unroll 8
-        for (int c = 32 * q4; c < 32 * q4 + 32; ++c) {
-            const float x = bf(Kb, r * LQ + c);
-            n = fmaf(x, x, n);
-        }
-        n = quad_sum(n);
+        const float n = row_norm2(Kb, r, q4);
         if (q4 == 0) {
             nrm[r] = n;
             const float denom = n + a.eps;
@@ -1098,34 +1144,28 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
     }
     // A (unit lower, fp32, into F0) and P (bf16) from K K^T and Q K^T on the
     // tensor cores: the 20 lower 16 x 8 tiles, dealt out to the warps
-    for (int idx = warp; idx < 20; idx += 8) {
-        int mt, nt;
-        lower_tile(idx, mt, nt);
-        float qk[4] = {0.f, 0.f, 0.f, 0.f}, kk[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+        float qk[3][4], kk[3][4];
+        int mt[3], nt[3];
+        qk_kk_tiles(qk, kk, mt, nt, Qb, Kb, warp, lane);
 #pragma unroll
-        for (int ks = 0; ks < DK / 16; ++ks) {
-            uint32_t aq[4], ak[4], bk[4];
-            a_row(aq, Qb + 16 * mt * LQ + 16 * ks, LQ, lane);
-            a_row(ak, Kb + 16 * mt * LQ + 16 * ks, LQ, lane);
-            // K^T columns 8 nt .. 8 nt + 7 (and the next 8, unused)
-            b_col2(bk, Kb + 8 * nt * LQ + 16 * ks, LQ, lane);
-            mma(qk, aq, bk[0], bk[1]);
-            mma(kk, ak, bk[0], bk[1]);
-        }
+        for (int x = 0; x < 3; ++x) {
+            if (x == 2 && warp >= 4) break;
 #pragma unroll
-        for (int hm = 0; hm < 2; ++hm) {
-            const int r = 16 * mt + g8 + 8 * hm;
+            for (int hm = 0; hm < 2; ++hm) {
+                const int r = 16 * mt[x] + g8 + 8 * hm;
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int i = 8 * nt + 2 * t4 + e;
-                float av = i == r ? 1.f : 0.f, pv = 0.f;
-                if (i <= r) {
-                    const float dec = expf(gs[r] - gs[i]);
-                    pv = dec * qk[2 * hm + e];
-                    if (i < r) av = bs[r] * dec * kk[2 * hm + e];
+                for (int e = 0; e < 2; ++e) {
+                    const int i = 8 * nt[x] + 2 * t4 + e;
+                    float av = i == r ? 1.f : 0.f, pv = 0.f;
+                    if (i <= r) {
+                        const float dec = expf(gs[r] - gs[i]);
+                        pv = dec * qk[x][2 * hm + e];
+                        if (i < r) av = bs[r] * dec * kk[x][2 * hm + e];
+                    }
+                    F0f[r * LF + i] = av;
+                    Pb[r * LC + i] = __float2bfloat16_rn(pv);
                 }
-                F0f[r * LF + i] = av;
-                Pb[r * LC + i] = __float2bfloat16_rn(pv);
             }
         }
     }
@@ -1490,46 +1530,41 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
 
     // dGamma o Gamma (F2), Gamma o dP (bf16), D (over dA in F1) and the
     // A-part of dbeta, from Q K^T and K K^T of the lower tiles
-    for (int idx = warp; idx < 20; idx += 8) {
-        int mt, nt;
-        lower_tile(idx, mt, nt);
-        float qk[4] = {0.f, 0.f, 0.f, 0.f}, kk4[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+        float qk[3][4], kk4[3][4];
+        int mt[3], nt[3];
+        qk_kk_tiles(qk, kk4, mt, nt, Qb, Kb, warp, lane);
 #pragma unroll
-        for (int ks = 0; ks < DK / 16; ++ks) {
-            uint32_t aq[4], ak[4], bk[4];
-            a_row(aq, Qb + 16 * mt * LQ + 16 * ks, LQ, lane);
-            a_row(ak, Kb + 16 * mt * LQ + 16 * ks, LQ, lane);
-            b_col2(bk, Kb + 8 * nt * LQ + 16 * ks, LQ, lane);
-            mma(qk, aq, bk[0], bk[1]);
-            mma(kk4, ak, bk[0], bk[1]);
-        }
+        for (int x = 0; x < 3; ++x) {
+            if (x == 2 && warp >= 4) break;
 #pragma unroll
-        for (int hm = 0; hm < 2; ++hm) {
-            const int r = 16 * mt + g8 + 8 * hm;
-            float dbp = 0.f;
+            for (int hm = 0; hm < 2; ++hm) {
+                const int r = 16 * mt[x] + g8 + 8 * hm;
+                float dbp = 0.f;
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int i = 8 * nt + 2 * t4 + e;
-                float dgg = 0.f, dpt = 0.f, dd = 0.f;
-                if (i <= r) {
-                    const float gmm = expf(gs[r] - gs[i]);
-                    const float dpv = F0f[r * LF + i];
-                    float dgm = dpv * qk[2 * hm + e];
-                    dpt = gmm * dpv;
-                    if (i < r) {
-                        const float dav = F1f[r * LF + i];
-                        dgm = fmaf(dav * bs[r], kk4[2 * hm + e], dgm);
-                        dd = bs[r] * gmm * dav;
-                        dbp = fmaf(dav * gmm, kk4[2 * hm + e], dbp);
+                for (int e = 0; e < 2; ++e) {
+                    const int i = 8 * nt[x] + 2 * t4 + e;
+                    float dgg = 0.f, dpt = 0.f, dd = 0.f;
+                    if (i <= r) {
+                        const float gmm = expf(gs[r] - gs[i]);
+                        const float dpv = F0f[r * LF + i];
+                        float dgm = dpv * qk[x][2 * hm + e];
+                        dpt = gmm * dpv;
+                        if (i < r) {
+                            const float dav = F1f[r * LF + i];
+                            dgm = fmaf(dav * bs[r], kk4[x][2 * hm + e], dgm);
+                            dd = bs[r] * gmm * dav;
+                            dbp = fmaf(dav * gmm, kk4[x][2 * hm + e], dbp);
+                        }
+                        dgg = dgm * gmm;
                     }
-                    dgg = dgm * gmm;
+                    F2f[r * LF + i] = dgg;
+                    Gdp[r * LC + i] = __float2bfloat16_rn(dpt);
+                    F1f[r * LF + i] = dd;
                 }
-                F2f[r * LF + i] = dgg;
-                Gdp[r * LC + i] = __float2bfloat16_rn(dpt);
-                F1f[r * LF + i] = dd;
+                dbp = quad_sum(dbp);
+                if (t4 == 0) atomicAdd(&db[r], dbp);
             }
-            dbp = quad_sum(dbp);
-            if (t4 == 0) atomicAdd(&db[r], dbp);
         }
     }
     __syncthreads();
@@ -1766,13 +1801,7 @@ kla_bwd_state_lm_kernel(BwdArgs a) {
         if (ch > 0) fetch(ch - 1);   // in flight during this chunk
         {   // ||k||^2 (four threads per row), beta, cumulative decay
             const int r = tid >> 2, q4i = tid & 3;
-            float n = 0.f;
-#pragma unroll 8
-            for (int c = 32 * q4i; c < 32 * q4i + 32; ++c) {
-                const float x = lm::bf(Kb, r * LQ + c);
-                n = fmaf(x, x, n);
-            }
-            n = lm::quad_sum(n);
+            const float n = lm::row_norm2(Kb, r, q4i);
             if (q4i == 0 && !a.gdn) {
                 const float denom = n + a.eps;
                 bs[r] = denom == 0.f ? 0.f : bs[r] / denom;
@@ -1795,33 +1824,28 @@ kla_bwd_state_lm_kernel(BwdArgs a) {
             lam[tid] = expf(gs[C - 1] - gs[tid]);
         }
         // A (fp32) and P (bf16) from K K^T and Q K^T: the 20 lower tiles
-        for (int idx = warp; idx < 20; idx += 8) {
-            int mt, nt;
-            lower_tile(idx, mt, nt);
-            float qk[4] = {0.f, 0.f, 0.f, 0.f}, kk[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            float qk[3][4], kk[3][4];
+            int mt[3], nt[3];
+            lm::qk_kk_tiles(qk, kk, mt, nt, Qb, Kb, warp, lane);
 #pragma unroll
-            for (int ks = 0; ks < DK / 16; ++ks) {
-                uint32_t aq[4], ak[4], bk[4];
-                a_row(aq, Qb + 16 * mt * LQ + 16 * ks, LQ, lane);
-                a_row(ak, Kb + 16 * mt * LQ + 16 * ks, LQ, lane);
-                lm::b_col2(bk, Kb + 8 * nt * LQ + 16 * ks, LQ, lane);
-                mma(qk, aq, bk[0], bk[1]);
-                mma(kk, ak, bk[0], bk[1]);
-            }
+            for (int x = 0; x < 3; ++x) {
+                if (x == 2 && warp >= 4) break;
 #pragma unroll
-            for (int hm = 0; hm < 2; ++hm) {
-                const int r = 16 * mt + g8 + 8 * hm;
+                for (int hm = 0; hm < 2; ++hm) {
+                    const int r = 16 * mt[x] + g8 + 8 * hm;
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int i = 8 * nt + 2 * t4 + e;
-                    float av = i == r ? 1.f : 0.f, pv = 0.f;
-                    if (i <= r) {
-                        const float dec = expf(gs[r] - gs[i]);
-                        pv = dec * qk[2 * hm + e];
-                        if (i < r) av = bs[r] * dec * kk[2 * hm + e];
+                    for (int e = 0; e < 2; ++e) {
+                        const int i = 8 * nt[x] + 2 * t4 + e;
+                        float av = i == r ? 1.f : 0.f, pv = 0.f;
+                        if (i <= r) {
+                            const float dec = expf(gs[r] - gs[i]);
+                            pv = dec * qk[x][2 * hm + e];
+                            if (i < r) av = bs[r] * dec * kk[x][2 * hm + e];
+                        }
+                        Af[r * LF + i] = av;
+                        Pb[r * LC + i] = __float2bfloat16_rn(pv);
                     }
-                    Af[r * LF + i] = av;
-                    Pb[r * LC + i] = __float2bfloat16_rn(pv);
                 }
             }
         }

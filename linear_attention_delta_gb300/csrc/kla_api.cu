@@ -353,8 +353,7 @@ extern "C" kla_status kla_chunk_bwd_workspace_size(int B, int T, int H,
                                                    size_t* bytes) {
     if (!bytes || B < 0 || T < 0 || H < 0 || dk <= 0 || dv <= 0 || C <= 0)
         return KLA_ERR_INVALID_ARG;
-    *bytes = sizeof(float) *
-             kla::chunk_bwd_workspace_floats(B, T, H, dk, dv, C);
+    *bytes = kla::chunk_bwd_workspace_bytes(B, T, H, dk, dv, C);
     return KLA_OK;
 }
 
@@ -421,8 +420,7 @@ extern "C" kla_status kla_chunk_bwd(
     const bool empty = (long long)B * H == 0;
     if (!empty && T > 0) {
         if (!workspace || !aligned(workspace, 16)) return KLA_ERR_INVALID_ARG;
-        const size_t need =
-            sizeof(float) * kla::chunk_bwd_workspace_floats(B, T, H, dk, dv, C);
+        const size_t need = kla::chunk_bwd_workspace_bytes(B, T, H, dk, dv, C);
         if (workspace_bytes < need) return KLA_ERR_INVALID_ARG;
         const size_t elt = dtype == KLA_BF16 ? 2 : 4;
         const size_t tok = (size_t)B * T * H;
@@ -449,10 +447,11 @@ extern "C" kla_status kla_chunk_bwd(
                                              cudaMemcpyDeviceToDevice, s));
         return from_cuda(cudaMemsetAsync(h0_grad, 0, bytes, s));
     }
-    const size_t half = kla::chunk_bwd_workspace_floats(B, T, H, dk, dv, C) / 2;
+    const size_t nst = kla::chunk_bwd_state_floats(B, T, H, dk, dv, C);
     float* ws = static_cast<float*>(workspace);
     a.ckpt = ws;
-    a.dsck = ws + half;
+    a.dsck = ws + nst;
+    a.rec = reinterpret_cast<uint8_t*>(ws + 2 * nst);   // 16-byte aligned
     return from_cuda(kla::launch_chunk_bwd(a, s));
 }
 

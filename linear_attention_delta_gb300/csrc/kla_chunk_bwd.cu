@@ -1033,6 +1033,16 @@ __device__ __forceinline__ void qk_kk_tiles(float (&qk)[3][4],
 }
 }  // namespace lm
 
+// ------------------------------------ per-chunk records of the backward
+// What the two tensor-core backward kernels need of a chunk and that does
+// not depend on the state or on dO: T = A^{-1} and P (bf16, 64 x 64, rows
+// of 64, zeros above the diagonal), the cumulative log decay g, beta and
+// ||k||^2 (fp32), one record per (batch, head, chunk) in the workspace.
+namespace brec {
+constexpr int T_OFF = 0, P_OFF = 8192, G_OFF = 16384, B_OFF = 16640,
+              N_OFF = 16896, BYTES = 17152;
+}  // namespace brec
+
 template <typename IO>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 kla_bwd_grad_lm_kernel(BwdArgs a) {
@@ -1085,7 +1095,8 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
     const float* Sg = a.ckpt + ((size_t)bh * nch + ch) * DK * dv;
     const float* dSg = a.dsck + ((size_t)bh * nch + ch) * DK * dv;
 
-    {   // q, k rows (bf16, 16-byte loads straight to shared memory), gates
+    {   // q, k rows (bf16, 16-byte loads straight to shared memory); T, P
+        // (bf16), g, beta and ||k||^2 from the chunk's record
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int idx = tid + u * kBwdThreads;   // 64 rows x 16 chunks
@@ -1102,78 +1113,28 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
             *reinterpret_cast<uint4*>(Qb + r * LQ + 8 * c8) = qv;
             *reinterpret_cast<uint4*>(Kb + r * LQ + 8 * c8) = kv;
         }
+        const uint8_t* rec = a.rec + ((size_t)bh * nch + ch) * brec::BYTES;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {   // 512 pieces of 16 bytes each
+            const int u = tid + m * kBwdThreads, r = u >> 3, c8 = u & 7;
+            *reinterpret_cast<uint4*>(Tb + r * LC + 8 * c8) =
+                reinterpret_cast<const uint4*>(rec + brec::T_OFF)[u];
+            *reinterpret_cast<uint4*>(Pb + r * LC + 8 * c8) =
+                reinterpret_cast<const uint4*>(rec + brec::P_OFF)[u];
+        }
         if (tid < C) {
-            const int t = t0 + tid;
-            const size_t off = ((size_t)b * T + t) * H + h;
-            gs[tid] = t < T ? a.log_alpha[off] : 0.f;
-            bs[tid] = t < T ? a.eta[off] : 0.f;
+            gs[tid] = reinterpret_cast<const float*>(rec + brec::G_OFF)[tid];
+            bs[tid] = reinterpret_cast<const float*>(rec + brec::B_OFF)[tid];
+            nrm[tid] = reinterpret_cast<const float*>(rec + brec::N_OFF)[tid];
             db[tid] = dgam[tid] = dlam[tid] = 0.f;
         }
         if (tid == 0) dgc[0] = 0.f;
-        // zero P (its upper part is never written) and the final phase's
-        // Gamma o dP happens over S later (cleared there)
-        for (int i = tid; i < C * LC / 2; i += kBwdThreads)
-            reinterpret_cast<uint32_t*>(Pb)[i] = 0u;
-    }
-    __syncthreads();
-    {   // ||k||^2 (four threads per row), beta, cumulative decay
-        const int r = tid >> 2, q4 = tid & 3;
-        const float n = row_norm2(Kb, r, q4);
-        if (q4 == 0) {
-            nrm[r] = n;
-            const float denom = n + a.eps;
-            if (!a.gdn) bs[r] = denom == 0.f ? 0.f : bs[r] / denom;
-        }
-        if (warp == 0) {   // inclusive scan of the 64 log decays
-            float x0 = gs[2 * lane], x1 = gs[2 * lane + 1];
-            float s = x0 + x1;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, s, off);
-                if (lane >= off) s += y;
-            }
-            gs[2 * lane] = s - x1;
-            gs[2 * lane + 1] = s;
-        }
     }
     __syncthreads();
     if (tid < C) {
         gam[tid] = expf(gs[tid]);
         lam[tid] = expf(gs[C - 1] - gs[tid]);
         gb[tid] = -gam[tid] * bs[tid];
-    }
-    // A (unit lower, fp32, into F0) and P (bf16) from K K^T and Q K^T on the
-    // tensor cores: the 20 lower 16 x 8 tiles, dealt out to the warps
-    {
-        float qk[3][4], kk[3][4];
-        int mt[3], nt[3];
-        qk_kk_tiles(qk, kk, mt, nt, Qb, Kb, warp, lane);
-#pragma unroll
-        for (int x = 0; x < 3; ++x) {
-            if (x == 2 && warp >= 4) break;
-#pragma unroll
-            for (int hm = 0; hm < 2; ++hm) {
-                const int r = 16 * mt[x] + g8 + 8 * hm;
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int i = 8 * nt[x] + 2 * t4 + e;
-                    float av = i == r ? 1.f : 0.f, pv = 0.f;
-                    if (i <= r) {
-                        const float dec = expf(gs[r] - gs[i]);
-                        pv = dec * qk[x][2 * hm + e];
-                        if (i < r) av = bs[r] * dec * kk[x][2 * hm + e];
-                    }
-                    F0f[r * LF + i] = av;
-                    Pb[r * LC + i] = __float2bfloat16_rn(pv);
-                }
-            }
-        }
-    }
-    __syncthreads();
-    invert_lower64(F0f, LF, F1f, LF, Xf);   // lower part of F1 (X free yet)
-    for (int i = tid; i < C * C; i += kBwdThreads) {   // T (bf16, lower)
-        const int r = i >> 6, c = i & 63;
-        Tb[r * LC + c] = __float2bfloat16_rn(c <= r ? F1f[r * LF + c] : 0.f);
     }
 
     // dq, dk of this warp's rows 16 mo .. and columns 64 co .. (fragments)
@@ -1648,20 +1609,159 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
     }
 }
 
+// One CTA per (batch, head, chunk), all chunks in parallel: q, k and the
+// gates of the chunk, beta from ||k||^2, the cumulative decay, A and P from
+// K K^T and Q K^T on the tensor cores, T = A^{-1}; the record.
+namespace bp {
+constexpr int QB = 0;
+constexpr int KB = QB + lm::C * lm::LQ * 2;
+constexpr int PB = KB + lm::C * lm::LQ * 2;
+constexpr int AF = PB + lm::C * lm::LC * 2;
+constexpr int TF = AF + lm::C * lm::LF * 4;
+constexpr int YS = TF + lm::C * lm::LF * 4;   // 8 warps x 16 x 8 fp32
+constexpr int VEC = YS + 8 * 128 * 4;         // gs, bs, nrm
+constexpr int BYTES = VEC + 3 * lm::C * 4;
+static_assert(2 * (BYTES + 1024) <= 233472, "two CTAs per SM");
+}  // namespace bp
+
+template <typename IO>
+__global__ void __launch_bounds__(kBwdThreads, 2)
+kla_bwd_prep_kernel(BwdArgs a) {
+    using namespace lm;
+    extern __shared__ __align__(16) uint8_t smraw[];
+    bf16* Qb = reinterpret_cast<bf16*>(smraw + bp::QB);
+    bf16* Kb = reinterpret_cast<bf16*>(smraw + bp::KB);
+    bf16* Pb = reinterpret_cast<bf16*>(smraw + bp::PB);
+    float* Af = reinterpret_cast<float*>(smraw + bp::AF);
+    float* Tf = reinterpret_cast<float*>(smraw + bp::TF);
+    float* Ys = reinterpret_cast<float*>(smraw + bp::YS);
+    float* gs = reinterpret_cast<float*>(smraw + bp::VEC);
+    float* bs = gs + C;
+    float* nrm = gs + 2 * C;
+
+    const int T = a.T, H = a.H;
+    const int nch = (T + C - 1) / C;
+    const long blk = blockIdx.x;
+    const int bh = (int)(blk / nch), ch = (int)(blk % nch);
+    const int b = bh / H, h = bh % H;
+    const int t0 = ch * C;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g8 = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {   // q, k: 64 rows x 16 pieces of 16 bytes
+        const int idx = tid + u * kBwdThreads;
+        const int r = idx >> 4, c8 = idx & 15;
+        const int t = t0 + r;
+        uint4 qv = make_uint4(0, 0, 0, 0), kv = make_uint4(0, 0, 0, 0);
+        if (t < T) {
+            const size_t off = (((size_t)b * T + t) * H + h) * DK + 8 * c8;
+            qv = *reinterpret_cast<const uint4*>(
+                static_cast<const IO*>(a.q) + off);
+            kv = *reinterpret_cast<const uint4*>(
+                static_cast<const IO*>(a.k) + off);
+        }
+        *reinterpret_cast<uint4*>(Qb + r * LQ + 8 * c8) = qv;
+        *reinterpret_cast<uint4*>(Kb + r * LQ + 8 * c8) = kv;
+    }
+    if (tid < C) {
+        const int t = t0 + tid;
+        const size_t off = ((size_t)b * T + t) * H + h;
+        gs[tid] = t < T ? a.log_alpha[off] : 0.f;
+        bs[tid] = t < T ? a.eta[off] : 0.f;
+    }
+    for (int i = tid; i < C * LC / 2; i += kBwdThreads)   // P's upper part
+        reinterpret_cast<uint32_t*>(Pb)[i] = 0u;
+    __syncthreads();
+    {   // ||k||^2 (four threads per row), beta, cumulative decay
+        const int r = tid >> 2, q4 = tid & 3;
+        const float n = row_norm2(Kb, r, q4);
+        if (q4 == 0) {
+            nrm[r] = n;
+            const float denom = n + a.eps;
+            if (!a.gdn) bs[r] = denom == 0.f ? 0.f : bs[r] / denom;
+        }
+        if (warp == 0) {   // inclusive scan of the 64 log decays
+            const float x0 = gs[2 * lane], x1 = gs[2 * lane + 1];
+            float sc = x0 + x1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, sc, off);
+                if (lane >= off) sc += y;
+            }
+            gs[2 * lane] = sc - x1;
+            gs[2 * lane + 1] = sc;
+        }
+    }
+    __syncthreads();
+    {   // A (unit lower, fp32) and P (bf16) from K K^T and Q K^T
+        float qk[3][4], kk[3][4];
+        int mt[3], nt[3];
+        qk_kk_tiles(qk, kk, mt, nt, Qb, Kb, warp, lane);
+#pragma unroll
+        for (int x = 0; x < 3; ++x) {
+            if (x == 2 && warp >= 4) break;
+#pragma unroll
+            for (int hm = 0; hm < 2; ++hm) {
+                const int r = 16 * mt[x] + g8 + 8 * hm;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int i = 8 * nt[x] + 2 * t4 + e;
+                    float av = i == r ? 1.f : 0.f, pv = 0.f;
+                    if (i <= r) {
+                        const float dec = expf(gs[r] - gs[i]);
+                        pv = dec * qk[x][2 * hm + e];
+                        if (i < r) av = bs[r] * dec * kk[x][2 * hm + e];
+                    }
+                    Af[r * LF + i] = av;
+                    Pb[r * LC + i] = __float2bfloat16_rn(pv);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    invert_lower64(Af, LF, Tf, LF, Ys);   // ends with a barrier
+    uint8_t* rec = a.rec + ((size_t)bh * nch + ch) * brec::BYTES;
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {   // T and P rows, 8 bf16 per 16 bytes
+        const int u = tid + m * kBwdThreads;   // 512 pieces each
+        const int r = u >> 3, c8 = u & 7;
+        float tv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = 8 * c8 + e;
+            tv[e] = c <= r ? Tf[r * LF + c] : 0.f;
+        }
+        uint4 tw;
+        tw.x = tc::pack_bf16x2(tv[0], tv[1]);
+        tw.y = tc::pack_bf16x2(tv[2], tv[3]);
+        tw.z = tc::pack_bf16x2(tv[4], tv[5]);
+        tw.w = tc::pack_bf16x2(tv[6], tv[7]);
+        *reinterpret_cast<uint4*>(rec + brec::T_OFF + (r * C + 8 * c8) * 2) =
+            tw;
+        *reinterpret_cast<uint4*>(rec + brec::P_OFF + (r * C + 8 * c8) * 2) =
+            *reinterpret_cast<const uint4*>(Pb + r * LC + 8 * c8);
+    }
+    if (tid < C) {
+        reinterpret_cast<float*>(rec + brec::G_OFF)[tid] = gs[tid];
+        reinterpret_cast<float*>(rec + brec::B_OFF)[tid] = bs[tid];
+        reinterpret_cast<float*>(rec + brec::N_OFF)[tid] = nrm[tid];
+    }
+}
+
 // ------------------------- reverse state recurrence, bf16 operand tiles
 // kla_bwd_state_kernel's per-chunk algebra for bf16, dk = 128, C = 64 and
-// 64-column dv slices, every product on the tensor cores: A and P from
-// K K^T and Q K^T of the exact bf16 inputs, dU~ = P^T dO + Diag(lambda) K dS',
-// dF = T^T dU~ and dS = gamma_C dS' + Q^T Diag(gamma) dO
+// 64-column dv slices, every product on the tensor cores: dU~ = P^T dO +
+// Diag(lambda) K dS', dF = T^T dU~ and dS = gamma_C dS' + Q^T Diag(gamma) dO
 // - K^T Diag(gamma beta) dF as m16n8k16 MMAs (bf16 operands, fp32
 // accumulation) whose operands are bf16 tiles read by ldmatrix, in the
-// layout of kla_bwd_grad_lm_kernel.  dS itself stays in fp32 registers for
-// the whole walk (warp w owns key rows 16 w .. 16 w + 15, all 64 columns of
-// the slice) and is copied to shared memory in bf16, as the operand of
-// K dS', once per chunk.
+// layout of kla_bwd_grad_lm_kernel; T, P and the gates come from the
+// chunk's record (kla_bwd_prep_kernel).  dS itself stays in fp32 registers
+// for the whole walk (warp w owns key rows 16 w .. 16 w + 15, all 64
+// columns of the slice) and is copied to shared memory in bf16, as the
+// operand of K dS', once per chunk.
 namespace sm2 {
 constexpr int C = 64, DK = 128, DV = 64;
-constexpr int LQ = DK + 8, LC = C + 8, LV = DV + 8, LF = C + 1;
+constexpr int LQ = DK + 8, LC = C + 8, LV = DV + 8;
 constexpr int QB = 0;
 constexpr int KB = QB + C * LQ * 2;
 constexpr int DOB = KB + C * LQ * 2;   // dO
@@ -1671,15 +1771,13 @@ constexpr int TB = PB + C * LC * 2;
 constexpr int DSB = TB + C * LC * 2;   // dS' (DK x DV)
 constexpr int DUB = DSB + DK * LV * 2;
 constexpr int DFS = DUB + C * LV * 2;  // -Diag(gamma beta) dF
-constexpr int AF = DFS + C * LV * 2;   // A (fp32)
-constexpr int TF = AF + C * LF * 4;    // A^{-1} (fp32)
-constexpr int VEC = TF + C * LF * 4;   // gs, bs, gam, lam
+constexpr int VEC = DFS + C * LV * 2;  // gs, bs, gam, lam
 constexpr int BYTES = VEC + 4 * C * 4;
 static_assert(BYTES <= 232448, "shared memory");
 static_assert(KB % 16 == 0 && DOB % 16 == 0 && DOG % 16 == 0 &&
                   PB % 16 == 0 && TB % 16 == 0 && DSB % 16 == 0 &&
-                  DUB % 16 == 0 && DFS % 16 == 0,
-              "ldmatrix rows are 16-byte aligned");
+                  DUB % 16 == 0 && DFS % 16 == 0 && VEC % 16 == 0,
+              "16-byte aligned rows");
 }  // namespace sm2
 
 template <typename IO>
@@ -1700,8 +1798,6 @@ kla_bwd_state_lm_kernel(BwdArgs a) {
     bf16* dSb = reinterpret_cast<bf16*>(smraw + DSB);
     bf16* dUb = reinterpret_cast<bf16*>(smraw + DUB);
     bf16* dFs = reinterpret_cast<bf16*>(smraw + DFS);
-    float* Af = reinterpret_cast<float*>(smraw + AF);
-    float* Tf = reinterpret_cast<float*>(smraw + TF);
     float* gs = reinterpret_cast<float*>(smraw + VEC);
     float* bs = gs + C;
     float* gam = gs + 2 * C;
@@ -1727,17 +1823,15 @@ kla_bwd_state_lm_kernel(BwdArgs a) {
             dS[nt][e] =
                 a.dhT ? a.dhT[((size_t)bh * DK + c) * dv + j0 + j] : 0.f;
         }
-    for (int i = tid; i < C * LC / 2; i += kBwdThreads)   // P's upper part
-        reinterpret_cast<uint32_t*>(Pb)[i] = 0u;
 
-    // The tiles of a chunk (q, k: 64 x 128, dO: 64 x 64, bf16) and its gates
-    // are loaded into registers, 16 bytes a load, while the previous chunk
-    // computes, and stored to shared memory (unconverted) when it is done.
+    // A chunk's tiles (q, k: 64 x 128, dO: 64 x 64, bf16) and its record (T,
+    // P, g, beta) are loaded into registers, 16 bytes a load, while the
+    // previous chunk computes, and stored to shared memory (unconverted)
+    // when it is done.
     const uint4* q4 = static_cast<const uint4*>(a.q);
     const uint4* k4 = static_cast<const uint4*>(a.k);
     const uint4* d4 = static_cast<const uint4*>(a.dout);
-    uint4 pq[4], pk[4], pd[2];
-    float pla = 0.f, peta = 0.f;
+    uint4 pq[4], pk[4], pd[2], pt[2], pp[2], pg;
     auto fetch = [&](int c) {
         const int t0c = c * C;
 #pragma unroll
@@ -1755,12 +1849,14 @@ kla_bwd_state_lm_kernel(BwdArgs a) {
                 ((((size_t)b * T + t) * H + h) * dv + j0) / 8 + tid % 8;
             pd[m] = t < T ? d4[e] : make_uint4(0, 0, 0, 0);
         }
-        if (tid < C) {
-            const int t = t0c + tid;
-            const size_t off = ((size_t)b * T + t) * H + h;
-            pla = t < T ? a.log_alpha[off] : 0.f;
-            peta = t < T ? a.eta[off] : 0.f;
+        const uint4* rc = reinterpret_cast<const uint4*>(
+            a.rec + ((size_t)bh * nch + c) * brec::BYTES);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {   // piece tid + 256 m of T and of P
+            pt[m] = rc[brec::T_OFF / 16 + tid + 256 * m];
+            pp[m] = rc[brec::P_OFF / 16 + tid + 256 * m];
         }
+        if (tid < 32) pg = rc[brec::G_OFF / 16 + tid];   // g, then beta
     };
     fetch(nch - 1);
     // this warp's tiles of the C x DV products: rows 16 (w >> 1), columns
@@ -1775,13 +1871,14 @@ kla_bwd_state_lm_kernel(BwdArgs a) {
             *reinterpret_cast<uint4*>(Kb + r * LQ + 8 * c8) = pk[m];
         }
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
+        for (int m = 0; m < 2; ++m) {
             *reinterpret_cast<uint4*>(dOb + (tid / 8 + 32 * m) * LV +
                                       8 * (tid % 8)) = pd[m];
-        if (tid < C) {
-            gs[tid] = pla;
-            bs[tid] = peta;
+            const int u = tid + 256 * m, r = u >> 3, c8 = u & 7;
+            *reinterpret_cast<uint4*>(Tb + r * LC + 8 * c8) = pt[m];
+            *reinterpret_cast<uint4*>(Pb + r * LC + 8 * c8) = pp[m];
         }
+        if (tid < 32) reinterpret_cast<uint4*>(gs)[tid] = pg;
         {   // dL/dS at the end of this chunk: to the workspace (fp32) and,
             // in bf16, to shared memory as an operand
             float* out = a.dsck + ((size_t)bh * nch + ch) * DK * dv + j0;
@@ -1799,58 +1896,14 @@ kla_bwd_state_lm_kernel(BwdArgs a) {
         }
         __syncthreads();
         if (ch > 0) fetch(ch - 1);   // in flight during this chunk
-        {   // ||k||^2 (four threads per row), beta, cumulative decay
-            const int r = tid >> 2, q4i = tid & 3;
-            const float n = lm::row_norm2(Kb, r, q4i);
-            if (q4i == 0 && !a.gdn) {
-                const float denom = n + a.eps;
-                bs[r] = denom == 0.f ? 0.f : bs[r] / denom;
-            }
-            if (warp == 0) {   // inclusive scan of the 64 log decays
-                const float x0 = gs[2 * lane], x1 = gs[2 * lane + 1];
-                float s = x0 + x1;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, s, off);
-                    if (lane >= off) s += y;
-                }
-                gs[2 * lane] = s - x1;
-                gs[2 * lane + 1] = s;
-            }
-        }
-        __syncthreads();
         if (tid < C) {
             gam[tid] = expf(gs[tid]);
             lam[tid] = expf(gs[C - 1] - gs[tid]);
         }
-        // A (fp32) and P (bf16) from K K^T and Q K^T: the 20 lower tiles
-        {
-            float qk[3][4], kk[3][4];
-            int mt[3], nt[3];
-            lm::qk_kk_tiles(qk, kk, mt, nt, Qb, Kb, warp, lane);
-#pragma unroll
-            for (int x = 0; x < 3; ++x) {
-                if (x == 2 && warp >= 4) break;
-#pragma unroll
-                for (int hm = 0; hm < 2; ++hm) {
-                    const int r = 16 * mt[x] + g8 + 8 * hm;
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int i = 8 * nt[x] + 2 * t4 + e;
-                        float av = i == r ? 1.f : 0.f, pv = 0.f;
-                        if (i <= r) {
-                            const float dec = expf(gs[r] - gs[i]);
-                            pv = dec * qk[x][2 * hm + e];
-                            if (i < r) av = bs[r] * dec * kk[x][2 * hm + e];
-                        }
-                        Af[r * LF + i] = av;
-                        Pb[r * LC + i] = __float2bfloat16_rn(pv);
-                    }
-                }
-            }
-        }
         __syncthreads();
-        {   // Diag(gamma) dO (bf16)
+
+        // Diag(gamma) dO (bf16) and dU~ = P^T dO + Diag(lambda) K dS'
+        {
             const int r = tid >> 2, c16 = 16 * (tid & 3);
             const float gr = gam[r];
 #pragma unroll
@@ -1861,15 +1914,6 @@ kla_bwd_state_lm_kernel(BwdArgs a) {
                     tc::pack_bf16x2(gr * x0, gr * x1);
             }
         }
-        // T = A^{-1} (ends with a barrier; dU~'s tile is free scratch here)
-        lm::invert_lower64(Af, LF, Tf, LF, reinterpret_cast<float*>(dUb));
-        for (int i = tid; i < C * C; i += kBwdThreads) {   // T (bf16, lower)
-            const int r = i >> 6, c = i & 63;
-            Tb[r * LC + c] = __float2bfloat16_rn(c <= r ? Tf[r * LF + c] : 0.f);
-        }
-        __syncthreads();
-
-        // dU~ = P^T dO + Diag(lambda) K dS'
         {
             float kd[4][4] = {}, pd4[4][4] = {};
 #pragma unroll
@@ -1925,13 +1969,13 @@ kla_bwd_state_lm_kernel(BwdArgs a) {
 #pragma unroll
             for (int hm = 0; hm < 2; ++hm) {
                 const int r = 16 * pm + g8 + 8 * hm;
-                const float s = -gam[r] * bs[r];
+                const float sc = -gam[r] * bs[r];
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
                     const int j = pn + 8 * nt + 2 * t4;
                     *reinterpret_cast<uint32_t*>(dFs + r * LV + j) =
-                        tc::pack_bf16x2(s * df[nt][2 * hm],
-                                        s * df[nt][2 * hm + 1]);
+                        tc::pack_bf16x2(sc * df[nt][2 * hm],
+                                        sc * df[nt][2 * hm + 1]);
                 }
             }
         }
@@ -1995,9 +2039,33 @@ cudaError_t launch_shape(const BwdArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const long bhs = (long)a.B * a.H;
     const long nch = (a.T + a.C - 1) / a.C;
+    auto a16 = [](const void* p) {
+        return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+    };
+    // the gradient step on the tensor cores (16-byte loads of q, k, v,
+    // o_grad)
+    const bool grad_tc = DK == kTcDK && DVT == 32 &&
+                         std::is_same<IO, __nv_bfloat16>::value &&
+                         a.C == kTcC && a16(a.q) && a16(a.k) && a16(a.v) &&
+                         a16(a.dout);
+    const bool state_tc = DK == kTcDK && DVS == kTcDV &&
+                          std::is_same<IO, __nv_bfloat16>::value &&
+                          state_tc_ok(a);
+    if constexpr (DK == kTcDK && std::is_same<IO, __nv_bfloat16>::value) {
+        if (grad_tc || state_tc) {   // their per-chunk records
+            if (!a.rec) return cudaErrorInvalidValue;
+            auto kp = kla_bwd_prep_kernel<IO>;
+            e = cudaFuncSetAttribute(
+                kp, cudaFuncAttributeMaxDynamicSharedMemorySize, bp::BYTES);
+            if (e != cudaSuccess) return e;
+            kp<<<(unsigned)(bhs * nch), kBwdThreads, bp::BYTES, stream>>>(a);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+    }
     if constexpr (DK == kTcDK && DVS == kTcDV &&
                   std::is_same<IO, __nv_bfloat16>::value) {
-        if (state_tc_ok(a)) {   // the reverse recurrence on the tensor cores
+        if (state_tc) {   // the reverse recurrence on the tensor cores
             auto kt = kla_bwd_state_lm_kernel<IO>;
             e = cudaFuncSetAttribute(
                 kt, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2::BYTES);
@@ -2016,12 +2084,7 @@ cudaError_t launch_shape(const BwdArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if constexpr (DK == kTcDK && DVT == 32 &&
                   std::is_same<IO, __nv_bfloat16>::value) {
-        auto a16 = [](const void* p) {
-            return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
-        };
-        // the per-chunk products on the tensor cores (16-byte loads of q,
-        // k, v, o_grad)
-        if (a.C == kTcC && a16(a.q) && a16(a.k) && a16(a.v) && a16(a.dout)) {
+        if (grad_tc) {
             auto km = kla_bwd_grad_lm_kernel<IO>;
             e = cudaFuncSetAttribute(
                 km, cudaFuncAttributeMaxDynamicSharedMemorySize, lm::BYTES);
@@ -2065,11 +2128,20 @@ cudaError_t launch_dtype(const BwdArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-size_t chunk_bwd_workspace_floats(int B, int T, int H, int dk, int dv,
-                                  int C) {
+size_t chunk_bwd_state_floats(int B, int T, int H, int dk, int dv, int C) {
     if (C <= 0) return 0;
     const size_t nch = (size_t)(T + C - 1) / C;
-    return 2 * (size_t)B * H * nch * dk * dv;
+    return (size_t)B * H * nch * dk * dv;
+}
+
+size_t chunk_bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int C) {
+    if (C <= 0) return 0;
+    const size_t nch = (size_t)(T + C - 1) / C;
+    const size_t rec = (dk == kTcDK && C == kTcC)
+                           ? (size_t)B * H * nch * brec::BYTES
+                           : 0;
+    return 2 * sizeof(float) * chunk_bwd_state_floats(B, T, H, dk, dv, C) +
+           rec;
 }
 
 cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t stream) {

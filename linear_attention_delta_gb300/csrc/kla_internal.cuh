@@ -80,6 +80,7 @@ struct BwdArgs {
     float* dsck;         // workspace: dL/dS at every chunk end
     int B, T, H, dk, dv, C;
     kla_dtype dtype;
+    uint8_t* rec = nullptr;   // workspace: per-chunk records (tensor-core path)
 };
 
 struct DecodeArgs {
@@ -130,7 +131,11 @@ cudaError_t launch_state_selftest(cudaStream_t stream);
 // recurrence and the per-chunk gradients (CUDA cores, fp32).
 cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_precond_keys(const PrecondArgs& a, cudaStream_t stream);
-size_t chunk_bwd_workspace_floats(int B, int T, int H, int dk, int dv, int C);
+// Workspace of kla_chunk_bwd: the fp32 states at every chunk start and
+// dL/dS at every chunk end (chunk_bwd_state_floats each), then, for dk = 128
+// and C = 64, the tensor-core kernels' per-chunk records.
+size_t chunk_bwd_state_floats(int B, int T, int H, int dk, int dv, int C);
+size_t chunk_bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int C);
 // Every argument check of kla_chunk_bwd except those on the workspace and
 // the step rule (a.ckpt, a.dsck are not looked at).
 kla_status check_chunk_bwd_args(const BwdArgs& a);

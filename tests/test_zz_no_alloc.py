@@ -4,10 +4,10 @@ its scratch in a fixed 32 MiB array inside the library.
 
 This file is named so that pytest collects it last: its GPU test checks the
 entry point against kla_chunk_bwd (caller-provided workspace) on three calls
-in a row -- a problem that fills the array exactly, a small one, then the
-large one again with new inputs, so that the third call finds the first two
-calls' contents all over the array; it must pass both alone in a fresh
-process and after every other test.
+in a row -- the largest problem of its shape that fits the array, a small
+one, then the large one again with new inputs, so that the third call finds
+the first two calls' contents all over the array; it must pass both alone in
+a fresh process and after every other test.
 """
 import ctypes
 from dataclasses import replace
@@ -26,9 +26,11 @@ ORACLE_KEYS = {"q_grad": "dq", "k_grad": "dk", "v_grad": "dv",
                "log_alpha_grad": "dlog_alpha", "eta_grad": "deta",
                "h0_grad": "dh0"}
 LIMIT = 32 << 20
-# B, T, H with dk = dv = 128, C = 64 whose workspace is exactly the array:
-# 2 tensors x B H ceil(T/64) x 128 x 128 fp32 = 2 x 256 x 64 KiB
-FULL = dict(B=1, T=4096, H=4)
+# per (batch, head, chunk) with dk = dv = 128, C = 64: two fp32 128 x 128
+# states and a 17,152-byte record; B1 H4 T3584 is 224 of them, the most of
+# whole chunks that fit (226 would; 228, at T = 3585, do not)
+PER_CHUNK = 2 * 128 * 128 * 4 + 17152
+FULL = dict(B=1, T=3584, H=4)
 
 
 def _call(lib, T, q=0x10000):
@@ -41,17 +43,19 @@ def _call(lib, T, q=0x10000):
                                      None)
 
 
-def test_size_limit_is_exact_and_checked_after_the_arguments():
+def test_size_limit_is_checked_after_the_arguments():
     """Host-side only (nothing is launched on any of these paths): the
-    workspace of B1 T4096 H4 d128 C64 is exactly 32 MiB; one more token (one
-    more chunk) is refused with KLA_ERR_UNSUPPORTED_SHAPE; a null input
-    is reported as KLA_ERR_INVALID_ARG even when the problem is too large."""
+    workspace of B1 T3584 H4 d128 C64 is 224 chunk records and fits in the
+    32 MiB; one more token (four more chunks) does not and is refused with
+    KLA_ERR_UNSUPPORTED_SHAPE; a null input is reported as
+    KLA_ERR_INVALID_ARG even when the problem is too large."""
     lib = kla.load_library()
     assert kla.chunk_bwd_workspace_size(FULL["B"], FULL["T"], FULL["H"],
-                                        128, 128, 64) == LIMIT
-    assert kla.chunk_bwd_workspace_size(1, 4097, 4, 128, 128, 64) > LIMIT
-    assert _call(lib, 4097) == -2          # KLA_ERR_UNSUPPORTED_SHAPE
-    assert _call(lib, 4097, q=None) == -1  # KLA_ERR_INVALID_ARG first
+                                        128, 128, 64) == 224 * PER_CHUNK
+    assert 224 * PER_CHUNK <= LIMIT < 228 * PER_CHUNK
+    assert kla.chunk_bwd_workspace_size(1, 3585, 4, 128, 128, 64) > LIMIT
+    assert _call(lib, 3585) == -2          # KLA_ERR_UNSUPPORTED_SHAPE
+    assert _call(lib, 3585, q=None) == -1  # KLA_ERR_INVALID_ARG first
     assert _call(lib, 1 << 20) == -2
 
 
@@ -71,8 +75,8 @@ def _case(w, seed, **sizes):
 
 @pytest.mark.gpu
 def test_noalloc_backward_matches_workspace_backward_three_calls():
-    """Three calls in a row: the array-filling 1B-layer problem, a small fp32
-    one, then the large one again on new inputs.  Each result equals the one
+    """Three calls in a row: the largest 1B-layer-shaped problem that fits
+    the array, a small fp32 one, then the large one again on new inputs.  Each result equals the one
     kla_chunk_bwd gives with a caller-allocated workspace up to the order of
     the kernels' atomic sums; the small one and the last large one are also
     held to the oracle's reverse mode at the fp32 / bf16 bounds."""

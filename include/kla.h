@@ -399,7 +399,9 @@ KLA_API kla_status kla_decode_step_kw(const void* q, const void* k,
  * state at every chunk start and the gradient of the loss with respect to
  * the state at every chunk end) and, for dk = 128 and C = 64, 17,152 bytes
  * per (batch, head, chunk) of per-chunk records (the inverse, P and the
- * gates of the chunk) for the tensor-core kernels.  Writes 0 for an empty
+ * gates of the chunk) for the tensor-core kernels, plus, when also
+ * dv = 128, 16,640 bytes per (batch, head, chunk) for the records of the
+ * two-kernel forward that writes the checkpoints.  Writes 0 for an empty
  * problem.  Errors:
  * KLA_ERR_INVALID_ARG (null `bytes`, negative size, C <= 0).
  */
@@ -467,7 +469,7 @@ KLA_API kla_status kla_chunk_bwd(const void* q, const void* k, const void* v,
  * loads the library holds it until the process exits).  The argument checks
  * of kla_chunk_bwd run first (KLA_ERR_INVALID_ARG, KLA_ERR_UNSUPPORTED_SHAPE);
  * then a problem whose kla_chunk_bwd_workspace_size exceeds 32 MiB (for
- * dk = dv = 128: B * H * ceil(T / C) > 226 with C = 64, > 256 with other C)
+ * dk = dv = 128: B * H * ceil(T / C) > 203 with C = 64, > 256 with other C)
  * is rejected with KLA_ERR_UNSUPPORTED_SHAPE.  Either way nothing is
  * launched.
  *

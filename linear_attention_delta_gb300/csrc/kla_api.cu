@@ -451,7 +451,12 @@ extern "C" kla_status kla_chunk_bwd(
     float* ws = static_cast<float*>(workspace);
     a.ckpt = ws;
     a.dsck = ws + nst;
-    a.rec = reinterpret_cast<uint8_t*>(ws + 2 * nst);   // 16-byte aligned
+    if (dk == 128 && C == 64) {   // the tensor-core kernels' records
+        const size_t nch = ((size_t)T + C - 1) / C;
+        a.rec = reinterpret_cast<uint8_t*>(ws + 2 * nst);   // 16-byte aligned
+        if (dv == 128)   // and the two-kernel forward's, for the checkpoints
+            a.fwd_rec = a.rec + (size_t)B * H * nch * kla::bwdrec::BYTES;
+    }
     return from_cuda(kla::launch_chunk_bwd(a, s));
 }
 

@@ -1035,13 +1035,10 @@ __device__ __forceinline__ void qk_kk_tiles(float (&qk)[3][4],
 
 // ------------------------------------ per-chunk records of the backward
 // What the two tensor-core backward kernels need of a chunk and that does
-// not depend on the state or on dO: T = A^{-1} and P (bf16, 64 x 64, rows
-// of 64, zeros above the diagonal), the cumulative log decay g, beta and
-// ||k||^2 (fp32), one record per (batch, head, chunk) in the workspace.
-namespace brec {
-constexpr int T_OFF = 0, P_OFF = 8192, G_OFF = 16384, B_OFF = 16640,
-              N_OFF = 16896, BYTES = 17152;
-}  // namespace brec
+// not depend on the state or on dO (layout bwdrec): written by the
+// two-kernel forward's pre-pass when the checkpoints come from that path,
+// else by kla_bwd_prep_kernel.
+namespace brec = bwdrec;
 
 template <typename IO>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -2052,7 +2049,7 @@ cudaError_t launch_shape(const BwdArgs& a, cudaStream_t stream) {
                           std::is_same<IO, __nv_bfloat16>::value &&
                           state_tc_ok(a);
     if constexpr (DK == kTcDK && std::is_same<IO, __nv_bfloat16>::value) {
-        if (grad_tc || state_tc) {   // their per-chunk records
+        if ((grad_tc || state_tc) && !a.rec_ready) {   // their records
             if (!a.rec) return cudaErrorInvalidValue;
             auto kp = kla_bwd_prep_kernel<IO>;
             e = cudaFuncSetAttribute(
@@ -2140,20 +2137,33 @@ size_t chunk_bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int C) {
     const size_t rec = (dk == kTcDK && C == kTcC)
                            ? (size_t)B * H * nch * brec::BYTES
                            : 0;
+    const size_t fwd = (dk == kTcDK && dv == kTcDK && C == kTcC)
+                           ? chunk_tc2_workspace_bytes(B, T, H)
+                           : 0;
     return 2 * sizeof(float) * chunk_bwd_state_floats(B, T, H, dk, dv, C) +
-           rec;
+           rec + fwd;
 }
 
-cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t stream) {
-    if ((long)a.B * a.H == 0 || a.T == 0) return cudaSuccess;
-    if (a.C > kBwdMaxC) return cudaErrorInvalidValue;
-    // 1. states at every chunk start (a forward pass, o not written; the
-    // tensor-core kernel where it applies)
+cudaError_t launch_chunk_bwd(const BwdArgs& a_in, cudaStream_t stream) {
+    if ((long)a_in.B * a_in.H == 0 || a_in.T == 0) return cudaSuccess;
+    if (a_in.C > kBwdMaxC) return cudaErrorInvalidValue;
+    BwdArgs a = a_in;
+    // 1. states at every chunk start (a forward pass, o not written): the
+    // two-kernel tensor-core path, whose pre-pass also writes the
+    // backward's per-chunk records, where it applies; else the fused
+    // tensor-core kernel or the CUDA-core one
     FwdArgs f{a.q, a.k, a.v, a.log_alpha, a.eta, a.eps, a.gdn, a.h0,
               nullptr, nullptr, a.B, a.T, a.H, a.dk, a.dv, a.C, a.dtype};
     f.ckpt = a.ckpt;
-    cudaError_t e = chunk_tc_eligible(f) ? launch_chunk_tc(f, stream)
-                                         : launch_chunk_simt(f, stream);
+    cudaError_t e;
+    if (a.rec && a.fwd_rec && chunk_tc2_eligible(f)) {
+        f.bwd_rec = a.rec;
+        e = launch_chunk_tc2(f, a.fwd_rec, stream);
+        a.rec_ready = true;
+    } else {
+        e = chunk_tc_eligible(f) ? launch_chunk_tc(f, stream)
+                                 : launch_chunk_simt(f, stream);
+    }
     if (e != cudaSuccess) return e;
     // 2 and 3. dS' per chunk and dh0, then the gradients
     if (a.dtype == KLA_BF16) return launch_dtype<__nv_bfloat16>(a, stream);

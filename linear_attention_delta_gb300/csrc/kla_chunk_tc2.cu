@@ -126,6 +126,7 @@ struct PrepParams {
     float eps;
     int gdn;
     int T, H, nchunks;
+    uint8_t* brec;       // null, or the backward's records [B, H, nchunks]
 };
 
 // acc (16 x 8, fragment layout) += A (16 x 16 packed fp32 block) x
@@ -213,6 +214,9 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int bh = blockIdx.x / p.nchunks;
     const int b = bh / p.H, h = bh % p.H;
     const int t0 = c * kC;
+    uint8_t* brec = p.brec ? p.brec + ((size_t)bh * p.nchunks + c) *
+                                          bwdrec::BYTES
+                           : nullptr;
     constexpr uint64_t kLimit = 2000000000ull;
 
     if (tid == 0) {
@@ -309,6 +313,12 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
             const float denom = kk + p.eps;
             const float br = p.gdn ? et : (denom == 0.f ? 0.f : et / denom);
             betas[r] = br;
+            if (brec) {   // gates of the backward's record (g in natural log)
+                reinterpret_cast<float*>(brec + bwdrec::G_OFF)[r] =
+                    g2 * 0.6931471805599453f;
+                reinterpret_cast<float*>(brec + bwdrec::B_OFF)[r] = br;
+                reinterpret_cast<float*>(brec + bwdrec::N_OFF)[r] = kk;
+            }
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 if (m > I) break;
@@ -357,6 +367,9 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
                     v.z = tc::pack_bf16x2(e[4], e[5]);
                     v.w = tc::pack_bf16x2(e[6], e[7]);
                     *reinterpret_cast<uint4*>(out + kRecPTU + swz(r, i)) = v;
+                    if (brec)   // P, rows of 64, for the backward
+                        *reinterpret_cast<uint4*>(brec + bwdrec::P_OFF +
+                                                  (r * kC + i) * 2) = v;
                 }
             }
         }
@@ -423,6 +436,15 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
             v.z = tc::pack_bf16x2(tb.x * bb.x, tb.y * bb.y);
             v.w = tc::pack_bf16x2(tb.z * bb.z, tb.w * bb.w);
             *reinterpret_cast<uint4*>(out + kRecTU + swz(r, c0 + j)) = v;
+            if (brec) {   // T itself, rows of 64, for the backward
+                uint4 w;
+                w.x = tc::pack_bf16x2(ta.x, ta.y);
+                w.y = tc::pack_bf16x2(ta.z, ta.w);
+                w.z = tc::pack_bf16x2(tb.x, tb.y);
+                w.w = tc::pack_bf16x2(tb.z, tb.w);
+                *reinterpret_cast<uint4*>(brec + bwdrec::T_OFF +
+                                          (r * kC + col) * 2) = w;
+            }
         }
     }
     if (tid < kC) reinterpret_cast<float*>(out + kRecG)[tid] = g2s[tid];
@@ -1037,7 +1059,7 @@ cudaError_t launch_prep_tc2(const FwdArgs& a, void* rec, cudaStream_t stream) {
     cudaError_t e = set_smem((const void*)kla_prep_kernel, kPSmem, g_prep_attr);
     if (e != cudaSuccess) return e;
     PrepParams pp{a.log_alpha, a.eta, static_cast<uint8_t*>(rec), a.eps, a.gdn,
-                  a.T, a.H, nchunks};
+                  a.T, a.H, nchunks, a.bwd_rec};
     kla_prep_kernel<<<(unsigned)nprep, kPrepThreads, kPSmem, stream>>>(mq, mk,
                                                                       pp);
     return cudaGetLastError();

@@ -47,6 +47,9 @@ struct FwdArgs {
     // tensor-core kernel only: v is a zeroed [1, 64, H, dv] tile standing
     // for an all-zero V (every other load falls outside it and reads zeros)
     bool v_zero = false;
+    // two-kernel path only, may be null: the pre-pass also writes the
+    // backward's per-chunk records (bwdrec layout) here
+    uint8_t* bwd_rec = nullptr;
 };
 
 struct PrecondArgs {
@@ -81,7 +84,17 @@ struct BwdArgs {
     int B, T, H, dk, dv, C;
     kla_dtype dtype;
     uint8_t* rec = nullptr;   // workspace: per-chunk records (tensor-core path)
+    uint8_t* fwd_rec = nullptr;   // workspace: the forward pre-pass's records
+    bool rec_ready = false;   // rec written by the checkpointing forward
 };
+
+// Per-chunk record of the backward's tensor-core kernels (bytes): T = A^{-1}
+// and P (bf16, 64 x 64, rows of 64, zeros above the diagonal), the
+// cumulative log decay g (natural log), beta and ||k||^2 (fp32).
+namespace bwdrec {
+constexpr int T_OFF = 0, P_OFF = 8192, G_OFF = 16384, B_OFF = 16640,
+              N_OFF = 16896, BYTES = 17152;
+}  // namespace bwdrec
 
 struct DecodeArgs {
     const void* q;

@@ -27,10 +27,11 @@ ORACLE_KEYS = {"q_grad": "dq", "k_grad": "dk", "v_grad": "dv",
                "h0_grad": "dh0"}
 LIMIT = 32 << 20
 # per (batch, head, chunk) with dk = dv = 128, C = 64: two fp32 128 x 128
-# states and a 17,152-byte record; B1 H4 T3584 is 224 of them, the most of
-# whole chunks that fit (226 would; 228, at T = 3585, do not)
-PER_CHUNK = 2 * 128 * 128 * 4 + 17152
-FULL = dict(B=1, T=3584, H=4)
+# states, the backward's 17,152-byte record and the forward pre-pass's
+# 16,640-byte one; B1 H4 T3200 is 200 of them, the most of whole chunks
+# that fit (203 would; 204, at T = 3201, do not)
+PER_CHUNK = 2 * 128 * 128 * 4 + 17152 + 16640
+FULL = dict(B=1, T=3200, H=4)
 
 
 def _call(lib, T, q=0x10000):
@@ -45,17 +46,17 @@ def _call(lib, T, q=0x10000):
 
 def test_size_limit_is_checked_after_the_arguments():
     """Host-side only (nothing is launched on any of these paths): the
-    workspace of B1 T3584 H4 d128 C64 is 224 chunk records and fits in the
+    workspace of B1 T3200 H4 d128 C64 is 200 chunk records and fits in the
     32 MiB; one more token (four more chunks) does not and is refused with
     KLA_ERR_UNSUPPORTED_SHAPE; a null input is reported as
     KLA_ERR_INVALID_ARG even when the problem is too large."""
     lib = kla.load_library()
     assert kla.chunk_bwd_workspace_size(FULL["B"], FULL["T"], FULL["H"],
-                                        128, 128, 64) == 224 * PER_CHUNK
-    assert 224 * PER_CHUNK <= LIMIT < 228 * PER_CHUNK
-    assert kla.chunk_bwd_workspace_size(1, 3585, 4, 128, 128, 64) > LIMIT
-    assert _call(lib, 3585) == -2          # KLA_ERR_UNSUPPORTED_SHAPE
-    assert _call(lib, 3585, q=None) == -1  # KLA_ERR_INVALID_ARG first
+                                        128, 128, 64) == 200 * PER_CHUNK
+    assert 200 * PER_CHUNK <= LIMIT < 204 * PER_CHUNK
+    assert kla.chunk_bwd_workspace_size(1, 3201, 4, 128, 128, 64) > LIMIT
+    assert _call(lib, 3201) == -2          # KLA_ERR_UNSUPPORTED_SHAPE
+    assert _call(lib, 3201, q=None) == -1  # KLA_ERR_INVALID_ARG first
     assert _call(lib, 1 << 20) == -2
 
 

@@ -1399,8 +1399,9 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
                     if (t < T) {
                         const size_t off =
                             (((size_t)b * T + t) * H + h) * dv + j0 + j;
-                        static_cast<IO*>(a.dv_)[off] = from_f32<IO>(x0);
-                        static_cast<IO*>(a.dv_)[off + 1] = from_f32<IO>(x1);
+                        *reinterpret_cast<uint32_t*>(
+                            static_cast<IO*>(a.dv_) + off) =
+                            tc::pack_bf16x2(x0, x1);
                     }
                 }
                 dbp = quad_sum(dbp);
@@ -1463,11 +1464,9 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
             s += __shfl_xor_sync(0xffffffffu, s, off);
         if (lane == 0) atomicAdd(dgc, s);
     }
-    // dP (lower incl.) into F0, dA (strictly lower) into F1, zeros above
-    for (int i = tid; i < C * LF; i += kBwdThreads) F0f[i] = F1f[i] = 0.f;
-    for (int i = tid; i < C * LC / 2; i += kBwdThreads)
-        reinterpret_cast<uint32_t*>(Gdp)[i] = 0u;
-    __syncthreads();
+    // dP (lower incl.) into F0, dA (strictly lower) into F1 (only these
+    // entries are read below; the final tiles of Gamma o dP are written in
+    // full, zeros above the diagonal included)
 #pragma unroll
     for (int x = 0; x < 3; ++x) {
         const int idx = warp + 8 * x;
@@ -1527,41 +1526,53 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
     }
     __syncthreads();
 
-    // per row: dg, deta, dn (dn replaces dbeta in db); D + D^T (bf16)
-    if (tid < C) {
-        const int r = tid;
-        float gsum = dgam[r] * gam[r] - dlam[r] * lam[r];
-        for (int i = 0; i <= r; ++i) gsum += F2f[r * LF + i];
-        for (int rr = r; rr < C; ++rr) gsum -= F2f[rr * LF + r];
-        if (r == C - 1) {
-            for (int t = 0; t < C; ++t) gsum = fmaf(dlam[t], lam[t], gsum);
-            gsum = fmaf(dgc[0], gam[C - 1], gsum);
+    // per row (four threads each): dg, deta, dn (dn replaces dbeta in db);
+    // D + D^T (bf16) from D's strictly lower part
+    {
+        const int r = tid >> 2, q4 = tid & 3;
+        float sp = 0.f;
+        for (int i = q4; i <= r; i += 4) sp += F2f[r * LF + i];
+        for (int rr = r + q4; rr < C; rr += 4) sp -= F2f[rr * LF + r];
+        if (r == C - 1)
+            for (int t = q4; t < C; t += 4) sp = fmaf(dlam[t], lam[t], sp);
+        sp = quad_sum(sp);
+        if (q4 == 0) {
+            float gsum = sp + dgam[r] * gam[r] - dlam[r] * lam[r];
+            if (r == C - 1) gsum = fmaf(dgc[0], gam[C - 1], gsum);
+            dg[r] = gsum;
+            const float dbeta = db[r];
+            float deta, dn = 0.f;
+            if (a.gdn) {
+                deta = dbeta;
+            } else {
+                const float denom = nrm[r] + a.eps;
+                deta = denom == 0.f ? 0.f : dbeta / denom;
+                if (denom != 0.f) dn = -dbeta * bs[r] / denom;
+            }
+            const int t = t0 + r;
+            if (t < T) a.deta[((size_t)b * T + t) * H + h] = deta;
+            db[r] = dn;
         }
-        dg[r] = gsum;
-        const float dbeta = db[r];
-        float deta, dn = 0.f;
-        if (a.gdn) {
-            deta = dbeta;
-        } else {
-            const float denom = nrm[r] + a.eps;
-            deta = denom == 0.f ? 0.f : dbeta / denom;
-            if (denom != 0.f) dn = -dbeta * bs[r] / denom;
-        }
-        const int t = t0 + r;
-        if (t < T) a.deta[((size_t)b * T + t) * H + h] = deta;
-        db[r] = dn;
     }
     for (int i = tid; i < C * C; i += kBwdThreads) {
         const int r = i >> 6, c = i & 63;
-        Ddt[r * LC + c] =
-            __float2bfloat16_rn(F1f[r * LF + c] + F1f[c * LF + r]);
+        const float d =
+            c < r ? F1f[r * LF + c] : c > r ? F1f[c * LF + r] : 0.f;
+        Ddt[r * LC + c] = __float2bfloat16_rn(d);
     }
     __syncthreads();
-    if (tid < C) {   // dlog_alpha_j = sum_{r >= j} dg_r
-        float acc = 0.f;
-        for (int r = tid; r < C; ++r) acc += dg[r];
-        const int t = t0 + tid;
-        if (t < T) a.dlog_alpha[((size_t)b * T + t) * H + h] = acc;
+    if (warp == 0) {   // dlog_alpha_j = sum_{r >= j} dg_r (a suffix scan)
+        const float x0 = dg[2 * lane], x1 = dg[2 * lane + 1];
+        float sc = x0 + x1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_down_sync(0xffffffffu, sc, off);
+            if (lane + off < 32) sc += y;
+        }
+        const int t = t0 + 2 * lane;
+        const size_t off = ((size_t)b * T + t) * H + h;
+        if (t < T) a.dlog_alpha[off] = sc;
+        if (t + 1 < T) a.dlog_alpha[off + H] = sc - x0;
     }
 
     // dq += (Gamma o dP) K;  dk += (Gamma o dP)^T Q + (D + D^T) K

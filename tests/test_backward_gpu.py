@@ -111,6 +111,20 @@ def test_bf16_d128(rule):
     check(inp, do, dhT, 64, rule)
 
 
+@pytest.mark.parametrize("dv", [64, 32])
+def test_bf16_dk128_narrower_values(dv):
+    """bf16, dk = 128, C = 64 with dv = 64 or 32: the checkpoints come from
+    the CUDA-core forward and the per-chunk records from the backward's own
+    pre-pass; dv = 64 runs the tensor-core recurrence, dv = 32 the
+    CUDA-core one; both the tensor-core gradient kernel.  With h0 and a
+    ragged last chunk."""
+    from dataclasses import replace
+    w = replace(gen.LAYER_1B, dv=dv)
+    inp = gen.prefill_inputs(w, B=2, T=150, H=2)
+    do, dhT = upstream(inp, 27)
+    check(inp, do, dhT, 64)
+
+
 def test_bf16_full_size_sampled_heads():
     """The 1B layer (B4 T4096 H16) on the GPU; heads (b=1, h=3..4) are
     followed by the oracle's reverse mode over all 4096 tokens."""

@@ -432,12 +432,16 @@ KLA_API kla_status kla_chunk_bwd_workspace_size(int B, int T, int H, int dk,
  *                  owned by the caller; its contents on entry do not matter
  *                  and are garbage on return
  *
- * Three launches: the forward pass writing the state at every chunk start
- * (the tensor-core kernel where kla_chunk_fwd_ex's KLA_ALGO_AUTO would use
- * it); the reverse recurrence of dL/dS over the chunks (on the tensor cores
- * with tf32 operands for bf16, dk = 128, C = 64 and 16-byte-aligned q, k,
- * o_grad; else on the CUDA cores in fp32); the per-chunk gradients (CUDA
- * cores, fp32).  Supported shapes as for kla_chunk_fwd.  No output may
+ * The forward pass writing the state at every chunk start (the two-kernel
+ * tensor-core path where kla_chunk_fwd_ex's KLA_ALGO_AUTO would use it, its
+ * pre-pass also writing the per-chunk records of the backward; else the
+ * fused tensor-core kernel or the CUDA-core one, and for dk = 128, C = 64,
+ * bf16 a pre-pass of its own for the records); the reverse recurrence of
+ * dL/dS over the chunks; the per-chunk gradients.  The last two run on the
+ * tensor cores (bf16 operands, fp32 accumulation) for bf16, dk = 128,
+ * C = 64 and 16-byte-aligned q, k, v, o_grad (the recurrence also needs dv
+ * a multiple of 64), else on the CUDA cores in fp32.  Supported shapes as
+ * for kla_chunk_fwd.  No output may
  * overlap an input, another output or the workspace, and the workspace may
  * overlap no input (byte ranges from the sizes).  Errors:
  * KLA_ERR_INVALID_ARG (null required pointer, negative size, bad enum,

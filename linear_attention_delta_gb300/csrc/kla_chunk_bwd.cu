@@ -1001,25 +1001,26 @@ __device__ __forceinline__ float row_norm2(const bf16* Kb, int r, int q4) {
 }
 
 // Q K^T and K K^T on this warp's lower 16 x 8 tiles of the C x C products
-// (tile indices warp, warp + 8, warp + 16 below 20: three tiles for warps
-// 0..3, two for the others), the tiles' MMA chains interleaved.
-__device__ __forceinline__ void qk_kk_tiles(float (&qk)[3][4],
-                                            float (&kk)[3][4], int (&mt)[3],
-                                            int (&nt)[3], const bf16* Qb,
-                                            const bf16* Kb, int warp,
-                                            int lane) {
-    const int n = warp < 4 ? 3 : 2;
+// (tile indices warp + NW x below 20, for NW warps), the tiles' MMA chains
+// interleaved.
+template <int NW = 8>
+__device__ __forceinline__ void qk_kk_tiles(
+    float (&qk)[(20 + NW - 1) / NW][4], float (&kk)[(20 + NW - 1) / NW][4],
+    int (&mt)[(20 + NW - 1) / NW], int (&nt)[(20 + NW - 1) / NW],
+    const bf16* Qb, const bf16* Kb, int warp, int lane) {
+    constexpr int XT = (20 + NW - 1) / NW;
 #pragma unroll
-    for (int x = 0; x < 3; ++x) {
-        lower_tile(x < n ? warp + 8 * x : warp, mt[x], nt[x]);
+    for (int x = 0; x < XT; ++x) {
+        const int idx = warp + NW * x;
+        lower_tile(idx < 20 ? idx : warp, mt[x], nt[x]);
 #pragma unroll
         for (int e = 0; e < 4; ++e) qk[x][e] = kk[x][e] = 0.f;
     }
 #pragma unroll
     for (int ks = 0; ks < DK / 16; ++ks) {
 #pragma unroll
-        for (int x = 0; x < 3; ++x) {
-            if (x < n) {
+        for (int x = 0; x < XT; ++x) {
+            if (warp + NW * x < 20) {
                 uint32_t aq[4], ak[4], bk[4];
                 a_row(aq, Qb + 16 * mt[x] * LQ + 16 * ks, LQ, lane);
                 a_row(ak, Kb + 16 * mt[x] * LQ + 16 * ks, LQ, lane);
@@ -1040,10 +1041,17 @@ __device__ __forceinline__ void qk_kk_tiles(float (&qk)[3][4],
 // else by kla_bwd_prep_kernel.
 namespace brec = bwdrec;
 
-template <typename IO>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+template <typename IO, int NW>
+__global__ void __launch_bounds__(32 * NW, 1)
 kla_bwd_grad_lm_kernel(BwdArgs a) {
     using namespace lm;
+    // NW warps: the C x DVT products' 16 x 8 tiles (TPW per warp, WPR warps
+    // per 16-row block), the 20 lower 16 x 8 tiles of the C x C products
+    // (XT at most per warp) and the dq / dk fragments (rows 16 (w & 3),
+    // CQ columns) are dealt out to them
+    constexpr int NT = 32 * NW, WPR = NW / 4, TPW = 4 / WPR;
+    constexpr int XT = (20 + NW - 1) / NW, CQ = 128 / WPR, NQ = CQ / 8;
+    static_assert(NW == 8 || NW == 16, "8 or 16 warps");
     extern __shared__ __align__(16) uint8_t smraw[];
     bf16* Qb = reinterpret_cast<bf16*>(smraw + QB);
     bf16* Kb = reinterpret_cast<bf16*>(smraw + KB);
@@ -1095,8 +1103,8 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
     {   // q, k rows (bf16, 16-byte loads straight to shared memory); T, P
         // (bf16), g, beta and ||k||^2 from the chunk's record
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int idx = tid + u * kBwdThreads;   // 64 rows x 16 chunks
+        for (int u = 0; u < 1024 / NT; ++u) {
+            const int idx = tid + u * NT;   // 64 rows x 16 chunks
             const int r = idx >> 4, c8 = idx & 15;
             const int t = t0 + r;
             uint4 qv = make_uint4(0, 0, 0, 0), kv = make_uint4(0, 0, 0, 0);
@@ -1112,8 +1120,8 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
         }
         const uint8_t* rec = a.rec + ((size_t)bh * nch + ch) * brec::BYTES;
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {   // 512 pieces of 16 bytes each
-            const int u = tid + m * kBwdThreads, r = u >> 3, c8 = u & 7;
+        for (int m = 0; m < 512 / NT; ++m) {   // 512 pieces of 16 bytes
+            const int u = tid + m * NT, r = u >> 3, c8 = u & 7;
             *reinterpret_cast<uint4*>(Tb + r * LC + 8 * c8) =
                 reinterpret_cast<const uint4*>(rec + brec::T_OFF)[u];
             *reinterpret_cast<uint4*>(Pb + r * LC + 8 * c8) =
@@ -1134,22 +1142,23 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
         gb[tid] = -gam[tid] * bs[tid];
     }
 
-    // dq, dk of this warp's rows 16 mo .. and columns 64 co .. (fragments)
-    const int mo = warp & 3, co = 64 * (warp >> 2);
-    float dq[8][4], dk[8][4];
+    // dq, dk of this warp's rows 16 mo .. and columns CQ co .. (fragments)
+    const int mo = warp & 3, co = CQ * (warp >> 2);
+    float dq[NQ][4], dk[NQ][4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < NQ; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) dq[nt][e] = dk[nt][e] = 0.f;
-    // dP, dA of this warp's lower tiles (idx = warp, warp + 8, warp + 16)
-    float dPa[3][4], dAa[3][4];
+    // dP, dA of this warp's lower tiles (idx = warp + NW x)
+    float dPa[XT][4], dAa[XT][4];
 #pragma unroll
-    for (int x = 0; x < 3; ++x)
+    for (int x = 0; x < XT; ++x)
 #pragma unroll
         for (int e = 0; e < 4; ++e) dPa[x][e] = dAa[x][e] = 0.f;
-    // this warp's two 16 x 8 tiles of the C x DVT products: rows 16 (w >> 1),
-    // columns 16 (w & 1) .. + 15
-    const int pm = warp >> 1, pn = 16 * (warp & 1);
+    // this warp's TPW 16 x 8 tiles of the C x DVT products: rows 16 pm,
+    // columns pn .. pn + 8 TPW - 1 (the B fragments are loaded two tiles
+    // at a time; with one tile per warp the second is not used)
+    const int pm = warp / WPR, pn = 8 * TPW * (warp % WPR);
     float sdot = 0.f;
     __syncthreads();
 
@@ -1160,22 +1169,24 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
     uint8_t* stage = smraw + F0;
     auto stage_issue = [&](int jn) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int idx = tid + u * kBwdThreads;   // 128 rows x 8
+        for (int u = 0; u < 1024 / NT; ++u) {
+            const int idx = tid + u * NT;   // 128 rows x 8
             const int c = idx >> 3, j4 = idx & 7;
             cp_async16(stage + (c * DVT + 4 * j4) * 4,
                        Sg + (size_t)c * dv + jn + 4 * j4, true);
             cp_async16(stage + STG_DS + (c * DVT + 4 * j4) * 4,
                        dSg + (size_t)c * dv + jn + 4 * j4, true);
         }
-        const int r = tid >> 2, j8 = tid & 3;        // 64 rows x 4
-        const int t = t0 + r;
-        const size_t off =
-            (((size_t)b * T + (t < T ? t : t0)) * H + h) * dv + jn + 8 * j8;
-        cp_async16(stage + STG_V + (r * DVT + 8 * j8) * 2,
-                   static_cast<const IO*>(a.v) + off, t < T);
-        cp_async16(stage + STG_DO + (r * DVT + 8 * j8) * 2,
-                   static_cast<const IO*>(a.dout) + off, t < T);
+        if (tid < 256) {
+            const int r = tid >> 2, j8 = tid & 3;   // 64 rows x 4
+            const int t = t0 + r;
+            const size_t off = (((size_t)b * T + (t < T ? t : t0)) * H + h) *
+                                   dv + jn + 8 * j8;
+            cp_async16(stage + STG_V + (r * DVT + 8 * j8) * 2,
+                       static_cast<const IO*>(a.v) + off, t < T);
+            cp_async16(stage + STG_DO + (r * DVT + 8 * j8) * 2,
+                       static_cast<const IO*>(a.dout) + off, t < T);
+        }
         cp_async_commit();
     };
 
@@ -1183,21 +1194,23 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
         {   // S, dS' (DK x DVT fp32 -> bf16), V (fp32), dO (bf16, and
             // Diag(gamma) dO): from global memory for the first step (every
             // load issued before the stores), from the staging area after
-            float4 sv[4], dsv[4];
-            const int r = tid >> 2, j8 = tid & 3;        // 64 rows x 4
+            constexpr int U = 1024 / NT;
+            float4 sv[U], dsv[U];
+            const bool vt = tid < 256;   // V and dO: 64 rows x 4 pieces
+            const int r = (tid & 255) >> 2, j8 = tid & 3;
             const int t = t0 + r;
             uint4 vv = make_uint4(0, 0, 0, 0), dov = make_uint4(0, 0, 0, 0);
             if (j0 == 0) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int idx = tid + u * kBwdThreads;   // 128 rows x 8
+                for (int u = 0; u < U; ++u) {
+                    const int idx = tid + u * NT;   // 128 rows x 8
                     const int c = idx >> 3, j4 = idx & 7;
                     sv[u] = *reinterpret_cast<const float4*>(
                         Sg + (size_t)c * dv + j0 + 4 * j4);
                     dsv[u] = *reinterpret_cast<const float4*>(
                         dSg + (size_t)c * dv + j0 + 4 * j4);
                 }
-                if (t < T) {
+                if (vt && t < T) {
                     const size_t off =
                         (((size_t)b * T + t) * H + h) * dv + j0 + 8 * j8;
                     vv = *reinterpret_cast<const uint4*>(
@@ -1208,23 +1221,25 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
             } else {
                 cp_async_wait_all();
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int idx = tid + u * kBwdThreads;
+                for (int u = 0; u < U; ++u) {
+                    const int idx = tid + u * NT;
                     const int c = idx >> 3, j4 = idx & 7;
                     sv[u] = *reinterpret_cast<const float4*>(
                         stage + (c * DVT + 4 * j4) * 4);
                     dsv[u] = *reinterpret_cast<const float4*>(
                         stage + STG_DS + (c * DVT + 4 * j4) * 4);
                 }
-                vv = *reinterpret_cast<const uint4*>(
-                    stage + STG_V + (r * DVT + 8 * j8) * 2);
-                dov = *reinterpret_cast<const uint4*>(
-                    stage + STG_DO + (r * DVT + 8 * j8) * 2);
+                if (vt) {
+                    vv = *reinterpret_cast<const uint4*>(
+                        stage + STG_V + (r * DVT + 8 * j8) * 2);
+                    dov = *reinterpret_cast<const uint4*>(
+                        stage + STG_DO + (r * DVT + 8 * j8) * 2);
+                }
             }
             if (j0 + DVT < dv) stage_issue(j0 + DVT);   // next step in flight
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int idx = tid + u * kBwdThreads;
+            for (int u = 0; u < U; ++u) {
+                const int idx = tid + u * NT;
                 const int c = idx >> 3, j = 4 * (idx & 7);
                 sdot = fmaf(sv[u].x, dsv[u].x, sdot);
                 sdot = fmaf(sv[u].y, dsv[u].y, sdot);
@@ -1238,6 +1253,7 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
                 *reinterpret_cast<uint2*>(Sb + c * LV + j) = s2;
                 *reinterpret_cast<uint2*>(dSb + c * LV + j) = d2;
             }
+            if (vt) {
             *reinterpret_cast<uint4*>(dOb + r * LV + 8 * j8) = dov;
             const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
             const uint32_t dw[4] = {dov.x, dov.y, dov.z, dov.w};
@@ -1253,30 +1269,32 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
                                          gr * __uint_as_float(dw[e] & 0xffff0000u));
             }
             *reinterpret_cast<uint4*>(dOg + r * LV + 8 * j8) = dg4;
+            }
         }
         __syncthreads();
 
         // K S, Q S: X = V - Diag(gamma) K S, F = Diag(beta) X,
         // dgamma += dO . Q S
         {
-            float ks[2][4] = {}, qs[2][4] = {};
+            float ks[TPW][4] = {}, qs[TPW][4] = {};
 #pragma unroll
             for (int kk = 0; kk < DK / 16; ++kk) {
                 uint32_t ak[4], aq[4], bs4[4];
                 a_row(ak, Kb + 16 * pm * LQ + 16 * kk, LQ, lane);
                 a_row(aq, Qb + 16 * pm * LQ + 16 * kk, LQ, lane);
                 b_row2(bs4, Sb + 16 * kk * LV + pn, LV, lane);
-                mma(ks[0], ak, bs4[0], bs4[1]);
-                mma(ks[1], ak, bs4[2], bs4[3]);
-                mma(qs[0], aq, bs4[0], bs4[1]);
-                mma(qs[1], aq, bs4[2], bs4[3]);
+#pragma unroll
+                for (int nt = 0; nt < TPW; ++nt) {
+                    mma(ks[nt], ak, bs4[2 * nt], bs4[2 * nt + 1]);
+                    mma(qs[nt], aq, bs4[2 * nt], bs4[2 * nt + 1]);
+                }
             }
 #pragma unroll
             for (int hm = 0; hm < 2; ++hm) {
                 const int r = 16 * pm + g8 + 8 * hm;
                 float dgp = 0.f;
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
+                for (int nt = 0; nt < TPW; ++nt) {
                     const int j = pn + 8 * nt + 2 * t4;
                     float xs[2];
 #pragma unroll
@@ -1300,20 +1318,21 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
 
         // U~ = T F (T lower triangular)
         {
-            float u[2][4] = {};
+            float u[TPW][4] = {};
             for (int kk = 0; kk <= pm; ++kk) {
                 uint32_t at[4], bf4[4];
                 a_row(at, Tb + 16 * pm * LC + 16 * kk, LC, lane);
                 b_row2(bf4, Fb + 16 * kk * LV + pn, LV, lane);
-                mma(u[0], at, bf4[0], bf4[1]);
-                mma(u[1], at, bf4[2], bf4[3]);
+#pragma unroll
+                for (int nt = 0; nt < TPW; ++nt)
+                    mma(u[nt], at, bf4[2 * nt], bf4[2 * nt + 1]);
             }
 #pragma unroll
             for (int hm = 0; hm < 2; ++hm) {
                 const int r = 16 * pm + g8 + 8 * hm;
                 const float lr = lam[r];
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
+                for (int nt = 0; nt < TPW; ++nt) {
                     const int j = pn + 8 * nt + 2 * t4;
                     const float u0 = u[nt][2 * hm], u1 = u[nt][2 * hm + 1];
                     Uf[r * LX + j] = u0;
@@ -1329,21 +1348,23 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
 
         // dU~ = P^T dO + Diag(lambda) K dS';  dlambda_r += (K dS')_r . U~_r
         {
-            float kd[2][4] = {}, pd[2][4] = {};
+            float kd[TPW][4] = {}, pd[TPW][4] = {};
 #pragma unroll
             for (int kk = 0; kk < DK / 16; ++kk) {
                 uint32_t ak[4], bd4[4];
                 a_row(ak, Kb + 16 * pm * LQ + 16 * kk, LQ, lane);
                 b_row2(bd4, dSb + 16 * kk * LV + pn, LV, lane);
-                mma(kd[0], ak, bd4[0], bd4[1]);
-                mma(kd[1], ak, bd4[2], bd4[3]);
+#pragma unroll
+                for (int nt = 0; nt < TPW; ++nt)
+                    mma(kd[nt], ak, bd4[2 * nt], bd4[2 * nt + 1]);
             }
             for (int kk = pm; kk < C / 16; ++kk) {   // P^T(r, i) = P(i, r)
                 uint32_t ap[4], bo4[4];
                 a_trn(ap, Pb + 16 * kk * LC + 16 * pm, LC, lane);
                 b_row2(bo4, dOb + 16 * kk * LV + pn, LV, lane);
-                mma(pd[0], ap, bo4[0], bo4[1]);
-                mma(pd[1], ap, bo4[2], bo4[3]);
+#pragma unroll
+                for (int nt = 0; nt < TPW; ++nt)
+                    mma(pd[nt], ap, bo4[2 * nt], bo4[2 * nt + 1]);
             }
 #pragma unroll
             for (int hm = 0; hm < 2; ++hm) {
@@ -1351,7 +1372,7 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
                 const float lr = lam[r];
                 float dlp = 0.f;
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
+                for (int nt = 0; nt < TPW; ++nt) {
                     const int j = pn + 8 * nt + 2 * t4;
                     const float k0 = kd[nt][2 * hm], k1 = kd[nt][2 * hm + 1];
                     *reinterpret_cast<uint32_t*>(dUb + r * LV + j) =
@@ -1369,13 +1390,14 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
         // dF = T^T dU~; dV = Diag(beta) dF; dbeta += dF . X;
         // dgamma -= dX . K S
         {
-            float df[2][4] = {};
+            float df[TPW][4] = {};
             for (int kk = pm; kk < C / 16; ++kk) {   // T^T(r, i) = T(i, r)
                 uint32_t at[4], bu4[4];
                 a_trn(at, Tb + 16 * kk * LC + 16 * pm, LC, lane);
                 b_row2(bu4, dUb + 16 * kk * LV + pn, LV, lane);
-                mma(df[0], at, bu4[0], bu4[1]);
-                mma(df[1], at, bu4[2], bu4[3]);
+#pragma unroll
+                for (int nt = 0; nt < TPW; ++nt)
+                    mma(df[nt], at, bu4[2 * nt], bu4[2 * nt + 1]);
             }
 #pragma unroll
             for (int hm = 0; hm < 2; ++hm) {
@@ -1384,7 +1406,7 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
                 const float br = bs[r], gbr = gb[r];
                 float dbp = 0.f, dgp = 0.f;
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
+                for (int nt = 0; nt < TPW; ++nt) {
                     const int j = pn + 8 * nt + 2 * t4;
                     const float f0 = df[nt][2 * hm], f1 = df[nt][2 * hm + 1];
                     const float x0 = br * f0, x1 = br * f1;
@@ -1416,8 +1438,8 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
 
         // dP += dO U~^T, dA -= dF U~^T (this warp's lower tiles, registers)
 #pragma unroll
-        for (int x = 0; x < 3; ++x) {
-            const int idx = warp + 8 * x;
+        for (int x = 0; x < XT; ++x) {
+            const int idx = warp + NW * x;
             if (idx >= 20) break;
             int mt, nt;
             lower_tile(idx, mt, nt);
@@ -1441,7 +1463,7 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
             a_row(au, Ulb + 16 * mo * LV + 16 * kk, LV, lane);
             a_row(af, dFs + 16 * mo * LV + 16 * kk, LV, lane);
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {   // pairs of 8-column tiles
+            for (int np = 0; np < NQ / 2; ++np) {   // pairs of 8-column tiles
                 const int c0 = co + 16 * np;
                 uint32_t bs4[4], bd4[4];
                 // B(j, c) = S(c, j)
@@ -1468,8 +1490,8 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
     // entries are read below; the final tiles of Gamma o dP are written in
     // full, zeros above the diagonal included)
 #pragma unroll
-    for (int x = 0; x < 3; ++x) {
-        const int idx = warp + 8 * x;
+    for (int x = 0; x < XT; ++x) {
+        const int idx = warp + NW * x;
         if (idx >= 20) break;
         int mt, nt;
         lower_tile(idx, mt, nt);
@@ -1488,12 +1510,12 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
     // dGamma o Gamma (F2), Gamma o dP (bf16), D (over dA in F1) and the
     // A-part of dbeta, from Q K^T and K K^T of the lower tiles
     {
-        float qk[3][4], kk4[3][4];
-        int mt[3], nt[3];
-        qk_kk_tiles(qk, kk4, mt, nt, Qb, Kb, warp, lane);
+        float qk[XT][4], kk4[XT][4];
+        int mt[XT], nt[XT];
+        qk_kk_tiles<NW>(qk, kk4, mt, nt, Qb, Kb, warp, lane);
 #pragma unroll
-        for (int x = 0; x < 3; ++x) {
-            if (x == 2 && warp >= 4) break;
+        for (int x = 0; x < XT; ++x) {
+            if (warp + NW * x >= 20) break;
 #pragma unroll
             for (int hm = 0; hm < 2; ++hm) {
                 const int r = 16 * mt[x] + g8 + 8 * hm;
@@ -1528,7 +1550,7 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
 
     // per row (four threads each): dg, deta, dn (dn replaces dbeta in db);
     // D + D^T (bf16) from D's strictly lower part
-    {
+    if (tid < 256) {
         const int r = tid >> 2, q4 = tid & 3;
         float sp = 0.f;
         for (int i = q4; i <= r; i += 4) sp += F2f[r * LF + i];
@@ -1554,7 +1576,7 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
             db[r] = dn;
         }
     }
-    for (int i = tid; i < C * C; i += kBwdThreads) {
+    for (int i = tid; i < C * C; i += NT) {
         const int r = i >> 6, c = i & 63;
         const float d =
             c < r ? F1f[r * LF + c] : c > r ? F1f[c * LF + r] : 0.f;
@@ -1583,7 +1605,7 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
         if (up) a_trn(apt, Gdp + 16 * kk * LC + 16 * mo, LC, lane);
         a_row(ad, Ddt + 16 * mo * LC + 16 * kk, LC, lane);
 #pragma unroll
-        for (int np = 0; np < 4; ++np) {
+        for (int np = 0; np < NQ / 2; ++np) {
             const int c0 = co + 16 * np;
             uint32_t bk4[4], bq4[4];
             b_row2(bk4, Kb + 16 * kk * LQ + c0, LQ, lane);
@@ -1603,7 +1625,7 @@ kla_bwd_grad_lm_kernel(BwdArgs a) {
         if (t >= T) continue;
         const float dn2 = 2.f * db[r];
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
+        for (int nt = 0; nt < NQ; ++nt) {
             const int c = co + 8 * nt + 2 * t4;
             const size_t off = (((size_t)b * T + t) * H + h) * DK + c;
             IO* q2 = static_cast<IO*>(a.dq) + off;
@@ -2093,11 +2115,13 @@ cudaError_t launch_shape(const BwdArgs& a, cudaStream_t stream) {
     if constexpr (DK == kTcDK && DVT == 32 &&
                   std::is_same<IO, __nv_bfloat16>::value) {
         if (grad_tc) {
-            auto km = kla_bwd_grad_lm_kernel<IO>;
+            constexpr int kGradWarps = 8;   // 16 warps (128 registers) measured slower
+            auto km = kla_bwd_grad_lm_kernel<IO, kGradWarps>;
             e = cudaFuncSetAttribute(
                 km, cudaFuncAttributeMaxDynamicSharedMemorySize, lm::BYTES);
             if (e != cudaSuccess) return e;
-            km<<<(unsigned)(bhs * nch), kBwdThreads, lm::BYTES, stream>>>(a);
+            km<<<(unsigned)(bhs * nch), 32 * kGradWarps, lm::BYTES, stream>>>(
+                a);
             return cudaGetLastError();
         }
     }

@@ -143,10 +143,12 @@ KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
 /*
  * kla_chunk_fwd_workspace_size -- bytes of device workspace kla_chunk_fwd_ws
  * needs with this algorithm: for bf16, dk = dv = 128, C = 64 and KLA_ALGO_TC
- * or KLA_ALGO_AUTO, the pre-pass records of the two-kernel tensor-core path,
- * 16,640 bytes per (batch, head, chunk of 64 tokens); 0 otherwise (those
- * paths need none).  Errors: KLA_ERR_INVALID_ARG (null `bytes`, negative
- * size, bad enum), KLA_ERR_UNSUPPORTED_SHAPE (dk, dv or C outside the set).
+ * or KLA_ALGO_AUTO, the pre-pass records of the two-kernel tensor-core path
+ * (16,640 bytes per (batch, head, chunk of 64 tokens)), one 4-byte ready
+ * flag per record (rounded up to 16 bytes in all) and 1,040 bytes of the
+ * pre-pass's work counters; 0 otherwise (those paths need none).  Errors:
+ * KLA_ERR_INVALID_ARG (null `bytes`, negative size, bad enum),
+ * KLA_ERR_UNSUPPORTED_SHAPE (dk, dv or C outside the set).
  */
 KLA_API kla_status kla_chunk_fwd_workspace_size(int B, int T, int H, int dk,
                                                 int dv, int C,
@@ -179,8 +181,9 @@ KLA_API kla_status kla_chunk_fwd_ws(const void* q, const void* k,
  * kla_chunk_fwd_seq needs: fp32 start and end states of the 2 x B x P
  * segment runs (4 tensors [B, P, H, 128, 128]), O_hom [B, T, H, 128] bf16,
  * the bf16 start states [B, P, H, 128, 128], a [64, H, 128] bf16 zero
- * tile and the records of the two-kernel path's pre-pass (16,640 bytes per
- * (batch, head, 64-token chunk)), each rounded up to 256 bytes; 0 when
+ * tile and the two-kernel path's pre-pass workspace over all B P segments
+ * (kla_chunk_fwd_workspace_size of B P sequences of T / P tokens), each
+ * rounded up to 256 bytes; 0 when
  * there is nothing to split.  segments = 0 picks P as
  * kla_chunk_fwd_seq does (for the current device).  Errors:
  * KLA_ERR_INVALID_ARG (null `bytes`, negative size or segments),
@@ -400,8 +403,9 @@ KLA_API kla_status kla_decode_step_kw(const void* q, const void* k,
  * the state at every chunk end) and, for dk = 128 and C = 64, 17,152 bytes
  * per (batch, head, chunk) of per-chunk records (the inverse, P and the
  * gates of the chunk) for the tensor-core kernels, plus, when also
- * dv = 128, 16,640 bytes per (batch, head, chunk) for the records of the
- * two-kernel forward that writes the checkpoints.  Writes 0 for an empty
+ * dv = 128, the workspace of the two-kernel forward that writes the
+ * checkpoints (kla_chunk_fwd_workspace_size: 16,644 bytes per (batch, head,
+ * chunk), rounded up to 16 bytes, and 1,040 bytes).  Writes 0 for an empty
  * problem.  Errors:
  * KLA_ERR_INVALID_ARG (null `bytes`, negative size, C <= 0).
  */

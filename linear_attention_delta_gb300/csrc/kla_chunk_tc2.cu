@@ -45,6 +45,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -119,6 +120,19 @@ static_assert(kPL % 16 == 0 && kPT % 16 == 0, "float4 rows");
 // five CTAs per SM (the driver keeps 1 KB of each CTA's shared memory)
 static_assert(5 * (kPSmem + 1024) <= 233472, "pre-pass shared memory");
 
+// Work distribution of the pre-pass.  Its grid is persistent (as many CTAs
+// as fit at once); each CTA takes chunk-heads from a counter in chunk-major
+// order (every head's chunk 0, then chunk 1, ...) and raises the record's
+// ready flag once the record is in memory.  Past item `release`, only the
+// CTAs of the first `reserved_sms` SMs to register keep taking work; the
+// others exit, and their SMs take the state pass, which starts on chunk 0
+// while the reserved SMs finish the last chunks.  Control words (zeroed
+// before each launch): next item below `release`, next item from
+// `release`, SMs registered as reserved, then one role per SM id (0 unset,
+// 1 reserved, 2 released, 3 being decided).
+constexpr int kMaxSmId = 256;
+constexpr int kCtrlWords = 4 + kMaxSmId;
+
 struct PrepParams {
     const float* log_alpha;
     const float* eta;
@@ -127,6 +141,11 @@ struct PrepParams {
     int gdn;
     int T, H, nchunks;
     uint8_t* brec;       // null, or the backward's records [B, H, nchunks]
+    unsigned int* ready; // [B, H, nchunks] record flags (1: in memory)
+    unsigned int* ctrl;  // kCtrlWords control words
+    int items;           // B H nchunks
+    int release;         // items taken by every SM; the rest by reserved SMs
+    int reserved_sms;
 };
 
 // acc (16 x 8, fragment layout) += A (16 x 16 packed fp32 block) x
@@ -204,37 +223,104 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kPMisc);
     float* wtot = reinterpret_cast<float*>(sm + kPMisc + 4);
     int* failed_flag = reinterpret_cast<int*>(sm + kPMisc + 8);
+    int* item_slot = reinterpret_cast<int*>(sm + kPMisc + 12);
     uint8_t* out = sm + kPKQ;   // record image, over the consumed K / Q
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // the state pass may be scheduled once every pre-pass CTA has started;
-    // it waits for this grid's completion before it reads a record
+    // it reads a record only after its ready flag is up
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int c = blockIdx.x % p.nchunks;
-    const int bh = blockIdx.x / p.nchunks;
-    const int b = bh / p.H, h = bh % p.H;
-    const int t0 = c * kC;
-    uint8_t* brec = p.brec ? p.brec + ((size_t)bh * p.nchunks + c) *
-                                          bwdrec::BYTES
-                           : nullptr;
     constexpr uint64_t kLimit = 2000000000ull;
+    const int nbh = p.items / p.nchunks;
 
+    // thread 0's work state: whether this SM keeps working past `release`,
+    // whether items below it remain, and the item whose record store is in
+    // flight (its flag goes up once the store has completed)
+    bool reserved = true, below = true;
+    int pending = -1, next = -1;
+    // the next item: chunk-major, below `release` from every SM, past it from
+    // the reserved SMs only (-1: none left for this CTA)
+    auto claim = [&]() -> int {
+        if (below) {
+            const unsigned int i = atomicAdd(p.ctrl + 0, 1u);
+            if (i < (unsigned)p.release) return (int)i;
+            below = false;
+        }
+        if (!reserved) return -1;
+        const unsigned int i = (unsigned)p.release + atomicAdd(p.ctrl + 1, 1u);
+        return i < (unsigned)p.items ? (int)i : -1;
+    };
+    // the record of item i is in memory: its flag goes up (thread 0, which
+    // issued the record's bulk store)
+    auto publish = [&](int i) {
+        tc::tma_store_wait_all<0>();
+        tc::fence_proxy_async_global();
+        tc::st_release_gpu(p.ready + i, 1u);
+    };
     if (tid == 0) {
         tc::prefetch_tmap(&tm_q);
         tc::prefetch_tmap(&tm_k);
         for (int i = 0; i < 3; ++i) tc::mbar_init(&bars[i], 1);
         *failed_flag = 0;
         tc::fence_mbar_init();
-        tc::mbar_arrive_expect_tx(&bars[0], 32768);
-        tc::tma_load_4d(sm + kPKQ, &tm_k, &bars[0], 0, h, t0, b);
-        tc::tma_load_4d(sm + kPKQ + 8192, &tm_q, &bars[0], 0, h, t0, b);
-        tc::tma_load_4d(sm + kPKQ + 16384, &tm_k, &bars[0], 64, h, t0, b);
-        tc::tma_load_4d(sm + kPKQ + 24576, &tm_q, &bars[0], 64, h, t0, b);
+        const unsigned int sid = tc::smid();
+        if (p.release < p.items && sid < (unsigned)kMaxSmId) {
+            // the first CTA of an SM decides its role for all of them
+            unsigned int* role = p.ctrl + 4 + sid;
+            unsigned int r = atomicCAS(role, 0u, 3u);
+            if (r == 0u) {
+                r = atomicAdd(p.ctrl + 2, 1u) < (unsigned)p.reserved_sms ? 1u
+                                                                         : 2u;
+                atomicExch(role, r);
+            } else if (r == 3u) {
+                const uint64_t w0 = tc::globaltimer_ns();
+                while (r == 3u && tc::globaltimer_ns() - w0 < kLimit) {
+                    __nanosleep(32);
+                    r = tc::ld_acquire_gpu(role);
+                }
+            }
+            reserved = r != 2u;   // undecided after the limit: keep working
+        }
+        next = claim();
     }
     if (warp == 0) {
         tc::tmem_alloc(tmem_slot, 64);   // five CTAs per SM fit in TMEM
         tc::tmem_relinquish();
     }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool failed = false;
+
+    for (uint32_t it = 0;; ++it) {
+    const uint32_t ph = it & 1u;
+    if (tid == 0) {
+        const int item = next;   // claimed while the previous tiles landed
+        *item_slot = item;
+        if (item >= 0) {
+            const int cc = item / nbh, bb = item % nbh;
+            const int hh = bb % p.H, b0 = bb / p.H;
+            tc::mbar_arrive_expect_tx(&bars[0], 32768);
+            tc::tma_load_4d(sm + kPKQ, &tm_k, &bars[0], 0, hh, cc * kC, b0);
+            tc::tma_load_4d(sm + kPKQ + 8192, &tm_q, &bars[0], 0, hh, cc * kC, b0);
+            tc::tma_load_4d(sm + kPKQ + 16384, &tm_k, &bars[0], 64, hh, cc * kC, b0);
+            tc::tma_load_4d(sm + kPKQ + 24576, &tm_q, &bars[0], 64, hh, cc * kC, b0);
+        } else if (pending >= 0) {
+            publish(pending);
+            pending = -1;
+        }
+    }
+    __syncthreads();
+    const int item = *item_slot;
+    if (item < 0) break;
+    const int c = item / nbh;
+    const int bh = item % nbh;
+    const int b = bh / p.H, h = bh % p.H;
+    const int t0 = c * kC;
+    uint8_t* brec = p.brec ? p.brec + ((size_t)bh * p.nchunks + c) *
+                                          bwdrec::BYTES
+                           : nullptr;
     // gates of this chunk: cumulative log2 decay (two warp scans)
     float la = 0.f, et = 0.f;
     if (tid < kC && t0 + tid < p.T) {
@@ -251,10 +337,7 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         if (tid == 31) *wtot = g2;
     }
-    tc::tc_fence_before();
     __syncthreads();
-    tc::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
     if (tid >= 32 && tid < kC) g2 += *wtot;
     if (tid < kC) g2s[tid] = g2;
     // Gamma_ri = 2^(g_r - g_m) e_i with g_m the g of the last column m of
@@ -268,7 +351,8 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     // G = [K; Q] K^T: lanes 0..63 K K^T, lanes 64..127 Q K^T (columns 0..63)
     if (tid == 0) {
-        if (tc::mbar_wait(&bars[0], 0, kLimit)) {
+        next = claim();   // while this item's tiles land
+        if (tc::mbar_wait(&bars[0], ph, kLimit)) {
             tc::tc_fence_after();
             constexpr uint32_t idG = tc::idesc_bf16(128, 64, false, false);
 #pragma unroll
@@ -278,23 +362,26 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
                              desc_k(sbase + kPKQ + off), idG, ks > 0);
             }
             tc::mma_commit(&bars[1]);
+            if (pending >= 0) {   // the previous item's record (long done)
+                publish(pending);
+                pending = -1;
+            }
         } else {
             *reinterpret_cast<volatile int*>(failed_flag) = 1;
         }
     }
     __syncthreads();   // g2s complete; the issuing lane rejoined
     bool ok = *reinterpret_cast<volatile int*>(failed_flag) == 0;
-    ok = ok && tc::mbar_wait(&bars[1], 0, kLimit);
+    ok = ok && tc::mbar_wait(&bars[1], ph, kLimit);
     ok = !__syncthreads_or(!ok);
     if (!ok) {
         if (tid == 0) {
             atomicOr(&g_fault_word2, 1u);
-            tc::mbar_wait(&bars[0], 0, 100000000ull);   // copies in flight
-            tc::mbar_wait(&bars[1], 0, 100000000ull);   // the MMAs, if issued
+            tc::mbar_wait(&bars[0], ph, 100000000ull);   // copies in flight
+            tc::mbar_wait(&bars[1], ph, 100000000ull);   // the MMAs, if issued
         }
-        __syncthreads();
-        if (warp == 0) tc::tmem_dealloc(tmem, 64);
-        return;
+        failed = true;
+        break;
     }
     tc::tc_fence_after();
     {
@@ -465,7 +552,7 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc::mma_commit(&bars[2]);
     }
     __syncwarp();
-    ok = tc::mbar_wait(&bars[2], 0, kLimit);
+    ok = tc::mbar_wait(&bars[2], ph, kLimit);
     if (!__syncthreads_or(!ok)) {
         tc::tc_fence_after();
         if (tid >= kC) {   // PTU rows over P
@@ -492,12 +579,21 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
             tc::bulk_store(p.rec + ((size_t)bh * p.nchunks + c) * kRecBytes,
                            out, kRecBytes);
             tc::tma_store_commit();
-            tc::tma_store_wait_read<0>();
+            tc::tma_store_wait_read<0>();   // the image may be overwritten
+            pending = bh * p.nchunks + c;
         }
-    } else if (tid == 0) {
-        atomicOr(&g_fault_word2, 1u);
-        tc::mbar_wait(&bars[2], 0, 100000000ull);
+    } else {
+        if (tid == 0) {
+            atomicOr(&g_fault_word2, 1u);
+            tc::mbar_wait(&bars[2], ph, 100000000ull);
+        }
+        failed = true;
     }
+    __syncthreads();
+    if (failed) break;
+    }   // items
+    if (tid == 0 && pending >= 0) publish(pending);
+    tc::tc_fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 64);
 }
@@ -566,6 +662,8 @@ struct StateParams {
     int T, H, nchunks;
     uint64_t wait_ns;     // limit of every mbarrier wait
     int no_issue;         // self-test: the producer issues nothing
+    const unsigned int* ready;   // record flags of a running pre-pass, or
+                                 // null (the records are in memory)
 };
 
 // Write 64 fp32 values as one 128-byte swizzled bf16 row.
@@ -632,6 +730,10 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
     int* issued = reinterpret_cast<int*>(sm + kSMisc + 8);
     volatile int* vabort = abort_flag;
 
+    // a second state pass sharing the pre-pass (launched right after this
+    // one as its programmatic dependent) may start once every CTA of this
+    // grid is resident; it too reads records by their flags
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x, warp = tid >> 5;
     const int bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H;
@@ -665,16 +767,22 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // launched as a programmatic dependent of the pre-pass: everything above
-    // overlaps its last wave; the records are read only after this
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Without ready flags this is a programmatic dependent that reads the
+    // records once the pre-pass grid has completed (a no-op when launched
+    // normally); with them it reads each record once its flag is up, while
+    // the pre-pass may still be running.
+    if (!p.ready) asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Loads of chunk c into its stage (TMA tiles of K, Q, V and the record
     // of the pre-pass): the first kNS by thread 0 at the start, then chunk
     // c >= kNS by lane 0 of the helper group that prepares it, as soon as
-    // the chain has released the stage (chunk c - kNS done).  Chunks two
-    // rings ahead are prefetched into L2.
+    // the chain has released the stage (chunk c - kNS done).  With flags,
+    // the record's flag is awaited first (while the chain still holds the
+    // stage).  Chunks two rings ahead are prefetched into L2 (a record not
+    // yet written is fetched again when it is loaded: L2 is coherent).
     const uint8_t* rec0 = p.rec + (size_t)bh * nchunks * kRecBytes;
+    const unsigned int* ready0 = p.ready ? p.ready + (size_t)bh * nchunks
+                                         : nullptr;
     auto prefetch = [&](int c) {
         const int t0 = c * kC;
         tc::tma_prefetch_4d(&tm_k, 0, h, t0, b);
@@ -684,7 +792,26 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc::tma_prefetch_4d(&tm_v, j0, h, t0, b);
         tc::bulk_prefetch_l2(rec0 + (size_t)c * kRecBytes, kRecBytes);
     };
-    auto issue_loads = [&](int c) {
+    // false when the record's flag did not come up in time (the caller
+    // raises the abort flag and issues no copy of the chunk).  A helper's
+    // issuing lane reads the flag of its next chunk while its current
+    // copies land (peek_record), so that the issue, which is on the path of
+    // every chunk, seldom waits for a flag.
+    int peeked = -1;   // a chunk whose flag this thread has seen up
+    auto await_record = [&](int c) {
+        if (!ready0 || c == peeked) return true;
+        if (!tc::flag_wait(ready0 + c, 1u, vabort, p.wait_ns)) return false;
+        tc::fence_proxy_async_global();   // before the bulk load that follows
+        return true;
+    };
+    auto peek_record = [&](int c) {
+        if (!ready0 || c >= nchunks) return;
+        if (tc::ld_acquire_gpu(ready0 + c) == 1u) {
+            tc::fence_proxy_async_global();
+            peeked = c;
+        }
+    };
+    auto issue_tiles = [&](int c) {
         const int s = c % kNS;
         uint8_t* st = sm + s * kStage;
         uint64_t* bar = &bars[kBFull + s];
@@ -695,17 +822,27 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc::tma_load_4d(st + kSK1, &tm_k, bar, 64, h, t0, b);
         tc::tma_load_4d(st + kSQ1, &tm_q, bar, 64, h, t0, b);
         tc::tma_load_4d(st + kSV, &tm_v, bar, j0, h, t0, b);
-        tc::bulk_load(st + kSTU, rec0 + (size_t)c * kRecBytes, kRecBytes,
-                      bar);
         atomicMax(issued, c + 1);
+    };
+    auto issue_record = [&](int c) {
+        tc::bulk_load(sm + (c % kNS) * kStage + kSTU,
+                      rec0 + (size_t)c * kRecBytes, kRecBytes,
+                      &bars[kBFull + c % kNS]);
         if (c + 2 * kNS < nchunks) prefetch(c + 2 * kNS);
     };
     if (tid == 0 && !p.no_issue) {
         tc::prefetch_tmap(&tm_q);
         tc::prefetch_tmap(&tm_k);
         tc::prefetch_tmap(&tm_v);
+        for (int c = 0; c < kNS && c < nchunks; ++c) {   // stage by stage
+            issue_tiles(c);
+            if (!await_record(c)) {
+                *vabort = 1;
+                break;
+            }
+            issue_record(c);
+        }
         for (int c = kNS; c < 2 * kNS && c < nchunks; ++c) prefetch(c);
-        for (int c = 0; c < kNS && c < nchunks; ++c) issue_loads(c);
     }
 
     if (tid >= kChainThreads) {
@@ -729,14 +866,19 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
                 // this group's lane 0 loads the chunk once the chain is done
                 // with chunk c - kNS (the helpers wait for the data anyway;
                 // the chain's own thread would pay the issue on its path)
-                ok = tc::mbar_wait_or_abort(&bars[kBEmpty + s],
+                ok = await_record(c) &&
+                     tc::mbar_wait_or_abort(&bars[kBEmpty + s],
                                             ((c - kNS) / kNS) & 1, vabort,
                                             p.wait_ns);
-                if (ok)
-                    issue_loads(c);
-                else
+                if (ok) {
+                    issue_tiles(c);
+                    issue_record(c);
+                } else {
                     *vabort = 1;
+                }
             }
+            if (hl == 0 && !p.no_issue && c + kHelperGroups >= kNS)
+                peek_record(c + kHelperGroups);
             __syncwarp();
             ok = ok && tc::mbar_wait_or_abort(&bars[kBFull + s],
                                               (c / kNS) & 1, vabort, p.wait_ns);
@@ -1034,9 +1176,21 @@ std::atomic<unsigned long long> g_prep_attr{0}, g_state_attr[2];
 
 }  // namespace
 
-size_t chunk_tc2_workspace_bytes(int B, int T, int H) {
+size_t chunk_tc2_record_bytes(int B, int T, int H) {
     const size_t nch = ((size_t)T + kC - 1) / kC;
     return (size_t)B * H * nch * kRecBytes;
+}
+
+namespace {
+size_t flag_bytes(int B, int T, int H) {
+    const size_t nch = ((size_t)T + kC - 1) / kC;
+    return ((size_t)B * H * nch * 4 + 15) / 16 * 16;
+}
+}  // namespace
+
+size_t chunk_tc2_workspace_bytes(int B, int T, int H) {
+    return chunk_tc2_record_bytes(B, T, H) + flag_bytes(B, T, H) +
+           kCtrlWords * 4;
 }
 
 bool chunk_tc2_eligible(const FwdArgs& a) {
@@ -1046,27 +1200,121 @@ bool chunk_tc2_eligible(const FwdArgs& a) {
            (!a.hT || aligned16(a.hT)) && get_encoder();
 }
 
-cudaError_t launch_prep_tc2(const FwdArgs& a, void* rec, cudaStream_t stream) {
+namespace {
+
+// Chunk indices (of every head) the whole GPU prepares before SMs go to the
+// state pass: the fewest such that the reserved SMs, producing the rest in
+// order, stay ahead of the state pass.  The rates are GB300 measurements on
+// the 1B and 340M layers (a pre-pass item takes ~9.5 us with five per SM;
+// the state pass starts its chain ~6 us after its SMs are free and takes
+// ~1.6 us per chunk); a sweep of the release point put the best times at
+// 42 of 64 and 22 of 32 chunk indices, where this gives 43 and 22.  A wrong
+// estimate costs time, never correctness: the state pass waits for each
+// flag.
+int release_chunks(int nbh, int nchunks, int reserved_sms, int per_sm) {
+    const double item_us = 9.5, start_us = 6.0, chunk_us = 1.6;
+    const double rate = reserved_sms * per_sm / item_us;   // items per us
+    for (int kc = 0; kc < nchunks; ++kc) {
+        bool ok = true;
+        for (int j = kc; j < nchunks && ok; ++j)
+            ok = (j - kc + 1) * nbh / rate <= start_us + chunk_us * j;
+        if (ok) return kc;
+    }
+    return nchunks;
+}
+
+struct DeviceShape {
+    int sms = 0, prep_per_sm = 0;
+};
+
+cudaError_t device_shape(DeviceShape* d) {
+    static std::atomic<unsigned long long> cached[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) {
+        const unsigned long long v = cached[dev].load();
+        if (v) {
+            d->sms = (int)(v >> 32);
+            d->prep_per_sm = (int)(v & 0xffffffffu);
+            return cudaSuccess;
+        }
+    }
+    e = cudaDeviceGetAttribute(&d->sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // CTAs of the pre-pass resident per SM: five by construction (launch
+    // bounds, shared memory, TMEM), fewer if this device's shared memory or
+    // register file holds fewer
+    int smem_sm = 0;
+    e = cudaDeviceGetAttribute(&smem_sm,
+                               cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kla_prep_kernel);
+    if (e != cudaSuccess) return e;
+    const int by_smem = smem_sm / (kPSmem + 1024);
+    const int by_regs = 65536 / (std::max(fa.numRegs, 1) * kPrepThreads);
+    d->prep_per_sm = std::min(5, std::min(by_smem, by_regs));
+    if (d->sms <= 0 || d->prep_per_sm <= 0) return cudaErrorInvalidValue;
+    if (dev < 64)
+        cached[dev].store(((unsigned long long)d->sms << 32) |
+                          (unsigned)d->prep_per_sm);
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_prep_tc2(const FwdArgs& a, void* ws, cudaStream_t stream,
+                            int state_ctas) {
     if ((long)a.B * a.H == 0 || a.T == 0) return cudaSuccess;
     if (!get_encoder()) return cudaErrorNotSupported;
-    if (!rec || !aligned16(rec)) return cudaErrorInvalidValue;
+    if (!ws || !aligned16(ws)) return cudaErrorInvalidValue;
     CUtensorMap mq, mk;
     if (!make_map(&mq, a.q, a.B, a.T, a.H) || !make_map(&mk, a.k, a.B, a.T, a.H))
         return cudaErrorInvalidValue;
     const int nchunks = (a.T + kC - 1) / kC;
-    const long nprep = (long)a.B * a.H * nchunks;
-    if (nprep > 0x7fffffffL) return cudaErrorInvalidValue;
+    const long nbh = (long)a.B * a.H;
+    const long items = nbh * nchunks;
+    if (items > 0x7fffffffL) return cudaErrorInvalidValue;
     cudaError_t e = set_smem((const void*)kla_prep_kernel, kPSmem, g_prep_attr);
     if (e != cudaSuccess) return e;
-    PrepParams pp{a.log_alpha, a.eta, static_cast<uint8_t*>(rec), a.eps, a.gdn,
-                  a.T, a.H, nchunks, a.bwd_rec};
-    kla_prep_kernel<<<(unsigned)nprep, kPrepThreads, kPSmem, stream>>>(mq, mk,
-                                                                      pp);
+    DeviceShape d;
+    e = device_shape(&d);
+    if (e != cudaSuccess) return e;
+    uint8_t* rec = static_cast<uint8_t*>(ws);
+    unsigned int* ready = reinterpret_cast<unsigned int*>(
+        rec + chunk_tc2_record_bytes(a.B, a.T, a.H));
+    unsigned int* ctrl = reinterpret_cast<unsigned int*>(
+        reinterpret_cast<uint8_t*>(ready) + flag_bytes(a.B, a.T, a.H));
+    e = cudaMemsetAsync(ready, 0, flag_bytes(a.B, a.T, a.H) + kCtrlWords * 4,
+                        stream);
+    if (e != cudaSuccess) return e;
+    // SMs left to the pre-pass once the state pass runs (when it leaves some)
+    const int reserved = state_ctas > 0 && state_ctas < d.sms
+                             ? d.sms - state_ctas
+                             : 0;
+    const long release =
+        reserved ? nbh * release_chunks((int)nbh, nchunks, reserved,
+                                        d.prep_per_sm)
+                 : items;
+    const long grid = std::min(items, (long)d.sms * d.prep_per_sm);
+    PrepParams pp{a.log_alpha, a.eta, rec, a.eps, a.gdn, a.T, a.H, nchunks,
+                  a.bwd_rec, ready, ctrl, (int)items, (int)release,
+                  reserved};
+    kla_prep_kernel<<<(unsigned)grid, kPrepThreads, kPSmem, stream>>>(mq, mk,
+                                                                     pp);
     return cudaGetLastError();
 }
 
+const unsigned int* chunk_tc2_ready(const void* ws, int B, int T, int H) {
+    return reinterpret_cast<const unsigned int*>(
+        static_cast<const uint8_t*>(ws) + chunk_tc2_record_bytes(B, T, H));
+}
+
+int chunk_tc2_state_ctas(int B, int H) { return B * H * (kD / kNV); }
+
 cudaError_t launch_state_tc2(const FwdArgs& a, const void* rec,
-                             cudaStream_t stream, bool after_prep) {
+                             const unsigned int* ready, cudaStream_t stream) {
     if ((long)a.B * a.H == 0 || a.T == 0) return cudaSuccess;
     if (!get_encoder()) return cudaErrorNotSupported;
     if ((a.o == nullptr) == (a.ckpt == nullptr)) return cudaErrorInvalidValue;
@@ -1083,7 +1331,7 @@ cudaError_t launch_state_tc2(const FwdArgs& a, const void* rec,
     if (e != cudaSuccess) return e;
     StateParams sp{a.h0, static_cast<__nv_bfloat16*>(a.o), a.hT, a.ckpt,
                    static_cast<const uint8_t*>(rec), a.T, a.H, nchunks,
-                   2000000000ull, 0};
+                   2000000000ull, 0, ready};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((long)a.B * a.H), kD / kNV);
     cfg.blockDim = dim3(kStateThreads);
@@ -1093,16 +1341,18 @@ cudaError_t launch_state_tc2(const FwdArgs& a, const void* rec,
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = after_prep ? 1 : 0;
+    cfg.numAttrs = ready ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, sp);
 }
 
 cudaError_t launch_chunk_tc2(const FwdArgs& a, void* workspace,
                              cudaStream_t stream) {
     if ((a.o == nullptr) == (a.ckpt == nullptr)) return cudaErrorInvalidValue;
-    cudaError_t e = launch_prep_tc2(a, workspace, stream);
+    cudaError_t e = launch_prep_tc2(a, workspace, stream,
+                                    chunk_tc2_state_ctas(a.B, a.H));
     if (e != cudaSuccess) return e;
-    return launch_state_tc2(a, workspace, stream, true);
+    return launch_state_tc2(a, workspace,
+                            chunk_tc2_ready(workspace, a.B, a.T, a.H), stream);
 }
 
 namespace {
@@ -1123,7 +1373,7 @@ cudaError_t launch_state_selftest(cudaStream_t stream) {
     // one CTA, one chunk; its waits give up after 1 ms
     StateParams sp{nullptr, static_cast<__nv_bfloat16*>(base), nullptr,
                    nullptr, static_cast<const uint8_t*>(base), kC, 1, 1,
-                   1000000ull, 1};
+                   1000000ull, 1, nullptr};
     kla_state_kernel<false><<<dim3(1, 1), kStateThreads, kSSmem, stream>>>(
         m, m, m, m, sp);
     return cudaGetLastError();

@@ -120,21 +120,35 @@ cudaError_t launch_chunk_tc(const FwdArgs& a, cudaStream_t stream);
 bool chunk_tc_eligible(const FwdArgs& a);
 // Two-kernel tensor-core forward (chunk-parallel pre-pass, then the state
 // pass): bf16, dk = dv = 128, C = 64, no separate write keys.  The workspace
-// holds the pre-pass records: chunk_tc2_workspace_bytes(B, T, H) bytes,
-// 16-byte aligned.  Takes exactly one of a.o and a.ckpt.
+// (chunk_tc2_workspace_bytes(B, T, H) bytes, 16-byte aligned) holds the
+// pre-pass records (chunk_tc2_record_bytes(B, T, H) bytes), then one ready
+// flag per record and the pre-pass's work counters.  Takes exactly one of
+// a.o and a.ckpt.
 bool chunk_tc2_eligible(const FwdArgs& a);
+size_t chunk_tc2_record_bytes(int B, int T, int H);
 size_t chunk_tc2_workspace_bytes(int B, int T, int H);
 cudaError_t launch_chunk_tc2(const FwdArgs& a, void* workspace,
                              cudaStream_t stream);
 // Its two launches apart: the pre-pass writes the records of a.q, a.k and
-// the gates (a.v, a.o, a.h0 unused); the state pass reads them.  Two state
-// passes may share one pre-pass when they differ only in v, h0, o, hT.
-// after_prep: the pre-pass is the launch right before on this stream; the
-// state pass is then launched as its programmatic dependent (its set-up
-// overlaps the pre-pass's last wave).
-cudaError_t launch_prep_tc2(const FwdArgs& a, void* rec, cudaStream_t stream);
+// the gates (a.v, a.o, a.h0 unused) into the workspace ws, each followed by
+// its ready flag; the state pass reads them.  Two state passes may share
+// one pre-pass when they differ only in v, h0, o, hT (the second may start
+// at a later sequence of the first: rec and ready then point there).
+// ready: the flags of rec's records when the state pass follows the
+// pre-pass (or another state pass that follows it) directly on this
+// stream; it is then launched as a programmatic dependent and reads each
+// record as soon as its flag is up.  Null: the records are complete (stream
+// order), and the launch is a plain one.  state_ctas: CTAs of the state
+// passes launched with flags (the pre-pass hands its last chunks to the SMs
+// they leave free); 0 when none is.
+cudaError_t launch_prep_tc2(const FwdArgs& a, void* ws, cudaStream_t stream,
+                            int state_ctas);
 cudaError_t launch_state_tc2(const FwdArgs& a, const void* rec,
-                             cudaStream_t stream, bool after_prep);
+                             const unsigned int* ready, cudaStream_t stream);
+// The flags of the records in a workspace of chunk_tc2_workspace_bytes(B,
+// T, H) bytes, and the CTAs of one state pass over B sequences of H heads.
+const unsigned int* chunk_tc2_ready(const void* ws, int B, int T, int H);
+int chunk_tc2_state_ctas(int B, int H);
 cudaError_t read_and_clear_fault2(unsigned int* word);
 // One CTA of the state-pass kernel whose producer issues no copy and whose
 // waits give up after 1 ms: it takes the kernel's abort path and sets the

@@ -402,16 +402,22 @@ extern "C" kla_status kla_chunk_fwd_seq(
         hom.B = P - 1;
     }
     if (kla::chunk_tc2_eligible(zs)) {
-        // one pre-pass over all B P segments, then the two state passes;
-        // with B = 1 the homogeneous run starts at segment 1's records
+        // one pre-pass over all B P segments, then the two state passes on
+        // the same stream, each a programmatic dependent of the launch
+        // before it, so that both run beside the pre-pass's last chunks and
+        // read each record once its flag is up; with B = 1 the homogeneous
+        // run starts at segment 1's records and flags
         char* rec = ws + L.rec;
-        const char* rec_hom =
-            rec + (B == 1 ? kla::chunk_tc2_workspace_bytes(1, tseg, H) : 0);
-        KLA_TRY(kla::launch_prep_tc2(zs, rec, s));
-        KLA_TRY(cudaEventRecord(A.fork, s));
-        KLA_TRY(cudaStreamWaitEvent(A.s, A.fork, 0));
-        KLA_TRY(kla::launch_state_tc2(zs, rec, s, true));
-        KLA_TRY(kla::launch_state_tc2(hom, rec_hom, A.s, false));
+        const unsigned int* ready = kla::chunk_tc2_ready(rec, B * P, tseg, H);
+        const size_t seg1 = B == 1 ? (size_t)H * (tseg / kC) : 0;
+        KLA_TRY(kla::launch_prep_tc2(
+            zs, rec, s,
+            kla::chunk_tc2_state_ctas(zs.B, H) +
+                kla::chunk_tc2_state_ctas(hom.B, H)));
+        KLA_TRY(kla::launch_state_tc2(zs, rec, ready, s));
+        KLA_TRY(kla::launch_state_tc2(
+            hom, rec + seg1 * kla::chunk_tc2_record_bytes(1, kC, 1),
+            ready + seg1, s));
     } else {
         if (!kla::chunk_tc_eligible(zs)) return KLA_ERR_UNSUPPORTED_SHAPE;
         KLA_TRY(kla::launch_chunk_tc(zs, s));

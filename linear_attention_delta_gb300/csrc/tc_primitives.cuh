@@ -461,91 +461,55 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src,
 namespace kla {
 namespace tc {
 
-// ------------------------------------------------------------ clusters
+// ------------------------------------------- hand-over between two grids
+//
+// A record written by one CTA with a bulk store and read by a CTA of another
+// grid with a bulk load: the writer waits for its store to complete, orders
+// it before its generic-proxy flag store (proxy fence) and publishes the
+// flag with release semantics at GPU scope; the reader acquires the flag and
+// orders that before its own bulk load (proxy fence).
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Barrier over all threads of all CTAs of the cluster (release / acquire).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile(
-        "barrier.cluster.arrive.release.aligned;\n\t"
-        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+__device__ __forceinline__ void st_release_gpu(unsigned int* p,
+                                               unsigned int v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(
+                     reinterpret_cast<uint64_t>(p)),
+                 "r"(v)
+                 : "memory");
 }
 
-// Arrive (release, cluster scope) on the mbarrier at the same shared-memory
-// offset as `bar` in CTA `rank` of the cluster.
-__device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar,
-                                                    uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-                 : "=r"(remote)
-                 : "r"(smem_u32(bar)), "r"(rank));
-    asm volatile(
-        "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
-            remote)
-        : "memory");
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];"
+                 : "=r"(v)
+                 : "l"(reinterpret_cast<uint64_t>(p))
+                 : "memory");
+    return v;
 }
 
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar,
-                                                      uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], "
-        "%2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// As mbar_wait_or_abort, with cluster-scope acquire (for barriers that
-// other CTAs of the cluster arrive on).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar,
-                                                  uint32_t parity,
-                                                  const volatile int* abort,
-                                                  uint64_t limit_ns) {
-    const uint32_t a = smem_u32(bar);
+// Poll *flag until it equals `want` (true), `limit_ns` nanoseconds pass or
+// *abort (when given) becomes non-zero (false).
+static __device__ __noinline__ bool flag_wait(const unsigned int* flag,
+                                              unsigned int want,
+                                              const volatile int* abort,
+                                              uint64_t limit_ns) {
+    if (ld_acquire_gpu(flag) == want) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait_cluster(a, parity)) return true;
+        __nanosleep(64);
+        if (ld_acquire_gpu(flag) == want) return true;
         if (abort && *abort) return false;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 
-// TMA tile load multicast to the CTAs of the cluster in `mask` (same
-// shared-memory offset and mbarrier offset in each).
-__device__ __forceinline__ void tma_load_4d_mc(void* dst, const void* tmap,
-                                               uint64_t* bar, int c0, int c1,
-                                               int c2, int c3,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::"
-        "complete_tx::bytes.multicast::cluster [%0], [%1, {%3, %4, %5, %6}], "
-        "[%2], %7;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0),
-        "r"(c1), "r"(c2), "r"(c3), "h"(mask)
-        : "memory");
-}
-
-// Bulk copy multicast to the CTAs of the cluster in `mask`.
-__device__ __forceinline__ void bulk_load_mc(void* dst, const void* src,
-                                             uint32_t bytes, uint64_t* bar,
-                                             uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes."
-        "multicast::cluster [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)),
-        "h"(mask)
-        : "memory");
+__device__ __forceinline__ unsigned int smid() {
+    unsigned int r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
 }
 
 }  // namespace tc

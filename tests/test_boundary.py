@@ -232,10 +232,12 @@ def test_host_fwd_workspace_size(lib):
         4, 4096, 16, 128, 128, 64, 1, ctypes.byref(n)) == OK
     # two slots of one segment (512 tokens: q, k, v, o bf16, two fp32
     # gates), two fp32 states and the forward's own workspace for one
-    # segment (the pre-pass records of the default two-kernel path)
+    # segment (that of the default two-kernel path), each rounded up to
+    # 256 bytes
     rows = 4 * 512 * 16
     fwd = kla.chunk_fwd_workspace_size(4, 512, 16, 128, 128, 64,
                                        kla.torch.bfloat16)
+    fwd = (fwd + 255) // 256 * 256
     assert n.value == (2 * rows * (4 * 128 * 2 + 8) +
                        2 * 4 * 16 * 128 * 128 * 4 + fwd)
     assert lib.kla_chunk_fwd_host_workspace_size(
@@ -270,7 +272,9 @@ def test_seq_fwd_workspace_size_and_host_checks(lib):
     assert lib.kla_chunk_fwd_seq_workspace_size(
         1, 131072, 16, 128, 128, 64, 1, 2, ctypes.byref(n)) == OK
     st = 1 * 2 * 16 * 128 * 128
-    rec = 16 * (131072 // 64) * 16640    # pre-pass records, all chunks
+    nrec = 16 * (131072 // 64)           # pre-pass records, all chunks
+    rec = nrec * 16640 + nrec * 4 + 1040   # records, flags, counters
+    rec = (rec + 255) // 256 * 256
     assert n.value == (4 * st * 4 + 131072 * 16 * 128 * 2 + st * 2
                        + 64 * 16 * 128 * 2 + rec)
     # one segment: nothing to split, no workspace
@@ -360,12 +364,15 @@ def test_overlapping_buffers_are_refused_on_host(lib):
 
 
 def test_forward_workspace_size_and_missing_workspace(lib):
-    """The two-kernel tensor-core path needs 16640 bytes per (batch, head,
-    64-token chunk); the other paths need none; kla_chunk_fwd_ws refuses a
-    missing workspace when one is needed, before any device call."""
+    """The two-kernel tensor-core path needs a 16,640-byte record and a
+    4-byte ready flag per (batch, head, 64-token chunk), the flags rounded up
+    to 16 bytes, and 1,040 bytes of work counters; the other paths need none;
+    kla_chunk_fwd_ws refuses a missing workspace when one is needed, before
+    any device call."""
+    n = 2 * 3 * 4
     assert kla.chunk_fwd_workspace_size(2, 200, 3, 128, 128, 64,
                                         kla.torch.bfloat16, "tc") == \
-        2 * 3 * 4 * 16640
+        n * 16640 + (n * 4 + 15) // 16 * 16 + 1040
     for algo in ("simt", "tc_fused"):
         assert kla.chunk_fwd_workspace_size(2, 200, 3, 128, 128, 64,
                                             kla.torch.bfloat16, algo) == 0

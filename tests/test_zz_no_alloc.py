@@ -28,9 +28,11 @@ ORACLE_KEYS = {"q_grad": "dq", "k_grad": "dk", "v_grad": "dv",
 LIMIT = 32 << 20
 # per (batch, head, chunk) with dk = dv = 128, C = 64: two fp32 128 x 128
 # states, the backward's 17,152-byte record and the forward pre-pass's
-# 16,640-byte one; B1 H4 T3200 is 200 of them, the most of whole chunks
-# that fit (203 would; 204, at T = 3201, do not)
-PER_CHUNK = 2 * 128 * 128 * 4 + 17152 + 16640
+# 16,640-byte one with its 4-byte ready flag, plus 1,040 bytes of the
+# pre-pass's work counters in all; B1 H4 T3200 is 200 chunks, the most of
+# whole chunks that fit (203 would; 204, at T = 3201, do not)
+PER_CHUNK = 2 * 128 * 128 * 4 + 17152 + 16640 + 4
+FIXED = 1040
 FULL = dict(B=1, T=3200, H=4)
 
 
@@ -52,8 +54,9 @@ def test_size_limit_is_checked_after_the_arguments():
     KLA_ERR_INVALID_ARG even when the problem is too large."""
     lib = kla.load_library()
     assert kla.chunk_bwd_workspace_size(FULL["B"], FULL["T"], FULL["H"],
-                                        128, 128, 64) == 200 * PER_CHUNK
-    assert 200 * PER_CHUNK <= LIMIT < 204 * PER_CHUNK
+                                        128, 128, 64) == \
+        200 * PER_CHUNK + FIXED
+    assert 200 * PER_CHUNK + FIXED <= LIMIT < 204 * PER_CHUNK + FIXED
     assert kla.chunk_bwd_workspace_size(1, 3201, 4, 128, 128, 64) > LIMIT
     assert _call(lib, 3201) == -2          # KLA_ERR_UNSUPPORTED_SHAPE
     assert _call(lib, 3201, q=None) == -1  # KLA_ERR_INVALID_ARG first

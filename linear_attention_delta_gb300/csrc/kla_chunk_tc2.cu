@@ -294,303 +294,303 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
     bool failed = false;
 
     for (uint32_t it = 0;; ++it) {
-    const uint32_t ph = it & 1u;
-    if (tid == 0) {
-        const int item = next;   // claimed while the previous tiles landed
-        *item_slot = item;
-        if (item >= 0) {
-            const int cc = item / nbh, bb = item % nbh;
-            const int hh = bb % p.H, b0 = bb / p.H;
-            tc::mbar_arrive_expect_tx(&bars[0], 32768);
-            tc::tma_load_4d(sm + kPKQ, &tm_k, &bars[0], 0, hh, cc * kC, b0);
-            tc::tma_load_4d(sm + kPKQ + 8192, &tm_q, &bars[0], 0, hh, cc * kC, b0);
-            tc::tma_load_4d(sm + kPKQ + 16384, &tm_k, &bars[0], 64, hh, cc * kC, b0);
-            tc::tma_load_4d(sm + kPKQ + 24576, &tm_q, &bars[0], 64, hh, cc * kC, b0);
-        } else if (pending >= 0) {
-            publish(pending);
-            pending = -1;
-        }
-    }
-    __syncthreads();
-    const int item = *item_slot;
-    if (item < 0) break;
-    const int c = item / nbh;
-    const int bh = item % nbh;
-    const int b = bh / p.H, h = bh % p.H;
-    const int t0 = c * kC;
-    uint8_t* brec = p.brec ? p.brec + ((size_t)bh * p.nchunks + c) *
-                                          bwdrec::BYTES
-                           : nullptr;
-    // gates of this chunk: cumulative log2 decay (two warp scans)
-    float la = 0.f, et = 0.f;
-    if (tid < kC && t0 + tid < p.T) {
-        const size_t off = ((size_t)b * p.T + t0 + tid) * p.H + h;
-        la = p.log_alpha[off];
-        et = p.eta[off];
-    }
-    float g2 = la * kLog2e;
-    if (tid < kC) {
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, g2, off);
-            if (lane >= off) g2 += y;
-        }
-        if (tid == 31) *wtot = g2;
-    }
-    __syncthreads();
-    if (tid >= 32 && tid < kC) g2 += *wtot;
-    if (tid < kC) g2s[tid] = g2;
-    // Gamma_ri = 2^(g_r - g_m) e_i with g_m the g of the last column m of
-    // i's 16-column tile and e_i = 2^(g_m - g_i) <= 1: one ex2 per row and
-    // tile instead of one per element (a tile whose g spans more than 2^96
-    // takes the direct form, so that neither factor can overflow)
-    float* ecol = reinterpret_cast<float*>(sm + kPE);
-    if (tid < kC)
-        ecol[tid] = tc::ex2(__shfl_sync(0xffffffffu, g2, (lane & 16) | 15) -
-                            g2);
-
-    // G = [K; Q] K^T: lanes 0..63 K K^T, lanes 64..127 Q K^T (columns 0..63)
-    if (tid == 0) {
-        next = claim();   // while this item's tiles land
-        if (tc::mbar_wait(&bars[0], ph, kLimit)) {
-            tc::tc_fence_after();
-            constexpr uint32_t idG = tc::idesc_bf16(128, 64, false, false);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                tc::mma_bf16(tmem, desc_k(sbase + kPKQ + off),
-                             desc_k(sbase + kPKQ + off), idG, ks > 0);
-            }
-            tc::mma_commit(&bars[1]);
-            if (pending >= 0) {   // the previous item's record (long done)
+        const uint32_t ph = it & 1u;
+        if (tid == 0) {
+            const int item = next;   // claimed while the previous tiles landed
+            *item_slot = item;
+            if (item >= 0) {
+                const int cc = item / nbh, bb = item % nbh;
+                const int hh = bb % p.H, b0 = bb / p.H;
+                tc::mbar_arrive_expect_tx(&bars[0], 32768);
+                tc::tma_load_4d(sm + kPKQ, &tm_k, &bars[0], 0, hh, cc * kC, b0);
+                tc::tma_load_4d(sm + kPKQ + 8192, &tm_q, &bars[0], 0, hh, cc * kC, b0);
+                tc::tma_load_4d(sm + kPKQ + 16384, &tm_k, &bars[0], 64, hh, cc * kC, b0);
+                tc::tma_load_4d(sm + kPKQ + 24576, &tm_q, &bars[0], 64, hh, cc * kC, b0);
+            } else if (pending >= 0) {
                 publish(pending);
                 pending = -1;
             }
-        } else {
-            *reinterpret_cast<volatile int*>(failed_flag) = 1;
         }
-    }
-    __syncthreads();   // g2s complete; the issuing lane rejoined
-    bool ok = *reinterpret_cast<volatile int*>(failed_flag) == 0;
-    ok = ok && tc::mbar_wait(&bars[1], ph, kLimit);
-    ok = !__syncthreads_or(!ok);
-    if (!ok) {
-        if (tid == 0) {
-            atomicOr(&g_fault_word2, 1u);
-            tc::mbar_wait(&bars[0], ph, 100000000ull);   // copies in flight
-            tc::mbar_wait(&bars[1], ph, 100000000ull);   // the MMAs, if issued
+        __syncthreads();
+        const int item = *item_slot;
+        if (item < 0) break;
+        const int c = item / nbh;
+        const int bh = item % nbh;
+        const int b = bh / p.H, h = bh % p.H;
+        const int t0 = c * kC;
+        uint8_t* brec = p.brec ? p.brec + ((size_t)bh * p.nchunks + c) *
+                                              bwdrec::BYTES
+                               : nullptr;
+        // gates of this chunk: cumulative log2 decay (two warp scans)
+        float la = 0.f, et = 0.f;
+        if (tid < kC && t0 + tid < p.T) {
+            const size_t off = ((size_t)b * p.T + t0 + tid) * p.H + h;
+            la = p.log_alpha[off];
+            et = p.eta[off];
         }
-        failed = true;
-        break;
-    }
-    tc::tc_fence_after();
-    {
-        float x[64];
-        const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
-        tc::tmem_ld32(ta, x);
-        tc::tmem_ld32(ta + 32, x + 32);
-        tc::tmem_ld_wait();
+        float g2 = la * kLog2e;
         if (tid < kC) {
-            // A row r = tid: beta_r Gamma_ri (K K^T)_ri for i < r (fp32),
-            // into the packed blocks (I, m), m <= I, of its block row I
-            const int r = tid, I = r >> 4;
-            float kk = 0.f;   // ||k_r||^2, the diagonal of K K^T
-#pragma unroll
-            for (int i = 0; i < 64; ++i) kk = i == r ? x[i] : kk;
-            const float denom = kk + p.eps;
-            const float br = p.gdn ? et : (denom == 0.f ? 0.f : et / denom);
-            betas[r] = br;
-            if (brec) {   // gates of the backward's record (g in natural log)
-                reinterpret_cast<float*>(brec + bwdrec::G_OFF)[r] =
-                    g2 * 0.6931471805599453f;
-                reinterpret_cast<float*>(brec + bwdrec::B_OFF)[r] = br;
-                reinterpret_cast<float*>(brec + bwdrec::N_OFF)[r] = kk;
+    #pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, g2, off);
+                if (lane >= off) g2 += y;
             }
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                if (m > I) break;
-                float* Lr = Lt + bidx(I, m) * kBlk + (r & 15) * kBs - 16 * m;
-                const float gm = g2s[16 * m + 15];
-                const bool fact = fabsf(g2s[16 * m] - gm) <= 96.f;
-                const float bf = br * tc::ex2(g2 - gm);
-#pragma unroll
-                for (int i = 16 * m; i < 16 * m + 16; i += 4) {
-                    const float4 e = *reinterpret_cast<const float4*>(ecol + i);
-                    const float4 gi = *reinterpret_cast<const float4*>(g2s + i);
-                    float4 a;
-                    a.x = fact ? bf * e.x : br * tc::ex2(g2 - gi.x);
-                    a.y = fact ? bf * e.y : br * tc::ex2(g2 - gi.y);
-                    a.z = fact ? bf * e.z : br * tc::ex2(g2 - gi.z);
-                    a.w = fact ? bf * e.w : br * tc::ex2(g2 - gi.w);
-                    a.x = i + 0 < r ? a.x * x[i + 0] : 0.f;
-                    a.y = i + 1 < r ? a.y * x[i + 1] : 0.f;
-                    a.z = i + 2 < r ? a.z * x[i + 2] : 0.f;
-                    a.w = i + 3 < r ? a.w * x[i + 3] : 0.f;
-                    *reinterpret_cast<float4*>(Lr + i) = a;
-                }
-            }
-        } else {
-            // P row r = tid - 64: Gamma_ri (Q K^T)_ri for i <= r, as bf16
-            // operand rows behind TU in the record image
-            const int r = tid - kC;
-            const float gr = g2s[r];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const float gm = g2s[16 * m + 15];
-                const bool fact = fabsf(g2s[16 * m] - gm) <= 96.f;
-                const float f = tc::ex2(gr - gm);
-#pragma unroll
-                for (int i = 16 * m; i < 16 * m + 16; i += 8) {
-                    float e[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float gam =
-                            fact ? f * ecol[i + k] : tc::ex2(gr - g2s[i + k]);
-                        e[k] = i + k <= r ? gam * x[i + k] : 0.f;
-                    }
-                    uint4 v;
-                    v.x = tc::pack_bf16x2(e[0], e[1]);
-                    v.y = tc::pack_bf16x2(e[2], e[3]);
-                    v.z = tc::pack_bf16x2(e[4], e[5]);
-                    v.w = tc::pack_bf16x2(e[6], e[7]);
-                    *reinterpret_cast<uint4*>(out + kRecPTU + swz(r, i)) = v;
-                    if (brec)   // P, rows of 64, for the backward
-                        *reinterpret_cast<uint4*>(brec + bwdrec::P_OFF +
-                                                  (r * kC + i) * 2) = v;
-                }
-            }
+            if (tid == 31) *wtot = g2;
         }
-    }
-    __syncthreads();
-    // diagonal blocks T_bb = (I + L_bb)^{-1}: thread (bb, cl) solves column
-    // cl by substitution (threads 0..63)
-    if (tid < kC) {
-        const int bb = tid >> 4, cl = tid & 15;
-        const float* Lb = Lt + bidx(bb, bb) * kBlk;
-        float xv[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) xv[r] = (r == cl) ? 1.f : 0.f;
-#pragma unroll
-        for (int r = 1; r < 16; ++r) {
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < r; i += 2) {
-                a0 = fmaf(Lb[r * kBs + i], xv[i], a0);
-                if (i + 1 < r) a1 = fmaf(Lb[r * kBs + i + 1], xv[i + 1], a1);
-            }
-            if (r > cl) xv[r] = -(a0 + a1);
-        }
-        __syncwarp();   // this warp's two blocks of L are read: T over them
-        float* Tb = Lt + bidx(bb, bb) * kBlk + cl;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Tb[r * kBs] = xv[r];
-    }
-    __syncthreads();
-    float* Y = reinterpret_cast<float*>(sm + kPY) + warp * 128;
-    // level 1: (1,0), (2,1), (3,2); 6 slabs of 8 columns on 4 warps
-    for (int job = warp; job < 6; job += 4) {
-        const int I = (job >> 1) + 1;
-        offdiag_slab(Lt, Tt, Y, I, I - 1, 8 * (job & 1), lane);
-        __syncwarp();
-    }
-    __syncthreads();
-    // level 2: (2,0), (3,1)
-    offdiag_slab(Lt, Tt, Y, 2 + (warp >> 1), warp >> 1, 8 * (warp & 1), lane);
-    __syncthreads();
-    // level 3: (3,0)
-    if (warp < 2) offdiag_slab(Lt, Tt, Y, 3, 0, 8 * warp, lane);
-    __syncthreads();
+        __syncthreads();
+        if (tid >= 32 && tid < kC) g2 += *wtot;
+        if (tid < kC) g2s[tid] = g2;
+        // Gamma_ri = 2^(g_r - g_m) e_i with g_m the g of the last column m of
+        // i's 16-column tile and e_i = 2^(g_m - g_i) <= 1: one ex2 per row and
+        // tile instead of one per element (a tile whose g spans more than 2^96
+        // takes the direct form, so that neither factor can overflow)
+        float* ecol = reinterpret_cast<float*>(sm + kPE);
+        if (tid < kC)
+            ecol[tid] = tc::ex2(__shfl_sync(0xffffffffu, g2, (lane & 16) | 15) -
+                                g2);
 
-    // TU = T Diag(beta) as bf16 operand rows: thread -> (row, 32 columns)
-    {
-        const int r = tid >> 1, c0 = 32 * (tid & 1);
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-            uint4 v;
-            const int col = c0 + j, I = r >> 4, J = col >> 4;
-            const float* tr =
-                tblock(Lt, Tt, I, J < I ? J : I) + (r & 15) * kBs + (col & 15);
-            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);   // J > I
-            const float4 ta =
-                J <= I ? *reinterpret_cast<const float4*>(tr) : z;
-            const float4 tb =
-                J <= I ? *reinterpret_cast<const float4*>(tr + 4) : z;
-            const float4 ba = *reinterpret_cast<const float4*>(betas + c0 + j);
-            const float4 bb =
-                *reinterpret_cast<const float4*>(betas + c0 + j + 4);
-            v.x = tc::pack_bf16x2(ta.x * ba.x, ta.y * ba.y);
-            v.y = tc::pack_bf16x2(ta.z * ba.z, ta.w * ba.w);
-            v.z = tc::pack_bf16x2(tb.x * bb.x, tb.y * bb.y);
-            v.w = tc::pack_bf16x2(tb.z * bb.z, tb.w * bb.w);
-            *reinterpret_cast<uint4*>(out + kRecTU + swz(r, c0 + j)) = v;
-            if (brec) {   // T itself, rows of 64, for the backward
-                uint4 w;
-                w.x = tc::pack_bf16x2(ta.x, ta.y);
-                w.y = tc::pack_bf16x2(ta.z, ta.w);
-                w.z = tc::pack_bf16x2(tb.x, tb.y);
-                w.w = tc::pack_bf16x2(tb.z, tb.w);
-                *reinterpret_cast<uint4*>(brec + bwdrec::T_OFF +
-                                          (r * kC + col) * 2) = w;
+        // G = [K; Q] K^T: lanes 0..63 K K^T, lanes 64..127 Q K^T (columns 0..63)
+        if (tid == 0) {
+            next = claim();   // while this item's tiles land
+            if (tc::mbar_wait(&bars[0], ph, kLimit)) {
+                tc::tc_fence_after();
+                constexpr uint32_t idG = tc::idesc_bf16(128, 64, false, false);
+    #pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                    tc::mma_bf16(tmem, desc_k(sbase + kPKQ + off),
+                                 desc_k(sbase + kPKQ + off), idG, ks > 0);
+                }
+                tc::mma_commit(&bars[1]);
+                if (pending >= 0) {   // the previous item's record (long done)
+                    publish(pending);
+                    pending = -1;
+                }
+            } else {
+                *reinterpret_cast<volatile int*>(failed_flag) = 1;
             }
         }
-    }
-    if (tid < kC) reinterpret_cast<float*>(out + kRecG)[tid] = g2s[tid];
-    tc::fence_proxy_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
-    // PTU = P TU on the tensor cores: [TU; P] TU, lanes 64..127, over G's
-    // columns (G was read out before the barriers above); TU is K-major as
-    // the A rows and MN-major as B
-    if (tid == 0) {
+        __syncthreads();   // g2s complete; the issuing lane rejoined
+        bool ok = *reinterpret_cast<volatile int*>(failed_flag) == 0;
+        ok = ok && tc::mbar_wait(&bars[1], ph, kLimit);
+        ok = !__syncthreads_or(!ok);
+        if (!ok) {
+            if (tid == 0) {
+                atomicOr(&g_fault_word2, 1u);
+                tc::mbar_wait(&bars[0], ph, 100000000ull);   // copies in flight
+                tc::mbar_wait(&bars[1], ph, 100000000ull);   // the MMAs, if issued
+            }
+            failed = true;
+            break;
+        }
         tc::tc_fence_after();
-        constexpr uint32_t idP = tc::idesc_bf16(128, 64, false, true);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16(tmem, desc_k(sbase + kPKQ + kRecTU + ks * 32),
-                         desc_mn(sbase + kPKQ + kRecTU + ks * 2048, 0), idP,
-                         ks > 0);
-        tc::mma_commit(&bars[2]);
-    }
-    __syncwarp();
-    ok = tc::mbar_wait(&bars[2], ph, kLimit);
-    if (!__syncthreads_or(!ok)) {
-        tc::tc_fence_after();
-        if (tid >= kC) {   // PTU rows over P
-            const int r = tid - kC;
+        {
             float x[64];
             const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
             tc::tmem_ld32(ta, x);
             tc::tmem_ld32(ta + 32, x + 32);
             tc::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                uint4 v;
-                v.x = tc::pack_bf16x2(x[8 * j + 0], x[8 * j + 1]);
-                v.y = tc::pack_bf16x2(x[8 * j + 2], x[8 * j + 3]);
-                v.z = tc::pack_bf16x2(x[8 * j + 4], x[8 * j + 5]);
-                v.w = tc::pack_bf16x2(x[8 * j + 6], x[8 * j + 7]);
-                *reinterpret_cast<uint4*>(out + kRecPTU + swz(r, 8 * j)) = v;
+            if (tid < kC) {
+                // A row r = tid: beta_r Gamma_ri (K K^T)_ri for i < r (fp32),
+                // into the packed blocks (I, m), m <= I, of its block row I
+                const int r = tid, I = r >> 4;
+                float kk = 0.f;   // ||k_r||^2, the diagonal of K K^T
+    #pragma unroll
+                for (int i = 0; i < 64; ++i) kk = i == r ? x[i] : kk;
+                const float denom = kk + p.eps;
+                const float br = p.gdn ? et : (denom == 0.f ? 0.f : et / denom);
+                betas[r] = br;
+                if (brec) {   // gates of the backward's record (g in natural log)
+                    reinterpret_cast<float*>(brec + bwdrec::G_OFF)[r] =
+                        g2 * 0.6931471805599453f;
+                    reinterpret_cast<float*>(brec + bwdrec::B_OFF)[r] = br;
+                    reinterpret_cast<float*>(brec + bwdrec::N_OFF)[r] = kk;
+                }
+    #pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    if (m > I) break;
+                    float* Lr = Lt + bidx(I, m) * kBlk + (r & 15) * kBs - 16 * m;
+                    const float gm = g2s[16 * m + 15];
+                    const bool fact = fabsf(g2s[16 * m] - gm) <= 96.f;
+                    const float bf = br * tc::ex2(g2 - gm);
+    #pragma unroll
+                    for (int i = 16 * m; i < 16 * m + 16; i += 4) {
+                        const float4 e = *reinterpret_cast<const float4*>(ecol + i);
+                        const float4 gi = *reinterpret_cast<const float4*>(g2s + i);
+                        float4 a;
+                        a.x = fact ? bf * e.x : br * tc::ex2(g2 - gi.x);
+                        a.y = fact ? bf * e.y : br * tc::ex2(g2 - gi.y);
+                        a.z = fact ? bf * e.z : br * tc::ex2(g2 - gi.z);
+                        a.w = fact ? bf * e.w : br * tc::ex2(g2 - gi.w);
+                        a.x = i + 0 < r ? a.x * x[i + 0] : 0.f;
+                        a.y = i + 1 < r ? a.y * x[i + 1] : 0.f;
+                        a.z = i + 2 < r ? a.z * x[i + 2] : 0.f;
+                        a.w = i + 3 < r ? a.w * x[i + 3] : 0.f;
+                        *reinterpret_cast<float4*>(Lr + i) = a;
+                    }
+                }
+            } else {
+                // P row r = tid - 64: Gamma_ri (Q K^T)_ri for i <= r, as bf16
+                // operand rows behind TU in the record image
+                const int r = tid - kC;
+                const float gr = g2s[r];
+    #pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float gm = g2s[16 * m + 15];
+                    const bool fact = fabsf(g2s[16 * m] - gm) <= 96.f;
+                    const float f = tc::ex2(gr - gm);
+    #pragma unroll
+                    for (int i = 16 * m; i < 16 * m + 16; i += 8) {
+                        float e[8];
+    #pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const float gam =
+                                fact ? f * ecol[i + k] : tc::ex2(gr - g2s[i + k]);
+                            e[k] = i + k <= r ? gam * x[i + k] : 0.f;
+                        }
+                        uint4 v;
+                        v.x = tc::pack_bf16x2(e[0], e[1]);
+                        v.y = tc::pack_bf16x2(e[2], e[3]);
+                        v.z = tc::pack_bf16x2(e[4], e[5]);
+                        v.w = tc::pack_bf16x2(e[6], e[7]);
+                        *reinterpret_cast<uint4*>(out + kRecPTU + swz(r, i)) = v;
+                        if (brec)   // P, rows of 64, for the backward
+                            *reinterpret_cast<uint4*>(brec + bwdrec::P_OFF +
+                                                      (r * kC + i) * 2) = v;
+                    }
+                }
             }
         }
+        __syncthreads();
+        // diagonal blocks T_bb = (I + L_bb)^{-1}: thread (bb, cl) solves column
+        // cl by substitution (threads 0..63)
+        if (tid < kC) {
+            const int bb = tid >> 4, cl = tid & 15;
+            const float* Lb = Lt + bidx(bb, bb) * kBlk;
+            float xv[16];
+    #pragma unroll
+            for (int r = 0; r < 16; ++r) xv[r] = (r == cl) ? 1.f : 0.f;
+    #pragma unroll
+            for (int r = 1; r < 16; ++r) {
+                float a0 = 0.f, a1 = 0.f;
+    #pragma unroll
+                for (int i = 0; i < r; i += 2) {
+                    a0 = fmaf(Lb[r * kBs + i], xv[i], a0);
+                    if (i + 1 < r) a1 = fmaf(Lb[r * kBs + i + 1], xv[i + 1], a1);
+                }
+                if (r > cl) xv[r] = -(a0 + a1);
+            }
+            __syncwarp();   // this warp's two blocks of L are read: T over them
+            float* Tb = Lt + bidx(bb, bb) * kBlk + cl;
+    #pragma unroll
+            for (int r = 0; r < 16; ++r) Tb[r * kBs] = xv[r];
+        }
+        __syncthreads();
+        float* Y = reinterpret_cast<float*>(sm + kPY) + warp * 128;
+        // level 1: (1,0), (2,1), (3,2); 6 slabs of 8 columns on 4 warps
+        for (int job = warp; job < 6; job += 4) {
+            const int I = (job >> 1) + 1;
+            offdiag_slab(Lt, Tt, Y, I, I - 1, 8 * (job & 1), lane);
+            __syncwarp();
+        }
+        __syncthreads();
+        // level 2: (2,0), (3,1)
+        offdiag_slab(Lt, Tt, Y, 2 + (warp >> 1), warp >> 1, 8 * (warp & 1), lane);
+        __syncthreads();
+        // level 3: (3,0)
+        if (warp < 2) offdiag_slab(Lt, Tt, Y, 3, 0, 8 * warp, lane);
+        __syncthreads();
+
+        // TU = T Diag(beta) as bf16 operand rows: thread -> (row, 32 columns)
+        {
+            const int r = tid >> 1, c0 = 32 * (tid & 1);
+    #pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+                uint4 v;
+                const int col = c0 + j, I = r >> 4, J = col >> 4;
+                const float* tr =
+                    tblock(Lt, Tt, I, J < I ? J : I) + (r & 15) * kBs + (col & 15);
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);   // J > I
+                const float4 ta =
+                    J <= I ? *reinterpret_cast<const float4*>(tr) : z;
+                const float4 tb =
+                    J <= I ? *reinterpret_cast<const float4*>(tr + 4) : z;
+                const float4 ba = *reinterpret_cast<const float4*>(betas + c0 + j);
+                const float4 bb =
+                    *reinterpret_cast<const float4*>(betas + c0 + j + 4);
+                v.x = tc::pack_bf16x2(ta.x * ba.x, ta.y * ba.y);
+                v.y = tc::pack_bf16x2(ta.z * ba.z, ta.w * ba.w);
+                v.z = tc::pack_bf16x2(tb.x * bb.x, tb.y * bb.y);
+                v.w = tc::pack_bf16x2(tb.z * bb.z, tb.w * bb.w);
+                *reinterpret_cast<uint4*>(out + kRecTU + swz(r, c0 + j)) = v;
+                if (brec) {   // T itself, rows of 64, for the backward
+                    uint4 w;
+                    w.x = tc::pack_bf16x2(ta.x, ta.y);
+                    w.y = tc::pack_bf16x2(ta.z, ta.w);
+                    w.z = tc::pack_bf16x2(tb.x, tb.y);
+                    w.w = tc::pack_bf16x2(tb.z, tb.w);
+                    *reinterpret_cast<uint4*>(brec + bwdrec::T_OFF +
+                                              (r * kC + col) * 2) = w;
+                }
+            }
+        }
+        if (tid < kC) reinterpret_cast<float*>(out + kRecG)[tid] = g2s[tid];
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
         __syncthreads();
-        if (tid == 0) {   // the record, one bulk copy
-            tc::bulk_store(p.rec + ((size_t)bh * p.nchunks + c) * kRecBytes,
-                           out, kRecBytes);
-            tc::tma_store_commit();
-            tc::tma_store_wait_read<0>();   // the image may be overwritten
-            pending = bh * p.nchunks + c;
-        }
-    } else {
+        // PTU = P TU on the tensor cores: [TU; P] TU, lanes 64..127, over G's
+        // columns (G was read out before the barriers above); TU is K-major as
+        // the A rows and MN-major as B
         if (tid == 0) {
-            atomicOr(&g_fault_word2, 1u);
-            tc::mbar_wait(&bars[2], ph, 100000000ull);
+            tc::tc_fence_after();
+            constexpr uint32_t idP = tc::idesc_bf16(128, 64, false, true);
+    #pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tmem, desc_k(sbase + kPKQ + kRecTU + ks * 32),
+                             desc_mn(sbase + kPKQ + kRecTU + ks * 2048, 0), idP,
+                             ks > 0);
+            tc::mma_commit(&bars[2]);
         }
-        failed = true;
-    }
-    __syncthreads();
-    if (failed) break;
+        __syncwarp();
+        ok = tc::mbar_wait(&bars[2], ph, kLimit);
+        if (!__syncthreads_or(!ok)) {
+            tc::tc_fence_after();
+            if (tid >= kC) {   // PTU rows over P
+                const int r = tid - kC;
+                float x[64];
+                const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
+                tc::tmem_ld32(ta, x);
+                tc::tmem_ld32(ta + 32, x + 32);
+                tc::tmem_ld_wait();
+    #pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint4 v;
+                    v.x = tc::pack_bf16x2(x[8 * j + 0], x[8 * j + 1]);
+                    v.y = tc::pack_bf16x2(x[8 * j + 2], x[8 * j + 3]);
+                    v.z = tc::pack_bf16x2(x[8 * j + 4], x[8 * j + 5]);
+                    v.w = tc::pack_bf16x2(x[8 * j + 6], x[8 * j + 7]);
+                    *reinterpret_cast<uint4*>(out + kRecPTU + swz(r, 8 * j)) = v;
+                }
+            }
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            __syncthreads();
+            if (tid == 0) {   // the record, one bulk copy
+                tc::bulk_store(p.rec + ((size_t)bh * p.nchunks + c) * kRecBytes,
+                               out, kRecBytes);
+                tc::tma_store_commit();
+                tc::tma_store_wait_read<0>();   // the image may be overwritten
+                pending = bh * p.nchunks + c;
+            }
+        } else {
+            if (tid == 0) {
+                atomicOr(&g_fault_word2, 1u);
+                tc::mbar_wait(&bars[2], ph, 100000000ull);
+            }
+            failed = true;
+        }
+        __syncthreads();
+        if (failed) break;
     }   // items
     if (tid == 0 && pending >= 0) publish(pending);
     tc::tc_fence_before();

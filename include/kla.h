@@ -145,7 +145,7 @@ KLA_API kla_status kla_chunk_fwd_ex(const void* q, const void* k, const void* v,
  * needs with this algorithm: for bf16, dk = dv = 128, C = 64 and KLA_ALGO_TC
  * or KLA_ALGO_AUTO, the pre-pass records of the two-kernel tensor-core path
  * (16,640 bytes per (batch, head, chunk of 64 tokens)), one 4-byte ready
- * flag per record (rounded up to 16 bytes in all) and 1,040 bytes of the
+ * flag per record (rounded up to 16 bytes in all) and 528 bytes of the
  * pre-pass's work counters; 0 otherwise (those paths need none).  Errors:
  * KLA_ERR_INVALID_ARG (null `bytes`, negative size, bad enum),
  * KLA_ERR_UNSUPPORTED_SHAPE (dk, dv or C outside the set).
@@ -405,7 +405,7 @@ KLA_API kla_status kla_decode_step_kw(const void* q, const void* k,
  * gates of the chunk) for the tensor-core kernels, plus, when also
  * dv = 128, the workspace of the two-kernel forward that writes the
  * checkpoints (kla_chunk_fwd_workspace_size: 16,644 bytes per (batch, head,
- * chunk), rounded up to 16 bytes, and 1,040 bytes).  Writes 0 for an empty
+ * chunk), rounded up to 16 bytes, and 528 bytes).  Writes 0 for an empty
  * problem.  Errors:
  * KLA_ERR_INVALID_ARG (null `bytes`, negative size, C <= 0).
  */

@@ -124,14 +124,16 @@ static_assert(5 * (kPSmem + 1024) <= 233472, "pre-pass shared memory");
 // as fit at once); each CTA takes chunk-heads from a counter in chunk-major
 // order (every head's chunk 0, then chunk 1, ...) and raises the record's
 // ready flag once the record is in memory.  Past item `release`, only the
-// CTAs of the first `reserved_sms` SMs to register keep taking work; the
-// others exit, and their SMs take the state pass, which starts on chunk 0
-// while the reserved SMs finish the last chunks.  Control words (zeroed
+// CTAs of the first reserved_sms / 2 TPCs (SM ids 2t and 2t + 1) to
+// register keep taking work; the others exit, and their SMs take the state
+// pass, which starts on chunk 0 while the reserved SMs finish the last
+// chunks.  Roles go by TPC because a state-pass CTA whose TPC mate kept
+// pre-pass CTAs ran its chain up to 20 % slower.  Control words (zeroed
 // before each launch): next item below `release`, next item from
-// `release`, SMs registered as reserved, then one role per SM id (0 unset,
+// `release`, TPCs registered as reserved, then one role per TPC (0 unset,
 // 1 reserved, 2 released, 3 being decided).
 constexpr int kMaxSmId = 256;
-constexpr int kCtrlWords = 4 + kMaxSmId;
+constexpr int kCtrlWords = 4 + kMaxSmId / 2;
 
 struct PrepParams {
     const float* log_alpha;
@@ -265,12 +267,13 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc::fence_mbar_init();
         const unsigned int sid = tc::smid();
         if (p.release < p.items && sid < (unsigned)kMaxSmId) {
-            // the first CTA of an SM decides its role for all of them
-            unsigned int* role = p.ctrl + 4 + sid;
+            // the first CTA of a TPC decides its role for all of them
+            unsigned int* role = p.ctrl + 4 + (sid >> 1);
             unsigned int r = atomicCAS(role, 0u, 3u);
             if (r == 0u) {
-                r = atomicAdd(p.ctrl + 2, 1u) < (unsigned)p.reserved_sms ? 1u
-                                                                         : 2u;
+                r = atomicAdd(p.ctrl + 2, 1u) < (unsigned)p.reserved_sms / 2
+                        ? 1u
+                        : 2u;
                 atomicExch(role, r);
             } else if (r == 3u) {
                 const uint64_t w0 = tc::globaltimer_ns();

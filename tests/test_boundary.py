@@ -273,7 +273,7 @@ def test_seq_fwd_workspace_size_and_host_checks(lib):
         1, 131072, 16, 128, 128, 64, 1, 2, ctypes.byref(n)) == OK
     st = 1 * 2 * 16 * 128 * 128
     nrec = 16 * (131072 // 64)           # pre-pass records, all chunks
-    rec = nrec * 16640 + nrec * 4 + 1040   # records, flags, counters
+    rec = nrec * 16640 + nrec * 4 + 528   # records, flags, counters
     rec = (rec + 255) // 256 * 256
     assert n.value == (4 * st * 4 + 131072 * 16 * 128 * 2 + st * 2
                        + 64 * 16 * 128 * 2 + rec)
@@ -366,13 +366,13 @@ def test_overlapping_buffers_are_refused_on_host(lib):
 def test_forward_workspace_size_and_missing_workspace(lib):
     """The two-kernel tensor-core path needs a 16,640-byte record and a
     4-byte ready flag per (batch, head, 64-token chunk), the flags rounded up
-    to 16 bytes, and 1,040 bytes of work counters; the other paths need none;
+    to 16 bytes, and 528 bytes of work counters; the other paths need none;
     kla_chunk_fwd_ws refuses a missing workspace when one is needed, before
     any device call."""
     n = 2 * 3 * 4
     assert kla.chunk_fwd_workspace_size(2, 200, 3, 128, 128, 64,
                                         kla.torch.bfloat16, "tc") == \
-        n * 16640 + (n * 4 + 15) // 16 * 16 + 1040
+        n * 16640 + (n * 4 + 15) // 16 * 16 + 528
     for algo in ("simt", "tc_fused"):
         assert kla.chunk_fwd_workspace_size(2, 200, 3, 128, 128, 64,
                                             kla.torch.bfloat16, algo) == 0

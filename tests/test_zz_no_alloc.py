@@ -28,11 +28,11 @@ ORACLE_KEYS = {"q_grad": "dq", "k_grad": "dk", "v_grad": "dv",
 LIMIT = 32 << 20
 # per (batch, head, chunk) with dk = dv = 128, C = 64: two fp32 128 x 128
 # states, the backward's 17,152-byte record and the forward pre-pass's
-# 16,640-byte one with its 4-byte ready flag, plus 1,040 bytes of the
+# 16,640-byte one with its 4-byte ready flag, plus 528 bytes of the
 # pre-pass's work counters in all; B1 H4 T3200 is 200 chunks, the most of
 # whole chunks that fit (203 would; 204, at T = 3201, do not)
 PER_CHUNK = 2 * 128 * 128 * 4 + 17152 + 16640 + 4
-FIXED = 1040
+FIXED = 528
 FULL = dict(B=1, T=3200, H=4)
 
 

@@ -14,6 +14,7 @@
 // the first (whose run started from the true initial state).  With one
 // sequence the homogeneous run skips the first segment, whose Phi and O_hom
 // are never used.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -166,95 +167,129 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4],
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// o[rows of segment s] += O_hom,s S_s, 128 rows of one (b, s >= 1, h) per
-// CTA; warp w forms rows 16 w .. 16 w + 15, all 128 columns (m16n8k16,
-// bf16 operands, fp32 accumulation), added to o in fp32 and rounded once.
+// o[rows of segment s] += O_hom,s S_s.  One CTA takes a run of 128-row
+// tiles of one (b, s >= 1, h): S_s is loaded once, and the next tiles of
+// O_hom and o come in (cp.async, double-buffered) while the current ones
+// are used; warp w forms rows 16 w .. 16 w + 15 of a tile, all 128 columns
+// (m16n8k16, bf16 operands, fp32 accumulation), added to o in fp32 and
+// rounded once in shared memory, and the tile goes back to o in 16-byte
+// row pieces.
 constexpr int kRows = 128;
 constexpr int kLd = kD + 8;        // bf16 row stride: conflict-free fragments
-__global__ void __launch_bounds__(256)
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src,
+                                           bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__global__ void __launch_bounds__(256, 1)
 add_segment_start(__nv_bfloat16* __restrict__ o,
                   const __nv_bfloat16* __restrict__ ohom,
                   const __nv_bfloat16* __restrict__ sst, int T, int H, int P,
-                  int tseg) {
+                  int tseg, int tiles_per_cta) {
     extern __shared__ __align__(16) uint8_t smem[];
-    __nv_bfloat16* As = reinterpret_cast<__nv_bfloat16*>(smem);
-    __nv_bfloat16* Bs = As + kRows * kLd;
+    __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(smem);
+    __nv_bfloat16* As0 = Bs + kD * kLd;                 // two O_hom tiles
+    __nv_bfloat16* Os0 = As0 + 2 * kRows * kLd;         // two o tiles
     const int h = blockIdx.y;
     const int b = blockIdx.z / (P - 1), s = blockIdx.z % (P - 1) + 1;
-    const int r_base = blockIdx.x * kRows;          // row within the segment
+    const int ntiles = (tseg + kRows - 1) / kRows;
+    const int t_begin = blockIdx.x * tiles_per_cta;
+    const int t_end = min(t_begin + tiles_per_cta, ntiles);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t row_stride = (size_t)H * kD;
     auto tok = [&](int r) { return (size_t)b * T + (size_t)s * tseg + r; };
     const int g = lane >> 2, q = lane & 3;
     const int ra = warp * 16 + g;
 
-    // this thread's o entries first, so that their loads are in flight
-    // while the tiles come in and the products run
-    uint32_t old[2][kD / 8];
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int r = r_base + ra + 8 * half;
-        const __nv_bfloat16* orow = o + tok(r) * row_stride + (size_t)h * kD;
-#pragma unroll
-        for (int nt = 0; nt < kD / 8; ++nt)
-            old[half][nt] = r < tseg ? *reinterpret_cast<const uint32_t*>(
-                                           orow + 8 * nt + 2 * q)
-                                     : 0u;
-    }
-
-    for (int i = tid; i < kRows * (kD / 8); i += 256) {
-        const int r = i / (kD / 8), c8 = i % (kD / 8);
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (r_base + r < tseg)
-            v = *reinterpret_cast<const uint4*>(
-                ohom + tok(r_base + r) * row_stride + (size_t)h * kD + 8 * c8);
-        *reinterpret_cast<uint4*>(As + r * kLd + 8 * c8) = v;
-    }
+    auto load_tile = [&](int t, int buf) {
+        for (int i = tid; i < kRows * (kD / 8); i += 256) {
+            const int r = i / (kD / 8), c8 = i % (kD / 8);
+            const int row = t * kRows + r;
+            const bool valid = row < tseg;
+            const size_t off =
+                tok(valid ? row : 0) * row_stride + (size_t)h * kD + 8 * c8;
+            cp_async16(As0 + (buf * kRows + r) * kLd + 8 * c8, ohom + off,
+                       valid);
+            cp_async16(Os0 + (buf * kRows + r) * kLd + 8 * c8, o + off, valid);
+        }
+    };
     const __nv_bfloat16* S =
         sst + (((size_t)(b * P + s) * H + h) * kD) * kD;   // [dv][dk]
     for (int i = tid; i < kD * (kD / 8); i += 256) {
         const int n = i / (kD / 8), c8 = i % (kD / 8);
-        *reinterpret_cast<uint4*>(Bs + n * kLd + 8 * c8) =
-            *reinterpret_cast<const uint4*>(S + (size_t)n * kD + 8 * c8);
+        cp_async16(Bs + n * kLd + 8 * c8, S + (size_t)n * kD + 8 * c8, true);
     }
-    __syncthreads();
+    if (t_begin < t_end) load_tile(t_begin, 0);
+    cp_async_commit();
 
-    float acc[kD / 8][4];
+    for (int t = t_begin; t < t_end; ++t) {
+        const int buf = (t - t_begin) & 1;
+        const __nv_bfloat16* As = As0 + buf * kRows * kLd;
+        __nv_bfloat16* Os = Os0 + buf * kRows * kLd;
+        if (t + 1 < t_end)   // the next tiles into the other buffers
+            load_tile(t + 1, buf ^ 1);
+        cp_async_commit();
+        cp_async_wait<1>();   // all but the group just committed
+        __syncthreads();
+
+        float acc[kD / 8][4];
 #pragma unroll
-    for (int nt = 0; nt < kD / 8; ++nt)
-        acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+        for (int nt = 0; nt < kD / 8; ++nt)
+            acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < kD / 16; ++ks) {
-        const int k0 = 16 * ks + 2 * q;
-        uint32_t a[4];
-        a[0] = *reinterpret_cast<const uint32_t*>(As + ra * kLd + k0);
-        a[1] = *reinterpret_cast<const uint32_t*>(As + (ra + 8) * kLd + k0);
-        a[2] = *reinterpret_cast<const uint32_t*>(As + ra * kLd + k0 + 8);
-        a[3] = *reinterpret_cast<const uint32_t*>(As + (ra + 8) * kLd + k0 + 8);
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            const int k0 = 16 * ks + 2 * q;
+            uint32_t a[4];
+            a[0] = *reinterpret_cast<const uint32_t*>(As + ra * kLd + k0);
+            a[1] = *reinterpret_cast<const uint32_t*>(As + (ra + 8) * kLd + k0);
+            a[2] = *reinterpret_cast<const uint32_t*>(As + ra * kLd + k0 + 8);
+            a[3] =
+                *reinterpret_cast<const uint32_t*>(As + (ra + 8) * kLd + k0 + 8);
 #pragma unroll
-        for (int nt = 0; nt < kD / 8; ++nt) {
-            const __nv_bfloat16* bn = Bs + (8 * nt + g) * kLd + k0;
-            mma_bf16_16816(acc[nt], a, *reinterpret_cast<const uint32_t*>(bn),
-                           *reinterpret_cast<const uint32_t*>(bn + 8));
+            for (int nt = 0; nt < kD / 8; ++nt) {
+                const __nv_bfloat16* bn = Bs + (8 * nt + g) * kLd + k0;
+                mma_bf16_16816(acc[nt], a,
+                               *reinterpret_cast<const uint32_t*>(bn),
+                               *reinterpret_cast<const uint32_t*>(bn + 8));
+            }
         }
-    }
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int r = r_base + ra + 8 * half;
-        if (r >= tseg) continue;
-        __nv_bfloat16* orow = o + tok(r) * row_stride + (size_t)h * kD;
+        for (int half = 0; half < 2; ++half) {
+            __nv_bfloat162* orow = reinterpret_cast<__nv_bfloat162*>(
+                Os + (ra + 8 * half) * kLd + 2 * q);
 #pragma unroll
-        for (int nt = 0; nt < kD / 8; ++nt) {
-            const float2 o0 = __bfloat1622float2(
-                *reinterpret_cast<const __nv_bfloat162*>(&old[half][nt]));
-            *reinterpret_cast<__nv_bfloat162*>(orow + 8 * nt + 2 * q) =
-                __floats2bfloat162_rn(o0.x + acc[nt][2 * half],
-                                      o0.y + acc[nt][2 * half + 1]);
+            for (int nt = 0; nt < kD / 8; ++nt) {
+                const float2 o0 = __bfloat1622float2(orow[4 * nt]);
+                orow[4 * nt] = __floats2bfloat162_rn(
+                    o0.x + acc[nt][2 * half], o0.y + acc[nt][2 * half + 1]);
+            }
         }
+        __syncthreads();
+        for (int i = tid; i < kRows * (kD / 8); i += 256) {
+            const int r = i / (kD / 8), c8 = i % (kD / 8);
+            const int row = t * kRows + r;
+            if (row < tseg)
+                *reinterpret_cast<uint4*>(o + tok(row) * row_stride +
+                                          (size_t)h * kD + 8 * c8) =
+                    *reinterpret_cast<const uint4*>(Os + r * kLd + 8 * c8);
+        }
+        __syncthreads();   // these buffers are refilled next iteration
     }
+    cp_async_wait<0>();
 }
 
-constexpr size_t kAddSmem = 2 * (size_t)kRows * kLd * sizeof(__nv_bfloat16);
+constexpr size_t kAddSmem = 5 * (size_t)kRows * kLd * sizeof(__nv_bfloat16);
 
 // Second stream and events of one device, created on first use.
 struct Aux {
@@ -430,10 +465,17 @@ extern "C" kla_status kla_chunk_fwd_seq(
     chain_states<<<dim3((unsigned)(B * H), kD / kCombCols), 256, 0, s>>>(
         hts, phi, sst, hT, P, H);
     KLA_TRY(cudaGetLastError());
-    add_segment_start<<<dim3((unsigned)((tseg + kRows - 1) / kRows),
+    // runs of tiles: about four waves of one CTA per SM
+    const int ntiles = (tseg + kRows - 1) / kRows;
+    const long all_tiles = (long)ntiles * H * B * (P - 1);
+    const long slots = kla::device_sm_count();
+    const int per_cta =
+        (int)std::max(1L, std::min((long)ntiles, (all_tiles + 4 * slots - 1) /
+                                                     (4 * slots)));
+    add_segment_start<<<dim3((unsigned)((ntiles + per_cta - 1) / per_cta),
                              (unsigned)H, (unsigned)(B * (P - 1))),
                         256, kAddSmem, s>>>(
-        static_cast<__nv_bfloat16*>(o), ohom, sst, T, H, P, tseg);
+        static_cast<__nv_bfloat16*>(o), ohom, sst, T, H, P, tseg, per_cta);
     KLA_TRY(cudaGetLastError());
 #undef KLA_TRY
     return KLA_OK;

@@ -743,39 +743,6 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int j0 = blockIdx.y * kNV;
     const int nchunks = p.nchunks;
 
-    if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i) tc::mbar_init(&bars[i], 1);
-        *abort_flag = 0;
-        *issued = 0;
-        tc::fence_mbar_init();
-    }
-    if (warp == 0) {
-        tc::tmem_alloc(tmem_slot, kTmemCols);
-        tc::tmem_relinquish();
-    }
-    float S[kNV];
-    if (tid < kChainThreads) {   // S rows (key dims) of this column slice
-        const float* src =
-            p.h0 ? p.h0 + ((size_t)bh * kD + tid) * kD + j0 : nullptr;
-#pragma unroll
-        for (int j = 0; j < kNV; j += 4) {
-            const float4 v = src ? *reinterpret_cast<const float4*>(src + j)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-            S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
-        }
-        st_row(sm + kSS, tid, S);
-    }
-    tc::fence_proxy_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    // Without ready flags this is a programmatic dependent that reads the
-    // records once the pre-pass grid has completed (a no-op when launched
-    // normally); with them it reads each record once its flag is up, while
-    // the pre-pass may still be running.
-    if (!p.ready) asm volatile("griddepcontrol.wait;" ::: "memory");
-
     // Loads of chunk c into its stage (TMA tiles of K, Q, V and the record
     // of the pre-pass): the first kNS by thread 0 at the start, then chunk
     // c >= kNS by lane 0 of the helper group that prepares it, as soon as
@@ -833,12 +800,47 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
                       &bars[kBFull + c % kNS]);
         if (c + 2 * kNS < nchunks) prefetch(c + 2 * kNS);
     };
-    if (tid == 0 && !p.no_issue) {
-        tc::prefetch_tmap(&tm_q);
-        tc::prefetch_tmap(&tm_k);
-        tc::prefetch_tmap(&tm_v);
-        for (int c = 0; c < kNS && c < nchunks; ++c) {   // stage by stage
-            issue_tiles(c);
+    if (tid == 0) {
+        for (int i = 0; i < kNumBars; ++i) tc::mbar_init(&bars[i], 1);
+        *abort_flag = 0;
+        *issued = 0;
+        tc::fence_mbar_init();
+        if (!p.no_issue) {   // the first tiles: inputs, ready at launch
+            tc::prefetch_tmap(&tm_q);
+            tc::prefetch_tmap(&tm_k);
+            tc::prefetch_tmap(&tm_v);
+            for (int c = 0; c < kNS && c < nchunks; ++c) issue_tiles(c);
+        }
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    float S[kNV];
+    if (tid < kChainThreads) {   // S rows (key dims) of this column slice
+        const float* src =
+            p.h0 ? p.h0 + ((size_t)bh * kD + tid) * kD + j0 : nullptr;
+#pragma unroll
+        for (int j = 0; j < kNV; j += 4) {
+            const float4 v = src ? *reinterpret_cast<const float4*>(src + j)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
+        }
+        st_row(sm + kSS, tid, S);
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // Without ready flags this is a programmatic dependent that reads the
+    // records once the pre-pass grid has completed (a no-op when launched
+    // normally); with them it reads each record once its flag is up, while
+    // the pre-pass may still be running.
+    if (!p.ready) asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    if (tid == 0 && !p.no_issue) {   // the first records, once flagged
+        for (int c = 0; c < kNS && c < nchunks; ++c) {
             if (!await_record(c)) {
                 *vabort = 1;
                 break;

@@ -358,6 +358,31 @@ def test_tensor_core_path_against_oracle(T):
     check_fwd(inp, "tc")
 
 
+def test_two_kernel_forward_is_deterministic():
+    """The pre-pass hands chunk-heads out through a counter and picks its
+    reserved SMs by which TPCs register first, so the schedule differs from
+    call to call; every record is still computed by the same arithmetic, so
+    repeated calls give bit-identical o and hT (1B layer: the state pass
+    starts on the released SMs while the reserved ones finish)."""
+    d = to_dev(gen.prefill_inputs(gen.LAYER_1B))
+    outs = []
+    for _ in range(3):
+        o, hT = kla.chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"],
+                              d["eta"], d["eps"], d["h0"], C=64, algo="tc")
+        outs.append((o, hT))
+    torch.cuda.synchronize()
+    for o, hT in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(hT, outs[0][1])
+
+
+def test_two_kernel_forward_with_more_state_ctas_than_sms():
+    """B * H * 2 state-pass CTAs above the SM count: no SM is released, the
+    pre-pass runs to the end on every SM and the state pass reads the
+    records by their flags as its CTAs find room (B 8, H 16: 256 CTAs)."""
+    inp = gen.prefill_inputs(gen.LAYER_1B, B=8, T=200, H=16)
+    check_fwd(inp, "tc")
+
+
 def test_tensor_core_and_cuda_core_paths_agree():
     inp = gen.prefill_inputs(gen.LONG_CTX, B=1, T=640, H=2)
     o1, h1 = run_fwd(inp, "tc")

@@ -71,8 +71,10 @@ typedef enum {
     KLA_ALGO_AUTO = 0,   /* tensor-core path when eligible, else CUDA cores */
     KLA_ALGO_SIMT = 1,   /* fp32 CUDA-core chunkwise kernel (any supported shape) */
     KLA_ALGO_TC = 2,     /* tcgen05 tensor cores, two kernels: a chunk-parallel
-                            pre-pass and the sequential state pass (bf16,
-                            dk = dv = 128, C = 64; needs a workspace) */
+                            pre-pass and the sequential state pass, which
+                            starts on the SMs the pre-pass releases and reads
+                            each record once it is written (bf16, dk = dv =
+                            128, C = 64; needs a workspace) */
     KLA_ALGO_TC_FUSED = 3 /* tcgen05 tensor cores, one fused kernel per
                             (batch, head, dv half) (same shapes; no workspace) */
 } kla_algo;
@@ -204,9 +206,10 @@ KLA_API kla_status kla_chunk_fwd_seq_workspace_size(int B, int T, int H,
  * with B_s, O0_s from the segment run from a zero state and Phi_s, O_hom,s
  * from the run from the identity with V = 0.  Both runs are the two-kernel
  * tensor-core forward over the B P segments: one pre-pass (its records
- * depend on q, k and the gates only) serves the two state passes, which run
- * at the same time on `stream` and on a second stream of the library (with
- * B = 1 the second run skips segment 0, whose Phi and O_hom are not
+ * depend on q, k and the gates only) serves the two state passes, which
+ * follow it on `stream` as programmatic dependents, so that both run at
+ * once and beside the pre-pass, reading each record once it is written
+ * (with B = 1 the second run skips segment 0, whose Phi and O_hom are not
  * needed); a small kernel chains S_{s+1} =
  * Phi_s S_s + B_s and a tensor-core kernel adds O_hom,s S_s to o of every
  * segment after the first.  The pages have no counterpart: it reorders the

@@ -372,11 +372,12 @@ KLA_API kla_status kla_precond_keys(const void* k, const float* A0,
  * ([B, T, H, dk], dtype, read; e.g. from kla_precond_keys): the chunkwise
  * form with A = I + strict_lower(Diag(beta)(Gamma o K Kw^T)),
  * P = Gamma o Q Kw^T and the state written along Kw, the residual read along
- * K.  Runs on the tensor-core kernel (its write-key mode) where
- * kla_chunk_fwd_ex's KLA_ALGO_AUTO would (bf16, dk = dv = 128, C = 64,
- * 16-byte-aligned tensors, k_write included), else on the CUDA-core kernel.
- * k_write must not overlap o.  Errors as for kla_chunk_fwd_ex (NULL k_write is
- * KLA_ERR_INVALID_ARG).
+ * K.  Takes the path kla_chunk_fwd_ex's KLA_ALGO_AUTO would (for bf16,
+ * dk = dv = 128, C = 64 and 16-byte-aligned tensors, k_write included: the
+ * two-kernel tensor-core path, G = [K; Q] Kw^T in its pre-pass and
+ * Diag(Gamma_C) Kw in its state pass, with stream-ordered scratch for its
+ * records), else the CUDA-core kernel.  k_write must not overlap o.  Errors
+ * as for kla_chunk_fwd_ex (NULL k_write is KLA_ERR_INVALID_ARG).
  */
 KLA_API kla_status kla_chunk_fwd_kw(const void* q, const void* k,
                                     const void* k_write, const void* v,
@@ -385,6 +386,23 @@ KLA_API kla_status kla_chunk_fwd_kw(const void* q, const void* k,
                                     float* hT, int B, int T, int H, int dk,
                                     int dv, int C, kla_dtype dtype,
                                     kla_step_rule rule, kla_stream_t stream);
+
+/*
+ * kla_chunk_fwd_kw_ex -- kla_chunk_fwd_kw with an explicit path, as
+ * kla_chunk_fwd_ex's `algo`: KLA_ALGO_TC the two-kernel path, KLA_ALGO_TC_FUSED
+ * the fused tensor-core kernel's write-key mode, KLA_ALGO_SIMT the CUDA-core
+ * kernel.  Errors as for kla_chunk_fwd_kw, plus KLA_ERR_UNSUPPORTED_SHAPE
+ * when a tensor-core path is asked for a shape it does not take.
+ */
+KLA_API kla_status kla_chunk_fwd_kw_ex(const void* q, const void* k,
+                                       const void* k_write, const void* v,
+                                       const float* log_alpha,
+                                       const float* eta, float eps,
+                                       const float* h0, void* o, float* hT,
+                                       int B, int T, int H, int dk, int dv,
+                                       int C, kla_dtype dtype, kla_algo algo,
+                                       kla_step_rule rule,
+                                       kla_stream_t stream);
 
 /*
  * kla_decode_step_kw -- kla_decode_step_ex with a separate write key

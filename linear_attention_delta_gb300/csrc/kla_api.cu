@@ -225,10 +225,24 @@ extern "C" kla_status kla_chunk_fwd_kw(const void* q, const void* k,
                                        int C, kla_dtype dtype,
                                        kla_step_rule rule,
                                        kla_stream_t stream) {
+    return kla_chunk_fwd_kw_ex(q, k, k_write, v, log_alpha, eta, eps, h0, o,
+                               hT, B, T, H, dk, dv, C, dtype, KLA_ALGO_AUTO,
+                               rule, stream);
+}
+
+extern "C" kla_status kla_chunk_fwd_kw_ex(const void* q, const void* k,
+                                          const void* k_write, const void* v,
+                                          const float* log_alpha,
+                                          const float* eta, float eps,
+                                          const float* h0, void* o, float* hT,
+                                          int B, int T, int H, int dk, int dv,
+                                          int C, kla_dtype dtype,
+                                          kla_algo algo, kla_step_rule rule,
+                                          kla_stream_t stream) {
     if (!k_write && (long long)B * H > 0 && T > 0) return KLA_ERR_INVALID_ARG;
     return chunk_fwd_impl(q, k, k_write, v, log_alpha, eta, eps, h0, o, hT, B,
-                          T, H, dk, dv, C, dtype, KLA_ALGO_AUTO, rule, nullptr,
-                          0, stream);
+                          T, H, dk, dv, C, dtype, algo, rule, nullptr, 0,
+                          stream);
 }
 
 extern "C" kla_status kla_precond_keys(const void* k, const float* A0,

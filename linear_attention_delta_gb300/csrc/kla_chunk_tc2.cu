@@ -109,16 +109,26 @@ constexpr int kPKQ = 0;          // K_0 | Q_0 | K_1 | Q_1 (TMA), 32 KB; after G
 constexpr int kPL = kRecBytes;   // L (strictly lower part of A), packed, and
 constexpr int kPY = kPL + kPackBytes;   // 4 warps x 16 x 8 fp32 scratch
 constexpr int kPT = 32768;       // T below its diagonal blocks, packed
-constexpr int kPG = kPT + 6 * kBlk * 4;      // g2[64]
-constexpr int kPBeta = kPG + 256;            // beta[64]
-constexpr int kPE = kPBeta + 256;            // column factors e_i[64]
-constexpr int kPBars = kPE + 256;            // 3 mbarriers
-constexpr int kPMisc = kPBars + 24;          // TMEM slot, warp total, flag
-constexpr int kPSmem = kPMisc + 16 + 1024;
+constexpr int kPKW = 32768;      // write keys Kw_0 | Kw_1 (TMA, write-key
+                                 // mode), read by G only: T goes over them
+// the rest of the map, after T (or after the write keys)
+template <bool kKw>
+struct PrepMap {
+    static constexpr int G = kKw ? kPKW + 16384 : kPT + 6 * kBlk * 4;  // g2
+    static constexpr int Beta = G + 256;          // beta[64]
+    static constexpr int E = Beta + 256;          // column factors e_i[64]
+    static constexpr int Bars = E + 256;          // 3 mbarriers
+    static constexpr int Misc = Bars + 24;        // TMEM slot, words
+    static constexpr int Smem = Misc + 32 + 1024;
+    static constexpr int PerSm = kKw ? 4 : 5;     // CTAs resident per SM
+};
 static_assert(kPY + 4 * 16 * 8 * 4 <= kPT, "pre-pass map");
 static_assert(kPL % 16 == 0 && kPT % 16 == 0, "float4 rows");
-// five CTAs per SM (the driver keeps 1 KB of each CTA's shared memory)
-static_assert(5 * (kPSmem + 1024) <= 233472, "pre-pass shared memory");
+static_assert(kPT + 6 * kBlk * 4 <= PrepMap<true>::G, "T within the keys");
+// five (four with write keys) CTAs per SM (the driver keeps 1 KB of each
+// CTA's shared memory)
+static_assert(5 * (PrepMap<false>::Smem + 1024) <= 233472, "pre-pass smem");
+static_assert(4 * (PrepMap<true>::Smem + 1024) <= 233472, "pre-pass smem");
 
 // Work distribution of the pre-pass.  Its grid is persistent (as many CTAs
 // as fit at once); each CTA takes chunk-heads from a counter in chunk-major
@@ -210,22 +220,27 @@ __device__ void offdiag_slab(float* L, float* T, float* Y, int I, int J,
     dst[(g + 8) * kBs + 2 * t + 1] = -d[3];
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 5)
+// kKw: separate write keys (tm_kw): G = [K; Q] Kw^T, so that beta's
+// denominator is k . kw, A uses K Kw^T and P uses Q Kw^T.
+template <bool kKw>
+__global__ void __launch_bounds__(kPrepThreads, PrepMap<kKw>::PerSm)
 kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
-                const __grid_constant__ CUtensorMap tm_k, PrepParams p) {
+                const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_kw, PrepParams p) {
+    using PM = PrepMap<kKw>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = tc::smem_u32(sm);
     float* Lt = reinterpret_cast<float*>(sm + kPL);
     float* Tt = reinterpret_cast<float*>(sm + kPT);
-    float* g2s = reinterpret_cast<float*>(sm + kPG);
-    float* betas = reinterpret_cast<float*>(sm + kPBeta);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPBars);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kPMisc);
-    float* wtot = reinterpret_cast<float*>(sm + kPMisc + 4);
-    int* failed_flag = reinterpret_cast<int*>(sm + kPMisc + 8);
-    int* item_slot = reinterpret_cast<int*>(sm + kPMisc + 12);
+    float* g2s = reinterpret_cast<float*>(sm + PM::G);
+    float* betas = reinterpret_cast<float*>(sm + PM::Beta);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PM::Bars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PM::Misc);
+    float* wtot = reinterpret_cast<float*>(sm + PM::Misc + 4);
+    int* failed_flag = reinterpret_cast<int*>(sm + PM::Misc + 8);
+    int* item_slot = reinterpret_cast<int*>(sm + PM::Misc + 12);
     uint8_t* out = sm + kPKQ;   // record image, over the consumed K / Q
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -262,6 +277,7 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (tid == 0) {
         tc::prefetch_tmap(&tm_q);
         tc::prefetch_tmap(&tm_k);
+        if constexpr (kKw) tc::prefetch_tmap(&tm_kw);
         for (int i = 0; i < 3; ++i) tc::mbar_init(&bars[i], 1);
         *failed_flag = 0;
         tc::fence_mbar_init();
@@ -304,11 +320,15 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (item >= 0) {
                 const int cc = item / nbh, bb = item % nbh;
                 const int hh = bb % p.H, b0 = bb / p.H;
-                tc::mbar_arrive_expect_tx(&bars[0], 32768);
+                tc::mbar_arrive_expect_tx(&bars[0], kKw ? 32768 + 16384 : 32768);
                 tc::tma_load_4d(sm + kPKQ, &tm_k, &bars[0], 0, hh, cc * kC, b0);
                 tc::tma_load_4d(sm + kPKQ + 8192, &tm_q, &bars[0], 0, hh, cc * kC, b0);
                 tc::tma_load_4d(sm + kPKQ + 16384, &tm_k, &bars[0], 64, hh, cc * kC, b0);
                 tc::tma_load_4d(sm + kPKQ + 24576, &tm_q, &bars[0], 64, hh, cc * kC, b0);
+                if constexpr (kKw) {
+                    tc::tma_load_4d(sm + kPKW, &tm_kw, &bars[0], 0, hh, cc * kC, b0);
+                    tc::tma_load_4d(sm + kPKW + 8192, &tm_kw, &bars[0], 64, hh, cc * kC, b0);
+                }
             } else if (pending >= 0) {
                 publish(pending);
                 pending = -1;
@@ -347,7 +367,7 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
         // i's 16-column tile and e_i = 2^(g_m - g_i) <= 1: one ex2 per row and
         // tile instead of one per element (a tile whose g spans more than 2^96
         // takes the direct form, so that neither factor can overflow)
-        float* ecol = reinterpret_cast<float*>(sm + kPE);
+        float* ecol = reinterpret_cast<float*>(sm + PM::E);
         if (tid < kC)
             ecol[tid] = tc::ex2(__shfl_sync(0xffffffffu, g2, (lane & 16) | 15) -
                                 g2);
@@ -360,9 +380,14 @@ kla_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
                 constexpr uint32_t idG = tc::idesc_bf16(128, 64, false, false);
     #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
+                    // A: [K; Q]; B: the keys' rows of the same tiles, or the
+                    // write keys
                     const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                    const uint32_t offw =
+                        kKw ? kPKW + (ks >> 2) * 8192 + (ks & 3) * 32
+                            : kPKQ + off;
                     tc::mma_bf16(tmem, desc_k(sbase + kPKQ + off),
-                                 desc_k(sbase + kPKQ + off), idG, ks > 0);
+                                 desc_k(sbase + offw), idG, ks > 0);
                 }
                 tc::mma_commit(&bars[1]);
                 if (pending >= 0) {   // the previous item's record (long done)
@@ -667,6 +692,7 @@ struct StateParams {
     int no_issue;         // self-test: the producer issues nothing
     const unsigned int* ready;   // record flags of a running pre-pass, or
                                  // null (the records are in memory)
+    const __nv_bfloat16* kw;     // write keys [B, T, H, 128] (write-key mode)
 };
 
 // Write 64 fp32 values as one 128-byte swizzled bf16 row.
@@ -717,7 +743,9 @@ __device__ __forceinline__ uint4 scale8(uint4 u, __nv_bfloat162 s) {
     return r;
 }
 
-template <bool kCkpt>
+// kKw: separate write keys: the state takes Kw^T Diag(Gamma_C) U~ (the
+// residual and W keep the keys).
+template <bool kCkpt, bool kKw>
 __global__ void __launch_bounds__(kStateThreads, 1)
 kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_k,
@@ -913,7 +941,23 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const int cj = ((j + r) & 7) << 4;
                     const uint4 u = *reinterpret_cast<const uint4*>(krow + cj);
                     *reinterpret_cast<uint4*>(krow + cj) = scale8(u, gam);
-                    kG[j] = scale8(u, gamC);
+                    if constexpr (!kKw) kG[j] = scale8(u, gamC);
+                }
+                if constexpr (kKw) {
+                    // this row's write keys straight from global memory (in
+                    // flight during the MMAs below), 16-byte piece
+                    // ((j + r) mod 8) xor (r mod 8) at step j, so that it
+                    // lands where the swizzled tile keeps it
+                    const int t = c * kC + r;
+                    const __nv_bfloat16* kwrow =
+                        p.kw + (((size_t)b * p.T + (t < p.T ? t : 0)) * p.H +
+                                h) * kD + hh * 64;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        kG[j] = t < p.T
+                                    ? __ldg(reinterpret_cast<const uint4*>(
+                                          kwrow + 8 * (((j + r) & 7) ^ (r & 7))))
+                                    : make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             tc::fence_proxy_async_smem();
@@ -945,12 +989,13 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
                 break;
             }
             tc::tc_fence_after();
-            {   // Diag(Gamma_C) K over [TU; PTU] (read by the finished MMAs)
+            {   // Diag(Gamma_C) K (or Kw) over [TU; PTU] (read by the
+                // finished MMAs)
                 uint8_t* grow = st + kSTU + hh * 8192 + r * 128;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     *reinterpret_cast<uint4*>(grow + (((j + r) & 7) << 4)) =
-                        kG[j];
+                        kKw ? scale8(kG[j], gamC) : kG[j];
             }
             if (hl < kC) {
                 // -W row hl over Kg (both halves; read by the finished MMA)
@@ -1177,7 +1222,7 @@ cudaError_t set_smem(const void* kern, int bytes, std::atomic<unsigned long long
     return e;
 }
 
-std::atomic<unsigned long long> g_prep_attr{0}, g_state_attr[2];
+std::atomic<unsigned long long> g_prep_attr[2], g_state_attr[3];
 
 }  // namespace
 
@@ -1200,7 +1245,8 @@ size_t chunk_tc2_workspace_bytes(int B, int T, int H) {
 
 bool chunk_tc2_eligible(const FwdArgs& a) {
     return a.dtype == KLA_BF16 && a.dk == kD && a.dv == kD && a.C == kC &&
-           !a.kw && aligned16(a.q) && aligned16(a.k) && aligned16(a.v) &&
+           (!a.kw || (aligned16(a.kw) && !a.ckpt)) && aligned16(a.q) &&
+           aligned16(a.k) && aligned16(a.v) &&
            (!a.o || aligned16(a.o)) && (!a.h0 || aligned16(a.h0)) &&
            (!a.hT || aligned16(a.hT)) && get_encoder();
 }
@@ -1232,6 +1278,8 @@ struct DeviceShape {
     int sms = 0, prep_per_sm = 0;
 };
 
+// SM count and resident pre-pass CTAs per SM of instantiation kKw.
+template <bool kKw>
 cudaError_t device_shape(DeviceShape* d) {
     static std::atomic<unsigned long long> cached[64];
     int dev = 0;
@@ -1247,19 +1295,20 @@ cudaError_t device_shape(DeviceShape* d) {
     }
     e = cudaDeviceGetAttribute(&d->sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    // CTAs of the pre-pass resident per SM: five by construction (launch
-    // bounds, shared memory, TMEM), fewer if this device's shared memory or
-    // register file holds fewer
+    // CTAs of the pre-pass resident per SM: five (four with write keys) by
+    // construction (launch bounds, shared memory, TMEM), fewer if this
+    // device's shared memory or register file holds fewer
     int smem_sm = 0;
     e = cudaDeviceGetAttribute(&smem_sm,
                                cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kla_prep_kernel);
+    e = cudaFuncGetAttributes(&fa, kla_prep_kernel<kKw>);
     if (e != cudaSuccess) return e;
-    const int by_smem = smem_sm / (kPSmem + 1024);
+    const int by_smem = smem_sm / (PrepMap<kKw>::Smem + 1024);
     const int by_regs = 65536 / (std::max(fa.numRegs, 1) * kPrepThreads);
-    d->prep_per_sm = std::min(5, std::min(by_smem, by_regs));
+    d->prep_per_sm =
+        std::min(PrepMap<kKw>::PerSm, std::min(by_smem, by_regs));
     if (d->sms <= 0 || d->prep_per_sm <= 0) return cudaErrorInvalidValue;
     if (dev < 64)
         cached[dev].store(((unsigned long long)d->sms << 32) |
@@ -1274,17 +1323,25 @@ cudaError_t launch_prep_tc2(const FwdArgs& a, void* ws, cudaStream_t stream,
     if ((long)a.B * a.H == 0 || a.T == 0) return cudaSuccess;
     if (!get_encoder()) return cudaErrorNotSupported;
     if (!ws || !aligned16(ws)) return cudaErrorInvalidValue;
-    CUtensorMap mq, mk;
-    if (!make_map(&mq, a.q, a.B, a.T, a.H) || !make_map(&mk, a.k, a.B, a.T, a.H))
+    CUtensorMap mq, mk, mkw;
+    if (!make_map(&mq, a.q, a.B, a.T, a.H) ||
+        !make_map(&mk, a.k, a.B, a.T, a.H) ||
+        !make_map(&mkw, a.kw ? a.kw : a.k, a.B, a.T, a.H))
         return cudaErrorInvalidValue;
+    if (a.kw && a.bwd_rec) return cudaErrorInvalidValue;   // forward only
     const int nchunks = (a.T + kC - 1) / kC;
     const long nbh = (long)a.B * a.H;
     const long items = nbh * nchunks;
     if (items > 0x7fffffffL) return cudaErrorInvalidValue;
-    cudaError_t e = set_smem((const void*)kla_prep_kernel, kPSmem, g_prep_attr);
+    const bool kw = a.kw != nullptr;
+    const void* kern = kw ? (const void*)kla_prep_kernel<true>
+                          : (const void*)kla_prep_kernel<false>;
+    cudaError_t e = set_smem(
+        kern, kw ? PrepMap<true>::Smem : PrepMap<false>::Smem,
+        g_prep_attr[kw ? 1 : 0]);
     if (e != cudaSuccess) return e;
     DeviceShape d;
-    e = device_shape(&d);
+    e = kw ? device_shape<true>(&d) : device_shape<false>(&d);
     if (e != cudaSuccess) return e;
     uint8_t* rec = static_cast<uint8_t*>(ws);
     unsigned int* ready = reinterpret_cast<unsigned int*>(
@@ -1306,8 +1363,13 @@ cudaError_t launch_prep_tc2(const FwdArgs& a, void* ws, cudaStream_t stream,
     PrepParams pp{a.log_alpha, a.eta, rec, a.eps, a.gdn, a.T, a.H, nchunks,
                   a.bwd_rec, ready, ctrl, (int)items, (int)release,
                   reserved};
-    kla_prep_kernel<<<(unsigned)grid, kPrepThreads, kPSmem, stream>>>(mq, mk,
-                                                                     pp);
+    if (kw)
+        kla_prep_kernel<true><<<(unsigned)grid, kPrepThreads,
+                                PrepMap<true>::Smem, stream>>>(mq, mk, mkw, pp);
+    else
+        kla_prep_kernel<false><<<(unsigned)grid, kPrepThreads,
+                                 PrepMap<false>::Smem, stream>>>(mq, mk, mkw,
+                                                                 pp);
     return cudaGetLastError();
 }
 
@@ -1329,14 +1391,18 @@ cudaError_t launch_state_tc2(const FwdArgs& a, const void* rec,
         !make_map(&mk, a.k, a.B, a.T, a.H) || !make_v_map(&mv, a) ||
         !make_map(&mo, a.o ? a.o : a.q, a.B, a.T, a.H))
         return cudaErrorInvalidValue;
+    if (a.kw && a.ckpt) return cudaErrorInvalidValue;   // forward only
     const int nchunks = (a.T + kC - 1) / kC;
-    auto kern = a.ckpt ? kla_state_kernel<true> : kla_state_kernel<false>;
-    cudaError_t e =
-        set_smem((const void*)kern, kSSmem, g_state_attr[a.ckpt ? 1 : 0]);
+    const int which = a.ckpt ? 1 : a.kw ? 2 : 0;
+    auto kern = which == 1   ? kla_state_kernel<true, false>
+                : which == 2 ? kla_state_kernel<false, true>
+                             : kla_state_kernel<false, false>;
+    cudaError_t e = set_smem((const void*)kern, kSSmem, g_state_attr[which]);
     if (e != cudaSuccess) return e;
     StateParams sp{a.h0, static_cast<__nv_bfloat16*>(a.o), a.hT, a.ckpt,
                    static_cast<const uint8_t*>(rec), a.T, a.H, nchunks,
-                   2000000000ull, 0, ready};
+                   2000000000ull, 0, ready,
+                   static_cast<const __nv_bfloat16*>(a.kw)};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((long)a.B * a.H), kD / kNV);
     cfg.blockDim = dim3(kStateThreads);
@@ -1373,13 +1439,15 @@ cudaError_t launch_state_selftest(cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     CUtensorMap m;
     if (!make_map(&m, base, 1, kC, 1)) return cudaErrorInvalidValue;
-    e = set_smem((const void*)kla_state_kernel<false>, kSSmem, g_state_attr[0]);
+    e = set_smem((const void*)kla_state_kernel<false, false>, kSSmem,
+                 g_state_attr[0]);
     if (e != cudaSuccess) return e;
     // one CTA, one chunk; its waits give up after 1 ms
     StateParams sp{nullptr, static_cast<__nv_bfloat16*>(base), nullptr,
                    nullptr, static_cast<const uint8_t*>(base), kC, 1, 1,
-                   1000000ull, 1, nullptr};
-    kla_state_kernel<false><<<dim3(1, 1), kStateThreads, kSSmem, stream>>>(
+                   1000000ull, 1, nullptr, nullptr};
+    kla_state_kernel<false, false><<<dim3(1, 1), kStateThreads, kSSmem,
+                                     stream>>>(
         m, m, m, m, sp);
     return cudaGetLastError();
 }

@@ -54,6 +54,9 @@ SIGNATURES = {
                               _I, _VP]),
     "kla_chunk_fwd_kw": (_I, [_VP, _VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
                               _FP, _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
+    "kla_chunk_fwd_kw_ex": (_I, [_VP, _VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
+                                 _FP, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                                 _VP]),
     "kla_decode_step_kw": (_I, [_VP, _VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
                                 _I, _I, _I, _I, _I, _I, _VP]),
     "kla_chunk_fwd_seq_workspace_size": (
@@ -456,8 +459,8 @@ def precond_keys(k, A0=None, x: float = 1.5, delta: float = 1e-6,
 
 def chunk_fwd_kw(q, k, k_write, v, log_alpha, eta, eps: float = 1e-6,
                  h0=None, C: int = 64, o=None, hT=None, want_state=True,
-                 stream=None, rule: str = "kaczmarz"):
-    """Forward pass with separate write keys (``kla_chunk_fwd_kw``); see
+                 stream=None, rule: str = "kaczmarz", algo: str = "auto"):
+    """Forward pass with separate write keys (``kla_chunk_fwd_kw_ex``); see
     ``chunk_fwd`` for the other arguments."""
     for n, t in (("q", q), ("k", k), ("k_write", k_write), ("v", v)):
         _check_cuda(n, t, q.dtype)
@@ -471,12 +474,12 @@ def chunk_fwd_kw(q, k, k_write, v, log_alpha, eta, eps: float = 1e-6,
         o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     if hT is None and want_state:
         hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
-    st = load_library().kla_chunk_fwd_kw(
+    st = load_library().kla_chunk_fwd_kw_ex(
         _ptr(q), _ptr(k), _ptr(k_write), _ptr(v), _ptr(log_alpha), _ptr(eta),
         float(eps), _ptr(h0), _ptr(o), _ptr(hT), B, T, H, dk, dv, int(C),
-        DTYPES[q.dtype], RULES[rule], _stream(stream))
+        DTYPES[q.dtype], ALGOS[algo], RULES[rule], _stream(stream))
     if st != KLA_OK:
-        raise KlaError("kla_chunk_fwd_kw", st)
+        raise KlaError("kla_chunk_fwd_kw_ex", st)
     return o, hT
 
 

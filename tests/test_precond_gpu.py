@@ -94,16 +94,19 @@ def test_forward_fp32(rule, C, T):
     assert rel_err(o, o_ref) <= 1e-4 and rel_err(hT, h_ref) <= 1e-4
 
 
+@pytest.mark.parametrize("algo", ["tc", "tc_fused"])
 @pytest.mark.parametrize("rule", ["kaczmarz", "given"])
 @pytest.mark.parametrize("T", [50, 128, 400])
-def test_forward_bf16_d128(rule, T):
-    """bf16, dk = dv = 128, C = 64: the tensor-core kernel's write-key mode
-    (one chunk, whole chunks, a ragged tail)."""
+def test_forward_bf16_d128(rule, T, algo):
+    """bf16, dk = dv = 128, C = 64: the write-key modes of the two-kernel
+    path and of the fused tensor-core kernel (one chunk, whole chunks, a
+    ragged tail)."""
     inp = aniso(gen.prefill_inputs(gen.LAYER_1B, B=1, T=T, H=2), 4)
     d = dev(inp)
     kw, _ = kla.precond_keys(d["k"], x=X, delta=DELTA)
     o, hT = kla.chunk_fwd_kw(d["q"], d["k"], kw, d["v"], d["log_alpha"],
-                             d["eta"], d["eps"], d["h0"], C=64, rule=rule)
+                             d["eta"], d["eps"], d["h0"], C=64, rule=rule,
+                             algo=algo)
     torch.cuda.synchronize()
     o_ref, h_ref, _, _ = oracle.pkla_fwd(inp["q"], inp["k"], inp["v"],
                                          inp["log_alpha"], inp["eta"],
@@ -143,17 +146,18 @@ def test_prefill_then_decode_handoff():
     assert rel_err(A, A_ref) <= 1e-5
 
 
-def test_write_keys_equal_to_keys_give_the_plain_forward():
-    """With k_write = k the write-key mode of the fused tensor-core kernel
-    computes exactly what its plain mode does (same operands, same order):
-    bit-identical o and state."""
+@pytest.mark.parametrize("algo", ["tc", "tc_fused"])
+def test_write_keys_equal_to_keys_give_the_plain_forward(algo):
+    """With k_write = k the write-key mode of each tensor-core path computes
+    exactly what its plain mode does (same operands, same order): o and the
+    state are bit-identical."""
     inp = gen.prefill_inputs(gen.LAYER_1B, B=2, T=300, H=3)
     d = dev(inp)
     o1, h1 = kla.chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["eta"],
-                           d["eps"], d["h0"], C=64, algo="tc_fused")
+                           d["eps"], d["h0"], C=64, algo=algo)
     o2, h2 = kla.chunk_fwd_kw(d["q"], d["k"], d["k"], d["v"],
                               d["log_alpha"], d["eta"], d["eps"], d["h0"],
-                              C=64)
+                              C=64, algo=algo)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(h1, h2)
 

@@ -421,9 +421,9 @@ def bench_backward(w, inp, steps, warmup, world):
 
 def bench_precond(w, inp, steps, warmup, world):
     """The diagonal-preconditioned variant on the forward's inputs: the
-    write-key scan plus the two-key forward (the tensor-core kernel's
-    write-key mode for bf16 d128 C64, else the CUDA-core kernel), beside the
-    plain forward on the same path."""
+    write-key scan plus the two-key forward (the two-kernel tensor-core
+    path's write-key instantiations for bf16 d128 C64, else the CUDA-core
+    kernel), beside the plain forward on the same path."""
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
          for k, v in inp.items()}
     o = torch.empty_like(d["v"])

@@ -389,10 +389,15 @@ KLA_API kla_status kla_chunk_fwd_kw(const void* q, const void* k,
 
 /*
  * kla_chunk_fwd_kw_ex -- kla_chunk_fwd_kw with an explicit path, as
- * kla_chunk_fwd_ex's `algo`: KLA_ALGO_TC the two-kernel path, KLA_ALGO_TC_FUSED
- * the fused tensor-core kernel's write-key mode, KLA_ALGO_SIMT the CUDA-core
- * kernel.  Errors as for kla_chunk_fwd_kw, plus KLA_ERR_UNSUPPORTED_SHAPE
- * when a tensor-core path is asked for a shape it does not take.
+ * kla_chunk_fwd_ex's `algo` (KLA_ALGO_TC the two-kernel path,
+ * KLA_ALGO_TC_FUSED the fused tensor-core kernel's write-key mode,
+ * KLA_ALGO_SIMT the CUDA-core kernel), and an optional workspace as
+ * kla_chunk_fwd_ws's (kla_chunk_fwd_workspace_size(...) bytes for `algo`,
+ * 16-byte aligned, overlapping no argument k_write included; NULL: the
+ * library takes stream-ordered scratch when the path needs a workspace).
+ * Errors as for kla_chunk_fwd_kw, plus KLA_ERR_UNSUPPORTED_SHAPE when a
+ * tensor-core path is asked for a shape it does not take and
+ * KLA_ERR_INVALID_ARG for a small, misaligned or overlapping workspace.
  */
 KLA_API kla_status kla_chunk_fwd_kw_ex(const void* q, const void* k,
                                        const void* k_write, const void* v,
@@ -401,7 +406,8 @@ KLA_API kla_status kla_chunk_fwd_kw_ex(const void* q, const void* k,
                                        const float* h0, void* o, float* hT,
                                        int B, int T, int H, int dk, int dv,
                                        int C, kla_dtype dtype, kla_algo algo,
-                                       kla_step_rule rule,
+                                       kla_step_rule rule, void* workspace,
+                                       size_t workspace_bytes,
                                        kla_stream_t stream);
 
 /*

@@ -147,7 +147,8 @@ static kla_status chunk_fwd_impl(const void* q, const void* k, const void* kw,
                                  {log_alpha, (size_t)B * T * H * 4},
                                  {eta, (size_t)B * T * H * 4},
                                  {h0, sizeof(float) * B * H * dk * dv},
-                                 {hT, sizeof(float) * B * H * dk * dv}};
+                                 {hT, sizeof(float) * B * H * dk * dv},
+                                 {kw, (size_t)B * T * H * dk * 2}};
             const Span ws[] = {{workspace, need}};
             if (any_overlap(bufs, ws)) return KLA_ERR_INVALID_ARG;
             return from_cuda(kla::launch_chunk_tc2(a, workspace, s));
@@ -227,7 +228,7 @@ extern "C" kla_status kla_chunk_fwd_kw(const void* q, const void* k,
                                        kla_stream_t stream) {
     return kla_chunk_fwd_kw_ex(q, k, k_write, v, log_alpha, eta, eps, h0, o,
                                hT, B, T, H, dk, dv, C, dtype, KLA_ALGO_AUTO,
-                               rule, stream);
+                               rule, nullptr, 0, stream);
 }
 
 extern "C" kla_status kla_chunk_fwd_kw_ex(const void* q, const void* k,
@@ -238,11 +239,13 @@ extern "C" kla_status kla_chunk_fwd_kw_ex(const void* q, const void* k,
                                           int B, int T, int H, int dk, int dv,
                                           int C, kla_dtype dtype,
                                           kla_algo algo, kla_step_rule rule,
+                                          void* workspace,
+                                          size_t workspace_bytes,
                                           kla_stream_t stream) {
     if (!k_write && (long long)B * H > 0 && T > 0) return KLA_ERR_INVALID_ARG;
     return chunk_fwd_impl(q, k, k_write, v, log_alpha, eta, eps, h0, o, hT, B,
-                          T, H, dk, dv, C, dtype, algo, rule, nullptr, 0,
-                          stream);
+                          T, H, dk, dv, C, dtype, algo, rule, workspace,
+                          workspace_bytes, stream);
 }
 
 extern "C" kla_status kla_precond_keys(const void* k, const float* A0,

@@ -56,7 +56,7 @@ SIGNATURES = {
                               _FP, _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
     "kla_chunk_fwd_kw_ex": (_I, [_VP, _VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
                                  _FP, _I, _I, _I, _I, _I, _I, _I, _I, _I,
-                                 _VP]),
+                                 _VP, ctypes.c_size_t, _VP]),
     "kla_decode_step_kw": (_I, [_VP, _VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
                                 _I, _I, _I, _I, _I, _I, _VP]),
     "kla_chunk_fwd_seq_workspace_size": (
@@ -459,9 +459,11 @@ def precond_keys(k, A0=None, x: float = 1.5, delta: float = 1e-6,
 
 def chunk_fwd_kw(q, k, k_write, v, log_alpha, eta, eps: float = 1e-6,
                  h0=None, C: int = 64, o=None, hT=None, want_state=True,
-                 stream=None, rule: str = "kaczmarz", algo: str = "auto"):
+                 stream=None, rule: str = "kaczmarz", algo: str = "auto",
+                 workspace=None):
     """Forward pass with separate write keys (``kla_chunk_fwd_kw_ex``); see
-    ``chunk_fwd`` for the other arguments."""
+    ``chunk_fwd`` for the other arguments (``workspace`` as there: allocated
+    here, by torch, when the path needs one and none is given)."""
     for n, t in (("q", q), ("k", k), ("k_write", k_write), ("v", v)):
         _check_cuda(n, t, q.dtype)
     _check_cuda("log_alpha", log_alpha, torch.float32)
@@ -474,10 +476,16 @@ def chunk_fwd_kw(q, k, k_write, v, log_alpha, eta, eps: float = 1e-6,
         o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     if hT is None and want_state:
         hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    need = chunk_fwd_workspace_size(B, T, H, dk, dv, C, q.dtype, algo)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is not None:
+        _check_cuda("workspace", workspace, torch.uint8)
     st = load_library().kla_chunk_fwd_kw_ex(
         _ptr(q), _ptr(k), _ptr(k_write), _ptr(v), _ptr(log_alpha), _ptr(eta),
         float(eps), _ptr(h0), _ptr(o), _ptr(hT), B, T, H, dk, dv, int(C),
-        DTYPES[q.dtype], ALGOS[algo], RULES[rule], _stream(stream))
+        DTYPES[q.dtype], ALGOS[algo], RULES[rule], _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _stream(stream))
     if st != KLA_OK:
         raise KlaError("kla_chunk_fwd_kw_ex", st)
     return o, hT

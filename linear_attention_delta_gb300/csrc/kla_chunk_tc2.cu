@@ -997,27 +997,47 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
                     *reinterpret_cast<uint4*>(grow + (((j + r) & 7) << 4)) =
                         kKw ? scale8(kG[j], gamC) : kG[j];
             }
+            // the four 32-column blocks of this row, handed to put(q4, x):
+            // block q + 1 comes in from TMEM while block q is written out
+            // (in the write-key instantiation one at a time: its register
+            // budget has no room for the second block)
+            auto four_blocks = [&](auto&& put) {
+                if constexpr (kKw) {
+#pragma unroll 1
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        float x[32];
+                        tc::tmem_ld32(tl + colH + 32 * q4, x);
+                        tc::tmem_ld_wait();
+                        put(q4, x);
+                    }
+                } else {
+                    float xa[32], xb[32];
+                    tc::tmem_ld32(tl + colH, xa);
+                    tc::tmem_ld_wait();
+                    tc::tmem_ld32(tl + colH + 32, xb);
+                    put(0, xa);
+                    tc::tmem_ld_wait();
+                    tc::tmem_ld32(tl + colH + 64, xa);
+                    put(1, xb);
+                    tc::tmem_ld_wait();
+                    tc::tmem_ld32(tl + colH + 96, xb);
+                    put(2, xa);
+                    tc::tmem_ld_wait();
+                    put(3, xb);
+                }
+            };
             if (hl < kC) {
                 // -W row hl over Kg (both halves; read by the finished MMA)
-#pragma unroll 1
-                for (int q4 = 0; q4 < 4; ++q4) {   // 32 columns at a time
-                    float x[32];
-                    tc::tmem_ld32(tl + colH + 32 * q4, x);
-                    tc::tmem_ld_wait();
-                    st_half_row(st + ((q4 >> 1) ? kSK1 : kSK0), hl, q4 & 1,
-                                x);
-                }
+                four_blocks([&](int q4, const float* x) {
+                    st_half_row(st + ((q4 >> 1) ? kSK1 : kSK0), hl, q4 & 1, x);
+                });
             } else {
                 // Q' row = gamma_r Q_r + (-PTU Kg)_r over Q (in place; packed
                 // bf16 fma, the TMEM values rounded to bf16 first)
                 const int rq = hl - kC;
                 const __nv_bfloat162 gq =
                     __float2bfloat162_rn(tc::ex2(g2[rq]));
-#pragma unroll 1
-                for (int q4 = 0; q4 < 4; ++q4) {   // 32 columns at a time
-                    float x[32];
-                    tc::tmem_ld32(tl + colH + 32 * q4, x);
-                    tc::tmem_ld_wait();
+                four_blocks([&](int q4, const float* x) {
                     uint8_t* qrow = st + ((q4 >> 1) ? kSQ1 : kSQ0) + rq * 128;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -1035,7 +1055,7 @@ kla_state_kernel(const __grid_constant__ CUtensorMap tm_q,
                             tc::pack_bf16x2(xj[6], xj[7]))));
                         *pq = u;
                     }
-                }
+                });
             }
             tc::fence_proxy_async_smem();
             tc::tc_fence_before();

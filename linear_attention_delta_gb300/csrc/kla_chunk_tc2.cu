@@ -17,13 +17,22 @@
 // Only the last three lines involve the state; everything else depends on
 // the chunk's own inputs.
 //
-// Pre-pass (kla_prep_kernel): one CTA per chunk-head, all in parallel.  G =
-// [K; Q] K^T on the tensor cores (tcgen05, TMEM accumulator); beta from its
-// diagonal; A in fp32 and P in bf16; T = A^{-1} by blocks (fp32
-// substitution on the 16x16 diagonal blocks, tf32 warp-level MMAs for the
-// rest); PTU = P TU on the tensor cores; TU and PTU written to global
-// memory (one bulk copy) as the exact shared-memory image of a 128-row
-// K-major bf16 tensor-core operand [TU; PTU], followed by g.
+// Pre-pass (kla_prep_kernel): a persistent grid whose CTAs take
+// chunk-heads in chunk-major order, all independent.  G = [K; Q] K^T on the
+// tensor cores (tcgen05, TMEM accumulator); beta from its diagonal; A in
+// fp32 and P in bf16; T = A^{-1} by blocks (fp32 substitution on the 16x16
+// diagonal blocks, tf32 warp-level MMAs for the rest); PTU = P TU on the
+// tensor cores; TU and PTU written to global memory (one bulk copy) as the
+// exact shared-memory image of a 128-row K-major bf16 tensor-core operand
+// [TU; PTU], followed by g, and the record's ready flag raised.  Past a
+// release point only the CTAs of a few reserved TPCs keep working, so that
+// the state pass, launched as a programmatic dependent, runs on the other
+// SMs beside the pre-pass's last chunks and reads each record once its flag
+// is up.
+//
+// With separate write keys Kw (the preconditioned variant) G = [K; Q] Kw^T
+// (so beta's denominator is k . kw, A uses K Kw^T and P uses Q Kw^T) and the
+// state takes Kw^T Diag(Gamma_C) U~; W, Q' and the residual keep K.
 //
 // State pass (kla_state_kernel): one CTA per (batch, head, 64 columns of
 // dv), walking the chunks in order.  Two helper warpgroups prepare the next

@@ -8,7 +8,9 @@
 // from the identity with V = 0 (then S_t = Phi_t and o_t = Phi_t^T q_t).
 // Both runs are the forward kernel itself, with the P segments of every
 // sequence taken as P sequences of one batch ([B, T, H, d] is
-// [B P, T / P, H, d]); they run at the same time on two streams.  A small
+// [B P, T / P, H, d]); on the two-kernel path they share one pre-pass and
+// run at the same time as programmatic dependents on the caller's stream
+// (on the fused kernel, on two streams).  A small
 // kernel then chains the start states, S_{s+1} = Phi_s S_s + B_s, and a
 // tensor-core kernel adds O_hom,s S_s to the outputs of every segment after
 // the first (whose run started from the true initial state).  With one

@@ -363,6 +363,23 @@ def test_overlapping_buffers_are_refused_on_host(lib):
     assert st == INVALID
 
 
+def test_write_key_forward_checks_on_host(lib):
+    """kla_chunk_fwd_kw_ex refuses, before any device call, a missing
+    k_write, a k_write not aligned to its element type and an o that
+    overlaps k_write."""
+    V = ctypes.c_void_p
+    b = _bufs(12)
+    args = lambda kw, o: (V(b[0]), V(b[1]), kw, V(b[3]), V(b[4]), V(b[5]),
+                          1e-6, None, o, None, 1, 64, 1, 128, 128, 64, 1, 0,
+                          0, None, 0, None)
+    assert lib.kla_chunk_fwd_kw_ex(*args(None, V(b[6]))) == INVALID
+    assert lib.kla_chunk_fwd_kw_ex(*args(V(b[2] + 1), V(b[6]))) == INVALID
+    assert lib.kla_chunk_fwd_kw_ex(*args(V(b[2]), V(b[2] + 256))) == INVALID
+    assert lib.kla_chunk_fwd_kw(V(b[0]), V(b[1]), None, V(b[3]), V(b[4]),
+                                V(b[5]), 1e-6, None, V(b[6]), None, 1, 64, 1,
+                                128, 128, 64, 1, 0, None) == INVALID
+
+
 def test_forward_workspace_size_and_missing_workspace(lib):
     """The two-kernel tensor-core path needs a 16,640-byte record and a
     4-byte ready flag per (batch, head, 64-token chunk), the flags rounded up

@@ -345,10 +345,11 @@ def bench_prefill_e2e(w, inp, steps, warmup):
     return ms, h2d, d2h
 
 
-def bench_decode(w, steps, warmup, distinct=50):
+def bench_decode(w, steps, warmup, distinct=50, gpu_index=0):
     """`steps` consecutive decode steps over the full state; token inputs
     cycle through `distinct` independently drawn steps (the state itself
-    evolves through every step)."""
+    evolves through every step).  Returns ms per step and the SM clocks
+    sampled over the timed steps."""
     d = gen.decode_inputs(w, steps=distinct)
     dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
            for k, v in d.items()}
@@ -367,15 +368,16 @@ def bench_decode(w, steps, warmup, distinct=50):
     torch.cuda.synchronize()
     e0, e1 = (torch.cuda.Event(enable_timing=True),
               torch.cuda.Event(enable_timing=True))
-    e0.record(stream)
-    for i in range(steps):
-        step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    with ClockSampler(gpu_index) as clk:
+        e0.record(stream)
+        for i in range(steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     if kla.device_status() != 0:
         raise RuntimeError("device-side timeout in decode")
-    return ms / steps
+    return ms / steps, clk.summary()
 
 
 def bench_backward(w, inp, steps, warmup, world):
@@ -714,7 +716,7 @@ def run_only(args):
                           "ms_per_launch": round(pf["ms"], 5)}))
     else:
         w = gen.DECODE
-        ms = bench_decode(w, args.steps, args.warmup)
+        ms, _ = bench_decode(w, args.steps, args.warmup)
         print(json.dumps({"only": "decode", "workload": w.name,
                           "ms_per_launch": round(ms, 5)}))
 
@@ -773,10 +775,12 @@ def run_ours(args):
 
     if not args.no_decode:
         dw = gen.DECODE
-        dms = bench_decode(dw, args.decode_steps, 20)
+        dms, dclk = bench_decode(dw, args.decode_steps, 20, gpu_index=local)
         gbs = decode_bytes(dw) / (dms * 1e-3) / 1e9
+        # the decode section's own clocks: median SM MHz, throttle reasons
         extra["decode"] = {"sps": sig(1e3 / dms, 5), "ms": sig(dms),
-                           "gbs": sig(gbs), "frac": sig(gbs / hbm, 3)}
+                           "gbs": sig(gbs), "frac": sig(gbs / hbm, 3),
+                           "mhz": dclk["sm_mhz"], "thr": dclk["reasons"]}
 
     if not args.no_configs:
         _, extra["c1"] = prefill_point(gen.LAYER_340M, world, local, hbm)

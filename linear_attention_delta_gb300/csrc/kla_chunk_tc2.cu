@@ -1288,11 +1288,15 @@ namespace {
 // the 1B and 340M layers (a pre-pass item takes ~9.5 us with five per SM;
 // the state pass starts its chain ~6 us after its SMs are free and takes
 // ~1.6 us per chunk); a sweep of the release point put the best times at
-// 42 of 64 and 22 of 32 chunk indices, where this gives 43 and 22.  A wrong
+// 42 of 64 and 22 of 32 chunk indices, where this gives 43 and 22.  With
+// write keys (four per SM) the same rates give 48 of 64 on the 1B layer,
+// where a sweep put the best at 42-44 and 48 costs 2%: an item time of
+// 7.1 us, fitted to that sweep rather than timed, gives 42.  A wrong
 // estimate costs time, never correctness: the state pass waits for each
 // flag.
-int release_chunks(int nbh, int nchunks, int reserved_sms, int per_sm) {
-    const double item_us = 9.5, start_us = 6.0, chunk_us = 1.6;
+int release_chunks(int nbh, int nchunks, int reserved_sms, int per_sm,
+                   double item_us) {
+    const double start_us = 6.0, chunk_us = 1.6;
     const double rate = reserved_sms * per_sm / item_us;   // items per us
     for (int kc = 0; kc < nchunks; ++kc) {
         bool ok = true;
@@ -1386,7 +1390,7 @@ cudaError_t launch_prep_tc2(const FwdArgs& a, void* ws, cudaStream_t stream,
                              : 0;
     const long release =
         reserved ? nbh * release_chunks((int)nbh, nchunks, reserved,
-                                        d.prep_per_sm)
+                                        d.prep_per_sm, kw ? 7.1 : 9.5)
                  : items;
     const long grid = std::min(items, (long)d.sms * d.prep_per_sm);
     PrepParams pp{a.log_alpha, a.eta, rec, a.eps, a.gdn, a.T, a.H, nchunks,

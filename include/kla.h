@@ -372,6 +372,45 @@ KLA_API kla_status kla_precond_keys(const void* k, const float* A0,
                                     kla_dtype dtype, kla_stream_t stream);
 
 /*
+ * kla_precond_keys_workspace_size -- bytes of device workspace
+ * kla_precond_keys_ex takes: with dk = 128 and T > 64, two fp32 rows of dk
+ * per (b, h, 64-token chunk) (B H ceil(T / 64) 1024 bytes), else 0.  Errors:
+ * KLA_ERR_INVALID_ARG (NULL bytes, negative sizes, dtype),
+ * KLA_ERR_UNSUPPORTED_SHAPE (dk).
+ *
+ * kla_precond_keys_ex -- kla_precond_keys with an optional workspace.  With
+ * dk = 128 and 16-byte-aligned k and k_write the library takes its chunked
+ * form: per (b, h, chunk) the sum of k^2 over the chunk, a scan of those
+ * sums over the chunks of each (b, h) (A before each chunk, and A_T), then
+ * the chunk's tokens in order from that A (three launches on `stream`,
+ * each later one a programmatic dependent of the one before; with T <= 64,
+ * a decode step for instance, the last alone, from A0).  Its
+ * partial sums are grouped by chunk, so A_T and kw differ from the other
+ * form's by fp32 rounding only.  Other shapes take one kernel without a
+ * workspace (one cluster of CTAs per (b, h)).
+ *
+ *   workspace  device memory of at least
+ *              kla_precond_keys_workspace_size(...) bytes, 16-byte aligned,
+ *              overlapping no argument, owned by the caller, contents on
+ *              entry irrelevant; or NULL (stream-ordered scratch when the
+ *              chunked form runs)
+ *
+ * kla_precond_keys is kla_precond_keys_ex with a NULL workspace.  Errors as
+ * for kla_precond_keys, plus KLA_ERR_INVALID_ARG for a small, misaligned or
+ * overlapping workspace.
+ */
+KLA_API kla_status kla_precond_keys_workspace_size(int B, int T, int H,
+                                                   int dk, kla_dtype dtype,
+                                                   size_t* bytes);
+KLA_API kla_status kla_precond_keys_ex(const void* k, const float* A0,
+                                       void* k_write, float* AT, int B,
+                                       int T, int H, int dk, float x,
+                                       float delta, kla_dtype dtype,
+                                       void* workspace,
+                                       size_t workspace_bytes,
+                                       kla_stream_t stream);
+
+/*
  * kla_chunk_fwd_kw -- kla_chunk_fwd_ex with separate write keys k_write
  * ([B, T, H, dk], dtype, read; e.g. from kla_precond_keys): the chunkwise
  * form with A = I + strict_lower(Diag(beta)(Gamma o K Kw^T)),

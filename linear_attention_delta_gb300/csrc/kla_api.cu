@@ -248,10 +248,26 @@ extern "C" kla_status kla_chunk_fwd_kw_ex(const void* q, const void* k,
                           workspace_bytes, stream);
 }
 
-extern "C" kla_status kla_precond_keys(const void* k, const float* A0,
-                                       void* k_write, float* AT, int B, int T,
-                                       int H, int dk, float x, float delta,
-                                       kla_dtype dtype, kla_stream_t stream) {
+extern "C" kla_status kla_precond_keys_workspace_size(int B, int T, int H,
+                                                      int dk, kla_dtype dtype,
+                                                      size_t* bytes) {
+    if (!bytes) return KLA_ERR_INVALID_ARG;
+    *bytes = 0;
+    if (B < 0 || T < 0 || H < 0 || dk <= 0) return KLA_ERR_INVALID_ARG;
+    if (dtype != KLA_F32 && dtype != KLA_BF16) return KLA_ERR_INVALID_ARG;
+    if (!supported_dim(dk)) return KLA_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)B * H > 0x7fffffffLL) return KLA_ERR_UNSUPPORTED_SHAPE;
+    if (dk == 128) *bytes = kla::precond_chunked_bytes(B, T, H);
+    return KLA_OK;
+}
+
+extern "C" kla_status kla_precond_keys_ex(const void* k, const float* A0,
+                                          void* k_write, float* AT, int B,
+                                          int T, int H, int dk, float x,
+                                          float delta, kla_dtype dtype,
+                                          void* workspace,
+                                          size_t workspace_bytes,
+                                          kla_stream_t stream) {
     if (B < 0 || T < 0 || H < 0 || dk <= 0) return KLA_ERR_INVALID_ARG;
     if (dtype != KLA_F32 && dtype != KLA_BF16) return KLA_ERR_INVALID_ARG;
     if (!(x > 1.f) || !std::isfinite(x) || !(delta >= 0.f) ||
@@ -279,8 +295,37 @@ extern "C" kla_status kla_precond_keys(const void* k, const float* A0,
             return KLA_ERR_INVALID_ARG;
     }
     kla::PrecondArgs a{k, A0, k_write, AT, B, T, H, dk, x, delta, dtype};
-    return from_cuda(
-        kla::launch_precond_keys(a, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!kla::precond_chunked_eligible(a))
+        return from_cuda(kla::launch_precond_keys(a, s));
+    const size_t need = kla::precond_chunked_bytes(B, T, H);
+    if (workspace) {
+        if (workspace_bytes < need || !aligned(workspace, 16))
+            return KLA_ERR_INVALID_ARG;
+        const size_t kb = (size_t)B * T * H * dk * elt;
+        const size_t ab = sizeof(float) * (size_t)B * H * dk;
+        const Span bufs[] = {{k, kb}, {T > 0 ? k_write : nullptr, kb},
+                             {A0, ab}, {AT, ab}};
+        const Span ws[] = {{workspace, need}};
+        if (any_overlap(bufs, ws)) return KLA_ERR_INVALID_ARG;
+        return from_cuda(kla::launch_precond_chunked(a, workspace, s));
+    }
+    if (need == 0)   // T <= 64: no scan, no workspace
+        return from_cuda(kla::launch_precond_chunked(a, nullptr, s));
+    // stream-ordered scratch from the device's current memory pool
+    void* scratch = nullptr;
+    if (cudaMallocAsync(&scratch, need, s) != cudaSuccess) return KLA_ERR_CUDA;
+    const cudaError_t e = kla::launch_precond_chunked(a, scratch, s);
+    const cudaError_t f = cudaFreeAsync(scratch, s);
+    return from_cuda(e != cudaSuccess ? e : f);
+}
+
+extern "C" kla_status kla_precond_keys(const void* k, const float* A0,
+                                       void* k_write, float* AT, int B, int T,
+                                       int H, int dk, float x, float delta,
+                                       kla_dtype dtype, kla_stream_t stream) {
+    return kla_precond_keys_ex(k, A0, k_write, AT, B, T, H, dk, x, delta,
+                               dtype, nullptr, 0, stream);
 }
 
 extern "C" kla_status kla_chunk_fwd(const void* q, const void* k,

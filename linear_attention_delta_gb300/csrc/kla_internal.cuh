@@ -157,7 +157,15 @@ cudaError_t launch_state_selftest(cudaStream_t stream);
 // Backward pass: the checkpointing forward, the reverse state-gradient
 // recurrence and the per-chunk gradients (CUDA cores, fp32).
 cudaError_t launch_chunk_bwd(const BwdArgs& a, cudaStream_t stream);
+// Write keys: the cluster kernel (any supported dk, no workspace) ...
 cudaError_t launch_precond_keys(const PrecondArgs& a, cudaStream_t stream);
+// ... and the chunked form (dk = 128, k and kw 16-byte aligned), which takes
+// precond_chunked_bytes of fp32 workspace (the per-chunk sums of k^2 and A
+// before each chunk; none when T <= 64) and fills every SM.
+bool precond_chunked_eligible(const PrecondArgs& a);
+size_t precond_chunked_bytes(int B, int T, int H);
+cudaError_t launch_precond_chunked(const PrecondArgs& a, void* workspace,
+                                   cudaStream_t stream);
 // Workspace of kla_chunk_bwd: the fp32 states at every chunk start and
 // dL/dS at every chunk end (chunk_bwd_state_floats each), then, for dk = 128
 // and C = 64, the tensor-core kernels' per-chunk records.

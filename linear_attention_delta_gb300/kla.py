@@ -52,6 +52,10 @@ SIGNATURES = {
                                    _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
     "kla_precond_keys": (_I, [_VP, _FP, _VP, _FP, _I, _I, _I, _I, _F, _F,
                               _I, _VP]),
+    "kla_precond_keys_workspace_size": (
+        _I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
+    "kla_precond_keys_ex": (_I, [_VP, _FP, _VP, _FP, _I, _I, _I, _I, _F, _F,
+                                 _I, _VP, ctypes.c_size_t, _VP]),
     "kla_chunk_fwd_kw": (_I, [_VP, _VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
                               _FP, _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
     "kla_chunk_fwd_kw_ex": (_I, [_VP, _VP, _VP, _VP, _FP, _FP, _F, _FP, _VP,
@@ -434,10 +438,24 @@ def _bwd_noalloc_call(q, k, v, log_alpha, eta, o_grad, hT_grad, eps, h0, C,
         DTYPES[q.dtype], RULES[rule], _stream(stream))
 
 
+def precond_keys_workspace_size(B, T, H, dk, dtype) -> int:
+    """Bytes of device workspace ``precond_keys`` takes
+    (``kla_precond_keys_workspace_size``); 0 when its kernel needs none."""
+    n = ctypes.c_size_t(0)
+    st = load_library().kla_precond_keys_workspace_size(
+        B, T, H, dk, DTYPES[dtype], ctypes.byref(n))
+    if st != KLA_OK:
+        raise KlaError("kla_precond_keys_workspace_size", st)
+    return n.value
+
+
 def precond_keys(k, A0=None, x: float = 1.5, delta: float = 1e-6,
-                 k_write=None, AT=None, want_AT: bool = True, stream=None):
+                 k_write=None, AT=None, want_AT: bool = True, stream=None,
+                 workspace=None):
     """Write keys of the diagonal-preconditioned variant
-    (``kla_precond_keys``).  k [B,T,H,dk]; A0 [B,H,dk] fp32 or None.
+    (``kla_precond_keys_ex``).  k [B,T,H,dk]; A0 [B,H,dk] fp32 or None.
+    ``workspace``: a device buffer of ``precond_keys_workspace_size`` bytes
+    or None (allocated here, by torch, when the kernel takes one).
     Returns (k_write, A_T); A_T is None unless ``want_AT``."""
     _check_cuda("k", k)
     if A0 is not None:
@@ -449,11 +467,17 @@ def precond_keys(k, A0=None, x: float = 1.5, delta: float = 1e-6,
         k_write = torch.empty_like(k)
     if AT is None and want_AT:
         AT = torch.empty((B, H, dk), dtype=torch.float32, device=k.device)
-    st = load_library().kla_precond_keys(
+    need = precond_keys_workspace_size(B, T, H, dk, k.dtype)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=k.device)
+    nbytes = 0 if workspace is None else workspace.numel() * \
+        workspace.element_size()
+    st = load_library().kla_precond_keys_ex(
         _ptr(k), _ptr(A0), _ptr(k_write), _ptr(AT), B, T, H, dk, float(x),
-        float(delta), DTYPES[k.dtype], _stream(stream))
+        float(delta), DTYPES[k.dtype], _ptr(workspace), nbytes,
+        _stream(stream))
     if st != KLA_OK:
-        raise KlaError("kla_precond_keys", st)
+        raise KlaError("kla_precond_keys_ex", st)
     return k_write, AT
 
 

@@ -214,6 +214,39 @@ def test_precond_entry_points_reject_bad_arguments_on_host(lib):
                None) == INVALID
 
 
+def test_precond_workspace_size_and_checks_on_host(lib):
+    """kla_precond_keys_ex's chunked form (dk = 128) takes two fp32 rows of
+    dk per (batch, head, 64-token chunk), none for a single chunk (T <= 64)
+    or another dk; a small, misaligned or overlapping workspace is refused
+    before any device call."""
+    bf16 = kla.torch.bfloat16
+    assert kla.precond_keys_workspace_size(2, 200, 3, 128, bf16) == \
+        2 * 3 * 4 * 1024
+    assert kla.precond_keys_workspace_size(2, 65, 3, 128, bf16) == \
+        2 * 3 * 2 * 1024
+    for T in (0, 1, 64):
+        assert kla.precond_keys_workspace_size(2, T, 3, 128, bf16) == 0
+    assert kla.precond_keys_workspace_size(2, 200, 3, 64, bf16) == 0
+    n = ctypes.c_size_t(0)
+    ws_size = lib.kla_precond_keys_workspace_size
+    assert ws_size(1, 128, 1, 128, 1, None) == INVALID
+    assert ws_size(1, -1, 1, 128, 1, ctypes.byref(n)) == INVALID
+    assert ws_size(1, 128, 1, 24, 1, ctypes.byref(n)) == UNSUPPORTED
+    V = ctypes.c_void_p
+    k, kw = 0x100000, 0x200000        # B1 T128 H1 dk128 bf16: 32 KiB each
+    need = 2 * 1024                   # two chunks
+    assert kla.precond_keys_workspace_size(1, 128, 1, 128, bf16) == need
+
+    def pk(ws, nbytes):
+        return lib.kla_precond_keys_ex(V(k), None, V(kw), None, 1, 128, 1,
+                                       128, 1.5, 1e-6, 1, V(ws), nbytes,
+                                       None)
+    assert pk(0x300000, need - 1) == INVALID                 # small
+    assert pk(0x300008, need) == INVALID                     # misaligned
+    assert pk(k + 0x4000, need) == INVALID                   # inside k
+    assert pk(kw + 0x7ff0, need) == INVALID                  # overlaps kw
+
+
 HP = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(6)]   # distinct
 
 

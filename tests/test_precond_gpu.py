@@ -54,10 +54,20 @@ def dev(inp):
     (gen.TINY, dict(T=0)),
     (replace(gen.TINY, dk=32, dv=32), dict(T=777)),
     (replace(gen.TINY, dk=64), dict(B=1, T=1029, H=3)),
+    (gen.LAYER_1B, dict(B=2, T=1, H=2)),
+    (gen.LAYER_1B, dict(B=2, T=64, H=3)),
+    (gen.LAYER_1B, dict(B=2, T=65, H=2)),
     (gen.LAYER_1B, dict(B=2, T=300, H=2)),
+    (gen.LAYER_1B, dict(B=1, T=4096, H=2)),
     (gen.LAYER_1B, dict(B=1, T=4100, H=2)),
+    (replace(gen.LAYER_1B, dtype="f32"), dict(B=1, T=2048, H=2)),
+    (replace(gen.LAYER_1B, dtype="f32"), dict(B=1, T=2100, H=3)),
 ])
 def test_write_keys_and_second_moments(w, sizes):
+    """dk = 128 takes the chunked form: one launch from A0 for a single
+    chunk (T = 1, 64), else sums, scan and weighting over 64-token chunks
+    (T = 65: a one-token last chunk; 300, 2100: ragged; 4100: 65 chunks,
+    two batches of the scan's loads); other dk the cluster kernel."""
     inp = aniso(gen.prefill_inputs(w, **sizes), 1)
     B, T, H, dk = inp["k"].shape
     A0 = torch.from_numpy(np.random.default_rng(2).uniform(
@@ -75,6 +85,48 @@ def test_write_keys_and_second_moments(w, sizes):
         return
     assert rel_err(kw, kw_ref) <= tol
     assert rel_err(AT, A_ref) <= 1e-5
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_write_keys_misaligned_take_the_cluster_kernel(dtype):
+    """dk = 128 keys that are not 16-byte aligned (a view one element into
+    its buffer) take the cluster kernel; same bounds against the oracle."""
+    w = gen.LAYER_1B if dtype == torch.bfloat16 else \
+        replace(gen.LAYER_1B, dtype="f32")
+    inp = aniso(gen.prefill_inputs(w, B=1, T=200, H=2), 7)
+    B, T, H, dk = inp["k"].shape
+    buf = torch.empty(inp["k"].numel() + 1, dtype=dtype, device="cuda")
+    k = buf[1:].view(B, T, H, dk)
+    k.copy_(inp["k"].cuda())
+    assert k.data_ptr() % 16 != 0
+    kw, AT = kla.precond_keys(k, None, x=X, delta=DELTA)
+    torch.cuda.synchronize()
+    _, _, A_ref, kw_ref = oracle.pkla_fwd(inp["q"], inp["k"], inp["v"],
+                                          inp["log_alpha"], inp["eta"],
+                                          inp["eps"], None, x=X, delta=DELTA)
+    assert rel_err(kw, kw_ref) <= TOL[dtype]
+    assert rel_err(AT, A_ref) <= 1e-5
+
+
+def test_write_keys_plain_entry_point_equals_workspace_form():
+    """kla_precond_keys (the library's stream-ordered scratch) and
+    kla_precond_keys_ex with a caller workspace run the same kernels: the
+    same bits."""
+    import ctypes
+    inp = aniso(gen.prefill_inputs(gen.LAYER_1B, B=2, T=700, H=3), 8)
+    k = inp["k"].cuda()
+    B, T, H, dk = k.shape
+    A0 = torch.rand(B, H, dk, device="cuda") * 4
+    kw1, AT1 = kla.precond_keys(k, A0, x=X, delta=DELTA)
+    kw2, AT2 = torch.empty_like(k), torch.empty_like(A0)
+    st = kla.load_library().kla_precond_keys(
+        ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(A0.data_ptr()),
+        ctypes.c_void_p(kw2.data_ptr()), ctypes.c_void_p(AT2.data_ptr()),
+        B, T, H, dk, X, DELTA, kla.DTYPES[k.dtype],
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(kw1, kw2) and torch.equal(AT1, AT2)
 
 
 @pytest.mark.parametrize("rule", ["kaczmarz", "given"])

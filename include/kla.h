@@ -393,7 +393,7 @@ KLA_API kla_status kla_precond_keys(const void* k, const float* A0,
  *              kla_precond_keys_workspace_size(...) bytes, 16-byte aligned,
  *              overlapping no argument, owned by the caller, contents on
  *              entry irrelevant; or NULL (stream-ordered scratch when the
- *              chunked form runs)
+ *              chunked form needs a workspace: T > 64)
  *
  * kla_precond_keys is kla_precond_keys_ex with a NULL workspace.  Errors as
  * for kla_precond_keys, plus KLA_ERR_INVALID_ARG for a small, misaligned or
